@@ -1,0 +1,208 @@
+"""CPU oracle for the MoE layer forward pass -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's
+CPU-baseline / reference leg may import this package.  The product path (the
+CUDA library and its binding in ``token_level_top_gb300``) never does.
+
+The arithmetic lives in ``moe_oracle.c`` (plain C, single thread, built with
+``-O2 -ffp-contract=off``); this module only builds it, loads it with ctypes
+and marshals numpy arrays.  bf16 tensors are passed as their raw 16-bit
+patterns (``numpy.uint16``); the C code widens them exactly to fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_HDR = os.path.join(_HERE, "moe_oracle.h")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library (gcc, -ffp-contract=off)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-fPIC",
+               "-shared", "-Wall", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            lib.oracle_capacity.argtypes = [ctypes.c_int64, I, I, ctypes.c_double, ctypes.c_int64]
+            lib.oracle_capacity.restype = ctypes.c_int64
+            lib.oracle_route.argtypes = [I, I, I, I, P, P, P, P, ctypes.c_float, P,
+                                         P, P, P, P, P, P, P]
+            lib.oracle_route.restype = I
+            lib.oracle_preference.argtypes = [I, P, P]
+            lib.oracle_preference.restype = I
+            lib.oracle_dispatch.argtypes = [I, I, I, ctypes.c_int64, P, P, P, P, P, P, P, P, P, P]
+            lib.oracle_dispatch.restype = I
+            lib.oracle_expert_row.argtypes = [I, I, P, P, P, P, P]
+            lib.oracle_expert_row.restype = None
+            lib.oracle_combine_rows.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, P]
+            lib.oracle_combine_rows.restype = I
+            lib.oracle_expert_slots.argtypes = [I, I, I, I, I, P, P, P, P, P, P, I, I, P]
+            lib.oracle_expert_slots.restype = I
+            _lib = lib
+    return _lib
+
+
+class OracleError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"oracle {what} returned status {status}")
+        self.status = status
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    if a is None:
+        return None
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def capacity(T: int, k: int, E: int, cf: float, explicit: int = 0) -> int:
+    """C = ceil(T*k*cf/E) with cf as an exact decimal (six fractional digits)."""
+    return int(_load().oracle_capacity(T, k, E, cf, explicit))
+
+
+def preference(s_row) -> np.ndarray:
+    s_row = _c(s_row, np.float32)
+    order = np.empty(s_row.shape[0], np.int32)
+    st = _load().oracle_preference(s_row.shape[0], _ptr(s_row), _ptr(order))
+    if st:
+        raise OracleError(st, "preference")
+    return order
+
+
+def route(k, h=None, wr=None, bias=None, usage=None, lam=0.0, logits_in=None, E=None):
+    """Router step.  h [T,d] / wr [E,d] as uint16 bf16 bits, or logits_in [T,E] fp32.
+
+    Returns dict(logits, scores, ids, topk_p, counts_pre, f, P)."""
+    lib = _load()
+    if logits_in is not None:
+        logits_in = _c(logits_in, np.float32)
+        T, E = logits_in.shape
+        d = 0
+    else:
+        h = _c(h, np.uint16)
+        wr = _c(wr, np.uint16)
+        T, d = h.shape
+        E = wr.shape[0]
+    bias = _c(bias, np.float32)
+    usage = _c(usage, np.float32)
+    out = dict(logits=np.empty((T, E), np.float32), scores=np.empty((T, E), np.float32),
+               ids=np.empty((T, k), np.int32), topk_p=np.empty((T, k), np.float32),
+               counts_pre=np.empty(E, np.int32), f=np.empty(E, np.float32),
+               P=np.empty(E, np.float32))
+    st = lib.oracle_route(T, d, E, k, _ptr(h), _ptr(wr), _ptr(bias), _ptr(usage), float(lam),
+                          _ptr(logits_in), _ptr(out["logits"]), _ptr(out["scores"]),
+                          _ptr(out["ids"]), _ptr(out["topk_p"]), _ptr(out["counts_pre"]),
+                          _ptr(out["f"]), _ptr(out["P"]))
+    if st:
+        raise OracleError(st, "route")
+    return out
+
+
+def dispatch(scores, k: int, C: int):
+    """Capacity-capped dispatch on penalised scores [T,E] fp32.
+
+    Returns dict(assign, slot, flags, counts, offsets, perm, cw, n_rerouted, n_dropped)."""
+    lib = _load()
+    scores = _c(scores, np.float32)
+    T, E = scores.shape
+    out = dict(assign=np.empty((T, k), np.int32), slot=np.empty((T, k), np.int32),
+               flags=np.empty((T, k), np.uint8), counts=np.empty(E, np.int32),
+               offsets=np.empty(E + 1, np.int32), perm=np.full(T * k, -1, np.int32),
+               cw=np.empty((T, k), np.float32))
+    nre = np.zeros(1, np.int32)
+    ndr = np.zeros(1, np.int32)
+    st = lib.oracle_dispatch(T, E, k, int(C), _ptr(scores), _ptr(out["assign"]),
+                             _ptr(out["slot"]), _ptr(out["flags"]), _ptr(out["counts"]),
+                             _ptr(out["offsets"]), _ptr(out["perm"]), _ptr(out["cw"]),
+                             _ptr(nre), _ptr(ndr))
+    if st:
+        raise OracleError(st, "dispatch")
+    out["perm"] = out["perm"][: int(out["offsets"][-1])]
+    out["n_rerouted"] = int(nre[0])
+    out["n_dropped"] = int(ndr[0])
+    return out
+
+
+def expert_row(x, w1, w3, w2) -> np.ndarray:
+    """y = W2 (silu(W1 x) * W3 x) for one token, in double.  bf16 bits in."""
+    x, w1, w3, w2 = (_c(a, np.uint16) for a in (x, w1, w3, w2))
+    F, d = w1.shape
+    y = np.empty(d, np.float64)
+    _load().oracle_expert_row(d, F, _ptr(x), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(y))
+    return y
+
+
+def combine_rows(h, w1, w3, w2, assign, cw, tokens) -> np.ndarray:
+    """Layer output rows (fp32) for the listed tokens, given a dispatch."""
+    h, w1, w3, w2 = (_c(a, np.uint16) for a in (h, w1, w3, w2))
+    assign = _c(assign, np.int32)
+    cw = _c(cw, np.float32)
+    tokens = _c(tokens, np.int32)
+    T, d = h.shape
+    E, F, _ = w1.shape
+    k = assign.shape[1]
+    out = np.empty((tokens.shape[0], d), np.float32)
+    st = _load().oracle_combine_rows(T, d, E, k, F, _ptr(h), _ptr(w1), _ptr(w3), _ptr(w2),
+                                     _ptr(assign), _ptr(cw), _ptr(tokens), tokens.shape[0],
+                                     _ptr(out))
+    if st:
+        raise OracleError(st, "combine_rows")
+    return out
+
+
+def expert_slots(h, w1, w3, w2, assign, perm, row0: int, row1: int) -> np.ndarray:
+    """Per-slot expert outputs (fp32) for slots [row0, row1) in slot order."""
+    h, w1, w3, w2 = (_c(a, np.uint16) for a in (h, w1, w3, w2))
+    assign = _c(assign, np.int32)
+    perm = _c(perm, np.int32)
+    T, d = h.shape
+    E, F, _ = w1.shape
+    k = assign.shape[1]
+    out = np.empty((row1 - row0, d), np.float32)
+    st = _load().oracle_expert_slots(T, d, E, k, F, _ptr(h), _ptr(w1), _ptr(w3), _ptr(w2),
+                                     _ptr(assign), _ptr(perm), row0, row1, _ptr(out))
+    if st:
+        raise OracleError(st, "expert_slots")
+    return out
+
+
+def layer_forward(h, wr, w1, w3, w2, k, C, bias=None, usage=None, lam=0.0, tokens=None,
+                  logits_in=None):
+    """Whole layer: route, dispatch, experts and combine.
+
+    ``tokens`` limits the (expensive) expert part to a sample of token rows.
+    ``logits_in`` replaces the router GEMM (shared-logit comparisons)."""
+    r = route(k, h=h, wr=wr, bias=bias, usage=usage, lam=lam, logits_in=logits_in)
+    dsp = dispatch(r["scores"], k, C)
+    T = r["scores"].shape[0]
+    if tokens is None:
+        tokens = np.arange(T, dtype=np.int32)
+    out = combine_rows(h, w1, w3, w2, dsp["assign"], dsp["cw"], tokens)
+    return r, dsp, out

@@ -1,0 +1,310 @@
+/*
+ * moe_oracle.c -- plain CPU reference of one MoE FFN layer's forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY (see moe_oracle.h): used by the tests, the smoke
+ * check and the benchmark's CPU-baseline leg, never by the product path.
+ * Build with -O2 -ffp-contract=off so that no fused multiply-add changes the
+ * fp32 score arithmetic.
+ *
+ * The steps follow the pages in order:
+ *   1. logits z = h . W_router (+ bias)          [coreui] §3.1, [csdn] §3.1
+ *   2. penalty s_i = z_i - lambda * usage_i       [mhpn] §2.3 (second layer),
+ *      applied before top-k                       [cnnetsun] §3.1 step 4
+ *   3. softmax over experts and top-k picks      [coreui] §3.1
+ *   4. f_i (top-k counts / T) and P_i (mean p_i) [cnnetsun] §4.2, [coreui] §3.1
+ *   5. capacity-capped dispatch with reroute     [mhpn] §2.3 (third layer),
+ *      capacity ceil(T*k/E*cf)                   [coreui] §5.2, [2kiu] §2
+ *   6. SwiGLU experts W2(silu(W1 x) * W3 x)      [mhpn] §3.1, [2kiu] §1
+ *   7. weighted combine, weights renormalised    [mhpn] §4.3
+ *      over the experts actually used
+ */
+#include "moe_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+static float bf16_to_f32(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+int64_t oracle_capacity(int64_t T, int k, int E, double cf, int64_t explicit_cap)
+{
+    if (explicit_cap > 0) return explicit_cap;
+    if (T <= 0 || k <= 0 || E <= 0 || !(cf > 0.0)) return 0;
+    /* cf as an exact decimal: cf = cf_micro / 10^6. */
+    int64_t cf_micro = llround(cf * 1e6);
+    int64_t num = T * (int64_t)k * cf_micro;
+    int64_t den = (int64_t)E * 1000000;
+    return (num + den - 1) / den;
+}
+
+/* Score order used everywhere: a ranks before b when s_a > s_b, or when the
+ * scores are equal and a has the lower index.  -0.0 and +0.0 compare equal. */
+static int ranks_before(float sa, int a, float sb, int b)
+{
+    if (sa > sb) return 1;
+    if (sa < sb) return 0;
+    return a < b;
+}
+
+int oracle_preference(int E, const float* s_row, int32_t* order)
+{
+    for (int e = 0; e < E; ++e)
+        if (isnan(s_row[e])) return 5;
+    /* insertion sort by the score order */
+    for (int e = 0; e < E; ++e) {
+        int pos = e;
+        while (pos > 0 && ranks_before(s_row[e], e, s_row[order[pos - 1]], order[pos - 1])) {
+            order[pos] = order[pos - 1];
+            --pos;
+        }
+        order[pos] = e;
+    }
+    return 0;
+}
+
+/* Softmax of one row of scores, in double.  Limits: when the largest score is
+ * +inf the mass is shared equally by the +inf entries; when every score is
+ * -inf the distribution is uniform. */
+static void softmax_row(int E, const float* s, double* p)
+{
+    double m = -INFINITY;
+    for (int e = 0; e < E; ++e)
+        if ((double)s[e] > m) m = (double)s[e];
+    if (isinf(m)) {
+        int n = 0;
+        for (int e = 0; e < E; ++e) n += ((double)s[e] == m);
+        for (int e = 0; e < E; ++e) p[e] = ((double)s[e] == m) ? 1.0 / n : 0.0;
+        return;
+    }
+    double z = 0.0;
+    for (int e = 0; e < E; ++e) {
+        p[e] = exp((double)s[e] - m);
+        z += p[e];
+    }
+    for (int e = 0; e < E; ++e) p[e] /= z;
+}
+
+int oracle_route(int T, int d, int E, int k, const uint16_t* h, const uint16_t* wr,
+                 const float* bias, const float* usage, float lambda, const float* logits_in,
+                 float* logits, float* scores, int32_t* ids, float* topk_p,
+                 int32_t* counts_pre, float* f, float* P)
+{
+    if (T < 0 || E <= 0 || k <= 0 || k > E) return 1;
+    if (!logits_in && (d <= 0 || !h || !wr)) return 1;
+
+    int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
+    double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    double* psum = (double*)calloc((size_t)E, sizeof(double));
+    int status = 0;
+    for (int e = 0; e < E; ++e) counts_pre[e] = 0;
+
+    for (int t = 0; t < T && status == 0; ++t) {
+        float* z = logits + (size_t)t * E;
+        float* s = scores + (size_t)t * E;
+        /* step 1: z = h_t . W_router (+ b) */
+        for (int e = 0; e < E; ++e) {
+            if (logits_in) {
+                z[e] = logits_in[(size_t)t * E + e];
+            } else {
+                double acc = 0.0;
+                const uint16_t* ht = h + (size_t)t * d;
+                const uint16_t* we = wr + (size_t)e * d;
+                for (int i = 0; i < d; ++i)
+                    acc += (double)bf16_to_f32(ht[i]) * (double)bf16_to_f32(we[i]);
+                if (bias) acc += (double)bias[e];
+                z[e] = (float)acc;
+            }
+        }
+        /* step 2: s = z - fl(lambda * usage), fp32, no FMA */
+        for (int e = 0; e < E; ++e) {
+            if (!usage || lambda == 0.0f) {
+                s[e] = z[e];
+            } else {
+                volatile float pen = lambda * usage[e];
+                s[e] = z[e] - pen;
+            }
+        }
+        /* step 3: preference order, top-k ids, softmax probabilities */
+        if (oracle_preference(E, s, order)) { status = 5; break; }
+        softmax_row(E, s, p);
+        for (int r = 0; r < k; ++r) {
+            ids[(size_t)t * k + r] = order[r];
+            topk_p[(size_t)t * k + r] = (float)p[order[r]];
+            counts_pre[order[r]] += 1;
+        }
+        for (int e = 0; e < E; ++e) psum[e] += p[e];
+    }
+    /* step 4: f_i = counts_pre_i / T, P_i = mean over tokens of p_i */
+    for (int e = 0; e < E; ++e) {
+        f[e] = T > 0 ? (float)((double)counts_pre[e] / (double)T) : 0.0f;
+        P[e] = T > 0 ? (float)(psum[e] / (double)T) : 0.0f;
+    }
+    free(order);
+    free(p);
+    free(psum);
+    return status;
+}
+
+int oracle_dispatch(int T, int E, int k, int64_t C, const float* scores,
+                    int32_t* assign, int32_t* slot, uint8_t* flags, int32_t* counts,
+                    int32_t* offsets, int32_t* perm, float* cw,
+                    int32_t* n_rerouted, int32_t* n_dropped)
+{
+    if (T < 0 || E <= 0 || k <= 0 || k > E || C < 0) return 1;
+    int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)T * (size_t)E);
+    int64_t* fill = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    int status = 0;
+
+    for (int t = 0; t < T; ++t)
+        if (oracle_preference(E, scores + (size_t)t * E, order + (size_t)t * E)) { status = 5; break; }
+
+    int32_t nre = 0, ndrop = 0;
+    if (status == 0) {
+        /* Rank-major, token-minor: every rank-0 choice before any rank-1 choice. */
+        for (int r = 0; r < k; ++r) {
+            for (int t = 0; t < T; ++t) {
+                const int32_t* pi = order + (size_t)t * E;
+                int32_t chosen = -1;
+                /* The token's own pick is pi[r]; when that expert is full (or
+                 * already serves this token) walk on to the next candidate. */
+                for (int j = r; j < E && chosen < 0; ++j) {
+                    int32_t e = pi[j];
+                    if (fill[e] >= C) continue;
+                    int held = 0;
+                    for (int q = 0; q < r; ++q) held |= (assign[(size_t)t * k + q] == e);
+                    if (held) continue;
+                    chosen = e;
+                }
+                size_t idx = (size_t)t * k + r;
+                if (chosen < 0) {
+                    assign[idx] = -1;
+                    slot[idx] = -1;
+                    flags[idx] = 2;
+                    ++ndrop;
+                } else {
+                    assign[idx] = chosen;
+                    slot[idx] = (int32_t)fill[chosen];
+                    fill[chosen] += 1;
+                    flags[idx] = (chosen != pi[r]) ? 1 : 0;
+                    nre += (chosen != pi[r]);
+                }
+            }
+        }
+        offsets[0] = 0;
+        for (int e = 0; e < E; ++e) {
+            counts[e] = (int32_t)fill[e];
+            offsets[e + 1] = offsets[e] + counts[e];
+        }
+        for (int t = 0; t < T; ++t)
+            for (int r = 0; r < k; ++r) {
+                size_t idx = (size_t)t * k + r;
+                if (assign[idx] >= 0) perm[offsets[assign[idx]] + slot[idx]] = (int32_t)idx;
+            }
+        /* Combine weights: softmax probability of the expert actually used,
+         * renormalised over the token's kept experts. */
+        for (int t = 0; t < T; ++t) {
+            softmax_row(E, scores + (size_t)t * E, p);
+            double tot = 0.0;
+            for (int r = 0; r < k; ++r) {
+                int32_t e = assign[(size_t)t * k + r];
+                if (e >= 0) tot += p[e];
+            }
+            for (int r = 0; r < k; ++r) {
+                int32_t e = assign[(size_t)t * k + r];
+                cw[(size_t)t * k + r] = (e >= 0 && tot > 0.0) ? (float)(p[e] / tot) : 0.0f;
+            }
+        }
+        *n_rerouted = nre;
+        *n_dropped = ndrop;
+    }
+    free(order);
+    free(fill);
+    free(p);
+    return status;
+}
+
+static double silu(double x) { return x / (1.0 + exp(-x)); }
+
+void oracle_expert_row(int d, int F, const uint16_t* x, const uint16_t* w1,
+                       const uint16_t* w3, const uint16_t* w2, double* y)
+{
+    double* xf = (double*)malloc(sizeof(double) * (size_t)d);
+    double* a = (double*)malloc(sizeof(double) * (size_t)F);
+    for (int i = 0; i < d; ++i) xf[i] = (double)bf16_to_f32(x[i]);
+    for (int j = 0; j < F; ++j) {
+        const uint16_t* g_row = w1 + (size_t)j * d;
+        const uint16_t* u_row = w3 + (size_t)j * d;
+        double g = 0.0, u = 0.0;
+        for (int i = 0; i < d; ++i) {
+            g += (double)bf16_to_f32(g_row[i]) * xf[i];
+            u += (double)bf16_to_f32(u_row[i]) * xf[i];
+        }
+        a[j] = silu(g) * u;
+    }
+    for (int i = 0; i < d; ++i) {
+        const uint16_t* row = w2 + (size_t)i * F;
+        double acc = 0.0;
+        for (int j = 0; j < F; ++j) acc += (double)bf16_to_f32(row[j]) * a[j];
+        y[i] = acc;
+    }
+    free(xf);
+    free(a);
+}
+
+int oracle_combine_rows(int T, int d, int E, int k, int F, const uint16_t* h,
+                        const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
+                        const int32_t* assign, const float* cw,
+                        const int32_t* tokens, int ntok, float* out_rows)
+{
+    if (d <= 0 || F <= 0 || E <= 0 || k <= 0) return 1;
+    double* y = (double*)malloc(sizeof(double) * (size_t)d);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int i = 0; i < ntok; ++i) {
+        int t = tokens[i];
+        if (t < 0 || t >= T) { free(y); free(acc); return 1; }
+        for (int c = 0; c < d; ++c) acc[c] = 0.0;
+        for (int r = 0; r < k; ++r) {
+            int32_t e = assign[(size_t)t * k + r];
+            if (e < 0) continue;
+            if (e >= E) { free(y); free(acc); return 1; }
+            size_t wsz = (size_t)F * d;
+            oracle_expert_row(d, F, h + (size_t)t * d, w1 + (size_t)e * wsz, w3 + (size_t)e * wsz,
+                              w2 + (size_t)e * wsz, y);
+            double w = (double)cw[(size_t)t * k + r];
+            for (int c = 0; c < d; ++c) acc[c] += w * y[c];
+        }
+        for (int c = 0; c < d; ++c) out_rows[(size_t)i * d + c] = (float)acc[c];
+    }
+    free(y);
+    free(acc);
+    return 0;
+}
+
+int oracle_expert_slots(int T, int d, int E, int k, int F, const uint16_t* h,
+                        const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
+                        const int32_t* assign, const int32_t* perm,
+                        int row0, int row1, float* y_slots)
+{
+    if (d <= 0 || F <= 0 || E <= 0 || k <= 0 || row0 < 0 || row1 < row0) return 1;
+    double* y = (double*)malloc(sizeof(double) * (size_t)d);
+    size_t wsz = (size_t)F * d;
+    for (int i = row0; i < row1; ++i) {
+        int32_t idx = perm[i];
+        int t = idx / k;
+        if (t < 0 || t >= T) { free(y); return 1; }
+        int32_t e = assign[idx];
+        if (e < 0 || e >= E) { free(y); return 1; }
+        oracle_expert_row(d, F, h + (size_t)t * d, w1 + (size_t)e * wsz, w3 + (size_t)e * wsz,
+                          w2 + (size_t)e * wsz, y);
+        for (int c = 0; c < d; ++c) y_slots[(size_t)(i - row0) * d + c] = (float)y[c];
+    }
+    free(y);
+    return 0;
+}

@@ -1,0 +1,99 @@
+/*
+ * moe_oracle.h -- plain, slow, single-threaded CPU reference for the forward
+ * pass of one sparsely activated Mixture-of-Experts FFN layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link,
+ * load or call this code: only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg use it.  It shares no code, header, table or
+ * helper with the CUDA library under token_level_top_gb300/csrc.
+ *
+ * Pages cited (the method's only description):
+ *   [mhpn]     "GPT-4稀疏激活真相：万亿参数模型的MoE工程落地实践"
+ *              (www.mhpn.cn/news/895310)
+ *   [coreui]   "MoE架构揭秘：逐Token路由与活跃参数量的工程真相"
+ *              (www.coreui.cn/article/2635427.html)
+ *   [cnnetsun] "MoE稀疏激活原理与工程实践：从2%激活率到高效推理"
+ *              (cnnetsun.cn/a/3071834)
+ *   [csdn]     untitled page, adg.csdn.net/6a3116e610ee7a33f27ddf1c.html
+ *   [2kiu]     MoE page at www.2kiu.com/news/5042631/
+ *
+ * Precision: bf16 inputs are widened exactly to fp32.  Dot products, the
+ * softmax, combine weights and the expert FFN are evaluated in double and
+ * rounded once to fp32 where an fp32 output is defined.  The two values that
+ * decide integers -- the logits z and the penalised scores s -- are fp32, as
+ * the router is kept in fp32 ([coreui] §5.2, router_dtype=float32), and s is
+ * formed with separately rounded fp32 operations (no fused multiply-add).
+ *
+ * Status codes match the library's meaning: 0 ok, 1 invalid argument,
+ * 5 non-finite (NaN) score.
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Expert capacity C = ceil(T*k*cf/E), computed exactly with cf read as a
+ * decimal with six fractional digits ([coreui] §5.2 writes
+ * expert_capacity = ceil(batch_size*top_k/num_experts*1.3); §3.3 gives the
+ * factor alpha in 1.2..1.5).  explicit_cap > 0 overrides the formula. */
+int64_t oracle_capacity(int64_t T, int k, int E, double cf, int64_t explicit_cap);
+
+/* Router: logits, penalised scores, top-k ids and probabilities, and the
+ * load statistics f and P.
+ *   h        [T,d] bf16 bits (ignored when logits_in != NULL)
+ *   wr       [E,d] bf16 bits, row e is expert e's gate vector
+ *   bias     [E] fp32 or NULL (added to the GEMM output)
+ *   usage    [E] fp32 or NULL; lambda the penalty weight
+ *   logits_in[T,E] fp32 or NULL: final logits given directly (bias not added)
+ * Outputs (all required): logits [T,E], scores [T,E], ids [T,k],
+ * topk_p [T,k] (softmax probability of each pick), counts_pre [E], f [E], P [E].
+ * Returns 0, or 5 if any score is NaN (outputs then undefined). */
+int oracle_route(int T, int d, int E, int k, const uint16_t* h, const uint16_t* wr,
+                 const float* bias, const float* usage, float lambda, const float* logits_in,
+                 float* logits, float* scores, int32_t* ids, float* topk_p,
+                 int32_t* counts_pre, float* f, float* P);
+
+/* The preference order of one token: experts sorted by score, descending,
+ * ties to the lower index.  order[E] out.  Returns 0, or 5 on NaN. */
+int oracle_preference(int E, const float* s_row, int32_t* order);
+
+/* Capacity-capped dispatch, literal sequential form: all rank-0 choices in
+ * token order, then all rank-1 choices, ...  Outputs: assign [T,k] (-1 =
+ * dropped), slot [T,k] (-1 when dropped), flags [T,k] (bit0 rerouted, bit1
+ * dropped), counts [E], offsets [E+1], perm [sum counts] (= t*k+r in slot
+ * order), cw [T,k] combine weights, n_rerouted, n_dropped.
+ * Returns 0, 1 (bad args) or 5 (NaN score). */
+int oracle_dispatch(int T, int E, int k, int64_t C, const float* scores,
+                    int32_t* assign, int32_t* slot, uint8_t* flags, int32_t* counts,
+                    int32_t* offsets, int32_t* perm, float* cw,
+                    int32_t* n_rerouted, int32_t* n_dropped);
+
+/* One expert on one token: y = W2_e (silu(W1_e x) * (W3_e x)), in double.
+ *   x [d] bf16 bits; w1, w3 [F,d] and w2 [d,F] bf16 bits of expert e. */
+void oracle_expert_row(int d, int F, const uint16_t* x, const uint16_t* w1,
+                       const uint16_t* w3, const uint16_t* w2, double* y);
+
+/* Expert FFN + probability-weighted combine for a list of tokens:
+ * out_rows[i] = sum over kept ranks r (rank order) of cw[t,r] * y(t, assign[t,r]),
+ * t = tokens[i]; a token with no kept rank gets 0.
+ *   h [T,d], w1/w3 [E,F,d], w2 [E,d,F] bf16 bits; out_rows [ntok,d] fp32. */
+int oracle_combine_rows(int T, int d, int E, int k, int F, const uint16_t* h,
+                        const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
+                        const int32_t* assign, const float* cw,
+                        const int32_t* tokens, int ntok, float* out_rows);
+
+/* Expert outputs per slot, in slot order: y_slots[i] = y(t, e) for the kept
+ * entry perm[i] = t*k+r with e = assign[t,r], for slots i in [row0, row1). */
+int oracle_expert_slots(int T, int d, int E, int k, int F, const uint16_t* h,
+                        const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
+                        const int32_t* assign, const int32_t* perm,
+                        int row0, int row1, float* y_slots);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

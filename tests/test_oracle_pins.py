@@ -1,0 +1,508 @@
+"""Pins for the CPU oracle: values the pages print, closed forms, invariants,
+brute force on tiny inputs and special cases that reduce to library routines.
+
+Every check here is independent of the oracle's own code paths, so that a
+plausible mistake in it (a dropped term, a wrong sign or index, a transposed
+operand, a rank-minor dispatch order) fails at least one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from token_level_top_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as fh:
+        return json.load(fh)
+
+
+def bf16(a):
+    return synth.bf16_bits(torch.as_tensor(np.asarray(a, np.float32)).to(torch.bfloat16))
+
+
+def widen(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# --------------------------------------------------------------------------- capacity
+
+def test_capacity_page_value():
+    g = golden("capacity_coreui_5_2.json")
+    assert oracle.capacity(g["T"], g["k"], g["E"], g["cf"]) == g["C"]
+
+
+@pytest.mark.parametrize("T,k,E,cf,C", [
+    (256, 2, 8, 1.25, 80), (4096, 2, 8, 1.25, 1280), (64, 2, 8, 1.25, 20),
+    (16384, 2, 64, 1.0, 512), (8192, 2, 16, 1.0, 1024),
+    (10, 2, 8, 1.0, 3),            # 2.5 rounds up
+    (100, 2, 26, 1.3, 10),         # exactly 10: a binary 1.3 would give 10.000...02 -> 11
+    (1, 1, 64, 1.0, 1),
+])
+def test_capacity_closed_form(T, k, E, cf, C):
+    assert oracle.capacity(T, k, E, cf) == C
+
+
+def test_capacity_explicit_override():
+    assert oracle.capacity(4096, 2, 8, 1.25, 7) == 7
+
+
+# --------------------------------------------------------------------------- router
+
+def test_preference_matches_sorted_with_ties():
+    rng = np.random.default_rng(1)
+    for _ in range(200):
+        E = int(rng.integers(1, 12))
+        s = rng.integers(-3, 3, E).astype(np.float32)   # many ties
+        if rng.random() < 0.3:
+            s[rng.integers(0, E)] = -0.0
+        want = sorted(range(E), key=lambda e: (-float(s[e]), e))
+        assert oracle.preference(s).tolist() == want
+
+
+def test_preference_signed_zero_and_inf():
+    s = np.array([0.0, -0.0, np.inf, -np.inf, 0.0], np.float32)
+    assert oracle.preference(s).tolist() == [2, 0, 1, 4, 3]
+
+
+def test_topk_is_best_subset_brute_force():
+    """Top-k set = the k-subset whose sorted score list is lexicographically
+    best, ties going to the lexicographically smaller index list."""
+    rng = np.random.default_rng(2)
+    for _ in range(150):
+        E = int(rng.integers(2, 7))
+        k = int(rng.integers(1, min(3, E) + 1))
+        T = 3
+        z = rng.integers(-2, 3, (T, E)).astype(np.float32)
+        r = oracle.route(k, logits_in=z)
+        for t in range(T):
+            best = None
+            for sub in itertools.combinations(range(E), k):
+                key = tuple(sorted(((-float(z[t, e]), e) for e in sub)))
+                if best is None or key < best[0]:
+                    best = (key, sub)
+            want = [e for _, e in best[0]]
+            assert r["ids"][t].tolist() == want
+
+
+def test_equal_logits_pick_lowest_indices():
+    z = np.zeros((4, 8), np.float32)
+    r = oracle.route(2, logits_in=z)
+    assert (r["ids"] == np.array([0, 1])).all()
+    np.testing.assert_allclose(r["topk_p"], 1.0 / 8, rtol=1e-7)
+
+
+def test_logits_match_float64_matmul():
+    rng = np.random.default_rng(3)
+    h = bf16(rng.standard_normal((37, 96)))
+    wr = bf16(rng.standard_normal((5, 96)) * 0.02)
+    bias = rng.standard_normal(5).astype(np.float32)
+    r = oracle.route(2, h=h, wr=wr, bias=bias)
+    want = widen(h).astype(np.float64) @ widen(wr).astype(np.float64).T + bias.astype(np.float64)
+    np.testing.assert_allclose(r["logits"], want.astype(np.float32), rtol=2e-7, atol=1e-7)
+    # h is [T,d] and W_r is [E,d]: a transposed operand cannot give this shape
+    assert r["logits"].shape == (37, 5)
+
+
+def test_penalty_is_two_rounded_fp32_ops():
+    # z - fl(lambda*u) with values where a fused multiply-add rounds differently
+    # z equals fl(lambda*u) for expert 0, so the unfused score is exactly 0
+    # while a fused multiply-add leaves the product's rounding error behind.
+    lam = np.float32(0.7)
+    u = np.array([0.6369616985321045, 1.0 / 3.0, 0.1], np.float32)
+    z = np.array([[float(np.float32(lam * u[0])), 1.0, 0.5]], np.float32)
+    r = oracle.route(1, logits_in=z, usage=u, lam=float(lam))
+    pen = (lam * u).astype(np.float32)
+    want = (z - pen).astype(np.float32)
+    assert np.array_equal(r["scores"], want)
+    fused = (z.astype(np.float64) - lam.astype(np.float64) * u.astype(np.float64)).astype(np.float32)
+    assert not np.array_equal(fused, want), "case must separate fused from unfused"
+
+
+def test_penalty_special_cases():
+    rng = np.random.default_rng(4)
+    z = rng.standard_normal((50, 6)).astype(np.float32)
+    u = rng.random(6).astype(np.float32)
+    base = oracle.route(2, logits_in=z)
+    zero_lam = oracle.route(2, logits_in=z, usage=u, lam=0.0)
+    assert np.array_equal(base["ids"], zero_lam["ids"])
+    assert np.array_equal(base["scores"], zero_lam["scores"])
+    # a heavily used expert is never picked
+    u2 = np.zeros(6, np.float32)
+    u2[3] = 1e6
+    pen = oracle.route(2, logits_in=z, usage=u2, lam=1.0)
+    assert not (pen["ids"] == 3).any()
+    # the penalty lowers the score (sign): expert 3 loses exactly lambda*u
+    assert np.array_equal(pen["scores"][:, 3], (z[:, 3] - np.float32(1e6)).astype(np.float32))
+
+
+def test_softmax_and_stats_match_scipy():
+    from scipy.special import softmax
+    rng = np.random.default_rng(5)
+    T, E, k = 300, 7, 2
+    z = (rng.standard_normal((T, E)) * 1.3).astype(np.float32)
+    u = rng.random(E).astype(np.float32)
+    r = oracle.route(k, logits_in=z, usage=u, lam=0.8)
+    p = softmax(r["scores"].astype(np.float64), axis=1)
+    np.testing.assert_allclose(r["topk_p"], np.take_along_axis(p, r["ids"].astype(np.int64), 1),
+                               rtol=1e-6)
+    np.testing.assert_allclose(r["P"], p.mean(0), rtol=1e-6)
+    assert abs(float(r["P"].astype(np.float64).sum()) - 1.0) < 1e-6
+    assert r["counts_pre"].sum() == T * k
+    assert abs(float(r["f"].astype(np.float64).sum()) - k) < 1e-5
+    want_counts = np.bincount(r["ids"].ravel(), minlength=E)
+    assert np.array_equal(r["counts_pre"], want_counts)
+    np.testing.assert_allclose(r["f"], want_counts / T, rtol=1e-7)
+
+
+def test_softmax_limits():
+    z = np.array([[np.inf, 1.0, np.inf, 0.0], [-np.inf] * 4], np.float32)
+    r = oracle.route(2, logits_in=z)
+    assert r["ids"][0].tolist() == [0, 2]
+    np.testing.assert_allclose(r["topk_p"][0], [0.5, 0.5])
+    np.testing.assert_allclose(r["topk_p"][1], [0.25, 0.25])
+
+
+def test_nan_score_is_an_error():
+    z = np.zeros((3, 4), np.float32)
+    z[1, 2] = np.nan
+    with pytest.raises(oracle.OracleError) as ei:
+        oracle.route(2, logits_in=z)
+    assert ei.value.status == 5
+    with pytest.raises(oracle.OracleError):
+        oracle.dispatch(z, 2, 4)
+
+
+# --------------------------------------------------------------------------- dispatch
+
+def test_worked_case_128_identical_tokens():
+    """128 identical tokens, E=8, k=2, cf=1.0 -> C=32 (closed form)."""
+    C = oracle.capacity(128, 2, 8, 1.0)
+    assert C == 32
+    s = np.tile(np.arange(8, 0, -1, dtype=np.float32), (128, 1))   # prefers 0 > 1 > ... > 7
+    d = oracle.dispatch(s, 2, C)
+    for t in range(128):
+        g = t // 32
+        assert d["assign"][t].tolist() == [g, g + 4]
+        assert d["slot"][t].tolist() == [t % 32, t % 32]
+    assert d["n_rerouted"] == 224 and d["n_dropped"] == 0
+    assert (d["counts"] == 32).all()
+    assert d["flags"][:32, 0].tolist() == [0] * 32
+    assert (d["flags"][32:, 0] == 1).all() and (d["flags"][:, 1] == 1).all()
+
+
+def test_page_overflow_case():
+    g = golden("overflow_mhpn_2_3.json")
+    T, E, C = g["T"], g["E"], g["C"]
+    s = np.zeros((T, E), np.float32)
+    s[:, g["first"]] = 2.0
+    s[:, g["second"]] = 1.0
+    d = oracle.dispatch(s, g["k"], C)
+    assert (d["assign"][:127, 0] == g["first"]).all()
+    assert d["counts"][g["first"]] == g["expect_first_count"]
+    assert d["assign"][127, 0] == g["expect_token_127"]
+    assert d["n_rerouted"] == g["expect_rerouted"] and d["flags"][127, 0] == 1
+
+
+def test_drop_case():
+    s = np.array([[2.0, 1.0], [2.0, 1.0]], np.float32)
+    d = oracle.dispatch(s, 2, 1)
+    assert d["assign"].tolist() == [[0, -1], [1, -1]]
+    assert d["flags"].tolist() == [[0, 2], [1, 2]]
+    assert d["n_dropped"] == 2 and d["n_rerouted"] == 1
+    assert d["cw"].tolist() == [[1.0, 0.0], [1.0, 0.0]]
+
+
+def test_capacity_zero_drops_everything():
+    s = np.random.default_rng(0).standard_normal((5, 4)).astype(np.float32)
+    d = oracle.dispatch(s, 2, 0)
+    assert (d["assign"] == -1).all() and d["n_dropped"] == 10 and d["perm"].size == 0
+
+
+def _greedy_any_position(s, k, C):
+    """Each entry takes the first expert in the WHOLE preference list that is
+    not full and not already serving the token (rank-major, token-minor)."""
+    T, E = s.shape
+    pref = [sorted(range(E), key=lambda e: (-float(s[t, e]), e)) for t in range(T)]
+    fill = [0] * E
+    assign = [[-1] * k for _ in range(T)]
+    for r in range(k):
+        for t in range(T):
+            for e in pref[t]:
+                if fill[e] < C and e not in assign[t][:r]:
+                    assign[t][r] = e
+                    fill[e] += 1
+                    break
+    return assign
+
+
+def _queue_simulation(s, k, C):
+    """Independent form: arrivals enter per-expert queues in the order
+    (rank, token); a queue at its limit bounces the arrival to the token's
+    next candidate (cyclic from its own pick, skipping the token's experts)."""
+    T, E = s.shape
+    queues = {e: [] for e in range(E)}
+    assign = [[-1] * k for _ in range(T)]
+    for r in range(k):
+        for t in range(T):
+            cand = sorted(range(E), key=lambda e: (-float(s[t, e]), e))
+            for e in cand[r:] + cand[:r]:
+                if e in assign[t]:
+                    continue
+                if len(queues[e]) < C:
+                    queues[e].append((t, r))
+                    assign[t][r] = e
+                    break
+    slots = {}
+    for e, q in queues.items():
+        for i, tr in enumerate(q):
+            slots[tr] = i
+    return assign, slots
+
+
+def test_dispatch_brute_force_tiny():
+    rng = np.random.default_rng(6)
+    for _ in range(400):
+        T = int(rng.integers(1, 7))
+        E = int(rng.integers(1, 6))
+        k = int(rng.integers(1, min(3, E) + 1))
+        C = int(rng.integers(0, 4))
+        s = rng.integers(-2, 3, (T, E)).astype(np.float32)
+        d = oracle.dispatch(s, k, C)
+        assert d["assign"].tolist() == _greedy_any_position(s, k, C)
+        qa, qs = _queue_simulation(s, k, C)
+        assert d["assign"].tolist() == qa
+        for t in range(T):
+            for r in range(k):
+                if qa[t][r] >= 0:
+                    assert d["slot"][t, r] == qs[(t, r)]
+
+
+def _check_dispatch_invariants(s, k, C, d):
+    T, E = s.shape
+    assign, slot, flags = d["assign"], d["slot"], d["flags"]
+    kept = assign >= 0
+    assert (d["counts"] <= C).all()
+    assert d["counts"].sum() == T * k - d["n_dropped"] == kept.sum()
+    assert np.array_equal(d["counts"], np.bincount(assign[kept], minlength=E))
+    assert d["offsets"][0] == 0 and np.array_equal(np.diff(d["offsets"]), d["counts"])
+    for t in range(T):
+        e_t = assign[t][assign[t] >= 0]
+        assert len(set(e_t.tolist())) == len(e_t)          # distinct experts per token
+    for e in range(E):
+        sl = np.sort(slot[assign == e])
+        assert np.array_equal(sl, np.arange(d["counts"][e]))
+    perm = d["perm"]
+    assert sorted(perm.tolist()) == sorted(np.flatnonzero(kept.ravel()).tolist())
+    for i, idx in enumerate(perm):
+        e = assign.ravel()[idx]
+        assert d["offsets"][e] <= i < d["offsets"][e + 1]
+        assert slot.ravel()[idx] == i - d["offsets"][e]
+    pref = np.array([oracle.preference(s[t]) for t in range(T)])
+    for t in range(T):
+        for r in range(k):
+            if assign[t, r] < 0:
+                assert flags[t, r] == 2
+                held = set(assign[t][assign[t] >= 0].tolist())
+                assert all(d["counts"][e] == C or e in held for e in range(E))
+            else:
+                assert flags[t, r] == (1 if assign[t, r] != pref[t, r] else 0)
+    assert d["n_rerouted"] == int((flags == 1).sum()) and d["n_dropped"] == int((flags == 2).sum())
+    cw = d["cw"]
+    tot = np.where(kept, cw, 0).sum(1)
+    assert np.all(np.abs(tot[kept.any(1)] - 1.0) < 1e-6)
+    assert (cw[~kept] == 0).all()
+
+
+@pytest.mark.parametrize("T,E,k,cf,skew", [(500, 8, 2, 1.0, 0.0), (300, 16, 2, 1.0, 2.0),
+                                            (200, 5, 3, 1.0, 1.0), (64, 8, 1, 1.25, 0.5)])
+def test_dispatch_invariants_random(T, E, k, cf, skew):
+    rng = np.random.default_rng(T + E)
+    s = rng.standard_normal((T, E)).astype(np.float32)
+    s[:, 0] += skew
+    s[T // 3: T // 3 + 40] = s[T // 3]       # a run of identical tokens
+    C = oracle.capacity(T, k, E, cf)
+    d = oracle.dispatch(s, k, C)
+    _check_dispatch_invariants(s, k, C, d)
+    assert d["assign"].tolist() == _greedy_any_position(s, k, C)
+
+
+def test_no_overflow_is_plain_topk_with_stable_slots():
+    rng = np.random.default_rng(7)
+    T, E, k = 120, 6, 2
+    s = rng.standard_normal((T, E)).astype(np.float32)
+    d = oracle.dispatch(s, k, T)
+    r = oracle.route(k, logits_in=s)
+    assert np.array_equal(d["assign"], r["ids"]) and d["n_rerouted"] == 0
+    seen = {}
+    for r_ in range(k):
+        for t in range(T):
+            e = int(d["assign"][t, r_])
+            assert d["slot"][t, r_] == seen.get(e, 0)
+            seen[e] = seen.get(e, 0) + 1
+
+
+def test_rank_major_order_matters():
+    """All rank-0 picks are placed before any rank-1 pick: token 1's first
+    choice beats token 0's second choice to the last slot."""
+    s = np.array([[3.0, 2.0, 0.0], [2.0, 3.0, 0.0]], np.float32)
+    d = oracle.dispatch(s, 2, 1)
+    # rank 0: t0 -> 0, t1 -> 1; rank 1: t0 wants 1 (full) -> 2; t1 wants 0 (full), 2 full -> drop
+    assert d["assign"].tolist() == [[0, 2], [1, -1]]
+
+
+# --------------------------------------------------------------------------- combine weights
+
+def test_combine_weight_page_example():
+    g = golden("combine_mhpn_4_3.json")
+    s = np.log(np.array([g["p"]], np.float64)).astype(np.float32)
+    d = oracle.dispatch(s, 2, 10)
+    # expert order follows the scores: p[1] > p[0]
+    got = {int(e): float(w) for e, w in zip(d["assign"][0], d["cw"][0])}
+    assert abs(got[0] - g["w"][0]) <= g["tol"] and abs(got[1] - g["w"][1]) <= g["tol"]
+    assert abs(got[0] - 2.1 / 5.8) < 1e-6
+
+
+def test_reroute_weight_uses_the_expert_actually_used():
+    # C=1.  Rank 0: token 0 takes expert 0, token 1 finds 0 full and takes 1.
+    # Rank 1: token 0 wants 1 (full) and takes 2; token 1 holds 1, so its next
+    # candidate is 3.  Token 1 uses (1, 3) and its weights renormalise p1, p3.
+    s = np.log(np.array([[0.5, 0.3, 0.15, 0.05], [0.55, 0.25, 0.05, 0.15]],
+                        np.float64)).astype(np.float32)
+    d = oracle.dispatch(s, 2, 1)
+    assert d["assign"].tolist() == [[0, 2], [1, 3]]
+    assert d["flags"].tolist() == [[0, 1], [1, 1]]
+    np.testing.assert_allclose(d["cw"][1], [0.25 / 0.4, 0.15 / 0.4], rtol=1e-6)
+    np.testing.assert_allclose(d["cw"][0], [0.5 / 0.65, 0.15 / 0.65], rtol=1e-6)
+
+
+def test_k1_weight_is_one():
+    s = np.random.default_rng(8).standard_normal((40, 5)).astype(np.float32)
+    d = oracle.dispatch(s, 1, 40)
+    assert (d["cw"] == 1.0).all()
+
+
+# --------------------------------------------------------------------------- experts
+
+def test_dense_swiglu_reduces_to_torch():
+    """E=1, k=1, no overflow: the layer is a dense SwiGLU FFN."""
+    rng = np.random.default_rng(9)
+    T, d, F = 9, 32, 48
+    h = bf16(rng.standard_normal((T, d)))
+    wr = bf16(rng.standard_normal((1, d)))
+    w1 = bf16(rng.standard_normal((1, F, d)) / math.sqrt(d))
+    w3 = bf16(rng.standard_normal((1, F, d)) / math.sqrt(d))
+    w2 = bf16(rng.standard_normal((1, d, F)) / math.sqrt(F))
+    r, dsp, out = oracle.layer_forward(h, wr, w1, w3, w2, k=1, C=T)
+    x = torch.from_numpy(widen(h)).double()
+    g = x @ torch.from_numpy(widen(w1)[0]).double().T
+    u = x @ torch.from_numpy(widen(w3)[0]).double().T
+    y = (torch.nn.functional.silu(g) * u) @ torch.from_numpy(widen(w2)[0]).double().T
+    np.testing.assert_allclose(out, y.numpy(), rtol=1e-6, atol=1e-6)
+
+
+def test_gate_and_up_branches_are_not_swapped():
+    """x = e_0; W1 rows c_j e_0 and W3 rows e_0 give a_j = silu(c_j);
+    swapping the branches gives a_j = silu(1) * c_j instead.  W2 = identity."""
+    d = F = 8
+    c = np.linspace(-3, 3, F)
+    x = np.zeros(d)
+    x[0] = 1.0
+    w1 = np.zeros((F, d))
+    w1[:, 0] = c
+    w3 = np.zeros((F, d))
+    w3[:, 0] = 1.0
+    w2 = np.eye(d, F)
+    y = oracle.expert_row(bf16(x), bf16(w1), bf16(w3), bf16(w2))
+    cb = widen(bf16(c)).astype(np.float64)
+    want = cb / (1.0 + np.exp(-cb))
+    np.testing.assert_allclose(y, want, rtol=1e-12)
+    swapped = oracle.expert_row(bf16(x), bf16(w3), bf16(w1), bf16(w2))
+    assert not np.allclose(swapped, want)
+
+
+def test_down_projection_orientation():
+    """W2 is [d, F] (out x in): a one-hot W2 row picks one activation."""
+    d, F = 4, 6
+    x = np.zeros(d)
+    x[1] = 1.0
+    w1 = np.zeros((F, d))
+    w1[:, 1] = 1.0
+    w3 = np.zeros((F, d))
+    w3[:, 1] = np.arange(1, F + 1)
+    w2 = np.zeros((d, F))
+    w2[2, 5] = 1.0
+    y = oracle.expert_row(bf16(x), bf16(w1), bf16(w3), bf16(w2))
+    s1 = 1.0 / (1.0 + math.exp(-1.0))
+    np.testing.assert_allclose(y, [0, 0, s1 * 6, 0], rtol=1e-12)
+
+
+def test_combine_rows_weights_and_drops():
+    rng = np.random.default_rng(10)
+    T, d, E, F, k = 6, 16, 3, 24, 2
+    h = bf16(rng.standard_normal((T, d)))
+    w1 = bf16(rng.standard_normal((E, F, d)) / 4)
+    w3 = bf16(rng.standard_normal((E, F, d)) / 4)
+    w2 = bf16(rng.standard_normal((E, d, F)) / 5)
+    assign = np.array([[0, 1], [2, -1], [-1, -1], [1, 0], [2, 0], [0, 2]], np.int32)
+    cw = np.array([[0.25, 0.75], [1, 0], [0, 0], [0.5, 0.5], [0.1, 0.9], [0.6, 0.4]], np.float32)
+    out = oracle.combine_rows(h, w1, w3, w2, assign, cw, np.arange(T))
+    assert (out[2] == 0).all()
+    for t in range(T):
+        want = np.zeros(d)
+        for r in range(k):
+            e = assign[t, r]
+            if e >= 0:
+                want += cw[t, r] * oracle.expert_row(h[t], w1[e], w3[e], w2[e])
+        np.testing.assert_allclose(out[t], want, rtol=1e-6, atol=1e-7)
+
+
+def test_expert_slots_follow_perm():
+    rng = np.random.default_rng(11)
+    T, d, E, F, k = 20, 16, 4, 32, 2
+    h = bf16(rng.standard_normal((T, d)))
+    w1 = bf16(rng.standard_normal((E, F, d)) / 4)
+    w3 = bf16(rng.standard_normal((E, F, d)) / 4)
+    w2 = bf16(rng.standard_normal((E, d, F)) / 5)
+    s = rng.standard_normal((T, E)).astype(np.float32)
+    dsp = oracle.dispatch(s, k, oracle.capacity(T, k, E, 1.0))
+    ys = oracle.expert_slots(h, w1, w3, w2, dsp["assign"], dsp["perm"], 0, dsp["perm"].size)
+    for i, idx in enumerate(dsp["perm"]):
+        t, r = divmod(int(idx), k)
+        e = dsp["assign"][t, r]
+        np.testing.assert_allclose(ys[i], oracle.expert_row(h[t], w1[e], w3[e], w2[e]),
+                                   rtol=1e-6, atol=1e-7)
+
+
+# --------------------------------------------------------------------------- the five workloads
+
+@pytest.mark.parametrize("name", synth.CONFIG_ORDER)
+def test_workload_router_statistics(name):
+    """Routing + dispatch of each workload's seeded inputs satisfy the
+    invariants, and the skewed workload's expert-0 rank-1 share is the
+    calibrated 42.66%."""
+    shape = synth.CONFIGS[name]
+    C = oracle.capacity(shape.T, shape.k, shape.E, shape.cf, shape.capacity)
+    if shape.T * shape.d <= 8192 * 4096:
+        h, wr, bias, usage = synth.router_inputs(shape)
+        r = oracle.route(shape.k, h=synth.bf16_bits(h), wr=synth.bf16_bits(wr),
+                         bias=None if bias is None else bias.numpy(),
+                         usage=None if usage is None else usage.numpy(), lam=shape.lam)
+        s = r["scores"]
+        assert r["counts_pre"].sum() == shape.T * shape.k
+    else:
+        rng = np.random.default_rng(shape.seed)
+        s = (rng.standard_normal((shape.T, shape.E)) * 0.02 * math.sqrt(shape.d)).astype(np.float32)
+    d = oracle.dispatch(s, shape.k, C)
+    assert (d["counts"] <= C).all()
+    assert d["counts"].sum() == shape.T * shape.k - d["n_dropped"]
+    if name == "skewed":
+        assert abs((oracle.route(2, logits_in=s)["ids"][:, 0] == 0).mean() - 0.4266) < 1e-3

@@ -1,0 +1,340 @@
+"""Benchmark: MoE-layer forward tokens/s on one GB300 (or N independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+A step is one full forward pass of the layer (router GEMM, routing, dispatch,
+gate-up GEMM with SwiGLU, down GEMM with the weighted combine, finalize) over
+one batch of the workload's seeded synthetic tokens, through the C ABI
+(moe_layer_forward), inputs resident in HBM.  Rank 0 prints one JSON line.
+
+Multi-GPU: one process per GPU (torchrun), each runs an independent replica
+of the layer on its own batch ("replicas only": the layer has no exchange
+step on one node with every expert resident); value = all ranks' tokens /
+the slowest rank's time.
+
+--impl reference times the CPU oracle (single thread) on a bounded sample of
+the same workload: routing and dispatch of the whole batch plus the expert FFN
+of a sample of kept rows, extrapolated by the kept-row count.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from token_level_top_gb300 import moe, synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at Mixtral shape (top-2); % of BF16 tensor / HBM roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "mixtral_prefill"
+KERNELS_PER_STEP = 7  # router GEMM, route, dispatch (2), gate-up, down, finalize
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.CONFIG_ORDER)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+def dist_setup(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index: int):
+        self.dev = dev_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200",
+                                          "-i", str(self.dev)], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def layer_inputs(shape, device="cuda"):
+    h, wr, bias, usage = synth.router_inputs(shape)
+    w1, w3, w2 = synth.expert_weights(shape, device=device)
+    L = dict(h=h.to(device), wr=wr.to(device), w1=w1, w3=w3, w2=w2,
+             bias=None if bias is None else bias.to(device),
+             usage=None if usage is None else usage.to(device))
+    L["w13"] = moe.pack_w13(w1, w3)
+    return L
+
+
+def oracle_sample(shape, h, wr, bias, usage, w1, w3, w2, budget_s=12.0, seed=0):
+    """Time the oracle: route + dispatch of the whole batch, expert FFN + combine
+    of sampled kept rows until ~budget_s; extrapolate by kept rows."""
+    import oracle
+    hb, wb = synth.bf16_bits(h), synth.bf16_bits(wr)
+    bnp = None if bias is None else bias.cpu().numpy()
+    unp = None if usage is None else usage.cpu().numpy()
+    C = oracle.capacity(shape.T, shape.k, shape.E, shape.cf, shape.capacity)
+    t0 = time.perf_counter()
+    r = oracle.route(shape.k, h=hb, wr=wb, bias=bnp, usage=unp, lam=shape.lam)
+    d = oracle.dispatch(r["scores"], shape.k, C)
+    t_rd = time.perf_counter() - t0
+    kept = int(d["offsets"][-1])
+    w1b, w3b, w2b = synth.bf16_bits(w1), synth.bf16_bits(w3), synth.bf16_bits(w2)
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(kept)
+    rows, t_ffn = 0, 0.0
+    while rows < kept and (t_rd + t_ffn) < budget_s:
+        i = int(order[rows])
+        t1 = time.perf_counter()
+        oracle.expert_slots(hb, w1b, w3b, w2b, d["assign"], d["perm"], i, i + 1)
+        t_ffn += time.perf_counter() - t1
+        rows += 1
+    t_total = t_rd + (t_ffn / max(rows, 1)) * kept
+    return dict(t_route_dispatch=t_rd, ffn_rows=rows, kept=kept, t_ffn_sample=t_ffn,
+                t_total=t_total, tokens_per_s=shape.T / t_total)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    shape = synth.CONFIGS[args.workload]
+    h, wr, bias, usage = synth.router_inputs(shape)
+    w1, w3, w2 = synth.expert_weights(shape, device="cpu")
+    per_step = max(2.0, 60.0 / max(args.steps + args.warmup, 1))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        res = oracle_sample(shape, h, wr, bias, usage, w1, w3, w2, budget_s=per_step, seed=i)
+        if i >= args.warmup:
+            vals.append(res)
+    v = statistics.median(r["tokens_per_s"] for r in vals)
+    sample = (f"per step: route+dispatch of all {shape.T} tokens, expert FFN of "
+              f"{vals[-1]['ffn_rows']} of {vals[-1]['kept']} kept rows, extrapolated by kept rows")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * shape.T / v, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(shape),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(shape):
+    return {"workload": shape.name, "T": shape.T, "d_model": shape.d, "E": shape.E, "k": shape.k,
+            "d_ff": shape.F, "cf": shape.cf, "lambda": shape.lam,
+            "capacity": moe.capacity(shape.T, shape.k, shape.E, shape.cf, shape.capacity),
+            "parallelism": "replicas", "l2": "inputs larger than L2: every step streams "
+            f"{3 * shape.E * shape.F * shape.d * 2 / 1e9:.2f} GB of expert weights"}
+
+
+def run_ours(args, rank, world, local):
+    assert torch.cuda.is_available(), "the CUDA path needs a GPU (there is no CPU fallback)"
+    from token_level_top_gb300 import build
+    if world == 1 or rank == 0:
+        build.build()
+    barrier(world)
+    moe.lib()
+    shape = synth.CONFIGS[args.workload]
+    L = layer_inputs(shape)
+    cfg = moe.Config.of(shape)
+    ws = moe.workspace(cfg)
+    out = torch.empty(shape.T, shape.d, dtype=torch.bfloat16, device="cuda")
+    # kept rows of this batch (routing is deterministic, identical every step)
+    _, aux = moe.layer_forward(cfg, ws, L["h"], L["wr"], L["w13"], L["w2"], L["bias"], L["usage"],
+                               aux=True, out=out)
+    kept = int(aux["counts"].sum().item())
+    st = moe.device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({moe.STATUS.get(st)})")
+
+    def step(evs=None):
+        moe.layer_forward(cfg, ws, L["h"], L["wr"], L["w13"], L["w2"], L["bias"], L["usage"],
+                          stage_events=evs, out=out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stage_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)]
+                 for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(args.steps):
+        step(stage_evs[i])
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    ms_max = max_over_ranks(ms, world)
+    st = moe.device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({moe.STATUS.get(st)}) after the timed region")
+    stage_ms = {n: statistics.mean(stage_evs[i][j].elapsed_time(stage_evs[i][j + 1])
+                                   for i in range(args.steps))
+                for j, n in enumerate(moe.STAGE_NAMES)}
+
+    # end to end from pinned host memory through moe_layer_forward_host
+    h_host = L["h"].cpu().pin_memory()
+    o_host = torch.empty(shape.T, shape.d, dtype=torch.bfloat16).pin_memory()
+    moe.layer_forward_host(cfg, ws, h_host, L["wr"], L["w13"], L["w2"], o_host, L["bias"],
+                           L["usage"])
+    barrier(world)
+    te0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        moe.layer_forward_host(cfg, ws, h_host, L["wr"], L["w13"], L["w2"], o_host, L["bias"],
+                               L["usage"])
+    te = max_over_ranks(time.perf_counter() - te0, world)
+
+    peaks, peak_kind = load_peaks()
+    d, F, T = shape.d, shape.F, shape.T
+    flops = {"gate_up": 2.0 * kept * d * 2 * F, "down": 2.0 * kept * F * d}
+    dom = max(("gate_up", "down"), key=lambda n: stage_ms[n])
+    achieved = flops[dom] / (stage_ms[dom] * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    expert_tflops = (flops["gate_up"] + flops["down"]) / (
+        (stage_ms["gate_up"] + stage_ms["down"]) * 1e-3) / 1e12
+    weight_bytes = 3.0 * shape.E * F * d * 2
+    value = world * T * args.steps / (ms_max * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(shape),
+        "roofline": {"kernel": f"moe_gemm_kernel ({dom.replace('_', '-')})", "bound": "tensor",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long loop)"},
+        "expert_gemm_tflops": expert_tflops,
+        "weight_stream_gbs": weight_bytes / ((stage_ms["gate_up"] + stage_ms["down"]) * 1e-3) / 1e9,
+        "stages_ms": stage_ms, "kept_rows": kept,
+        "clocks": clk,
+        "e2e": {"value": world * T * args.e2e_steps / te, "unit": UNIT,
+                "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res = oracle_sample(shape, L["h"].cpu(), L["wr"].cpu(),
+                            None if L["bias"] is None else L["bias"].cpu(),
+                            None if L["usage"] is None else L["usage"].cpu(),
+                            L["w1"], L["w3"], L["w2"])
+        line["cpu_baseline"] = {
+            "value": res["tokens_per_s"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"route+dispatch of all {T} tokens ({res['t_route_dispatch']:.2f} s), "
+                       f"expert FFN of {res['ffn_rows']} of {res['kept']} kept rows "
+                       f"({res['t_ffn_sample']:.1f} s), extrapolated by kept rows")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

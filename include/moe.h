@@ -1,0 +1,209 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MoE-layer forward library, libmoe.so.
+ *
+ * One sparsely activated Mixture-of-Experts FFN layer, forward only, on one
+ * GPU with every expert resident in HBM:
+ *
+ *   router GEMM -> load penalty -> softmax + top-k -> capacity-capped
+ *   dispatch with reroute/drop -> grouped SwiGLU experts -> weighted combine
+ *
+ * Pages that state the method (cited below by their bracketed key):
+ *   [mhpn]     "GPT-4稀疏激活真相：万亿参数模型的MoE工程落地实践"
+ *              (www.mhpn.cn/news/895310)
+ *   [coreui]   "MoE架构揭秘：逐Token路由与活跃参数量的工程真相"
+ *              (www.coreui.cn/article/2635427.html)
+ *   [cnnetsun] "MoE稀疏激活原理与工程实践：从2%激活率到高效推理"
+ *              (cnnetsun.cn/a/3071834)
+ *   [csdn]     untitled page, adg.csdn.net/6a3116e610ee7a33f27ddf1c.html
+ *   [2kiu]     MoE page at www.2kiu.com/news/5042631/
+ *
+ * Conventions for every entry point
+ *   - Pointers named *_dev are DEVICE pointers owned by the caller; the
+ *     library never allocates, frees or synchronises on the forward path
+ *     (the lesson of the per-expert cudaMallocAsync leak on [cnnetsun] §5.2).
+ *     All scratch lives in the caller's workspace `ws` (size from
+ *     moe_workspace_size, 256-byte aligned, initialised once with
+ *     moe_workspace_init).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous and stream-ordered; they enqueue kernels and small memset
+ *     nodes only.
+ *   - Argument, shape, alignment and workspace errors are returned
+ *     synchronously, before anything is enqueued.  Errors detected on the
+ *     device (NaN scores, a bounded wait that ran out) set a status word in
+ *     the workspace, read with moe_get_device_status.  Kernels never trap.
+ *   - bf16 tensors are IEEE bfloat16, row-major, 16-byte aligned.
+ *   - Supported: 1 <= k <= 8, k <= E <= 255, d_model % 64 == 0,
+ *     d_ff % 128 == 0, T >= 1 (T = 0 is a no-op).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* null required pointer, bad shape or value */
+    MOE_ERR_UNSUPPORTED = 2,   /* shape outside the supported set above */
+    MOE_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte (ws: 256-byte) aligned */
+    MOE_ERR_WORKSPACE = 4,     /* ws_bytes < moe_workspace_size(cfg) */
+    MOE_ERR_NONFINITE = 5,     /* device: a score was NaN */
+    MOE_ERR_TIMEOUT = 6,       /* device: a bounded wait ran out */
+    MOE_ERR_CUDA = 7           /* a CUDA runtime call failed */
+} moe_status_t;
+
+/* Layer shape.  Capacity C = ceil(T*k*cf/E) unless capacity > 0. */
+typedef struct {
+    int32_t T;        /* tokens in the batch */
+    int32_t d_model;  /* hidden size d */
+    int32_t E;        /* number of experts */
+    int32_t k;        /* experts per token (top-k) */
+    int32_t d_ff;     /* expert intermediate size F */
+    double cf;        /* capacity factor, read as a decimal with 6 fractional digits */
+    int32_t capacity; /* > 0: explicit per-expert capacity, overrides cf */
+    float lambda;     /* load-penalty weight (0 = no penalty) */
+    uint32_t flags;   /* reserved, must be 0 */
+} moe_config_t;
+
+/* Number of stage boundaries recorded by moe_layer_forward's stage_events. */
+#define MOE_NUM_STAGES 6
+
+/* Expert capacity C = ceil(T*k*cf/E), exact, with cf read as a decimal with
+ * six fractional digits ([coreui] §5.2: ceil(batch*top_k/num_experts*1.3);
+ * [coreui] §3.3: Capacity = (Batch*K)/N*alpha).  explicit_cap > 0 is
+ * returned as is.  Returns 0 for non-positive inputs. */
+int64_t moe_capacity(int64_t T, int32_t k, int32_t E, double cf, int32_t explicit_cap);
+
+/* Bytes of workspace that every call with this config needs (0 on a bad
+ * config).  The workspace is reusable across calls with the same or a
+ * smaller config; calls that share one workspace must not overlap. */
+size_t moe_workspace_size(const moe_config_t* cfg);
+
+/* Clears the workspace's device status word.  Call once after allocating a
+ * workspace (enqueued on `stream`). */
+moe_status_t moe_workspace_init(void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, returns the device status word recorded in `ws`
+ * since the last read (MOE_OK if none) and clears it. */
+moe_status_t moe_get_device_status(void* ws_dev, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status_t st);
+
+/* Re-lays out the gate and up projections into the fused gate-up operand.
+ *   w1_dev, w3_dev  [E, F, d] bf16 (nn.Linear out x in: W1 = gate, W3 = up)
+ *   w13_dev         [E, 2F, d] bf16 out.  For each expert, block j of 256
+ *                   rows holds W1 rows [128j, 128j+128) followed by W3 rows
+ *                   [128j, 128j+128), so one 256-row tile carries matching
+ *                   gate and up columns ([mhpn] §3.1, [2kiu] §1: the
+ *                   W1/W2/W3 SwiGLU expert).
+ * Requires F % 128 == 0, d % 64 == 0. */
+moe_status_t moe_pack_w13(int32_t E, int32_t F, int32_t d, const void* w1_dev,
+                          const void* w3_dev, void* w13_dev, void* stream);
+
+/* Router: logits, penalised scores, top-k picks and load statistics.
+ *   z = h . W_r^T (+ b)                       [coreui] §3.1, [csdn] §3.1
+ *   s_i = z_i - lambda * usage_i (fp32, no FMA) [mhpn] §2.3 (second check),
+ *                                             [cnnetsun] §3.1 (before top-k)
+ *   p = softmax(s); picks = the k best s, ties to the lower expert index
+ *   f_i = (#picks of i)/T, P_i = mean_t p_i   [cnnetsun] §4.2, [coreui] §3.1
+ * Inputs:
+ *   h_dev        [T, d] bf16 (ignored when logits_in_dev != NULL)
+ *   w_router_dev [E, d] bf16 (row e = expert e's gate vector)
+ *   bias_dev     [E] fp32 or NULL        usage_dev [E] fp32 or NULL
+ *   logits_in_dev[T, E] fp32 or NULL: final logits given (no GEMM, no bias)
+ * Outputs (each may be NULL unless noted):
+ *   logits_out_dev [T, E] fp32; scores_out_dev [T, E] fp32 (penalised);
+ *   topk_ids_dev [T, k] int32 (required); topk_w_dev [T, k] fp32 (softmax
+ *   probability of each pick); counts_pre_dev [E] int32 (picks per expert
+ *   before capacity); f_dev [E], P_dev [E] fp32.
+ * NaN scores set MOE_ERR_NONFINITE on the device (NaN then ranks last). */
+moe_status_t moe_route(const moe_config_t* cfg, const void* h_dev, const void* w_router_dev,
+                       const float* bias_dev, const float* usage_dev,
+                       const float* logits_in_dev, float* logits_out_dev, float* scores_out_dev,
+                       int32_t* topk_ids_dev, float* topk_w_dev, int32_t* counts_pre_dev,
+                       float* f_dev, float* P_dev, void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Capacity-capped dispatch on penalised scores ([mhpn] §2.3, third check;
+ * [2kiu] §2; [coreui] §3.3).  Slots fill in entry order (rank, token): every
+ * rank-0 pick before any rank-1 pick, tokens in index order.  An entry takes
+ * the first expert of its preference order that is not full and not already
+ * serving the token; when none is left it is dropped.
+ *   scores_dev [T, E] fp32 (penalised scores, e.g. moe_route's scores_out)
+ * Outputs (all required):
+ *   assign_dev [T, k] int32 expert used (-1 = dropped); slot_dev [T, k] int32
+ *   position in the expert's slot list (-1 = dropped); flags_dev [T, k] u8
+ *   (bit0 rerouted, bit1 dropped); counts_dev [E] int32; offsets_dev [E+1]
+ *   int32 (exclusive scan of counts); perm_dev [T*k] int32: slot order, entry
+ *   perm[offsets[e] + slot] = t*k + r, entries past offsets[E] untouched;
+ *   combine_w_dev [T, k] fp32: p of the expert used, renormalised over the
+ *   token's kept experts ([mhpn] §4.3), 0 when dropped; n_rerouted_dev [1],
+ *   n_dropped_dev [1] int32. */
+moe_status_t moe_dispatch(const moe_config_t* cfg, const float* scores_dev, int32_t* assign_dev,
+                          int32_t* slot_dev, uint8_t* flags_dev, int32_t* counts_dev,
+                          int32_t* offsets_dev, int32_t* perm_dev, float* combine_w_dev,
+                          int32_t* n_rerouted_dev, int32_t* n_dropped_dev,
+                          void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Grouped SwiGLU experts over the dispatched slots ([mhpn] §3.1; [2kiu] §1;
+ * [cnnetsun] §3.2 step 1, tokens grouped into E sub-batches):
+ *   for slot i of expert e (offsets[e] <= i < offsets[e+1]), t = perm[i]/k:
+ *   y_slots[i] = W2_e (silu(W1_e h_t) * (W3_e h_t))
+ *   h_dev [T, d] bf16; perm_dev, offsets_dev as from moe_dispatch;
+ *   w13_dev [E, 2F, d] bf16 from moe_pack_w13; w2_dev [E, d, F] bf16;
+ *   y_slots_dev [T*k, d] bf16 out (rows past offsets[E] untouched).
+ * The intermediate silu(g)*u is rounded to bf16 between the two GEMMs. */
+moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* h_dev, const int32_t* perm_dev,
+                            const int32_t* offsets_dev, const void* w13_dev, const void* w2_dev,
+                            void* y_slots_dev, void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Probability-weighted combine back to token order ([mhpn] §4.3; [2kiu] §3
+ * step 5): out[t] = sum over kept r, in rank order, of combine_w[t,r] *
+ * y_slots[offsets[assign[t,r]] + slot[t,r]]; tokens with nothing kept get 0.
+ * Accumulates in fp32, stores bf16.  out_dev [T, d] bf16. */
+moe_status_t moe_combine(const moe_config_t* cfg, const void* y_slots_dev,
+                         const int32_t* assign_dev, const int32_t* slot_dev,
+                         const int32_t* offsets_dev, const float* combine_w_dev, void* out_dev,
+                         void* stream);
+
+/* The fused layer: route, dispatch, experts with the token gather fused into
+ * the gate-up GEMM's operand load and the weighted scatter fused into the
+ * down GEMM's epilogue (fp32 accumulation, bf16 output).
+ *   h_dev [T, d] bf16; w_router_dev [E, d]; bias_dev, usage_dev as in
+ *   moe_route; w13_dev [E, 2F, d]; w2_dev [E, d, F]; out_dev [T, d] bf16.
+ * Optional outputs (NULL to skip): logits_out [T,E], assign/slot [T,k] int32,
+ *   flags [T,k] u8, counts [E] int32, f/P [E] fp32.
+ * stage_events: NULL, or MOE_NUM_STAGES+1 cudaEvent_t recorded on `stream`
+ *   at the boundaries route | dispatch | zero | gate-up | down | finalize. */
+moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* h_dev,
+                               const void* w_router_dev, const float* bias_dev,
+                               const float* usage_dev, const void* w13_dev, const void* w2_dev,
+                               void* out_dev, float* logits_out_dev, int32_t* assign_dev,
+                               int32_t* slot_dev, uint8_t* flags_dev, int32_t* counts_dev,
+                               float* f_dev, float* P_dev, void* const* stage_events,
+                               void* ws_dev, size_t ws_bytes, void* stream);
+
+/* The same layer from host memory, end to end: copies h (pinned host,
+ * [T,d] bf16) to the workspace, runs moe_layer_forward and copies the output
+ * back to out_host ([T,d] bf16), all on `stream`; returns after the stream
+ * has finished.  Weights stay resident on the device. */
+moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* h_host,
+                                    const void* w_router_dev, const float* bias_dev,
+                                    const float* usage_dev, const void* w13_dev,
+                                    const void* w2_dev, void* out_host,
+                                    void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Failure-path check: launches one kernel whose bounded wait has nothing to
+ * wait for; after `budget_cycles` SM clock cycles it records MOE_ERR_TIMEOUT
+ * in the workspace status word and returns.  Used by the tests. */
+moe_status_t moe_debug_timeout_probe(void* ws_dev, size_t ws_bytes, int64_t budget_cycles,
+                                     void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,128 @@
+"""The C-ABI library without a GPU: it loads, exports every function that
+include/moe.h declares, and its host-side logic (capacity, workspace sizing,
+synchronous argument checks) behaves as documented.  No call here reaches a
+kernel: every case returns before anything is enqueued."""
+import ctypes
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from token_level_top_gb300 import build, moe, synth
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return moe.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = moe.header_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(L, n), f"libmoe.so does not export {n}"
+    assert set(names) == set(moe._SIGS), "binding signatures out of sync with include/moe.h"
+
+
+def test_capacity_matches_oracle(L):
+    rng = np.random.default_rng(0)
+    for _ in range(500):
+        T = int(rng.integers(1, 100000))
+        k = int(rng.integers(1, 9))
+        E = int(rng.integers(1, 256))
+        cf = float(np.round(rng.uniform(0.1, 4.0), int(rng.integers(0, 7))))
+        if cf <= 0:
+            continue
+        assert L.moe_capacity(T, k, E, cf, 0) == oracle.capacity(T, k, E, cf)
+    for shape in synth.CONFIGS.values():
+        assert L.moe_capacity(shape.T, shape.k, shape.E, shape.cf, 0) == math.ceil(
+            round(shape.T * shape.k * shape.cf / shape.E, 9))
+    assert L.moe_capacity(32, 2, 64, 1.3, 0) == 2
+    assert L.moe_capacity(100, 2, 26, 1.3, 0) == 10
+    assert L.moe_capacity(100, 2, 26, 1.3, 7) == 7
+    assert L.moe_capacity(0, 2, 8, 1.0, 0) == 0
+
+
+def _cfg(**kw):
+    d = dict(T=256, d_model=512, E=8, k=2, d_ff=1024, cf=1.25, capacity=0, lam=0.0)
+    d.update(kw)
+    return moe.Config(**d).c()
+
+
+def test_workspace_size(L):
+    sizes = []
+    for shape in synth.CONFIGS.values():
+        c = moe.Config.of(shape).c()
+        n = L.moe_workspace_size(ctypes.byref(c))
+        assert n > 0 and n % 256 == 0
+        sizes.append(n)
+    assert sizes[1] > sizes[0]
+    for bad in [dict(E=256), dict(k=9), dict(k=3, E=2), dict(d_model=100), dict(d_ff=200),
+                dict(cf=0.0), dict(T=-1)]:
+        c = _cfg(**bad)
+        assert L.moe_workspace_size(ctypes.byref(c)) == 0, bad
+    c = _cfg()
+    c.flags = 1
+    assert L.moe_workspace_size(ctypes.byref(c)) == 0
+
+
+FAKE = 0x7f0000000000  # never dereferenced: every case below fails validation first
+
+
+def test_route_argument_checks(L):
+    c = _cfg()
+    ws_n = L.moe_workspace_size(ctypes.byref(c))
+    P = ctypes.c_void_p
+    args = lambda **o: [ctypes.byref(o.get("cfg", c)), P(o.get("h", FAKE)), P(o.get("wr", FAKE)),
+                        None, None, None, None, None, P(o.get("ids", FAKE)), None, None, None, None,
+                        P(o.get("ws", FAKE)), o.get("n", ws_n), None]
+    assert L.moe_route(*args(ids=None)) == 1
+    assert L.moe_route(*args(h=None)) == 1
+    assert L.moe_route(*args(h=FAKE + 8)) == 3
+    assert L.moe_route(*args(ws=FAKE + 128)) == 3
+    assert L.moe_route(*args(ws=None)) == 1
+    assert L.moe_route(*args(n=ws_n - 1)) == 4
+    assert L.moe_route(*args(cfg=_cfg(E=300))) == 2
+    assert L.moe_route(None, *args()[1:]) == 1
+
+
+def test_layer_forward_argument_checks(L):
+    c = _cfg()
+    n = L.moe_workspace_size(ctypes.byref(c))
+    P = ctypes.c_void_p
+    base = [P(FAKE)] * 2 + [None, None] + [P(FAKE)] * 3 + [None] * 8
+    call = lambda cfg, ptrs, ws=FAKE, nb=n: L.moe_layer_forward(ctypes.byref(cfg), *ptrs, P(ws), nb,
+                                                                None)
+    assert call(c, base, nb=n - 256) == 4
+    bad = list(base)
+    bad[5] = P(FAKE + 2)                       # w2 misaligned
+    assert call(c, bad) == 3
+    bad = list(base)
+    bad[6] = None                              # out missing
+    assert call(c, bad) == 1
+    assert call(_cfg(d_ff=192), base) == 2     # d_ff % 128 != 0
+    assert call(_cfg(k=0), base) == 1
+
+
+def test_dispatch_and_ffn_argument_checks(L):
+    c = _cfg()
+    n = L.moe_workspace_size(ctypes.byref(c))
+    P = ctypes.c_void_p
+    outs = [P(FAKE)] * 9    # assign, slot, flags, counts, offsets, perm, cw, n_rerouted, n_dropped
+    assert L.moe_dispatch(ctypes.byref(c), None, *outs, P(FAKE), n, None) == 1
+    assert L.moe_dispatch(ctypes.byref(c), P(FAKE), *outs[:-1], None, P(FAKE), n, None) == 1
+    assert L.moe_expert_ffn(ctypes.byref(c), P(FAKE + 4), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                            P(FAKE), P(FAKE), n, None) == 3
+    assert L.moe_combine(ctypes.byref(c), None, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                         None) == 1
+    assert L.moe_pack_w13(8, 100, 512, P(FAKE), P(FAKE), P(FAKE), None) == 2
+    assert L.moe_pack_w13(8, 128, 512, P(FAKE), P(FAKE + 1), P(FAKE), None) == 3
+    assert L.moe_debug_timeout_probe(P(FAKE), 256, 0, None) == 1
+    assert L.moe_workspace_init(P(FAKE + 64), 4096, None) == 3
+
+
+def test_status_strings(L):
+    for code, text in moe.STATUS.items():
+        assert L.moe_status_string(code).decode() == text

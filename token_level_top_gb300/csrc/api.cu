@@ -1,0 +1,540 @@
+// api.cu -- the C ABI of libmoe: argument checks, workspace layout and the
+// ordering of the kernels on the caller's stream.  No allocation, no
+// synchronisation on the forward path (moe_layer_forward_host and
+// moe_get_device_status are the documented synchronous exceptions).
+#include <math.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+constexpr int kMaxE = 255;  // expert ids are kept in bytes; 255 marks "none"
+constexpr int kMaxK = 8;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Shape checks shared by every entry point; `need_ff` adds the expert-FFN ones.
+moe_status_t check_config(const moe_config_t* c, bool need_ff)
+{
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->flags != 0) return MOE_ERR_INVALID_ARG;
+    if (c->T < 0 || c->E <= 0 || c->k <= 0) return MOE_ERR_INVALID_ARG;
+    if (c->k > c->E) return MOE_ERR_INVALID_ARG;
+    if (c->capacity < 0) return MOE_ERR_INVALID_ARG;
+    if (c->capacity == 0 && !(c->cf > 0.0 && c->cf <= 100.0)) return MOE_ERR_INVALID_ARG;
+    if (!isfinite(c->lambda)) return MOE_ERR_INVALID_ARG;
+    if (c->E > kMaxE || c->k > kMaxK) return MOE_ERR_UNSUPPORTED;
+    if (c->d_model <= 0 || c->d_model % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if (need_ff && (c->d_ff <= 0 || c->d_ff % 128 != 0)) return MOE_ERR_UNSUPPORTED;
+    if (static_cast<long long>(c->T) * c->k > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status_t check_ws(const moe_config_t* c, void* ws, size_t ws_bytes, WsLayout* L)
+{
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned(ws, 256)) return MOE_ERR_MISALIGNED;
+    if (!layout_for(*c, L)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < L->total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+int64_t capacity_of(const moe_config_t& c)
+{
+    return moe_capacity(c.T, c.k, c.E, c.cf, c.capacity);
+}
+
+struct Ev {
+    void* const* ev;
+    cudaStream_t s;
+    void mark(int i) const
+    {
+        if (ev && ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
+    }
+};
+
+}  // namespace
+
+int num_sms()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+int router_splits(int T, int d)
+{
+    const int mt = (T + kBM - 1) / kBM;
+    const int kb = d / kBK;
+    int S = (320 + mt - 1) / std::max(mt, 1);
+    S = std::max(1, std::min(S, std::max(1, kb / 2)));
+    // no empty split: (S - 1) * ceil(kb / S) < kb
+    while (S > 1 && (S - 1) * ((kb + S - 1) / S) >= kb) --S;
+    return S;
+}
+
+bool layout_for(const moe_config_t& c, WsLayout* L)
+{
+    const size_t T = static_cast<size_t>(std::max(c.T, 0));
+    const size_t E = static_cast<size_t>(c.E), k = static_cast<size_t>(c.k);
+    const size_t d = static_cast<size_t>(c.d_model), F = static_cast<size_t>(std::max(c.d_ff, 0));
+    WsLayout w;
+    w.nchunks = static_cast<int>((T + kChunk - 1) / kChunk);
+    w.splits = router_splits(static_cast<int>(T), static_cast<int>(d));
+    w.epad = static_cast<int>(std::max<size_t>(32, round_up(E, 32)));
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += round_up(std::max<size_t>(bytes, 1), 256);
+        return o;
+    };
+    const size_t nch = static_cast<size_t>(w.nchunks);
+    w.status = take(256);
+    w.ctrl = take(CTRL_WORDS * 4);
+    w.part = take(static_cast<size_t>(w.splits) * T * E * 4);
+    w.scores = take(T * E * 4);
+    w.ids = take(T * k * 4);
+    w.prefs = take(T * kPrefLen);
+    w.crank = take(T * k * 4);
+    w.hist = take(k * nch * E * 4);
+    w.base = take(k * nch * E * 4 + T * k);
+    w.ppart = take(nch * E * 4);
+    w.assign = take(T * k * 4);
+    w.slot = take(T * k * 4);
+    w.flags = take(T * k);
+    w.counts = take(E * 4);
+    w.offsets = take((E + 1) * 4);
+    w.perm = take(T * k * 4);
+    w.cw = take(T * k * 4);
+    w.act = take(T * k * F * 2);
+    w.out_acc = take(T * d * 4);
+    w.y_slots = (k > 2) ? take(T * k * d * 2) : 0;
+    w.h_stage = take(T * d * 2);
+    w.out_stage = take(T * d * 2);
+    w.total = off;
+    *L = w;
+    return true;
+}
+
+namespace {
+
+moe_status_t run_route(const moe_config_t& c, const WsLayout& L, const void* h, const void* wr,
+                       const float* bias, const float* usage, const float* logits_in,
+                       float* logits_out, float* scores_out, int32_t* ids_user, float* topk_w,
+                       void* ws, cudaStream_t s)
+{
+    int* status = ws_at<int>(ws, L.status);
+    if (!logits_in) {
+        GemmLaunch g{};
+        g.kind = GK_ROUTER;
+        g.E = c.E;
+        g.T = c.T;
+        g.topk = c.k;
+        g.d = c.d_model;
+        g.F = c.d_ff;
+        g.a_ptr = h;
+        g.b_ptr = wr;
+        g.router_part = ws_at<float>(ws, L.part);
+        g.splits = L.splits;
+        g.epad = L.epad;
+        g.status = status;
+        g.budget = kSpinBudget;
+        cudaError_t e = launch_gemm(g, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    RouteArgs a{};
+    a.T = c.T;
+    a.E = c.E;
+    a.k = c.k;
+    a.d = c.d_model;
+    a.splits = L.splits;
+    a.epad = L.epad;
+    a.nchunks = L.nchunks;
+    a.part = logits_in ? nullptr : ws_at<float>(ws, L.part);
+    a.logits_in = logits_in;
+    a.bias = logits_in ? nullptr : bias;
+    a.usage = usage;
+    a.lambda = c.lambda;
+    a.logits_out = logits_out;
+    a.scores_user = scores_out;
+    a.scores_ws = ws_at<float>(ws, L.scores);
+    a.ids_user = ids_user;
+    a.topk_w = topk_w;
+    a.ids_ws = ws_at<int32_t>(ws, L.ids);
+    a.prefs = ws_at<uint8_t>(ws, L.prefs);
+    a.crank = ws_at<int32_t>(ws, L.crank);
+    a.hist = ws_at<int32_t>(ws, L.hist);
+    a.ppart = ws_at<float>(ws, L.ppart);
+    a.status = status;
+    return cuda_status(launch_route(a, s));
+}
+
+moe_status_t run_stats(const moe_config_t& c, const WsLayout& L, int32_t* counts_pre, float* f,
+                       float* P, void* ws, cudaStream_t s)
+{
+    if (!counts_pre && !f && !P) return MOE_OK;
+    StatsArgs a{};
+    a.T = c.T;
+    a.E = c.E;
+    a.k = c.k;
+    a.nchunks = L.nchunks;
+    a.hist = ws_at<int32_t>(ws, L.hist);
+    a.ppart = ws_at<float>(ws, L.ppart);
+    a.counts_pre = counts_pre;
+    a.f = f;
+    a.P = P;
+    return cuda_status(launch_route_stats(a, s));
+}
+
+struct DispatchOut {
+    int32_t *assign, *slot, *counts, *offsets, *perm;
+    uint8_t* flags;
+    float* cw;
+    int32_t *n_rerouted, *n_dropped;
+};
+
+moe_status_t run_dispatch(const moe_config_t& c, const WsLayout& L, const float* scores,
+                          const DispatchOut& o, void* ws, cudaStream_t s)
+{
+    DispatchArgs a{};
+    a.T = c.T;
+    a.E = c.E;
+    a.k = c.k;
+    a.nchunks = L.nchunks;
+    a.C = capacity_of(c);
+    a.scores = scores;
+    a.ids = ws_at<int32_t>(ws, L.ids);
+    a.prefs = ws_at<uint8_t>(ws, L.prefs);
+    a.crank = ws_at<int32_t>(ws, L.crank);
+    a.hist = ws_at<int32_t>(ws, L.hist);
+    a.base = ws_at<int32_t>(ws, L.base);
+    a.ctrl = ws_at<int32_t>(ws, L.ctrl);
+    a.assign = o.assign;
+    a.slot = o.slot;
+    a.flags = o.flags;
+    a.counts = o.counts;
+    a.offsets = o.offsets;
+    a.perm = o.perm;
+    a.cw = o.cw;
+    a.n_rerouted = o.n_rerouted;
+    a.n_dropped = o.n_dropped;
+    a.status = ws_at<int>(ws, L.status);
+    return cuda_status(launch_dispatch(a, s));
+}
+
+GemmLaunch expert_gemm(const moe_config_t& c, const WsLayout& L, int kind, void* ws)
+{
+    GemmLaunch g{};
+    g.kind = kind;
+    g.E = c.E;
+    g.T = c.T;
+    g.topk = c.k;
+    g.d = c.d_model;
+    g.F = c.d_ff;
+    g.status = ws_at<int>(ws, L.status);
+    g.budget = kSpinBudget;
+    return g;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int64_t moe_capacity(int64_t T, int32_t k, int32_t E, double cf, int32_t explicit_cap)
+{
+    if (explicit_cap > 0) return explicit_cap;
+    if (T <= 0 || k <= 0 || E <= 0 || !(cf > 0.0) || cf > 100.0) return 0;
+    const long long cf_micro = llround(cf * 1e6);  // cf as a decimal, 6 fractional digits
+    const long long num = static_cast<long long>(T) * k * cf_micro;
+    const long long den = static_cast<long long>(E) * 1000000LL;
+    return (num + den - 1) / den;
+}
+
+size_t moe_workspace_size(const moe_config_t* cfg)
+{
+    if (check_config(cfg, cfg && cfg->d_ff > 0) != MOE_OK) return 0;
+    WsLayout L;
+    if (!layout_for(*cfg, &L)) return 0;
+    return L.total;
+}
+
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream)
+{
+    if (!ws || ws_bytes < 256) return MOE_ERR_INVALID_ARG;
+    if (!aligned(ws, 256)) return MOE_ERR_MISALIGNED;
+    return cuda_status(cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_get_device_status(void* ws, void* stream)
+{
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned(ws, 256)) return MOE_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int host = 0;
+    if (cudaMemcpyAsync(&host, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    return static_cast<moe_status_t>(host);
+}
+
+const char* moe_status_string(moe_status_t st)
+{
+    switch (st) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+        case MOE_ERR_MISALIGNED: return "misaligned pointer";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_NONFINITE: return "non-finite (NaN) score";
+        case MOE_ERR_TIMEOUT: return "bounded device wait timed out";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+    }
+    return "unknown status";
+}
+
+moe_status_t moe_pack_w13(int32_t E, int32_t F, int32_t d, const void* w1, const void* w3,
+                          void* w13, void* stream)
+{
+    if (E <= 0 || F <= 0 || d <= 0 || !w1 || !w3 || !w13) return MOE_ERR_INVALID_ARG;
+    if (F % 128 != 0 || d % 64 != 0 || E > kMaxE) return MOE_ERR_UNSUPPORTED;
+    if (!aligned(w1, 16) || !aligned(w3, 16) || !aligned(w13, 16)) return MOE_ERR_MISALIGNED;
+    return cuda_status(launch_pack_w13(E, F, d, w1, w3, w13, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const void* h, const void* w_router,
+                       const float* bias, const float* usage, const float* logits_in,
+                       float* logits_out, float* scores_out, int32_t* topk_ids, float* topk_w,
+                       int32_t* counts_pre, float* f, float* P, void* ws, size_t ws_bytes,
+                       void* stream)
+{
+    moe_status_t st = check_config(cfg, false);
+    if (st != MOE_OK) return st;
+    if (!topk_ids) return MOE_ERR_INVALID_ARG;
+    if (!logits_in && (!h || !w_router)) return MOE_ERR_INVALID_ARG;
+    if (!logits_in && (!aligned(h, 16) || !aligned(w_router, 16))) return MOE_ERR_MISALIGNED;
+    WsLayout L;
+    st = check_ws(cfg, ws, ws_bytes, &L);
+    if (st != MOE_OK) return st;
+    if (cfg->T == 0) return MOE_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = run_route(*cfg, L, h, w_router, bias, usage, logits_in, logits_out, scores_out, topk_ids,
+                   topk_w, ws, s);
+    if (st != MOE_OK) return st;
+    return run_stats(*cfg, L, counts_pre, f, P, ws, s);
+}
+
+moe_status_t moe_dispatch(const moe_config_t* cfg, const float* scores, int32_t* assign,
+                          int32_t* slot, uint8_t* flags, int32_t* counts, int32_t* offsets,
+                          int32_t* perm, float* combine_w, int32_t* n_rerouted,
+                          int32_t* n_dropped, void* ws, size_t ws_bytes, void* stream)
+{
+    moe_status_t st = check_config(cfg, false);
+    if (st != MOE_OK) return st;
+    if (!scores || !assign || !slot || !flags || !counts || !offsets || !perm || !combine_w ||
+        !n_rerouted || !n_dropped)
+        return MOE_ERR_INVALID_ARG;
+    WsLayout L;
+    st = check_ws(cfg, ws, ws_bytes, &L);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cfg->T == 0) {
+        // nothing to place: zero counts/offsets and the two totals
+        if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * cfg->E, s) != cudaSuccess ||
+            cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (cfg->E + 1), s) != cudaSuccess ||
+            cudaMemsetAsync(n_rerouted, 0, sizeof(int32_t), s) != cudaSuccess ||
+            cudaMemsetAsync(n_dropped, 0, sizeof(int32_t), s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    // preference prefixes, chunk histograms and ranks of the given scores
+    RouteArgs a{};
+    a.T = cfg->T;
+    a.E = cfg->E;
+    a.k = cfg->k;
+    a.d = cfg->d_model;
+    a.splits = L.splits;
+    a.epad = L.epad;
+    a.nchunks = L.nchunks;
+    a.logits_in = scores;
+    a.ids_ws = ws_at<int32_t>(ws, L.ids);
+    a.prefs = ws_at<uint8_t>(ws, L.prefs);
+    a.crank = ws_at<int32_t>(ws, L.crank);
+    a.hist = ws_at<int32_t>(ws, L.hist);
+    a.ppart = ws_at<float>(ws, L.ppart);
+    a.status = ws_at<int>(ws, L.status);
+    if (launch_route(a, s) != cudaSuccess) return MOE_ERR_CUDA;
+    DispatchOut o{assign, slot, counts, offsets, perm, flags, combine_w, n_rerouted, n_dropped};
+    return run_dispatch(*cfg, L, scores, o, ws, s);
+}
+
+moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* h, const int32_t* perm,
+                            const int32_t* offsets, const void* w13, const void* w2,
+                            void* y_slots, void* ws, size_t ws_bytes, void* stream)
+{
+    moe_status_t st = check_config(cfg, true);
+    if (st != MOE_OK) return st;
+    if (!h || !perm || !offsets || !w13 || !w2 || !y_slots) return MOE_ERR_INVALID_ARG;
+    if (!aligned(h, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(y_slots, 16))
+        return MOE_ERR_MISALIGNED;
+    WsLayout L;
+    st = check_ws(cfg, ws, ws_bytes, &L);
+    if (st != MOE_OK) return st;
+    if (cfg->T == 0) return MOE_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    GemmLaunch g = expert_gemm(*cfg, L, GK_GATEUP, ws);
+    g.a_ptr = h;
+    g.b_ptr = w13;
+    g.offsets = offsets;
+    g.perm = perm;
+    g.act = ws_at<void>(ws, L.act);
+    if (launch_gemm(g, s) != cudaSuccess) return MOE_ERR_CUDA;
+    GemmLaunch g2 = expert_gemm(*cfg, L, GK_DOWN_SLOTS, ws);
+    g2.a_ptr = ws_at<void>(ws, L.act);
+    g2.b_ptr = w2;
+    g2.offsets = offsets;
+    g2.perm = perm;
+    g2.y_slots = y_slots;
+    return cuda_status(launch_gemm(g2, s));
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* y_slots, const int32_t* assign,
+                         const int32_t* slot, const int32_t* offsets, const float* combine_w,
+                         void* out, void* stream)
+{
+    moe_status_t st = check_config(cfg, false);
+    if (st != MOE_OK) return st;
+    if (!y_slots || !assign || !slot || !offsets || !combine_w || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned(y_slots, 16) || !aligned(out, 16)) return MOE_ERR_MISALIGNED;
+    if (cfg->T == 0) return MOE_OK;
+    return cuda_status(launch_combine(cfg->T, cfg->d_model, cfg->k, y_slots, assign, slot, offsets,
+                                      combine_w, out, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* h, const void* w_router,
+                               const float* bias, const float* usage, const void* w13,
+                               const void* w2, void* out, float* logits_out, int32_t* assign,
+                               int32_t* slot, uint8_t* flags, int32_t* counts, float* f, float* P,
+                               void* const* stage_events, void* ws, size_t ws_bytes, void* stream)
+{
+    moe_status_t st = check_config(cfg, true);
+    if (st != MOE_OK) return st;
+    if (!h || !w_router || !w13 || !w2 || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned(h, 16) || !aligned(w_router, 16) || !aligned(w13, 16) || !aligned(w2, 16) ||
+        !aligned(out, 16))
+        return MOE_ERR_MISALIGNED;
+    WsLayout L;
+    st = check_ws(cfg, ws, ws_bytes, &L);
+    if (st != MOE_OK) return st;
+    if (cfg->T == 0) return MOE_OK;
+    const moe_config_t& c = *cfg;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Ev ev{stage_events, s};
+
+    ev.mark(0);
+    st = run_route(c, L, h, w_router, bias, usage, nullptr, logits_out, nullptr, nullptr, nullptr,
+                   ws, s);
+    if (st != MOE_OK) return st;
+    ev.mark(1);
+    DispatchOut o;
+    o.assign = assign ? assign : ws_at<int32_t>(ws, L.assign);
+    o.slot = slot ? slot : ws_at<int32_t>(ws, L.slot);
+    o.flags = flags ? flags : ws_at<uint8_t>(ws, L.flags);
+    o.counts = counts ? counts : ws_at<int32_t>(ws, L.counts);
+    o.offsets = ws_at<int32_t>(ws, L.offsets);
+    o.perm = ws_at<int32_t>(ws, L.perm);
+    o.cw = ws_at<float>(ws, L.cw);
+    o.n_rerouted = nullptr;
+    o.n_dropped = nullptr;
+    st = run_dispatch(c, L, ws_at<float>(ws, L.scores), o, ws, s);
+    if (st != MOE_OK) return st;
+    st = run_stats(c, L, nullptr, f, P, ws, s);
+    if (st != MOE_OK) return st;
+    ev.mark(2);
+    const bool fused = c.k <= 2;  // at most two fp32 addends per element: order-free
+    float* acc = ws_at<float>(ws, L.out_acc);
+    if (fused &&
+        cudaMemsetAsync(acc, 0, sizeof(float) * static_cast<size_t>(c.T) * c.d_model, s) !=
+            cudaSuccess)
+        return MOE_ERR_CUDA;
+    ev.mark(3);
+    GemmLaunch g = expert_gemm(c, L, GK_GATEUP, ws);
+    g.a_ptr = h;
+    g.b_ptr = w13;
+    g.offsets = o.offsets;
+    g.perm = o.perm;
+    g.act = ws_at<void>(ws, L.act);
+    if (launch_gemm(g, s) != cudaSuccess) return MOE_ERR_CUDA;
+    ev.mark(4);
+    GemmLaunch g2 = expert_gemm(c, L, fused ? GK_DOWN_SCATTER : GK_DOWN_SLOTS, ws);
+    g2.a_ptr = ws_at<void>(ws, L.act);
+    g2.b_ptr = w2;
+    g2.offsets = o.offsets;
+    g2.perm = o.perm;
+    g2.cw = o.cw;
+    g2.out_acc = acc;
+    g2.y_slots = fused ? nullptr : ws_at<void>(ws, L.y_slots);
+    if (launch_gemm(g2, s) != cudaSuccess) return MOE_ERR_CUDA;
+    ev.mark(5);
+    cudaError_t e = fused ? launch_finalize(c.T, c.d_model, acc, out, s)
+                          : launch_combine(c.T, c.d_model, c.k, ws_at<void>(ws, L.y_slots), o.assign,
+                                           o.slot, o.offsets, o.cw, out, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    ev.mark(6);
+    return MOE_OK;
+}
+
+moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* h_host,
+                                    const void* w_router, const float* bias, const float* usage,
+                                    const void* w13, const void* w2, void* out_host, void* ws,
+                                    size_t ws_bytes, void* stream)
+{
+    moe_status_t st = check_config(cfg, true);
+    if (st != MOE_OK) return st;
+    if (!h_host || !out_host) return MOE_ERR_INVALID_ARG;
+    WsLayout L;
+    st = check_ws(cfg, ws, ws_bytes, &L);
+    if (st != MOE_OK) return st;
+    if (cfg->T == 0) return MOE_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes = static_cast<size_t>(cfg->T) * cfg->d_model * 2;
+    void* h_dev = ws_at<void>(ws, L.h_stage);
+    void* out_dev = ws_at<void>(ws, L.out_stage);
+    if (cudaMemcpyAsync(h_dev, h_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    st = moe_layer_forward(cfg, h_dev, w_router, bias, usage, w13, w2, out_dev, nullptr, nullptr,
+                           nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, ws, ws_bytes, stream);
+    if (st != MOE_OK) return st;
+    if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(s));
+}
+
+moe_status_t moe_debug_timeout_probe(void* ws, size_t ws_bytes, int64_t budget_cycles, void* stream)
+{
+    if (!ws || ws_bytes < 256 || budget_cycles <= 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned(ws, 256)) return MOE_ERR_MISALIGNED;
+    return cuda_status(
+        launch_timeout_probe(static_cast<int*>(ws), budget_cycles, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,496 @@
+// gemm.cu -- persistent tcgen05/TMEM GEMM with TMA-fed operands for the
+// three dense contractions of the MoE layer:
+//
+//   GK_ROUTER        logits partials  = h . W_r^T          (K split across CTAs)
+//   GK_GATEUP        act = silu(x W1^T) * (x W3^T), x = h rows gathered by perm
+//   GK_DOWN_SCATTER  out_acc[t] += cw[t,r] * (act W2^T)    (weighted scatter)
+//   GK_DOWN_SLOTS    y_slots     = act W2^T                 (slot order, bf16)
+//
+// The router is the linear map of the token's hidden state to expert logits
+// ([coreui] §3.1 "Logits生成"; [csdn] §3.1 h @ W_gate); the experts are the
+// SwiGLU FFNs W2(silu(W1 x) * W3 x) ([mhpn] §3.1; [2kiu] §1) run over each
+// expert's group of tokens ([cnnetsun] §3.2 step 1), and the down projection
+// is combined back to token order with the router weights ([mhpn] §4.3;
+// [2kiu] §3 step 5).
+//
+// One CTA per SM (or two for the router), 6 warps:
+//   warp 0    TMA producer: A tile 128 x 64 (tiled, or gathered 4 rows per
+//             tile::gather4 by all 32 lanes) and B tile BN x 64, 128-byte
+//             swizzle, into a ring of `stages` shared-memory slots;
+//   warp 1    allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=16)
+//             into one of two TMEM accumulators and commits to mbarriers;
+//   warps 2-5 epilogue: tcgen05.ld of their 32 TMEM lanes, fused math, store.
+// Tiles are scheduled statically (tile += gridDim.x) from per-expert row
+// counts read on the device, so no host synchronisation is needed.  Every
+// wait is bounded; on expiry the CTA records MOE_ERR_TIMEOUT, drains what it
+// issued and exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+struct GemmParams {
+    int kind, E, T, topk, d, F;
+    int kb_total;      // K / 64
+    int bn;            // N tile
+    int n_tiles;       // N tiles per expert
+    int m_tiles;       // router: ceil(T / 128)
+    int splits;        // router K splits
+    int kb_per_split;  // router K blocks per split
+    int stages;
+    uint32_t tmem_cols;
+    const int32_t* offsets;
+    const int32_t* perm;
+    const float* cw;
+    float* out_acc;
+    __nv_bfloat16* act;
+    __nv_bfloat16* y_slots;
+    float* router_part;
+    int* status;
+    long long budget;
+};
+
+struct TileInfo {
+    int e, m, n, kb0, kb1, split;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile,
+                                                const int* s_tile_start, const int* s_offs)
+{
+    TileInfo ti;
+    if (p.kind == GK_ROUTER) {
+        ti.e = 0;
+        ti.n = 0;
+        ti.m = tile % p.m_tiles;
+        ti.split = tile / p.m_tiles;
+        ti.kb0 = ti.split * p.kb_per_split;
+        ti.kb1 = min(p.kb_total, ti.kb0 + p.kb_per_split);
+        return ti;
+    }
+    int lo = 0, hi = p.E - 1;  // largest e with tile_start[e] <= tile
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (s_tile_start[mid] <= tile)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int e = lo;
+    const int cnt = s_offs[e + 1] - s_offs[e];
+    const int mt = (cnt + kBM - 1) / kBM;
+    const int local = tile - s_tile_start[e];
+    ti.e = e;
+    ti.m = local % mt;  // m fastest: the row tiles of one weight tile run together
+    ti.n = local / mt;
+    ti.kb0 = 0;
+    ti.kb1 = p.kb_total;
+    ti.split = 0;
+    return ti;
+}
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int stages = p.stages;
+    const uint32_t a_bytes = kBM * kBK * 2;
+    const uint32_t b_bytes = static_cast<uint32_t>(p.bn) * kBK * 2;
+    uint8_t* sA = smem;
+    uint8_t* sB = sA + stages * a_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + stages * b_bytes);
+    uint64_t* full_bar = bars;
+    uint64_t* empty_bar = bars + stages;
+    uint64_t* tfull_bar = bars + 2 * stages;
+    uint64_t* tempty_bar = bars + 2 * stages + 2;
+    int* s_tile_start = reinterpret_cast<int*>(bars + 2 * stages + 4);
+    int* s_offs = s_tile_start + (p.E + 1);
+    volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(s_offs + (p.E + 1));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        for (int i = 0; i < stages; ++i) {
+            mbar_init(smem_u32(&full_bar[i]), 1);
+            mbar_init(smem_u32(&empty_bar[i]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&tfull_bar[b]), 1);
+            mbar_init(smem_u32(&tempty_bar[b]), 4);
+        }
+        mbar_fence_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), p.tmem_cols);
+        tmem_relinquish();
+    }
+    if (p.kind != GK_ROUTER && warp == 2) {
+        // tile_start[e] = sum over e' < e of ceil(count_e' / 128) * n_tiles
+        int carry = 0;
+        for (int base = 0; base <= p.E; base += 32) {
+            const int e = base + lane;
+            int o = 0, o1 = 0;
+            if (e <= p.E) o = p.offsets[e];
+            if (e < p.E) o1 = p.offsets[e + 1];
+            if (e <= p.E) s_offs[e] = o;
+            int tiles = (e < p.E) ? ((o1 - o + kBM - 1) / kBM) * p.n_tiles : 0;
+            int incl = tiles;
+            for (int off = 1; off < 32; off <<= 1) {
+                int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            if (e <= p.E) s_tile_start[e] = carry + incl - tiles;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+    const int total_tiles = (p.kind == GK_ROUTER) ? p.m_tiles * p.splits : s_tile_start[p.E];
+    const uint32_t idesc = idesc_bf16_f32(kBM, p.bn);
+    bool ok = true;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load in flight + its parity
+        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+            const TileInfo ti = decode_tile(p, tile, s_tile_start, s_offs);
+            int r0 = 0, r1 = 0, r2 = 0, r3 = 0, arow = 0, brow = 0;
+            if (p.kind == GK_GATEUP) {
+                const int off = s_offs[ti.e];
+                const int cnt = s_offs[ti.e + 1] - off;
+                const int j0 = ti.m * kBM + lane * 4;
+                const int fallback = p.perm[off + ti.m * kBM] / p.topk;  // a valid row
+                r0 = (j0 + 0 < cnt) ? p.perm[off + j0 + 0] / p.topk : fallback;
+                r1 = (j0 + 1 < cnt) ? p.perm[off + j0 + 1] / p.topk : fallback;
+                r2 = (j0 + 2 < cnt) ? p.perm[off + j0 + 2] / p.topk : fallback;
+                r3 = (j0 + 3 < cnt) ? p.perm[off + j0 + 3] / p.topk : fallback;
+                brow = ti.e * 2 * p.F + ti.n * kExpertBN;
+            } else if (p.kind == GK_ROUTER) {
+                arow = ti.m * kBM;
+                brow = 0;
+            } else {
+                arow = s_offs[ti.e] + ti.m * kBM;
+                brow = ti.e * p.d + ti.n * p.bn;
+            }
+            for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
+                if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, p.budget)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&full_bar[stage]);
+                if (lane == 0) mbar_arrive_expect_tx(fb, a_bytes + b_bytes);
+                __syncwarp();
+                const int x = kb * kBK;
+                const uint32_t dA = smem_u32(sA + stage * a_bytes);
+                if (p.kind == GK_GATEUP) {
+                    tma_gather4(dA + lane * 4 * 128, &tmA, x, r0, r1, r2, r3, fb);
+                } else if (lane == 0) {
+                    tma_load_2d(dA, &tmA, x, arow, fb);
+                }
+                if (lane == 0) tma_load_2d(smem_u32(sB + stage * b_bytes), &tmB, x, brow, fb);
+                issued_mask |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (!ok) {
+            record_error(p.status, MOE_ERR_TIMEOUT);
+            // let the copies this warp issued land before the CTA exits
+            for (int s = 0; s < stages; ++s)
+                if (issued_mask & (1u << s))
+                    mbar_wait(smem_u32(&full_bar[s]), (issued_parity >> s) & 1, p.budget);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            int last_b = -1;
+            uint32_t last_par = 0;
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
+                const TileInfo ti = decode_tile(p, tile, s_tile_start, s_offs);
+                const int b = it & 1;
+                const uint32_t acc_par = (it >> 1) & 1;
+                if (!mbar_wait(smem_u32(&tempty_bar[b]), acc_par ^ 1, p.budget)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * p.bn);
+                for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
+                    if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.budget)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + stage * a_bytes);
+                    const uint32_t b0 = smem_u32(sB + stage * b_bytes);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        mma_bf16(d_tmem, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc,
+                                 (kb > ti.kb0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&empty_bar[stage]));
+                    if (++stage == stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&tfull_bar[b]));
+                last_b = b;
+                last_par = acc_par;
+            }
+            if (!ok) record_error(p.status, MOE_ERR_TIMEOUT);
+            // all MMAs issued must be complete before TMEM is released
+            if (last_b >= 0) mbar_wait(smem_u32(&tfull_bar[last_b]), last_par, p.budget);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
+            const TileInfo ti = decode_tile(p, tile, s_tile_start, s_offs);
+            const int b = it & 1;
+            const uint32_t acc_par = (it >> 1) & 1;
+            if (!mbar_wait(smem_u32(&tfull_bar[b]), acc_par, p.budget)) {
+                record_error(p.status, MOE_ERR_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(b * p.bn);
+            uint32_t v[32];
+            if (p.kind == GK_ROUTER) {
+                const int t = ti.m * kBM + row;
+                float* dst = p.router_part + (static_cast<size_t>(ti.split) * p.T + t) * p.E;
+                for (int c = 0; c < p.bn; c += 32) {
+                    tmem_ld32(taddr + c, v);
+                    tmem_ld_wait(v);
+                    if (t < p.T) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (c + j < p.E) dst[c + j] = __uint_as_float(v[j]);
+                    }
+                }
+            } else if (p.kind == GK_GATEUP) {
+                const int off = s_offs[ti.e];
+                const int cnt = s_offs[ti.e + 1] - off;
+                const int ri = ti.m * kBM + row;
+                uint32_t u[32];
+                __nv_bfloat16* dst = p.act + static_cast<size_t>(off + ri) * p.F + ti.n * (kExpertBN / 2);
+                for (int c = 0; c < kExpertBN / 2; c += 32) {
+                    tmem_ld32(taddr + c, v);                   // gate columns
+                    tmem_ld32(taddr + kExpertBN / 2 + c, u);   // matching up columns
+                    tmem_ld_wait2(v, u);
+                    if (ri < cnt) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float a0 = silu_f(__uint_as_float(v[2 * j])) * __uint_as_float(u[2 * j]);
+                            const float a1 =
+                                silu_f(__uint_as_float(v[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+                            pk[j] = pack_bf16x2(a0, a1);
+                        }
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    }
+                }
+            } else {
+                const int off = s_offs[ti.e];
+                const int cnt = s_offs[ti.e + 1] - off;
+                const int ri = ti.m * kBM + row;
+                const bool valid = ri < cnt;
+                const int slot = off + ri;
+                const int col0 = ti.n * p.bn;
+                if (p.kind == GK_DOWN_SCATTER) {
+                    const int idx = valid ? p.perm[slot] : 0;
+                    const float w = valid ? p.cw[idx] : 0.0f;
+                    float* dst = p.out_acc + static_cast<size_t>(idx / p.topk) * p.d + col0;
+                    for (int c = 0; c < p.bn; c += 32) {
+                        if (col0 + c >= p.d) break;  // uniform across the warp
+                        tmem_ld32(taddr + c, v);
+                        tmem_ld_wait(v);
+                        if (valid) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                float4 add = make_float4(w * __uint_as_float(v[4 * j]),
+                                                         w * __uint_as_float(v[4 * j + 1]),
+                                                         w * __uint_as_float(v[4 * j + 2]),
+                                                         w * __uint_as_float(v[4 * j + 3]));
+                                atomicAdd(reinterpret_cast<float4*>(dst + c + 4 * j), add);
+                            }
+                        }
+                    }
+                } else {
+                    __nv_bfloat16* dst = p.y_slots + static_cast<size_t>(slot) * p.d + col0;
+                    for (int c = 0; c < p.bn; c += 32) {
+                        if (col0 + c >= p.d) break;
+                        tmem_ld32(taddr + c, v);
+                        tmem_ld_wait(v);
+                        if (valid) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[b]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, p.tmem_cols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (row-major), box [box_rows, 64], 128-byte swizzle.
+bool make_map(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows)
+{
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t gdim[2] = {cols, rows};
+    cuuint64_t gstride[1] = {cols * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), gdim, gstride,
+                     box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+uint32_t pow2_cols(int n)
+{
+    uint32_t c = 32;
+    while (c < static_cast<uint32_t>(n)) c <<= 1;
+    return c;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
+{
+    GemmParams p{};
+    p.kind = g.kind;
+    p.E = g.E;
+    p.T = g.T;
+    p.topk = g.topk;
+    p.d = g.d;
+    p.F = g.F;
+    p.offsets = g.offsets;
+    p.perm = g.perm;
+    p.cw = g.cw;
+    p.out_acc = g.out_acc;
+    p.act = static_cast<__nv_bfloat16*>(g.act);
+    p.y_slots = static_cast<__nv_bfloat16*>(g.y_slots);
+    p.router_part = g.router_part;
+    p.status = g.status;
+    p.budget = g.budget;
+
+    CUtensorMap tmA, tmB;
+    int grid = 0;
+    const int sms = num_sms();
+    if (g.kind == GK_ROUTER) {
+        p.bn = g.epad;
+        p.kb_total = g.d / kBK;
+        p.m_tiles = (g.T + kBM - 1) / kBM;
+        p.splits = g.splits;
+        p.kb_per_split = (p.kb_total + g.splits - 1) / g.splits;
+        p.n_tiles = 1;
+        if (!make_map(&tmA, g.a_ptr, g.T, g.d, kBM)) return cudaErrorInvalidValue;
+        if (!make_map(&tmB, g.b_ptr, g.E, g.d, p.bn)) return cudaErrorInvalidValue;
+        grid = std::min(p.m_tiles * p.splits, 2 * sms);
+    } else if (g.kind == GK_GATEUP) {
+        p.bn = kExpertBN;
+        p.kb_total = g.d / kBK;
+        p.n_tiles = g.F / (kExpertBN / 2);
+        if (!make_map(&tmA, g.a_ptr, g.T, g.d, 1)) return cudaErrorInvalidValue;
+        if (!make_map(&tmB, g.b_ptr, static_cast<uint64_t>(g.E) * 2 * g.F, g.d, kExpertBN))
+            return cudaErrorInvalidValue;
+        const long long mt_max = (static_cast<long long>(g.T) * g.topk + kBM - 1) / kBM + g.E;
+        grid = static_cast<int>(std::min<long long>(mt_max * p.n_tiles, sms));
+    } else {
+        p.bn = kExpertBN;
+        p.kb_total = g.F / kBK;
+        p.n_tiles = (g.d + kExpertBN - 1) / kExpertBN;
+        if (!make_map(&tmA, g.a_ptr, static_cast<uint64_t>(g.T) * g.topk, g.F, kBM))
+            return cudaErrorInvalidValue;
+        if (!make_map(&tmB, g.b_ptr, static_cast<uint64_t>(g.E) * g.d, g.F, kExpertBN))
+            return cudaErrorInvalidValue;
+        const long long mt_max = (static_cast<long long>(g.T) * g.topk + kBM - 1) / kBM + g.E;
+        grid = static_cast<int>(std::min<long long>(mt_max * p.n_tiles, sms));
+    }
+    const uint32_t a_bytes = kBM * kBK * 2;
+    const uint32_t b_bytes = static_cast<uint32_t>(p.bn) * kBK * 2;
+    const size_t fixed = 1024 + 64 + static_cast<size_t>(2 * (g.E + 1)) * 4 + 16 + 6 * 8;
+    const size_t budget_smem = 227 * 1024;
+    int stages = static_cast<int>((budget_smem - fixed) / (a_bytes + b_bytes + 16));
+    stages = std::max(2, std::min(stages, 8));
+    p.stages = stages;
+    p.tmem_cols = pow2_cols(2 * p.bn);
+    const size_t smem = fixed + static_cast<size_t>(stages) * (a_bytes + b_bytes + 16);
+
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        227 * 1024);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    if (grid <= 0) return cudaSuccess;
+    moe_gemm_kernel<<<grid, kGemmThreads, smem, s>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

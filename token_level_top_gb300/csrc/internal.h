@@ -1,0 +1,127 @@
+// internal.h -- declarations shared by the libmoe translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kChunk = 256;        // tokens per routing chunk (one route block)
+constexpr int kPrefLen = 8;        // preference-order prefix kept per token
+constexpr int kBM = 128;           // GEMM tile rows (tokens / slots)
+constexpr int kBK = 64;            // GEMM K per pipeline stage (128 bytes of bf16)
+constexpr int kExpertBN = 256;     // expert GEMM tile columns
+constexpr int kGemmThreads = 192;  // 6 warps: TMA, MMA, 4 x epilogue
+constexpr long long kSpinBudget = 2000000000LL;  // ~1 s of SM clock per bounded wait
+
+enum GemmKind : int { GK_ROUTER = 0, GK_GATEUP = 1, GK_DOWN_SCATTER = 2, GK_DOWN_SLOTS = 3 };
+
+// Byte offsets of every scratch region inside the caller's workspace.
+struct WsLayout {
+    int nchunks = 0;   // ceil(T / kChunk)
+    int splits = 0;    // router GEMM K-splits
+    int epad = 0;      // router N tile (E rounded up to 16, at least 16)
+    size_t status = 0, ctrl = 0, part = 0, scores = 0, ids = 0, prefs = 0, crank = 0, hist = 0,
+           base = 0, ppart = 0, assign = 0, slot = 0, flags = 0, counts = 0, offsets = 0,
+           perm = 0, cw = 0, act = 0, out_acc = 0, y_slots = 0, h_stage = 0, out_stage = 0;
+    size_t total = 0;
+};
+
+// ctrl block (int32 words)
+enum CtrlWord : int { CTRL_Q1 = 0, CTRL_NRE = 1, CTRL_NDROP = 2, CTRL_WORDS = 64 };
+
+bool layout_for(const moe_config_t& c, WsLayout* L);
+int router_splits(int T, int d);
+int num_sms();
+
+template <class T>
+inline T* ws_at(void* ws, size_t off)
+{
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// ---- launchers (all asynchronous on `stream`) ----
+struct RouteArgs {
+    int T, E, k, d, splits, epad, nchunks;
+    const float* part;       // [splits][T][E] router GEMM partial sums, or NULL
+    const float* logits_in;  // [T][E], or NULL
+    const float* bias;       // [E] or NULL (added to GEMM partial sums only)
+    const float* usage;      // [E] or NULL
+    float lambda;
+    float* logits_out;       // [T][E] or NULL
+    float* scores_user;      // [T][E] or NULL
+    float* scores_ws;        // [T][E] (always)
+    int32_t* ids_user;       // [T][k] or NULL
+    float* topk_w;           // [T][k] or NULL
+    int32_t* ids_ws;         // [T][k]
+    uint8_t* prefs;          // [T][kPrefLen]
+    int32_t* crank;          // [T][k]
+    int32_t* hist;           // [k*nchunks][E]
+    float* ppart;            // [nchunks][E]
+    int* status;
+};
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+
+struct StatsArgs {
+    int T, E, k, nchunks;
+    const int32_t* hist;
+    const float* ppart;
+    int32_t* counts_pre;  // or NULL
+    float* f;             // or NULL
+    float* P;             // or NULL
+};
+cudaError_t launch_route_stats(const StatsArgs& a, cudaStream_t s);
+
+struct DispatchArgs {
+    int T, E, k, nchunks;
+    int64_t C;
+    const float* scores;
+    const int32_t* ids;
+    const uint8_t* prefs;
+    const int32_t* crank;
+    const int32_t* hist;
+    int32_t* base;
+    int32_t* ctrl;
+    int32_t* assign;
+    int32_t* slot;
+    uint8_t* flags;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* perm;
+    float* cw;
+    int32_t* n_rerouted;  // or NULL
+    int32_t* n_dropped;   // or NULL
+    int* status;
+};
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
+
+struct GemmLaunch {
+    int kind;
+    int E, T, topk, d, F;
+    const void* a_ptr;  // router/gate-up: h [T,d]; down: act [T*k, F]
+    const void* b_ptr;  // router: W_r [E,d]; gate-up: W13 [E,2F,d]; down: W2 [E,d,F]
+    const int32_t* offsets;
+    const int32_t* perm;
+    const float* cw;
+    float* out_acc;
+    void* act;
+    void* y_slots;
+    float* router_part;
+    int splits, epad;
+    int* status;
+    long long budget;
+};
+cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
+
+cudaError_t launch_pack_w13(int E, int F, int d, const void* w1, const void* w3, void* w13,
+                            cudaStream_t s);
+cudaError_t launch_finalize(int T, int d, const float* acc, void* out, cudaStream_t s);
+cudaError_t launch_combine(int T, int d, int k, const void* y_slots, const int32_t* assign,
+                           const int32_t* slot, const int32_t* offsets, const float* cw, void* out,
+                           cudaStream_t s);
+cudaError_t launch_timeout_probe(int* status, long long budget, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,249 @@
+// route.cu -- router epilogue: scores, preference order, softmax, top-k and
+// the load statistics, one group of lanes per token.
+//
+//   z = sum of the router GEMM's K-split partial sums (+ bias), or given logits
+//   s = z - lambda*usage (two rounded fp32 ops)      [mhpn] §2.3; [cnnetsun] §3.1
+//   p = softmax(s); top-k = the k best s, ties to the lower index   [coreui] §3.1
+//   f_i = picks of i / T, P_i = mean p_i             [cnnetsun] §4.2; [coreui] §3.1
+//
+// Each block handles a chunk of kChunk consecutive tokens.  A token is owned
+// by G = min(32, pow2(E)) lanes, each lane holding EPL experts (e = lane + G*j);
+// the first kPrefLen entries of the preference order come out of repeated
+// group arg-max rounds with warp shuffles.  Per chunk the kernel also writes
+// the per-rank histogram of picks and each pick's stable rank among equal
+// picks in token order (warp __match_any_sync + a scan over warps): the
+// dispatch uses them to place every entry before the first capacity event in
+// parallel.  All reductions run in a fixed order, so results are
+// deterministic.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = kRouteThreads / 32;
+
+__device__ __forceinline__ float softmax_num(float s, float m)
+{
+    if (m == INFINITY) return (s == INFINITY) ? 1.0f : 0.0f;
+    if (m == -INFINITY) return 1.0f;
+    return expf(s - m);
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
+{
+    __shared__ int s_ids[kChunk * 8];
+    __shared__ int s_wcnt[kRouteWarps][256];
+    __shared__ float s_wsum[kRouteWarps][256];
+    __shared__ int s_nan;
+
+    const int E = a.E, k = a.k, T = a.T;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int G = 1;
+    while (G < E && G < 32) G <<= 1;
+    const int lg = lane & (G - 1);
+    const int grp = lane / G;
+    const int tpw = 32 / G;
+    const int L = E < kPrefLen ? E : kPrefLen;
+    const int chunk = blockIdx.x;
+    const int t_begin = chunk * kChunk;
+    if (threadIdx.x == 0) s_nan = 0;
+
+    float acc[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) acc[j] = 0.0f;
+    bool saw_nan = false;
+
+    for (int base = warp * tpw; base < kChunk; base += kRouteWarps * tpw) {
+        const int tl = base + grp;
+        const int t = t_begin + tl;
+        const bool valid = t < T;
+        float s[EPL];
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const int e = lg + G * j;
+            s[j] = -INFINITY;
+            if (valid && e < E) {
+                float z;
+                if (a.part) {
+                    z = 0.0f;
+                    for (int sp = 0; sp < a.splits; ++sp)
+                        z += a.part[(static_cast<size_t>(sp) * T + t) * E + e];
+                    if (a.bias) z += a.bias[e];
+                } else {
+                    z = a.logits_in[static_cast<size_t>(t) * E + e];
+                }
+                if (a.logits_out) a.logits_out[static_cast<size_t>(t) * E + e] = z;
+                float sc = z;
+                if (a.usage && a.lambda != 0.0f) sc = __fsub_rn(z, __fmul_rn(a.lambda, a.usage[e]));
+                if (isnan(sc)) {
+                    saw_nan = true;
+                    sc = -INFINITY;  // ranks last; the call reports MOE_ERR_NONFINITE
+                }
+                if (a.scores_ws) a.scores_ws[static_cast<size_t>(t) * E + e] = sc;
+                if (a.scores_user) a.scores_user[static_cast<size_t>(t) * E + e] = sc;
+                s[j] = sc;
+            }
+        }
+        // preference order prefix: L rounds of group arg-max
+        uint32_t picked = 0;
+        int pref[kPrefLen];
+        float pv[kPrefLen];
+#pragma unroll
+        for (int i = 0; i < kPrefLen; ++i) {
+            pref[i] = 255;
+            pv[i] = -INFINITY;
+            if (i < L) {
+                float bv = -INFINITY;
+                int bi = 0x7fffffff;
+#pragma unroll
+                for (int j = 0; j < EPL; ++j) {
+                    const int e = lg + G * j;
+                    if (e < E && !((picked >> j) & 1u) && ranks_before(s[j], e, bv, bi)) {
+                        bv = s[j];
+                        bi = e;
+                    }
+                }
+                for (int off = G >> 1; off >= 1; off >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off, G);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi, off, G);
+                    if (ranks_before(ov, oi, bv, bi)) {
+                        bv = ov;
+                        bi = oi;
+                    }
+                }
+                pref[i] = bi;
+                pv[i] = bv;
+                if ((bi & (G - 1)) == lg) picked |= 1u << (bi / G);
+            }
+        }
+        // softmax over the token's experts
+        const float m = pv[0];
+        float num[EPL];
+        float part_sum = 0.0f;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const int e = lg + G * j;
+            num[j] = (e < E) ? softmax_num(s[j], m) : 0.0f;
+            part_sum += num[j];
+        }
+        for (int off = G >> 1; off >= 1; off >>= 1)
+            part_sum += __shfl_xor_sync(0xffffffffu, part_sum, off, G);
+        const float zsum = part_sum;
+        if (valid) {
+#pragma unroll
+            for (int j = 0; j < EPL; ++j) acc[j] += num[j] / zsum;
+            if (lg == 0) {
+                uint32_t lo = 0, hi = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) lo |= static_cast<uint32_t>(pref[i] & 0xFF) << (8 * i);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) hi |= static_cast<uint32_t>(pref[4 + i] & 0xFF) << (8 * i);
+                reinterpret_cast<uint2*>(a.prefs)[t] = make_uint2(lo, hi);
+                for (int r = 0; r < k; ++r) {
+                    a.ids_ws[static_cast<size_t>(t) * k + r] = pref[r];
+                    if (a.ids_user) a.ids_user[static_cast<size_t>(t) * k + r] = pref[r];
+                    if (a.topk_w)
+                        a.topk_w[static_cast<size_t>(t) * k + r] = softmax_num(pv[r], m) / zsum;
+                    s_ids[tl * k + r] = pref[r];
+                }
+            }
+        } else if (lg == 0) {
+            for (int r = 0; r < k; ++r) s_ids[tl * k + r] = -1;
+        }
+    }
+    if (saw_nan) s_nan = 1;
+
+    // ---- P partial of this chunk: lanes -> warp (fixed order) -> chunk
+#pragma unroll
+    for (int j = 0; j < EPL; ++j)
+        for (int off = G; off < 32; off <<= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], off);
+    if (lane < G) {
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            const int e = lg + G * j;
+            if (e < E) s_wsum[warp][e] = acc[j];
+        }
+    }
+    for (int e = threadIdx.x; e < E; e += kRouteThreads)
+        for (int w = 0; w < kRouteWarps; ++w) s_wcnt[w][e] = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kRouteThreads) {
+        float tot = 0.0f;
+        for (int w = 0; w < kRouteWarps; ++w) tot += s_wsum[w][e];
+        a.ppart[static_cast<size_t>(chunk) * E + e] = tot;
+    }
+    if (threadIdx.x == 0 && s_nan) record_error(a.status, MOE_ERR_NONFINITE);
+
+    // ---- per rank: histogram of picks and stable rank within the chunk
+    const int tl = threadIdx.x;  // kRouteThreads == kChunk: one token per thread
+    const int t = t_begin + tl;
+    for (int r = 0; r < k; ++r) {
+        const int e = s_ids[tl * k + r];
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        const int rnk = __popc(peers & lanemask_lt());
+        if (e >= 0 && lane == __ffs(peers) - 1) s_wcnt[warp][e] = __popc(peers);
+        __syncthreads();
+        for (int ee = threadIdx.x; ee < E; ee += kRouteThreads) {
+            int run = 0;
+            for (int w = 0; w < kRouteWarps; ++w) {
+                const int c = s_wcnt[w][ee];
+                s_wcnt[w][ee] = run;  // exclusive prefix over warps
+                run += c;
+            }
+            a.hist[(static_cast<size_t>(r) * a.nchunks + chunk) * E + ee] = run;
+        }
+        __syncthreads();
+        if (e >= 0 && t < T) a.crank[static_cast<size_t>(t) * k + r] = s_wcnt[warp][e] + rnk;
+        __syncthreads();
+        for (int ee = threadIdx.x; ee < E; ee += kRouteThreads)
+            for (int w = 0; w < kRouteWarps; ++w) s_wcnt[w][ee] = 0;
+        __syncthreads();
+    }
+}
+
+__global__ void route_stats_kernel(const StatsArgs a)
+{
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+        long long cnt = 0;
+        const int Q = a.k * a.nchunks;
+        for (int q = 0; q < Q; ++q) cnt += a.hist[static_cast<size_t>(q) * a.E + e];
+        float psum = 0.0f;
+        for (int c = 0; c < a.nchunks; ++c) psum += a.ppart[static_cast<size_t>(c) * a.E + e];
+        if (a.counts_pre) a.counts_pre[e] = static_cast<int32_t>(cnt);
+        if (a.f) a.f[e] = static_cast<float>(static_cast<double>(cnt) / a.T);
+        if (a.P) a.P[e] = psum / static_cast<float>(a.T);
+    }
+}
+
+}  // namespace
+
+static_assert(kRouteThreads == kChunk, "one token per thread in the rank pass");
+
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s)
+{
+    if (a.T <= 0) return cudaSuccess;
+    const int grid = a.nchunks;
+    if (a.E <= 32)
+        route_kernel<1><<<grid, kRouteThreads, 0, s>>>(a);
+    else if (a.E <= 64)
+        route_kernel<2><<<grid, kRouteThreads, 0, s>>>(a);
+    else if (a.E <= 128)
+        route_kernel<4><<<grid, kRouteThreads, 0, s>>>(a);
+    else
+        route_kernel<8><<<grid, kRouteThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route_stats(const StatsArgs& a, cudaStream_t s)
+{
+    if (a.T <= 0) return cudaSuccess;
+    route_stats_kernel<<<1, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,264 @@
+"""Thin ctypes binding over libmoe.so (include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (device memory and streams come from
+PyTorch); calls are enqueued on the current torch stream.  There is no CPU
+fallback: if the library is missing, or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmoe.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
+NUM_STAGES = 6
+STAGE_NAMES = ["route", "dispatch", "zero", "gate_up", "down", "finalize"]
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "misaligned pointer",
+          4: "workspace too small", 5: "non-finite (NaN) score", 6: "bounded device wait timed out",
+          7: "CUDA runtime error"}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, 'unknown')} (status {status})")
+        self.status = status
+
+
+class MoEConfig(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("cf", ctypes.c_double),
+                ("capacity", ctypes.c_int32), ("lambda_", ctypes.c_float),
+                ("flags", ctypes.c_uint32)]
+
+
+@dataclass
+class Config:
+    T: int
+    d_model: int
+    E: int
+    k: int
+    d_ff: int
+    cf: float = 1.25
+    capacity: int = 0
+    lam: float = 0.0
+
+    def c(self) -> MoEConfig:
+        return MoEConfig(self.T, self.d_model, self.E, self.k, self.d_ff, float(self.cf),
+                         int(self.capacity), float(self.lam), 0)
+
+    @classmethod
+    def of(cls, shape, **kw):
+        d = dict(T=shape.T, d_model=shape.d, E=shape.E, k=shape.k, d_ff=shape.F, cf=shape.cf,
+                 capacity=shape.capacity, lam=shape.lam)
+        d.update(kw)
+        return cls(**d)
+
+
+_lib = None
+
+P = ctypes.c_void_p
+I32 = ctypes.c_int32
+SZ = ctypes.c_size_t
+CFG = ctypes.POINTER(MoEConfig)
+
+_SIGS = {
+    "moe_capacity": (ctypes.c_int64, [ctypes.c_int64, I32, I32, ctypes.c_double, I32]),
+    "moe_workspace_size": (SZ, [CFG]),
+    "moe_workspace_init": (I32, [P, SZ, P]),
+    "moe_get_device_status": (I32, [P, P]),
+    "moe_status_string": (ctypes.c_char_p, [I32]),
+    "moe_pack_w13": (I32, [I32, I32, I32, P, P, P, P]),
+    "moe_route": (I32, [CFG, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+    "moe_dispatch": (I32, [CFG, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+    "moe_expert_ffn": (I32, [CFG, P, P, P, P, P, P, P, SZ, P]),
+    "moe_combine": (I32, [CFG, P, P, P, P, P, P, P]),
+    "moe_layer_forward": (I32, [CFG, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+    "moe_layer_forward_host": (I32, [CFG, P, P, P, P, P, P, P, P, SZ, P]),
+    "moe_debug_timeout_probe": (I32, [P, SZ, ctypes.c_int64, P]),
+}
+
+
+def header_functions():
+    """Names of the functions include/moe.h declares."""
+    with open(HEADER) as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def lib():
+    """Load libmoe.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libmoe.so not found at {LIB_PATH}: run "
+                               "`python -m token_level_top_gb300.build` (CUDA path has no fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise MoEError(st, where)
+
+
+def capacity(T: int, k: int, E: int, cf: float, explicit: int = 0) -> int:
+    return int(lib().moe_capacity(T, k, E, cf, explicit))
+
+
+def workspace_size(cfg: Config) -> int:
+    c = cfg.c()
+    return int(lib().moe_workspace_size(ctypes.byref(c)))
+
+
+def workspace(cfg: Config, device="cuda") -> torch.Tensor:
+    """A workspace for ``cfg`` (torch allocation, 512-byte aligned), initialised."""
+    n = workspace_size(cfg)
+    if n == 0:
+        raise MoEError(1, "moe_workspace_size")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    _check(lib().moe_workspace_init(_p(ws), n, _stream()), "moe_workspace_init")
+    return ws
+
+
+def device_status(ws: torch.Tensor) -> int:
+    """Synchronises the current stream and returns (and clears) the device status."""
+    return int(lib().moe_get_device_status(_p(ws), _stream()))
+
+
+def check_device(ws: torch.Tensor, where: str = "device"):
+    _check(device_status(ws), where)
+
+
+def pack_w13(w1: torch.Tensor, w3: torch.Tensor) -> torch.Tensor:
+    E, F, d = w1.shape
+    w13 = torch.empty(E, 2 * F, d, dtype=torch.bfloat16, device=w1.device)
+    _check(lib().moe_pack_w13(E, F, d, _p(w1.contiguous()), _p(w3.contiguous()), _p(w13),
+                              _stream()), "moe_pack_w13")
+    return w13
+
+
+def route(cfg: Config, ws, h=None, wr=None, bias=None, usage=None, logits_in=None):
+    dev = ws.device
+    T, E, k = cfg.T, cfg.E, cfg.k
+    out = dict(logits=torch.empty(T, E, dtype=torch.float32, device=dev),
+               scores=torch.empty(T, E, dtype=torch.float32, device=dev),
+               ids=torch.empty(T, k, dtype=torch.int32, device=dev),
+               topk_w=torch.empty(T, k, dtype=torch.float32, device=dev),
+               counts_pre=torch.empty(E, dtype=torch.int32, device=dev),
+               f=torch.empty(E, dtype=torch.float32, device=dev),
+               P=torch.empty(E, dtype=torch.float32, device=dev))
+    c = cfg.c()
+    st = lib().moe_route(ctypes.byref(c), _p(h), _p(wr), _p(bias), _p(usage), _p(logits_in),
+                         _p(out["logits"]), _p(out["scores"]), _p(out["ids"]), _p(out["topk_w"]),
+                         _p(out["counts_pre"]), _p(out["f"]), _p(out["P"]), _p(ws), ws.numel(),
+                         _stream())
+    _check(st, "moe_route")
+    return out
+
+
+def dispatch(cfg: Config, ws, scores):
+    dev = ws.device
+    T, E, k = cfg.T, cfg.E, cfg.k
+    out = dict(assign=torch.empty(T, k, dtype=torch.int32, device=dev),
+               slot=torch.empty(T, k, dtype=torch.int32, device=dev),
+               flags=torch.empty(T, k, dtype=torch.uint8, device=dev),
+               counts=torch.empty(E, dtype=torch.int32, device=dev),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+               perm=torch.full((max(T * k, 1),), -1, dtype=torch.int32, device=dev),
+               cw=torch.empty(T, k, dtype=torch.float32, device=dev),
+               n_rerouted=torch.zeros(1, dtype=torch.int32, device=dev),
+               n_dropped=torch.zeros(1, dtype=torch.int32, device=dev))
+    c = cfg.c()
+    st = lib().moe_dispatch(ctypes.byref(c), _p(scores), _p(out["assign"]), _p(out["slot"]),
+                            _p(out["flags"]), _p(out["counts"]), _p(out["offsets"]),
+                            _p(out["perm"]), _p(out["cw"]), _p(out["n_rerouted"]),
+                            _p(out["n_dropped"]), _p(ws), ws.numel(), _stream())
+    _check(st, "moe_dispatch")
+    return out
+
+
+def expert_ffn(cfg: Config, ws, h, perm, offsets, w13, w2):
+    y = torch.empty(max(cfg.T * cfg.k, 1), cfg.d_model, dtype=torch.bfloat16, device=ws.device)
+    c = cfg.c()
+    st = lib().moe_expert_ffn(ctypes.byref(c), _p(h), _p(perm), _p(offsets), _p(w13), _p(w2), _p(y),
+                              _p(ws), ws.numel(), _stream())
+    _check(st, "moe_expert_ffn")
+    return y
+
+
+def combine(cfg: Config, y_slots, assign, slot, offsets, cw):
+    out = torch.empty(cfg.T, cfg.d_model, dtype=torch.bfloat16, device=y_slots.device)
+    c = cfg.c()
+    st = lib().moe_combine(ctypes.byref(c), _p(y_slots), _p(assign), _p(slot), _p(offsets), _p(cw),
+                           _p(out), _stream())
+    _check(st, "moe_combine")
+    return out
+
+
+def layer_forward(cfg: Config, ws, h, wr, w13, w2, bias=None, usage=None, aux=False,
+                  stage_events=None, out=None):
+    """The fused layer.  Returns out [T, d] bf16 (and a dict of routing outputs when aux)."""
+    dev = ws.device
+    T, E, k = cfg.T, cfg.E, cfg.k
+    if out is None:
+        out = torch.empty(T, cfg.d_model, dtype=torch.bfloat16, device=dev)
+    extras = None
+    if aux:
+        extras = dict(logits=torch.empty(T, E, dtype=torch.float32, device=dev),
+                      assign=torch.empty(T, k, dtype=torch.int32, device=dev),
+                      slot=torch.empty(T, k, dtype=torch.int32, device=dev),
+                      flags=torch.empty(T, k, dtype=torch.uint8, device=dev),
+                      counts=torch.empty(E, dtype=torch.int32, device=dev),
+                      f=torch.empty(E, dtype=torch.float32, device=dev),
+                      P=torch.empty(E, dtype=torch.float32, device=dev))
+    ev_arr = None
+    if stage_events is not None:
+        for e in stage_events:      # torch creates the CUDA event on its first record
+            if e.cuda_event == 0:
+                e.record()
+        ev_arr = (ctypes.c_void_p * (NUM_STAGES + 1))(*[ctypes.c_void_p(e.cuda_event)
+                                                        for e in stage_events])
+    g = (lambda n: _p(extras[n]) if extras else None)
+    c = cfg.c()
+    st = lib().moe_layer_forward(ctypes.byref(c), _p(h), _p(wr), _p(bias), _p(usage), _p(w13),
+                                 _p(w2), _p(out), g("logits"), g("assign"), g("slot"), g("flags"),
+                                 g("counts"), g("f"), g("P"),
+                                 ctypes.cast(ev_arr, ctypes.c_void_p) if ev_arr is not None else None,
+                                 _p(ws), ws.numel(), _stream())
+    _check(st, "moe_layer_forward")
+    return (out, extras) if aux else out
+
+
+def layer_forward_host(cfg: Config, ws, h_host, wr, w13, w2, out_host, bias=None, usage=None):
+    """End-to-end call from pinned host memory; returns after the stream finished."""
+    c = cfg.c()
+    st = lib().moe_layer_forward_host(ctypes.byref(c), _p(h_host), _p(wr), _p(bias), _p(usage),
+                                      _p(w13), _p(w2), _p(out_host), _p(ws), ws.numel(), _stream())
+    _check(st, "moe_layer_forward_host")
+    return out_host
+
+
+def timeout_probe(ws, budget_cycles: int):
+    _check(lib().moe_debug_timeout_probe(_p(ws), ws.numel(), int(budget_cycles), _stream()),
+           "moe_debug_timeout_probe")

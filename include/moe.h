@@ -203,6 +203,34 @@ moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* h_host,
 moe_status_t moe_debug_timeout_probe(void* ws_dev, size_t ws_bytes, int64_t budget_cycles,
                                      void* stream);
 
+/* Size of the fixed device array that moe_dispatch_static uses for scratch. */
+#define MOE_STATIC_SCRATCH_BYTES (4u << 20)
+
+/* moe_dispatch without a workspace, for callers that cannot allocate device
+ * memory: a plugin that only receives its input and output buffers from the
+ * engine that owns all allocations, or a loop whose rules forbid allocating
+ * after start-up.  The pages have no counterpart to this entry point; it
+ * exists for those callers only.
+ *
+ * Arguments and outputs are those of moe_dispatch (d_model and d_ff are not
+ * used); status_dev (NULL or one int32 on the device) receives the device
+ * status of this call (MOE_OK, or MOE_ERR_NONFINITE for a NaN score).
+ * Scratch lives in one file-scope device array of MOE_STATIC_SCRATCH_BYTES,
+ * held by every GPU that loads the library until the process exits.  Its
+ * device address is looked up with cudaGetSymbolAddress during the first call
+ * on each device (make that first call before any stream capture).  A config
+ * whose scratch does not fit (8 + 9k bytes per token plus (8k+4)*E bytes per
+ * 256 tokens, rounded up; about 135k tokens at E=64, k=2) returns
+ * MOE_ERR_UNSUPPORTED before anything is enqueued.  The call performs no
+ * allocation of any kind.  Every call shares the array and finds the previous
+ * call's contents in it (the status word is cleared per call); calls that
+ * overlap on the GPU race. */
+moe_status_t moe_dispatch_static(const moe_config_t* cfg, const float* scores_dev,
+                                 int32_t* assign_dev, int32_t* slot_dev, uint8_t* flags_dev,
+                                 int32_t* counts_dev, int32_t* offsets_dev, int32_t* perm_dev,
+                                 float* combine_w_dev, int32_t* n_rerouted_dev,
+                                 int32_t* n_dropped_dev, int32_t* status_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -82,6 +82,7 @@ _SIGS = {
     "moe_layer_forward": (I32, [CFG, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_layer_forward_host": (I32, [CFG, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_debug_timeout_probe": (I32, [P, SZ, ctypes.c_int64, P]),
+    "moe_dispatch_static": (I32, [CFG, P, P, P, P, P, P, P, P, P, P, P, P]),
 }
 
 
@@ -262,3 +263,27 @@ def layer_forward_host(cfg: Config, ws, h_host, wr, w13, w2, out_host, bias=None
 def timeout_probe(ws, budget_cycles: int):
     _check(lib().moe_debug_timeout_probe(_p(ws), ws.numel(), int(budget_cycles), _stream()),
            "moe_debug_timeout_probe")
+
+
+def dispatch_static(cfg: Config, scores, device="cuda"):
+    """moe_dispatch_static: the dispatch with the library's fixed scratch array
+    instead of a workspace (for callers that cannot allocate).  The output
+    tensors are allocated here by torch, as any caller's outputs would be."""
+    T, E, k = cfg.T, cfg.E, cfg.k
+    out = dict(assign=torch.empty(T, k, dtype=torch.int32, device=device),
+               slot=torch.empty(T, k, dtype=torch.int32, device=device),
+               flags=torch.empty(T, k, dtype=torch.uint8, device=device),
+               counts=torch.empty(E, dtype=torch.int32, device=device),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device=device),
+               perm=torch.full((max(T * k, 1),), -1, dtype=torch.int32, device=device),
+               cw=torch.empty(T, k, dtype=torch.float32, device=device),
+               n_rerouted=torch.zeros(1, dtype=torch.int32, device=device),
+               n_dropped=torch.zeros(1, dtype=torch.int32, device=device),
+               status=torch.full((1,), -1, dtype=torch.int32, device=device))
+    c = cfg.c()
+    st = lib().moe_dispatch_static(ctypes.byref(c), _p(scores), _p(out["assign"]), _p(out["slot"]),
+                                   _p(out["flags"]), _p(out["counts"]), _p(out["offsets"]),
+                                   _p(out["perm"]), _p(out["cw"]), _p(out["n_rerouted"]),
+                                   _p(out["n_dropped"]), _p(out["status"]), _stream())
+    _check(st, "moe_dispatch_static")
+    return out

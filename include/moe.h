@@ -178,7 +178,8 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* y_slots_dev,
  * Optional outputs (NULL to skip): logits_out [T,E], assign/slot [T,k] int32,
  *   flags [T,k] u8, counts [E] int32, f/P [E] fp32.
  * stage_events: NULL, or MOE_NUM_STAGES+1 cudaEvent_t recorded on `stream`
- *   at the boundaries route | dispatch | zero | gate-up | down | finalize. */
+ *   at the boundaries route | dispatch | prep (zero the fp32 accumulator,
+ *   gather the token rows in slot order) | gate-up | down | finalize. */
 moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* h_dev,
                                const void* w_router_dev, const float* bias_dev,
                                const float* usage_dev, const void* w13_dev, const void* w2_dev,
@@ -219,8 +220,8 @@ moe_status_t moe_debug_timeout_probe(void* ws_dev, size_t ws_bytes, int64_t budg
  * held by every GPU that loads the library until the process exits.  Its
  * device address is looked up with cudaGetSymbolAddress during the first call
  * on each device (make that first call before any stream capture).  A config
- * whose scratch does not fit (8 + 9k bytes per token plus (8k+4)*E bytes per
- * 256 tokens, rounded up; about 135k tokens at E=64, k=2) returns
+ * whose scratch does not fit (max(16, E rounded up to 16) + 9k bytes per token
+ * plus (8k+4)*E bytes per 256 tokens; about 48k tokens at E=64, k=2) returns
  * MOE_ERR_UNSUPPORTED before anything is enqueued.  The call performs no
  * allocation of any kind.  Every call shares the array and finds the previous
  * call's contents in it (the status word is cleared per call); calls that

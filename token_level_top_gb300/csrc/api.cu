@@ -110,7 +110,7 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
     w.part = take(static_cast<size_t>(w.splits) * T * E * 4);
     w.scores = take(T * E * 4);
     w.ids = take(T * k * 4);
-    w.prefs = take(T * kPrefLen);
+    w.prefs = take(T * static_cast<size_t>(pref_stride(c.E)));
     w.crank = take(T * k * 4);
     w.hist = take(k * nch * E * 4);
     w.base = take(k * nch * E * 4 + T * k);
@@ -122,6 +122,7 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
     w.offsets = take((E + 1) * 4);
     w.perm = take(T * k * 4);
     w.cw = take(T * k * 4);
+    w.xg = take(T * k * d * 2);
     w.act = take(T * k * F * 2);
     w.out_acc = take(T * d * 4);
     w.y_slots = (k > 2) ? take(T * k * d * 2) : 0;
@@ -401,8 +402,12 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* h, const int32_
     if (st != MOE_OK) return st;
     if (cfg->T == 0) return MOE_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* xg = ws_at<void>(ws, L.xg);
+    if (launch_gather_rows(cfg->T, cfg->d_model, cfg->k, cfg->E, h, perm, offsets, xg, s) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
     GemmLaunch g = expert_gemm(*cfg, L, GK_GATEUP, ws);
-    g.a_ptr = h;
+    g.a_ptr = xg;
     g.b_ptr = w13;
     g.offsets = offsets;
     g.perm = perm;
@@ -476,9 +481,12 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* h, const voi
         cudaMemsetAsync(acc, 0, sizeof(float) * static_cast<size_t>(c.T) * c.d_model, s) !=
             cudaSuccess)
         return MOE_ERR_CUDA;
+    void* xg = ws_at<void>(ws, L.xg);
+    if (launch_gather_rows(c.T, c.d_model, c.k, c.E, h, o.perm, o.offsets, xg, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
     ev.mark(3);
     GemmLaunch g = expert_gemm(c, L, GK_GATEUP, ws);
-    g.a_ptr = h;
+    g.a_ptr = xg;
     g.b_ptr = w13;
     g.offsets = o.offsets;
     g.perm = o.perm;

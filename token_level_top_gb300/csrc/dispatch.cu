@@ -14,11 +14,12 @@
 // chunks) + (stable rank inside its chunk) -- both written by the route
 // kernel.  Stage 1 (one CTA) scans the chunk histograms per expert, finds the
 // first chunk q1 in which some expert's running count passes C, and leaves
-// the per-chunk bases.  From chunk q1 on, one warp replays the entries 32 at a
-// time: __match_any_sync gives each lane its rank among lanes choosing the
-// same expert, a ballot finds the first lane that takes an expert's last
-// slot, everything up to it commits, and lanes after it that chose the
-// now-full expert choose again.  Stage 2 (grid-wide) writes the entries
+// the per-chunk bases.  From chunk q1 on, the CTA replays the entries in
+// windows of 256 consecutive entries of one rank, one per thread: each entry
+// picks its expert under the current full set, __match_any_sync and a prefix
+// over the warps give it its slot, a block minimum finds the first entry that
+// takes an expert's last slot, everything up to it commits, and entries after
+// it that chose the now-full expert choose again.  Stage 2 (grid-wide) writes the entries
 // before q1, the permutation in slot order and the combine weights
 // ([mhpn] §4.3: router probabilities renormalised over the experts used).
 #include <math.h>
@@ -29,8 +30,9 @@
 namespace moe {
 namespace {
 
-constexpr int kSerialThreads = 1024;
-constexpr size_t kSerialSmemCap = 200 * 1024;
+constexpr int kSerialThreads = 1024;  // one replay window = one entry per thread
+constexpr int kSerialWarps = kSerialThreads / 32;
+constexpr size_t kSerialSmemCap = 224 * 1024;  // dynamic shared memory of the replay CTA
 
 struct SerialArgs {
     DispatchArgs a;
@@ -39,61 +41,83 @@ struct SerialArgs {
 };
 
 // First expert of the preference order that is neither full nor held.  The
-// first kPrefLen entries come from the staged prefix; past it, the best
-// remaining expert is found from the scores with the same order.
-__device__ int choose_expert(const DispatchArgs& a, int t, int r, const uint8_t* pv,
-                             const uint8_t* asg, const int* s_fill)
+// first kPrefLen entries come from the token's staged prefix (16 bytes in
+// registers); past it the stored order is read 16 entries at a time.
+__device__ __forceinline__ int choose_expert(const DispatchArgs& a, int t, const uint4 pw,
+                                             const int (&held)[8], int nheld, const int* s_fill)
 {
-    const int E = a.E, k = a.k;
+    const int E = a.E;
     const int L = E < kPrefLen ? E : kPrefLen;
-    auto held = [&](int e) {
-        for (int q = 0; q < r; ++q)
-            if (asg[static_cast<size_t>(t) * k + q] == e) return true;
-        return false;
+    const uint32_t words[4] = {pw.x, pw.y, pw.z, pw.w};
+    auto is_held = [&](int e) {
+        bool h = false;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) h |= (q < nheld) && (held[q] == e);
+        return h;
     };
-    for (int i = 0; i < L; ++i) {
-        const int e = pv[i];
-        if (s_fill[e] < a.C && !held(e)) return e;
+#pragma unroll
+    for (int i = 0; i < kPrefLen; ++i) {
+        if (i >= L) break;
+        const int e = (words[i >> 2] >> (8 * (i & 3))) & 0xFF;
+        if (s_fill[e] < a.C && !is_held(e)) return e;
     }
     if (L == E) return -1;
-    float bv = -INFINITY;
-    int bi = -1;
-    const float* srow = a.scores + static_cast<size_t>(t) * E;
-    for (int e = 0; e < E; ++e) {
-        bool in_prefix = false;
-        for (int i = 0; i < L; ++i) in_prefix |= (pv[i] == e);
-        if (in_prefix || s_fill[e] >= a.C || held(e)) continue;
-        float s = srow[e];
-        if (isnan(s)) s = -INFINITY;
-        if (bi < 0 || ranks_before(s, e, bv, bi)) {
-            bv = s;
-            bi = e;
+    const uint8_t* orow = a.prefs + static_cast<size_t>(t) * pref_stride(E);
+    for (int p0 = kPrefLen; p0 < E; p0 += 16) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(orow + p0));
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (p0 + i >= E) return -1;
+            const int e = (ww[i >> 2] >> (8 * (i & 3))) & 0xFF;
+            if (s_fill[e] < a.C && !is_held(e)) return e;
         }
     }
-    return bi;
+    return -1;
 }
 
 __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(const SerialArgs sa)
 {
     extern __shared__ __align__(16) uint8_t dsm[];
     __shared__ int s_fill[256];
-    __shared__ int s_q1;
+    __shared__ int s_q1, s_cut, s_estar, s_nre, s_ndrop;
     const DispatchArgs& a = sa.a;
     const int E = a.E, T = a.T, k = a.k, nch = a.nchunks;
     const int Q = k * nch;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // dynamic shared memory: per expert and warp, the window's entry counts and
+    // their exclusive prefix (+ fill); then the staged tail data
+    int (*s_cnt)[kSerialWarps] = reinterpret_cast<int (*)[kSerialWarps]>(dsm);
+    int (*s_base)[kSerialWarps] = reinterpret_cast<int (*)[kSerialWarps]>(dsm + E * kSerialWarps * 4);
+    uint8_t* stage = dsm + 2 * E * kSerialWarps * 4;
 
-    if (tid == 0) s_q1 = Q;
+    if (tid == 0) {
+        s_q1 = Q;
+        s_cut = kSerialThreads;
+        s_nre = 0;
+        s_ndrop = 0;
+    }
+    for (int i = tid; i < kSerialWarps * E; i += kSerialThreads) (&s_cnt[0][0])[i] = 0;
+    static_assert(kSerialWarps == 32, "the cross-warp scan maps one warp count to each lane");
     __syncthreads();
     // ---- stage 1: running count per expert over chunks (rank-major order)
     int total = 0;
     if (tid < E) {
+        const int32_t* __restrict__ hist = a.hist;
+        int32_t* __restrict__ basep = a.base;
         int cum = 0, qe = Q;
-        for (int q = 0; q < Q; ++q) {
-            const int c = a.hist[static_cast<size_t>(q) * E + tid];
-            a.base[static_cast<size_t>(q) * E + tid] = cum;
-            cum += c;
-            if (qe == Q && cum > a.C) qe = q;
+        for (int q0 = 0; q0 < Q; q0 += 16) {
+            int c[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                c[j] = (q0 + j < Q) ? __ldg(hist + static_cast<size_t>(q0 + j) * E + tid) : 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (q0 + j >= Q) break;
+                basep[static_cast<size_t>(q0 + j) * E + tid] = cum;
+                cum += c[j];
+                if (qe == Q && cum > a.C) qe = q0 + j;
+            }
         }
         total = cum;
         atomicMin(&s_q1, qe);
@@ -102,85 +126,153 @@ __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(cons
     const int q1 = s_q1;
     if (tid < E) s_fill[tid] = (q1 < Q) ? a.base[static_cast<size_t>(q1) * E + tid] : total;
 
-    // ---- stage the preference prefixes and the entries' experts
-    const uint8_t* prefs = a.prefs;
+    // ---- stage the tail tokens' preference prefixes and their entries' experts
+    const int r1 = q1 / nch;
+    const int t1 = (q1 - r1 * nch) * kChunk;
+    const int tbeg = (q1 < Q && r1 == k - 1) ? t1 : 0;   // first token with a tail entry
+    const int ntail = (q1 < Q) ? T - tbeg : 0;
+    const int pst16 = pref_stride(E) / 16;   // uint4 words per stored order
+    const uint4* __restrict__ pfx_g = reinterpret_cast<const uint4*>(a.prefs) +
+                                      static_cast<size_t>(tbeg) * pst16;
+    const uint4* pfx = pfx_g;
+    int pfx_step = pst16;                    // staged copies keep only the first 16 bytes
     uint8_t* asg = sa.asg_global;
-    if (sa.use_smem) {
-        uint8_t* sp = dsm;
-        const uint4* src = reinterpret_cast<const uint4*>(a.prefs);
-        uint4* dst = reinterpret_cast<uint4*>(sp);
-        const int n16 = (T * kPrefLen) / 16;
-        for (int i = tid; i < n16; i += kSerialThreads) dst[i] = src[i];
-        for (int i = n16 * 16 + tid; i < T * kPrefLen; i += kSerialThreads) sp[i] = a.prefs[i];
-        prefs = sp;
-        asg = sp + static_cast<size_t>(T) * kPrefLen;
+    if (sa.use_smem && ntail > 0) {
+        uint4* sp = reinterpret_cast<uint4*>(stage);
+        for (int i0 = tid; i0 < ntail; i0 += 4 * kSerialThreads) {
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * kSerialThreads;
+                if (i < ntail) v[j] = pfx_g[static_cast<size_t>(i) * pst16];
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * kSerialThreads;
+                if (i < ntail) sp[i] = v[j];
+            }
+        }
+        pfx = sp;
+        pfx_step = 1;
+        asg = stage + static_cast<size_t>(ntail) * kPrefLen;
     }
-    for (int i = tid; i < T * k; i += kSerialThreads) {
-        const int t = i / k, r = i - t * k;
-        const int q = r * nch + t / kChunk;
-        asg[i] = (q < q1) ? static_cast<uint8_t>(a.ids[i]) : static_cast<uint8_t>(255);
+    {
+        // entry (t, r) is placed before the tail when its chunk r*nch + t/kChunk < q1
+        const int32_t* __restrict__ ids = a.ids;
+        for (int r = 0; r < k; ++r) {
+            for (int t0 = tbeg + tid; t0 < T; t0 += 4 * kSerialThreads) {
+                uint8_t v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = t0 + j * kSerialThreads;
+                    v[j] = 255;
+                    if (t < T && r * nch + (t >> 8) < q1)
+                        v[j] = static_cast<uint8_t>(__ldg(ids + static_cast<size_t>(t) * k + r));
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = t0 + j * kSerialThreads;
+                    if (t < T) asg[static_cast<size_t>(t - tbeg) * k + r] = v[j];
+                }
+            }
+        }
     }
+    static_assert(kChunk == 256, "chunk index is t >> 8");
     __syncthreads();
-    if (warp != 0) return;
 
-    // ---- stage 2: replay from chunk q1 with one warp
+    // ---- stage 2: replay from chunk q1, kSerialThreads consecutive entries of one rank
+    // per window; see the file comment.
     int nre = 0, ndrop = 0;
     if (q1 < Q) {
-        const int r1 = q1 / nch;
-        const int t1 = (q1 - r1 * nch) * kChunk;
         for (int r = r1; r < k; ++r) {
-            for (int t0 = (r == r1 ? t1 : 0); t0 < T; t0 += 32) {
-                const int t = t0 + lane;
+            for (int w0 = (r == r1 ? t1 : 0); w0 < T; w0 += kSerialThreads) {
+                const int t = w0 + tid;
                 const bool valid = t < T;
-                uint8_t pv[kPrefLen];
-                if (valid) {
-                    const uint2 w = reinterpret_cast<const uint2*>(prefs)[t];
+                uint4 pw = make_uint4(0, 0, 0, 0);
+                int held[8];
+                int nheld = 0;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        pv[i] = static_cast<uint8_t>(w.x >> (8 * i));
-                        pv[4 + i] = static_cast<uint8_t>(w.y >> (8 * i));
+                for (int q = 0; q < 8; ++q) held[q] = -1;
+                if (valid) {
+                    pw = pfx[static_cast<size_t>(t - tbeg) * pfx_step];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        if (q < r) {
+                            const int hq = asg[static_cast<size_t>(t - tbeg) * k + q];
+                            held[q] = (hq == 255) ? -1 : hq;
+                        }
                     }
+                    nheld = r;
                 }
-                int e = valid ? choose_expert(a, t, r, pv, asg, s_fill) : -1;
+                const int want = (valid && r < kPrefLen)
+                                     ? (int)(((r < 4 ? pw.x : r < 8 ? pw.y : r < 12 ? pw.z : pw.w) >>
+                                              (8 * (r & 3))) & 0xFF)
+                                     : -1;
+                int e = valid ? choose_expert(a, t, pw, held, nheld, s_fill) : -1;
                 bool active = valid;
                 while (true) {
+                    // ranks among the window's active entries that chose the same expert
                     const int key = active ? e : -2;
                     const uint32_t peers = __match_any_sync(0xffffffffu, key);
                     const int rnk = __popc(peers & lanemask_lt());
-                    const bool takes = active && e >= 0;
-                    const int before = takes ? s_fill[e] : 0;
-                    const bool last = takes && (static_cast<long long>(before) + rnk + 1 == a.C);
-                    const uint32_t ev = __ballot_sync(0xffffffffu, last);
-                    const int cut = ev ? (__ffs(ev) - 1) : 31;
-                    const bool commit = active && lane <= cut;
-                    const uint32_t cmask = __ballot_sync(0xffffffffu, commit);
+                    const bool leader = lane == __ffs(peers) - 1;
+                    if (active && e >= 0 && leader) s_cnt[e][warp] = __popc(peers);
+                    __syncthreads();
+                    // per expert, exclusive prefix over the warps (lane w holds warp w)
+                    for (int ee = warp; ee < E; ee += kSerialWarps) {
+                        const int c = s_cnt[ee][lane];
+                        int incl = c;
+#pragma unroll
+                        for (int off = 1; off < 32; off <<= 1) {
+                            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                            if (lane >= off) incl += v;
+                        }
+                        s_base[ee][lane] = s_fill[ee] + incl - c;
+                    }
+                    __syncthreads();
+                    int slot = 0;
+                    if (active && e >= 0) {
+                        slot = s_base[e][warp] + rnk;
+                        if (leader) s_cnt[e][warp] = 0;   // ready for the next round
+                    }
+                    // the first entry of the window that takes an expert's last slot
+                    const bool last = active && e >= 0 && (static_cast<long long>(slot) + 1 == a.C);
+                    const uint32_t evw = __ballot_sync(0xffffffffu, last);
+                    if (evw && lane == 0) atomicMin(&s_cut, warp * 32 + __ffs(evw) - 1);
+                    __syncthreads();
+                    const int cut = s_cut;
+                    const bool commit = active && tid <= cut;
                     if (commit) {
                         const size_t idx = static_cast<size_t>(t) * k + r;
+                        const size_t li = static_cast<size_t>(t - tbeg) * k + r;
                         if (e >= 0) {
-                            const int fl = (e != pv[r]) ? 1 : 0;
+                            const int fl = (e != want) ? 1 : 0;
                             a.assign[idx] = e;
-                            a.slot[idx] = before + rnk;
+                            a.slot[idx] = slot;
                             a.flags[idx] = static_cast<uint8_t>(fl);
-                            asg[idx] = static_cast<uint8_t>(e);
+                            asg[li] = static_cast<uint8_t>(e);
                             nre += fl;
                         } else {
                             a.assign[idx] = -1;
                             a.slot[idx] = -1;
                             a.flags[idx] = 2;
-                            asg[idx] = 255;
+                            asg[li] = 255;
                             ++ndrop;
                         }
                     }
-                    __syncwarp();
-                    if (commit && e >= 0) {
-                        const uint32_t cp = peers & cmask;
-                        if (lane == __ffs(cp) - 1) s_fill[e] = before + __popc(cp);
+                    if (tid == cut) s_estar = e;
+                    // new fill: each warp's leader adds its committed entries of the expert
+                    const uint32_t cmask = __ballot_sync(0xffffffffu, commit);
+                    if (active && e >= 0 && leader) {
+                        const int nc = __popc(peers & cmask);
+                        if (nc) atomicAdd(&s_fill[e], nc);
                     }
-                    __syncwarp();
-                    if (!ev) break;
-                    const int estar = __shfl_sync(0xffffffffu, e, cut);
-                    active = active && lane > cut;
-                    if (active && e == estar) e = choose_expert(a, t, r, pv, asg, s_fill);
+                    __syncthreads();
+                    if (cut >= kSerialThreads) break;   // no expert filled in this window
+                    const int estar = s_estar;
+                    active = active && tid > cut;
+                    if (active && e == estar) e = choose_expert(a, t, pw, held, nheld, s_fill);
+                    if (tid == 0) s_cut = kSerialThreads;   // read by all before the last barrier
                 }
             }
         }
@@ -189,6 +281,14 @@ __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(cons
         nre += __shfl_xor_sync(0xffffffffu, nre, off);
         ndrop += __shfl_xor_sync(0xffffffffu, ndrop, off);
     }
+    if (lane == 0) {
+        atomicAdd(&s_nre, nre);
+        atomicAdd(&s_ndrop, ndrop);
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    nre = s_nre;
+    ndrop = s_ndrop;
     if (lane == 0) {
         a.ctrl[CTRL_Q1] = q1;
         a.ctrl[CTRL_NRE] = nre;
@@ -242,7 +342,7 @@ __global__ void dispatch_finish_kernel(const DispatchArgs a)
     }
     // combine weights: p of each kept expert renormalised over the kept ones
     const float* srow = a.scores + static_cast<size_t>(t) * E;
-    const int top = a.prefs[static_cast<size_t>(t) * kPrefLen];
+    const int top = a.prefs[static_cast<size_t>(t) * pref_stride(E)];
     float mg = srow[top];
     if (isnan(mg)) mg = -INFINITY;
     float mk = -INFINITY;
@@ -282,13 +382,15 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s)
     if (a.T <= 0) return cudaSuccess;
     SerialArgs sa;
     sa.a = a;
+    // worst case: every token has a tail entry
+    const size_t scan_bytes = 2 * static_cast<size_t>(a.E) * kSerialWarps * 4;
     const size_t need = static_cast<size_t>(a.T) * (kPrefLen + a.k);
-    sa.use_smem = need <= kSerialSmemCap ? 1 : 0;
+    sa.use_smem = (scan_bytes + need) <= kSerialSmemCap ? 1 : 0;
     // without room in shared memory the replay keeps the entries' experts in
     // the (otherwise unused) tail of the rank table
     sa.asg_global = reinterpret_cast<uint8_t*>(a.base) +
                     static_cast<size_t>(a.k) * a.nchunks * a.E * sizeof(int32_t);
-    const size_t smem = sa.use_smem ? need : 0;
+    const size_t smem = scan_bytes + (sa.use_smem ? need : 0);
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(dispatch_serial_kernel,

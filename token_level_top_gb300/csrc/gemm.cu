@@ -2,7 +2,8 @@
 // three dense contractions of the MoE layer:
 //
 //   GK_ROUTER        logits partials  = h . W_r^T          (K split across CTAs)
-//   GK_GATEUP        act = silu(x W1^T) * (x W3^T), x = h rows gathered by perm
+//   GK_GATEUP        act = silu(x W1^T) * (x W3^T), x = the slot-ordered token rows
+//                    (tiled from x_perm, or gathered from h by tile::gather4)
 //   GK_DOWN_SCATTER  out_acc[t] += cw[t,r] * (act W2^T)    (weighted scatter)
 //   GK_DOWN_SLOTS    y_slots     = act W2^T                 (slot order, bf16)
 //
@@ -43,6 +44,7 @@ struct GemmParams {
     int splits;        // router K splits
     int kb_per_split;  // router K blocks per split
     int stages;
+    int gather4;       // gate-up: A rows gathered from h with tile::gather4 (else tiled from x_perm)
     uint32_t tmem_cols;
     const int32_t* offsets;
     const int32_t* perm;
@@ -173,13 +175,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int r0 = 0, r1 = 0, r2 = 0, r3 = 0, arow = 0, brow = 0;
             if (p.kind == GK_GATEUP) {
                 const int off = s_offs[ti.e];
-                const int cnt = s_offs[ti.e + 1] - off;
-                const int j0 = ti.m * kBM + lane * 4;
-                const int fallback = p.perm[off + ti.m * kBM] / p.topk;  // a valid row
-                r0 = (j0 + 0 < cnt) ? p.perm[off + j0 + 0] / p.topk : fallback;
-                r1 = (j0 + 1 < cnt) ? p.perm[off + j0 + 1] / p.topk : fallback;
-                r2 = (j0 + 2 < cnt) ? p.perm[off + j0 + 2] / p.topk : fallback;
-                r3 = (j0 + 3 < cnt) ? p.perm[off + j0 + 3] / p.topk : fallback;
+                if (p.gather4) {
+                    const int cnt = s_offs[ti.e + 1] - off;
+                    const int j0 = ti.m * kBM + lane * 4;
+                    const int fallback = p.perm[off + ti.m * kBM] / p.topk;  // a valid row
+                    r0 = (j0 + 0 < cnt) ? p.perm[off + j0 + 0] / p.topk : fallback;
+                    r1 = (j0 + 1 < cnt) ? p.perm[off + j0 + 1] / p.topk : fallback;
+                    r2 = (j0 + 2 < cnt) ? p.perm[off + j0 + 2] / p.topk : fallback;
+                    r3 = (j0 + 3 < cnt) ? p.perm[off + j0 + 3] / p.topk : fallback;
+                } else {
+                    arow = off + ti.m * kBM;
+                }
                 brow = ti.e * 2 * p.F + ti.n * kExpertBN;
             } else if (p.kind == GK_ROUTER) {
                 arow = ti.m * kBM;
@@ -198,7 +204,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 __syncwarp();
                 const int x = kb * kBK;
                 const uint32_t dA = smem_u32(sA + stage * a_bytes);
-                if (p.kind == GK_GATEUP) {
+                if (p.kind == GK_GATEUP && p.gather4) {
                     tma_gather4(dA + lane * 4 * 128, &tmA, x, r0, r1, r2, r3, fb);
                 } else if (lane == 0) {
                     tma_load_2d(dA, &tmA, x, arow, fb);
@@ -455,7 +461,13 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
         p.bn = kExpertBN;
         p.kb_total = g.d / kBK;
         p.n_tiles = g.F / (kExpertBN / 2);
-        if (!make_map(&tmA, g.a_ptr, g.T, g.d, 1)) return cudaErrorInvalidValue;
+        p.gather4 = g.gather4;
+        if (g.gather4) {
+            if (!make_map(&tmA, g.a_ptr, g.T, g.d, 1)) return cudaErrorInvalidValue;
+        } else {
+            if (!make_map(&tmA, g.a_ptr, static_cast<uint64_t>(g.T) * g.topk, g.d, kBM))
+                return cudaErrorInvalidValue;
+        }
         if (!make_map(&tmB, g.b_ptr, static_cast<uint64_t>(g.E) * 2 * g.F, g.d, kExpertBN))
             return cudaErrorInvalidValue;
         const long long mt_max = (static_cast<long long>(g.T) * g.topk + kBM - 1) / kBM + g.E;

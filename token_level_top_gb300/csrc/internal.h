@@ -10,7 +10,7 @@
 namespace moe {
 
 constexpr int kChunk = 256;        // tokens per routing chunk (one route block)
-constexpr int kPrefLen = 8;        // preference-order prefix kept per token
+constexpr int kPrefLen = 16;       // preference-order prefix staged per token by the dispatch
 constexpr int kBM = 128;           // GEMM tile rows (tokens / slots)
 constexpr int kBK = 64;            // GEMM K per pipeline stage (128 bytes of bf16)
 constexpr int kExpertBN = 256;     // expert GEMM tile columns
@@ -26,12 +26,15 @@ struct WsLayout {
     int epad = 0;      // router N tile (E rounded up to 16, at least 16)
     size_t status = 0, ctrl = 0, part = 0, scores = 0, ids = 0, prefs = 0, crank = 0, hist = 0,
            base = 0, ppart = 0, assign = 0, slot = 0, flags = 0, counts = 0, offsets = 0,
-           perm = 0, cw = 0, act = 0, out_acc = 0, y_slots = 0, h_stage = 0, out_stage = 0;
+           perm = 0, cw = 0, xg = 0, act = 0, out_acc = 0, y_slots = 0, h_stage = 0, out_stage = 0;
     size_t total = 0;
 };
 
 // ctrl block (int32 words)
 enum CtrlWord : int { CTRL_Q1 = 0, CTRL_NRE = 1, CTRL_NDROP = 2, CTRL_WORDS = 64 };
+
+// Bytes per token of the stored preference order: all E experts, padded to 16.
+__host__ __device__ inline int pref_stride(int E) { return E <= kPrefLen ? kPrefLen : (E + 15) / 16 * 16; }
 
 bool layout_for(const moe_config_t& c, WsLayout* L);
 int router_splits(int T, int d);
@@ -57,7 +60,7 @@ struct RouteArgs {
     int32_t* ids_user;       // [T][k] or NULL
     float* topk_w;           // [T][k] or NULL
     int32_t* ids_ws;         // [T][k]
-    uint8_t* prefs;          // [T][kPrefLen]
+    uint8_t* prefs;          // [T][pref_stride(E)] full preference order
     int32_t* crank;          // [T][k]
     int32_t* hist;           // [k*nchunks][E]
     float* ppart;            // [nchunks][E]
@@ -80,7 +83,7 @@ struct DispatchArgs {
     int64_t C;
     const float* scores;
     const int32_t* ids;
-    const uint8_t* prefs;
+    const uint8_t* prefs;    // [T][pref_stride(E)]
     const int32_t* crank;
     const int32_t* hist;
     int32_t* base;
@@ -111,6 +114,7 @@ struct GemmLaunch {
     void* y_slots;
     float* router_part;
     int splits, epad;
+    int gather4;  // gate-up: gather A rows from h (a_ptr = h) instead of tiles of x_perm
     int* status;
     long long budget;
 };
@@ -119,6 +123,8 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
 cudaError_t launch_pack_w13(int E, int F, int d, const void* w1, const void* w3, void* w13,
                             cudaStream_t s);
 cudaError_t launch_finalize(int T, int d, const float* acc, void* out, cudaStream_t s);
+cudaError_t launch_gather_rows(int T, int d, int k, int E, const void* h, const int32_t* perm,
+                               const int32_t* offsets, void* x_perm, cudaStream_t s);
 cudaError_t launch_combine(int T, int d, int k, const void* y_slots, const int32_t* assign,
                            const int32_t* slot, const int32_t* offsets, const float* cw, void* out,
                            cudaStream_t s);

@@ -69,6 +69,23 @@ __global__ void combine_kernel(int T, int d, int k, const uint4* __restrict__ y,
     }
 }
 
+// x_perm[i] = h[perm[i] / k] for the kept slots i < offsets[E]: the token rows
+// in slot order, so that the gate-up GEMM reads its A tiles with plain TMA
+// tile loads.  16 bytes per thread, rows of d bf16.
+__global__ void gather_rows_kernel(int rows_max, int d8, int k, int E, const uint4* __restrict__ h,
+                                   const int32_t* __restrict__ perm,
+                                   const int32_t* __restrict__ offsets, uint4* __restrict__ x)
+{
+    const int n = offsets[E];
+    const size_t total = static_cast<size_t>(min(n, rows_max)) * d8;
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t row = i / d8, c = i - row * d8;
+        const int t = perm[row] / k;
+        x[i] = h[static_cast<size_t>(t) * d8 + c];
+    }
+}
+
 // One thread waits on an mbarrier that nothing will ever complete, with the
 // library's bounded wait; when the budget runs out it records the timeout.
 __global__ void timeout_probe_kernel(int* status, long long budget)
@@ -107,6 +124,18 @@ cudaError_t launch_finalize(int T, int d, const float* acc, void* out, cudaStrea
     if (n4 == 0) return cudaSuccess;
     finalize_kernel<<<grid_for(n4, 256), 256, 0, s>>>(n4, reinterpret_cast<const float4*>(acc),
                                                        static_cast<uint2*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(int T, int d, int k, int E, const void* h, const int32_t* perm,
+                               const int32_t* offsets, void* x_perm, cudaStream_t s)
+{
+    const int rows_max = T * k;
+    const size_t total = static_cast<size_t>(rows_max) * (d / 8);
+    if (total == 0) return cudaSuccess;
+    gather_rows_kernel<<<grid_for(total, 256), 256, 0, s>>>(rows_max, d / 8, k, E,
+                                                             static_cast<const uint4*>(h), perm,
+                                                             offsets, static_cast<uint4*>(x_perm));
     return cudaGetLastError();
 }
 

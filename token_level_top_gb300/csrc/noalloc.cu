@@ -56,7 +56,7 @@ StaticLayout static_layout(const moe_config_t& c)
     L.status = take(256);
     L.ctrl = take(CTRL_WORDS * 4);
     L.ids = take(T * k * 4);
-    L.prefs = take(T * kPrefLen);
+    L.prefs = take(T * static_cast<size_t>(pref_stride(c.E)));
     L.crank = take(T * k * 4);
     L.hist = take(k * nch * E * 4);
     L.base = take(k * nch * E * 4 + T * k);  // + the replay's per-entry expert bytes

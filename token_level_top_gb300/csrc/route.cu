@@ -8,8 +8,10 @@
 //
 // Each block handles a chunk of kChunk consecutive tokens.  A token is owned
 // by G = min(32, pow2(E)) lanes, each lane holding EPL experts (e = lane + G*j);
-// the first kPrefLen entries of the preference order come out of repeated
-// group arg-max rounds with warp shuffles.  Per chunk the kernel also writes
+// each lane ranks its experts against all E scores (shuffled through the
+// group), which gives the whole preference order, stored as expert bytes per
+// token: the first k ranks are the top-k picks, the rest serve the
+// dispatch's reroutes.  Per chunk the kernel also writes
 // the per-rank histogram of picks and each pick's stable rank among equal
 // picks in token order (warp __match_any_sync + a scan over warps): the
 // dispatch uses them to place every entry before the first capacity event in
@@ -23,8 +25,9 @@
 namespace moe {
 namespace {
 
-constexpr int kRouteThreads = 256;
+constexpr int kRouteThreads = 1024;             // 32 warps share one chunk of tokens
 constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kRankWarps = kChunk / 32;          // the rank pass: one token per thread
 
 __device__ __forceinline__ float softmax_num(float s, float m)
 {
@@ -36,9 +39,9 @@ __device__ __forceinline__ float softmax_num(float s, float m)
 template <int EPL>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
 {
-    __shared__ int s_ids[kChunk * 8];
-    __shared__ int s_wcnt[kRouteWarps][256];
-    __shared__ float s_wsum[kRouteWarps][256];
+    __shared__ int16_t s_ids[kChunk * 8];
+    __shared__ int s_wcnt[kRankWarps][32 * EPL];
+    __shared__ float s_wsum[kRouteWarps][32 * EPL];
     __shared__ int s_nan;
 
     const int E = a.E, k = a.k, T = a.T;
@@ -48,7 +51,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
     const int lg = lane & (G - 1);
     const int grp = lane / G;
     const int tpw = 32 / G;
-    const int L = E < kPrefLen ? E : kPrefLen;
     const int chunk = blockIdx.x;
     const int t_begin = chunk * kChunk;
     if (threadIdx.x == 0) s_nan = 0;
@@ -89,40 +91,26 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
                 s[j] = sc;
             }
         }
-        // preference order prefix: L rounds of group arg-max
-        uint32_t picked = 0;
-        int pref[kPrefLen];
-        float pv[kPrefLen];
+        // Rank of each of this lane's experts in the token's preference order:
+        // the number of experts that rank before it (all E scores visit every
+        // lane of the group by shuffles).
+        int rank[EPL];
 #pragma unroll
-        for (int i = 0; i < kPrefLen; ++i) {
-            pref[i] = 255;
-            pv[i] = -INFINITY;
-            if (i < L) {
-                float bv = -INFINITY;
-                int bi = 0x7fffffff;
+        for (int j = 0; j < EPL; ++j) rank[j] = 0;
+        float m = -INFINITY;
+        for (int src = 0; src < G; ++src) {
 #pragma unroll
-                for (int j = 0; j < EPL; ++j) {
-                    const int e = lg + G * j;
-                    if (e < E && !((picked >> j) & 1u) && ranks_before(s[j], e, bv, bi)) {
-                        bv = s[j];
-                        bi = e;
-                    }
+            for (int jj = 0; jj < EPL; ++jj) {
+                const float v = __shfl_sync(0xffffffffu, s[jj], src, G);
+                const int ei = src + G * jj;
+                if (ei < E) {
+                    m = fmaxf(m, v);
+#pragma unroll
+                    for (int j = 0; j < EPL; ++j) rank[j] += ranks_before(v, ei, s[j], lg + G * j) ? 1 : 0;
                 }
-                for (int off = G >> 1; off >= 1; off >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off, G);
-                    const int oi = __shfl_xor_sync(0xffffffffu, bi, off, G);
-                    if (ranks_before(ov, oi, bv, bi)) {
-                        bv = ov;
-                        bi = oi;
-                    }
-                }
-                pref[i] = bi;
-                pv[i] = bv;
-                if ((bi & (G - 1)) == lg) picked |= 1u << (bi / G);
             }
         }
         // softmax over the token's experts
-        const float m = pv[0];
         float num[EPL];
         float part_sum = 0.0f;
 #pragma unroll
@@ -135,21 +123,19 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
             part_sum += __shfl_xor_sync(0xffffffffu, part_sum, off, G);
         const float zsum = part_sum;
         if (valid) {
+            uint8_t* prow = a.prefs + static_cast<size_t>(t) * pref_stride(E);
+            for (int i = E + lg; i < kPrefLen; i += G) prow[i] = 255;   // pad short orders
 #pragma unroll
-            for (int j = 0; j < EPL; ++j) acc[j] += num[j] / zsum;
-            if (lg == 0) {
-                uint32_t lo = 0, hi = 0;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) lo |= static_cast<uint32_t>(pref[i] & 0xFF) << (8 * i);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) hi |= static_cast<uint32_t>(pref[4 + i] & 0xFF) << (8 * i);
-                reinterpret_cast<uint2*>(a.prefs)[t] = make_uint2(lo, hi);
-                for (int r = 0; r < k; ++r) {
-                    a.ids_ws[static_cast<size_t>(t) * k + r] = pref[r];
-                    if (a.ids_user) a.ids_user[static_cast<size_t>(t) * k + r] = pref[r];
-                    if (a.topk_w)
-                        a.topk_w[static_cast<size_t>(t) * k + r] = softmax_num(pv[r], m) / zsum;
-                    s_ids[tl * k + r] = pref[r];
+            for (int j = 0; j < EPL; ++j) {
+                const int e = lg + G * j;
+                acc[j] += num[j] / zsum;
+                if (e < E) prow[rank[j]] = static_cast<uint8_t>(e);
+                if (e < E && rank[j] < k) {
+                    const size_t o = static_cast<size_t>(t) * k + rank[j];
+                    a.ids_ws[o] = e;
+                    if (a.ids_user) a.ids_user[o] = e;
+                    if (a.topk_w) a.topk_w[o] = num[j] / zsum;
+                    s_ids[tl * k + rank[j]] = static_cast<int16_t>(e);
                 }
             }
         } else if (lg == 0) {
@@ -170,7 +156,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
         }
     }
     for (int e = threadIdx.x; e < E; e += kRouteThreads)
-        for (int w = 0; w < kRouteWarps; ++w) s_wcnt[w][e] = 0;
+        for (int w = 0; w < kRankWarps; ++w) s_wcnt[w][e] = 0;
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += kRouteThreads) {
         float tot = 0.0f;
@@ -180,17 +166,23 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
     if (threadIdx.x == 0 && s_nan) record_error(a.status, MOE_ERR_NONFINITE);
 
     // ---- per rank: histogram of picks and stable rank within the chunk
-    const int tl = threadIdx.x;  // kRouteThreads == kChunk: one token per thread
+    // (the first kChunk threads, one token each; the other warps only join
+    // the barriers)
+    const bool ranker = threadIdx.x < kChunk;
+    const int tl = threadIdx.x;
     const int t = t_begin + tl;
     for (int r = 0; r < k; ++r) {
-        const int e = s_ids[tl * k + r];
-        const uint32_t peers = __match_any_sync(0xffffffffu, e);
-        const int rnk = __popc(peers & lanemask_lt());
-        if (e >= 0 && lane == __ffs(peers) - 1) s_wcnt[warp][e] = __popc(peers);
+        int e = -1, rnk = 0;
+        if (ranker) {
+            e = s_ids[tl * k + r];
+            const uint32_t peers = __match_any_sync(0xffffffffu, e);
+            rnk = __popc(peers & lanemask_lt());
+            if (e >= 0 && lane == __ffs(peers) - 1) s_wcnt[warp][e] = __popc(peers);
+        }
         __syncthreads();
         for (int ee = threadIdx.x; ee < E; ee += kRouteThreads) {
             int run = 0;
-            for (int w = 0; w < kRouteWarps; ++w) {
+            for (int w = 0; w < kRankWarps; ++w) {
                 const int c = s_wcnt[w][ee];
                 s_wcnt[w][ee] = run;  // exclusive prefix over warps
                 run += c;
@@ -198,10 +190,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
             a.hist[(static_cast<size_t>(r) * a.nchunks + chunk) * E + ee] = run;
         }
         __syncthreads();
-        if (e >= 0 && t < T) a.crank[static_cast<size_t>(t) * k + r] = s_wcnt[warp][e] + rnk;
+        if (ranker && e >= 0 && t < T) a.crank[static_cast<size_t>(t) * k + r] = s_wcnt[warp][e] + rnk;
         __syncthreads();
         for (int ee = threadIdx.x; ee < E; ee += kRouteThreads)
-            for (int w = 0; w < kRouteWarps; ++w) s_wcnt[w][ee] = 0;
+            for (int w = 0; w < kRankWarps; ++w) s_wcnt[w][ee] = 0;
         __syncthreads();
     }
 }
@@ -222,7 +214,7 @@ __global__ void route_stats_kernel(const StatsArgs a)
 
 }  // namespace
 
-static_assert(kRouteThreads == kChunk, "one token per thread in the rank pass");
+static_assert(kRouteThreads >= kChunk && kChunk % 32 == 0, "one token per thread in the rank pass");
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s)
 {

@@ -145,6 +145,26 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu capture of this kernel and
+    workload, or None when there is none or the kernel source changed since."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        rec = json.load(fh).get(kernel)
+    if not rec or rec.get("workload") != workload:
+        return None
+    h = hashlib.sha256()
+    for f in rec["sources"]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest()[:16] != rec["source_sha256_16"]:
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
 def layer_inputs(shape, device="cuda"):
     h, wr, bias, usage = synth.router_inputs(shape)
     w1, w3, w2 = synth.expert_weights(shape, device=device)
@@ -307,7 +327,7 @@ def run_ours(args, rank, world, local):
         roof = {"bound": "hbm", "achieved": bytes_[dom] / sec / 1e9, "peak": peak_bw,
                 "unit": "GB/s", "peak_kind": f"{peak_kind} HBM copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = recorded_traffic(f"moe_gemm_kernel ({dom.replace('_', '-')})", shape.name)
     roof["kernel"] = f"moe_gemm_kernel ({dom.replace('_', '-')})"
     roof["algorithmic_per_launch"] = {"flop": flops[dom], "bytes": bytes_[dom]}
     expert_tflops = (flops["gate_up"] + flops["down"]) / (

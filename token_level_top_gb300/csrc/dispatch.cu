@@ -40,26 +40,40 @@ struct SerialArgs {
     uint8_t* asg_global;  // [T*k] fallback when the staging does not fit in smem
 };
 
+// Experts already serving a token (its earlier ranks), packed one per byte
+// into two words; unused bytes hold 0xFF, which is never an expert id.
+struct Held {
+    uint32_t lo = 0xFFFFFFFFu, hi = 0xFFFFFFFFu;
+    __device__ __forceinline__ void set(int q, int e)
+    {
+        const uint32_t sh = 8 * (q & 3), m = ~(0xFFu << sh), v = static_cast<uint32_t>(e & 0xFF) << sh;
+        if (q < 4)
+            lo = (lo & m) | v;
+        else
+            hi = (hi & m) | v;
+    }
+    __device__ __forceinline__ bool has(int e) const
+    {
+        const uint32_t b = 0x01010101u * static_cast<uint32_t>(e);
+        const uint32_t x = lo ^ b, y = hi ^ b;   // a zero byte marks a match
+        return (((x - 0x01010101u) & ~x) | ((y - 0x01010101u) & ~y)) & 0x80808080u;
+    }
+};
+
 // First expert of the preference order that is neither full nor held.  The
 // first kPrefLen entries come from the token's staged prefix (16 bytes in
 // registers); past it the stored order is read 16 entries at a time.
-__device__ __forceinline__ int choose_expert(const DispatchArgs& a, int t, const uint4 pw,
-                                             const int (&held)[8], int nheld, const int* s_fill)
+__device__ __forceinline__ int choose_expert(const DispatchArgs& a, int cap, int t, const uint4 pw,
+                                             const Held& held, const int* s_fill)
 {
     const int E = a.E;
     const int L = E < kPrefLen ? E : kPrefLen;
     const uint32_t words[4] = {pw.x, pw.y, pw.z, pw.w};
-    auto is_held = [&](int e) {
-        bool h = false;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) h |= (q < nheld) && (held[q] == e);
-        return h;
-    };
 #pragma unroll
     for (int i = 0; i < kPrefLen; ++i) {
         if (i >= L) break;
         const int e = (words[i >> 2] >> (8 * (i & 3))) & 0xFF;
-        if (s_fill[e] < a.C && !is_held(e)) return e;
+        if (s_fill[e] < cap && !held.has(e)) return e;
     }
     if (L == E) return -1;
     const uint8_t* orow = a.prefs + static_cast<size_t>(t) * pref_stride(E);
@@ -70,7 +84,7 @@ __device__ __forceinline__ int choose_expert(const DispatchArgs& a, int t, const
         for (int i = 0; i < 16; ++i) {
             if (p0 + i >= E) return -1;
             const int e = (ww[i >> 2] >> (8 * (i & 3))) & 0xFF;
-            if (s_fill[e] < a.C && !is_held(e)) return e;
+            if (s_fill[e] < cap && !held.has(e)) return e;
         }
     }
     return -1;
@@ -84,6 +98,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(cons
     const DispatchArgs& a = sa.a;
     const int E = a.E, T = a.T, k = a.k, nch = a.nchunks;
     const int Q = k * nch;
+    const int cap = static_cast<int>(a.C);   // C <= T*k < 2^30
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // dynamic shared memory: per expert and warp, the window's entry counts and
     // their exclusive prefix (+ fill); then the staged tail data
@@ -189,26 +204,16 @@ __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(cons
                 const int t = w0 + tid;
                 const bool valid = t < T;
                 uint4 pw = make_uint4(0, 0, 0, 0);
-                int held[8];
-                int nheld = 0;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) held[q] = -1;
+                Held held;
                 if (valid) {
                     pw = pfx[static_cast<size_t>(t - tbeg) * pfx_step];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        if (q < r) {
-                            const int hq = asg[static_cast<size_t>(t - tbeg) * k + q];
-                            held[q] = (hq == 255) ? -1 : hq;
-                        }
-                    }
-                    nheld = r;
+                    for (int q = 0; q < r; ++q) held.set(q, asg[static_cast<size_t>(t - tbeg) * k + q]);
                 }
                 const int want = (valid && r < kPrefLen)
                                      ? (int)(((r < 4 ? pw.x : r < 8 ? pw.y : r < 12 ? pw.z : pw.w) >>
                                               (8 * (r & 3))) & 0xFF)
                                      : -1;
-                int e = valid ? choose_expert(a, t, pw, held, nheld, s_fill) : -1;
+                int e = valid ? choose_expert(a, cap, t, pw, held, s_fill) : -1;
                 bool active = valid;
                 while (true) {
                     // ranks among the window's active entries that chose the same expert
@@ -236,7 +241,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(cons
                         if (leader) s_cnt[e][warp] = 0;   // ready for the next round
                     }
                     // the first entry of the window that takes an expert's last slot
-                    const bool last = active && e >= 0 && (static_cast<long long>(slot) + 1 == a.C);
+                    const bool last = active && e >= 0 && slot + 1 == cap;
                     const uint32_t evw = __ballot_sync(0xffffffffu, last);
                     if (evw && lane == 0) atomicMin(&s_cut, warp * 32 + __ffs(evw) - 1);
                     __syncthreads();
@@ -271,7 +276,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(cons
                     if (cut >= kSerialThreads) break;   // no expert filled in this window
                     const int estar = s_estar;
                     active = active && tid > cut;
-                    if (active && e == estar) e = choose_expert(a, t, pw, held, nheld, s_fill);
+                    if (active && e == estar) e = choose_expert(a, cap, t, pw, held, s_fill);
                     if (tid == 0) s_cut = kSerialThreads;   // read by all before the last barrier
                 }
             }

@@ -488,7 +488,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     const size_t fixed = 1024 + 64 + static_cast<size_t>(2 * (g.E + 1)) * 4 + 16 + 6 * 8;
     const size_t budget_smem = 227 * 1024;
     int stages = static_cast<int>((budget_smem - fixed) / (a_bytes + b_bytes + 16));
-    stages = std::max(2, std::min(stages, 8));
+    stages = std::max(2, std::min(stages, g.kind == GK_ROUTER ? 4 : 8));   // router: 2 CTAs per SM
     p.stages = stages;
     p.tmem_cols = pow2_cols(2 * p.bn);
     const size_t smem = fixed + static_cast<size_t>(stages) * (a_bytes + b_bytes + 16);

@@ -91,22 +91,73 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
                 s[j] = sc;
             }
         }
-        // Rank of each of this lane's experts in the token's preference order:
-        // the number of experts that rank before it (all E scores visit every
-        // lane of the group by shuffles).
+        // The token's preference order.  Up to 32 experts: each lane counts the
+        // experts that rank before its own (all scores pass through the group by
+        // shuffles).  More: a bitonic sort of the (score, index) keys across the
+        // warp, element i = lane*EPL + j.
         int rank[EPL];
-#pragma unroll
-        for (int j = 0; j < EPL; ++j) rank[j] = 0;
         float m = -INFINITY;
-        for (int src = 0; src < G; ++src) {
-#pragma unroll
-            for (int jj = 0; jj < EPL; ++jj) {
-                const float v = __shfl_sync(0xffffffffu, s[jj], src, G);
-                const int ei = src + G * jj;
-                if (ei < E) {
+        float sv[EPL];
+        int se[EPL];
+        if (EPL == 1) {
+            rank[0] = 0;
+            for (int src = 0; src < G; ++src) {
+                const float v = __shfl_sync(0xffffffffu, s[0], src, G);
+                if (src < E) {
                     m = fmaxf(m, v);
+                    rank[0] += ranks_before(v, src, s[0], lg) ? 1 : 0;
+                }
+            }
+        } else {
 #pragma unroll
-                    for (int j = 0; j < EPL; ++j) rank[j] += ranks_before(v, ei, s[j], lg + G * j) ? 1 : 0;
+            for (int j = 0; j < EPL; ++j) {
+                const int e = lg + G * j;
+                sv[j] = (e < E) ? s[j] : -INFINITY;
+                se[j] = (e < E) ? e : 0x7fff + e;   // absent experts sort last
+                m = fmaxf(m, sv[j]);
+            }
+            for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            // network element i = lane*EPL + j (any starting placement sorts)
+            constexpr int N = 32 * EPL;
+#pragma unroll
+            for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll
+                for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                    if (stride < EPL) {
+#pragma unroll
+                        for (int j = 0; j < EPL; ++j) {
+                            const int pj = j ^ stride;
+                            if (pj > j) {
+                                const int i = lane * EPL + j;
+                                const bool asc = (i & size) == 0;
+                                const bool swap = asc ? ranks_before(sv[pj], se[pj], sv[j], se[j])
+                                                      : ranks_before(sv[j], se[j], sv[pj], se[pj]);
+                                if (swap) {
+                                    const float tv = sv[j];
+                                    sv[j] = sv[pj];
+                                    sv[pj] = tv;
+                                    const int te = se[j];
+                                    se[j] = se[pj];
+                                    se[pj] = te;
+                                }
+                            }
+                        }
+                    } else {
+                        const int dl = stride / EPL;
+#pragma unroll
+                        for (int j = 0; j < EPL; ++j) {
+                            const float ov = __shfl_xor_sync(0xffffffffu, sv[j], dl);
+                            const int oe = __shfl_xor_sync(0xffffffffu, se[j], dl);
+                            const int i = lane * EPL + j;
+                            const bool asc = (i & size) == 0;
+                            const bool low = (lane & dl) == 0;
+                            const bool other_better = ranks_before(ov, oe, sv[j], se[j]);
+                            if (other_better == (low == asc)) {
+                                sv[j] = ov;
+                                se[j] = oe;
+                            }
+                        }
+                    }
                 }
             }
         }
@@ -124,18 +175,34 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const RouteArgs a)
         const float zsum = part_sum;
         if (valid) {
             uint8_t* prow = a.prefs + static_cast<size_t>(t) * pref_stride(E);
-            for (int i = E + lg; i < kPrefLen; i += G) prow[i] = 255;   // pad short orders
 #pragma unroll
-            for (int j = 0; j < EPL; ++j) {
-                const int e = lg + G * j;
-                acc[j] += num[j] / zsum;
-                if (e < E) prow[rank[j]] = static_cast<uint8_t>(e);
-                if (e < E && rank[j] < k) {
-                    const size_t o = static_cast<size_t>(t) * k + rank[j];
-                    a.ids_ws[o] = e;
-                    if (a.ids_user) a.ids_user[o] = e;
-                    if (a.topk_w) a.topk_w[o] = num[j] / zsum;
-                    s_ids[tl * k + rank[j]] = static_cast<int16_t>(e);
+            for (int j = 0; j < EPL; ++j) acc[j] += num[j] / zsum;
+            if (EPL == 1) {
+                for (int i = E + lg; i < kPrefLen; i += G) prow[i] = 255;   // pad short orders
+                const int e = lg;
+                if (e < E) {
+                    prow[rank[0]] = static_cast<uint8_t>(e);
+                    if (rank[0] < k) {
+                        const size_t o = static_cast<size_t>(t) * k + rank[0];
+                        a.ids_ws[o] = e;
+                        if (a.ids_user) a.ids_user[o] = e;
+                        if (a.topk_w) a.topk_w[o] = num[0] / zsum;
+                        s_ids[tl * k + rank[0]] = static_cast<int16_t>(e);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < EPL; ++j) {
+                    const int pos = lane * EPL + j;   // sorted position
+                    const int e = se[j];
+                    if (pos < E) prow[pos] = static_cast<uint8_t>(e);
+                    if (pos < k) {
+                        const size_t o = static_cast<size_t>(t) * k + pos;
+                        a.ids_ws[o] = e;
+                        if (a.ids_user) a.ids_user[o] = e;
+                        if (a.topk_w) a.topk_w[o] = softmax_num(sv[j], m) / zsum;
+                        s_ids[tl * k + pos] = static_cast<int16_t>(e);
+                    }
                 }
             }
         } else if (lg == 0) {

@@ -178,8 +178,12 @@ def test_dispatch_repeatable():
 
 # ----------------------------------------------------------------------------- experts
 
+# the last three pair row tiles across a 2-CTA cluster (T*k >= 256*E), with odd
+# row-tile counts per expert among them
 @pytest.mark.parametrize("T,d,E,F,k,cf", [(300, 192, 5, 256, 2, 1.0), (256, 512, 8, 1024, 2, 1.25),
-                                          (40, 64, 3, 128, 1, 1.0), (600, 128, 6, 384, 3, 1.0)])
+                                          (40, 64, 3, 128, 1, 1.0), (600, 128, 6, 384, 3, 1.0),
+                                          (700, 128, 3, 256, 2, 1.0), (1300, 256, 2, 512, 2, 1.25),
+                                          (1000, 192, 4, 384, 2, 1.0)])
 def test_expert_ffn_vs_oracle(T, d, E, F, k, cf):
     shape = synth.MoEShape("t", T=T, d=d, E=E, F=F, k=k, cf=cf, seed=T + F)
     h, wr, _, _ = synth.router_inputs(shape)
@@ -268,7 +272,8 @@ def test_layer_forward_deterministic(name):
 
 
 @pytest.mark.parametrize("T,E,k,cap", [(1, 8, 2, 0), (300, 6, 1, 0), (300, 6, 3, 0),
-                                       (257, 4, 2, 30), (64, 1, 1, 0)])
+                                       (257, 4, 2, 30), (64, 1, 1, 0), (900, 3, 2, 0),
+                                       (1500, 2, 2, 700)])
 def test_layer_forward_edge_shapes(T, E, k, cap):
     shape = synth.MoEShape("edge", T=T, d=128, E=E, F=256, k=k, cf=1.0, capacity=cap, seed=T + E)
     Ld = make_layer(shape)

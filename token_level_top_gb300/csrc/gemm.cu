@@ -61,8 +61,14 @@ struct TileInfo {
     int e, m, n, kb0, kb1, split;
 };
 
+// Expert tiles are numbered expert by expert; within an expert, row units
+// fastest (the row tiles that share a weight tile run together), then column
+// tiles.  In paired mode a unit is two adjacent row tiles, one per CTA of the
+// cluster, which share each weight tile through multicast.
+template <bool PAIR>
 __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile,
-                                                const int* s_tile_start, const int* s_offs)
+                                                const int* s_tile_start, const int* s_offs,
+                                                int rank)
 {
     TileInfo ti;
     if (p.kind == GK_ROUTER) {
@@ -85,10 +91,11 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile,
     const int e = lo;
     const int cnt = s_offs[e + 1] - s_offs[e];
     const int mt = (cnt + kBM - 1) / kBM;
+    const int units = PAIR ? (mt + 1) / 2 : mt;
     const int local = tile - s_tile_start[e];
     ti.e = e;
-    ti.m = local % mt;  // m fastest: the row tiles of one weight tile run together
-    ti.n = local / mt;
+    ti.m = PAIR ? 2 * (local % units) + rank : local % units;
+    ti.n = local / units;
     ti.kb0 = 0;
     ti.kb1 = p.kb_total;
     ti.split = 0;
@@ -97,6 +104,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile,
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
 
+template <bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p)
@@ -106,7 +114,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int stages = p.stages;
     const uint32_t a_bytes = kBM * kBK * 2;
-    const uint32_t b_bytes = static_cast<uint32_t>(p.bn) * kBK * 2;
+    // paired: this CTA holds its 128 A rows and half of the BN weight rows
+    const uint32_t b_bytes = static_cast<uint32_t>(PAIR ? p.bn / 2 : p.bn) * kBK * 2;
     uint8_t* sA = smem;
     uint8_t* sB = sA + stages * a_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sB + stages * b_bytes);
@@ -120,6 +129,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
@@ -130,13 +140,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&tfull_bar[b]), 1);
-            mbar_init(smem_u32(&tempty_bar[b]), 4);
+            mbar_init(smem_u32(&tempty_bar[b]), PAIR ? 8 : 4);   // paired: both CTAs' epilogues
         }
         mbar_fence_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), p.tmem_cols);
-        tmem_relinquish();
+        if (PAIR) {   // one warp of each CTA of the pair, collectively
+            tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(s_tmem)), p.tmem_cols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(const_cast<uint32_t*>(s_tmem)), p.tmem_cols);
+            tmem_relinquish();
+        }
     }
     if (p.kind != GK_ROUTER && warp == 2) {
         // tile_start[e] = sum over e' < e of ceil(count_e' / 128) * n_tiles
@@ -147,7 +162,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (e <= p.E) o = p.offsets[e];
             if (e < p.E) o1 = p.offsets[e + 1];
             if (e <= p.E) s_offs[e] = o;
-            int tiles = (e < p.E) ? ((o1 - o + kBM - 1) / kBM) * p.n_tiles : 0;
+            const int mt = (o1 - o + kBM - 1) / kBM;
+            int tiles = (e < p.E) ? (PAIR ? (mt + 1) / 2 : mt) * p.n_tiles : 0;
             int incl = tiles;
             for (int off = 1; off < 32; off <<= 1) {
                 int v = __shfl_up_sync(0xffffffffu, incl, off);
@@ -160,9 +176,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (PAIR) cluster_sync_all();   // the peer's barriers exist before anything targets them
     const uint32_t tmem_base = *s_tmem;
     const int total_tiles = (p.kind == GK_ROUTER) ? p.m_tiles * p.splits : s_tile_start[p.E];
-    const uint32_t idesc = idesc_bf16_f32(kBM, p.bn);
+    const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, p.bn);
+    const bool leader = rank == 0;   // the paired MMAs are issued by CTA 0 of the cluster
+    // a cluster's two CTAs walk the same tile sequence
+    const int tile0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int tile_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
     bool ok = true;
 
     if (warp == 0) {
@@ -170,8 +191,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load in flight + its parity
-        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-            const TileInfo ti = decode_tile(p, tile, s_tile_start, s_offs);
+        for (int tile = tile0; tile < total_tiles && ok; tile += tile_step) {
+            const TileInfo ti = decode_tile<PAIR>(p, tile, s_tile_start, s_offs, rank);
             int r0 = 0, r1 = 0, r2 = 0, r3 = 0, arow = 0, brow = 0;
             if (p.kind == GK_GATEUP) {
                 const int off = s_offs[ti.e];
@@ -195,21 +216,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 brow = ti.e * p.d + ti.n * p.bn;
             }
             for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
-                if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, p.budget)) {
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, p.budget))) {
                     ok = false;
                     break;
                 }
-                const uint32_t fb = smem_u32(&full_bar[stage]);
-                if (lane == 0) mbar_arrive_expect_tx(fb, a_bytes + b_bytes);
+                // paired: both CTAs' copies count on the leader CTA's full barrier
+                const uint32_t fb = PAIR ? map_to_rank(smem_u32(&full_bar[stage]), 0)
+                                         : smem_u32(&full_bar[stage]);
+                if (lane == 0 && leader)
+                    mbar_arrive_expect_tx(smem_u32(&full_bar[stage]),
+                                          (PAIR ? 2u : 1u) * (a_bytes + b_bytes));
                 __syncwarp();
                 const int x = kb * kBK;
                 const uint32_t dA = smem_u32(sA + stage * a_bytes);
-                if (p.kind == GK_GATEUP && p.gather4) {
-                    tma_gather4(dA + lane * 4 * 128, &tmA, x, r0, r1, r2, r3, fb);
-                } else if (lane == 0) {
-                    tma_load_2d(dA, &tmA, x, arow, fb);
+                const uint32_t dB = smem_u32(sB + stage * b_bytes);
+                if (PAIR) {
+                    if (lane == 0) {
+                        tma_load_2d_pair(dA, &tmA, x, arow, fb);
+                        tma_load_2d_pair(dB, &tmB, x, brow + rank * (p.bn / 2), fb);
+                    }
+                } else {
+                    if (p.kind == GK_GATEUP && p.gather4)
+                        tma_gather4(dA + lane * 4 * 128, &tmA, x, r0, r1, r2, r3, fb);
+                    else if (lane == 0)
+                        tma_load_2d(dA, &tmA, x, arow, fb);
+                    if (lane == 0) tma_load_2d(dB, &tmB, x, brow, fb);
                 }
-                if (lane == 0) tma_load_2d(smem_u32(sB + stage * b_bytes), &tmB, x, brow, fb);
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == stages) {
@@ -220,21 +252,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         if (!ok) {
             record_error(p.status, MOE_ERR_TIMEOUT);
-            // let the copies this warp issued land before the CTA exits
-            for (int s = 0; s < stages; ++s)
-                if (issued_mask & (1u << s))
-                    mbar_wait(smem_u32(&full_bar[s]), (issued_parity >> s) & 1, p.budget);
+            // let the copies issued land before the CTA exits (paired: the leader's
+            // full barriers count both CTAs' copies; the final cluster barrier
+            // holds the peer until the leader has drained)
+            if (leader)
+                for (int s = 0; s < stages; ++s)
+                    if (issued_mask & (1u << s))
+                        mbar_wait(smem_u32(&full_bar[s]), (issued_parity >> s) & 1, p.budget);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
             int last_b = -1;
             uint32_t last_par = 0;
-            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
-                const TileInfo ti = decode_tile(p, tile, s_tile_start, s_offs);
+            for (int tile = tile0; tile < total_tiles && ok; tile += tile_step, ++it) {
+                const TileInfo ti = decode_tile<PAIR>(p, tile, s_tile_start, s_offs, rank);
                 const int b = it & 1;
                 const uint32_t acc_par = (it >> 1) & 1;
                 if (!mbar_wait(smem_u32(&tempty_bar[b]), acc_par ^ 1, p.budget)) {
@@ -253,17 +288,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t b0 = smem_u32(sB + stage * b_bytes);
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k) {
-                        mma_bf16(d_tmem, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc,
-                                 (kb > ti.kb0 || k > 0) ? 1u : 0u);
+                        const uint64_t ad = sdesc_k_sw128(a0 + k * 32), bd = sdesc_k_sw128(b0 + k * 32);
+                        const uint32_t acc = (kb > ti.kb0 || k > 0) ? 1u : 0u;
+                        if (PAIR)
+                            mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
+                        else
+                            mma_bf16(d_tmem, ad, bd, idesc, acc);
                     }
-                    mma_commit(smem_u32(&empty_bar[stage]));
+                    if (PAIR)   // frees the slot in both CTAs
+                        mma_commit_pair(smem_u32(&empty_bar[stage]));
+                    else
+                        mma_commit(smem_u32(&empty_bar[stage]));
                     if (++stage == stages) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&tfull_bar[b]));
+                if (PAIR)
+                    mma_commit_pair(smem_u32(&tfull_bar[b]));
+                else
+                    mma_commit(smem_u32(&tfull_bar[b]));
                 last_b = b;
                 last_par = acc_par;
             }
@@ -277,8 +322,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;
         int it = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
-            const TileInfo ti = decode_tile(p, tile, s_tile_start, s_offs);
+        for (int tile = tile0; tile < total_tiles; tile += tile_step, ++it) {
+            const TileInfo ti = decode_tile<PAIR>(p, tile, s_tile_start, s_offs, rank);
             const int b = it & 1;
             const uint32_t acc_par = (it >> 1) & 1;
             if (!mbar_wait(smem_u32(&tfull_bar[b]), acc_par, p.budget)) {
@@ -373,15 +418,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[b]));
+            if (lane == 0) {
+                if (PAIR && !leader)   // the leader's MMAs wait for both CTAs' epilogues
+                    mbar_arrive_cluster(map_to_rank(smem_u32(&tempty_bar[b]), 0));
+                else
+                    mbar_arrive(smem_u32(&tempty_bar[b]));
+            }
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync_all();   // no CTA leaves while its peer may still target it
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, p.tmem_cols);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, p.tmem_cols);
+        else
+            tmem_dealloc(tmem_base, p.tmem_cols);
     }
 }
 
@@ -447,6 +501,9 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     CUtensorMap tmA, tmB;
     int grid = 0;
     const int sms = num_sms();
+    // Row tiles are paired when the experts average at least two of them.
+    const bool pair = (g.kind != GK_ROUTER) && !g.gather4 &&
+                      static_cast<long long>(g.T) * g.topk >= 2LL * kBM * g.E;
     if (g.kind == GK_ROUTER) {
         p.bn = g.epad;
         p.kb_total = g.d / kBK;
@@ -468,7 +525,8 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
             if (!make_map(&tmA, g.a_ptr, static_cast<uint64_t>(g.T) * g.topk, g.d, kBM))
                 return cudaErrorInvalidValue;
         }
-        if (!make_map(&tmB, g.b_ptr, static_cast<uint64_t>(g.E) * 2 * g.F, g.d, kExpertBN))
+        if (!make_map(&tmB, g.b_ptr, static_cast<uint64_t>(g.E) * 2 * g.F, g.d,
+                      pair ? kExpertBN / 2 : kExpertBN))
             return cudaErrorInvalidValue;
         const long long mt_max = (static_cast<long long>(g.T) * g.topk + kBM - 1) / kBM + g.E;
         grid = static_cast<int>(std::min<long long>(mt_max * p.n_tiles, sms));
@@ -478,13 +536,14 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
         p.n_tiles = (g.d + kExpertBN - 1) / kExpertBN;
         if (!make_map(&tmA, g.a_ptr, static_cast<uint64_t>(g.T) * g.topk, g.F, kBM))
             return cudaErrorInvalidValue;
-        if (!make_map(&tmB, g.b_ptr, static_cast<uint64_t>(g.E) * g.d, g.F, kExpertBN))
+        if (!make_map(&tmB, g.b_ptr, static_cast<uint64_t>(g.E) * g.d, g.F,
+                      pair ? kExpertBN / 2 : kExpertBN))
             return cudaErrorInvalidValue;
         const long long mt_max = (static_cast<long long>(g.T) * g.topk + kBM - 1) / kBM + g.E;
         grid = static_cast<int>(std::min<long long>(mt_max * p.n_tiles, sms));
     }
     const uint32_t a_bytes = kBM * kBK * 2;
-    const uint32_t b_bytes = static_cast<uint32_t>(p.bn) * kBK * 2;
+    const uint32_t b_bytes = static_cast<uint32_t>(pair ? p.bn / 2 : p.bn) * kBK * 2;
     const size_t fixed = 1024 + 64 + static_cast<size_t>(2 * (g.E + 1)) * 4 + 16 + 6 * 8;
     const size_t budget_smem = 227 * 1024;
     int stages = static_cast<int>((budget_smem - fixed) / (a_bytes + b_bytes + 16));
@@ -496,13 +555,44 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        227 * 1024);
+        attr_err = cudaFuncSetAttribute(moe_gemm_kernel<false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(moe_gemm_kernel<true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (grid <= 0) return cudaSuccess;
-    moe_gemm_kernel<<<grid, kGemmThreads, smem, s>>>(tmA, tmB, p);
-    return cudaGetLastError();
+    if (!pair) {
+        moe_gemm_kernel<false><<<grid, kGemmThreads, smem, s>>>(tmA, tmB, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // a persistent grid of no more clusters than can be resident at once
+    static int cached_clusters[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int max_clusters = (dev >= 0 && dev < 64) ? cached_clusters[dev] : 0;
+    if (max_clusters <= 0) {
+        cfg.gridDim = dim3(2 * 64, 1, 1);
+        if (cudaOccupancyMaxActiveClusters(&max_clusters, moe_gemm_kernel<true>, &cfg) != cudaSuccess ||
+            max_clusters <= 0)
+            max_clusters = sms / 2;
+        if (dev >= 0 && dev < 64) cached_clusters[dev] = max_clusters;
+    }
+    const int clusters = std::max(1, std::min(grid / 2, max_clusters));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+    return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<true>, tmA, tmB, p);
 }
 
 }  // namespace moe

@@ -45,7 +45,7 @@ KERNELS_PER_STEP = 8  # router GEMM, route, dispatch (2), row gather, gate-up, d
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.CONFIG_ORDER)
@@ -97,7 +97,7 @@ def load_peaks():
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples during the timed region."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -112,13 +112,14 @@ class ClockSampler:
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100",
+                                          "--format=csv,noheader,nounits", "-lms", "50",
                                           "-i", str(self.dev)], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t_begin=None, t_end=None):
+        """Summary of the samples taken between the wall-clock times t_begin and t_end."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -127,22 +128,32 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
+        import datetime
         rows = []
         with open(self.path) as fh:
             for line in fh:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                if t_begin is not None and not (t_begin <= ts <= t_end):
+                    continue
+                rows.append(parts[1:])
         os.unlink(self.path)
         if not rows:
             return None
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
-                "samples": len(rows)}
+                "power_w_median": statistics.median(power) if power else None,
+                "samples": len(rows), "window": "timed region only"}
 
 
 def recorded_traffic(kernel: str, workload: str):
@@ -280,13 +291,16 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
     t0.record()
     for i in range(args.steps):
         step(stage_evs[i])
     t1.record()
     torch.cuda.synchronize()
+    wall1 = time.time()
     barrier(world)
-    clk = clocks.stop()
+    time.sleep(0.2)   # let the sampler flush its last lines
+    clk = clocks.stop(wall0, wall1)
     ms = t0.elapsed_time(t1)
     ms_max = max_over_ranks(ms, world)
     st = moe.device_status(ws)

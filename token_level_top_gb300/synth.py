@@ -12,9 +12,9 @@ Recipe (shapes and distributions of the five workloads):
     and ``W2 ~ N(0, 1/F)`` (variance 1/d_in), all rounded to bf16;
   * ``h``, ``W_r`` and the usage vector come from a CPU ``torch.Generator``
     seeded with the workload's seed, drawn in that order, so that they are the
-    same on every machine; the expert weights come from a second generator on
-    the target device seeded with ``seed + 1000`` (their values depend on the
-    device; every comparison gives both sides the same tensors);
+    same on every machine; each expert's weights come from its own generator
+    on the target device seeded with ``seed + 1000 + 7919 * e`` (their values
+    depend on the device; every comparison gives both sides the same tensors);
   * the skewed workload adds a router bias ``b = beta * e_0`` (beta fixed below
     so that expert 0 is the rank-1 pick of about 42% of tokens after the
     penalty) and a usage vector ``U[0, 1)^E`` with lambda = 0.8, and replaces

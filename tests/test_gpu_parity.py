@@ -146,6 +146,11 @@ DISPATCH_CASES = [
     ("T1", 1, 8, 2, 1.0, 0, "gauss"),
     ("E1", 77, 1, 1, 1.0, 0, "gauss"),
     ("E200", 4000, 200, 2, 1.1, 0, "skew"),
+    # one chunk (T <= 256): route and dispatch run as one block
+    ("small-E200", 256, 200, 2, 1.0, 0, "skew"),
+    ("small-E255-k8", 250, 255, 8, 1.0, 3, "gauss"),
+    ("small-E64-deep", 256, 64, 2, 1.0, 2, "identical"),
+    ("small-E128-k4", 199, 128, 4, 1.0, 0, "skew"),
 ]
 
 
@@ -273,7 +278,7 @@ def test_layer_forward_deterministic(name):
 
 @pytest.mark.parametrize("T,E,k,cap", [(1, 8, 2, 0), (300, 6, 1, 0), (300, 6, 3, 0),
                                        (257, 4, 2, 30), (64, 1, 1, 0), (900, 3, 2, 0),
-                                       (1500, 2, 2, 700)])
+                                       (1500, 2, 2, 700), (200, 40, 2, 2)])
 def test_layer_forward_edge_shapes(T, E, k, cap):
     shape = synth.MoEShape("edge", T=T, d=128, E=E, F=256, k=k, cf=1.0, capacity=cap, seed=T + E)
     Ld = make_layer(shape)

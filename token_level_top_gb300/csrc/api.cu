@@ -83,7 +83,7 @@ int router_splits(int T, int d)
     const int mt = (T + kBM - 1) / kBM;
     const int kb = d / kBK;
     int S = (320 + mt - 1) / std::max(mt, 1);
-    S = std::max(1, std::min(S, std::max(1, kb / 2)));
+    S = std::max(1, std::min(S, std::max(1, kb / 4)));   // at least 4 K steps per split
     // no empty split: (S - 1) * ceil(kb / S) < kb
     while (S > 1 && (S - 1) * ((kb + S - 1) / S) >= kb) --S;
     return S;
@@ -135,30 +135,31 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
 
 namespace {
 
-moe_status_t run_route(const moe_config_t& c, const WsLayout& L, const void* h, const void* wr,
-                       const float* bias, const float* usage, const float* logits_in,
-                       float* logits_out, float* scores_out, int32_t* ids_user, float* topk_w,
-                       void* ws, cudaStream_t s)
+// The router GEMM (skipped when logits are given).
+moe_status_t run_router_gemm(const moe_config_t& c, const WsLayout& L, const void* h,
+                             const void* wr, void* ws, cudaStream_t s)
 {
-    int* status = ws_at<int>(ws, L.status);
-    if (!logits_in) {
-        GemmLaunch g{};
-        g.kind = GK_ROUTER;
-        g.E = c.E;
-        g.T = c.T;
-        g.topk = c.k;
-        g.d = c.d_model;
-        g.F = c.d_ff;
-        g.a_ptr = h;
-        g.b_ptr = wr;
-        g.router_part = ws_at<float>(ws, L.part);
-        g.splits = L.splits;
-        g.epad = L.epad;
-        g.status = status;
-        g.budget = kSpinBudget;
-        cudaError_t e = launch_gemm(g, s);
-        if (e != cudaSuccess) return MOE_ERR_CUDA;
-    }
+    GemmLaunch g{};
+    g.kind = GK_ROUTER;
+    g.E = c.E;
+    g.T = c.T;
+    g.topk = c.k;
+    g.d = c.d_model;
+    g.F = c.d_ff;
+    g.a_ptr = h;
+    g.b_ptr = wr;
+    g.router_part = ws_at<float>(ws, L.part);
+    g.splits = L.splits;
+    g.epad = L.epad;
+    g.status = ws_at<int>(ws, L.status);
+    g.budget = kSpinBudget;
+    return cuda_status(launch_gemm(g, s));
+}
+
+RouteArgs route_args(const moe_config_t& c, const WsLayout& L, const float* bias,
+                     const float* usage, const float* logits_in, float* logits_out,
+                     float* scores_out, int32_t* ids_user, float* topk_w, void* ws)
+{
     RouteArgs a{};
     a.T = c.T;
     a.E = c.E;
@@ -182,8 +183,22 @@ moe_status_t run_route(const moe_config_t& c, const WsLayout& L, const void* h, 
     a.crank = ws_at<int32_t>(ws, L.crank);
     a.hist = ws_at<int32_t>(ws, L.hist);
     a.ppart = ws_at<float>(ws, L.ppart);
-    a.status = status;
-    return cuda_status(launch_route(a, s));
+    a.status = ws_at<int>(ws, L.status);
+    return a;
+}
+
+moe_status_t run_route(const moe_config_t& c, const WsLayout& L, const void* h, const void* wr,
+                       const float* bias, const float* usage, const float* logits_in,
+                       float* logits_out, float* scores_out, int32_t* ids_user, float* topk_w,
+                       void* ws, cudaStream_t s)
+{
+    if (!logits_in) {
+        moe_status_t st = run_router_gemm(c, L, h, wr, ws, s);
+        if (st != MOE_OK) return st;
+    }
+    return cuda_status(launch_route(route_args(c, L, bias, usage, logits_in, logits_out,
+                                               scores_out, ids_user, topk_w, ws),
+                                    s));
 }
 
 moe_status_t run_stats(const moe_config_t& c, const WsLayout& L, int32_t* counts_pre, float* f,
@@ -210,8 +225,8 @@ struct DispatchOut {
     int32_t *n_rerouted, *n_dropped;
 };
 
-moe_status_t run_dispatch(const moe_config_t& c, const WsLayout& L, const float* scores,
-                          const DispatchOut& o, void* ws, cudaStream_t s)
+DispatchArgs dispatch_args(const moe_config_t& c, const WsLayout& L, const float* scores,
+                           const DispatchOut& o, void* ws)
 {
     DispatchArgs a{};
     a.T = c.T;
@@ -236,7 +251,13 @@ moe_status_t run_dispatch(const moe_config_t& c, const WsLayout& L, const float*
     a.n_rerouted = o.n_rerouted;
     a.n_dropped = o.n_dropped;
     a.status = ws_at<int>(ws, L.status);
-    return cuda_status(launch_dispatch(a, s));
+    return a;
+}
+
+moe_status_t run_dispatch(const moe_config_t& c, const WsLayout& L, const float* scores,
+                          const DispatchOut& o, void* ws, cudaStream_t s)
+{
+    return cuda_status(launch_dispatch(dispatch_args(c, L, scores, o, ws), s));
 }
 
 GemmLaunch expert_gemm(const moe_config_t& c, const WsLayout& L, int kind, void* ws)
@@ -383,8 +404,11 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const float* scores, int32_t*
     a.hist = ws_at<int32_t>(ws, L.hist);
     a.ppart = ws_at<float>(ws, L.ppart);
     a.status = ws_at<int>(ws, L.status);
-    if (launch_route(a, s) != cudaSuccess) return MOE_ERR_CUDA;
     DispatchOut o{assign, slot, counts, offsets, perm, flags, combine_w, n_rerouted, n_dropped};
+    if (L.nchunks == 1)
+        return cuda_status(
+            launch_route_dispatch_small(a, dispatch_args(*cfg, L, scores, o, ws), s));
+    if (launch_route(a, s) != cudaSuccess) return MOE_ERR_CUDA;
     return run_dispatch(*cfg, L, scores, o, ws, s);
 }
 
@@ -403,7 +427,8 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* h, const int32_
     if (cfg->T == 0) return MOE_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void* xg = ws_at<void>(ws, L.xg);
-    if (launch_gather_rows(cfg->T, cfg->d_model, cfg->k, cfg->E, h, perm, offsets, xg, s) !=
+    if (launch_gather_rows(cfg->T, cfg->d_model, cfg->k, cfg->E, h, perm, offsets, xg, nullptr,
+                           s) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
     GemmLaunch g = expert_gemm(*cfg, L, GK_GATEUP, ws);
@@ -456,9 +481,14 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* h, const voi
     Ev ev{stage_events, s};
 
     ev.mark(0);
-    st = run_route(c, L, h, w_router, bias, usage, nullptr, logits_out, nullptr, nullptr, nullptr,
-                   ws, s);
+    st = run_router_gemm(c, L, h, w_router, ws, s);
     if (st != MOE_OK) return st;
+    const RouteArgs ra =
+        route_args(c, L, bias, usage, nullptr, logits_out, nullptr, nullptr, nullptr, ws);
+    // a batch of one chunk routes and dispatches in one kernel (the route stage
+    // then holds only the router GEMM, the dispatch stage both)
+    const bool small = L.nchunks == 1;
+    if (!small && launch_route(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
     ev.mark(1);
     DispatchOut o;
     o.assign = assign ? assign : ws_at<int32_t>(ws, L.assign);
@@ -470,19 +500,18 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* h, const voi
     o.cw = ws_at<float>(ws, L.cw);
     o.n_rerouted = nullptr;
     o.n_dropped = nullptr;
-    st = run_dispatch(c, L, ws_at<float>(ws, L.scores), o, ws, s);
-    if (st != MOE_OK) return st;
+    const DispatchArgs da = dispatch_args(c, L, ws_at<float>(ws, L.scores), o, ws);
+    if (cudaError_t e = small ? launch_route_dispatch_small(ra, da, s) : launch_dispatch(da, s);
+        e != cudaSuccess)
+        return MOE_ERR_CUDA;
     st = run_stats(c, L, nullptr, f, P, ws, s);
     if (st != MOE_OK) return st;
     ev.mark(2);
     const bool fused = c.k <= 2;  // at most two fp32 addends per element: order-free
     float* acc = ws_at<float>(ws, L.out_acc);
-    if (fused &&
-        cudaMemsetAsync(acc, 0, sizeof(float) * static_cast<size_t>(c.T) * c.d_model, s) !=
-            cudaSuccess)
-        return MOE_ERR_CUDA;
     void* xg = ws_at<void>(ws, L.xg);
-    if (launch_gather_rows(c.T, c.d_model, c.k, c.E, h, o.perm, o.offsets, xg, s) != cudaSuccess)
+    if (launch_gather_rows(c.T, c.d_model, c.k, c.E, h, o.perm, o.offsets, xg,
+                           fused ? acc : nullptr, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     ev.mark(3);
     GemmLaunch g = expert_gemm(c, L, GK_GATEUP, ws);

@@ -26,6 +26,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "route_block.cuh"
 
 namespace moe {
 namespace {
@@ -39,6 +40,18 @@ struct SerialArgs {
     int use_smem;
     uint8_t* asg_global;  // [T*k] fallback when the staging does not fit in smem
 };
+
+// Read-only loads through the non-coherent cache, except where the data was
+// written earlier in the same kernel (the fused small-batch kernel), which
+// needs plain loads.
+template <bool NC, typename V>
+__device__ __forceinline__ V ld_in(const V* p)
+{
+    if constexpr (NC)
+        return __ldg(p);
+    else
+        return *p;
+}
 
 // Experts already serving a token (its earlier ranks), packed one per byte
 // into two words; unused bytes hold 0xFF, which is never an expert id.
@@ -63,6 +76,7 @@ struct Held {
 // First expert of the preference order that is neither full nor held.  The
 // first kPrefLen entries come from the token's staged prefix (16 bytes in
 // registers); past it the stored order is read 16 entries at a time.
+template <bool NC>
 __device__ __forceinline__ int choose_expert(const DispatchArgs& a, int cap, int t, const uint4 pw,
                                              const Held& held, const int* s_fill)
 {
@@ -78,7 +92,7 @@ __device__ __forceinline__ int choose_expert(const DispatchArgs& a, int cap, int
     if (L == E) return -1;
     const uint8_t* orow = a.prefs + static_cast<size_t>(t) * pref_stride(E);
     for (int p0 = kPrefLen; p0 < E; p0 += 16) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(orow + p0));
+        const uint4 w = ld_in<NC>(reinterpret_cast<const uint4*>(orow + p0));
         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -90,9 +104,11 @@ __device__ __forceinline__ int choose_expert(const DispatchArgs& a, int cap, int
     return -1;
 }
 
-__global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(const SerialArgs sa)
+// The replay, by one block of kSerialThreads threads; dsm is the block's
+// dynamic shared memory (sized by the launchers below).
+template <bool NC>
+__device__ __forceinline__ void dispatch_serial_block(const SerialArgs& sa, uint8_t* dsm)
 {
-    extern __shared__ __align__(16) uint8_t dsm[];
     __shared__ int s_fill[256];
     __shared__ int s_q1, s_cut, s_estar, s_nre, s_ndrop;
     const DispatchArgs& a = sa.a;
@@ -118,14 +134,14 @@ __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(cons
     // ---- stage 1: running count per expert over chunks (rank-major order)
     int total = 0;
     if (tid < E) {
-        const int32_t* __restrict__ hist = a.hist;
+        const int32_t* hist = a.hist;
         int32_t* __restrict__ basep = a.base;
         int cum = 0, qe = Q;
         for (int q0 = 0; q0 < Q; q0 += 16) {
             int c[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                c[j] = (q0 + j < Q) ? __ldg(hist + static_cast<size_t>(q0 + j) * E + tid) : 0;
+                c[j] = (q0 + j < Q) ? ld_in<NC>(hist + static_cast<size_t>(q0 + j) * E + tid) : 0;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 if (q0 + j >= Q) break;
@@ -147,7 +163,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(cons
     const int tbeg = (q1 < Q && r1 == k - 1) ? t1 : 0;   // first token with a tail entry
     const int ntail = (q1 < Q) ? T - tbeg : 0;
     const int pst16 = pref_stride(E) / 16;   // uint4 words per stored order
-    const uint4* __restrict__ pfx_g = reinterpret_cast<const uint4*>(a.prefs) +
+    const uint4* pfx_g = reinterpret_cast<const uint4*>(a.prefs) +
                                       static_cast<size_t>(tbeg) * pst16;
     const uint4* pfx = pfx_g;
     int pfx_step = pst16;                    // staged copies keep only the first 16 bytes
@@ -171,9 +187,9 @@ __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(cons
         pfx_step = 1;
         asg = stage + static_cast<size_t>(ntail) * kPrefLen;
     }
-    {
+    if (ntail > 0) {
         // entry (t, r) is placed before the tail when its chunk r*nch + t/kChunk < q1
-        const int32_t* __restrict__ ids = a.ids;
+        const int32_t* ids = a.ids;
         for (int r = 0; r < k; ++r) {
             for (int t0 = tbeg + tid; t0 < T; t0 += 4 * kSerialThreads) {
                 uint8_t v[4];
@@ -182,7 +198,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(cons
                     const int t = t0 + j * kSerialThreads;
                     v[j] = 255;
                     if (t < T && r * nch + (t >> 8) < q1)
-                        v[j] = static_cast<uint8_t>(__ldg(ids + static_cast<size_t>(t) * k + r));
+                        v[j] = static_cast<uint8_t>(ld_in<NC>(ids + static_cast<size_t>(t) * k + r));
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -213,7 +229,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(cons
                                      ? (int)(((r < 4 ? pw.x : r < 8 ? pw.y : r < 12 ? pw.z : pw.w) >>
                                               (8 * (r & 3))) & 0xFF)
                                      : -1;
-                int e = valid ? choose_expert(a, cap, t, pw, held, s_fill) : -1;
+                int e = valid ? choose_expert<NC>(a, cap, t, pw, held, s_fill) : -1;
                 bool active = valid;
                 while (true) {
                     // ranks among the window's active entries that chose the same expert
@@ -276,7 +292,7 @@ __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(cons
                     if (cut >= kSerialThreads) break;   // no expert filled in this window
                     const int estar = s_estar;
                     active = active && tid > cut;
-                    if (active && e == estar) e = choose_expert(a, cap, t, pw, held, s_fill);
+                    if (active && e == estar) e = choose_expert<NC>(a, cap, t, pw, held, s_fill);
                     if (tid == 0) s_cut = kSerialThreads;   // read by all before the last barrier
                 }
             }
@@ -291,39 +307,46 @@ __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(cons
         atomicAdd(&s_ndrop, ndrop);
     }
     __syncthreads();
-    if (warp != 0) return;
-    nre = s_nre;
-    ndrop = s_ndrop;
-    if (lane == 0) {
-        a.ctrl[CTRL_Q1] = q1;
-        a.ctrl[CTRL_NRE] = nre;
-        a.ctrl[CTRL_NDROP] = ndrop;
-        if (a.n_rerouted) *a.n_rerouted = nre;
-        if (a.n_dropped) *a.n_dropped = ndrop;
-    }
-    // counts and exclusive offsets
-    int carry = 0;
-    for (int b = 0; b < E; b += 32) {
-        const int e = b + lane;
-        const int c = (e < E) ? s_fill[e] : 0;
-        int incl = c;
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += v;
+    if (warp == 0) {
+        nre = s_nre;
+        ndrop = s_ndrop;
+        if (lane == 0) {
+            a.ctrl[CTRL_Q1] = q1;
+            a.ctrl[CTRL_NRE] = nre;
+            a.ctrl[CTRL_NDROP] = ndrop;
+            if (a.n_rerouted) *a.n_rerouted = nre;
+            if (a.n_dropped) *a.n_dropped = ndrop;
         }
-        if (e < E) {
-            a.counts[e] = c;
-            a.offsets[e] = carry + incl - c;
+        // counts and exclusive offsets
+        int carry = 0;
+        for (int b = 0; b < E; b += 32) {
+            const int e = b + lane;
+            const int c = (e < E) ? s_fill[e] : 0;
+            int incl = c;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            if (e < E) {
+                a.counts[e] = c;
+                a.offsets[e] = carry + incl - c;
+            }
+            carry += __shfl_sync(0xffffffffu, incl, 31);
         }
-        carry += __shfl_sync(0xffffffffu, incl, 31);
+        if (lane == 0) a.offsets[E] = carry;
     }
-    if (lane == 0) a.offsets[E] = carry;
 }
 
-__global__ void dispatch_finish_kernel(const DispatchArgs a)
+__global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(const SerialArgs sa)
 {
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= a.T) return;
+    extern __shared__ __align__(16) uint8_t dsm[];
+    dispatch_serial_block<true>(sa, dsm);
+}
+
+// Token t's entries before the replay, its permutation entries and its
+// combine weights.
+__device__ __forceinline__ void dispatch_finish_token(const DispatchArgs& a, const int t)
+{
     const int E = a.E, k = a.k;
     const int q1 = a.ctrl[CTRL_Q1];
     const int c = t / kChunk;
@@ -380,6 +403,46 @@ __global__ void dispatch_finish_kernel(const DispatchArgs a)
         a.cw[static_cast<size_t>(t) * k + r] = (tot > 0.0f) ? num[r] / tot : 0.0f;
 }
 
+__global__ void dispatch_finish_kernel(const DispatchArgs a)
+{
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < a.T) dispatch_finish_token(a, t);
+}
+
+// A batch of one chunk (T <= kChunk) in one block: route, replay and finish
+// with block barriers between them instead of three launches.
+static_assert(detail::kRouteThreads == kSerialThreads, "one block runs both phases");
+static_assert(kChunk <= kSerialThreads, "one token per thread in the finish phase");
+
+template <int EPL>
+__global__ void __launch_bounds__(kSerialThreads, 1)
+    route_dispatch_small_kernel(const RouteArgs ra, const SerialArgs sa)
+{
+    extern __shared__ __align__(16) uint8_t dsm[];
+    detail::route_block<EPL>(ra, 0);
+    __syncthreads();
+    dispatch_serial_block<false>(sa, dsm);
+    __syncthreads();
+    if (static_cast<int>(threadIdx.x) < sa.a.T) dispatch_finish_token(sa.a, threadIdx.x);
+}
+
+constexpr size_t kSmallSmemCap = 96 * 1024;   // >= 2*255*32*4 + kChunk*(kPrefLen + 8)
+
+template <int EPL>
+cudaError_t launch_small(const RouteArgs& ra, const SerialArgs& sa, size_t smem, cudaStream_t s)
+{
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(route_dispatch_small_kernel<EPL>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmallSmemCap));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    route_dispatch_small_kernel<EPL><<<1, kSerialThreads, smem, s>>>(ra, sa);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s)
@@ -409,6 +472,23 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s)
     if (e != cudaSuccess) return e;
     dispatch_finish_kernel<<<(a.T + 255) / 256, 256, 0, s>>>(a);
     return cudaGetLastError();
+}
+
+cudaError_t launch_route_dispatch_small(const RouteArgs& ra, const DispatchArgs& a, cudaStream_t s)
+{
+    if (a.T <= 0) return cudaSuccess;
+    if (a.T > kChunk || ra.nchunks != 1 || a.nchunks != 1) return cudaErrorInvalidValue;
+    SerialArgs sa;
+    sa.a = a;
+    sa.use_smem = 1;
+    sa.asg_global = nullptr;
+    const size_t smem = 2 * static_cast<size_t>(a.E) * kSerialWarps * 4 +
+                        static_cast<size_t>(a.T) * (kPrefLen + a.k);
+    if (smem > kSmallSmemCap) return cudaErrorInvalidValue;
+    if (a.E <= 32) return launch_small<1>(ra, sa, smem, s);
+    if (a.E <= 64) return launch_small<2>(ra, sa, smem, s);
+    if (a.E <= 128) return launch_small<4>(ra, sa, smem, s);
+    return launch_small<8>(ra, sa, smem, s);
 }
 
 }  // namespace moe

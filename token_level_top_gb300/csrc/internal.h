@@ -100,6 +100,9 @@ struct DispatchArgs {
     int* status;
 };
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
+// Route and dispatch of a batch of one chunk (T <= kChunk, nchunks == 1) in a
+// single block: same results as launch_route followed by launch_dispatch.
+cudaError_t launch_route_dispatch_small(const RouteArgs& ra, const DispatchArgs& a, cudaStream_t s);
 
 struct GemmLaunch {
     int kind;
@@ -123,8 +126,11 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
 cudaError_t launch_pack_w13(int E, int F, int d, const void* w1, const void* w3, void* w13,
                             cudaStream_t s);
 cudaError_t launch_finalize(int T, int d, const float* acc, void* out, cudaStream_t s);
+// x_perm[j] = h[perm[j] / k] for the offsets[E] kept rows; when acc_zero is
+// not NULL the same grid also zeroes acc_zero[T][d] (fp32).
 cudaError_t launch_gather_rows(int T, int d, int k, int E, const void* h, const int32_t* perm,
-                               const int32_t* offsets, void* x_perm, cudaStream_t s);
+                               const int32_t* offsets, void* x_perm, float* acc_zero,
+                               cudaStream_t s);
 cudaError_t launch_combine(int T, int d, int k, const void* y_slots, const int32_t* assign,
                            const int32_t* slot, const int32_t* offsets, const float* cw, void* out,
                            cudaStream_t s);

@@ -74,12 +74,16 @@ __global__ void combine_kernel(int T, int d, int k, const uint4* __restrict__ y,
 // tile loads.  16 bytes per thread, rows of d bf16.
 __global__ void gather_rows_kernel(int rows_max, int d8, int k, int E, const uint4* __restrict__ h,
                                    const int32_t* __restrict__ perm,
-                                   const int32_t* __restrict__ offsets, uint4* __restrict__ x)
+                                   const int32_t* __restrict__ offsets, uint4* __restrict__ x,
+                                   float4* __restrict__ zero, size_t zero4)
 {
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    const size_t i0 = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+    // the fp32 output accumulator the down projection scatters into starts at zero
+    for (size_t i = i0; i < zero4; i += stride) zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     const int n = offsets[E];
     const size_t total = static_cast<size_t>(min(n, rows_max)) * d8;
-    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    for (size_t i = i0; i < total; i += stride) {
         const size_t row = i / d8, c = i - row * d8;
         const int t = perm[row] / k;
         x[i] = h[static_cast<size_t>(t) * d8 + c];
@@ -128,14 +132,16 @@ cudaError_t launch_finalize(int T, int d, const float* acc, void* out, cudaStrea
 }
 
 cudaError_t launch_gather_rows(int T, int d, int k, int E, const void* h, const int32_t* perm,
-                               const int32_t* offsets, void* x_perm, cudaStream_t s)
+                               const int32_t* offsets, void* x_perm, float* acc_zero,
+                               cudaStream_t s)
 {
     const int rows_max = T * k;
     const size_t total = static_cast<size_t>(rows_max) * (d / 8);
+    const size_t zero4 = acc_zero ? static_cast<size_t>(T) * d / 4 : 0;
     if (total == 0) return cudaSuccess;
-    gather_rows_kernel<<<grid_for(total, 256), 256, 0, s>>>(rows_max, d / 8, k, E,
-                                                             static_cast<const uint4*>(h), perm,
-                                                             offsets, static_cast<uint4*>(x_perm));
+    gather_rows_kernel<<<grid_for(total, 256), 256, 0, s>>>(
+        rows_max, d / 8, k, E, static_cast<const uint4*>(h), perm, offsets,
+        static_cast<uint4*>(x_perm), reinterpret_cast<float4*>(acc_zero), zero4);
     return cudaGetLastError();
 }
 

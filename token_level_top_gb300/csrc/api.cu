@@ -113,7 +113,7 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
     w.prefs = take(T * static_cast<size_t>(pref_stride(c.E)));
     w.crank = take(T * k * 4);
     w.hist = take(k * nch * E * 4);
-    w.base = take(k * nch * E * 4 + T * k);
+    w.base = take(dispatch_base_bytes(T, k, nch, E));
     w.ppart = take(nch * E * 4);
     w.assign = take(T * k * 4);
     w.slot = take(T * k * 4);

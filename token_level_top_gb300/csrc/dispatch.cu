@@ -14,12 +14,14 @@
 // chunks) + (stable rank inside its chunk) -- both written by the route
 // kernel.  Stage 1 (one CTA) scans the chunk histograms per expert, finds the
 // first chunk q1 in which some expert's running count passes C, and leaves
-// the per-chunk bases.  From chunk q1 on, the CTA replays the entries in
-// windows of 256 consecutive entries of one rank, one per thread: each entry
-// picks its expert under the current full set, __match_any_sync and a prefix
-// over the warps give it its slot, a block minimum finds the first entry that
-// takes an expert's last slot, everything up to it commits, and entries after
-// it that chose the now-full expert choose again.  Stage 2 (grid-wide) writes the entries
+// the per-chunk bases.  From chunk q1 on, one warp of the CTA replays the
+// entries in windows of 32 consecutive entries of one rank, one per lane:
+// each entry picks its expert under the current full set, __match_any_sync
+// gives it its rank among the window's entries of that expert (slot = fill +
+// rank), a ballot finds the first entry that takes an expert's last slot,
+// everything up to it commits, and entries after it that chose the now-full
+// expert choose again.  A single warp needs no block barriers, which on this
+// sequential chain cost more than the wider windows save.  Stage 2 (grid-wide) writes the entries
 // before q1, the permutation in slot order and the combine weights
 // ([mhpn] §4.3: router probabilities renormalised over the experts used).
 #include <math.h>
@@ -31,13 +33,23 @@
 namespace moe {
 namespace {
 
-constexpr int kSerialThreads = 1024;  // one replay window = one entry per thread
-constexpr int kSerialWarps = kSerialThreads / 32;
-constexpr size_t kSerialSmemCap = 224 * 1024;  // dynamic shared memory of the replay CTA
+constexpr int kSerialThreads = 1024;   // stage 1 and the staging
+constexpr int kReplayThreads = 256;    // the replay: one window entry per thread
+constexpr int kReplayWarps = kReplayThreads / 32;
+static_assert(kSerialThreads >= 255, "stage 1 needs a thread per expert");
+static_assert(kReplayThreads <= kSerialThreads && kReplayThreads % 32 == 0, "replay warps");
+// dynamic shared memory of the standalone replay block (+ about 14 KB static)
+constexpr size_t kSerialSmemCap = 208 * 1024;
+
+// Barrier among the replay's threads only (named barrier 1).
+__device__ __forceinline__ void replay_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kReplayThreads) : "memory");
+}
 
 struct SerialArgs {
     DispatchArgs a;
-    int use_smem;
+    int stage_cap;        // bytes of dynamic shared memory for the staged tail
     uint8_t* asg_global;  // [T*k] fallback when the staging does not fit in smem
 };
 
@@ -53,141 +65,194 @@ __device__ __forceinline__ V ld_in(const V* p)
         return *p;
 }
 
-// Experts already serving a token (its earlier ranks), packed one per byte
-// into two words; unused bytes hold 0xFF, which is never an expert id.
+// Experts already serving a token (its earlier ranks), one per byte in two
+// words; unused bytes hold 0xFF.
 struct Held {
     uint32_t lo = 0xFFFFFFFFu, hi = 0xFFFFFFFFu;
-    __device__ __forceinline__ void set(int q, int e)
+    int n = 0;
+    __device__ __forceinline__ void add(int e)
     {
-        const uint32_t sh = 8 * (q & 3), m = ~(0xFFu << sh), v = static_cast<uint32_t>(e & 0xFF) << sh;
-        if (q < 4)
+        const uint32_t sh = 8 * (n & 3), m = ~(0xFFu << sh), v = static_cast<uint32_t>(e & 0xFF) << sh;
+        if (n < 4)
             lo = (lo & m) | v;
         else
             hi = (hi & m) | v;
+        ++n;
     }
-    __device__ __forceinline__ bool has(int e) const
-    {
-        const uint32_t b = 0x01010101u * static_cast<uint32_t>(e);
-        const uint32_t x = lo ^ b, y = hi ^ b;   // a zero byte marks a match
-        return (((x - 0x01010101u) & ~x) | ((y - 0x01010101u) & ~y)) & 0x80808080u;
-    }
+    __device__ __forceinline__ uint32_t get(int q) const { return ((q < 4 ? lo : hi) >> (8 * (q & 3))) & 0xFF; }
 };
 
-// First expert of the preference order that is neither full nor held.  The
-// first kPrefLen entries come from the token's staged prefix (16 bytes in
-// registers); past it the stored order is read 16 entries at a time.
+// Bit j of the result = bit 7 of byte j of x (the four products land on bits
+// 28..31 without overlapping any other partial product).
+__device__ __forceinline__ uint32_t byte_msbs(uint32_t x)
+{
+    return ((x & 0x80808080u) * 0x00204081u) >> 28;
+}
+
+// First of 16 order positions (the low n valid) whose expert is neither full
+// (s_isfull[e] != 0) nor held, or -1.  Every position is looked at without an
+// early exit, so the 16 byte loads overlap; the held test compares 4
+// positions at a time.
+__device__ __forceinline__ int first_open16(const uint4 v, int n, const Held& held,
+                                            const uint8_t* s_isfull)
+{
+    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+    uint32_t closed = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        closed |= static_cast<uint32_t>(s_isfull[(wd[i >> 2] >> (8 * (i & 3))) & 0xFF]) << i;
+    for (int q = 0; q < held.n; ++q) {
+        const uint32_t rep = held.get(q) * 0x01010101u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) closed |= byte_msbs(__vcmpeq4(wd[j], rep)) << (4 * j);
+    }
+    const uint32_t ok = ~closed & (n >= 16 ? 0xFFFFu : (1u << n) - 1u);
+    if (!ok) return -1;
+    const int i = __ffs(ok) - 1;
+    const uint32_t w = i < 4 ? v.x : i < 8 ? v.y : i < 12 ? v.z : v.w;
+    return (w >> (8 * (i & 3))) & 0xFF;
+}
+
+// First expert of the token's preference order that is neither full nor
+// held.  prow holds the first nw 16-position words of the order (staged in
+// shared memory, or the stored row itself); the rest is read from the stored
+// order in global memory.
 template <bool NC>
-__device__ __forceinline__ int choose_expert(const DispatchArgs& a, int cap, int t, const uint4 pw,
-                                             const Held& held, const int* s_fill)
+__device__ __forceinline__ int choose_expert(const DispatchArgs& a, int t, const uint4* prow, int nw,
+                                             const Held& held, const uint8_t* s_isfull)
 {
     const int E = a.E;
-    const int L = E < kPrefLen ? E : kPrefLen;
-    const uint32_t words[4] = {pw.x, pw.y, pw.z, pw.w};
-#pragma unroll
-    for (int i = 0; i < kPrefLen; ++i) {
-        if (i >= L) break;
-        const int e = (words[i >> 2] >> (8 * (i & 3))) & 0xFF;
-        if (s_fill[e] < cap && !held.has(e)) return e;
+    for (int w = 0; w < nw; ++w) {
+        const int p0 = 16 * w;
+        if (p0 >= E) return -1;
+        const int e = first_open16(prow[w], min(16, E - p0), held, s_isfull);
+        if (e >= 0) return e;
     }
-    if (L == E) return -1;
-    const uint8_t* orow = a.prefs + static_cast<size_t>(t) * pref_stride(E);
-    for (int p0 = kPrefLen; p0 < E; p0 += 16) {
-        const uint4 w = ld_in<NC>(reinterpret_cast<const uint4*>(orow + p0));
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            if (p0 + i >= E) return -1;
-            const int e = (ww[i >> 2] >> (8 * (i & 3))) & 0xFF;
-            if (s_fill[e] < cap && !held.has(e)) return e;
-        }
+    const uint4* orow = reinterpret_cast<const uint4*>(a.prefs + static_cast<size_t>(t) * pref_stride(E));
+    for (int p0 = 16 * nw; p0 < E; p0 += 16) {
+        const int e = first_open16(ld_in<NC>(orow + p0 / 16), min(16, E - p0), held, s_isfull);
+        if (e >= 0) return e;
     }
     return -1;
 }
 
-// The replay, by one block of kSerialThreads threads; dsm is the block's
-// dynamic shared memory (sized by the launchers below).
+// Stage 1 and the replay, by one block of kSerialThreads threads (the replay
+// itself by its first kReplayThreads); dsm is the block's dynamic shared
+// memory (sa.stage_cap bytes for the staged tail).
 template <bool NC>
 __device__ __forceinline__ void dispatch_serial_block(const SerialArgs& sa, uint8_t* dsm)
 {
     __shared__ int s_fill[256];
+    __shared__ uint8_t s_isfull[256];       // 1 for a full expert (and for ids >= E)
+    __shared__ int s_seg[kSerialThreads];   // stage 1: per (segment, expert) counts
+    __shared__ int s_tot[256];
+    __shared__ int s_cnt[kReplayWarps * 256];   // replay: per (warp, expert) window counts
     __shared__ int s_q1, s_cut, s_estar, s_nre, s_ndrop;
     const DispatchArgs& a = sa.a;
     const int E = a.E, T = a.T, k = a.k, nch = a.nchunks;
     const int Q = k * nch;
     const int cap = static_cast<int>(a.C);   // C <= T*k < 2^30
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // dynamic shared memory: per expert and warp, the window's entry counts and
-    // their exclusive prefix (+ fill); then the staged tail data
-    int (*s_cnt)[kSerialWarps] = reinterpret_cast<int (*)[kSerialWarps]>(dsm);
-    int (*s_base)[kSerialWarps] = reinterpret_cast<int (*)[kSerialWarps]>(dsm + E * kSerialWarps * 4);
-    uint8_t* stage = dsm + 2 * E * kSerialWarps * 4;
 
+    // ---- stage 1: running count per expert over the chunk rows q (rank-major
+    // order).  Thread (j, e) = tid j*E + e sums rows [j*L, (j+1)*L) of expert e;
+    // a scan over the segments gives each its start; a second pass writes the
+    // bases and finds the first row whose running count passes C.
+    const int S = min(min(32, kSerialThreads / E), Q);   // segments per expert
+    const int L = (Q + S - 1) / S;
+    const int seg = tid / E, se = tid - seg * E;
+    const bool segt = seg < S;
+    const int32_t* hist = a.hist;
     if (tid == 0) {
         s_q1 = Q;
-        s_cut = kSerialThreads;
+        s_cut = kReplayThreads;
         s_nre = 0;
         s_ndrop = 0;
     }
-    for (int i = tid; i < kSerialWarps * E; i += kSerialThreads) (&s_cnt[0][0])[i] = 0;
-    static_assert(kSerialWarps == 32, "the cross-warp scan maps one warp count to each lane");
+    for (int i = tid; i < kReplayWarps * E; i += kSerialThreads) s_cnt[i] = 0;
+    int part = 0;
+    if (segt) {
+        const int q_end = min(Q, (seg + 1) * L);
+        for (int q0 = seg * L; q0 < q_end; q0 += 8) {
+            int c[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                c[j] = (q0 + j < q_end) ? ld_in<NC>(hist + static_cast<size_t>(q0 + j) * E + se) : 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) part += c[j];
+        }
+        s_seg[seg * E + se] = part;
+    }
     __syncthreads();
-    // ---- stage 1: running count per expert over chunks (rank-major order)
-    int total = 0;
     if (tid < E) {
-        const int32_t* hist = a.hist;
+        int run = 0;
+        for (int j = 0; j < S; ++j) {
+            const int c = s_seg[j * E + tid];
+            s_seg[j * E + tid] = run;
+            run += c;
+        }
+        s_tot[tid] = run;
+    }
+    __syncthreads();
+    if (segt) {
         int32_t* __restrict__ basep = a.base;
-        int cum = 0, qe = Q;
-        for (int q0 = 0; q0 < Q; q0 += 16) {
-            int c[16];
+        int cum = s_seg[seg * E + se], qe = Q;
+        const int q_end = min(Q, (seg + 1) * L);
+        for (int q0 = seg * L; q0 < q_end; q0 += 8) {
+            int c[8];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                c[j] = (q0 + j < Q) ? ld_in<NC>(hist + static_cast<size_t>(q0 + j) * E + tid) : 0;
+            for (int j = 0; j < 8; ++j)
+                c[j] = (q0 + j < q_end) ? ld_in<NC>(hist + static_cast<size_t>(q0 + j) * E + se) : 0;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                if (q0 + j >= Q) break;
-                basep[static_cast<size_t>(q0 + j) * E + tid] = cum;
+            for (int j = 0; j < 8; ++j) {
+                if (q0 + j >= q_end) break;
+                basep[static_cast<size_t>(q0 + j) * E + se] = cum;
                 cum += c[j];
                 if (qe == Q && cum > a.C) qe = q0 + j;
             }
         }
-        total = cum;
-        atomicMin(&s_q1, qe);
+        if (qe < Q) atomicMin(&s_q1, qe);
     }
     __syncthreads();
     const int q1 = s_q1;
-    if (tid < E) s_fill[tid] = (q1 < Q) ? a.base[static_cast<size_t>(q1) * E + tid] : total;
+    if (tid < E) s_fill[tid] = (q1 < Q) ? a.base[static_cast<size_t>(q1) * E + tid] : s_tot[tid];
+    if (tid < 256) s_isfull[tid] = (tid >= E || s_fill[tid] >= cap) ? 1 : 0;   // own s_fill entry
 
-    // ---- stage the tail tokens' preference prefixes and their entries' experts
+    // ---- stage the tail tokens' preference orders (as many leading 16-byte
+    // words as fit) and their entries' experts in shared memory; when not even
+    // one word fits, the orders stay in global memory and the experts go to
+    // the global fallback
     const int r1 = q1 / nch;
     const int t1 = (q1 - r1 * nch) * kChunk;
     const int tbeg = (q1 < Q && r1 == k - 1) ? t1 : 0;   // first token with a tail entry
     const int ntail = (q1 < Q) ? T - tbeg : 0;
     const int pst16 = pref_stride(E) / 16;   // uint4 words per stored order
-    const uint4* pfx_g = reinterpret_cast<const uint4*>(a.prefs) +
-                                      static_cast<size_t>(tbeg) * pst16;
-    const uint4* pfx = pfx_g;
-    int pfx_step = pst16;                    // staged copies keep only the first 16 bytes
+    const uint4* pfx = reinterpret_cast<const uint4*>(a.prefs) + static_cast<size_t>(tbeg) * pst16;
+    int nw = pst16;                          // words of each order reachable through pfx
     uint8_t* asg = sa.asg_global;
-    if (sa.use_smem && ntail > 0) {
-        uint4* sp = reinterpret_cast<uint4*>(stage);
-        for (int i0 = tid; i0 < ntail; i0 += 4 * kSerialThreads) {
-            uint4 v[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int i = i0 + j * kSerialThreads;
-                if (i < ntail) v[j] = pfx_g[static_cast<size_t>(i) * pst16];
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int i = i0 + j * kSerialThreads;
-                if (i < ntail) sp[i] = v[j];
-            }
-        }
-        pfx = sp;
-        pfx_step = 1;
-        asg = stage + static_cast<size_t>(ntail) * kPrefLen;
-    }
     if (ntail > 0) {
+        const int room = sa.stage_cap / ntail - k;   // bytes per token for its order
+        const int fit = room >= 16 ? min(room / 16, pst16) : 0;
+        if (fit > 0) {
+            uint4* sp = reinterpret_cast<uint4*>(dsm);
+            const int nwords = ntail * fit;
+            for (int i0 = tid; i0 < nwords; i0 += 4 * kSerialThreads) {
+                uint4 v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int i = i0 + j * kSerialThreads;
+                    if (i < nwords) v[j] = pfx[static_cast<size_t>(i / fit) * pst16 + i % fit];
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int i = i0 + j * kSerialThreads;
+                    if (i < nwords) sp[i] = v[j];
+                }
+            }
+            pfx = sp;
+            nw = fit;
+            asg = dsm + static_cast<size_t>(nwords) * 16;
+        }
         // entry (t, r) is placed before the tail when its chunk r*nch + t/kChunk < q1
         const int32_t* ids = a.ids;
         for (int r = 0; r < k; ++r) {
@@ -211,56 +276,48 @@ __device__ __forceinline__ void dispatch_serial_block(const SerialArgs& sa, uint
     static_assert(kChunk == 256, "chunk index is t >> 8");
     __syncthreads();
 
-    // ---- stage 2: replay from chunk q1, kSerialThreads consecutive entries of one rank
-    // per window; see the file comment.
+    if (tid >= kReplayThreads) return;   // the replay and the totals belong to the first warps
+
+    // ---- stage 2: replay from chunk q1, kReplayThreads consecutive entries of
+    // one rank per window; see the file comment.
     int nre = 0, ndrop = 0;
     if (q1 < Q) {
         for (int r = r1; r < k; ++r) {
-            for (int w0 = (r == r1 ? t1 : 0); w0 < T; w0 += kSerialThreads) {
+            for (int w0 = (r == r1 ? t1 : 0); w0 < T; w0 += kReplayThreads) {
                 const int t = w0 + tid;
                 const bool valid = t < T;
-                uint4 pw = make_uint4(0, 0, 0, 0);
+                const size_t ti = static_cast<size_t>(valid ? t - tbeg : 0);
+                const uint4* prow = pfx + ti * nw;
                 Held held;
+                int want = -1, e = -1;
                 if (valid) {
-                    pw = pfx[static_cast<size_t>(t - tbeg) * pfx_step];
-                    for (int q = 0; q < r; ++q) held.set(q, asg[static_cast<size_t>(t - tbeg) * k + q]);
+                    for (int q = 0; q < r; ++q) held.add(asg[ti * k + q]);
+                    const uint4 w = prow[0];   // r < k <= 8: the first word holds rank r's pick
+                    want = ((r < 4 ? w.x : w.y) >> (8 * (r & 3))) & 0xFF;
+                    e = choose_expert<NC>(a, t, prow, nw, held, s_isfull);
                 }
-                const int want = (valid && r < kPrefLen)
-                                     ? (int)(((r < 4 ? pw.x : r < 8 ? pw.y : r < 12 ? pw.z : pw.w) >>
-                                              (8 * (r & 3))) & 0xFF)
-                                     : -1;
-                int e = valid ? choose_expert<NC>(a, cap, t, pw, held, s_fill) : -1;
                 bool active = valid;
                 while (true) {
                     // ranks among the window's active entries that chose the same expert
-                    const int key = active ? e : -2;
-                    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+                    const uint32_t peers = __match_any_sync(0xffffffffu, active ? e : -2);
                     const int rnk = __popc(peers & lanemask_lt());
                     const bool leader = lane == __ffs(peers) - 1;
-                    if (active && e >= 0 && leader) s_cnt[e][warp] = __popc(peers);
-                    __syncthreads();
-                    // per expert, exclusive prefix over the warps (lane w holds warp w)
-                    for (int ee = warp; ee < E; ee += kSerialWarps) {
-                        const int c = s_cnt[ee][lane];
-                        int incl = c;
-#pragma unroll
-                        for (int off = 1; off < 32; off <<= 1) {
-                            const int v = __shfl_up_sync(0xffffffffu, incl, off);
-                            if (lane >= off) incl += v;
-                        }
-                        s_base[ee][lane] = s_fill[ee] + incl - c;
-                    }
-                    __syncthreads();
+                    const bool placed = active && e >= 0;
+                    if (placed && leader) s_cnt[warp * E + e] = __popc(peers);
+                    replay_sync();
+                    // slot = fill + the earlier warps' entries of the expert + rank in the warp
                     int slot = 0;
-                    if (active && e >= 0) {
-                        slot = s_base[e][warp] + rnk;
-                        if (leader) s_cnt[e][warp] = 0;   // ready for the next round
+                    if (placed) {
+                        slot = s_fill[e] + rnk;
+#pragma unroll
+                        for (int w = 0; w < kReplayWarps - 1; ++w)
+                            if (w < warp) slot += s_cnt[w * E + e];
                     }
                     // the first entry of the window that takes an expert's last slot
-                    const bool last = active && e >= 0 && slot + 1 == cap;
-                    const uint32_t evw = __ballot_sync(0xffffffffu, last);
+                    const uint32_t evw = __ballot_sync(0xffffffffu, placed && slot + 1 == cap);
                     if (evw && lane == 0) atomicMin(&s_cut, warp * 32 + __ffs(evw) - 1);
-                    __syncthreads();
+                    replay_sync();
+                    if (placed && leader) s_cnt[warp * E + e] = 0;   // all reads are done
                     const int cut = s_cut;
                     const bool commit = active && tid <= cut;
                     if (commit) {
@@ -284,16 +341,16 @@ __device__ __forceinline__ void dispatch_serial_block(const SerialArgs& sa, uint
                     if (tid == cut) s_estar = e;
                     // new fill: each warp's leader adds its committed entries of the expert
                     const uint32_t cmask = __ballot_sync(0xffffffffu, commit);
-                    if (active && e >= 0 && leader) {
+                    if (placed && leader) {
                         const int nc = __popc(peers & cmask);
-                        if (nc) atomicAdd(&s_fill[e], nc);
+                        if (nc && atomicAdd(&s_fill[e], nc) + nc >= cap) s_isfull[e] = 1;
                     }
-                    __syncthreads();
-                    if (cut >= kSerialThreads) break;   // no expert filled in this window
+                    replay_sync();
+                    if (cut >= kReplayThreads) break;   // no expert filled in this window
                     const int estar = s_estar;
                     active = active && tid > cut;
-                    if (active && e == estar) e = choose_expert<NC>(a, cap, t, pw, held, s_fill);
-                    if (tid == 0) s_cut = kSerialThreads;   // read by all before the last barrier
+                    if (active && e == estar) e = choose_expert<NC>(a, t, prow, nw, held, s_isfull);
+                    if (tid == 0) s_cut = kReplayThreads;   // read by all before the last barrier
                 }
             }
         }
@@ -306,35 +363,34 @@ __device__ __forceinline__ void dispatch_serial_block(const SerialArgs& sa, uint
         atomicAdd(&s_nre, nre);
         atomicAdd(&s_ndrop, ndrop);
     }
-    __syncthreads();
-    if (warp == 0) {
-        nre = s_nre;
-        ndrop = s_ndrop;
-        if (lane == 0) {
-            a.ctrl[CTRL_Q1] = q1;
-            a.ctrl[CTRL_NRE] = nre;
-            a.ctrl[CTRL_NDROP] = ndrop;
-            if (a.n_rerouted) *a.n_rerouted = nre;
-            if (a.n_dropped) *a.n_dropped = ndrop;
-        }
-        // counts and exclusive offsets
-        int carry = 0;
-        for (int b = 0; b < E; b += 32) {
-            const int e = b + lane;
-            const int c = (e < E) ? s_fill[e] : 0;
-            int incl = c;
-            for (int off = 1; off < 32; off <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += v;
-            }
-            if (e < E) {
-                a.counts[e] = c;
-                a.offsets[e] = carry + incl - c;
-            }
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) a.offsets[E] = carry;
+    replay_sync();
+    if (warp != 0) return;
+    nre = s_nre;
+    ndrop = s_ndrop;
+    if (lane == 0) {
+        a.ctrl[CTRL_Q1] = q1;
+        a.ctrl[CTRL_NRE] = nre;
+        a.ctrl[CTRL_NDROP] = ndrop;
+        if (a.n_rerouted) *a.n_rerouted = nre;
+        if (a.n_dropped) *a.n_dropped = ndrop;
     }
+    // counts and exclusive offsets
+    int carry = 0;
+    for (int b = 0; b < E; b += 32) {
+        const int e = b + lane;
+        const int c = (e < E) ? s_fill[e] : 0;
+        int incl = c;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (e < E) {
+            a.counts[e] = c;
+            a.offsets[e] = carry + incl - c;
+        }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) a.offsets[E] = carry;
 }
 
 __global__ void __launch_bounds__(kSerialThreads, 1) dispatch_serial_kernel(const SerialArgs sa)
@@ -412,21 +468,21 @@ __global__ void dispatch_finish_kernel(const DispatchArgs a)
 // A batch of one chunk (T <= kChunk) in one block: route, replay and finish
 // with block barriers between them instead of three launches.
 static_assert(detail::kRouteThreads == kSerialThreads, "one block runs both phases");
-static_assert(kChunk <= kSerialThreads, "one token per thread in the finish phase");
+static_assert(kChunk <= detail::kRouteThreads, "one token per thread in the finish phase");
 
 template <int EPL>
-__global__ void __launch_bounds__(kSerialThreads, 1)
+__global__ void __launch_bounds__(detail::kRouteThreads, 1)
     route_dispatch_small_kernel(const RouteArgs ra, const SerialArgs sa)
 {
     extern __shared__ __align__(16) uint8_t dsm[];
     detail::route_block<EPL>(ra, 0);
     __syncthreads();
-    dispatch_serial_block<false>(sa, dsm);
+    dispatch_serial_block<false>(sa, dsm);   // the replay warps return last
     __syncthreads();
     if (static_cast<int>(threadIdx.x) < sa.a.T) dispatch_finish_token(sa.a, threadIdx.x);
 }
 
-constexpr size_t kSmallSmemCap = 96 * 1024;   // >= 2*255*32*4 + kChunk*(kPrefLen + 8)
+constexpr size_t kSmallSmemCap = 68 * 1024;   // >= kChunk*(pref_stride(255) + 8)
 
 template <int EPL>
 cudaError_t launch_small(const RouteArgs& ra, const SerialArgs& sa, size_t smem, cudaStream_t s)
@@ -439,8 +495,21 @@ cudaError_t launch_small(const RouteArgs& ra, const SerialArgs& sa, size_t smem,
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    route_dispatch_small_kernel<EPL><<<1, kSerialThreads, smem, s>>>(ra, sa);
+    route_dispatch_small_kernel<EPL><<<1, detail::kRouteThreads, smem, s>>>(ra, sa);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace {
+
+// Without room in shared memory the replay keeps its per-entry experts in the
+// (otherwise unused) tail of the rank-base table.
+void set_fallback(SerialArgs& sa)
+{
+    const DispatchArgs& a = sa.a;
+    uint8_t* b = reinterpret_cast<uint8_t*>(a.base);
+    sa.asg_global = b + dispatch_asg_offset(a.k, a.nchunks, a.E);
 }
 
 }  // namespace
@@ -450,15 +519,12 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s)
     if (a.T <= 0) return cudaSuccess;
     SerialArgs sa;
     sa.a = a;
-    // worst case: every token has a tail entry
-    const size_t scan_bytes = 2 * static_cast<size_t>(a.E) * kSerialWarps * 4;
-    const size_t need = static_cast<size_t>(a.T) * (kPrefLen + a.k);
-    sa.use_smem = (scan_bytes + need) <= kSerialSmemCap ? 1 : 0;
-    // without room in shared memory the replay keeps the entries' experts in
-    // the (otherwise unused) tail of the rank table
-    sa.asg_global = reinterpret_cast<uint8_t*>(a.base) +
-                    static_cast<size_t>(a.k) * a.nchunks * a.E * sizeof(int32_t);
-    const size_t smem = scan_bytes + (sa.use_smem ? need : 0);
+    // room for the largest possible tail (every token), up to the cap; the
+    // block decides from the actual tail whether it fits
+    const size_t need = static_cast<size_t>(a.T) * (pref_stride(a.E) + a.k);
+    const size_t smem = need < kSerialSmemCap ? need : kSerialSmemCap;
+    sa.stage_cap = static_cast<int>(smem);
+    set_fallback(sa);
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(dispatch_serial_kernel,
@@ -480,11 +546,10 @@ cudaError_t launch_route_dispatch_small(const RouteArgs& ra, const DispatchArgs&
     if (a.T > kChunk || ra.nchunks != 1 || a.nchunks != 1) return cudaErrorInvalidValue;
     SerialArgs sa;
     sa.a = a;
-    sa.use_smem = 1;
-    sa.asg_global = nullptr;
-    const size_t smem = 2 * static_cast<size_t>(a.E) * kSerialWarps * 4 +
-                        static_cast<size_t>(a.T) * (kPrefLen + a.k);
+    const size_t smem = static_cast<size_t>(a.T) * (pref_stride(a.E) + a.k);
     if (smem > kSmallSmemCap) return cudaErrorInvalidValue;
+    sa.stage_cap = static_cast<int>(smem);
+    set_fallback(sa);
     if (a.E <= 32) return launch_small<1>(ra, sa, smem, s);
     if (a.E <= 64) return launch_small<2>(ra, sa, smem, s);
     if (a.E <= 128) return launch_small<4>(ra, sa, smem, s);

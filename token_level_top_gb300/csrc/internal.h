@@ -36,6 +36,15 @@ enum CtrlWord : int { CTRL_Q1 = 0, CTRL_NRE = 1, CTRL_NDROP = 2, CTRL_WORDS = 64
 // Bytes per token of the stored preference order: all E experts, padded to 16.
 __host__ __device__ inline int pref_stride(int E) { return E <= kPrefLen ? kPrefLen : (E + 15) / 16 * 16; }
 
+// The dispatch's rank-base table [k*nchunks][E] int32, followed by the
+// replay's fallback storage for each tail entry's expert (T*k bytes, at
+// dispatch_asg_offset) when its staging does not fit in shared memory.
+inline size_t dispatch_asg_offset(size_t k, size_t nch, size_t E) { return k * nch * E * 4; }
+inline size_t dispatch_base_bytes(size_t T, size_t k, size_t nch, size_t E)
+{
+    return dispatch_asg_offset(k, nch, E) + T * k;
+}
+
 bool layout_for(const moe_config_t& c, WsLayout* L);
 int router_splits(int T, int d);
 int num_sms();

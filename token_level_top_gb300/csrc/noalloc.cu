@@ -59,7 +59,7 @@ StaticLayout static_layout(const moe_config_t& c)
     L.prefs = take(T * static_cast<size_t>(pref_stride(c.E)));
     L.crank = take(T * k * 4);
     L.hist = take(k * nch * E * 4);
-    L.base = take(k * nch * E * 4 + T * k);  // + the replay's per-entry expert bytes
+    L.base = take(dispatch_base_bytes(T, k, nch, E));  // + the replay's fallback storage
     L.ppart = take(nch * E * 4);
     L.total = off;
     return L;

@@ -35,6 +35,11 @@
 namespace moe {
 namespace {
 
+// Down-scatter epilogue staging: one row of 32 fp32 per epilogue thread,
+// padded to 144 bytes so the 16-byte stores of 8 consecutive threads fall in
+// distinct banks.
+constexpr int kStageRowBytes = 144;
+
 struct GemmParams {
     int kind, E, T, topk, d, F;
     int kb_total;      // K / 64
@@ -44,6 +49,7 @@ struct GemmParams {
     int splits;        // router K splits
     int kb_per_split;  // router K blocks per split
     int stages;
+    int stage_bytes;   // down scatter: staging rows of the bulk-reduce epilogue (0: atomics)
     int gather4;       // gate-up: A rows gathered from h with tile::gather4 (else tiled from x_perm)
     uint32_t tmem_cols;
     const int32_t* offsets;
@@ -118,7 +124,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t b_bytes = static_cast<uint32_t>(PAIR ? p.bn / 2 : p.bn) * kBK * 2;
     uint8_t* sA = smem;
     uint8_t* sB = sA + stages * a_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + stages * b_bytes);
+    uint8_t* sStage = sB + stages * b_bytes;   // p.stage_bytes, 1024-aligned
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + p.stage_bytes);
     uint64_t* full_bar = bars;
     uint64_t* empty_bar = bars + stages;
     uint64_t* tfull_bar = bars + 2 * stages;
@@ -379,14 +386,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int slot = off + ri;
                 const int col0 = ti.n * p.bn;
                 if (p.kind == GK_DOWN_SCATTER) {
+                    // out_acc[token] += cw * row.  At most k <= 2 addends reach an
+                    // element, so the result does not depend on their order.
                     const int idx = valid ? p.perm[slot] : 0;
                     const float w = valid ? p.cw[idx] : 0.0f;
                     float* dst = p.out_acc + static_cast<size_t>(idx / p.topk) * p.d + col0;
+                    uint8_t* stg = sStage + static_cast<size_t>(row) * kStageRowBytes;
                     for (int c = 0; c < p.bn; c += 32) {
                         if (col0 + c >= p.d) break;  // uniform across the warp
                         tmem_ld32(taddr + c, v);
                         tmem_ld_wait(v);
-                        if (valid) {
+                        if (!valid) continue;
+                        if (p.stage_bytes) {
+                            // through this thread's staging row to one 128-byte bulk
+                            // reduce-add: one contiguous line per piece instead of
+                            // 32 lanes' scattered atomics
+                            bulk_wait_read_all();   // the previous piece has left the row
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                *reinterpret_cast<float4*>(stg + 16 * j) =
+                                    make_float4(w * __uint_as_float(v[4 * j]), w * __uint_as_float(v[4 * j + 1]),
+                                                w * __uint_as_float(v[4 * j + 2]),
+                                                w * __uint_as_float(v[4 * j + 3]));
+                            fence_proxy_async_shared();
+                            bulk_reduce_add_f32(dst + c, smem_u32(stg), 128);
+                            bulk_commit();
+                        } else {
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
                                 float4 add = make_float4(w * __uint_as_float(v[4 * j]),
@@ -425,6 +450,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     mbar_arrive(smem_u32(&tempty_bar[b]));
             }
         }
+        bulk_wait_all();   // this thread's bulk reduces are complete
     }
 
     tc_fence_before();
@@ -544,7 +570,14 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     }
     const uint32_t a_bytes = kBM * kBK * 2;
     const uint32_t b_bytes = static_cast<uint32_t>(pair ? p.bn / 2 : p.bn) * kBK * 2;
-    const size_t fixed = 1024 + 64 + static_cast<size_t>(2 * (g.E + 1)) * 4 + 16 + 6 * 8;
+    // The bulk-reduce epilogue pays off when it hides behind the next tile's
+    // main loop: at two or more tiles per SM on average.  With about one tile
+    // per SM (decode-sized batches) its fence and completion latencies are
+    // exposed and vector atomics finish sooner.
+    const bool bulk = g.kind == GK_DOWN_SCATTER &&
+                      static_cast<long long>(g.T) * g.topk / kBM * p.n_tiles >= 2LL * sms;
+    p.stage_bytes = bulk ? 4 * 32 * kStageRowBytes : 0;
+    const size_t fixed = 1024 + 64 + static_cast<size_t>(2 * (g.E + 1)) * 4 + 16 + 6 * 8 + p.stage_bytes;
     const size_t budget_smem = 227 * 1024;
     int stages = static_cast<int>((budget_smem - fixed) / (a_bytes + b_bytes + 16));
     stages = std::max(2, std::min(stages, g.kind == GK_ROUTER ? 4 : 8));   // router: 2 CTAs per SM

@@ -78,12 +78,14 @@ int num_sms()
     return cache[dev];
 }
 
-int router_splits(int T, int d)
+int router_splits(int T, int d, int E)
 {
     const int mt = (T + kBM - 1) / kBM;
     const int kb = d / kBK;
-    int S = (320 + mt - 1) / std::max(mt, 1);
-    S = std::max(1, std::min(S, std::max(1, kb / 4)));   // at least 4 K steps per split
+    // as many splits as fill one resident wave of router CTAs (a second,
+    // partial wave would double the makespan), at least 4 K steps each
+    int S = router_ctas_per_sm(E) * num_sms() / std::max(mt, 1);
+    S = std::max(1, std::min(S, std::max(1, kb / 4)));
     // no empty split: (S - 1) * ceil(kb / S) < kb
     while (S > 1 && (S - 1) * ((kb + S - 1) / S) >= kb) --S;
     return S;
@@ -96,7 +98,7 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
     const size_t d = static_cast<size_t>(c.d_model), F = static_cast<size_t>(std::max(c.d_ff, 0));
     WsLayout w;
     w.nchunks = static_cast<int>((T + kChunk - 1) / kChunk);
-    w.splits = router_splits(static_cast<int>(T), static_cast<int>(d));
+    w.splits = router_splits(static_cast<int>(T), static_cast<int>(d), c.E);
     w.epad = static_cast<int>(std::max<size_t>(32, round_up(E, 32)));
     size_t off = 0;
     auto take = [&](size_t bytes) {

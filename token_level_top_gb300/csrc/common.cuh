@@ -99,7 +99,7 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 
-// All threads of both CTAs of the cluster: arrive and wait.
+// All threads of all CTAs of the cluster: arrive and wait.
 __device__ __forceinline__ void cluster_sync_all()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
@@ -256,6 +256,21 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t ran
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
     return r;
+}
+
+// Loads from another CTA's shared memory (a shared::cluster address).
+__device__ __forceinline__ int ld_cluster_s32(uint32_t caddr)
+{
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(caddr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t caddr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar)

@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(detail::kRouteThreads, 1)
     route_dispatch_small_kernel(const RouteArgs ra, const SerialArgs sa)
 {
     extern __shared__ __align__(16) uint8_t dsm[];
-    detail::route_block<EPL>(ra, 0);
+    detail::route_block<EPL>(ra, 0, 1, 0);
     __syncthreads();
     dispatch_serial_block<false>(sa, dsm);   // the replay warps return last
     __syncthreads();

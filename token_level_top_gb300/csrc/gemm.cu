@@ -505,6 +505,24 @@ uint32_t pow2_cols(int n)
 
 }  // namespace
 
+namespace {
+
+constexpr int kRouterStages = 4;
+
+size_t gemm_fixed_smem(int E, int stage_bytes)
+{
+    return 1024 + 64 + static_cast<size_t>(2 * (E + 1)) * 4 + 16 + 6 * 8 + stage_bytes;
+}
+
+}  // namespace
+
+int router_ctas_per_sm(int E)
+{
+    const size_t epad = static_cast<size_t>(std::max(32, (E + 31) / 32 * 32));
+    const size_t smem = gemm_fixed_smem(E, 0) + kRouterStages * (kBM * kBK * 2 + epad * kBK * 2 + 16);
+    return smem <= 113 * 1024 ? 2 : 1;
+}
+
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
 {
     GemmParams p{};
@@ -539,7 +557,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
         p.n_tiles = 1;
         if (!make_map(&tmA, g.a_ptr, g.T, g.d, kBM)) return cudaErrorInvalidValue;
         if (!make_map(&tmB, g.b_ptr, g.E, g.d, p.bn)) return cudaErrorInvalidValue;
-        grid = std::min(p.m_tiles * p.splits, 2 * sms);
+        grid = std::min(p.m_tiles * p.splits, router_ctas_per_sm(g.E) * sms);
     } else if (g.kind == GK_GATEUP) {
         p.bn = kExpertBN;
         p.kb_total = g.d / kBK;
@@ -577,10 +595,10 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     const bool bulk = g.kind == GK_DOWN_SCATTER &&
                       static_cast<long long>(g.T) * g.topk / kBM * p.n_tiles >= 2LL * sms;
     p.stage_bytes = bulk ? 4 * 32 * kStageRowBytes : 0;
-    const size_t fixed = 1024 + 64 + static_cast<size_t>(2 * (g.E + 1)) * 4 + 16 + 6 * 8 + p.stage_bytes;
+    const size_t fixed = gemm_fixed_smem(g.E, p.stage_bytes);
     const size_t budget_smem = 227 * 1024;
     int stages = static_cast<int>((budget_smem - fixed) / (a_bytes + b_bytes + 16));
-    stages = std::max(2, std::min(stages, g.kind == GK_ROUTER ? 4 : 8));   // router: 2 CTAs per SM
+    stages = std::max(2, std::min(stages, g.kind == GK_ROUTER ? kRouterStages : 8));
     p.stages = stages;
     p.tmem_cols = pow2_cols(2 * p.bn);
     const size_t smem = fixed + static_cast<size_t>(stages) * (a_bytes + b_bytes + 16);

@@ -46,7 +46,8 @@ inline size_t dispatch_base_bytes(size_t T, size_t k, size_t nch, size_t E)
 }
 
 bool layout_for(const moe_config_t& c, WsLayout* L);
-int router_splits(int T, int d);
+int router_splits(int T, int d, int E);
+int router_ctas_per_sm(int E);   // router GEMM CTAs resident per SM (shared memory bound)
 int num_sms();
 
 template <class T>

@@ -6,7 +6,8 @@
 //   p = softmax(s); top-k = the k best s, ties to the lower index   [coreui] §3.1
 //   f_i = picks of i / T, P_i = mean p_i             [cnnetsun] §4.2; [coreui] §3.1
 //
-// Each block handles a chunk of kChunk consecutive tokens.  A token is owned
+// Each chunk of kChunk consecutive tokens is routed by a cluster of 1-8
+// blocks (as many as keep the grid within the SMs).  A token is owned
 // by G = min(32, pow2(E)) lanes, each lane holding EPL experts (e = lane + G*j);
 // each lane ranks its experts against all E scores (shuffled through the
 // group), which gives the whole preference order, stored as expert bytes per
@@ -26,10 +27,28 @@
 namespace moe {
 namespace {
 
+// Clusters of `cs` blocks, one cluster per chunk.
 template <int EPL>
-__global__ void __launch_bounds__(detail::kRouteThreads) route_kernel(const RouteArgs a)
+__global__ void __launch_bounds__(detail::kRouteThreads) route_kernel(const RouteArgs a, const int cs)
 {
-    detail::route_block<EPL>(a, blockIdx.x);
+    detail::route_block<EPL>(a, blockIdx.x / cs, cs, static_cast<int>(cluster_ctarank()));
+}
+
+template <int EPL>
+cudaError_t launch_route_cs(const RouteArgs& a, int cs, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.nchunks * cs));
+    cfg.blockDim = dim3(detail::kRouteThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, route_kernel<EPL>, a, cs);
 }
 
 __global__ void route_stats_kernel(const StatsArgs a)
@@ -53,15 +72,20 @@ static_assert(detail::kRouteThreads >= kChunk && kChunk % 32 == 0, "one token pe
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s)
 {
     if (a.T <= 0) return cudaSuccess;
-    const int grid = a.nchunks;
+    // one SM per block: split each chunk over as many blocks (a power of two,
+    // at most 8, the portable cluster size) as keep the grid within the SMs
+    int cs = 1;
+    while (cs < 8 && a.nchunks * cs * 2 <= num_sms()) cs *= 2;
+    cudaError_t e;
     if (a.E <= 32)
-        route_kernel<1><<<grid, detail::kRouteThreads, 0, s>>>(a);
+        e = launch_route_cs<1>(a, cs, s);
     else if (a.E <= 64)
-        route_kernel<2><<<grid, detail::kRouteThreads, 0, s>>>(a);
+        e = launch_route_cs<2>(a, cs, s);
     else if (a.E <= 128)
-        route_kernel<4><<<grid, detail::kRouteThreads, 0, s>>>(a);
+        e = launch_route_cs<4>(a, cs, s);
     else
-        route_kernel<8><<<grid, detail::kRouteThreads, 0, s>>>(a);
+        e = launch_route_cs<8>(a, cs, s);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

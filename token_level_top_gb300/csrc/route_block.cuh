@@ -1,6 +1,8 @@
 // route_block.cuh -- the routing of one 256-token chunk by one 1024-thread
-// block, shared by the route kernel and the fused small-batch kernel.
-// (Semantics and citations: see route.cu.)
+// block, or by a cluster of cs such blocks (each routes kChunk/cs of the
+// chunk's tokens; their per-expert pick counts and probability sums meet
+// through distributed shared memory).  Shared by the route kernel and the
+// fused small-batch kernel.  (Semantics and citations: see route.cu.)
 #pragma once
 
 #include <math.h>
@@ -22,13 +24,18 @@ __device__ __forceinline__ float softmax_num(float s, float m)
     return expf(s - m);
 }
 
-// One 256-token chunk of the routing, by a block of kRouteThreads threads.
+// Tokens [cr*kChunk/cs, (cr+1)*kChunk/cs) of chunk `chunk`, by a block of
+// kRouteThreads threads that is CTA cr of a cluster of cs (1, 2, 4 or 8)
+// routing the same chunk.  With cs > 1 every CTA of the cluster must call it.
 template <int EPL>
-__device__ __forceinline__ void route_block(const RouteArgs& a, const int chunk)
+__device__ __forceinline__ void route_block(const RouteArgs& a, const int chunk, const int cs,
+                                            const int cr)
 {
     __shared__ int16_t s_ids[kChunk * 8];
     __shared__ int s_wcnt[kRankWarps][32 * EPL];
     __shared__ float s_wsum[kRouteWarps][32 * EPL];
+    __shared__ int s_ctot[8][32 * EPL];   // per rank: this CTA's picks of each expert
+    __shared__ float s_psum[32 * EPL];    // this CTA's probability sum of each expert
     __shared__ int s_nan;
 
     const int E = a.E, k = a.k, T = a.T;
@@ -39,6 +46,8 @@ __device__ __forceinline__ void route_block(const RouteArgs& a, const int chunk)
     const int grp = lane / G;
     const int tpw = 32 / G;
     const int t_begin = chunk * kChunk;
+    const int sub = kChunk / cs;          // tokens of this CTA
+    const int tl0 = cr * sub;
     if (threadIdx.x == 0) s_nan = 0;
 
     float acc[EPL];
@@ -46,10 +55,11 @@ __device__ __forceinline__ void route_block(const RouteArgs& a, const int chunk)
     for (int j = 0; j < EPL; ++j) acc[j] = 0.0f;
     bool saw_nan = false;
 
-    for (int base = warp * tpw; base < kChunk; base += kRouteWarps * tpw) {
-        const int tl = base + grp;
+    for (int base = warp * tpw; base < sub; base += kRouteWarps * tpw) {
+        const bool mine = base + grp < sub;   // a token slot of this CTA
+        const int tl = tl0 + base + grp;
         const int t = t_begin + tl;
-        const bool valid = t < T;
+        const bool valid = mine && t < T;
         float s[EPL];
 #pragma unroll
         for (int j = 0; j < EPL; ++j) {
@@ -201,7 +211,7 @@ __device__ __forceinline__ void route_block(const RouteArgs& a, const int chunk)
                     }
                 }
             }
-        } else if (lg == 0) {
+        } else if (mine && lg == 0) {
             for (int r = 0; r < k; ++r) s_ids[tl * k + r] = -1;
         }
     }
@@ -224,17 +234,25 @@ __device__ __forceinline__ void route_block(const RouteArgs& a, const int chunk)
     for (int e = threadIdx.x; e < E; e += kRouteThreads) {
         float tot = 0.0f;
         for (int w = 0; w < kRouteWarps; ++w) tot += s_wsum[w][e];
-        a.ppart[static_cast<size_t>(chunk) * E + e] = tot;
+        if (cs == 1)
+            a.ppart[static_cast<size_t>(chunk) * E + e] = tot;
+        else
+            s_psum[e] = tot;
     }
     if (threadIdx.x == 0 && s_nan) record_error(a.status, MOE_ERR_NONFINITE);
 
-    // ---- per rank: histogram of picks and stable rank within the chunk
-    // (the first kChunk threads, one token each; the other warps only join
-    // the barriers)
-    const bool ranker = threadIdx.x < kChunk;
-    const int tl = threadIdx.x;
+    // ---- per rank: histogram of picks and stable rank within the chunk (the
+    // first `sub` threads, one token each; the other warps only join the
+    // barriers).  Within the CTA: in-warp rank + the earlier warps' counts;
+    // across the cluster: + the picks of the chunk's earlier CTAs.
+    const bool ranker = threadIdx.x < sub;
+    const int tl = tl0 + threadIdx.x;
     const int t = t_begin + tl;
-    for (int r = 0; r < k; ++r) {
+    int crl[8];   // rank within this CTA's tokens, per pick rank
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        crl[r] = 0;
+        if (r >= k) continue;   // uniform: every thread skips the same barriers
         int e = -1, rnk = 0;
         if (ranker) {
             e = s_ids[tl * k + r];
@@ -250,15 +268,46 @@ __device__ __forceinline__ void route_block(const RouteArgs& a, const int chunk)
                 s_wcnt[w][ee] = run;  // exclusive prefix over warps
                 run += c;
             }
-            a.hist[(static_cast<size_t>(r) * a.nchunks + chunk) * E + ee] = run;
+            s_ctot[r][ee] = run;
         }
         __syncthreads();
-        if (ranker && e >= 0 && t < T) a.crank[static_cast<size_t>(t) * k + r] = s_wcnt[warp][e] + rnk;
+        if (ranker && e >= 0) crl[r] = s_wcnt[warp][e] + rnk;
         __syncthreads();
         for (int ee = threadIdx.x; ee < E; ee += kRouteThreads)
             for (int w = 0; w < kRankWarps; ++w) s_wcnt[w][ee] = 0;
         __syncthreads();
     }
+    if (cs > 1) cluster_sync_all();   // every CTA's totals are in place
+    if (ranker && t < T) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            if (r >= k) break;
+            const int e = s_ids[tl * k + r];
+            if (e < 0) continue;
+            int base = 0;
+            for (int c = 0; c < cr; ++c) base += ld_cluster_s32(map_to_rank(smem_u32(&s_ctot[r][e]), c));
+            a.crank[static_cast<size_t>(t) * k + r] = base + crl[r];
+        }
+    }
+    if (cr == cs - 1) {
+        // the chunk's histogram: all CTAs' picks, in CTA order
+        for (int i = threadIdx.x; i < k * E; i += kRouteThreads) {
+            const int r = i / E, ee = i - r * E;
+            int tot = 0;
+            for (int c = 0; c < cs; ++c)
+                tot += (c == cr) ? s_ctot[r][ee] : ld_cluster_s32(map_to_rank(smem_u32(&s_ctot[r][ee]), c));
+            a.hist[(static_cast<size_t>(r) * a.nchunks + chunk) * E + ee] = tot;
+        }
+    }
+    if (cs > 1 && cr == 0) {
+        // the chunk's probability sums, in CTA order
+        for (int ee = threadIdx.x; ee < E; ee += kRouteThreads) {
+            float tot = s_psum[ee];
+            for (int c = 1; c < cs; ++c) tot += ld_cluster_f32(map_to_rank(smem_u32(&s_psum[ee]), c));
+            a.ppart[static_cast<size_t>(chunk) * E + ee] = tot;
+        }
+    }
+    if (cs > 1) cluster_sync_all();   // no CTA leaves while another reads its shared memory
 }
 
 

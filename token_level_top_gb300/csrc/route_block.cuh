@@ -34,7 +34,8 @@ __device__ __forceinline__ void route_block(const RouteArgs& a, const int chunk,
     __shared__ int16_t s_ids[kChunk * 8];
     __shared__ int s_wcnt[kRankWarps][32 * EPL];
     __shared__ float s_wsum[kRouteWarps][32 * EPL];
-    __shared__ int s_ctot[8][32 * EPL];   // per rank: this CTA's picks of each expert
+    __shared__ int s_ctot[8][32 * EPL];   // per rank: this CTA's picks of each expert (cs > 1)
+    __shared__ int16_t s_crl[kChunk * 8];   // rank of each pick among this CTA's (cs > 1)
     __shared__ float s_psum[32 * EPL];    // this CTA's probability sum of each expert
     __shared__ int s_nan;
 
@@ -248,11 +249,7 @@ __device__ __forceinline__ void route_block(const RouteArgs& a, const int chunk,
     const bool ranker = threadIdx.x < sub;
     const int tl = tl0 + threadIdx.x;
     const int t = t_begin + tl;
-    int crl[8];   // rank within this CTA's tokens, per pick rank
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        crl[r] = 0;
-        if (r >= k) continue;   // uniform: every thread skips the same barriers
+    for (int r = 0; r < k; ++r) {
         int e = -1, rnk = 0;
         if (ranker) {
             e = s_ids[tl * k + r];
@@ -268,25 +265,34 @@ __device__ __forceinline__ void route_block(const RouteArgs& a, const int chunk,
                 s_wcnt[w][ee] = run;  // exclusive prefix over warps
                 run += c;
             }
-            s_ctot[r][ee] = run;
+            if (cs == 1)
+                a.hist[(static_cast<size_t>(r) * a.nchunks + chunk) * E + ee] = run;
+            else
+                s_ctot[r][ee] = run;
         }
         __syncthreads();
-        if (ranker && e >= 0) crl[r] = s_wcnt[warp][e] + rnk;
+        if (ranker && e >= 0) {
+            const int c = s_wcnt[warp][e] + rnk;   // rank among this CTA's picks
+            if (cs == 1) {
+                if (t < T) a.crank[static_cast<size_t>(t) * k + r] = c;
+            } else {
+                s_crl[threadIdx.x * 8 + r] = static_cast<int16_t>(c);
+            }
+        }
         __syncthreads();
         for (int ee = threadIdx.x; ee < E; ee += kRouteThreads)
             for (int w = 0; w < kRankWarps; ++w) s_wcnt[w][ee] = 0;
         __syncthreads();
     }
-    if (cs > 1) cluster_sync_all();   // every CTA's totals are in place
+    if (cs == 1) return;
+    cluster_sync_all();   // every CTA's totals are in place
     if (ranker && t < T) {
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            if (r >= k) break;
+        for (int r = 0; r < k; ++r) {
             const int e = s_ids[tl * k + r];
             if (e < 0) continue;
             int base = 0;
             for (int c = 0; c < cr; ++c) base += ld_cluster_s32(map_to_rank(smem_u32(&s_ctot[r][e]), c));
-            a.crank[static_cast<size_t>(t) * k + r] = base + crl[r];
+            a.crank[static_cast<size_t>(t) * k + r] = base + s_crl[threadIdx.x * 8 + r];
         }
     }
     if (cr == cs - 1) {
@@ -299,7 +305,7 @@ __device__ __forceinline__ void route_block(const RouteArgs& a, const int chunk,
             a.hist[(static_cast<size_t>(r) * a.nchunks + chunk) * E + ee] = tot;
         }
     }
-    if (cs > 1 && cr == 0) {
+    if (cr == 0) {
         // the chunk's probability sums, in CTA order
         for (int ee = threadIdx.x; ee < E; ee += kRouteThreads) {
             float tot = s_psum[ee];
@@ -307,7 +313,7 @@ __device__ __forceinline__ void route_block(const RouteArgs& a, const int chunk,
             a.ppart[static_cast<size_t>(chunk) * E + ee] = tot;
         }
     }
-    if (cs > 1) cluster_sync_all();   // no CTA leaves while another reads its shared memory
+    cluster_sync_all();   // no CTA leaves while another reads its shared memory
 }
 
 

@@ -4,7 +4,7 @@
                     [--workload NAME] [--no-cpu-baseline]
 
 A step is one full forward pass of the layer (router GEMM, routing, dispatch,
-gate-up GEMM with SwiGLU, down GEMM with the weighted combine, finalize) over
+gate-up GEMM with SwiGLU, down GEMM, weighted combine) over
 one batch of the workload's seeded synthetic tokens, through the C ABI
 (moe_layer_forward), inputs resident in HBM.  Rank 0 prints one JSON line.
 
@@ -44,8 +44,8 @@ CHUNK = 256  # tokens per routing chunk; a batch of one chunk routes and dispatc
 
 
 def kernels_per_step(T):
-    """Kernels of this library one layer step launches (the out_acc memset is a copy-engine op)."""
-    # router GEMM, row gather, gate-up, down, finalize + route and dispatch:
+    """Kernels of this library one layer step launches."""
+    # router GEMM, row gather, gate-up, down, combine + route and dispatch:
     # one fused kernel for a single chunk, else route + dispatch replay + finish
     return 5 + (1 if T <= CHUNK else 3)
 

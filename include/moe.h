@@ -170,16 +170,19 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* y_slots_dev,
                          const int32_t* offsets_dev, const float* combine_w_dev, void* out_dev,
                          void* stream);
 
-/* The fused layer: route, dispatch, experts with the token gather fused into
- * the gate-up GEMM's operand load and the weighted scatter fused into the
- * down GEMM's epilogue (fp32 accumulation, bf16 output).
+/* The whole layer in one call, no host synchronisation: router GEMM, route,
+ * dispatch, the token rows gathered into slot order, the gate-up GEMM with the
+ * SwiGLU in its epilogue, the down GEMM writing each kept entry's output row
+ * (bf16) in slot order, and the combine: out[t] = sum over t's kept ranks, in
+ * rank order, of combine weight * output row (fp32), rounded to bf16 once.
  *   h_dev [T, d] bf16; w_router_dev [E, d]; bias_dev, usage_dev as in
  *   moe_route; w13_dev [E, 2F, d]; w2_dev [E, d, F]; out_dev [T, d] bf16.
  * Optional outputs (NULL to skip): logits_out [T,E], assign/slot [T,k] int32,
  *   flags [T,k] u8, counts [E] int32, f/P [E] fp32.
  * stage_events: NULL, or MOE_NUM_STAGES+1 cudaEvent_t recorded on `stream`
- *   at the boundaries route | dispatch | prep (zero the fp32 accumulator,
- *   gather the token rows in slot order) | gate-up | down | finalize. */
+ *   at the boundaries route | dispatch | prep (gather the token rows in slot
+ *   order) | gate-up | down | combine.  For T <= 256 route and dispatch run
+ *   as one kernel: the route stage then holds the router GEMM only. */
 moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* h_dev,
                                const void* w_router_dev, const float* bias_dev,
                                const float* usage_dev, const void* w13_dev, const void* w2_dev,

@@ -126,8 +126,7 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
     w.cw = take(T * k * 4);
     w.xg = take(T * k * d * 2);
     w.act = take(T * k * F * 2);
-    w.out_acc = take(T * d * 4);
-    w.y_slots = (k > 2) ? take(T * k * d * 2) : 0;
+    w.y_slots = take(T * k * d * 2);
     w.h_stage = take(T * d * 2);
     w.out_stage = take(T * d * 2);
     w.total = off;
@@ -273,6 +272,7 @@ GemmLaunch expert_gemm(const moe_config_t& c, const WsLayout& L, int kind, void*
     g.F = c.d_ff;
     g.status = ws_at<int>(ws, L.status);
     g.budget = kSpinBudget;
+    g.rows_cap = capacity_of(c);
     return g;
 }
 
@@ -429,9 +429,7 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* h, const int32_
     if (cfg->T == 0) return MOE_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void* xg = ws_at<void>(ws, L.xg);
-    if (launch_gather_rows(cfg->T, cfg->d_model, cfg->k, cfg->E, h, perm, offsets, xg, nullptr,
-                           s) !=
-        cudaSuccess)
+    if (launch_gather_rows(cfg->T, cfg->d_model, cfg->k, cfg->E, h, perm, offsets, xg, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     GemmLaunch g = expert_gemm(*cfg, L, GK_GATEUP, ws);
     g.a_ptr = xg;
@@ -509,11 +507,8 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* h, const voi
     st = run_stats(c, L, nullptr, f, P, ws, s);
     if (st != MOE_OK) return st;
     ev.mark(2);
-    const bool fused = c.k <= 2;  // at most two fp32 addends per element: order-free
-    float* acc = ws_at<float>(ws, L.out_acc);
     void* xg = ws_at<void>(ws, L.xg);
-    if (launch_gather_rows(c.T, c.d_model, c.k, c.E, h, o.perm, o.offsets, xg,
-                           fused ? acc : nullptr, s) != cudaSuccess)
+    if (launch_gather_rows(c.T, c.d_model, c.k, c.E, h, o.perm, o.offsets, xg, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     ev.mark(3);
     GemmLaunch g = expert_gemm(c, L, GK_GATEUP, ws);
@@ -524,20 +519,19 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* h, const voi
     g.act = ws_at<void>(ws, L.act);
     if (launch_gemm(g, s) != cudaSuccess) return MOE_ERR_CUDA;
     ev.mark(4);
-    GemmLaunch g2 = expert_gemm(c, L, fused ? GK_DOWN_SCATTER : GK_DOWN_SLOTS, ws);
+    // expert outputs in slot order (bf16), then each token's kept outputs
+    // weighted and summed in rank order (fp32)
+    GemmLaunch g2 = expert_gemm(c, L, GK_DOWN_SLOTS, ws);
     g2.a_ptr = ws_at<void>(ws, L.act);
     g2.b_ptr = w2;
     g2.offsets = o.offsets;
     g2.perm = o.perm;
-    g2.cw = o.cw;
-    g2.out_acc = acc;
-    g2.y_slots = fused ? nullptr : ws_at<void>(ws, L.y_slots);
+    g2.y_slots = ws_at<void>(ws, L.y_slots);
     if (launch_gemm(g2, s) != cudaSuccess) return MOE_ERR_CUDA;
     ev.mark(5);
-    cudaError_t e = fused ? launch_finalize(c.T, c.d_model, acc, out, s)
-                          : launch_combine(c.T, c.d_model, c.k, ws_at<void>(ws, L.y_slots), o.assign,
-                                           o.slot, o.offsets, o.cw, out, s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_combine(c.T, c.d_model, c.k, ws_at<void>(ws, L.y_slots), o.assign, o.slot, o.offsets, o.cw,
+                       out, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
     ev.mark(6);
     return MOE_OK;
 }

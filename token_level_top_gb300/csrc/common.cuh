@@ -316,34 +316,6 @@ __device__ __forceinline__ void tmem_ld_wait2(uint32_t (&a)[32], uint32_t (&b)[3
     asm volatile("" : MOE_RW32(b)::"memory");
 }
 
-// ----------------------------------------------------------------- bulk reduce
-// Generic-proxy writes to shared memory made by this thread become visible to
-// its later async-proxy (bulk copy) reads.
-__device__ __forceinline__ void fence_proxy_async_shared()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Atomically adds `bytes` (a multiple of 16) of fp32 from shared memory to
-// global memory, element by element; completion tracked by this thread's bulk groups.
-__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes)
-{
-    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
-                 ::"l"(gdst), "r"(ssrc), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// Waits until this thread's bulk operations have finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_all()
-{
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Waits until this thread's bulk operations have completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // ----------------------------------------------------------------- misc
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {

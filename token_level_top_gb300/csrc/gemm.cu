@@ -4,7 +4,6 @@
 //   GK_ROUTER        logits partials  = h . W_r^T          (K split across CTAs)
 //   GK_GATEUP        act = silu(x W1^T) * (x W3^T), x = the slot-ordered token rows
 //                    (tiled from x_perm, or gathered from h by tile::gather4)
-//   GK_DOWN_SCATTER  out_acc[t] += cw[t,r] * (act W2^T)    (weighted scatter)
 //   GK_DOWN_SLOTS    y_slots     = act W2^T                 (slot order, bf16)
 //
 // The router is the linear map of the token's hidden state to expert logits
@@ -35,11 +34,6 @@
 namespace moe {
 namespace {
 
-// Down-scatter epilogue staging: one row of 32 fp32 per epilogue thread,
-// padded to 144 bytes so the 16-byte stores of 8 consecutive threads fall in
-// distinct banks.
-constexpr int kStageRowBytes = 144;
-
 struct GemmParams {
     int kind, E, T, topk, d, F;
     int kb_total;      // K / 64
@@ -49,13 +43,10 @@ struct GemmParams {
     int splits;        // router K splits
     int kb_per_split;  // router K blocks per split
     int stages;
-    int stage_bytes;   // down scatter: staging rows of the bulk-reduce epilogue (0: atomics)
     int gather4;       // gate-up: A rows gathered from h with tile::gather4 (else tiled from x_perm)
     uint32_t tmem_cols;
     const int32_t* offsets;
     const int32_t* perm;
-    const float* cw;
-    float* out_acc;
     __nv_bfloat16* act;
     __nv_bfloat16* y_slots;
     float* router_part;
@@ -124,8 +115,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t b_bytes = static_cast<uint32_t>(PAIR ? p.bn / 2 : p.bn) * kBK * 2;
     uint8_t* sA = smem;
     uint8_t* sB = sA + stages * a_bytes;
-    uint8_t* sStage = sB + stages * b_bytes;   // p.stage_bytes, 1024-aligned
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + p.stage_bytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + stages * b_bytes);
     uint64_t* full_bar = bars;
     uint64_t* empty_bar = bars + stages;
     uint64_t* tfull_bar = bars + 2 * stages;
@@ -385,59 +375,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const bool valid = ri < cnt;
                 const int slot = off + ri;
                 const int col0 = ti.n * p.bn;
-                if (p.kind == GK_DOWN_SCATTER) {
-                    // out_acc[token] += cw * row.  At most k <= 2 addends reach an
-                    // element, so the result does not depend on their order.
-                    const int idx = valid ? p.perm[slot] : 0;
-                    const float w = valid ? p.cw[idx] : 0.0f;
-                    float* dst = p.out_acc + static_cast<size_t>(idx / p.topk) * p.d + col0;
-                    uint8_t* stg = sStage + static_cast<size_t>(row) * kStageRowBytes;
-                    for (int c = 0; c < p.bn; c += 32) {
-                        if (col0 + c >= p.d) break;  // uniform across the warp
-                        tmem_ld32(taddr + c, v);
-                        tmem_ld_wait(v);
-                        if (!valid) continue;
-                        if (p.stage_bytes) {
-                            // through this thread's staging row to one 128-byte bulk
-                            // reduce-add: one contiguous line per piece instead of
-                            // 32 lanes' scattered atomics
-                            bulk_wait_read_all();   // the previous piece has left the row
+                __nv_bfloat16* dst = p.y_slots + static_cast<size_t>(slot) * p.d + col0;
+                for (int c = 0; c < p.bn; c += 32) {
+                    if (col0 + c >= p.d) break;
+                    tmem_ld32(taddr + c, v);
+                    tmem_ld_wait(v);
+                    if (valid) {
+                        uint32_t pk[16];
 #pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                *reinterpret_cast<float4*>(stg + 16 * j) =
-                                    make_float4(w * __uint_as_float(v[4 * j]), w * __uint_as_float(v[4 * j + 1]),
-                                                w * __uint_as_float(v[4 * j + 2]),
-                                                w * __uint_as_float(v[4 * j + 3]));
-                            fence_proxy_async_shared();
-                            bulk_reduce_add_f32(dst + c, smem_u32(stg), 128);
-                            bulk_commit();
-                        } else {
+                        for (int j = 0; j < 16; ++j)
+                            pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c);
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                float4 add = make_float4(w * __uint_as_float(v[4 * j]),
-                                                         w * __uint_as_float(v[4 * j + 1]),
-                                                         w * __uint_as_float(v[4 * j + 2]),
-                                                         w * __uint_as_float(v[4 * j + 3]));
-                                atomicAdd(reinterpret_cast<float4*>(dst + c + 4 * j), add);
-                            }
-                        }
-                    }
-                } else {
-                    __nv_bfloat16* dst = p.y_slots + static_cast<size_t>(slot) * p.d + col0;
-                    for (int c = 0; c < p.bn; c += 32) {
-                        if (col0 + c >= p.d) break;
-                        tmem_ld32(taddr + c, v);
-                        tmem_ld_wait(v);
-                        if (valid) {
-                            uint32_t pk[16];
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                        }
+                        for (int j = 0; j < 4; ++j)
+                            d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                     }
                 }
             }
@@ -450,7 +401,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     mbar_arrive(smem_u32(&tempty_bar[b]));
             }
         }
-        bulk_wait_all();   // this thread's bulk reduces are complete
     }
 
     tc_fence_before();
@@ -509,9 +459,9 @@ namespace {
 
 constexpr int kRouterStages = 4;
 
-size_t gemm_fixed_smem(int E, int stage_bytes)
+size_t gemm_fixed_smem(int E)
 {
-    return 1024 + 64 + static_cast<size_t>(2 * (E + 1)) * 4 + 16 + 6 * 8 + stage_bytes;
+    return 1024 + 64 + static_cast<size_t>(2 * (E + 1)) * 4 + 16 + 6 * 8;
 }
 
 }  // namespace
@@ -519,7 +469,7 @@ size_t gemm_fixed_smem(int E, int stage_bytes)
 int router_ctas_per_sm(int E)
 {
     const size_t epad = static_cast<size_t>(std::max(32, (E + 31) / 32 * 32));
-    const size_t smem = gemm_fixed_smem(E, 0) + kRouterStages * (kBM * kBK * 2 + epad * kBK * 2 + 16);
+    const size_t smem = gemm_fixed_smem(E) + kRouterStages * (kBM * kBK * 2 + epad * kBK * 2 + 16);
     return smem <= 113 * 1024 ? 2 : 1;
 }
 
@@ -534,8 +484,6 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     p.F = g.F;
     p.offsets = g.offsets;
     p.perm = g.perm;
-    p.cw = g.cw;
-    p.out_acc = g.out_acc;
     p.act = static_cast<__nv_bfloat16*>(g.act);
     p.y_slots = static_cast<__nv_bfloat16*>(g.y_slots);
     p.router_part = g.router_part;
@@ -576,26 +524,33 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
         grid = static_cast<int>(std::min<long long>(mt_max * p.n_tiles, sms));
     } else {
         p.bn = kExpertBN;
+        if (!pair && g.rows_cap > 0 && g.rows_cap <= kBM) {
+            // Every expert holds at most one row tile, so the tile count is
+            // known: take the column tile (a multiple of 32, 128..256) that
+            // needs the fewest passes over the SMs times its width.
+            const long long mt = std::min<long long>(g.E, static_cast<long long>(g.T) * g.topk);
+            long long best = -1;
+            for (int bn = kExpertBN; bn >= 128; bn -= 32) {
+                const long long tiles = mt * ((g.d + bn - 1) / bn);
+                const long long cost = (tiles + sms - 1) / sms * bn;
+                if (best < 0 || cost < best) {
+                    best = cost;
+                    p.bn = bn;
+                }
+            }
+        }
         p.kb_total = g.F / kBK;
-        p.n_tiles = (g.d + kExpertBN - 1) / kExpertBN;
+        p.n_tiles = (g.d + p.bn - 1) / p.bn;
         if (!make_map(&tmA, g.a_ptr, static_cast<uint64_t>(g.T) * g.topk, g.F, kBM))
             return cudaErrorInvalidValue;
-        if (!make_map(&tmB, g.b_ptr, static_cast<uint64_t>(g.E) * g.d, g.F,
-                      pair ? kExpertBN / 2 : kExpertBN))
+        if (!make_map(&tmB, g.b_ptr, static_cast<uint64_t>(g.E) * g.d, g.F, pair ? p.bn / 2 : p.bn))
             return cudaErrorInvalidValue;
         const long long mt_max = (static_cast<long long>(g.T) * g.topk + kBM - 1) / kBM + g.E;
         grid = static_cast<int>(std::min<long long>(mt_max * p.n_tiles, sms));
     }
     const uint32_t a_bytes = kBM * kBK * 2;
     const uint32_t b_bytes = static_cast<uint32_t>(pair ? p.bn / 2 : p.bn) * kBK * 2;
-    // The bulk-reduce epilogue pays off when it hides behind the next tile's
-    // main loop: at two or more tiles per SM on average.  With about one tile
-    // per SM (decode-sized batches) its fence and completion latencies are
-    // exposed and vector atomics finish sooner.
-    const bool bulk = g.kind == GK_DOWN_SCATTER &&
-                      static_cast<long long>(g.T) * g.topk / kBM * p.n_tiles >= 2LL * sms;
-    p.stage_bytes = bulk ? 4 * 32 * kStageRowBytes : 0;
-    const size_t fixed = gemm_fixed_smem(g.E, p.stage_bytes);
+    const size_t fixed = gemm_fixed_smem(g.E);
     const size_t budget_smem = 227 * 1024;
     int stages = static_cast<int>((budget_smem - fixed) / (a_bytes + b_bytes + 16));
     stages = std::max(2, std::min(stages, g.kind == GK_ROUTER ? kRouterStages : 8));

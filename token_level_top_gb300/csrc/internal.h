@@ -17,7 +17,7 @@ constexpr int kExpertBN = 256;     // expert GEMM tile columns
 constexpr int kGemmThreads = 192;  // 6 warps: TMA, MMA, 4 x epilogue
 constexpr long long kSpinBudget = 2000000000LL;  // ~1 s of SM clock per bounded wait
 
-enum GemmKind : int { GK_ROUTER = 0, GK_GATEUP = 1, GK_DOWN_SCATTER = 2, GK_DOWN_SLOTS = 3 };
+enum GemmKind : int { GK_ROUTER = 0, GK_GATEUP = 1, GK_DOWN_SLOTS = 3 };
 
 // Byte offsets of every scratch region inside the caller's workspace.
 struct WsLayout {
@@ -26,7 +26,7 @@ struct WsLayout {
     int epad = 0;      // router N tile (E rounded up to 16, at least 16)
     size_t status = 0, ctrl = 0, part = 0, scores = 0, ids = 0, prefs = 0, crank = 0, hist = 0,
            base = 0, ppart = 0, assign = 0, slot = 0, flags = 0, counts = 0, offsets = 0,
-           perm = 0, cw = 0, xg = 0, act = 0, out_acc = 0, y_slots = 0, h_stage = 0, out_stage = 0;
+           perm = 0, cw = 0, xg = 0, act = 0, y_slots = 0, h_stage = 0, out_stage = 0;
     size_t total = 0;
 };
 
@@ -121,13 +121,12 @@ struct GemmLaunch {
     const void* b_ptr;  // router: W_r [E,d]; gate-up: W13 [E,2F,d]; down: W2 [E,d,F]
     const int32_t* offsets;
     const int32_t* perm;
-    const float* cw;
-    float* out_acc;
     void* act;
     void* y_slots;
     float* router_part;
     int splits, epad;
     int gather4;  // gate-up: gather A rows from h (a_ptr = h) instead of tiles of x_perm
+    long long rows_cap;  // most rows an expert can hold (the capacity C), or 0 if unknown
     int* status;
     long long budget;
 };
@@ -135,12 +134,9 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
 
 cudaError_t launch_pack_w13(int E, int F, int d, const void* w1, const void* w3, void* w13,
                             cudaStream_t s);
-cudaError_t launch_finalize(int T, int d, const float* acc, void* out, cudaStream_t s);
-// x_perm[j] = h[perm[j] / k] for the offsets[E] kept rows; when acc_zero is
-// not NULL the same grid also zeroes acc_zero[T][d] (fp32).
+// x_perm[j] = h[perm[j] / k] for the offsets[E] kept rows.
 cudaError_t launch_gather_rows(int T, int d, int k, int E, const void* h, const int32_t* perm,
-                               const int32_t* offsets, void* x_perm, float* acc_zero,
-                               cudaStream_t s);
+                               const int32_t* offsets, void* x_perm, cudaStream_t s);
 cudaError_t launch_combine(int T, int d, int k, const void* y_slots, const int32_t* assign,
                            const int32_t* slot, const int32_t* offsets, const float* cw, void* out,
                            cudaStream_t s);

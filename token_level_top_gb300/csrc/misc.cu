@@ -1,6 +1,6 @@
 // misc.cu -- bandwidth kernels around the GEMMs: the gate/up weight
-// re-layout, the fp32 -> bf16 finalize of the fused combine, the slot-order
-// combine used by moe_combine, and the bounded-wait failure probe.
+// re-layout, the row gather into slot order, the weighted combine of the
+// expert outputs, and the bounded-wait failure probe.
 #include "common.cuh"
 #include "internal.h"
 
@@ -26,61 +26,81 @@ __global__ void pack_w13_kernel(int E, int F, int d, const uint4* __restrict__ w
     }
 }
 
-// out = bf16(acc), 4 values per thread.  Rows whose choices were all dropped
-// received no contribution and stay 0.
-__global__ void finalize_kernel(size_t n4, const float4* __restrict__ acc, uint2* __restrict__ out)
-{
-    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const float4 v = acc[i];
-        out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
-    }
-}
-
-// out[t] = sum over kept r (rank order) of cw[t,r] * y_slots[offsets[e]+slot], 8 columns per thread.
+// out[t] = sum over kept r (rank order, fp32) of cw[t,r] * y_slots[offsets[e]+slot], rounded
+// to bf16 once.  One warp per (token, segment of 32*U 16-byte pieces of the
+// row): lanes 0..k-1 fetch the token's rows and weights, then each lane
+// streams U pieces per rank with all of them in flight.
+template <int U>
 __global__ void combine_kernel(int T, int d, int k, const uint4* __restrict__ y,
                                const int32_t* __restrict__ assign, const int32_t* __restrict__ slot,
                                const int32_t* __restrict__ offsets, const float* __restrict__ cw,
                                uint4* __restrict__ out)
 {
+    constexpr int kCombineUnroll = U;
+    const int lane = threadIdx.x & 31;
     const int d8 = d / 8;
-    const size_t total = static_cast<size_t>(T) * d8;
-    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const int t = static_cast<int>(i / d8);
-        const int c8 = static_cast<int>(i - static_cast<size_t>(t) * d8);
-        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int r = 0; r < k; ++r) {
-            const int e = assign[static_cast<size_t>(t) * k + r];
-            if (e < 0) continue;
-            const float w = cw[static_cast<size_t>(t) * k + r];
-            const size_t srow = static_cast<size_t>(offsets[e]) + slot[static_cast<size_t>(t) * k + r];
-            const uint4 v = y[srow * d8 + c8];
-            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+    const int nseg = (d8 + 32 * U - 1) / (32 * U);
+    const long long wid = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (wid >= static_cast<long long>(T) * nseg) return;   // whole warps
+    const int t = static_cast<int>(wid / nseg);
+    const int seg = static_cast<int>(wid - static_cast<long long>(t) * nseg);
+    int row = 0;
+    float w = 0.0f;
+    bool kept = false;
+    if (lane < k) {
+        const int e = assign[static_cast<size_t>(t) * k + lane];
+        if (e >= 0) {
+            row = offsets[e] + slot[static_cast<size_t>(t) * k + lane];
+            w = cw[static_cast<size_t>(t) * k + lane];
+            kept = true;
+        }
+    }
+    const uint32_t kmask = __ballot_sync(0xffffffffu, kept);
+    uint4* orow = out + static_cast<size_t>(t) * d8;
+    {
+        const int c0 = seg * 32 * U;
+        float acc[kCombineUnroll][8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&words[j]);
-                acc[2 * j] += w * __bfloat162float(b.x);
-                acc[2 * j + 1] += w * __bfloat162float(b.y);
+        for (int u = 0; u < kCombineUnroll; ++u)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[u][j] = 0.0f;
+        for (int r = 0; r < k; ++r) {
+            if (!((kmask >> r) & 1u)) continue;   // uniform across the warp
+            const uint4* yr = y + static_cast<size_t>(__shfl_sync(0xffffffffu, row, r)) * d8;
+            const float wr = __shfl_sync(0xffffffffu, w, r);
+            uint4 v[kCombineUnroll];
+#pragma unroll
+            for (int u = 0; u < kCombineUnroll; ++u) {
+                const int c = c0 + u * 32 + lane;
+                v[u] = c < d8 ? yr[c] : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kCombineUnroll; ++u) {
+                const uint32_t words[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&words[j]);
+                    acc[u][2 * j] += wr * __bfloat162float(b.x);
+                    acc[u][2 * j + 1] += wr * __bfloat162float(b.y);
+                }
             }
         }
-        out[i] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                            pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+#pragma unroll
+        for (int u = 0; u < kCombineUnroll; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < d8)
+                orow[c] = make_uint4(pack_bf16x2(acc[u][0], acc[u][1]), pack_bf16x2(acc[u][2], acc[u][3]),
+                                     pack_bf16x2(acc[u][4], acc[u][5]), pack_bf16x2(acc[u][6], acc[u][7]));
+        }
     }
 }
 
-// x_perm[i] = h[perm[i] / k] for the kept slots i < offsets[E]: the token rows
-// in slot order, so that the gate-up GEMM reads its A tiles with plain TMA
-// tile loads.  16 bytes per thread, rows of d bf16.
 __global__ void gather_rows_kernel(int rows_max, int d8, int k, int E, const uint4* __restrict__ h,
                                    const int32_t* __restrict__ perm,
-                                   const int32_t* __restrict__ offsets, uint4* __restrict__ x,
-                                   float4* __restrict__ zero, size_t zero4)
+                                   const int32_t* __restrict__ offsets, uint4* __restrict__ x)
 {
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     const size_t i0 = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
-    // the fp32 output accumulator the down projection scatters into starts at zero
-    for (size_t i = i0; i < zero4; i += stride) zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     const int n = offsets[E];
     const size_t total = static_cast<size_t>(min(n, rows_max)) * d8;
     for (size_t i = i0; i < total; i += stride) {
@@ -122,26 +142,14 @@ cudaError_t launch_pack_w13(int E, int F, int d, const void* w1, const void* w3,
     return cudaGetLastError();
 }
 
-cudaError_t launch_finalize(int T, int d, const float* acc, void* out, cudaStream_t s)
-{
-    const size_t n4 = static_cast<size_t>(T) * d / 4;
-    if (n4 == 0) return cudaSuccess;
-    finalize_kernel<<<grid_for(n4, 256), 256, 0, s>>>(n4, reinterpret_cast<const float4*>(acc),
-                                                       static_cast<uint2*>(out));
-    return cudaGetLastError();
-}
-
 cudaError_t launch_gather_rows(int T, int d, int k, int E, const void* h, const int32_t* perm,
-                               const int32_t* offsets, void* x_perm, float* acc_zero,
-                               cudaStream_t s)
+                               const int32_t* offsets, void* x_perm, cudaStream_t s)
 {
     const int rows_max = T * k;
     const size_t total = static_cast<size_t>(rows_max) * (d / 8);
-    const size_t zero4 = acc_zero ? static_cast<size_t>(T) * d / 4 : 0;
     if (total == 0) return cudaSuccess;
     gather_rows_kernel<<<grid_for(total, 256), 256, 0, s>>>(
-        rows_max, d / 8, k, E, static_cast<const uint4*>(h), perm, offsets,
-        static_cast<uint4*>(x_perm), reinterpret_cast<float4*>(acc_zero), zero4);
+        rows_max, d / 8, k, E, static_cast<const uint4*>(h), perm, offsets, static_cast<uint4*>(x_perm));
     return cudaGetLastError();
 }
 
@@ -149,11 +157,18 @@ cudaError_t launch_combine(int T, int d, int k, const void* y_slots, const int32
                            const int32_t* slot, const int32_t* offsets, const float* cw, void* out,
                            cudaStream_t s)
 {
-    const size_t total = static_cast<size_t>(T) * (d / 8);
-    if (total == 0) return cudaSuccess;
-    combine_kernel<<<grid_for(total, 256), 256, 0, s>>>(T, d, k, static_cast<const uint4*>(y_slots),
-                                                         assign, slot, offsets, cw,
-                                                         static_cast<uint4*>(out));
+    if (T <= 0 || d <= 0) return cudaSuccess;
+    // long pieces per warp for large batches, short ones (more warps) for small
+    const int U = T >= 2048 ? 4 : 1;
+    const long long warps = static_cast<long long>(T) * ((d / 8 + 32 * U - 1) / (32 * U));
+    const int per_block = 8;
+    const unsigned grid = static_cast<unsigned>((warps + per_block - 1) / per_block);
+    if (U == 4)
+        combine_kernel<4><<<grid, 32 * per_block, 0, s>>>(T, d, k, static_cast<const uint4*>(y_slots), assign,
+                                                           slot, offsets, cw, static_cast<uint4*>(out));
+    else
+        combine_kernel<1><<<grid, 32 * per_block, 0, s>>>(T, d, k, static_cast<const uint4*>(y_slots), assign,
+                                                           slot, offsets, cw, static_cast<uint4*>(out));
     return cudaGetLastError();
 }
 

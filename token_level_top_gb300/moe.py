@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libmoe.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
 NUM_STAGES = 6
-STAGE_NAMES = ["route", "dispatch", "prep", "gate_up", "down", "finalize"]
+STAGE_NAMES = ["route", "dispatch", "prep", "gate_up", "down", "combine"]
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "misaligned pointer",
           4: "workspace too small", 5: "non-finite (NaN) score", 6: "bounded device wait timed out",

@@ -278,7 +278,9 @@ def test_layer_forward_deterministic(name):
 
 @pytest.mark.parametrize("T,E,k,cap", [(1, 8, 2, 0), (300, 6, 1, 0), (300, 6, 3, 0),
                                        (257, 4, 2, 30), (64, 1, 1, 0), (900, 3, 2, 0),
-                                       (1500, 2, 2, 700), (200, 40, 2, 2)])
+                                       (1500, 2, 2, 700), (200, 40, 2, 2),
+                                       # general k: one choice per token, four per token
+                                       (2000, 8, 1, 0), (1200, 16, 4, 0), (600, 12, 4, 40)])
 def test_layer_forward_edge_shapes(T, E, k, cap):
     shape = synth.MoEShape("edge", T=T, d=128, E=E, F=256, k=k, cf=1.0, capacity=cap, seed=T + E)
     Ld = make_layer(shape)

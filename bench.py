@@ -43,11 +43,12 @@ CLOCK_LEAD_S = 0.25  # untimed lead-in for clock samples when the timed region i
 CHUNK = 256  # tokens per routing chunk; a batch of one chunk routes and dispatches in one kernel
 
 
-def kernels_per_step(T):
+def kernels_per_step(T, fp8=False):
     """Kernels of this library one layer step launches."""
     # router GEMM, row gather, gate-up, down, combine + route and dispatch:
-    # one fused kernel for a single chunk, else route + dispatch replay + finish
-    return 5 + (1 if T <= CHUNK else 3)
+    # one fused kernel for a single chunk, else route + dispatch replay + finish;
+    # FP8: the activation rows are quantised between the two expert GEMMs
+    return 5 + (1 if T <= CHUNK else 3) + (1 if fp8 else 0)
 
 
 def parse():
@@ -59,6 +60,9 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.CONFIG_ORDER)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--fp8-weights", action="store_true",
+                    help="expert GEMMs in e4m3: weights quantised per row once (moe_quantize_fp8), "
+                         "token and activation rows per row on the fly")
     return ap.parse_args()
 
 
@@ -270,7 +274,14 @@ def run_ours(args, rank, world, local):
     host_w = (L["w1"].cpu(), L["w3"].cpu(), L["w2"].cpu()) if want_cpu else None
     del L["w1"], L["w3"]
     torch.cuda.empty_cache()
-    cfg = moe.Config.of(shape)
+    fp8 = args.fp8_weights
+    if fp8:   # e4m3 expert weights, one fp32 scale per weight row
+        L["w13"] = moe.quantize_fp8(L["w13"])
+        L["w2"] = moe.quantize_fp8(L["w2"])
+        want_cpu = False
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    cfg = moe.Config.of(shape, flags=moe.FLAG_FP8 if fp8 else 0)
     ws = moe.workspace(cfg)
     out = torch.empty(shape.T, shape.d, dtype=torch.bfloat16, device="cuda")
     # kept rows of this batch (routing is deterministic, identical every step)
@@ -334,33 +345,50 @@ def run_ours(args, rank, world, local):
                                    for i in range(args.steps))
                 for j, n in enumerate(moe.STAGE_NAMES)}
 
-    # end to end from pinned host memory through moe_layer_forward_host
+    # end to end from pinned host memory through moe_layer_forward_host (FP8
+    # weights: the same copies around moe_layer_forward_fp8, from Python)
     h_host = L["h"].cpu().pin_memory()
     o_host = torch.empty(shape.T, shape.d, dtype=torch.bfloat16).pin_memory()
-    moe.layer_forward_host(cfg, ws, h_host, L["wr"], L["w13"], L["w2"], o_host, L["bias"],
-                           L["usage"])
+    h_dev = torch.empty_like(L["h"])
+
+    def e2e_step():
+        if fp8:
+            h_dev.copy_(h_host, non_blocking=True)
+            moe.layer_forward(cfg, ws, h_dev, L["wr"], L["w13"], L["w2"], L["bias"], L["usage"], out=out)
+            o_host.copy_(out, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        else:
+            moe.layer_forward_host(cfg, ws, h_host, L["wr"], L["w13"], L["w2"], o_host, L["bias"],
+                                   L["usage"])
+
+    e2e_step()
     barrier(world)
     te0 = time.perf_counter()
     for _ in range(args.e2e_steps):
-        moe.layer_forward_host(cfg, ws, h_host, L["wr"], L["w13"], L["w2"], o_host, L["bias"],
-                               L["usage"])
+        e2e_step()
     te = max_over_ranks(time.perf_counter() - te0, world)
 
     peaks, peak_kind = load_peaks()
     d, F, T = shape.d, shape.F, shape.T
     # algorithmic work per launch: kept rows only; every active expert's weights read once
     flops = {"gate_up": 2.0 * kept * d * 2 * F, "down": 2.0 * kept * F * d}
-    bytes_ = {"gate_up": active * 2.0 * F * d * 2 + kept * d * 2 + kept * F * 2,
-              "down": active * 1.0 * d * F * 2 + kept * F * 2 + kept * d * 4}
+    wb = 1 if fp8 else 2   # bytes per weight element (+ 4 per weight row for FP8 scales)
+    # (FP8: the GEMMs read 1-byte activation rows; the act quantisation pass
+    # between them is timed in the down stage)
+    bytes_ = {"gate_up": active * 2.0 * F * (d * wb + 4 * fp8) + kept * d * wb + kept * F * 2,
+              "down": active * 1.0 * d * (F * wb + 4 * fp8) + kept * F * wb + kept * d * 2}
     dom = max(("gate_up", "down"), key=lambda n: stage_ms[n])
     peak_tf = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    if fp8:   # e4m3 MMAs: the measured bf16 peak times the nominal e4m3 / bf16 ratio (4.5 / 2.25)
+        peak_tf *= 2.0
     peak_bw = float(peaks["hbm_gbs"])
     intensity = (flops["gate_up"] + flops["down"]) / (bytes_["gate_up"] + bytes_["down"])
     sec = stage_ms[dom] * 1e-3
     if intensity * 1e9 >= peak_tf * 1e12 / peak_bw:     # above the ridge: tensor bound
         roof = {"bound": "tensor", "achieved": flops[dom] / sec / 1e12, "peak": peak_tf,
                 "unit": "TFLOP/s",
-                "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long loop)"}
+                "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long loop)"
+                             + (" x 2, the nominal e4m3 / bf16 ratio" if fp8 else "")}
     else:
         roof = {"bound": "hbm", "achieved": bytes_[dom] / sec / 1e9, "peak": peak_bw,
                 "unit": "GB/s", "peak_kind": f"{peak_kind} HBM copy bandwidth"}
@@ -370,12 +398,15 @@ def run_ours(args, rank, world, local):
     roof["algorithmic_per_launch"] = {"flop": flops[dom], "bytes": bytes_[dom]}
     expert_tflops = (flops["gate_up"] + flops["down"]) / (
         (stage_ms["gate_up"] + stage_ms["down"]) * 1e-3) / 1e12
-    weight_bytes = 3.0 * active * F * d * 2
+    weight_bytes = 3.0 * active * F * d * wb
     value = world * T * args.steps / (ms_max * 1e-3)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": ("e4m3 expert weights and activations (fp32 row scales), fp32 accumulate"
+                  if fp8 else "bf16"),
+        "data": "synthetic",
         "config": workload_config(shape),
         "roofline": roof,
         "expert_gemm_tflops": expert_tflops,
@@ -385,7 +416,7 @@ def run_ours(args, rank, world, local):
         "e2e": ({"value": world * T * args.e2e_steps / te, "unit": UNIT,
                  "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2}
                 if args.e2e_steps > 0 else None),
-        "gpu_launches": kernels_per_step(shape.T) * args.steps,
+        "gpu_launches": kernels_per_step(shape.T, fp8) * args.steps,
     }
     if want_cpu:
         res = oracle_sample(shape, L["h"].cpu(), L["wr"].cpu(),

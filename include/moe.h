@@ -56,6 +56,10 @@ typedef enum {
     MOE_ERR_CUDA = 7           /* a CUDA runtime call failed */
 } moe_status_t;
 
+/* moe_config_t.flags: size the workspace for the FP8 entry points too (adds
+ * T*k*(d_ff + 8) bytes for the e4m3 activation rows and row scales). */
+#define MOE_FLAG_FP8 1u
+
 /* Layer shape.  Capacity C = ceil(T*k*cf/E) unless capacity > 0. */
 typedef struct {
     int32_t T;        /* tokens in the batch */
@@ -66,7 +70,7 @@ typedef struct {
     double cf;        /* capacity factor, read as a decimal with 6 fractional digits */
     int32_t capacity; /* > 0: explicit per-expert capacity, overrides cf */
     float lambda;     /* load-penalty weight (0 = no penalty) */
-    uint32_t flags;   /* reserved, must be 0 */
+    uint32_t flags;   /* 0, or MOE_FLAG_FP8 */
 } moe_config_t;
 
 /* Number of stage boundaries recorded by moe_layer_forward's stage_events. */
@@ -161,6 +165,32 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* h_dev, const in
                             const int32_t* offsets_dev, const void* w13_dev, const void* w2_dev,
                             void* y_slots_dev, void* ws_dev, size_t ws_bytes, void* stream);
 
+/* FP8 expert weights.  The pages quantise expert weights to cut the bytes
+ * moved ([2kiu] §5.1: INT4/INT6 per expert; [cnnetsun] §3.2: INT8, where the
+ * dequantisation cost ate the gain -- the bottleneck is moving data).  This
+ * library's form: e4m3 with one fp32 scale per weight row (output channel);
+ * the kernels stream the 8-bit tiles and widen them to bf16 in shared memory
+ * behind the copies; activations stay bf16.
+ *
+ * Per-row quantisation of a bf16 matrix w_dev [rows, cols] (row-major, cols a
+ * multiple of 8; w_dev 16-byte aligned, q_dev 8-byte aligned):
+ *   scales_dev[r] = max_c |w[r,c]| / 448 (1 for an all-zero row),
+ *   q_dev[r,c] = e4m3(w[r,c] / scales[r]), round to nearest even, saturating.
+ * Quantise W13 after moe_pack_w13 (rows E*2F, cols d) and W2 (rows E*d,
+ * cols F).  Errors: MOE_ERR_INVALID_ARG (rows < 0, cols not a positive
+ * multiple of 8, NULL), MOE_ERR_MISALIGNED. */
+moe_status_t moe_quantize_fp8(int64_t rows, int32_t cols, const void* w_dev, void* q_dev,
+                              float* scales_dev, void* stream);
+
+/* moe_expert_ffn with e4m3 weights: w13_q_dev [E, 2F, d] and w2_q_dev
+ * [E, d, F] from moe_quantize_fp8, w13_scale_dev [E*2F], w2_scale_dev [E*d]
+ * fp32.  Weight W = q * scale (per row); everything else as moe_expert_ffn. */
+moe_status_t moe_expert_ffn_fp8(const moe_config_t* cfg, const void* h_dev, const int32_t* perm_dev,
+                                const int32_t* offsets_dev, const void* w13_q_dev,
+                                const float* w13_scale_dev, const void* w2_q_dev,
+                                const float* w2_scale_dev, void* y_slots_dev, void* ws_dev,
+                                size_t ws_bytes, void* stream);
+
 /* Probability-weighted combine back to token order ([mhpn] §4.3; [2kiu] §3
  * step 5): out[t] = sum over kept r, in rank order, of combine_w[t,r] *
  * y_slots[offsets[assign[t,r]] + slot[t,r]]; tokens with nothing kept get 0.
@@ -190,6 +220,18 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* h_dev,
                                int32_t* slot_dev, uint8_t* flags_dev, int32_t* counts_dev,
                                float* f_dev, float* P_dev, void* const* stage_events,
                                void* ws_dev, size_t ws_bytes, void* stream);
+
+/* moe_layer_forward with e4m3 expert weights (as moe_expert_ffn_fp8); the
+ * router weights stay bf16. */
+moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* h_dev,
+                                   const void* w_router_dev, const float* bias_dev,
+                                   const float* usage_dev, const void* w13_q_dev,
+                                   const float* w13_scale_dev, const void* w2_q_dev,
+                                   const float* w2_scale_dev, void* out_dev,
+                                   float* logits_out_dev, int32_t* assign_dev, int32_t* slot_dev,
+                                   uint8_t* flags_dev, int32_t* counts_dev, float* f_dev,
+                                   float* P_dev, void* const* stage_events, void* ws_dev,
+                                   size_t ws_bytes, void* stream);
 
 /* The same layer from host memory, end to end: copies h (pinned host,
  * [T,d] bf16) to the workspace, runs moe_layer_forward and copies the output

@@ -62,6 +62,16 @@ def _load():
             lib.oracle_combine_rows.restype = I
             lib.oracle_expert_slots.argtypes = [I, I, I, I, I, P, P, P, P, P, P, I, I, P]
             lib.oracle_expert_slots.restype = I
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
+            lib.oracle_combine_rows_q8.argtypes = [I, I, I, I, I] + [P] * 7 + [I] + [P] * 3 + [I, P]
+            lib.oracle_combine_rows_q8.restype = I
+            lib.oracle_expert_slots_q8.argtypes = [I, I, I, I, I] + [P] * 7 + [I, P, P, I, I, P]
+            lib.oracle_expert_slots_q8.restype = I
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.oracle_quantize_row.argtypes = [I, P, P, P]
+            lib.oracle_quantize_row.restype = None
             _lib = lib
     return _lib
 
@@ -190,6 +200,69 @@ def expert_slots(h, w1, w3, w2, assign, perm, row0: int, row1: int) -> np.ndarra
                                      _ptr(assign), _ptr(perm), row0, row1, _ptr(out))
     if st:
         raise OracleError(st, "expert_slots")
+    return out
+
+
+def e4m3_value(code: int) -> float:
+    """Value of one e4m3 code (sign, 4-bit exponent bias 7, 3-bit mantissa)."""
+    return float(_load().oracle_e4m3_value(int(code) & 0xFF))
+
+
+def e4m3_encode(v: float) -> int:
+    """The e4m3 code nearest to v (ties to even), saturating at +-448."""
+    return int(_load().oracle_e4m3_encode(float(v)))
+
+
+def quantize_row(x):
+    """Row quantisation: (codes uint8, scale) with scale = max|x| / 448."""
+    x = _c(x, np.float32)
+    codes = np.empty(x.shape[0], np.uint8)
+    sc = np.empty(1, np.float32)
+    _load().oracle_quantize_row(x.shape[0], _ptr(x), _ptr(codes), _ptr(sc))
+    return codes, float(sc[0])
+
+
+def _q8(q1, s1, q3, s3, q2, s2):
+    return ([_c(a, np.uint8) for a in (q1, q3, q2)], [_c(a, np.float32) for a in (s1, s3, s2)])
+
+
+def combine_rows_q8(h, q1, s1, q3, s3, q2, s2, assign, cw, tokens, quant_act=True) -> np.ndarray:
+    """combine_rows with e4m3 expert weights: q1, q3 [E,F,d] codes with row scales
+    s1, s3 [E,F]; q2 [E,d,F] with s2 [E,d].  quant_act: token and activation
+    rows also enter the GEMMs as row-quantised e4m3 (the FP8 layer's form)."""
+    h = _c(h, np.uint16)
+    (q1, q3, q2), (s1, s3, s2) = _q8(q1, s1, q3, s3, q2, s2)
+    assign = _c(assign, np.int32)
+    cw = _c(cw, np.float32)
+    tokens = _c(tokens, np.int32)
+    T, d = h.shape
+    E, F, _ = q1.shape
+    k = assign.shape[1]
+    out = np.empty((tokens.shape[0], d), np.float32)
+    st = _load().oracle_combine_rows_q8(T, d, E, k, F, _ptr(h), _ptr(q1), _ptr(s1), _ptr(q3), _ptr(s3),
+                                        _ptr(q2), _ptr(s2), int(quant_act), _ptr(assign), _ptr(cw), _ptr(tokens),
+                                        tokens.shape[0], _ptr(out))
+    if st:
+        raise OracleError(st, "combine_rows_q8")
+    return out
+
+
+def expert_slots_q8(h, q1, s1, q3, s3, q2, s2, assign, perm, row0: int, row1: int,
+                    quant_act=True) -> np.ndarray:
+    """expert_slots with e4m3 expert weights (layouts and quant_act as combine_rows_q8)."""
+    h = _c(h, np.uint16)
+    (q1, q3, q2), (s1, s3, s2) = _q8(q1, s1, q3, s3, q2, s2)
+    assign = _c(assign, np.int32)
+    perm = _c(perm, np.int32)
+    T, d = h.shape
+    E, F, _ = q1.shape
+    k = assign.shape[1]
+    out = np.empty((row1 - row0, d), np.float32)
+    st = _load().oracle_expert_slots_q8(T, d, E, k, F, _ptr(h), _ptr(q1), _ptr(s1), _ptr(q3), _ptr(s3),
+                                        _ptr(q2), _ptr(s2), int(quant_act), _ptr(assign), _ptr(perm), row0, row1,
+                                        _ptr(out))
+    if st:
+        raise OracleError(st, "expert_slots_q8")
     return out
 
 

@@ -17,6 +17,9 @@
  *   6. SwiGLU experts W2(silu(W1 x) * W3 x)      [mhpn] §3.1, [2kiu] §1
  *   7. weighted combine, weights renormalised    [mhpn] §4.3
  *      over the experts actually used
+ *   (8. expert weights stored as 8-bit codes with one scale per row, the
+ *      bytes-moved concern of [cnnetsun] §3.2 and [2kiu] §5.1: decoded here
+ *      from the e4m3 format's definition and used in double precision.)
  */
 #include "moe_oracle.h"
 
@@ -30,6 +33,80 @@ static float bf16_to_f32(uint16_t b)
     float f;
     memcpy(&f, &u, sizeof f);
     return f;
+}
+
+/* e4m3 ("E4M3" 8-bit float): bit 7 sign, bits 6..3 exponent with bias 7, bits
+ * 2..0 mantissa; exponent field 0 holds subnormals m/8 * 2^-6; the codes with
+ * every exponent and mantissa bit set (0x7F, 0xFF) are NaN; there is no
+ * infinity, so the largest finite magnitude is 1.75 * 2^8 = 448. */
+double oracle_e4m3_value(uint8_t b)
+{
+    const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* The e4m3 code nearest to v, ties to the even code; magnitudes above 448
+ * (the largest finite value) give +-448; NaN gives 0x7F. */
+uint8_t oracle_e4m3_encode(float v)
+{
+    if (isnan(v)) return 0x7F;
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {   /* subnormal range: steps of 2^-9 */
+        double q = a / ldexp(1.0, -9);
+        double f = floor(q);
+        double m = (q - f > 0.5 || (q - f == 0.5 && fmod(f, 2.0) != 0.0)) ? f + 1.0 : f;
+        return sign | (uint8_t)m;   /* m == 8 is the code of 2^-6 */
+    }
+    int e;
+    double fr = frexp(a, &e);   /* a = fr * 2^e, fr in [0.5, 1) */
+    e -= 1;                     /* a = (2 fr) * 2^e, 2 fr in [1, 2) */
+    double q = (2.0 * fr - 1.0) * 8.0;
+    double f = floor(q);
+    double m = (q - f > 0.5 || (q - f == 0.5 && fmod(f, 2.0) != 0.0)) ? f + 1.0 : f;
+    if (m == 8.0) {
+        m = 0.0;
+        e += 1;
+    }
+    if (e + 7 > 15 || (e + 7 == 15 && m == 7.0)) return sign | 0x7E;
+    return sign | (uint8_t)(((e + 7) << 3) | (int)m);
+}
+
+/* Row-wise e4m3 quantisation: s = max |x| / 448 (fp32; 1 for an all-zero
+ * row), code_i = e4m3(x_i / s) with the quotient rounded to fp32. */
+void oracle_quantize_row(int n, const float* x, uint8_t* codes, float* scale)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int i = 0; i < n; ++i) codes[i] = oracle_e4m3_encode(x[i] / s);
+    *scale = s;
+}
+
+static uint16_t f32_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x40);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* One expert's weight matrix: bf16 bits, or e4m3 codes with one scale per row. */
+typedef struct {
+    const uint16_t* bf;
+    const uint8_t* q;
+    const float* s;
+    size_t cols;
+} Wmat;
+
+static double wval(const Wmat* w, size_t r, size_t c)
+{
+    if (w->bf) return (double)bf16_to_f32(w->bf[r * w->cols + c]);
+    return oracle_e4m3_value(w->q[r * w->cols + c]) * (double)w->s[r];
 }
 
 int64_t oracle_capacity(int64_t T, int k, int E, double cf, int64_t explicit_cap)
@@ -232,36 +309,80 @@ int oracle_dispatch(int T, int E, int k, int64_t C, const float* scores,
 
 static double silu(double x) { return x / (1.0 + exp(-x)); }
 
-void oracle_expert_row(int d, int F, const uint16_t* x, const uint16_t* w1,
-                       const uint16_t* w3, const uint16_t* w2, double* y)
+/* y = W2 (silu(W1 x) * W3 x) in double; W1, W3 [F][d], W2 [d][F]. */
+/* quant_act: x and a = silu(g)*u enter their products as per-row e4m3 codes
+ * times the row scale (a first rounded to bf16, as it is stored). */
+static void expert_row_w(int d, int F, const uint16_t* x, const Wmat* w1, const Wmat* w3,
+                         const Wmat* w2, int quant_act, double* y)
 {
     double* xf = (double*)malloc(sizeof(double) * (size_t)d);
     double* a = (double*)malloc(sizeof(double) * (size_t)F);
+    float* tmp = (float*)calloc((size_t)(d > F ? d : F), sizeof(float));
+    uint8_t* codes = (uint8_t*)malloc((size_t)(d > F ? d : F));
+    float sc = 1.0f;
     for (int i = 0; i < d; ++i) xf[i] = (double)bf16_to_f32(x[i]);
+    if (quant_act) {
+        for (int i = 0; i < d; ++i) tmp[i] = (float)xf[i];
+        oracle_quantize_row(d, tmp, codes, &sc);
+        for (int i = 0; i < d; ++i) xf[i] = oracle_e4m3_value(codes[i]) * (double)sc;
+    }
     for (int j = 0; j < F; ++j) {
-        const uint16_t* g_row = w1 + (size_t)j * d;
-        const uint16_t* u_row = w3 + (size_t)j * d;
         double g = 0.0, u = 0.0;
         for (int i = 0; i < d; ++i) {
-            g += (double)bf16_to_f32(g_row[i]) * xf[i];
-            u += (double)bf16_to_f32(u_row[i]) * xf[i];
+            g += wval(w1, (size_t)j, (size_t)i) * xf[i];
+            u += wval(w3, (size_t)j, (size_t)i) * xf[i];
         }
         a[j] = silu(g) * u;
     }
+    if (quant_act) {
+        for (int j = 0; j < F; ++j) tmp[j] = bf16_to_f32(f32_to_bf16_rne((float)a[j]));
+        oracle_quantize_row(F, tmp, codes, &sc);
+        for (int j = 0; j < F; ++j) a[j] = oracle_e4m3_value(codes[j]) * (double)sc;
+    }
+    free(tmp);
+    free(codes);
     for (int i = 0; i < d; ++i) {
-        const uint16_t* row = w2 + (size_t)i * F;
         double acc = 0.0;
-        for (int j = 0; j < F; ++j) acc += (double)bf16_to_f32(row[j]) * a[j];
+        for (int j = 0; j < F; ++j) acc += wval(w2, (size_t)i, (size_t)j) * a[j];
         y[i] = acc;
     }
     free(xf);
     free(a);
 }
 
-int oracle_combine_rows(int T, int d, int E, int k, int F, const uint16_t* h,
-                        const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
-                        const int32_t* assign, const float* cw,
-                        const int32_t* tokens, int ntok, float* out_rows)
+void oracle_expert_row(int d, int F, const uint16_t* x, const uint16_t* w1,
+                       const uint16_t* w3, const uint16_t* w2, double* y)
+{
+    const Wmat m1 = {w1, NULL, NULL, (size_t)d}, m3 = {w3, NULL, NULL, (size_t)d},
+               m2 = {w2, NULL, NULL, (size_t)F};
+    expert_row_w(d, F, x, &m1, &m3, &m2, 0, y);
+}
+
+/* The weight matrices of expert e: bf16 (q1 == NULL) or e4m3 codes + row scales. */
+typedef struct {
+    const uint16_t *w1, *w3, *w2;
+    const uint8_t *q1, *q3, *q2;
+    const float *s1, *s3, *s2;
+    int quant_act;
+} ExpertSet;
+
+static void expert_mats(const ExpertSet* x, int e, int d, int F, Wmat* m1, Wmat* m3, Wmat* m2)
+{
+    const size_t wsz = (size_t)F * d;
+    if (!x->q1) {
+        *m1 = (Wmat){x->w1 + (size_t)e * wsz, NULL, NULL, (size_t)d};
+        *m3 = (Wmat){x->w3 + (size_t)e * wsz, NULL, NULL, (size_t)d};
+        *m2 = (Wmat){x->w2 + (size_t)e * wsz, NULL, NULL, (size_t)F};
+    } else {
+        *m1 = (Wmat){NULL, x->q1 + (size_t)e * wsz, x->s1 + (size_t)e * F, (size_t)d};
+        *m3 = (Wmat){NULL, x->q3 + (size_t)e * wsz, x->s3 + (size_t)e * F, (size_t)d};
+        *m2 = (Wmat){NULL, x->q2 + (size_t)e * wsz, x->s2 + (size_t)e * d, (size_t)F};
+    }
+}
+
+static int combine_rows_x(int T, int d, int E, int k, int F, const uint16_t* h, const ExpertSet* W,
+                          const int32_t* assign, const float* cw, const int32_t* tokens, int ntok,
+                          float* out_rows)
 {
     if (d <= 0 || F <= 0 || E <= 0 || k <= 0) return 1;
     double* y = (double*)malloc(sizeof(double) * (size_t)d);
@@ -274,9 +395,9 @@ int oracle_combine_rows(int T, int d, int E, int k, int F, const uint16_t* h,
             int32_t e = assign[(size_t)t * k + r];
             if (e < 0) continue;
             if (e >= E) { free(y); free(acc); return 1; }
-            size_t wsz = (size_t)F * d;
-            oracle_expert_row(d, F, h + (size_t)t * d, w1 + (size_t)e * wsz, w3 + (size_t)e * wsz,
-                              w2 + (size_t)e * wsz, y);
+            Wmat m1, m3, m2;
+            expert_mats(W, e, d, F, &m1, &m3, &m2);
+            expert_row_w(d, F, h + (size_t)t * d, &m1, &m3, &m2, W->quant_act, y);
             double w = (double)cw[(size_t)t * k + r];
             for (int c = 0; c < d; ++c) acc[c] += w * y[c];
         }
@@ -287,24 +408,58 @@ int oracle_combine_rows(int T, int d, int E, int k, int F, const uint16_t* h,
     return 0;
 }
 
-int oracle_expert_slots(int T, int d, int E, int k, int F, const uint16_t* h,
+int oracle_combine_rows(int T, int d, int E, int k, int F, const uint16_t* h,
                         const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
-                        const int32_t* assign, const int32_t* perm,
-                        int row0, int row1, float* y_slots)
+                        const int32_t* assign, const float* cw,
+                        const int32_t* tokens, int ntok, float* out_rows)
+{
+    const ExpertSet W = {w1, w3, w2, NULL, NULL, NULL, NULL, NULL, NULL, 0};
+    return combine_rows_x(T, d, E, k, F, h, &W, assign, cw, tokens, ntok, out_rows);
+}
+
+int oracle_combine_rows_q8(int T, int d, int E, int k, int F, const uint16_t* h,
+                           const uint8_t* q1, const float* s1, const uint8_t* q3, const float* s3,
+                           const uint8_t* q2, const float* s2, int quant_act, const int32_t* assign,
+                           const float* cw, const int32_t* tokens, int ntok, float* out_rows)
+{
+    const ExpertSet W = {NULL, NULL, NULL, q1, q3, q2, s1, s3, s2, quant_act};
+    return combine_rows_x(T, d, E, k, F, h, &W, assign, cw, tokens, ntok, out_rows);
+}
+
+static int expert_slots_x(int T, int d, int E, int k, int F, const uint16_t* h, const ExpertSet* W,
+                          const int32_t* assign, const int32_t* perm, int row0, int row1, float* y_slots)
 {
     if (d <= 0 || F <= 0 || E <= 0 || k <= 0 || row0 < 0 || row1 < row0) return 1;
     double* y = (double*)malloc(sizeof(double) * (size_t)d);
-    size_t wsz = (size_t)F * d;
     for (int i = row0; i < row1; ++i) {
         int32_t idx = perm[i];
         int t = idx / k;
         if (t < 0 || t >= T) { free(y); return 1; }
         int32_t e = assign[idx];
         if (e < 0 || e >= E) { free(y); return 1; }
-        oracle_expert_row(d, F, h + (size_t)t * d, w1 + (size_t)e * wsz, w3 + (size_t)e * wsz,
-                          w2 + (size_t)e * wsz, y);
+        Wmat m1, m3, m2;
+        expert_mats(W, e, d, F, &m1, &m3, &m2);
+        expert_row_w(d, F, h + (size_t)t * d, &m1, &m3, &m2, W->quant_act, y);
         for (int c = 0; c < d; ++c) y_slots[(size_t)(i - row0) * d + c] = (float)y[c];
     }
     free(y);
     return 0;
+}
+
+int oracle_expert_slots(int T, int d, int E, int k, int F, const uint16_t* h,
+                        const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
+                        const int32_t* assign, const int32_t* perm,
+                        int row0, int row1, float* y_slots)
+{
+    const ExpertSet W = {w1, w3, w2, NULL, NULL, NULL, NULL, NULL, NULL, 0};
+    return expert_slots_x(T, d, E, k, F, h, &W, assign, perm, row0, row1, y_slots);
+}
+
+int oracle_expert_slots_q8(int T, int d, int E, int k, int F, const uint16_t* h,
+                           const uint8_t* q1, const float* s1, const uint8_t* q3, const float* s3,
+                           const uint8_t* q2, const float* s2, int quant_act, const int32_t* assign,
+                           const int32_t* perm, int row0, int row1, float* y_slots)
+{
+    const ExpertSet W = {NULL, NULL, NULL, q1, q3, q2, s1, s3, s2, quant_act};
+    return expert_slots_x(T, d, E, k, F, h, &W, assign, perm, row0, row1, y_slots);
 }

@@ -93,7 +93,33 @@ int oracle_expert_slots(int T, int d, int E, int k, int F, const uint16_t* h,
                         const int32_t* assign, const int32_t* perm,
                         int row0, int row1, float* y_slots);
 
+/* The value of an e4m3 code (sign, 4-bit exponent with bias 7, 3-bit
+ * mantissa, subnormals at exponent 0, 0x7F/0xFF NaN, no infinity). */
+double oracle_e4m3_value(uint8_t b);
+
+/* The e4m3 code nearest to v (ties to even), saturating at +-448. */
+uint8_t oracle_e4m3_encode(float v);
+
+/* Row quantisation: scale = max|x| / 448 (fp32; 1 for a zero row), codes[i] =
+ * e4m3(x[i] / scale). */
+void oracle_quantize_row(int n, const float* x, uint8_t* codes, float* scale);
+
+/* oracle_combine_rows / oracle_expert_slots with 8-bit expert weights: W1, W3
+ * as e4m3 codes q1, q3 [E][F][d] with row scales s1, s3 [E][F]; W2 as q2
+ * [E][d][F] with s2 [E][d]; weight = code value * row scale.  quant_act != 0:
+ * each token row x and each activation row silu(W1 x) * (W3 x) (rounded to
+ * bf16 first) also enters its GEMM as row-quantised e4m3 codes times scale. */
+int oracle_combine_rows_q8(int T, int d, int E, int k, int F, const uint16_t* h,
+                           const uint8_t* q1, const float* s1, const uint8_t* q3, const float* s3,
+                           const uint8_t* q2, const float* s2, int quant_act, const int32_t* assign,
+                           const float* cw, const int32_t* tokens, int ntok, float* out_rows);
+int oracle_expert_slots_q8(int T, int d, int E, int k, int F, const uint16_t* h,
+                           const uint8_t* q1, const float* s1, const uint8_t* q3, const float* s3,
+                           const uint8_t* q2, const float* s2, int quant_act, const int32_t* assign,
+                           const int32_t* perm, int row0, int row1, float* y_slots);
+
 #ifdef __cplusplus
 }
 #endif
+
 #endif

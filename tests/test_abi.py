@@ -64,8 +64,14 @@ def test_workspace_size(L):
         c = _cfg(**bad)
         assert L.moe_workspace_size(ctypes.byref(c)) == 0, bad
     c = _cfg()
-    c.flags = 1
+    c.flags = 2   # not a defined flag
     assert L.moe_workspace_size(ctypes.byref(c)) == 0
+    # MOE_FLAG_FP8 adds the e4m3 activation rows and the row scales
+    c = _cfg()
+    base = L.moe_workspace_size(ctypes.byref(c))
+    c.flags = moe.FLAG_FP8
+    grown = L.moe_workspace_size(ctypes.byref(c))
+    assert grown >= base + c.T * c.k * (c.d_ff + 8)
 
 
 FAKE = 0x7f0000000000  # never dereferenced: every case below fails validation first

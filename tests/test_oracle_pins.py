@@ -506,3 +506,101 @@ def test_workload_router_statistics(name):
     assert d["counts"].sum() == shape.T * shape.k - d["n_dropped"]
     if name == "skewed":
         assert abs((oracle.route(2, logits_in=s)["ids"][:, 0] == 0).mean() - 0.4266) < 1e-3
+
+
+# ----------------------------------------------------------------------------- e4m3 weights
+
+# Codes and values fixed by the e4m3 format: sign bit, exponent bias 7, three
+# mantissa bits, subnormals m/8 * 2^-6 at exponent 0, no infinity, 0x7F NaN.
+E4M3_KNOWN = [(0x00, 0.0), (0x80, -0.0), (0x38, 1.0), (0xB8, -1.0), (0x3C, 1.5), (0x40, 2.0),
+              (0x7E, 448.0), (0xFE, -448.0), (0x77, 240.0), (0x08, 2.0 ** -6), (0x01, 2.0 ** -9),
+              (0x07, 7 * 2.0 ** -9), (0x0F, 1.875 * 2.0 ** -6), (0x30, 0.5), (0x39, 1.125)]
+
+
+@pytest.mark.parametrize("code,value", E4M3_KNOWN)
+def test_e4m3_known_codes(code, value):
+    got = oracle.e4m3_value(code)
+    assert got == value and math.copysign(1.0, got) == math.copysign(1.0, value)
+
+
+def test_e4m3_nan_codes():
+    assert math.isnan(oracle.e4m3_value(0x7F)) and math.isnan(oracle.e4m3_value(0xFF))
+
+
+def test_e4m3_all_codes_match_torch():
+    """Every code against torch's float8_e4m3fn -> float conversion (a library routine)."""
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c in range(256):
+        got = oracle.e4m3_value(c)
+        if math.isnan(ref[c]):
+            assert math.isnan(got), c
+        else:
+            assert got == ref[c], (c, got, ref[c])
+
+
+def test_q8_experts_equal_bf16_experts_on_exact_weights():
+    """Weights that are e4m3 values times power-of-two row scales are exact in
+    bf16 too: the 8-bit path must then give the bf16 path's numbers exactly (a
+    dropped scale, a row/column mix-up or a wrong row stride breaks this)."""
+    rng = np.random.default_rng(11)
+    T, d, F, E, k = 6, 32, 24, 3, 2
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    q1, q3 = (rng.choice(finite, size=(E, F, d)) for _ in range(2))
+    q2 = rng.choice(finite, size=(E, d, F))
+    s1, s3 = (np.ldexp(1.0, rng.integers(-12, -4, size=(E, F))).astype(np.float32) for _ in range(2))
+    s2 = np.ldexp(1.0, rng.integers(-12, -4, size=(E, d))).astype(np.float32)
+    val = np.vectorize(oracle.e4m3_value)
+    w1 = val(q1) * s1[:, :, None]
+    w3 = val(q3) * s3[:, :, None]
+    w2 = val(q2) * s2[:, :, None]
+    h = bf16(rng.standard_normal((T, d)))
+    assign = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    assign[2, 1] = -1
+    cw = rng.random((T, k)).astype(np.float32)
+    toks = np.arange(T, dtype=np.int32)
+    got = oracle.combine_rows_q8(h, q1, s1, q3, s3, q2, s2, assign, cw, toks, quant_act=False)
+    want = oracle.combine_rows(h, bf16(w1), bf16(w3), bf16(w2), assign, cw, toks)
+    assert np.array_equal(got, want)
+    # a scale that is off by one row changes the result
+    s1_bad = np.roll(s1, 1, axis=1)
+    bad = oracle.combine_rows_q8(h, q1, s1_bad, q3, s3, q2, s2, assign, cw, toks, quant_act=False)
+    assert not np.array_equal(bad, want)
+
+
+def test_e4m3_encode_inverts_decode():
+    for c in range(256):
+        if c in (0x7F, 0xFF):
+            continue
+        assert oracle.e4m3_encode(oracle.e4m3_value(c)) == c, c
+
+
+@pytest.mark.parametrize("v,code", [(1.0625, 0x38), (1.1875, 0x3A), (3 * 2.0 ** -10, 0x02),
+                                    (2.0 ** -10, 0x00), (-(2.0 ** -10), 0x80), (448.0, 0x7E),
+                                    (460.0, 0x7E), (1e30, 0x7E), (-1e30, 0xFE),
+                                    (0.3, 0x2A)])   # 0.3 = 1.2*2^-2: 0.3125 (1.25*2^-2) is nearest
+def test_e4m3_encode_ties_and_saturation(v, code):
+    """Halfway values go to the even code; magnitudes past 448 saturate."""
+    assert oracle.e4m3_encode(v) == code
+
+
+def test_e4m3_encode_matches_torch():
+    """Round-to-nearest-even against torch's float8_e4m3fn conversion (within range)."""
+    rng = np.random.default_rng(5)
+    v = np.concatenate([rng.standard_normal(20000) * 10 ** rng.uniform(-4, 2.6, 20000),
+                        rng.uniform(-448, 448, 2000)]).astype(np.float32)
+    v = v[np.abs(v) < 464]   # torch turns larger magnitudes into NaN; the encoder saturates
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(x) for x in v], np.uint8)
+    assert v.size > 15000 and np.array_equal(got, ref)
+
+
+def test_quantize_row_matches_torch():
+    rng = np.random.default_rng(6)
+    x = (rng.standard_normal(700) * 3).astype(np.float32)
+    codes, sc = oracle.quantize_row(x)
+    assert sc == np.float32(np.abs(x).max()) / np.float32(448.0)
+    ref = torch.from_numpy(x / np.float32(sc)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+    codes0, sc0 = oracle.quantize_row(np.zeros(5, np.float32))
+    assert sc0 == 1.0 and not codes0.any()

@@ -26,7 +26,7 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 moe_status_t check_config(const moe_config_t* c, bool need_ff)
 {
     if (!c) return MOE_ERR_INVALID_ARG;
-    if (c->flags != 0) return MOE_ERR_INVALID_ARG;
+    if ((c->flags & ~MOE_FLAG_FP8) != 0) return MOE_ERR_INVALID_ARG;
     if (c->T < 0 || c->E <= 0 || c->k <= 0) return MOE_ERR_INVALID_ARG;
     if (c->k > c->E) return MOE_ERR_INVALID_ARG;
     if (c->capacity < 0) return MOE_ERR_INVALID_ARG;
@@ -127,6 +127,11 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
     w.xg = take(T * k * d * 2);
     w.act = take(T * k * F * 2);
     w.y_slots = take(T * k * d * 2);
+    if (c.flags & MOE_FLAG_FP8) {
+        w.act_q = take(T * k * F);
+        w.x_scale = take(T * k * 4);
+        w.act_scale = take(T * k * 4);
+    }
     w.h_stage = take(T * d * 2);
     w.out_stage = take(T * d * 2);
     w.total = off;
@@ -279,6 +284,154 @@ GemmLaunch expert_gemm(const moe_config_t& c, const WsLayout& L, int kind, void*
 }  // namespace
 }  // namespace moe
 
+namespace moe {
+namespace {
+
+// Expert weights: bf16, or e4m3 with one fp32 scale per weight row (s13, s2 non-NULL).
+struct ExpertWeights {
+    const void* w13;
+    const void* w2;
+    const float* s13;
+    const float* s2;
+    bool fp8() const { return s13 != nullptr; }
+    void apply(GemmLaunch& g, bool gate_up) const
+    {
+        g.b_ptr = gate_up ? w13 : w2;
+        g.fp8 = fp8() ? 1 : 0;
+        g.b_scale = gate_up ? s13 : s2;
+    }
+};
+
+// The two expert GEMMs over the kept slots: gather (and, with e4m3 weights,
+// quantise per row) the token rows, gate-up + SwiGLU into act, (quantise act
+// per row,) down into y_slots.  Stage marks after the gather and after gate-up.
+moe_status_t run_experts(const moe_config_t& c, const WsLayout& L, const void* h, const int32_t* perm,
+                         const int32_t* offsets, const ExpertWeights& W, void* y_slots, void* ws,
+                         cudaStream_t s, const Ev* ev)
+{
+    const size_t rows = static_cast<size_t>(c.T) * c.k;
+    void* xg = ws_at<void>(ws, L.xg);
+    void* act = ws_at<void>(ws, L.act);
+    const int32_t* kept = offsets + c.E;   // device count of kept rows
+    if (W.fp8()) {
+        if (launch_quantize_fp8(static_cast<long long>(rows), c.d_model, h, perm, c.k, kept, xg,
+                                ws_at<float>(ws, L.x_scale), s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    } else if (launch_gather_rows(c.T, c.d_model, c.k, c.E, h, perm, offsets, xg, s) != cudaSuccess) {
+        return MOE_ERR_CUDA;
+    }
+    if (ev) ev->mark(3);
+    GemmLaunch g = expert_gemm(c, L, GK_GATEUP, ws);
+    g.a_ptr = xg;
+    W.apply(g, true);
+    g.a_scale = W.fp8() ? ws_at<float>(ws, L.x_scale) : nullptr;
+    g.offsets = offsets;
+    g.perm = perm;
+    g.act = act;
+    if (launch_gemm(g, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (ev) ev->mark(4);
+    GemmLaunch g2 = expert_gemm(c, L, GK_DOWN_SLOTS, ws);
+    g2.a_ptr = act;
+    W.apply(g2, false);
+    if (W.fp8()) {
+        void* act_q = ws_at<void>(ws, L.act_q);
+        if (launch_quantize_fp8(static_cast<long long>(rows), c.d_ff, act, nullptr, 1, kept, act_q,
+                                ws_at<float>(ws, L.act_scale), s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        g2.a_ptr = act_q;
+        g2.a_scale = ws_at<float>(ws, L.act_scale);
+    }
+    g2.offsets = offsets;
+    g2.perm = perm;
+    g2.y_slots = y_slots;
+    return cuda_status(launch_gemm(g2, s));
+}
+
+moe_status_t expert_ffn_impl(const moe_config_t* cfg, const void* h, const int32_t* perm,
+                             const int32_t* offsets, const ExpertWeights& W, void* y_slots, void* ws,
+                             size_t ws_bytes, void* stream)
+{
+    moe_status_t st = check_config(cfg, true);
+    if (st != MOE_OK) return st;
+    const void* w13 = W.w13;
+    const void* w2 = W.w2;
+    if (!h || !perm || !offsets || !w13 || !w2 || !y_slots) return MOE_ERR_INVALID_ARG;
+    if (W.fp8() && (!W.s2 || !(cfg->flags & MOE_FLAG_FP8) || cfg->d_model % 128 != 0))
+        return W.s2 && (cfg->flags & MOE_FLAG_FP8) ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+    if (!aligned(h, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(y_slots, 16))
+        return MOE_ERR_MISALIGNED;
+    WsLayout L;
+    st = check_ws(cfg, ws, ws_bytes, &L);
+    if (st != MOE_OK) return st;
+    if (cfg->T == 0) return MOE_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return run_experts(*cfg, L, h, perm, offsets, W, y_slots, ws, s, nullptr);
+}
+
+moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* h, const void* w_router,
+                                const float* bias, const float* usage, const ExpertWeights& W, void* out,
+                                float* logits_out, int32_t* assign, int32_t* slot, uint8_t* flags,
+                                int32_t* counts, float* f, float* P, void* const* stage_events, void* ws,
+                                size_t ws_bytes, void* stream)
+{
+    const void* w13 = W.w13;
+    const void* w2 = W.w2;
+    if (W.fp8() && (!(cfg->flags & MOE_FLAG_FP8) || cfg->d_model % 128 != 0))
+        return (cfg->flags & MOE_FLAG_FP8) ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_config(cfg, true);
+    if (st != MOE_OK) return st;
+    if (!h || !w_router || !w13 || !w2 || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned(h, 16) || !aligned(w_router, 16) || !aligned(w13, 16) || !aligned(w2, 16) ||
+        !aligned(out, 16))
+        return MOE_ERR_MISALIGNED;
+    WsLayout L;
+    st = check_ws(cfg, ws, ws_bytes, &L);
+    if (st != MOE_OK) return st;
+    if (cfg->T == 0) return MOE_OK;
+    const moe_config_t& c = *cfg;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Ev ev{stage_events, s};
+
+    ev.mark(0);
+    st = run_router_gemm(c, L, h, w_router, ws, s);
+    if (st != MOE_OK) return st;
+    const RouteArgs ra =
+        route_args(c, L, bias, usage, nullptr, logits_out, nullptr, nullptr, nullptr, ws);
+    // a batch of one chunk routes and dispatches in one kernel (the route stage
+    // then holds only the router GEMM, the dispatch stage both)
+    const bool small = L.nchunks == 1;
+    if (!small && launch_route(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
+    ev.mark(1);
+    DispatchOut o;
+    o.assign = assign ? assign : ws_at<int32_t>(ws, L.assign);
+    o.slot = slot ? slot : ws_at<int32_t>(ws, L.slot);
+    o.flags = flags ? flags : ws_at<uint8_t>(ws, L.flags);
+    o.counts = counts ? counts : ws_at<int32_t>(ws, L.counts);
+    o.offsets = ws_at<int32_t>(ws, L.offsets);
+    o.perm = ws_at<int32_t>(ws, L.perm);
+    o.cw = ws_at<float>(ws, L.cw);
+    o.n_rerouted = nullptr;
+    o.n_dropped = nullptr;
+    const DispatchArgs da = dispatch_args(c, L, ws_at<float>(ws, L.scores), o, ws);
+    if (cudaError_t e = small ? launch_route_dispatch_small(ra, da, s) : launch_dispatch(da, s);
+        e != cudaSuccess)
+        return MOE_ERR_CUDA;
+    st = run_stats(c, L, nullptr, f, P, ws, s);
+    if (st != MOE_OK) return st;
+    ev.mark(2);
+    st = run_experts(c, L, h, o.perm, o.offsets, W, ws_at<void>(ws, L.y_slots), ws, s, &ev);
+    if (st != MOE_OK) return st;
+    ev.mark(5);
+    if (launch_combine(c.T, c.d_model, c.k, ws_at<void>(ws, L.y_slots), o.assign, o.slot, o.offsets, o.cw,
+                       out, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    ev.mark(6);
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
 using namespace moe;
 
 extern "C" {
@@ -414,37 +567,34 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const float* scores, int32_t*
     return run_dispatch(*cfg, L, scores, o, ws, s);
 }
 
+
 moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* h, const int32_t* perm,
                             const int32_t* offsets, const void* w13, const void* w2,
                             void* y_slots, void* ws, size_t ws_bytes, void* stream)
 {
-    moe_status_t st = check_config(cfg, true);
-    if (st != MOE_OK) return st;
-    if (!h || !perm || !offsets || !w13 || !w2 || !y_slots) return MOE_ERR_INVALID_ARG;
-    if (!aligned(h, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(y_slots, 16))
-        return MOE_ERR_MISALIGNED;
-    WsLayout L;
-    st = check_ws(cfg, ws, ws_bytes, &L);
-    if (st != MOE_OK) return st;
-    if (cfg->T == 0) return MOE_OK;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    void* xg = ws_at<void>(ws, L.xg);
-    if (launch_gather_rows(cfg->T, cfg->d_model, cfg->k, cfg->E, h, perm, offsets, xg, s) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    GemmLaunch g = expert_gemm(*cfg, L, GK_GATEUP, ws);
-    g.a_ptr = xg;
-    g.b_ptr = w13;
-    g.offsets = offsets;
-    g.perm = perm;
-    g.act = ws_at<void>(ws, L.act);
-    if (launch_gemm(g, s) != cudaSuccess) return MOE_ERR_CUDA;
-    GemmLaunch g2 = expert_gemm(*cfg, L, GK_DOWN_SLOTS, ws);
-    g2.a_ptr = ws_at<void>(ws, L.act);
-    g2.b_ptr = w2;
-    g2.offsets = offsets;
-    g2.perm = perm;
-    g2.y_slots = y_slots;
-    return cuda_status(launch_gemm(g2, s));
+    return expert_ffn_impl(cfg, h, perm, offsets, ExpertWeights{w13, w2, nullptr, nullptr}, y_slots, ws,
+                           ws_bytes, stream);
+}
+
+moe_status_t moe_expert_ffn_fp8(const moe_config_t* cfg, const void* h, const int32_t* perm,
+                                const int32_t* offsets, const void* w13_q, const float* w13_scale,
+                                const void* w2_q, const float* w2_scale, void* y_slots, void* ws,
+                                size_t ws_bytes, void* stream)
+{
+    if (!w13_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
+    return expert_ffn_impl(cfg, h, perm, offsets, ExpertWeights{w13_q, w2_q, w13_scale, w2_scale}, y_slots,
+                           ws, ws_bytes, stream);
+}
+
+moe_status_t moe_quantize_fp8(int64_t rows, int32_t cols, const void* w, void* q, float* scales,
+                              void* stream)
+{
+    if (rows < 0 || cols <= 0 || cols % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!w || !q || !scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || !aligned(q, 8)) return MOE_ERR_MISALIGNED;
+    return cuda_status(
+        launch_quantize_fp8(rows, cols, w, nullptr, 1, nullptr, q, scales, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const void* y_slots, const int32_t* assign,
@@ -466,74 +616,22 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* h, const voi
                                int32_t* slot, uint8_t* flags, int32_t* counts, float* f, float* P,
                                void* const* stage_events, void* ws, size_t ws_bytes, void* stream)
 {
-    moe_status_t st = check_config(cfg, true);
-    if (st != MOE_OK) return st;
-    if (!h || !w_router || !w13 || !w2 || !out) return MOE_ERR_INVALID_ARG;
-    if (!aligned(h, 16) || !aligned(w_router, 16) || !aligned(w13, 16) || !aligned(w2, 16) ||
-        !aligned(out, 16))
-        return MOE_ERR_MISALIGNED;
-    WsLayout L;
-    st = check_ws(cfg, ws, ws_bytes, &L);
-    if (st != MOE_OK) return st;
-    if (cfg->T == 0) return MOE_OK;
-    const moe_config_t& c = *cfg;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    Ev ev{stage_events, s};
+    return layer_forward_impl(cfg, h, w_router, bias, usage, ExpertWeights{w13, w2, nullptr, nullptr}, out,
+                              logits_out, assign, slot, flags, counts, f, P, stage_events, ws, ws_bytes,
+                              stream);
+}
 
-    ev.mark(0);
-    st = run_router_gemm(c, L, h, w_router, ws, s);
-    if (st != MOE_OK) return st;
-    const RouteArgs ra =
-        route_args(c, L, bias, usage, nullptr, logits_out, nullptr, nullptr, nullptr, ws);
-    // a batch of one chunk routes and dispatches in one kernel (the route stage
-    // then holds only the router GEMM, the dispatch stage both)
-    const bool small = L.nchunks == 1;
-    if (!small && launch_route(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
-    ev.mark(1);
-    DispatchOut o;
-    o.assign = assign ? assign : ws_at<int32_t>(ws, L.assign);
-    o.slot = slot ? slot : ws_at<int32_t>(ws, L.slot);
-    o.flags = flags ? flags : ws_at<uint8_t>(ws, L.flags);
-    o.counts = counts ? counts : ws_at<int32_t>(ws, L.counts);
-    o.offsets = ws_at<int32_t>(ws, L.offsets);
-    o.perm = ws_at<int32_t>(ws, L.perm);
-    o.cw = ws_at<float>(ws, L.cw);
-    o.n_rerouted = nullptr;
-    o.n_dropped = nullptr;
-    const DispatchArgs da = dispatch_args(c, L, ws_at<float>(ws, L.scores), o, ws);
-    if (cudaError_t e = small ? launch_route_dispatch_small(ra, da, s) : launch_dispatch(da, s);
-        e != cudaSuccess)
-        return MOE_ERR_CUDA;
-    st = run_stats(c, L, nullptr, f, P, ws, s);
-    if (st != MOE_OK) return st;
-    ev.mark(2);
-    void* xg = ws_at<void>(ws, L.xg);
-    if (launch_gather_rows(c.T, c.d_model, c.k, c.E, h, o.perm, o.offsets, xg, s) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    ev.mark(3);
-    GemmLaunch g = expert_gemm(c, L, GK_GATEUP, ws);
-    g.a_ptr = xg;
-    g.b_ptr = w13;
-    g.offsets = o.offsets;
-    g.perm = o.perm;
-    g.act = ws_at<void>(ws, L.act);
-    if (launch_gemm(g, s) != cudaSuccess) return MOE_ERR_CUDA;
-    ev.mark(4);
-    // expert outputs in slot order (bf16), then each token's kept outputs
-    // weighted and summed in rank order (fp32)
-    GemmLaunch g2 = expert_gemm(c, L, GK_DOWN_SLOTS, ws);
-    g2.a_ptr = ws_at<void>(ws, L.act);
-    g2.b_ptr = w2;
-    g2.offsets = o.offsets;
-    g2.perm = o.perm;
-    g2.y_slots = ws_at<void>(ws, L.y_slots);
-    if (launch_gemm(g2, s) != cudaSuccess) return MOE_ERR_CUDA;
-    ev.mark(5);
-    if (launch_combine(c.T, c.d_model, c.k, ws_at<void>(ws, L.y_slots), o.assign, o.slot, o.offsets, o.cw,
-                       out, s) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    ev.mark(6);
-    return MOE_OK;
+moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* h, const void* w_router,
+                                   const float* bias, const float* usage, const void* w13_q,
+                                   const float* w13_scale, const void* w2_q, const float* w2_scale,
+                                   void* out, float* logits_out, int32_t* assign, int32_t* slot,
+                                   uint8_t* flags, int32_t* counts, float* f, float* P,
+                                   void* const* stage_events, void* ws, size_t ws_bytes, void* stream)
+{
+    if (!w13_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
+    return layer_forward_impl(cfg, h, w_router, bias, usage, ExpertWeights{w13_q, w2_q, w13_scale, w2_scale},
+                              out, logits_out, assign, slot, flags, counts, f, P, stage_events, ws, ws_bytes,
+                              stream);
 }
 
 moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* h_host,

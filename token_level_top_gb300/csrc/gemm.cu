@@ -44,6 +44,8 @@ struct GemmParams {
     int kb_per_split;  // router K blocks per split
     int stages;
     int gather4;       // gate-up: A rows gathered from h with tile::gather4 (else tiled from x_perm)
+    const float* b_scale;  // FP8: the scale of each weight row (output channel)
+    const float* a_scale;  // FP8: the scale of each activation row (slot order)
     uint32_t tmem_cols;
     const int32_t* offsets;
     const int32_t* perm;
@@ -101,7 +103,13 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile,
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
 
-template <bool PAIR>
+// FP8: e4m3 activations and weights on tcgen05.mma.kind::f8f6f4.  A stage
+// row is 128 bytes either way (64 bf16 or 128 e4m3 values), so the tiles,
+// swizzle and descriptors are the bf16 ones; each MMA covers 32 bytes of K.
+// The per-row activation scale and per-row weight scale multiply the
+// accumulator in the epilogue.
+
+template <bool PAIR, bool FP8>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p)
@@ -176,7 +184,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (PAIR) cluster_sync_all();   // the peer's barriers exist before anything targets them
     const uint32_t tmem_base = *s_tmem;
     const int total_tiles = (p.kind == GK_ROUTER) ? p.m_tiles * p.splits : s_tile_start[p.E];
-    const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, p.bn);
+    const uint32_t idesc = FP8 ? idesc_e4m3_f32(PAIR ? 2 * kBM : kBM, p.bn)
+                               : idesc_bf16_f32(PAIR ? 2 * kBM : kBM, p.bn);
     const bool leader = rank == 0;   // the paired MMAs are issued by CTA 0 of the cluster
     // a cluster's two CTAs walk the same tile sequence
     const int tile0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
@@ -224,7 +233,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     mbar_arrive_expect_tx(smem_u32(&full_bar[stage]),
                                           (PAIR ? 2u : 1u) * (a_bytes + b_bytes));
                 __syncwarp();
-                const int x = kb * kBK;
+                const int x = kb * (FP8 ? 2 * kBK : kBK);   // K elements of a 128-byte row
                 const uint32_t dA = smem_u32(sA + stage * a_bytes);
                 const uint32_t dB = smem_u32(sB + stage * b_bytes);
                 if (PAIR) {
@@ -287,10 +296,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int k = 0; k < kBK / 16; ++k) {
                         const uint64_t ad = sdesc_k_sw128(a0 + k * 32), bd = sdesc_k_sw128(b0 + k * 32);
                         const uint32_t acc = (kb > ti.kb0 || k > 0) ? 1u : 0u;
-                        if (PAIR)
-                            mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
-                        else
-                            mma_bf16(d_tmem, ad, bd, idesc, acc);
+                        if (FP8) {
+                            if (PAIR)
+                                mma_e4m3_pair(d_tmem, ad, bd, idesc, acc);
+                            else
+                                mma_e4m3(d_tmem, ad, bd, idesc, acc);
+                        } else {
+                            if (PAIR)
+                                mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
+                            else
+                                mma_bf16(d_tmem, ad, bd, idesc, acc);
+                        }
                     }
                     if (PAIR)   // frees the slot in both CTAs
                         mma_commit_pair(smem_u32(&empty_bar[stage]));
@@ -349,10 +365,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int ri = ti.m * kBM + row;
                 uint32_t u[32];
                 __nv_bfloat16* dst = p.act + static_cast<size_t>(off + ri) * p.F + ti.n * (kExpertBN / 2);
+                // FP8: the scales of the tile's W1 and W3 rows (packed rows of W13)
+                // and of this thread's activation row
+                const float* gsc = FP8 ? p.b_scale + static_cast<size_t>(ti.e) * 2 * p.F + ti.n * kExpertBN : nullptr;
+                const float asc = (FP8 && ri < cnt) ? p.a_scale[off + ri] : 0.0f;
                 for (int c = 0; c < kExpertBN / 2; c += 32) {
                     tmem_ld32(taddr + c, v);                   // gate columns
                     tmem_ld32(taddr + kExpertBN / 2 + c, u);   // matching up columns
                     tmem_ld_wait2(v, u);
+                    if (FP8) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            v[j] = __float_as_uint(__uint_as_float(v[j]) * asc * __ldg(gsc + c + j));
+                            u[j] = __float_as_uint(__uint_as_float(u[j]) * asc * __ldg(gsc + kExpertBN / 2 + c + j));
+                        }
+                    }
                     if (ri < cnt) {
                         uint32_t pk[16];
 #pragma unroll
@@ -376,10 +403,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int slot = off + ri;
                 const int col0 = ti.n * p.bn;
                 __nv_bfloat16* dst = p.y_slots + static_cast<size_t>(slot) * p.d + col0;
+                const float* dsc = FP8 ? p.b_scale + static_cast<size_t>(ti.e) * p.d + col0 : nullptr;
+                const float asc = (FP8 && valid) ? p.a_scale[slot] : 0.0f;
                 for (int c = 0; c < p.bn; c += 32) {
                     if (col0 + c >= p.d) break;
                     tmem_ld32(taddr + c, v);
                     tmem_ld_wait(v);
+                    if (FP8) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + c + j < p.d)
+                                v[j] = __float_as_uint(__uint_as_float(v[j]) * asc * __ldg(dsc + c + j));
+                    }
                     if (valid) {
                         uint32_t pk[16];
 #pragma unroll
@@ -446,6 +481,22 @@ bool make_map(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, ui
     return r == CUDA_SUCCESS;
 }
 
+// 2-D e4m3 (byte) tensor [rows, cols] (row-major), box [box_rows, 128]: the
+// same 128-byte rows and swizzle as the bf16 boxes.
+bool make_map_e4m3(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows)
+{
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t gdim[2] = {cols, rows};
+    cuuint64_t gstride[1] = {cols};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(2 * kBK), box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), gdim, gstride, box,
+                     estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 uint32_t pow2_cols(int n)
 {
     uint32_t c = 32;
@@ -491,10 +542,18 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     p.budget = g.budget;
 
     CUtensorMap tmA, tmB;
+    // FP8: e4m3 activations and weights, each row with its scale
+    const bool fp8 = g.fp8 && g.kind != GK_ROUTER;
+    p.b_scale = fp8 ? g.b_scale : nullptr;
+    p.a_scale = fp8 ? g.a_scale : nullptr;
+    const int kstep = fp8 ? 2 * kBK : kBK;   // K elements per 128-byte stage row
+    auto map = [&](CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+        return fp8 ? make_map_e4m3(tm, ptr, rows, cols, box_rows) : make_map(tm, ptr, rows, cols, box_rows);
+    };
     int grid = 0;
     const int sms = num_sms();
     // Row tiles are paired when the experts average at least two of them.
-    const bool pair = (g.kind != GK_ROUTER) && !g.gather4 &&
+    const bool pair = (g.kind != GK_ROUTER) && !g.gather4 && !(fp8 && g.gather4) &&
                       static_cast<long long>(g.T) * g.topk >= 2LL * kBM * g.E;
     if (g.kind == GK_ROUTER) {
         p.bn = g.epad;
@@ -507,18 +566,18 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
         if (!make_map(&tmB, g.b_ptr, g.E, g.d, p.bn)) return cudaErrorInvalidValue;
         grid = std::min(p.m_tiles * p.splits, router_ctas_per_sm(g.E) * sms);
     } else if (g.kind == GK_GATEUP) {
+        if (fp8 && g.gather4) return cudaErrorInvalidValue;
         p.bn = kExpertBN;
-        p.kb_total = g.d / kBK;
+        p.kb_total = g.d / kstep;
         p.n_tiles = g.F / (kExpertBN / 2);
         p.gather4 = g.gather4;
         if (g.gather4) {
             if (!make_map(&tmA, g.a_ptr, g.T, g.d, 1)) return cudaErrorInvalidValue;
         } else {
-            if (!make_map(&tmA, g.a_ptr, static_cast<uint64_t>(g.T) * g.topk, g.d, kBM))
+            if (!map(&tmA, g.a_ptr, static_cast<uint64_t>(g.T) * g.topk, g.d, kBM))
                 return cudaErrorInvalidValue;
         }
-        if (!make_map(&tmB, g.b_ptr, static_cast<uint64_t>(g.E) * 2 * g.F, g.d,
-                      pair ? kExpertBN / 2 : kExpertBN))
+        if (!map(&tmB, g.b_ptr, static_cast<uint64_t>(g.E) * 2 * g.F, g.d, pair ? kExpertBN / 2 : kExpertBN))
             return cudaErrorInvalidValue;
         const long long mt_max = (static_cast<long long>(g.T) * g.topk + kBM - 1) / kBM + g.E;
         grid = static_cast<int>(std::min<long long>(mt_max * p.n_tiles, sms));
@@ -539,11 +598,11 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
                 }
             }
         }
-        p.kb_total = g.F / kBK;
+        p.kb_total = g.F / kstep;
         p.n_tiles = (g.d + p.bn - 1) / p.bn;
-        if (!make_map(&tmA, g.a_ptr, static_cast<uint64_t>(g.T) * g.topk, g.F, kBM))
+        if (!map(&tmA, g.a_ptr, static_cast<uint64_t>(g.T) * g.topk, g.F, kBM))
             return cudaErrorInvalidValue;
-        if (!make_map(&tmB, g.b_ptr, static_cast<uint64_t>(g.E) * g.d, g.F, pair ? p.bn / 2 : p.bn))
+        if (!map(&tmB, g.b_ptr, static_cast<uint64_t>(g.E) * g.d, g.F, pair ? p.bn / 2 : p.bn))
             return cudaErrorInvalidValue;
         const long long mt_max = (static_cast<long long>(g.T) * g.topk + kBM - 1) / kBM + g.E;
         grid = static_cast<int>(std::min<long long>(mt_max * p.n_tiles, sms));
@@ -561,16 +620,25 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(moe_gemm_kernel<false>,
+        attr_err = cudaFuncSetAttribute(moe_gemm_kernel<false, false>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(moe_gemm_kernel<true>,
+            attr_err = cudaFuncSetAttribute(moe_gemm_kernel<true, false>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(moe_gemm_kernel<false, true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(moe_gemm_kernel<true, true>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (grid <= 0) return cudaSuccess;
     if (!pair) {
-        moe_gemm_kernel<false><<<grid, kGemmThreads, smem, s>>>(tmA, tmB, p);
+        if (fp8)
+            moe_gemm_kernel<false, true><<<grid, kGemmThreads, smem, s>>>(tmA, tmB, p);
+        else
+            moe_gemm_kernel<false, false><<<grid, kGemmThreads, smem, s>>>(tmA, tmB, p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -591,14 +659,15 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     int max_clusters = (dev >= 0 && dev < 64) ? cached_clusters[dev] : 0;
     if (max_clusters <= 0) {
         cfg.gridDim = dim3(2 * 64, 1, 1);
-        if (cudaOccupancyMaxActiveClusters(&max_clusters, moe_gemm_kernel<true>, &cfg) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveClusters(&max_clusters, fp8 ? moe_gemm_kernel<true, true> : moe_gemm_kernel<true, false>, &cfg) != cudaSuccess ||
             max_clusters <= 0)
             max_clusters = sms / 2;
         if (dev >= 0 && dev < 64) cached_clusters[dev] = max_clusters;
     }
     const int clusters = std::max(1, std::min(grid / 2, max_clusters));
     cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
-    return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<true>, tmA, tmB, p);
+    return fp8 ? cudaLaunchKernelEx(&cfg, moe_gemm_kernel<true, true>, tmA, tmB, p)
+               : cudaLaunchKernelEx(&cfg, moe_gemm_kernel<true, false>, tmA, tmB, p);
 }
 
 }  // namespace moe

@@ -27,6 +27,9 @@ struct WsLayout {
     size_t status = 0, ctrl = 0, part = 0, scores = 0, ids = 0, prefs = 0, crank = 0, hist = 0,
            base = 0, ppart = 0, assign = 0, slot = 0, flags = 0, counts = 0, offsets = 0,
            perm = 0, cw = 0, xg = 0, act = 0, y_slots = 0, h_stage = 0, out_stage = 0;
+    // MOE_FLAG_FP8: e4m3 activation rows of the down GEMM and the row scales
+    // of both GEMMs' activations (the gate-up codes reuse the xg region)
+    size_t act_q = 0, x_scale = 0, act_scale = 0;
     size_t total = 0;
 };
 
@@ -127,6 +130,9 @@ struct GemmLaunch {
     int splits, epad;
     int gather4;  // gate-up: gather A rows from h (a_ptr = h) instead of tiles of x_perm
     long long rows_cap;  // most rows an expert can hold (the capacity C), or 0 if unknown
+    int fp8;                 // expert GEMMs: a_ptr and b_ptr hold e4m3 rows, each with
+    const float* a_scale;    //   its scale: a_scale per activation row (slot order),
+    const float* b_scale;    //   b_scale per weight row (W13: [E*2F], W2: [E*d])
     int* status;
     long long budget;
 };
@@ -140,6 +146,11 @@ cudaError_t launch_gather_rows(int T, int d, int k, int E, const void* h, const 
 cudaError_t launch_combine(int T, int d, int k, const void* y_slots, const int32_t* assign,
                            const int32_t* slot, const int32_t* offsets, const float* cw, void* out,
                            cudaStream_t s);
+// Per-row e4m3 quantisation of rows [0, rows) (bf16 [.., cols] -> codes + scales);
+// row r reads source row perm[r] / k when perm is not NULL; rows from *nrows
+// on are skipped when nrows is not NULL.
+cudaError_t launch_quantize_fp8(long long rows, int cols, const void* w, const int32_t* perm, int k,
+                                const int32_t* nrows, void* q, float* scales, cudaStream_t s);
 cudaError_t launch_timeout_probe(int* status, long long budget, cudaStream_t s);
 
 }  // namespace moe

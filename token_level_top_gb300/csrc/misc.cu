@@ -110,6 +110,54 @@ __global__ void gather_rows_kernel(int rows_max, int d8, int k, int E, const uin
     }
 }
 
+// Per-row FP8 (e4m3) quantisation, one warp per row:
+//   s[r] = max_c |w[r,c]| / 448 (448: the largest finite e4m3; 1 for an all-zero row),
+//   q[r,c] = e4m3(w[r,c] / s[r]), round to nearest even, saturated to +-448.
+// Row r reads source row perm[r] / k when perm is given (the token rows of
+// the kept slots), else row r; rows from *nrows on are skipped when nrows is
+// given (a device-side count).
+__global__ void quantize_fp8_kernel(long long rows, int cols, const uint4* __restrict__ w,
+                                    const int32_t* __restrict__ perm, int k,
+                                    const int32_t* __restrict__ nrows, uint2* __restrict__ q,
+                                    float* __restrict__ scales)
+{
+    const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= rows || (nrows && row >= *nrows)) return;   // whole warps
+    const int lane = threadIdx.x & 31;
+    const int c8 = cols / 8;
+    const long long srow = perm ? perm[row] / k : row;
+    const uint4* wr = w + srow * c8;
+    float amax = 0.0f;
+    for (int c = lane; c < c8; c += 32) {
+        const uint4 v = wr[c];
+        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&words[j]);
+            amax = fmaxf(amax, fmaxf(fabsf(__bfloat162float(b.x)), fabsf(__bfloat162float(b.y))));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+    if (lane == 0) scales[row] = sc;
+    uint2* qr = q + row * c8;
+    for (int c = lane; c < c8; c += 32) {
+        const uint4 v = wr[c];
+        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+        uint32_t packed[2] = {0, 0};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&words[j]);
+            const float x0 = __bfloat162float(b.x) / sc, x1 = __bfloat162float(b.y) / sc;
+            uint16_t two;   // element x0 in the low byte
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(two) : "f"(x1), "f"(x0));
+            packed[j >> 1] |= static_cast<uint32_t>(two) << (16 * (j & 1));
+        }
+        qr[c] = make_uint2(packed[0], packed[1]);
+    }
+}
+
 // One thread waits on an mbarrier that nothing will ever complete, with the
 // library's bounded wait; when the budget runs out it records the timeout.
 __global__ void timeout_probe_kernel(int* status, long long budget)
@@ -169,6 +217,16 @@ cudaError_t launch_combine(int T, int d, int k, const void* y_slots, const int32
     else
         combine_kernel<1><<<grid, 32 * per_block, 0, s>>>(T, d, k, static_cast<const uint4*>(y_slots), assign,
                                                            slot, offsets, cw, static_cast<uint4*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_fp8(long long rows, int cols, const void* w, const int32_t* perm, int k,
+                                const int32_t* nrows, void* q, float* scales, cudaStream_t s)
+{
+    if (rows <= 0) return cudaSuccess;
+    const int per_block = 8;
+    quantize_fp8_kernel<<<static_cast<unsigned>((rows + per_block - 1) / per_block), 32 * per_block, 0, s>>>(
+        rows, cols, static_cast<const uint4*>(w), perm, k, nrows, static_cast<uint2*>(q), scales);
     return cudaGetLastError();
 }
 

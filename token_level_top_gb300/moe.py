@@ -48,10 +48,11 @@ class Config:
     cf: float = 1.25
     capacity: int = 0
     lam: float = 0.0
+    flags: int = 0   # FLAG_FP8: the workspace also serves the e4m3 (FP8) entry points
 
     def c(self) -> MoEConfig:
         return MoEConfig(self.T, self.d_model, self.E, self.k, self.d_ff, float(self.cf),
-                         int(self.capacity), float(self.lam), 0)
+                         int(self.capacity), float(self.lam), int(self.flags))
 
     @classmethod
     def of(cls, shape, **kw):
@@ -60,6 +61,8 @@ class Config:
         d.update(kw)
         return cls(**d)
 
+
+FLAG_FP8 = 1   # MOE_FLAG_FP8
 
 _lib = None
 
@@ -83,6 +86,9 @@ _SIGS = {
     "moe_layer_forward_host": (I32, [CFG, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_debug_timeout_probe": (I32, [P, SZ, ctypes.c_int64, P]),
     "moe_dispatch_static": (I32, [CFG, P, P, P, P, P, P, P, P, P, P, P, P]),
+    "moe_quantize_fp8": (I32, [ctypes.c_int64, I32, P, P, P, P]),
+    "moe_expert_ffn_fp8": (I32, [CFG, P, P, P, P, P, P, P, P, P, SZ, P]),
+    "moe_layer_forward_fp8": (I32, [CFG] + [P] * 18 + [SZ, P]),
 }
 
 
@@ -159,6 +165,23 @@ def pack_w13(w1: torch.Tensor, w3: torch.Tensor) -> torch.Tensor:
     return w13
 
 
+def quantize_fp8(w: torch.Tensor):
+    """Per-row e4m3 quantisation (moe_quantize_fp8) of a bf16 tensor [..., cols]:
+    returns (q uint8, same shape; scales fp32, one per row)."""
+    w = w.contiguous()
+    cols = w.shape[-1]
+    rows = w.numel() // cols
+    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    sc = torch.empty(rows, dtype=torch.float32, device=w.device)
+    _check(lib().moe_quantize_fp8(rows, cols, _p(w), _p(q), _p(sc), _stream()), "moe_quantize_fp8")
+    return q, sc
+
+
+def _fp8(w):
+    """Expert weights as (q, scales) from quantize_fp8, or None for bf16 weights."""
+    return w if isinstance(w, tuple) else None
+
+
 def route(cfg: Config, ws, h=None, wr=None, bias=None, usage=None, logits_in=None):
     dev = ws.device
     T, E, k = cfg.T, cfg.E, cfg.k
@@ -202,8 +225,13 @@ def dispatch(cfg: Config, ws, scores):
 def expert_ffn(cfg: Config, ws, h, perm, offsets, w13, w2):
     y = torch.empty(max(cfg.T * cfg.k, 1), cfg.d_model, dtype=torch.bfloat16, device=ws.device)
     c = cfg.c()
-    st = lib().moe_expert_ffn(ctypes.byref(c), _p(h), _p(perm), _p(offsets), _p(w13), _p(w2), _p(y),
-                              _p(ws), ws.numel(), _stream())
+    if _fp8(w13):
+        (q13, s13), (q2, s2) = w13, w2
+        st = lib().moe_expert_ffn_fp8(ctypes.byref(c), _p(h), _p(perm), _p(offsets), _p(q13), _p(s13),
+                                      _p(q2), _p(s2), _p(y), _p(ws), ws.numel(), _stream())
+    else:
+        st = lib().moe_expert_ffn(ctypes.byref(c), _p(h), _p(perm), _p(offsets), _p(w13), _p(w2), _p(y),
+                                  _p(ws), ws.numel(), _stream())
     _check(st, "moe_expert_ffn")
     return y
 
@@ -219,7 +247,8 @@ def combine(cfg: Config, y_slots, assign, slot, offsets, cw):
 
 def layer_forward(cfg: Config, ws, h, wr, w13, w2, bias=None, usage=None, aux=False,
                   stage_events=None, out=None):
-    """The fused layer.  Returns out [T, d] bf16 (and a dict of routing outputs when aux)."""
+    """The fused layer.  Returns out [T, d] bf16 (and a dict of routing outputs when aux).
+    w13 / w2: bf16 tensors, or (q, scales) pairs from quantize_fp8 for e4m3 weights."""
     dev = ws.device
     T, E, k = cfg.T, cfg.E, cfg.k
     if out is None:
@@ -242,11 +271,16 @@ def layer_forward(cfg: Config, ws, h, wr, w13, w2, bias=None, usage=None, aux=Fa
                                                         for e in stage_events])
     g = (lambda n: _p(extras[n]) if extras else None)
     c = cfg.c()
-    st = lib().moe_layer_forward(ctypes.byref(c), _p(h), _p(wr), _p(bias), _p(usage), _p(w13),
-                                 _p(w2), _p(out), g("logits"), g("assign"), g("slot"), g("flags"),
-                                 g("counts"), g("f"), g("P"),
-                                 ctypes.cast(ev_arr, ctypes.c_void_p) if ev_arr is not None else None,
-                                 _p(ws), ws.numel(), _stream())
+    evp = ctypes.cast(ev_arr, ctypes.c_void_p) if ev_arr is not None else None
+    tail = (_p(out), g("logits"), g("assign"), g("slot"), g("flags"), g("counts"), g("f"), g("P"), evp,
+            _p(ws), ws.numel(), _stream())
+    if _fp8(w13):   # e4m3 expert weights: (q, scales) pairs from quantize_fp8
+        (q13, s13), (q2, s2) = w13, w2
+        st = lib().moe_layer_forward_fp8(ctypes.byref(c), _p(h), _p(wr), _p(bias), _p(usage), _p(q13),
+                                         _p(s13), _p(q2), _p(s2), *tail)
+    else:
+        st = lib().moe_layer_forward(ctypes.byref(c), _p(h), _p(wr), _p(bias), _p(usage), _p(w13),
+                                     _p(w2), *tail)
     _check(st, "moe_layer_forward")
     return (out, extras) if aux else out
 

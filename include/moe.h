@@ -165,12 +165,13 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* h_dev, const in
                             const int32_t* offsets_dev, const void* w13_dev, const void* w2_dev,
                             void* y_slots_dev, void* ws_dev, size_t ws_bytes, void* stream);
 
-/* FP8 expert weights.  The pages quantise expert weights to cut the bytes
- * moved ([2kiu] §5.1: INT4/INT6 per expert; [cnnetsun] §3.2: INT8, where the
- * dequantisation cost ate the gain -- the bottleneck is moving data).  This
- * library's form: e4m3 with one fp32 scale per weight row (output channel);
- * the kernels stream the 8-bit tiles and widen them to bf16 in shared memory
- * behind the copies; activations stay bf16.
+/* FP8 expert path.  The pages quantise expert weights to cut the bytes moved
+ * ([2kiu] §5.1: INT4/INT6 per expert; [cnnetsun] §3.2: INT8, where a
+ * dequantisation step ate the gain -- the bottleneck is moving data).  This
+ * library's form runs the expert GEMMs in e4m3 on the tensor cores, with no
+ * dequantisation pass: weights are quantised once per row (output channel),
+ * token rows and activation rows per row on the fly, the products accumulate
+ * in fp32 and the two row scales multiply the result.
  *
  * Per-row quantisation of a bf16 matrix w_dev [rows, cols] (row-major, cols a
  * multiple of 8; w_dev 16-byte aligned, q_dev 8-byte aligned):
@@ -182,9 +183,14 @@ moe_status_t moe_expert_ffn(const moe_config_t* cfg, const void* h_dev, const in
 moe_status_t moe_quantize_fp8(int64_t rows, int32_t cols, const void* w_dev, void* q_dev,
                               float* scales_dev, void* stream);
 
-/* moe_expert_ffn with e4m3 weights: w13_q_dev [E, 2F, d] and w2_q_dev
- * [E, d, F] from moe_quantize_fp8, w13_scale_dev [E*2F], w2_scale_dev [E*d]
- * fp32.  Weight W = q * scale (per row); everything else as moe_expert_ffn. */
+/* moe_expert_ffn in e4m3: w13_q_dev [E, 2F, d] and w2_q_dev [E, d, F] from
+ * moe_quantize_fp8 with w13_scale_dev [E*2F] and w2_scale_dev [E*d] (weight =
+ * code * row scale).  Each kept slot's token row is quantised per row the same
+ * way, as is each activation row silu(g)*u (after rounding to bf16); both
+ * GEMMs multiply e4m3 codes (tcgen05.mma.kind::f8f6f4, fp32 accumulate) and
+ * scale by the activation row's and the weight row's scales.  Needs
+ * cfg->flags & MOE_FLAG_FP8 (MOE_ERR_INVALID_ARG otherwise) and d a multiple
+ * of 128 (MOE_ERR_UNSUPPORTED otherwise); y_slots as moe_expert_ffn. */
 moe_status_t moe_expert_ffn_fp8(const moe_config_t* cfg, const void* h_dev, const int32_t* perm_dev,
                                 const int32_t* offsets_dev, const void* w13_q_dev,
                                 const float* w13_scale_dev, const void* w2_q_dev,
@@ -221,8 +227,10 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* h_dev,
                                float* f_dev, float* P_dev, void* const* stage_events,
                                void* ws_dev, size_t ws_bytes, void* stream);
 
-/* moe_layer_forward with e4m3 expert weights (as moe_expert_ffn_fp8); the
- * router weights stay bf16. */
+/* moe_layer_forward with the expert GEMMs in e4m3 (as moe_expert_ffn_fp8);
+ * routing, dispatch and the combine are unchanged (the router GEMM stays
+ * bf16).  Stage events as moe_layer_forward; the down stage includes the
+ * activation quantisation. */
 moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* h_dev,
                                    const void* w_router_dev, const float* bias_dev,
                                    const float* usage_dev, const void* w13_q_dev,

@@ -393,8 +393,9 @@ def run_ours(args, rank, world, local):
         roof = {"bound": "hbm", "achieved": bytes_[dom] / sec / 1e9, "peak": peak_bw,
                 "unit": "GB/s", "peak_kind": f"{peak_kind} HBM copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = recorded_traffic(f"moe_gemm_kernel ({dom.replace('_', '-')})", shape.name)
-    roof["kernel"] = f"moe_gemm_kernel ({dom.replace('_', '-')})"
+    kname = f"moe_gemm_kernel ({dom.replace('_', '-')}{', e4m3' if fp8 else ''})"
+    roof["traffic"] = recorded_traffic(kname, shape.name)
+    roof["kernel"] = kname
     roof["algorithmic_per_launch"] = {"flop": flops[dom], "bytes": bytes_[dom]}
     expert_tflops = (flops["gate_up"] + flops["down"]) / (
         (stage_ms["gate_up"] + stage_ms["down"]) * 1e-3) / 1e12

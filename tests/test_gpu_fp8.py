@@ -36,11 +36,35 @@ def quantized(Ld, shape):
     return (q13, s13), (q2, s2), ora
 
 
-@pytest.mark.parametrize("rows,cols", [(7, 64), (300, 512), (1000, 4096)])
+@pytest.mark.parametrize("rows,cols", [(7, 64), (300, 512), (1000, 4096), (3000, 512), (50, 6144),
+                                       (20, 8192), (33, 14336), (3, 65664)])
 def test_quantize_fp8_matches_torch(rows, cols):
     g = torch.Generator().manual_seed(rows + cols)
     w = (torch.randn(rows, cols, generator=g) * torch.rand(rows, 1, generator=g) * 3).to(torch.bfloat16)
     w[1] = 0   # an all-zero row: scale 1, codes 0
+    q, s = moe.quantize_fp8(w.cuda())
+    wf = w.float()
+    amax = wf.abs().amax(dim=1)
+    s_ref = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    assert torch.equal(s.cpu(), s_ref)
+    q_ref = (wf / s_ref[:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert torch.equal(q.cpu(), q_ref)
+
+
+def test_quantize_fp8_every_bf16_value():
+    """Each row holds every finite bf16 value of magnitude at most its maximum
+    (both signs; the rest zeros), at scales where some quotients land within a
+    few fp32 ulps of an e4m3 rounding midpoint: the codes must still be those
+    of the correctly rounded quotient."""
+    pos = (np.arange(0, 0x7F80, dtype=np.uint32) << 16).view(np.float32)
+    amaxes = [1.0, 3.0, 0.1, 100.5, 7e-3, 448.0, 1e-30, 2.5e5, 0.3, 1e-38]
+    cols = 40960
+    w = torch.zeros(len(amaxes), cols, dtype=torch.bfloat16)
+    for i, a in enumerate(amaxes):
+        a = torch.tensor(a).to(torch.bfloat16).float().item()
+        x = pos[pos <= a]
+        row = torch.from_numpy(np.concatenate([x, -x])).to(torch.bfloat16)
+        w[i, :row.numel()] = row
     q, s = moe.quantize_fp8(w.cuda())
     wf = w.float()
     amax = wf.abs().amax(dim=1)

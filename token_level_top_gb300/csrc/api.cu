@@ -131,6 +131,7 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
         w.act_q = take(T * k * F);
         w.x_scale = take(T * k * 4);
         w.act_scale = take(T * k * 4);
+        w.act_amax = take(T * k * 4);
     }
     w.h_stage = take(T * d * 2);
     w.out_stage = take(T * d * 2);
@@ -315,7 +316,8 @@ moe_status_t run_experts(const moe_config_t& c, const WsLayout& L, const void* h
     const int32_t* kept = offsets + c.E;   // device count of kept rows
     if (W.fp8()) {
         if (launch_quantize_fp8(static_cast<long long>(rows), c.d_model, h, perm, c.k, kept, xg,
-                                ws_at<float>(ws, L.x_scale), s) != cudaSuccess)
+                                ws_at<float>(ws, L.x_scale), s, nullptr, ws_at<float>(ws, L.act_amax)) !=
+            cudaSuccess)
             return MOE_ERR_CUDA;
     } else if (launch_gather_rows(c.T, c.d_model, c.k, c.E, h, perm, offsets, xg, s) != cudaSuccess) {
         return MOE_ERR_CUDA;
@@ -325,6 +327,7 @@ moe_status_t run_experts(const moe_config_t& c, const WsLayout& L, const void* h
     g.a_ptr = xg;
     W.apply(g, true);
     g.a_scale = W.fp8() ? ws_at<float>(ws, L.x_scale) : nullptr;
+    g.act_amax = W.fp8() ? ws_at<float>(ws, L.act_amax) : nullptr;   // zeroed by the pass above
     g.offsets = offsets;
     g.perm = perm;
     g.act = act;
@@ -336,7 +339,7 @@ moe_status_t run_experts(const moe_config_t& c, const WsLayout& L, const void* h
     if (W.fp8()) {
         void* act_q = ws_at<void>(ws, L.act_q);
         if (launch_quantize_fp8(static_cast<long long>(rows), c.d_ff, act, nullptr, 1, kept, act_q,
-                                ws_at<float>(ws, L.act_scale), s) != cudaSuccess)
+                                ws_at<float>(ws, L.act_scale), s, ws_at<float>(ws, L.act_amax)) != cudaSuccess)
             return MOE_ERR_CUDA;
         g2.a_ptr = act_q;
         g2.a_scale = ws_at<float>(ws, L.act_scale);

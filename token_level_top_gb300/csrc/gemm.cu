@@ -46,6 +46,7 @@ struct GemmParams {
     int gather4;       // gate-up: A rows gathered from h with tile::gather4 (else tiled from x_perm)
     const float* b_scale;  // FP8: the scale of each weight row (output channel)
     const float* a_scale;  // FP8: the scale of each activation row (slot order)
+    float* act_amax;       // FP8 gate-up: per activation row, atomically maxed with max |bf16 act|
     uint32_t tmem_cols;
     const int32_t* offsets;
     const int32_t* perm;
@@ -369,6 +370,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 // and of this thread's activation row
                 const float* gsc = FP8 ? p.b_scale + static_cast<size_t>(ti.e) * 2 * p.F + ti.n * kExpertBN : nullptr;
                 const float asc = (FP8 && ri < cnt) ? p.a_scale[off + ri] : 0.0f;
+                float rmax = 0.0f;   // FP8: max |act| over this thread's columns
                 for (int c = 0; c < kExpertBN / 2; c += 32) {
                     tmem_ld32(taddr + c, v);                   // gate columns
                     tmem_ld32(taddr + kExpertBN / 2 + c, u);   // matching up columns
@@ -388,6 +390,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             const float a1 =
                                 silu_f(__uint_as_float(v[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
                             pk[j] = pack_bf16x2(a0, a1);
+                            if (FP8) rmax = fmaxf(rmax, fmaxf(fabsf(a0), fabsf(a1)));
                         }
                         uint4* d4 = reinterpret_cast<uint4*>(dst + c);
 #pragma unroll
@@ -395,6 +398,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                     }
                 }
+                // The row maximum the activation quantiser needs, so that it
+                // reads each row once: rounding to bf16 is monotone, so the
+                // largest stored |value| is the rounded largest |value|; the
+                // bits of non-negative floats order as the floats do.
+                if (FP8 && p.act_amax && ri < cnt)
+                    atomicMax(reinterpret_cast<unsigned int*>(p.act_amax + off + ri),
+                              __float_as_uint(__bfloat162float(__float2bfloat16_rn(rmax))));
             } else {
                 const int off = s_offs[ti.e];
                 const int cnt = s_offs[ti.e + 1] - off;
@@ -546,6 +556,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     const bool fp8 = g.fp8 && g.kind != GK_ROUTER;
     p.b_scale = fp8 ? g.b_scale : nullptr;
     p.a_scale = fp8 ? g.a_scale : nullptr;
+    p.act_amax = fp8 ? g.act_amax : nullptr;
     const int kstep = fp8 ? 2 * kBK : kBK;   // K elements per 128-byte stage row
     auto map = [&](CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
         return fp8 ? make_map_e4m3(tm, ptr, rows, cols, box_rows) : make_map(tm, ptr, rows, cols, box_rows);

@@ -29,7 +29,7 @@ struct WsLayout {
            perm = 0, cw = 0, xg = 0, act = 0, y_slots = 0, h_stage = 0, out_stage = 0;
     // MOE_FLAG_FP8: e4m3 activation rows of the down GEMM and the row scales
     // of both GEMMs' activations (the gate-up codes reuse the xg region)
-    size_t act_q = 0, x_scale = 0, act_scale = 0;
+    size_t act_q = 0, x_scale = 0, act_scale = 0, act_amax = 0;
     size_t total = 0;
 };
 
@@ -133,6 +133,7 @@ struct GemmLaunch {
     int fp8;                 // expert GEMMs: a_ptr and b_ptr hold e4m3 rows, each with
     const float* a_scale;    //   its scale: a_scale per activation row (slot order),
     const float* b_scale;    //   b_scale per weight row (W13: [E*2F], W2: [E*d])
+    float* act_amax;         // gate-up: if set, atomically maxed with each act row's max |bf16 value|
     int* status;
     long long budget;
 };
@@ -148,9 +149,12 @@ cudaError_t launch_combine(int T, int d, int k, const void* y_slots, const int32
                            cudaStream_t s);
 // Per-row e4m3 quantisation of rows [0, rows) (bf16 [.., cols] -> codes + scales);
 // row r reads source row perm[r] / k when perm is not NULL; rows from *nrows
-// on are skipped when nrows is not NULL.
+// on are skipped when nrows is not NULL.  amax_in, when given, holds each
+// row's max |value| already (one pass over the row instead of two);
+// zero_rows, when given, gets 0 written at each quantised row's index.
 cudaError_t launch_quantize_fp8(long long rows, int cols, const void* w, const int32_t* perm, int k,
-                                const int32_t* nrows, void* q, float* scales, cudaStream_t s);
+                                const int32_t* nrows, void* q, float* scales, cudaStream_t s,
+                                const float* amax_in = nullptr, float* zero_rows = nullptr);
 cudaError_t launch_timeout_probe(int* status, long long budget, cudaStream_t s);
 
 }  // namespace moe

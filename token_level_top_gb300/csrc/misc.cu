@@ -110,52 +110,124 @@ __global__ void gather_rows_kernel(int rows_max, int d8, int k, int E, const uin
     }
 }
 
-// Per-row FP8 (e4m3) quantisation, one warp per row:
+// Per-row FP8 (e4m3) quantisation:
 //   s[r] = max_c |w[r,c]| / 448 (448: the largest finite e4m3; 1 for an all-zero row),
 //   q[r,c] = e4m3(w[r,c] / s[r]), round to nearest even, saturated to +-448.
 // Row r reads source row perm[r] / k when perm is given (the token rows of
 // the kept slots), else row r; rows from *nrows on are skipped when nrows is
 // given (a device-side count).
+
+__device__ __forceinline__ float amax8(const uint4 v, float amax)
+{
+    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&words[j]);
+        amax = fmaxf(amax, fmaxf(fabsf(__bfloat162float(b.x)), fabsf(__bfloat162float(b.y))));
+    }
+    return amax;
+}
+
+__device__ __forceinline__ uint2 e4m3_8(const uint4 v, float sc)
+{
+    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+    uint32_t packed[2] = {0, 0};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&words[j]);
+        const float x0 = __bfloat162float(b.x) / sc, x1 = __bfloat162float(b.y) / sc;
+        uint16_t two;   // element x0 in the low byte
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(two) : "f"(x1), "f"(x0));
+        packed[j >> 1] |= static_cast<uint32_t>(two) << (16 * (j & 1));
+    }
+    return make_uint2(packed[0], packed[1]);
+}
+
+// Each row's max |value| not yet known, longer rows: one warp per row, two
+// passes over it (the second partly from L2).
 __global__ void quantize_fp8_kernel(long long rows, int cols, const uint4* __restrict__ w,
                                     const int32_t* __restrict__ perm, int k,
                                     const int32_t* __restrict__ nrows, uint2* __restrict__ q,
-                                    float* __restrict__ scales)
+                                    float* __restrict__ scales, float* __restrict__ zero_rows)
 {
     const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (row >= rows || (nrows && row >= *nrows)) return;   // whole warps
     const int lane = threadIdx.x & 31;
     const int c8 = cols / 8;
-    const long long srow = perm ? perm[row] / k : row;
-    const uint4* wr = w + srow * c8;
+    const uint4* wr = w + (perm ? perm[row] / k : row) * c8;
     float amax = 0.0f;
-    for (int c = lane; c < c8; c += 32) {
-        const uint4 v = wr[c];
-        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&words[j]);
-            amax = fmaxf(amax, fmaxf(fabsf(__bfloat162float(b.x)), fabsf(__bfloat162float(b.y))));
-        }
-    }
+#pragma unroll 4
+    for (int c = lane; c < c8; c += 32) amax = amax8(__ldg(wr + c), amax);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
-    if (lane == 0) scales[row] = sc;
-    uint2* qr = q + row * c8;
-    for (int c = lane; c < c8; c += 32) {
-        const uint4 v = wr[c];
-        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-        uint32_t packed[2] = {0, 0};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&words[j]);
-            const float x0 = __bfloat162float(b.x) / sc, x1 = __bfloat162float(b.y) / sc;
-            uint16_t two;   // element x0 in the low byte
-            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(two) : "f"(x1), "f"(x0));
-            packed[j >> 1] |= static_cast<uint32_t>(two) << (16 * (j & 1));
-        }
-        qr[c] = make_uint2(packed[0], packed[1]);
+    if (lane == 0) {
+        scales[row] = sc;
+        if (zero_rows) zero_rows[row] = 0.0f;
     }
+    uint2* qr = q + row * c8;
+#pragma unroll 4
+    for (int c = lane; c < c8; c += 32) qr[c] = e4m3_8(__ldg(wr + c), sc);
+}
+
+// Each row's max |value| not yet known, rows of at most 256 * 8 * P values:
+// one 256-thread block per row, which holds the row in registers (P 16-byte
+// pieces a thread), reduces its maximum and quantises it: one read.
+template <int P>
+__global__ void __launch_bounds__(256) quantize_fp8_block_kernel(
+    int cols, const uint4* __restrict__ w, const int32_t* __restrict__ perm, int k,
+    const int32_t* __restrict__ nrows, uint2* __restrict__ q, float* __restrict__ scales,
+    float* __restrict__ zero_rows)
+{
+    __shared__ float s_wmax[8];
+    const long long row = blockIdx.x;
+    if (nrows && row >= *nrows) return;   // the whole block
+    const int c8 = cols / 8;
+    const uint4* wr = w + (perm ? perm[row] / k : row) * c8;
+    uint4 v[P];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+        const int c = threadIdx.x + 256 * i;
+        v[i] = c < c8 ? __ldg(wr + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < P; ++i) amax = amax8(v[i], amax);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if ((threadIdx.x & 31) == 0) s_wmax[threadIdx.x >> 5] = amax;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, s_wmax[i]);
+    const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+    if (threadIdx.x == 0) {
+        scales[row] = sc;
+        if (zero_rows) zero_rows[row] = 0.0f;
+    }
+    uint2* qr = q + row * c8;
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+        const int c = threadIdx.x + 256 * i;
+        if (c < c8) qr[c] = e4m3_8(v[i], sc);
+    }
+}
+
+// Each row's max |value| given: one block per row, one pass.
+__global__ void quantize_fp8_amax_kernel(int cols, const uint4* __restrict__ w, const int32_t* __restrict__ perm,
+                                         int k, const int32_t* __restrict__ nrows,
+                                         const float* __restrict__ amax_in, uint2* __restrict__ q,
+                                         float* __restrict__ scales)
+{
+    const long long row = blockIdx.x;
+    if (nrows && row >= *nrows) return;
+    const float amax = amax_in[row];
+    const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+    if (threadIdx.x == 0) scales[row] = sc;
+    const int c8 = cols / 8;
+    const uint4* wr = w + (perm ? perm[row] / k : row) * c8;
+    uint2* qr = q + row * c8;
+#pragma unroll 4
+    for (int c = threadIdx.x; c < c8; c += blockDim.x) qr[c] = e4m3_8(__ldg(wr + c), sc);
 }
 
 // One thread waits on an mbarrier that nothing will ever complete, with the
@@ -221,12 +293,34 @@ cudaError_t launch_combine(int T, int d, int k, const void* y_slots, const int32
 }
 
 cudaError_t launch_quantize_fp8(long long rows, int cols, const void* w, const int32_t* perm, int k,
-                                const int32_t* nrows, void* q, float* scales, cudaStream_t s)
+                                const int32_t* nrows, void* q, float* scales, cudaStream_t s,
+                                const float* amax_in, float* zero_rows)
 {
     if (rows <= 0) return cudaSuccess;
+    if (amax_in) {
+        if (zero_rows || rows > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+        quantize_fp8_amax_kernel<<<static_cast<unsigned>(rows), 256, 0, s>>>(
+            cols, static_cast<const uint4*>(w), perm, k, nrows, amax_in, static_cast<uint2*>(q), scales);
+        return cudaGetLastError();
+    }
+    // a block per row while the rows fit one resident wave (a batch of a few
+    // hundred tokens); beyond that, a warp per row schedules better
+    const int c8 = cols / 8;
+    if (c8 <= 256 * 4 && rows <= 8LL * num_sms()) {
+        const unsigned grid = static_cast<unsigned>(rows);
+        const uint4* w4 = static_cast<const uint4*>(w);
+        uint2* q2 = static_cast<uint2*>(q);
+        if (c8 <= 256)
+            quantize_fp8_block_kernel<1><<<grid, 256, 0, s>>>(cols, w4, perm, k, nrows, q2, scales, zero_rows);
+        else if (c8 <= 512)
+            quantize_fp8_block_kernel<2><<<grid, 256, 0, s>>>(cols, w4, perm, k, nrows, q2, scales, zero_rows);
+        else
+            quantize_fp8_block_kernel<4><<<grid, 256, 0, s>>>(cols, w4, perm, k, nrows, q2, scales, zero_rows);
+        return cudaGetLastError();
+    }
     const int per_block = 8;
     quantize_fp8_kernel<<<static_cast<unsigned>((rows + per_block - 1) / per_block), 32 * per_block, 0, s>>>(
-        rows, cols, static_cast<const uint4*>(w), perm, k, nrows, static_cast<uint2*>(q), scales);
+        rows, cols, static_cast<const uint4*>(w), perm, k, nrows, static_cast<uint2*>(q), scales, zero_rows);
     return cudaGetLastError();
 }
 

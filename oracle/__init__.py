@@ -49,9 +49,11 @@ def _load():
             I = ctypes.c_int
             lib.oracle_capacity.argtypes = [ctypes.c_int64, I, I, ctypes.c_double, ctypes.c_int64]
             lib.oracle_capacity.restype = ctypes.c_int64
-            lib.oracle_route.argtypes = [I, I, I, I, P, P, P, P, ctypes.c_float, P,
+            lib.oracle_route.argtypes = [I, I, I, I, P, P, P, P, ctypes.c_float, ctypes.c_float, P,
                                          P, P, P, P, P, P, P]
             lib.oracle_route.restype = I
+            lib.oracle_router_logits.argtypes = [I, I, I, I, I, ctypes.c_float, P, P, P, P, P, P, P]
+            lib.oracle_router_logits.restype = I
             lib.oracle_preference.argtypes = [I, P, P]
             lib.oracle_preference.restype = I
             lib.oracle_dispatch.argtypes = [I, I, I, ctypes.c_int64, P, P, P, P, P, P, P, P, P, P]
@@ -106,8 +108,9 @@ def preference(s_row) -> np.ndarray:
     return order
 
 
-def route(k, h=None, wr=None, bias=None, usage=None, lam=0.0, logits_in=None, E=None):
-    """Router step.  h [T,d] / wr [E,d] as uint16 bf16 bits, or logits_in [T,E] fp32.
+def route(k, h=None, wr=None, bias=None, usage=None, lam=0.0, logits_in=None, E=None, tau=1.0):
+    """Router step.  h [T,d] / wr [E,d] as uint16 bf16 bits, or logits_in [T,E] fp32;
+    tau the temperature (scores s = z / tau - lam * usage).
 
     Returns dict(logits, scores, ids, topk_p, counts_pre, f, P)."""
     lib = _load()
@@ -127,11 +130,35 @@ def route(k, h=None, wr=None, bias=None, usage=None, lam=0.0, logits_in=None, E=
                counts_pre=np.empty(E, np.int32), f=np.empty(E, np.float32),
                P=np.empty(E, np.float32))
     st = lib.oracle_route(T, d, E, k, _ptr(h), _ptr(wr), _ptr(bias), _ptr(usage), float(lam),
-                          _ptr(logits_in), _ptr(out["logits"]), _ptr(out["scores"]),
+                          float(tau), _ptr(logits_in), _ptr(out["logits"]), _ptr(out["scores"]),
                           _ptr(out["ids"]), _ptr(out["topk_p"]), _ptr(out["counts_pre"]),
                           _ptr(out["f"]), _ptr(out["P"]))
     if st:
         raise OracleError(st, "route")
+    return out
+
+
+NORM_NONE, NORM_LAYER, NORM_L2 = 0, 1, 2
+
+
+def router_logits(h, w, w2=None, bias=None, gamma=None, beta=None, norm=NORM_NONE, eps=1e-5):
+    """Router front end: logits [T,E] fp32 from h [T,d] (bf16 bits), optionally
+    normalised per row (NORM_LAYER with gamma/beta [d], or NORM_L2), then either
+    x.W^T (w [E,d]) or the two-layer router silu(x.W1^T).W2^T (w = W1 [H,d],
+    w2 = W2 [E,H]); bf16 bits for the weights, bias [E] fp32."""
+    lib = _load()
+    h = _c(h, np.uint16)
+    w = _c(w, np.uint16)
+    w2 = _c(w2, np.uint16)
+    T, d = h.shape
+    E = w2.shape[0] if w2 is not None else w.shape[0]
+    H = w.shape[0] if w2 is not None else 0
+    gamma, beta, bias = _c(gamma, np.float32), _c(beta, np.float32), _c(bias, np.float32)
+    out = np.empty((T, E), np.float32)
+    st = lib.oracle_router_logits(T, d, E, H, int(norm), float(eps), _ptr(h), _ptr(gamma), _ptr(beta),
+                                  _ptr(w), _ptr(w2), _ptr(bias), _ptr(out))
+    if st:
+        raise OracleError(st, "router_logits")
     return out
 
 

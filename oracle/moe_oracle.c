@@ -7,7 +7,10 @@
  * fp32 score arithmetic.
  *
  * The steps follow the pages in order:
+ *   0. optional router front end: LayerNorm or L2 normalisation of h
+ *      ([2kiu] §5.2), a two-layer router silu(x W1) W2 ([cnnetsun] §3.1)
  *   1. logits z = h . W_router (+ bias)          [coreui] §3.1, [csdn] §3.1
+ *      (scores divided by a temperature tau      [cnnetsun] §3.1 step 3)
  *   2. penalty s_i = z_i - lambda * usage_i       [mhpn] §2.3 (second layer),
  *      applied before top-k                       [cnnetsun] §3.1 step 4
  *   3. softmax over experts and top-k picks      [coreui] §3.1
@@ -168,11 +171,12 @@ static void softmax_row(int E, const float* s, double* p)
 }
 
 int oracle_route(int T, int d, int E, int k, const uint16_t* h, const uint16_t* wr,
-                 const float* bias, const float* usage, float lambda, const float* logits_in,
-                 float* logits, float* scores, int32_t* ids, float* topk_p,
-                 int32_t* counts_pre, float* f, float* P)
+                 const float* bias, const float* usage, float lambda, float tau,
+                 const float* logits_in, float* logits, float* scores, int32_t* ids,
+                 float* topk_p, int32_t* counts_pre, float* f, float* P)
 {
     if (T < 0 || E <= 0 || k <= 0 || k > E) return 1;
+    if (!(tau > 0.0f) || isinf(tau)) return 1;
     if (!logits_in && (d <= 0 || !h || !wr)) return 1;
 
     int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
@@ -198,13 +202,15 @@ int oracle_route(int T, int d, int E, int k, const uint16_t* h, const uint16_t* 
                 z[e] = (float)acc;
             }
         }
-        /* step 2: s = z - fl(lambda * usage), fp32, no FMA */
+        /* step 2: s = fl(z / tau) - fl(lambda * usage), fp32, no FMA; the
+         * temperature divides the scores before the penalty is taken off */
         for (int e = 0; e < E; ++e) {
+            volatile float zt = z[e] / tau;
             if (!usage || lambda == 0.0f) {
-                s[e] = z[e];
+                s[e] = zt;
             } else {
                 volatile float pen = lambda * usage[e];
-                s[e] = z[e] - pen;
+                s[e] = zt - pen;
             }
         }
         /* step 3: preference order, top-k ids, softmax probabilities */
@@ -226,6 +232,65 @@ int oracle_route(int T, int d, int E, int k, const uint16_t* h, const uint16_t* 
     free(p);
     free(psum);
     return status;
+}
+
+int oracle_router_logits(int T, int d, int E, int hidden, int norm, float eps,
+                         const uint16_t* h, const float* gamma, const float* beta,
+                         const uint16_t* w, const uint16_t* w2, const float* bias,
+                         float* logits)
+{
+    if (T < 0 || d <= 0 || E <= 0 || hidden < 0 || norm < 0 || norm > 2 || !(eps >= 0.0f)) return 1;
+    if (!h || !w || !logits || (hidden > 0 && !w2)) return 1;
+    double* x = (double*)malloc(sizeof(double) * (size_t)d);
+    double* a = (double*)malloc(sizeof(double) * (size_t)(hidden > 0 ? hidden : 1));
+    for (int t = 0; t < T; ++t) {
+        const uint16_t* ht = h + (size_t)t * d;
+        for (int i = 0; i < d; ++i) x[i] = (double)bf16_to_f32(ht[i]);
+        if (norm == 1) {
+            /* LayerNorm over the row: mean, mean squared deviation */
+            double mean = 0.0, var = 0.0;
+            for (int i = 0; i < d; ++i) mean += x[i];
+            mean /= (double)d;
+            for (int i = 0; i < d; ++i) var += (x[i] - mean) * (x[i] - mean);
+            var /= (double)d;
+            const double inv = 1.0 / sqrt(var + (double)eps);
+            for (int i = 0; i < d; ++i)
+                x[i] = (x[i] - mean) * inv * (gamma ? (double)gamma[i] : 1.0) + (beta ? (double)beta[i] : 0.0);
+        } else if (norm == 2) {
+            double ss = 0.0;
+            for (int i = 0; i < d; ++i) ss += x[i] * x[i];
+            double nrm = sqrt(ss);
+            if (nrm < (double)eps) nrm = (double)eps;
+            for (int i = 0; i < d; ++i) x[i] = nrm > 0.0 ? x[i] / nrm : 0.0;
+        }
+        float* zt = logits + (size_t)t * E;
+        if (hidden == 0) {
+            for (int e = 0; e < E; ++e) {
+                double acc = 0.0;
+                const uint16_t* we = w + (size_t)e * d;
+                for (int i = 0; i < d; ++i) acc += x[i] * (double)bf16_to_f32(we[i]);
+                if (bias) acc += (double)bias[e];
+                zt[e] = (float)acc;
+            }
+        } else {
+            for (int j = 0; j < hidden; ++j) {
+                double u = 0.0;
+                const uint16_t* wj = w + (size_t)j * d;
+                for (int i = 0; i < d; ++i) u += x[i] * (double)bf16_to_f32(wj[i]);
+                a[j] = u / (1.0 + exp(-u));
+            }
+            for (int e = 0; e < E; ++e) {
+                double acc = 0.0;
+                const uint16_t* we = w2 + (size_t)e * hidden;
+                for (int j = 0; j < hidden; ++j) acc += a[j] * (double)bf16_to_f32(we[j]);
+                if (bias) acc += (double)bias[e];
+                zt[e] = (float)acc;
+            }
+        }
+    }
+    free(x);
+    free(a);
+    return 0;
 }
 
 int oracle_dispatch(int T, int E, int k, int64_t C, const float* scores,

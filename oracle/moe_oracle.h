@@ -48,14 +48,38 @@ int64_t oracle_capacity(int64_t T, int k, int E, double cf, int64_t explicit_cap
  *   wr       [E,d] bf16 bits, row e is expert e's gate vector
  *   bias     [E] fp32 or NULL (added to the GEMM output)
  *   usage    [E] fp32 or NULL; lambda the penalty weight
+ *   tau      temperature, > 0: s = z / tau - lambda * usage ([cnnetsun] §3.1
+ *            steps 3-4: the scores are divided by tau, then the penalty is
+ *            taken off, before softmax and top-k; [2kiu] §2, third measure)
  *   logits_in[T,E] fp32 or NULL: final logits given directly (bias not added)
  * Outputs (all required): logits [T,E], scores [T,E], ids [T,k],
  * topk_p [T,k] (softmax probability of each pick), counts_pre [E], f [E], P [E].
- * Returns 0, or 5 if any score is NaN (outputs then undefined). */
+ * Returns 0, 1 on a bad argument, or 5 if any score is NaN (outputs then
+ * undefined). */
 int oracle_route(int T, int d, int E, int k, const uint16_t* h, const uint16_t* wr,
-                 const float* bias, const float* usage, float lambda, const float* logits_in,
-                 float* logits, float* scores, int32_t* ids, float* topk_p,
-                 int32_t* counts_pre, float* f, float* P);
+                 const float* bias, const float* usage, float lambda, float tau,
+                 const float* logits_in, float* logits, float* scores, int32_t* ids,
+                 float* topk_p, int32_t* counts_pre, float* f, float* P);
+
+/* Router front ends that produce the logits z ([cnnetsun] §3.1 steps 1-2;
+ * [2kiu] §5.2; [mhpn] §3.1 lists a router of Embedding -> LayerNorm ->
+ * Linear -> activation -> Linear):
+ *   x_t = h_t                                       norm 0
+ *   x_t = (h_t - mean) / sqrt(var + eps) * g + b    norm 1 (LayerNorm over d;
+ *         var the mean squared deviation; g, b = gamma, beta, NULL = 1, 0)
+ *   x_t = h_t / max(||h_t||_2, eps)                 norm 2 (L2 normalisation)
+ *   z_t = x_t . W^T + bias                          hidden 0, W [E,d]
+ *   z_t = silu(x_t . W1^T) . W2^T + bias            hidden H > 0 (the two-layer
+ *         router: W1 [H,d] with H = 2E on the page, W2 [E,H]; silu(u) =
+ *         u / (1 + exp(-u)))
+ * All in double from the bf16 inputs, each z rounded once to fp32.
+ *   h [T,d], w [E,d] or [H,d], w2 [E,H] (hidden > 0, else NULL): bf16 bits;
+ *   gamma, beta [d] fp32 or NULL; bias [E] fp32 or NULL; logits [T,E] out.
+ * Returns 0 or 1 (bad argument). */
+int oracle_router_logits(int T, int d, int E, int hidden, int norm, float eps,
+                         const uint16_t* h, const float* gamma, const float* beta,
+                         const uint16_t* w, const uint16_t* w2, const float* bias,
+                         float* logits);
 
 /* The preference order of one token: experts sorted by score, descending,
  * ties to the lower index.  order[E] out.  Returns 0, or 5 on NaN. */

@@ -604,3 +604,129 @@ def test_quantize_row_matches_torch():
     assert np.array_equal(codes, ref)
     codes0, sc0 = oracle.quantize_row(np.zeros(5, np.float32))
     assert sc0 == 1.0 and not codes0.any()
+
+
+# --------------------------------------------------------------------------- router variants
+# Temperature ([cnnetsun] §3.1 step 3; [2kiu] §2), normalisation before the
+# router ([2kiu] §5.2), the two-layer router silu(x W1) W2 ([cnnetsun] §3.1 step 2).
+
+
+def _eye(n):
+    return bf16(np.eye(n))
+
+
+def test_layernorm_worked_example():
+    # mean 2.5, mean squared deviation 1.25: x = (h - 2.5) / sqrt(1.25)
+    z = oracle.router_logits(bf16([[1, 2, 3, 4]]), _eye(4), norm=oracle.NORM_LAYER, eps=0.0)
+    s = 1.0 / math.sqrt(1.25)
+    np.testing.assert_allclose(z[0], [-1.5 * s, -0.5 * s, 0.5 * s, 1.5 * s], rtol=1e-7)
+    # gamma scales and beta shifts each normalised component
+    z = oracle.router_logits(bf16([[1, 2, 3, 4]]), _eye(4), gamma=[1, 2, 3, 4], beta=[0.5, 0, 0, -1],
+                             norm=oracle.NORM_LAYER, eps=0.0)
+    np.testing.assert_allclose(z[0], [-1.5 * s + 0.5, -1.0 * s, 1.5 * s, 6.0 * s - 1.0], rtol=1e-7)
+
+
+def test_layernorm_shift_and_scale_invariance():
+    rng = np.random.default_rng(21)
+    h = rng.integers(-20, 20, (6, 16)).astype(np.float32)
+    w = bf16(rng.standard_normal((5, 16)))
+    a = oracle.router_logits(bf16(h), w, norm=oracle.NORM_LAYER, eps=0.0)
+    b = oracle.router_logits(bf16(3 * h + 7), w, norm=oracle.NORM_LAYER, eps=0.0)   # exact in bf16
+    np.testing.assert_allclose(a, b, rtol=1e-6, atol=1e-6)
+
+
+def test_layernorm_router_reduces_to_torch():
+    rng = np.random.default_rng(22)
+    T, d, E = 11, 64, 6
+    h = bf16(rng.standard_normal((T, d)) * 3 + 1)
+    w = bf16(rng.standard_normal((E, d)) * 0.1)
+    gamma = (1 + 0.1 * rng.standard_normal(d)).astype(np.float32)
+    beta = (0.1 * rng.standard_normal(d)).astype(np.float32)
+    bias = rng.standard_normal(E).astype(np.float32)
+    z = oracle.router_logits(h, w, gamma=gamma, beta=beta, bias=bias, norm=oracle.NORM_LAYER, eps=1e-5)
+    x = torch.nn.functional.layer_norm(torch.from_numpy(widen(h)).double(), (d,),
+                                       torch.from_numpy(gamma).double(), torch.from_numpy(beta).double(), 1e-5)
+    want = x @ torch.from_numpy(widen(w)).double().T + torch.from_numpy(bias).double()
+    np.testing.assert_allclose(z, want.numpy().astype(np.float32), rtol=2e-7, atol=1e-6)
+
+
+def test_l2_norm_worked_example_and_torch():
+    z = oracle.router_logits(bf16([[3, 4, 0, 0], [0, 0, 0, 0]]), _eye(4), norm=oracle.NORM_L2, eps=1e-12)
+    np.testing.assert_allclose(z, [[0.6, 0.8, 0, 0], [0, 0, 0, 0]], rtol=1e-7)
+    rng = np.random.default_rng(23)
+    h = bf16(rng.standard_normal((9, 32)) * 50)
+    w = bf16(rng.standard_normal((4, 32)))
+    z = oracle.router_logits(h, w, norm=oracle.NORM_L2, eps=1e-12)
+    x = torch.nn.functional.normalize(torch.from_numpy(widen(h)).double(), p=2.0, dim=1, eps=1e-12)
+    want = x @ torch.from_numpy(widen(w)).double().T
+    np.testing.assert_allclose(z, want.numpy().astype(np.float32), rtol=2e-7, atol=1e-7)
+
+
+def test_two_layer_router_identity_is_silu():
+    # W1 = W2 = I: z = silu(h); silu(1) = 1 / (1 + e^-1), silu(-1) = -e^-1 / (1 + e^-1)
+    z = oracle.router_logits(bf16([[0, 1, -1, 2]]), _eye(4), w2=_eye(4))
+    e1 = math.exp(-1.0)
+    np.testing.assert_allclose(z[0], [0.0, 1 / (1 + e1), -e1 / (1 + e1), 2 / (1 + math.exp(-2.0))], rtol=1e-7)
+
+
+def test_two_layer_router_orientation():
+    # W1 [H=2, d=3] picks h0 and h2 into the hidden units; W2 [E=2, H=2] swaps them
+    w1 = bf16([[1, 0, 0], [0, 0, 1]])
+    w2 = bf16([[0, 1], [1, 0]])
+    z = oracle.router_logits(bf16([[1, 5, 2]]), w1, w2=w2, bias=[0.25, -0.5])
+    silu = lambda u: u / (1 + math.exp(-u))
+    np.testing.assert_allclose(z[0], [silu(2.0) + 0.25, silu(1.0) - 0.5], rtol=1e-7)
+
+
+def test_two_layer_router_reduces_to_torch():
+    rng = np.random.default_rng(24)
+    T, d, E = 13, 128, 8
+    H = 2 * E
+    h = bf16(rng.standard_normal((T, d)))
+    w1 = bf16(rng.standard_normal((H, d)) * 0.1)
+    w2 = bf16(rng.standard_normal((E, H)) * 0.3)
+    z = oracle.router_logits(h, w1, w2=w2, norm=oracle.NORM_LAYER, eps=1e-5)
+    x = torch.nn.functional.layer_norm(torch.from_numpy(widen(h)).double(), (d,), eps=1e-5)
+    a = torch.nn.functional.silu(x @ torch.from_numpy(widen(w1)).double().T)
+    want = a @ torch.from_numpy(widen(w2)).double().T
+    np.testing.assert_allclose(z, want.numpy().astype(np.float32), rtol=2e-7, atol=1e-7)
+
+
+def test_temperature_comes_before_the_penalty():
+    # z = [1.0, 0.8], usage = [1, 0], lambda = 0.3.  tau = 1: s = [0.7, 0.8], expert 1
+    # first; tau = 0.5: s = [2.0 - 0.3, 1.6] = [1.7, 1.6], expert 0 first.  Penalising
+    # before dividing would give [1.4, 1.6] and keep expert 1 first.
+    z = np.array([[1.0, 0.8]], np.float32)
+    u = np.array([1.0, 0.0], np.float32)
+    r1 = oracle.route(1, logits_in=z, usage=u, lam=0.3, tau=1.0)
+    r2 = oracle.route(1, logits_in=z, usage=u, lam=0.3, tau=0.5)
+    assert r1["ids"][0, 0] == 1 and r2["ids"][0, 0] == 0
+    pen = np.float32(0.3) * np.float32(1.0)
+    assert r2["scores"][0, 0] == np.float32(np.float32(2.0) - pen)
+    assert r2["scores"][0, 1] == np.float32(1.6)
+    # the logits output is the raw z, not divided
+    assert np.array_equal(r2["logits"], z)
+
+
+def test_temperature_sharpens_softmax():
+    from scipy.special import softmax
+    rng = np.random.default_rng(25)
+    z = rng.standard_normal((40, 8)).astype(np.float32)
+    for tau in (0.5, 0.7, 2.0):
+        r = oracle.route(2, logits_in=z, tau=tau)
+        s = (z / np.float32(tau)).astype(np.float32)
+        assert np.array_equal(r["scores"], s)
+        p = softmax(s.astype(np.float64), axis=1)
+        np.testing.assert_allclose(r["topk_p"], np.take_along_axis(p, r["ids"], 1), rtol=1e-6)
+        # a positive scale keeps the ranking (no new ties at these values)
+        assert np.array_equal(r["ids"], oracle.route(2, logits_in=z)["ids"])
+    # a smaller tau gives the top pick more probability
+    p5 = oracle.route(1, logits_in=z, tau=0.5)["topk_p"]
+    p1 = oracle.route(1, logits_in=z, tau=1.0)["topk_p"]
+    assert np.all(p5 >= p1)
+
+
+@pytest.mark.parametrize("tau", [0.0, -1.0, float("inf"), float("nan")])
+def test_temperature_must_be_positive(tau):
+    with pytest.raises(oracle.OracleError):
+        oracle.route(1, logits_in=np.zeros((2, 3), np.float32), tau=tau)

@@ -43,12 +43,14 @@ CLOCK_LEAD_S = 0.25  # untimed lead-in for clock samples when the timed region i
 CHUNK = 256  # tokens per routing chunk; a batch of one chunk routes and dispatches in one kernel
 
 
-def kernels_per_step(T, fp8=False):
+def kernels_per_step(T, fp8=False, norm=0, hidden=0):
     """Kernels of this library one layer step launches."""
     # router GEMM, row gather, gate-up, down, combine + route and dispatch:
     # one fused kernel for a single chunk, else route + dispatch replay + finish;
-    # FP8: the activation rows are quantised between the two expert GEMMs
-    return 5 + (1 if T <= CHUNK else 3) + (1 if fp8 else 0)
+    # FP8: the activation rows are quantised between the two expert GEMMs;
+    # router variants: the normalisation before the router GEMM, the
+    # two-layer router's second layer after it
+    return 5 + (1 if T <= CHUNK else 3) + (1 if fp8 else 0) + (1 if norm else 0) + (1 if hidden else 0)
 
 
 def parse():
@@ -63,6 +65,12 @@ def parse():
     ap.add_argument("--fp8-weights", action="store_true",
                     help="expert GEMMs in e4m3: weights quantised per row once (moe_quantize_fp8), "
                          "token and activation rows per row on the fly")
+    ap.add_argument("--tau", type=float, default=1.0, help="router temperature")
+    ap.add_argument("--router-norm", default="none", choices=["none", "layer", "l2"],
+                    help="normalise the token rows before the router (LayerNorm or L2)")
+    ap.add_argument("--router-hidden", type=int, default=0,
+                    help="H > 0: the two-layer router silu(x W1^T) W2^T with H hidden units "
+                         "(-1: H = 2E)")
     return ap.parse_args()
 
 
@@ -252,8 +260,9 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(shape):
-    return {"workload": shape.name, "T": shape.T, "d_model": shape.d, "E": shape.E, "k": shape.k,
+def workload_config(shape, router=None):
+    extra = {"router": router} if router else {}
+    return {**extra, "workload": shape.name, "T": shape.T, "d_model": shape.d, "E": shape.E, "k": shape.k,
             "d_ff": shape.F, "cf": shape.cf, "lambda": shape.lam,
             "capacity": moe.capacity(shape.T, shape.k, shape.E, shape.cf, shape.capacity),
             "parallelism": "replicas", "l2": "inputs larger than L2: every step streams "
@@ -281,11 +290,27 @@ def run_ours(args, rank, world, local):
         want_cpu = False
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
-    cfg = moe.Config.of(shape, flags=moe.FLAG_FP8 if fp8 else 0)
+    norm = {"none": moe.NORM_NONE, "layer": moe.NORM_LAYER, "l2": moe.NORM_L2}[args.router_norm]
+    hidden = 2 * shape.E if args.router_hidden < 0 else args.router_hidden
+    variant = norm != moe.NORM_NONE or hidden > 0 or args.tau != 1.0
+    router_desc = None
+    wr, bias = L["wr"], L["bias"]
+    if variant:   # the router variants: their own seeded weights, the bias in the Router
+        # no bias and no LayerNorm shift: the experts' loads stay as even as
+        # with the workload's own router, so that the dispatch does the same work
+        rw = synth.router_variant_weights(shape.d, shape.E, hidden, norm == moe.NORM_LAYER,
+                                          seed=shape.seed + 11, bias=False, beta=False)
+        if not hidden and not norm:
+            rw["w"], rw["bias"] = L["wr"].cpu(), (None if L["bias"] is None else L["bias"].cpu())
+        wr = moe.Router(**{n: (None if v is None else v.cuda()) for n, v in rw.items()})
+        bias = None
+        router_desc = {"tau": args.tau, "norm": args.router_norm, "hidden": hidden}
+    cfg = moe.Config.of(shape, flags=moe.FLAG_FP8 if fp8 else 0, tau=args.tau, router_norm=norm,
+                        norm_eps=1e-5 if norm == moe.NORM_LAYER else 1e-12, router_hidden=hidden)
     ws = moe.workspace(cfg)
     out = torch.empty(shape.T, shape.d, dtype=torch.bfloat16, device="cuda")
     # kept rows of this batch (routing is deterministic, identical every step)
-    _, aux = moe.layer_forward(cfg, ws, L["h"], L["wr"], L["w13"], L["w2"], L["bias"], L["usage"],
+    _, aux = moe.layer_forward(cfg, ws, L["h"], wr, L["w13"], L["w2"], bias, L["usage"],
                                aux=True, out=out)
     counts = aux["counts"].cpu()
     kept = int(counts.sum().item())
@@ -295,7 +320,7 @@ def run_ours(args, rank, world, local):
         raise RuntimeError(f"device status {st} ({moe.STATUS.get(st)})")
 
     def step(evs=None):
-        moe.layer_forward(cfg, ws, L["h"], L["wr"], L["w13"], L["w2"], L["bias"], L["usage"],
+        moe.layer_forward(cfg, ws, L["h"], wr, L["w13"], L["w2"], bias, L["usage"],
                           stage_events=evs, out=out)
 
     w0 = torch.cuda.Event(enable_timing=True)
@@ -352,9 +377,9 @@ def run_ours(args, rank, world, local):
     h_dev = torch.empty_like(L["h"])
 
     def e2e_step():
-        if fp8:
+        if fp8 or variant:
             h_dev.copy_(h_host, non_blocking=True)
-            moe.layer_forward(cfg, ws, h_dev, L["wr"], L["w13"], L["w2"], L["bias"], L["usage"], out=out)
+            moe.layer_forward(cfg, ws, h_dev, wr, L["w13"], L["w2"], bias, L["usage"], out=out)
             o_host.copy_(out, non_blocking=True)
             torch.cuda.current_stream().synchronize()
         else:
@@ -408,7 +433,7 @@ def run_ours(args, rank, world, local):
         "dtype": ("e4m3 expert weights and activations (fp32 row scales), fp32 accumulate"
                   if fp8 else "bf16"),
         "data": "synthetic",
-        "config": workload_config(shape),
+        "config": workload_config(shape, router_desc),
         "roofline": roof,
         "expert_gemm_tflops": expert_tflops,
         "weight_stream_gbs": weight_bytes / ((stage_ms["gate_up"] + stage_ms["down"]) * 1e-3) / 1e9,
@@ -417,7 +442,7 @@ def run_ours(args, rank, world, local):
         "e2e": ({"value": world * T * args.e2e_steps / te, "unit": UNIT,
                  "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2}
                 if args.e2e_steps > 0 else None),
-        "gpu_launches": kernels_per_step(shape.T, fp8) * args.steps,
+        "gpu_launches": kernels_per_step(shape.T, fp8, norm, hidden) * args.steps,
     }
     if want_cpu:
         res = oracle_sample(shape, L["h"].cpu(), L["wr"].cpu(),

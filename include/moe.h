@@ -57,7 +57,8 @@ typedef enum {
 } moe_status_t;
 
 /* moe_config_t.flags: size the workspace for the FP8 entry points too (adds
- * T*k*(d_ff + 8) bytes for the e4m3 activation rows and row scales). */
+ * T*k*(d_ff + 12) bytes for the e4m3 activation rows, their scales and row
+ * maxima). */
 #define MOE_FLAG_FP8 1u
 
 /* Layer shape.  Capacity C = ceil(T*k*cf/E) unless capacity > 0. */
@@ -71,7 +72,36 @@ typedef struct {
     int32_t capacity; /* > 0: explicit per-expert capacity, overrides cf */
     float lambda;     /* load-penalty weight (0 = no penalty) */
     uint32_t flags;   /* 0, or MOE_FLAG_FP8 */
+    /* Router variants (all zero: the plain linear router, no temperature). */
+    float tau;              /* temperature, 0 (= 1) or finite > 0: s = z / tau - lambda*usage */
+    uint32_t router_norm;   /* MOE_ROUTER_NORM_*: normalisation of h before the router */
+    float norm_eps;         /* epsilon of that normalisation, finite >= 0 */
+    int32_t router_hidden;  /* 0: linear router; H in [1, 256]: the two-layer router */
 } moe_config_t;
+
+/* moe_config_t.router_norm ([2kiu] §5.2: a LayerNorm before the router, or
+ * L2-normalised inputs; [mhpn] §3.1: a router that begins with a LayerNorm).
+ * Needs d_model <= 16384. */
+#define MOE_ROUTER_NORM_NONE 0u
+#define MOE_ROUTER_NORM_LAYER 1u   /* (h - mean) / sqrt(var + eps) * gamma + beta, over d */
+#define MOE_ROUTER_NORM_L2 2u      /* h / max(||h||_2, eps) */
+
+/* Router weights for the router variants (moe_router_logits,
+ * moe_layer_forward_router).  All device pointers, 16-byte aligned.
+ *   w           [E, d] bf16, row e = expert e's gate vector; with
+ *               router_hidden = H > 0, W1 [H, d] (row j = hidden unit j)
+ *   w2          [E, H] bf16 when router_hidden > 0 (else NULL): the two-layer
+ *               router z = silu(x . W1^T) . W2^T ([cnnetsun] §3.1 step 2: W1
+ *               d x 2E, W2 2E x E); E * H <= 16384
+ *   bias        [E] fp32 added to z, or NULL
+ *   norm_gamma, norm_beta  [d] fp32 LayerNorm scale and shift, or NULL (1, 0) */
+typedef struct {
+    const void* w;
+    const void* w2;
+    const float* bias;
+    const float* norm_gamma;
+    const float* norm_beta;
+} moe_router_t;
 
 /* Number of stage boundaries recorded by moe_layer_forward's stage_events. */
 #define MOE_NUM_STAGES 6
@@ -111,8 +141,9 @@ moe_status_t moe_pack_w13(int32_t E, int32_t F, int32_t d, const void* w1_dev,
 
 /* Router: logits, penalised scores, top-k picks and load statistics.
  *   z = h . W_r^T (+ b)                       [coreui] §3.1, [csdn] §3.1
- *   s_i = z_i - lambda * usage_i (fp32, no FMA) [mhpn] §2.3 (second check),
- *                                             [cnnetsun] §3.1 (before top-k)
+ *   s_i = z_i / tau - lambda * usage_i        [mhpn] §2.3 (second check),
+ *     (fp32, the division and the product     [cnnetsun] §3.1 steps 3-4 (tau,
+ *     each rounded, no FMA; tau = cfg->tau)    then the penalty, before top-k)
  *   p = softmax(s); picks = the k best s, ties to the lower expert index
  *   f_i = (#picks of i)/T, P_i = mean_t p_i   [cnnetsun] §4.2, [coreui] §3.1
  * Inputs:
@@ -125,7 +156,10 @@ moe_status_t moe_pack_w13(int32_t E, int32_t F, int32_t d, const void* w1_dev,
  *   topk_ids_dev [T, k] int32 (required); topk_w_dev [T, k] fp32 (softmax
  *   probability of each pick); counts_pre_dev [E] int32 (picks per expert
  *   before capacity); f_dev [E], P_dev [E] fp32.
- * NaN scores set MOE_ERR_NONFINITE on the device (NaN then ranks last). */
+ * NaN scores set MOE_ERR_NONFINITE on the device (NaN then ranks last).
+ * The plain linear router only: a config with router_norm or router_hidden
+ * set returns MOE_ERR_INVALID_ARG unless logits_in_dev is given (use
+ * moe_router_logits for those routers' logits). */
 moe_status_t moe_route(const moe_config_t* cfg, const void* h_dev, const void* w_router_dev,
                        const float* bias_dev, const float* usage_dev,
                        const float* logits_in_dev, float* logits_out_dev, float* scores_out_dev,
@@ -218,7 +252,9 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* y_slots_dev,
  * stage_events: NULL, or MOE_NUM_STAGES+1 cudaEvent_t recorded on `stream`
  *   at the boundaries route | dispatch | prep (gather the token rows in slot
  *   order) | gate-up | down | combine.  For T <= 256 route and dispatch run
- *   as one kernel: the route stage then holds the router GEMM only. */
+ *   as one kernel: the route stage then holds the router GEMM only.
+ * The linear router with cfg->tau; router_norm and router_hidden must be 0
+ * (MOE_ERR_INVALID_ARG otherwise; moe_layer_forward_router takes those). */
 moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* h_dev,
                                const void* w_router_dev, const float* bias_dev,
                                const float* usage_dev, const void* w13_dev, const void* w2_dev,
@@ -240,6 +276,31 @@ moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* h_dev,
                                    uint8_t* flags_dev, int32_t* counts_dev, float* f_dev,
                                    float* P_dev, void* const* stage_events, void* ws_dev,
                                    size_t ws_bytes, void* stream);
+
+/* The router variants' logits: z = front end of cfg applied to h, for the
+ * router in `router` (see moe_router_t): normalisation of each token row
+ * (cfg->router_norm, cfg->norm_eps; the normalised rows are rounded to bf16
+ * for the router GEMM), then the linear router or, with router_hidden = H,
+ * the two-layer router (fp32 hidden units, silu, W2 in fp32 accumulation),
+ * plus the bias.  logits_dev [T, E] fp32 out.  Feed them to moe_route as
+ * logits_in_dev for the route step. */
+moe_status_t moe_router_logits(const moe_config_t* cfg, const void* h_dev, const moe_router_t* router,
+                               float* logits_dev, void* ws_dev, size_t ws_bytes, void* stream);
+
+/* The whole layer (as moe_layer_forward) with any router variant of cfg
+ * (temperature, normalisation, two-layer router) and bf16 or e4m3 experts:
+ * w13_scale_dev and w2_scale_dev NULL for bf16 weights, or the row scales of
+ * e4m3 weights (as moe_layer_forward_fp8, which needs MOE_FLAG_FP8).  The
+ * route stage holds the router front end.  logits_out_dev receives z (before
+ * the temperature and the penalty). */
+moe_status_t moe_layer_forward_router(const moe_config_t* cfg, const void* h_dev,
+                                      const moe_router_t* router, const float* usage_dev,
+                                      const void* w13_dev, const float* w13_scale_dev,
+                                      const void* w2_dev, const float* w2_scale_dev, void* out_dev,
+                                      float* logits_out_dev, int32_t* assign_dev, int32_t* slot_dev,
+                                      uint8_t* flags_dev, int32_t* counts_dev, float* f_dev,
+                                      float* P_dev, void* const* stage_events, void* ws_dev,
+                                      size_t ws_bytes, void* stream);
 
 /* The same layer from host memory, end to end: copies h (pinned host,
  * [T,d] bf16) to the workspace, runs moe_layer_forward and copies the output

@@ -132,3 +132,42 @@ def test_dispatch_and_ffn_argument_checks(L):
 def test_status_strings(L):
     for code, text in moe.STATUS.items():
         assert L.moe_status_string(code).decode() == text
+
+
+def test_router_variant_config_checks(L):
+    for bad in [dict(tau=-1.0), dict(tau=float("inf")), dict(tau=float("nan")), dict(router_norm=3),
+                dict(norm_eps=-1.0), dict(router_hidden=-1), dict(router_hidden=257),
+                dict(E=128, router_hidden=256)]:
+        c = _cfg(**bad)
+        assert L.moe_workspace_size(ctypes.byref(c)) == 0, bad
+    base = L.moe_workspace_size(ctypes.byref(_cfg()))
+    # tau alone needs no room; the normalised rows and the hidden router add theirs
+    assert L.moe_workspace_size(ctypes.byref(_cfg(tau=0.7))) == base
+    assert L.moe_workspace_size(ctypes.byref(_cfg(router_norm=1))) > base
+    assert L.moe_workspace_size(ctypes.byref(_cfg(router_hidden=16))) > base
+
+
+def test_router_variant_argument_checks(L):
+    P = ctypes.c_void_p
+    c = _cfg(router_hidden=16, router_norm=1)
+    n = L.moe_workspace_size(ctypes.byref(c))
+    r = moe.MoERouter(FAKE, FAKE, None, None, None)
+    call = lambda cfg, rt, nb=n, h=FAKE: L.moe_router_logits(ctypes.byref(cfg), P(h), ctypes.byref(rt),
+                                                             P(FAKE), P(FAKE), nb, None)
+    assert call(c, r, nb=n - 256) == 4
+    assert call(c, moe.MoERouter(FAKE, None, None, None, None)) == 1   # the hidden router needs W2
+    assert call(_cfg(), moe.MoERouter(FAKE, FAKE, None, None, None)) == 1   # W2 without a hidden width
+    assert call(_cfg(), moe.MoERouter(FAKE, None, None, FAKE, None)) == 1   # gamma without LayerNorm
+    assert call(c, moe.MoERouter(FAKE, FAKE + 2, None, None, None)) == 3
+    assert call(c, r, h=FAKE + 4) == 3
+    assert L.moe_router_logits(ctypes.byref(c), P(FAKE), None, P(FAKE), P(FAKE), n, None) == 1
+    # the plain entry points do not take these routers' weights
+    ids = P(FAKE)
+    assert L.moe_route(ctypes.byref(c), P(FAKE), P(FAKE), None, None, None, None, None, ids, None, None,
+                       None, None, P(FAKE), n, None) == 1
+    base = [P(FAKE)] * 2 + [None, None] + [P(FAKE)] * 3 + [None] * 8
+    assert L.moe_layer_forward(ctypes.byref(c), *base, P(FAKE), n, None) == 1
+    # layer with the router struct: scales must come in pairs
+    lf = lambda s13, s2: L.moe_layer_forward_router(ctypes.byref(c), P(FAKE), ctypes.byref(r), None, P(FAKE),
+                                                    s13, P(FAKE), s2, P(FAKE), *([None] * 8), P(FAKE), n, None)
+    assert lf(P(FAKE), None) == 1

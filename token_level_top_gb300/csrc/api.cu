@@ -32,6 +32,14 @@ moe_status_t check_config(const moe_config_t* c, bool need_ff)
     if (c->capacity < 0) return MOE_ERR_INVALID_ARG;
     if (c->capacity == 0 && !(c->cf > 0.0 && c->cf <= 100.0)) return MOE_ERR_INVALID_ARG;
     if (!isfinite(c->lambda)) return MOE_ERR_INVALID_ARG;
+    if (!(c->tau == 0.0f || (c->tau > 0.0f && isfinite(c->tau)))) return MOE_ERR_INVALID_ARG;
+    if (c->router_norm > MOE_ROUTER_NORM_L2 || !(c->norm_eps >= 0.0f && isfinite(c->norm_eps)))
+        return MOE_ERR_INVALID_ARG;
+    if (c->router_hidden < 0) return MOE_ERR_INVALID_ARG;
+    if (c->router_hidden > kMaxRouterHidden ||
+        static_cast<long long>(c->router_hidden) * c->E > kMaxRouterWeights2)
+        return MOE_ERR_UNSUPPORTED;
+    if (c->router_norm != MOE_ROUTER_NORM_NONE && c->d_model > 16384) return MOE_ERR_UNSUPPORTED;
     if (c->E > kMaxE || c->k > kMaxK) return MOE_ERR_UNSUPPORTED;
     if (c->d_model <= 0 || c->d_model % 64 != 0) return MOE_ERR_UNSUPPORTED;
     if (need_ff && (c->d_ff <= 0 || c->d_ff % 128 != 0)) return MOE_ERR_UNSUPPORTED;
@@ -98,8 +106,11 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
     const size_t d = static_cast<size_t>(c.d_model), F = static_cast<size_t>(std::max(c.d_ff, 0));
     WsLayout w;
     w.nchunks = static_cast<int>((T + kChunk - 1) / kChunk);
-    w.splits = router_splits(static_cast<int>(T), static_cast<int>(d), c.E);
-    w.epad = static_cast<int>(std::max<size_t>(32, round_up(E, 32)));
+    // the router GEMM's output columns: the experts, or the two-layer router's hidden units
+    w.nr = c.router_hidden > 0 ? c.router_hidden : c.E;
+    const size_t NR = static_cast<size_t>(w.nr);
+    w.splits = router_splits(static_cast<int>(T), static_cast<int>(d), w.nr);
+    w.epad = static_cast<int>(std::max<size_t>(32, round_up(NR, 32)));
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -109,7 +120,7 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
     const size_t nch = static_cast<size_t>(w.nchunks);
     w.status = take(256);
     w.ctrl = take(CTRL_WORDS * 4);
-    w.part = take(static_cast<size_t>(w.splits) * T * E * 4);
+    w.part = take(static_cast<size_t>(w.splits) * T * NR * 4);
     w.scores = take(T * E * 4);
     w.ids = take(T * k * 4);
     w.prefs = take(T * static_cast<size_t>(pref_stride(c.E)));
@@ -133,6 +144,8 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
         w.act_scale = take(T * k * 4);
         w.act_amax = take(T * k * 4);
     }
+    if (c.router_norm != MOE_ROUTER_NORM_NONE) w.xn = take(T * d * 2);
+    if (c.router_hidden > 0) w.zr = take(T * E * 4);
     w.h_stage = take(T * d * 2);
     w.out_stage = take(T * d * 2);
     w.total = off;
@@ -142,13 +155,14 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
 
 namespace {
 
-// The router GEMM (skipped when logits are given).
+// The router GEMM (skipped when logits are given): h . W^T over L.nr output
+// columns (the experts, or the two-layer router's hidden units).
 moe_status_t run_router_gemm(const moe_config_t& c, const WsLayout& L, const void* h,
                              const void* wr, void* ws, cudaStream_t s)
 {
     GemmLaunch g{};
     g.kind = GK_ROUTER;
-    g.E = c.E;
+    g.E = L.nr;
     g.T = c.T;
     g.topk = c.k;
     g.d = c.d_model;
@@ -161,6 +175,57 @@ moe_status_t run_router_gemm(const moe_config_t& c, const WsLayout& L, const voi
     g.status = ws_at<int>(ws, L.status);
     g.budget = kSpinBudget;
     return cuda_status(launch_gemm(g, s));
+}
+
+// The router weights of any variant (moe_router_t without the C type).
+struct RouterWeights {
+    const void* w;        // [E, d], or W1 [H, d]
+    const void* w2;       // [E, H] or NULL
+    const float* bias;    // [E] or NULL
+    const float* gamma;   // [d] or NULL
+    const float* beta;    // [d] or NULL
+};
+
+bool router_args_ok(const moe_config_t& c, const RouterWeights& R)
+{
+    if (!R.w || (c.router_hidden > 0) != (R.w2 != nullptr)) return false;
+    if (c.router_norm != MOE_ROUTER_NORM_LAYER && (R.gamma || R.beta)) return false;
+    return true;
+}
+
+bool router_aligned(const RouterWeights& R)
+{
+    return aligned(R.w, 16) && (!R.w2 || aligned(R.w2, 16)) && (!R.gamma || aligned(R.gamma, 16)) &&
+           (!R.beta || aligned(R.beta, 16));
+}
+
+// The router front end up to the logits: the normalisation (into L.xn), the
+// router GEMM on h or on it, and for the two-layer router the head that
+// writes z (with the bias) into L.zr.  Returns in *logits where the route
+// step finds the logits (L.zr), or NULL when it sums the GEMM partials itself
+// (and adds the bias).
+moe_status_t run_router_front(const moe_config_t& c, const WsLayout& L, const void* h,
+                              const RouterWeights& R, void* ws, cudaStream_t s, const float** logits)
+{
+    const void* x = h;
+    if (c.router_norm != MOE_ROUTER_NORM_NONE) {
+        const float eps = c.norm_eps;
+        if (launch_router_norm(c.T, c.d_model, static_cast<int>(c.router_norm), eps, h, R.gamma, R.beta,
+                               ws_at<void>(ws, L.xn), s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        x = ws_at<void>(ws, L.xn);
+    }
+    moe_status_t st = run_router_gemm(c, L, x, R.w, ws, s);
+    if (st != MOE_OK) return st;
+    *logits = nullptr;
+    if (c.router_hidden > 0) {
+        float* z = ws_at<float>(ws, L.zr);
+        if (launch_router_head(c.T, c.E, c.router_hidden, L.splits, ws_at<float>(ws, L.part), R.w2, R.bias,
+                               z, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        *logits = z;
+    }
+    return MOE_OK;
 }
 
 RouteArgs route_args(const moe_config_t& c, const WsLayout& L, const float* bias,
@@ -180,6 +245,7 @@ RouteArgs route_args(const moe_config_t& c, const WsLayout& L, const float* bias
     a.bias = logits_in ? nullptr : bias;
     a.usage = usage;
     a.lambda = c.lambda;
+    a.tau = c.tau;
     a.logits_out = logits_out;
     a.scores_user = scores_out;
     a.scores_ws = ws_at<float>(ws, L.scores);
@@ -371,21 +437,20 @@ moe_status_t expert_ffn_impl(const moe_config_t* cfg, const void* h, const int32
     return run_experts(*cfg, L, h, perm, offsets, W, y_slots, ws, s, nullptr);
 }
 
-moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* h, const void* w_router,
-                                const float* bias, const float* usage, const ExpertWeights& W, void* out,
+moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* h, const RouterWeights& R,
+                                const float* usage, const ExpertWeights& W, void* out,
                                 float* logits_out, int32_t* assign, int32_t* slot, uint8_t* flags,
                                 int32_t* counts, float* f, float* P, void* const* stage_events, void* ws,
                                 size_t ws_bytes, void* stream)
 {
     const void* w13 = W.w13;
     const void* w2 = W.w2;
-    if (W.fp8() && (!(cfg->flags & MOE_FLAG_FP8) || cfg->d_model % 128 != 0))
-        return (cfg->flags & MOE_FLAG_FP8) ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
     moe_status_t st = check_config(cfg, true);
     if (st != MOE_OK) return st;
-    if (!h || !w_router || !w13 || !w2 || !out) return MOE_ERR_INVALID_ARG;
-    if (!aligned(h, 16) || !aligned(w_router, 16) || !aligned(w13, 16) || !aligned(w2, 16) ||
-        !aligned(out, 16))
+    if (W.fp8() && (!(cfg->flags & MOE_FLAG_FP8) || cfg->d_model % 128 != 0))
+        return (cfg->flags & MOE_FLAG_FP8) ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+    if (!h || !w13 || !w2 || !out || !router_args_ok(*cfg, R)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(h, 16) || !router_aligned(R) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16))
         return MOE_ERR_MISALIGNED;
     WsLayout L;
     st = check_ws(cfg, ws, ws_bytes, &L);
@@ -396,10 +461,11 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* h, const vo
     Ev ev{stage_events, s};
 
     ev.mark(0);
-    st = run_router_gemm(c, L, h, w_router, ws, s);
+    const float* zr = nullptr;
+    st = run_router_front(c, L, h, R, ws, s, &zr);
     if (st != MOE_OK) return st;
     const RouteArgs ra =
-        route_args(c, L, bias, usage, nullptr, logits_out, nullptr, nullptr, nullptr, ws);
+        route_args(c, L, R.bias, usage, zr, logits_out, nullptr, nullptr, nullptr, ws);
     // a batch of one chunk routes and dispatches in one kernel (the route stage
     // then holds only the router GEMM, the dispatch stage both)
     const bool small = L.nchunks == 1;
@@ -511,6 +577,8 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* h, const void* w_rou
     if (st != MOE_OK) return st;
     if (!topk_ids) return MOE_ERR_INVALID_ARG;
     if (!logits_in && (!h || !w_router)) return MOE_ERR_INVALID_ARG;
+    if (!logits_in && (cfg->router_norm != MOE_ROUTER_NORM_NONE || cfg->router_hidden != 0))
+        return MOE_ERR_INVALID_ARG;   // those routers' logits come from moe_router_logits
     if (!logits_in && (!aligned(h, 16) || !aligned(w_router, 16))) return MOE_ERR_MISALIGNED;
     WsLayout L;
     st = check_ws(cfg, ws, ws_bytes, &L);
@@ -619,9 +687,11 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* h, const voi
                                int32_t* slot, uint8_t* flags, int32_t* counts, float* f, float* P,
                                void* const* stage_events, void* ws, size_t ws_bytes, void* stream)
 {
-    return layer_forward_impl(cfg, h, w_router, bias, usage, ExpertWeights{w13, w2, nullptr, nullptr}, out,
-                              logits_out, assign, slot, flags, counts, f, P, stage_events, ws, ws_bytes,
-                              stream);
+    if (cfg && (cfg->router_norm != MOE_ROUTER_NORM_NONE || cfg->router_hidden != 0))
+        return MOE_ERR_INVALID_ARG;
+    return layer_forward_impl(cfg, h, RouterWeights{w_router, nullptr, bias, nullptr, nullptr}, usage,
+                              ExpertWeights{w13, w2, nullptr, nullptr}, out, logits_out, assign, slot, flags,
+                              counts, f, P, stage_events, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* h, const void* w_router,
@@ -632,9 +702,49 @@ moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* h, const
                                    void* const* stage_events, void* ws, size_t ws_bytes, void* stream)
 {
     if (!w13_scale || !w2_scale) return MOE_ERR_INVALID_ARG;
-    return layer_forward_impl(cfg, h, w_router, bias, usage, ExpertWeights{w13_q, w2_q, w13_scale, w2_scale},
-                              out, logits_out, assign, slot, flags, counts, f, P, stage_events, ws, ws_bytes,
-                              stream);
+    if (cfg && (cfg->router_norm != MOE_ROUTER_NORM_NONE || cfg->router_hidden != 0))
+        return MOE_ERR_INVALID_ARG;
+    return layer_forward_impl(cfg, h, RouterWeights{w_router, nullptr, bias, nullptr, nullptr}, usage,
+                              ExpertWeights{w13_q, w2_q, w13_scale, w2_scale}, out, logits_out, assign, slot,
+                              flags, counts, f, P, stage_events, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_router_logits(const moe_config_t* cfg, const void* h, const moe_router_t* router,
+                               float* logits, void* ws, size_t ws_bytes, void* stream)
+{
+    moe_status_t st = check_config(cfg, false);
+    if (st != MOE_OK) return st;
+    if (!h || !router || !logits) return MOE_ERR_INVALID_ARG;
+    const RouterWeights R{router->w, router->w2, router->bias, router->norm_gamma, router->norm_beta};
+    if (!router_args_ok(*cfg, R)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(h, 16) || !router_aligned(R)) return MOE_ERR_MISALIGNED;
+    WsLayout L;
+    st = check_ws(cfg, ws, ws_bytes, &L);
+    if (st != MOE_OK) return st;
+    if (cfg->T == 0) return MOE_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const float* zr = nullptr;
+    st = run_router_front(*cfg, L, h, R, ws, s, &zr);
+    if (st != MOE_OK) return st;
+    if (zr)
+        return cuda_status(cudaMemcpyAsync(logits, zr, sizeof(float) * cfg->T * cfg->E,
+                                           cudaMemcpyDeviceToDevice, s));
+    return cuda_status(launch_router_sum(cfg->T, cfg->E, L.splits, ws_at<float>(ws, L.part), R.bias, logits, s));
+}
+
+moe_status_t moe_layer_forward_router(const moe_config_t* cfg, const void* h, const moe_router_t* router,
+                                      const float* usage, const void* w13, const float* w13_scale,
+                                      const void* w2, const float* w2_scale, void* out, float* logits_out,
+                                      int32_t* assign, int32_t* slot, uint8_t* flags, int32_t* counts,
+                                      float* f, float* P, void* const* stage_events, void* ws,
+                                      size_t ws_bytes, void* stream)
+{
+    if (!router || (w13_scale == nullptr) != (w2_scale == nullptr)) return MOE_ERR_INVALID_ARG;
+    return layer_forward_impl(cfg, h,
+                              RouterWeights{router->w, router->w2, router->bias, router->norm_gamma,
+                                            router->norm_beta},
+                              usage, ExpertWeights{w13, w2, w13_scale, w2_scale}, out, logits_out, assign, slot,
+                              flags, counts, f, P, stage_events, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* h_host,

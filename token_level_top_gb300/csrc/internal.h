@@ -30,6 +30,9 @@ struct WsLayout {
     // MOE_FLAG_FP8: e4m3 activation rows of the down GEMM and the row scales
     // of both GEMMs' activations (the gate-up codes reuse the xg region)
     size_t act_q = 0, x_scale = 0, act_scale = 0, act_amax = 0;
+    size_t xn = 0;     // router input after normalisation [T, d] bf16 (router_norm != 0)
+    size_t zr = 0;     // two-layer router logits [T, E] fp32 (router_hidden > 0)
+    int nr = 0;        // router GEMM output columns: E, or the hidden width H
     size_t total = 0;
 };
 
@@ -67,6 +70,7 @@ struct RouteArgs {
     const float* bias;       // [E] or NULL (added to GEMM partial sums only)
     const float* usage;      // [E] or NULL
     float lambda;
+    float tau;               // temperature: s = z / tau - lambda*usage (0 or 1: none)
     float* logits_out;       // [T][E] or NULL
     float* scores_user;      // [T][E] or NULL
     float* scores_ws;        // [T][E] (always)
@@ -155,6 +159,19 @@ cudaError_t launch_combine(int T, int d, int k, const void* y_slots, const int32
 cudaError_t launch_quantize_fp8(long long rows, int cols, const void* w, const int32_t* perm, int k,
                                 const int32_t* nrows, void* q, float* scales, cudaStream_t s,
                                 const float* amax_in = nullptr, float* zero_rows = nullptr);
+// Router front end.  x = LayerNorm(h) (mode 1; gamma, beta [d] or NULL) or
+// h / max(||h||, eps) (mode 2), bf16 [T, d]; d <= 16384.
+cudaError_t launch_router_norm(int T, int d, int mode, float eps, const void* h, const float* gamma,
+                               const float* beta, void* x, cudaStream_t s);
+// z [T, E] = silu(sum of the splits x [T, H] partials) . W2^T (+ bias), W2 [E, H]
+// bf16; H <= kMaxRouterHidden and E * H <= kMaxRouterWeights2.
+constexpr int kMaxRouterHidden = 256;
+constexpr int kMaxRouterWeights2 = 16384;
+cudaError_t launch_router_head(int T, int E, int H, int splits, const float* part, const void* w2,
+                               const float* bias, float* z, cudaStream_t s);
+// z [T, E] = the sum of the splits x [T, E] partials (split order) + bias.
+cudaError_t launch_router_sum(int T, int E, int splits, const float* part, const float* bias, float* z,
+                              cudaStream_t s);
 cudaError_t launch_timeout_probe(int* status, long long budget, cudaStream_t s);
 
 }  // namespace moe

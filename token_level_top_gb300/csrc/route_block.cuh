@@ -87,8 +87,9 @@ __device__ __forceinline__ void route_block(const RouteArgs& a, const int chunk,
                     z = a.logits_in[static_cast<size_t>(t) * E + e];
                 }
                 if (a.logits_out) a.logits_out[static_cast<size_t>(t) * E + e] = z;
-                float sc = z;
-                if (a.usage && a.lambda != 0.0f) sc = __fsub_rn(z, __fmul_rn(a.lambda, a.usage[e]));
+                // the temperature divides the score before the penalty comes off
+                float sc = (a.tau != 0.0f && a.tau != 1.0f) ? __fdiv_rn(z, a.tau) : z;
+                if (a.usage && a.lambda != 0.0f) sc = __fsub_rn(sc, __fmul_rn(a.lambda, a.usage[e]));
                 if (isnan(sc)) {
                     saw_nan = true;
                     sc = -INFINITY;  // ranks last; the call reports MOE_ERR_NONFINITE

@@ -35,7 +35,13 @@ class MoEConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("k", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("cf", ctypes.c_double),
                 ("capacity", ctypes.c_int32), ("lambda_", ctypes.c_float),
-                ("flags", ctypes.c_uint32)]
+                ("flags", ctypes.c_uint32), ("tau", ctypes.c_float), ("router_norm", ctypes.c_uint32),
+                ("norm_eps", ctypes.c_float), ("router_hidden", ctypes.c_int32)]
+
+
+class MoERouter(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("norm_gamma", ctypes.c_void_p), ("norm_beta", ctypes.c_void_p)]
 
 
 @dataclass
@@ -49,10 +55,15 @@ class Config:
     capacity: int = 0
     lam: float = 0.0
     flags: int = 0   # FLAG_FP8: the workspace also serves the e4m3 (FP8) entry points
+    tau: float = 1.0           # router temperature
+    router_norm: int = 0       # NORM_LAYER / NORM_L2: normalise h before the router
+    norm_eps: float = 1e-5
+    router_hidden: int = 0     # H > 0: the two-layer router silu(x W1^T) W2^T
 
     def c(self) -> MoEConfig:
         return MoEConfig(self.T, self.d_model, self.E, self.k, self.d_ff, float(self.cf),
-                         int(self.capacity), float(self.lam), int(self.flags))
+                         int(self.capacity), float(self.lam), int(self.flags), float(self.tau),
+                         int(self.router_norm), float(self.norm_eps), int(self.router_hidden))
 
     @classmethod
     def of(cls, shape, **kw):
@@ -63,6 +74,23 @@ class Config:
 
 
 FLAG_FP8 = 1   # MOE_FLAG_FP8
+NORM_NONE, NORM_LAYER, NORM_L2 = 0, 1, 2   # MOE_ROUTER_NORM_*
+
+
+@dataclass
+class Router:
+    """Router weights of the router variants (moe_router_t): w [E,d] bf16, or W1
+    [H,d] with w2 = W2 [E,H] for the two-layer router; bias [E] fp32; gamma,
+    beta [d] fp32 for the LayerNorm before the router."""
+    w: torch.Tensor
+    w2: torch.Tensor = None
+    bias: torch.Tensor = None
+    gamma: torch.Tensor = None
+    beta: torch.Tensor = None
+
+    def c(self) -> MoERouter:
+        return MoERouter(*[None if t is None else t.data_ptr()
+                           for t in (self.w, self.w2, self.bias, self.gamma, self.beta)])
 
 _lib = None
 
@@ -70,6 +98,7 @@ P = ctypes.c_void_p
 I32 = ctypes.c_int32
 SZ = ctypes.c_size_t
 CFG = ctypes.POINTER(MoEConfig)
+RTR = ctypes.POINTER(MoERouter)
 
 _SIGS = {
     "moe_capacity": (ctypes.c_int64, [ctypes.c_int64, I32, I32, ctypes.c_double, I32]),
@@ -89,6 +118,8 @@ _SIGS = {
     "moe_quantize_fp8": (I32, [ctypes.c_int64, I32, P, P, P, P]),
     "moe_expert_ffn_fp8": (I32, [CFG, P, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_layer_forward_fp8": (I32, [CFG] + [P] * 18 + [SZ, P]),
+    "moe_router_logits": (I32, [CFG, P, RTR, P, P, SZ, P]),
+    "moe_layer_forward_router": (I32, [CFG, P, RTR] + [P] * 15 + [SZ, P]),
 }
 
 
@@ -201,6 +232,16 @@ def route(cfg: Config, ws, h=None, wr=None, bias=None, usage=None, logits_in=Non
     return out
 
 
+def router_logits(cfg: Config, ws, h, router: Router):
+    """The logits [T, E] fp32 of cfg's router variant (normalisation, two-layer router)."""
+    z = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=ws.device)
+    c, r = cfg.c(), router.c()
+    st = lib().moe_router_logits(ctypes.byref(c), _p(h), ctypes.byref(r), _p(z), _p(ws), ws.numel(),
+                                 _stream())
+    _check(st, "moe_router_logits")
+    return z
+
+
 def dispatch(cfg: Config, ws, scores):
     dev = ws.device
     T, E, k = cfg.T, cfg.E, cfg.k
@@ -248,7 +289,9 @@ def combine(cfg: Config, y_slots, assign, slot, offsets, cw):
 def layer_forward(cfg: Config, ws, h, wr, w13, w2, bias=None, usage=None, aux=False,
                   stage_events=None, out=None):
     """The fused layer.  Returns out [T, d] bf16 (and a dict of routing outputs when aux).
-    w13 / w2: bf16 tensors, or (q, scales) pairs from quantize_fp8 for e4m3 weights."""
+    wr: the router weight [E, d] bf16, or a Router (any router variant of cfg; its
+    bias is the router's, so bias stays None).  w13 / w2: bf16 tensors, or
+    (q, scales) pairs from quantize_fp8 for e4m3 weights."""
     dev = ws.device
     T, E, k = cfg.T, cfg.E, cfg.k
     if out is None:
@@ -274,7 +317,14 @@ def layer_forward(cfg: Config, ws, h, wr, w13, w2, bias=None, usage=None, aux=Fa
     evp = ctypes.cast(ev_arr, ctypes.c_void_p) if ev_arr is not None else None
     tail = (_p(out), g("logits"), g("assign"), g("slot"), g("flags"), g("counts"), g("f"), g("P"), evp,
             _p(ws), ws.numel(), _stream())
-    if _fp8(w13):   # e4m3 expert weights: (q, scales) pairs from quantize_fp8
+    if isinstance(wr, Router):
+        if bias is not None:
+            raise ValueError("the router's bias belongs in the Router")
+        (q13, s13), (q2, s2) = (w13, w2) if _fp8(w13) else ((w13, None), (w2, None))
+        r = wr.c()
+        st = lib().moe_layer_forward_router(ctypes.byref(c), _p(h), ctypes.byref(r), _p(usage), _p(q13),
+                                            _p(s13), _p(q2), _p(s2), *tail)
+    elif _fp8(w13):   # e4m3 expert weights: (q, scales) pairs from quantize_fp8
         (q13, s13), (q2, s2) = w13, w2
         st = lib().moe_layer_forward_fp8(ctypes.byref(c), _p(h), _p(wr), _p(bias), _p(usage), _p(q13),
                                          _p(s13), _p(q2), _p(s2), *tail)

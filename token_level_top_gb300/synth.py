@@ -19,6 +19,12 @@ Recipe (shapes and distributions of the five workloads):
     so that expert 0 is the rank-1 pick of about 42% of tokens after the
     penalty) and a usage vector ``U[0, 1)^E`` with lambda = 0.8, and replaces
     every 4th block of 128 tokens by one hidden vector repeated 128 times.
+  * router variants (``router_variant_weights``): the linear router ``W ~
+    N(0, 0.02^2)`` as above, or the two-layer router's ``W1 [H, d] ~ N(0,
+    0.02^2)`` and ``W2 [E, H]`` Gaussian with each row centred (zero sum) and
+    scaled to unit norm (about N(0, 1/H) per element); a bias ``~ N(0, 0.1^2)``; the
+    LayerNorm's ``gamma ~ 1 + N(0, 0.1^2)`` and ``beta ~ N(0, 0.1^2)``; from a
+    CPU generator with the given seed.
 """
 from __future__ import annotations
 
@@ -113,3 +119,34 @@ def with_shape(shape: MoEShape, **kw) -> MoEShape:
 def bf16_bits(t: torch.Tensor):
     """Raw bf16 bit patterns as a numpy uint16 array (for the oracle)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def router_variant_weights(d: int, E: int, H: int, layernorm: bool, seed: int, bias: bool = True,
+                           beta: bool = True):
+    """Router weights for the router variants: dict(w, w2, bias, gamma, beta) on
+    the CPU (w [E, d] bf16, or W1 [H, d] and w2 [E, H] bf16 when H > 0; gamma and
+    beta [d] fp32 when layernorm; None where not used).  bias=False and
+    beta=False leave out the two terms that give each expert a constant
+    offset, so that the experts' loads stay as even as the plain router's."""
+    g = torch.Generator().manual_seed(seed)
+    if H:
+        w = (torch.randn(H, d, generator=g) * 0.02).to(torch.bfloat16)
+        w2 = torch.randn(E, H, generator=g)
+        # rows centred and of unit norm: silu's outputs have a positive mean,
+        # which a W2 row with a nonzero sum would turn into a constant advantage
+        # for its expert, and a row of larger norm would give its expert a
+        # wider score spread and so more top-k picks
+        if H > 1:
+            w2 = w2 - w2.mean(dim=1, keepdim=True)
+        w2 = (w2 / w2.norm(dim=1, keepdim=True).clamp_min(1e-12)).to(torch.bfloat16)
+    else:
+        w = (torch.randn(E, d, generator=g) * 0.02).to(torch.bfloat16)
+        w2 = None
+    b = torch.randn(E, generator=g) * 0.1 if bias else None
+    gamma = shift = None
+    if layernorm:
+        gamma = 1 + 0.1 * torch.randn(d, generator=g)
+        shift = 0.1 * torch.randn(d, generator=g)
+        if not beta:
+            shift = None
+    return dict(w=w, w2=w2, bias=b, gamma=gamma, beta=shift)

@@ -54,6 +54,8 @@ def _load():
             lib.oracle_route.restype = I
             lib.oracle_router_logits.argtypes = [I, I, I, I, I, ctypes.c_float, P, P, P, P, P, P, P]
             lib.oracle_router_logits.restype = I
+            lib.oracle_layer_backward.argtypes = [I, I, I, I, I, ctypes.c_float] + [P] * 15
+            lib.oracle_layer_backward.restype = I
             lib.oracle_preference.argtypes = [I, P, P]
             lib.oracle_preference.restype = I
             lib.oracle_dispatch.argtypes = [I, I, I, ctypes.c_int64, P, P, P, P, P, P, P, P, P, P]
@@ -306,3 +308,28 @@ def layer_forward(h, wr, w1, w3, w2, k, C, bias=None, usage=None, lam=0.0, token
         tokens = np.arange(T, dtype=np.int32)
     out = combine_rows(h, w1, w3, w2, dsp["assign"], dsp["cw"], tokens)
     return r, dsp, out
+
+
+def layer_backward(h, wr, w1, w3, w2, scores, assign, dout, tau=1.0, dP=None):
+    """Backward pass for a fixed dispatch.  h [T,d], wr [E,d], w1/w3 [E,F,d], w2 [E,d,F]
+    as bf16 bits; scores [T,E] fp32 (the forward's penalised scores); assign [T,k];
+    dout [T,d] fp32; dP [E] (dL/dP of a load-balancing loss) or None.
+    Returns dict(dh, dwr, dbias, dw1, dw3, dw2) in double."""
+    lib = _load()
+    h, wr, w1, w3, w2 = (_c(a, np.uint16) for a in (h, wr, w1, w3, w2))
+    scores = _c(scores, np.float32)
+    assign = _c(assign, np.int32)
+    dout = _c(dout, np.float32)
+    dP = _c(dP, np.float32)
+    T, d = h.shape
+    E, F, _ = w1.shape
+    k = assign.shape[1]
+    out = dict(dh=np.empty((T, d)), dwr=np.empty((E, d)), dbias=np.empty(E), dw1=np.empty((E, F, d)),
+               dw3=np.empty((E, F, d)), dw2=np.empty((E, d, F)))
+    st = lib.oracle_layer_backward(T, d, E, k, F, float(tau), _ptr(h), _ptr(wr), _ptr(w1), _ptr(w3), _ptr(w2),
+                                   _ptr(scores), _ptr(assign), _ptr(dout), _ptr(dP), _ptr(out["dh"]),
+                                   _ptr(out["dwr"]), _ptr(out["dbias"]), _ptr(out["dw1"]), _ptr(out["dw3"]),
+                                   _ptr(out["dw2"]))
+    if st:
+        raise OracleError(st, "layer_backward")
+    return out

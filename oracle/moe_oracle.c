@@ -528,3 +528,122 @@ int oracle_expert_slots_q8(int T, int d, int E, int k, int F, const uint16_t* h,
     const ExpertSet W = {NULL, NULL, NULL, q1, q3, q2, s1, s3, s2, quant_act};
     return expert_slots_x(T, d, E, k, F, h, &W, assign, perm, row0, row1, y_slots);
 }
+
+/* The layer's backward pass, in the order of the forward run backwards:
+ * combine -> down projection -> SwiGLU -> gate and up projections for each
+ * kept (t, r), then the combine weights -> renormalisation -> softmax ->
+ * temperature -> router GEMM for each token. */
+int oracle_layer_backward(int T, int d, int E, int k, int F, float tau, const uint16_t* h,
+                          const uint16_t* wr, const uint16_t* w1, const uint16_t* w3,
+                          const uint16_t* w2, const float* scores, const int32_t* assign,
+                          const float* dout, const float* dP, double* dh, double* dwr,
+                          double* dbias, double* dw1, double* dw3, double* dw2)
+{
+    if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E || F <= 0) return 1;
+    if (!(tau > 0.0f) || isinf(tau)) return 1;
+    const size_t wsz = (size_t)F * d;
+    memset(dh, 0, sizeof(double) * (size_t)T * d);
+    memset(dwr, 0, sizeof(double) * (size_t)E * d);
+    memset(dbias, 0, sizeof(double) * (size_t)E);
+    memset(dw1, 0, sizeof(double) * E * wsz);
+    memset(dw3, 0, sizeof(double) * E * wsz);
+    memset(dw2, 0, sizeof(double) * E * wsz);
+    double* x = (double*)malloc(sizeof(double) * (size_t)d);
+    double* g = (double*)malloc(sizeof(double) * (size_t)F);
+    double* u = (double*)malloc(sizeof(double) * (size_t)F);
+    double* a = (double*)malloc(sizeof(double) * (size_t)F);
+    double* da = (double*)malloc(sizeof(double) * (size_t)F);
+    double* dy = (double*)malloc(sizeof(double) * (size_t)d);
+    double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    double* dp = (double*)malloc(sizeof(double) * (size_t)E);
+    double* cw = (double*)malloc(sizeof(double) * (size_t)k);
+    double* dcw = (double*)malloc(sizeof(double) * (size_t)k);
+    int status = 0;
+    for (int t = 0; t < T && status == 0; ++t) {
+        const uint16_t* ht = h + (size_t)t * d;
+        const float* gt = dout + (size_t)t * d;
+        for (int i = 0; i < d; ++i) x[i] = (double)bf16_to_f32(ht[i]);
+        softmax_row(E, scores + (size_t)t * E, p);
+        /* the renormalised combine weights of t's kept ranks */
+        double S = 0.0;
+        for (int r = 0; r < k; ++r) {
+            const int32_t e = assign[(size_t)t * k + r];
+            if (e < -1 || e >= E) { status = 1; break; }
+            if (e >= 0) S += p[e];
+        }
+        if (status) break;
+        for (int r = 0; r < k; ++r) {
+            const int32_t e = assign[(size_t)t * k + r];
+            cw[r] = (e >= 0 && S > 0.0) ? p[e] / S : 0.0;
+            dcw[r] = 0.0;
+            if (e < 0) continue;
+            const uint16_t* W1 = w1 + (size_t)e * wsz;
+            const uint16_t* W3 = w3 + (size_t)e * wsz;
+            const uint16_t* W2 = w2 + (size_t)e * wsz;
+            /* forward of the expert: g, u, a = silu(g) * u, then dcw = dout . y */
+            for (int j = 0; j < F; ++j) {
+                double gg = 0.0, uu = 0.0;
+                for (int i = 0; i < d; ++i) {
+                    gg += (double)bf16_to_f32(W1[(size_t)j * d + i]) * x[i];
+                    uu += (double)bf16_to_f32(W3[(size_t)j * d + i]) * x[i];
+                }
+                g[j] = gg;
+                u[j] = uu;
+                a[j] = silu(gg) * uu;
+            }
+            for (int c = 0; c < d; ++c) {
+                double y = 0.0;
+                for (int j = 0; j < F; ++j) y += (double)bf16_to_f32(W2[(size_t)c * F + j]) * a[j];
+                dcw[r] += (double)gt[c] * y;
+                dy[c] = cw[r] * (double)gt[c];
+            }
+            /* down projection: da = W2^T dy, dW2 += dy a^T */
+            for (int j = 0; j < F; ++j) da[j] = 0.0;
+            double* DW2 = dw2 + (size_t)e * wsz;
+            for (int c = 0; c < d; ++c) {
+                for (int j = 0; j < F; ++j) {
+                    da[j] += (double)bf16_to_f32(W2[(size_t)c * F + j]) * dy[c];
+                    DW2[(size_t)c * F + j] += dy[c] * a[j];
+                }
+            }
+            /* SwiGLU: a = silu(g) u, silu'(g) = sig(g) (1 + g (1 - sig(g))) */
+            double* DW1 = dw1 + (size_t)e * wsz;
+            double* DW3 = dw3 + (size_t)e * wsz;
+            for (int j = 0; j < F; ++j) {
+                const double sg = 1.0 / (1.0 + exp(-g[j]));
+                const double dg = da[j] * u[j] * sg * (1.0 + g[j] * (1.0 - sg));
+                const double du = da[j] * silu(g[j]);
+                for (int i = 0; i < d; ++i) {
+                    dh[(size_t)t * d + i] += (double)bf16_to_f32(W1[(size_t)j * d + i]) * dg +
+                                             (double)bf16_to_f32(W3[(size_t)j * d + i]) * du;
+                    DW1[(size_t)j * d + i] += dg * x[i];
+                    DW3[(size_t)j * d + i] += du * x[i];
+                }
+            }
+        }
+        /* combine weights -> probabilities: cw_r = p_{e_r} / S over the kept ranks */
+        for (int e = 0; e < E; ++e) dp[e] = dP ? (double)dP[e] / (double)T : 0.0;
+        if (S > 0.0) {
+            double m = 0.0;
+            for (int r = 0; r < k; ++r) m += dcw[r] * cw[r];
+            for (int r = 0; r < k; ++r) {
+                const int32_t e = assign[(size_t)t * k + r];
+                if (e >= 0) dp[e] += (dcw[r] - m) / S;
+            }
+        }
+        /* softmax, then s = z / tau - lambda * usage */
+        double pd = 0.0;
+        for (int e = 0; e < E; ++e) pd += p[e] * dp[e];
+        for (int e = 0; e < E; ++e) {
+            const double dz = p[e] * (dp[e] - pd) / (double)tau;
+            dbias[e] += dz;
+            const uint16_t* we = wr + (size_t)e * d;
+            for (int i = 0; i < d; ++i) {
+                dh[(size_t)t * d + i] += dz * (double)bf16_to_f32(we[i]);
+                dwr[(size_t)e * d + i] += dz * x[i];
+            }
+        }
+    }
+    free(x); free(g); free(u); free(a); free(da); free(dy); free(p); free(dp); free(cw); free(dcw);
+    return status;
+}

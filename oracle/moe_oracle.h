@@ -142,6 +142,30 @@ int oracle_expert_slots_q8(int T, int d, int E, int k, int F, const uint16_t* h,
                            const uint8_t* q2, const float* s2, int quant_act, const int32_t* assign,
                            const int32_t* perm, int row0, int row1, float* y_slots);
 
+/* Backward pass of the layer for one dispatch (training; not on the forward
+ * path).  The forward is out[t] = sum over t's kept ranks r of
+ * cw[t,r] * y_e(h_t) with e = assign[t,r], y_e(x) = W2_e (silu(W1_e x) * W3_e x),
+ * cw[t,r] = p[t,e] / sum over t's kept ranks r' of p[t,assign[t,r']] (the
+ * renormalised weights, [mhpn] §4.3), p = softmax(s) over the experts, s =
+ * z / tau - lambda * usage, z = h W_r^T + bias ([coreui] §3.1, [cnnetsun]
+ * §3.1).  The routing decisions (assign) are held fixed: the top-k choice and
+ * the capacity are piecewise constant, so gradients flow through the combine
+ * weights and the experts only.  The load-balancing loss of the pages comes in
+ * through its gradient with respect to the mean probabilities P_i = mean_t
+ * p[t,i] ([coreui] §3.1 writes it from the per-batch mean probabilities;
+ * [2kiu] §2 and [mhpn] §3 give other forms of the same sum of squared loads):
+ * dP [E] (NULL = none) adds dP_i / T to every dL/dp[t,i].
+ * Inputs: h [T,d], wr [E,d], w1, w3 [E,F,d], w2 [E,d,F] bf16 bits; scores
+ * [T,E] the forward's penalised scores s (fp32); assign [T,k] (-1 =
+ * dropped); dout [T,d] = dL/dout (fp32).
+ * Outputs (double, all required, overwritten): dh [T,d], dwr [E,d], dbias [E],
+ * dw1, dw3 [E,F,d], dw2 [E,d,F].  Returns 0 or 1 (bad argument). */
+int oracle_layer_backward(int T, int d, int E, int k, int F, float tau, const uint16_t* h,
+                          const uint16_t* wr, const uint16_t* w1, const uint16_t* w3,
+                          const uint16_t* w2, const float* scores, const int32_t* assign,
+                          const float* dout, const float* dP, double* dh, double* dwr,
+                          double* dbias, double* dw1, double* dw3, double* dw2);
+
 #ifdef __cplusplus
 }
 #endif

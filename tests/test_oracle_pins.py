@@ -730,3 +730,107 @@ def test_temperature_sharpens_softmax():
 def test_temperature_must_be_positive(tau):
     with pytest.raises(oracle.OracleError):
         oracle.route(1, logits_in=np.zeros((2, 3), np.float32), tau=tau)
+
+
+# --------------------------------------------------------------------------- backward
+# The layer's gradients for a fixed dispatch, against torch autograd on a plain
+# torch forward (double): the routing decisions are held fixed, the combine
+# weights are the renormalised softmax probabilities of the kept experts, and a
+# load-balancing term sum_i dP_i * P_i brings in the gradient of an aux loss.
+
+def _torch_backward(h, wr, b, w1, w3, w2, usage, lam, tau, k, C, dout, dP):
+    dd = lambda a: torch.from_numpy(np.asarray(a, np.float64)).requires_grad_(True)
+    H, WR, B = dd(widen(h)), dd(widen(wr)), dd(b)
+    W1, W3, W2 = dd(widen(w1)), dd(widen(w3)), dd(widen(w2))
+    z = H @ WR.T + B
+    s = z / tau - lam * torch.from_numpy(usage.astype(np.float64))
+    s_used = s + (s.detach().float().double() - s.detach())   # the fp32 scores, gradient unchanged
+    scores = s_used.detach().float().numpy()
+    assign = oracle.dispatch(scores, k, C)["assign"]
+    p = torch.softmax(s_used, dim=1)
+    T = h.shape[0]
+    rows = []
+    for t in range(T):
+        kept = [int(e) for e in assign[t] if e >= 0]
+        acc = torch.zeros(H.shape[1], dtype=torch.float64)
+        if kept:
+            S = sum(p[t, e] for e in kept)
+            for e in kept:
+                a = torch.nn.functional.silu(W1[e] @ H[t]) * (W3[e] @ H[t])
+                acc = acc + p[t, e] / S * (W2[e] @ a)
+        rows.append(acc)
+    out = torch.stack(rows)
+    L = (out * torch.from_numpy(dout.astype(np.float64))).sum() + (torch.from_numpy(dP.astype(np.float64)) *
+                                                                   p.mean(dim=0)).sum()
+    grads = torch.autograd.grad(L, [H, WR, B, W1, W3, W2])
+    return scores, assign, [g.numpy() for g in grads]
+
+
+@pytest.mark.parametrize("T,d,E,F,k,C,lam,tau", [(24, 16, 5, 12, 2, 8, 0.3, 0.7),
+                                                 (20, 16, 4, 8, 1, 4, 0.0, 1.0),
+                                                 (18, 8, 6, 8, 3, 6, 0.5, 2.0),
+                                                 (16, 8, 4, 8, 2, 2, 0.0, 0.5)])
+def test_backward_matches_torch_autograd(T, d, E, F, k, C, lam, tau):
+    tau = float(np.float32(tau))   # the temperature is an fp32 value of the config
+    rng = np.random.default_rng(T * 31 + E)
+    h = bf16(rng.standard_normal((T, d)))
+    wr = bf16(rng.standard_normal((E, d)) * 0.5)
+    b = rng.standard_normal(E).astype(np.float32) * 0.1
+    w1 = bf16(rng.standard_normal((E, F, d)) / math.sqrt(d))
+    w3 = bf16(rng.standard_normal((E, F, d)) / math.sqrt(d))
+    w2 = bf16(rng.standard_normal((E, d, F)) / math.sqrt(F))
+    usage = rng.random(E).astype(np.float32)
+    dout = rng.standard_normal((T, d)).astype(np.float32)
+    dP = rng.standard_normal(E).astype(np.float32)
+    scores, assign, want = _torch_backward(h, wr, b, w1, w3, w2, usage, lam, tau, k, C, dout, dP)
+    # the cases exercise reroutes and drops
+    dsp = oracle.dispatch(scores, k, C)
+    assert dsp["n_rerouted"] + dsp["n_dropped"] > 0
+    g = oracle.layer_backward(h, wr, w1, w3, w2, scores, assign, dout, tau=tau, dP=dP)
+    for name, ref in zip(["dh", "dwr", "dbias", "dw1", "dw3", "dw2"], want):
+        np.testing.assert_allclose(g[name], ref, rtol=1e-9, atol=1e-12, err_msg=name)
+
+
+def test_backward_dense_swiglu_is_torch_autograd():
+    """E = 1, k = 1, no drops: the combine weight is 1 and the router gets no
+    gradient; the expert gradients are those of a dense SwiGLU FFN."""
+    rng = np.random.default_rng(40)
+    T, d, F = 7, 16, 24
+    h = bf16(rng.standard_normal((T, d)))
+    wr = bf16(rng.standard_normal((1, d)))
+    w1 = bf16(rng.standard_normal((1, F, d)) / 4)
+    w3 = bf16(rng.standard_normal((1, F, d)) / 4)
+    w2 = bf16(rng.standard_normal((1, d, F)) / 4)
+    dout = rng.standard_normal((T, d)).astype(np.float32)
+    g = oracle.layer_backward(h, wr, w1, w3, w2, np.zeros((T, 1), np.float32), np.zeros((T, 1), np.int32), dout)
+    x = torch.from_numpy(widen(h)).double().requires_grad_(True)
+    m1, m3, m2 = (torch.from_numpy(widen(w)[0]).double().requires_grad_(True) for w in (w1, w3, w2))
+    y = (torch.nn.functional.silu(x @ m1.T) * (x @ m3.T)) @ m2.T
+    gx, g1, g3, g2 = torch.autograd.grad((y * torch.from_numpy(dout).double()).sum(), [x, m1, m3, m2])
+    np.testing.assert_allclose(g["dh"], gx.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g["dw1"][0], g1.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g["dw3"][0], g3.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g["dw2"][0], g2.numpy(), rtol=1e-10, atol=1e-12)
+    assert np.all(g["dwr"] == 0) and np.all(g["dbias"] == 0)
+
+
+def test_backward_dropped_token_gets_only_the_aux_gradient():
+    # C = 0: every pick is dropped, the output is 0; only dP reaches the router
+    rng = np.random.default_rng(41)
+    T, d, E, F = 5, 8, 3, 8
+    h = bf16(rng.standard_normal((T, d)))
+    wr = bf16(rng.standard_normal((E, d)))
+    w = bf16(rng.standard_normal((E, F, d)))
+    w2 = bf16(rng.standard_normal((E, d, F)))
+    s = rng.standard_normal((T, E)).astype(np.float32)
+    assign = np.full((T, 2), -1, np.int32)
+    dout = rng.standard_normal((T, d)).astype(np.float32)
+    g0 = oracle.layer_backward(h, wr, w, w, w2, s, assign, dout)
+    assert np.all(g0["dh"] == 0) and np.all(g0["dw1"] == 0) and np.all(g0["dw2"] == 0) and np.all(g0["dwr"] == 0)
+    dP = np.array([1.0, -2.0, 0.5], np.float32)
+    g1 = oracle.layer_backward(h, wr, w, w, w2, s, assign, dout, dP=dP)
+    # dL/dz[t,i] = p_i (dP_i - sum_j p_j dP_j) / T; the bias gradient sums it over t
+    p = np.exp(s - s.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    dz = p * (dP - (p * dP).sum(1, keepdims=True)) / T
+    np.testing.assert_allclose(g1["dbias"], dz.sum(0), rtol=1e-6)

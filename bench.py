@@ -43,6 +43,9 @@ CLOCK_LEAD_S = 0.25  # untimed lead-in for clock samples when the timed region i
 CHUNK = 256  # tokens per routing chunk; a batch of one chunk routes and dispatches in one kernel
 
 
+BACKWARD_KERNELS = 8   # fill, pad, SwiGLU backward, router backward, dh, two widenings, bias sum
+
+
 def kernels_per_step(T, fp8=False, norm=0, hidden=0):
     """Kernels of this library one layer step launches."""
     # router GEMM, row gather, gate-up, down, combine + route and dispatch:
@@ -65,6 +68,9 @@ def parse():
     ap.add_argument("--fp8-weights", action="store_true",
                     help="expert GEMMs in e4m3: weights quantised per row once (moe_quantize_fp8), "
                          "token and activation rows per row on the fly")
+    ap.add_argument("--backward", action="store_true",
+                    help="time a training step of the layer: the forward, then moe_layer_backward "
+                         "(dL/dout drawn once; every gradient written each step)")
     ap.add_argument("--tau", type=float, default=1.0, help="router temperature")
     ap.add_argument("--router-norm", default="none", choices=["none", "layer", "l2"],
                     help="normalise the token rows before the router (LayerNorm or L2)")
@@ -305,9 +311,17 @@ def run_ours(args, rank, world, local):
         wr = moe.Router(**{n: (None if v is None else v.cuda()) for n, v in rw.items()})
         bias = None
         router_desc = {"tau": args.tau, "norm": args.router_norm, "hidden": hidden}
-    cfg = moe.Config.of(shape, flags=moe.FLAG_FP8 if fp8 else 0, tau=args.tau, router_norm=norm,
+    bwd = args.backward
+    if bwd and (fp8 or norm or hidden):
+        raise SystemExit("--backward runs with bf16 experts and the linear router")
+    flags = (moe.FLAG_FP8 if fp8 else 0) | (moe.FLAG_BACKWARD if bwd else 0)
+    cfg = moe.Config.of(shape, flags=flags, tau=args.tau, router_norm=norm,
                         norm_eps=1e-5 if norm == moe.NORM_LAYER else 1e-12, router_hidden=hidden)
     ws = moe.workspace(cfg)
+    dout = None
+    if bwd:   # dL/dout ~ N(0, 1), bf16, drawn once
+        dout = torch.randn(shape.T, shape.d, generator=torch.Generator().manual_seed(shape.seed + 3))
+        dout = dout.to(torch.bfloat16).cuda()
     out = torch.empty(shape.T, shape.d, dtype=torch.bfloat16, device="cuda")
     # kept rows of this batch (routing is deterministic, identical every step)
     _, aux = moe.layer_forward(cfg, ws, L["h"], wr, L["w13"], L["w2"], bias, L["usage"],
@@ -319,9 +333,13 @@ def run_ours(args, rank, world, local):
     if st != 0:
         raise RuntimeError(f"device status {st} ({moe.STATUS.get(st)})")
 
-    def step(evs=None):
+    def step(evs=None, bev=None):
         moe.layer_forward(cfg, ws, L["h"], wr, L["w13"], L["w2"], bias, L["usage"],
                           stage_events=evs, out=out)
+        if bwd:
+            moe.layer_backward(cfg, ws, L["h"], L["wr"], L["w13"], L["w2"], dout)
+            if bev is not None:
+                bev.record()
 
     w0 = torch.cuda.Event(enable_timing=True)
     w1 = torch.cuda.Event(enable_timing=True)
@@ -333,6 +351,7 @@ def run_ours(args, rank, world, local):
     step_ms = w0.elapsed_time(w1) / max(args.warmup, 1)
     stage_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)]
                  for _ in range(args.steps)]
+    bwd_evs = [torch.cuda.Event(enable_timing=True) if bwd else None for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -351,7 +370,7 @@ def run_ours(args, rank, world, local):
         step()
     t0.record()
     for i in range(args.steps):
-        step(stage_evs[i])
+        step(stage_evs[i], bwd_evs[i])
     t1.record()
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -369,6 +388,9 @@ def run_ours(args, rank, world, local):
     stage_ms = {n: statistics.mean(stage_evs[i][j].elapsed_time(stage_evs[i][j + 1])
                                    for i in range(args.steps))
                 for j, n in enumerate(moe.STAGE_NAMES)}
+    if bwd:
+        stage_ms["backward"] = statistics.mean(stage_evs[i][-1].elapsed_time(bwd_evs[i])
+                                               for i in range(args.steps))
 
     # end to end from pinned host memory through moe_layer_forward_host (FP8
     # weights: the same copies around moe_layer_forward_fp8, from Python)
@@ -376,8 +398,16 @@ def run_ours(args, rank, world, local):
     o_host = torch.empty(shape.T, shape.d, dtype=torch.bfloat16).pin_memory()
     h_dev = torch.empty_like(L["h"])
 
+    dh_host = torch.empty(shape.T, shape.d, dtype=torch.float32).pin_memory() if bwd else None
+
     def e2e_step():
-        if fp8 or variant:
+        if bwd:   # h in, forward, backward, dL/dh out
+            h_dev.copy_(h_host, non_blocking=True)
+            moe.layer_forward(cfg, ws, h_dev, wr, L["w13"], L["w2"], bias, L["usage"], out=out)
+            g = moe.layer_backward(cfg, ws, h_dev, L["wr"], L["w13"], L["w2"], dout)
+            dh_host.copy_(g["dh"], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        elif fp8 or variant:
             h_dev.copy_(h_host, non_blocking=True)
             moe.layer_forward(cfg, ws, h_dev, wr, L["w13"], L["w2"], bias, L["usage"], out=out)
             o_host.copy_(out, non_blocking=True)
@@ -422,6 +452,20 @@ def run_ours(args, rank, world, local):
     roof["traffic"] = recorded_traffic(kname, shape.name)
     roof["kernel"] = kname
     roof["algorithmic_per_launch"] = {"flop": flops[dom], "bytes": bytes_[dom]}
+    bwd_line = None
+    if bwd:
+        # the backward's GEMM work on the kept rows: g and u recomputed (2 d 2F), W2^T dout
+        # (2 d F), dx (2 2F d), dW2 (2 d F), dW13 (2 2F d) per row; the padded rows of each
+        # expert's block (E x C rows in all) are extra work the GEMMs also do
+        bflops = 16.0 * kept * d * F
+        sec_b = stage_ms["backward"] * 1e-3
+        cap = moe.capacity(shape.T, shape.k, shape.E, shape.cf, shape.capacity)
+        rows_pad = shape.E * min(cap, shape.T)
+        bwd_line = {"stage_ms": stage_ms["backward"], "algorithmic_tflop": bflops / 1e12,
+                    "achieved_tflops": bflops / sec_b / 1e12, "peak": peak_tf,
+                    "frac": bflops / sec_b / 1e12 / peak_tf, "padded_rows": rows_pad, "kept_rows": kept,
+                    "gemms": "cuBLAS strided-batched (bf16 in, fp32 accumulate)",
+                    "kernels": "this library's: pad, SwiGLU backward, router backward, dh, bias sum"}
     expert_tflops = (flops["gate_up"] + flops["down"]) / (
         (stage_ms["gate_up"] + stage_ms["down"]) * 1e-3) / 1e12
     weight_bytes = 3.0 * active * F * d * wb
@@ -440,10 +484,14 @@ def run_ours(args, rank, world, local):
         "stages_ms": stage_ms, "kept_rows": kept,
         "clocks": clk,
         "e2e": ({"value": world * T * args.e2e_steps / te, "unit": UNIT,
-                 "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2}
+                 "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * (4 if bwd else 2)}
                 if args.e2e_steps > 0 else None),
-        "gpu_launches": kernels_per_step(shape.T, fp8, norm, hidden) * args.steps,
+        "gpu_launches": (kernels_per_step(shape.T, fp8, norm, hidden) + (BACKWARD_KERNELS if bwd else 0))
+        * args.steps,
     }
+    if bwd:
+        line["metric"] = METRIC + " (training step: forward + backward)"
+        line["backward"] = bwd_line
     if want_cpu:
         res = oracle_sample(shape, L["h"].cpu(), L["wr"].cpu(),
                             None if L["bias"] is None else L["bias"].cpu(),

@@ -60,6 +60,9 @@ typedef enum {
  * T*k*(d_ff + 12) bytes for the e4m3 activation rows, their scales and row
  * maxima). */
 #define MOE_FLAG_FP8 1u
+/* moe_config_t.flags: size the workspace for moe_layer_backward too (adds
+ * about E*C*(8d + 18F) bytes, C the capacity, plus T*(4d + 4E + 4k) + 4E*d). */
+#define MOE_FLAG_BACKWARD 2u
 
 /* Layer shape.  Capacity C = ceil(T*k*cf/E) unless capacity > 0. */
 typedef struct {
@@ -71,7 +74,7 @@ typedef struct {
     double cf;        /* capacity factor, read as a decimal with 6 fractional digits */
     int32_t capacity; /* > 0: explicit per-expert capacity, overrides cf */
     float lambda;     /* load-penalty weight (0 = no penalty) */
-    uint32_t flags;   /* 0, or MOE_FLAG_FP8 */
+    uint32_t flags;   /* 0, or MOE_FLAG_FP8 and/or MOE_FLAG_BACKWARD */
     /* Router variants (all zero: the plain linear router, no temperature). */
     float tau;              /* temperature, 0 (= 1) or finite > 0: s = z / tau - lambda*usage */
     uint32_t router_norm;   /* MOE_ROUTER_NORM_*: normalisation of h before the router */
@@ -311,6 +314,35 @@ moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* h_host,
                                     const float* usage_dev, const void* w13_dev,
                                     const void* w2_dev, void* out_host,
                                     void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Backward pass of moe_layer_forward (training; not on the forward path).
+ * The routing decisions of the forward are held fixed (top-k and capacity are
+ * piecewise constant); gradients flow through the experts and through the
+ * combine weights cw[t,r] = p[t,e_r] / sum over t's kept ranks of p ([mhpn]
+ * §4.3) into the softmax, the temperature and the router GEMM ([coreui] §3.1).
+ *   ws_dev    the workspace of the moe_layer_forward call (bf16 experts, the
+ *             linear router) whose gradients these are, sized with
+ *             MOE_FLAG_BACKWARD, untouched by any other call since: the
+ *             forward's scores, kept-slot order and combine weights are read
+ *             from it.
+ *   h_dev, w_router_dev, w13_dev, w2_dev   the forward's inputs (bf16)
+ *   dout_dev  [T, d] bf16: dL/dout
+ *   dP_dev    [E] fp32 or NULL: dL/dP for a load-balancing loss written from
+ *             the mean probabilities P_i = mean_t p[t,i] ([coreui] §3.1; e.g.
+ *             2*alpha*P_i for alpha * sum_i P_i^2); adds dP_i / T to dL/dp[t,i]
+ * Outputs (fp32, overwritten): dh_dev [T, d]; dw_router_dev [E, d] and
+ * dbias_dev [E] (each may be NULL); dw13_dev [E, 2F, d] in the packed W13
+ * layout (moe_pack_w13); dw2_dev [E, d, F].
+ * Each expert's kept rows are padded to C rows for strided-batched GEMMs;
+ * those plain GEMMs run in cuBLAS (the first call on a device creates its
+ * cuBLAS handle), the rest in this library's kernels.  Requires
+ * MOE_FLAG_BACKWARD (MOE_ERR_INVALID_ARG otherwise), router_norm = 0 and
+ * router_hidden = 0 (MOE_ERR_UNSUPPORTED otherwise). */
+moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* h_dev, const void* w_router_dev,
+                                const void* w13_dev, const void* w2_dev, const void* dout_dev,
+                                const float* dP_dev, float* dh_dev, float* dw_router_dev,
+                                float* dbias_dev, float* dw13_dev, float* dw2_dev, void* ws_dev,
+                                size_t ws_bytes, void* stream);
 
 /* Failure-path check: launches one kernel whose bounded wait has nothing to
  * wait for; after `budget_cycles` SM clock cycles it records MOE_ERR_TIMEOUT

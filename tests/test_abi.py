@@ -64,7 +64,7 @@ def test_workspace_size(L):
         c = _cfg(**bad)
         assert L.moe_workspace_size(ctypes.byref(c)) == 0, bad
     c = _cfg()
-    c.flags = 2   # not a defined flag
+    c.flags = 4   # not a defined flag
     assert L.moe_workspace_size(ctypes.byref(c)) == 0
     # MOE_FLAG_FP8 adds the e4m3 activation rows and the row scales
     c = _cfg()
@@ -72,6 +72,10 @@ def test_workspace_size(L):
     c.flags = moe.FLAG_FP8
     grown = L.moe_workspace_size(ctypes.byref(c))
     assert grown >= base + c.T * c.k * (c.d_ff + 8)
+    # MOE_FLAG_BACKWARD adds the padded per-expert blocks (E x C rows)
+    c.flags = moe.FLAG_BACKWARD
+    cap = moe.capacity(c.T, c.k, c.E, c.cf)
+    assert L.moe_workspace_size(ctypes.byref(c)) >= base + c.E * cap * (8 * c.d_model + 18 * c.d_ff)
 
 
 FAKE = 0x7f0000000000  # never dereferenced: every case below fails validation first
@@ -171,3 +175,19 @@ def test_router_variant_argument_checks(L):
     lf = lambda s13, s2: L.moe_layer_forward_router(ctypes.byref(c), P(FAKE), ctypes.byref(r), None, P(FAKE),
                                                     s13, P(FAKE), s2, P(FAKE), *([None] * 8), P(FAKE), n, None)
     assert lf(P(FAKE), None) == 1
+
+
+def test_backward_argument_checks(L):
+    P = ctypes.c_void_p
+    c = _cfg(flags=moe.FLAG_BACKWARD)
+    n = L.moe_workspace_size(ctypes.byref(c))
+    ptrs = lambda **o: [P(o.get(k, FAKE)) if o.get(k, FAKE) is not None else None
+                        for k in ("h", "wr", "w13", "w2", "dout")] + [None] + \
+        [P(o.get(k, FAKE)) if o.get(k, FAKE) is not None else None for k in ("dh", "dwr", "db", "dw13", "dw2")]
+    call = lambda cfg, nb=n, **o: L.moe_layer_backward(ctypes.byref(cfg), *ptrs(**o), P(FAKE), nb, None)
+    assert call(_cfg()) == 1                       # workspace not sized for the backward
+    assert call(c, dout=None) == 1
+    assert call(c, dw2=None) == 1
+    assert call(c, dh=FAKE + 4) == 3
+    assert call(c, nb=n - 256) == 4
+    assert call(_cfg(flags=moe.FLAG_BACKWARD, router_hidden=16)) == 2

@@ -26,7 +26,7 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 moe_status_t check_config(const moe_config_t* c, bool need_ff)
 {
     if (!c) return MOE_ERR_INVALID_ARG;
-    if ((c->flags & ~MOE_FLAG_FP8) != 0) return MOE_ERR_INVALID_ARG;
+    if ((c->flags & ~(MOE_FLAG_FP8 | MOE_FLAG_BACKWARD)) != 0) return MOE_ERR_INVALID_ARG;
     if (c->T < 0 || c->E <= 0 || c->k <= 0) return MOE_ERR_INVALID_ARG;
     if (c->k > c->E) return MOE_ERR_INVALID_ARG;
     if (c->capacity < 0) return MOE_ERR_INVALID_ARG;
@@ -59,6 +59,13 @@ moe_status_t check_ws(const moe_config_t* c, void* ws, size_t ws_bytes, WsLayout
 int64_t capacity_of(const moe_config_t& c)
 {
     return moe_capacity(c.T, c.k, c.E, c.cf, c.capacity);
+}
+
+// Rows of each expert's padded block in the backward pass: an expert holds at
+// most C slots, and at most one per token.
+long long backward_rows(const moe_config_t& c)
+{
+    return std::min<long long>(capacity_of(c), std::max(c.T, 0));
 }
 
 struct Ev {
@@ -146,6 +153,8 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
     }
     if (c.router_norm != MOE_ROUTER_NORM_NONE) w.xn = take(T * d * 2);
     if (c.router_hidden > 0) w.zr = take(T * E * 4);
+    if (c.flags & MOE_FLAG_BACKWARD)
+        w.bwd = take(backward_bytes(static_cast<long long>(T), c.d_model, c.E, c.k, c.d_ff, backward_rows(c)));
     w.h_stage = take(T * d * 2);
     w.out_stage = take(T * d * 2);
     w.total = off;
@@ -771,6 +780,59 @@ moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* h_host,
     if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     return cuda_status(cudaStreamSynchronize(s));
+}
+
+moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* h, const void* w_router, const void* w13,
+                                const void* w2, const void* dout, const float* dP, float* dh, float* dw_router,
+                                float* dbias, float* dw13, float* dw2, void* ws, size_t ws_bytes, void* stream)
+{
+    moe_status_t st = check_config(cfg, true);
+    if (st != MOE_OK) return st;
+    if (!(cfg->flags & MOE_FLAG_BACKWARD)) return MOE_ERR_INVALID_ARG;
+    if (cfg->router_norm != MOE_ROUTER_NORM_NONE || cfg->router_hidden != 0) return MOE_ERR_UNSUPPORTED;
+    const bool any = cfg->T > 0;   // with no tokens only the weight gradients (zeros) are written
+    if (!w_router || !w13 || !w2 || !dw13 || !dw2 || (any && (!h || !dout || !dh))) return MOE_ERR_INVALID_ARG;
+    if (!aligned(w_router, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(dw13, 16) || !aligned(dw2, 16) ||
+        (any && (!aligned(h, 16) || !aligned(dout, 16) || !aligned(dh, 16))))
+        return MOE_ERR_MISALIGNED;
+    WsLayout L;
+    st = check_ws(cfg, ws, ws_bytes, &L);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const moe_config_t& c = *cfg;
+    if (!any) {   // no tokens: every gradient is zero
+        const size_t wbytes = static_cast<size_t>(c.E) * c.d_ff * c.d_model * 4;
+        if (cudaMemsetAsync(dw13, 0, 2 * wbytes, s) != cudaSuccess || cudaMemsetAsync(dw2, 0, wbytes, s) != cudaSuccess ||
+            (dw_router && cudaMemsetAsync(dw_router, 0, sizeof(float) * c.E * c.d_model, s) != cudaSuccess) ||
+            (dbias && cudaMemsetAsync(dbias, 0, sizeof(float) * c.E, s) != cudaSuccess))
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    BackwardArgs a{};
+    a.T = c.T;
+    a.E = c.E;
+    a.k = c.k;
+    a.d = c.d_model;
+    a.F = c.d_ff;
+    a.C = backward_rows(c);
+    a.tau = c.tau;
+    a.scores = ws_at<float>(ws, L.scores);
+    a.perm = ws_at<int32_t>(ws, L.perm);
+    a.offsets = ws_at<int32_t>(ws, L.offsets);
+    a.cw = ws_at<float>(ws, L.cw);
+    a.h = h;
+    a.w_router = w_router;
+    a.w13 = w13;
+    a.w2 = w2;
+    a.dout = dout;
+    a.dP = dP;
+    a.dh = dh;
+    a.dw_router = dw_router;
+    a.dbias = dbias;
+    a.dw13 = dw13;
+    a.dw2 = dw2;
+    a.scratch = ws_at<void>(ws, L.bwd);
+    return cuda_status(run_backward(a, s));
 }
 
 moe_status_t moe_debug_timeout_probe(void* ws, size_t ws_bytes, int64_t budget_cycles, void* stream)

@@ -31,6 +31,7 @@ struct WsLayout {
     // of both GEMMs' activations (the gate-up codes reuse the xg region)
     size_t act_q = 0, x_scale = 0, act_scale = 0, act_amax = 0;
     size_t xn = 0;     // router input after normalisation [T, d] bf16 (router_norm != 0)
+    size_t bwd = 0;    // backward scratch (MOE_FLAG_BACKWARD)
     size_t zr = 0;     // two-layer router logits [T, E] fp32 (router_hidden > 0)
     int nr = 0;        // router GEMM output columns: E, or the hidden width H
     size_t total = 0;
@@ -172,6 +173,32 @@ cudaError_t launch_router_head(int T, int E, int H, int splits, const float* par
 // z [T, E] = the sum of the splits x [T, E] partials (split order) + bias.
 cudaError_t launch_router_sum(int T, int E, int splits, const float* part, const float* bias, float* z,
                               cudaStream_t s);
+// The backward pass (backward.cu).  Reads the forward's routing state (scores, perm,
+// offsets, cw) and writes the gradients; scratch holds backward_bytes(...) bytes.
+struct BackwardArgs {
+    int T, E, k, d, F;
+    long long C;             // capacity: the rows of each expert's padded block
+    float tau;               // 0 or 1: none
+    const float* scores;     // [T, E] the forward's penalised scores
+    const int32_t* perm;     // kept slots in slot order: t*k + r
+    const int32_t* offsets;  // [E + 1]
+    const float* cw;         // [T, k] combine weights
+    const void* h;           // [T, d] bf16
+    const void* w_router;    // [E, d] bf16
+    const void* w13;         // [E, 2F, d] bf16
+    const void* w2;          // [E, d, F] bf16
+    const void* dout;        // [T, d] bf16
+    const float* dP;         // [E] or NULL
+    float* dh;               // [T, d]
+    float* dw_router;        // [E, d] or NULL
+    float* dbias;            // [E] or NULL
+    float* dw13;             // [E, 2F, d]
+    float* dw2;              // [E, d, F]
+    void* scratch;
+};
+size_t backward_bytes(long long T, int d, int E, int k, int F, long long C);
+cudaError_t run_backward(const BackwardArgs& a, cudaStream_t s);
+
 cudaError_t launch_timeout_probe(int* status, long long budget, cudaStream_t s);
 
 }  // namespace moe

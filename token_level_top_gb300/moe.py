@@ -74,6 +74,7 @@ class Config:
 
 
 FLAG_FP8 = 1   # MOE_FLAG_FP8
+FLAG_BACKWARD = 2   # MOE_FLAG_BACKWARD
 NORM_NONE, NORM_LAYER, NORM_L2 = 0, 1, 2   # MOE_ROUTER_NORM_*
 
 
@@ -119,6 +120,7 @@ _SIGS = {
     "moe_expert_ffn_fp8": (I32, [CFG, P, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_layer_forward_fp8": (I32, [CFG] + [P] * 18 + [SZ, P]),
     "moe_router_logits": (I32, [CFG, P, RTR, P, P, SZ, P]),
+    "moe_layer_backward": (I32, [CFG] + [P] * 12 + [SZ, P]),
     "moe_layer_forward_router": (I32, [CFG, P, RTR] + [P] * 15 + [SZ, P]),
 }
 
@@ -333,6 +335,26 @@ def layer_forward(cfg: Config, ws, h, wr, w13, w2, bias=None, usage=None, aux=Fa
                                      _p(w2), *tail)
     _check(st, "moe_layer_forward")
     return (out, extras) if aux else out
+
+
+def layer_backward(cfg: Config, ws, h, wr, w13, w2, dout, dP=None, router_grads=True):
+    """Gradients of the layer for the forward last run in ws (cfg with FLAG_BACKWARD):
+    dict(dh [T,d], dw13 [E,2F,d], dw2 [E,d,F], dwr [E,d], dbias [E]), all fp32.
+    dout [T,d] bf16; dP [E] fp32 = dL/dP of a load-balancing loss, or None."""
+    dev = ws.device
+    T, d, E, F = cfg.T, cfg.d_model, cfg.E, cfg.d_ff
+    g = dict(dh=torch.empty(T, d, dtype=torch.float32, device=dev),
+             dw13=torch.empty(E, 2 * F, d, dtype=torch.float32, device=dev),
+             dw2=torch.empty(E, d, F, dtype=torch.float32, device=dev))
+    if router_grads:
+        g["dwr"] = torch.empty(E, d, dtype=torch.float32, device=dev)
+        g["dbias"] = torch.empty(E, dtype=torch.float32, device=dev)
+    c = cfg.c()
+    st = lib().moe_layer_backward(ctypes.byref(c), _p(h), _p(wr), _p(w13), _p(w2), _p(dout), _p(dP), _p(g["dh"]),
+                                  _p(g.get("dwr")), _p(g.get("dbias")), _p(g["dw13"]), _p(g["dw2"]), _p(ws),
+                                  ws.numel(), _stream())
+    _check(st, "moe_layer_backward")
+    return g
 
 
 def layer_forward_host(cfg: Config, ws, h_host, wr, w13, w2, out_host, bias=None, usage=None):

@@ -61,7 +61,9 @@ typedef enum {
  * maxima). */
 #define MOE_FLAG_FP8 1u
 /* moe_config_t.flags: size the workspace for moe_layer_backward too (adds
- * about E*C*(8d + 18F) bytes, C the capacity, plus T*(4d + 4E + 4k) + 4E*d). */
+ * about E*C'*(8d + 10F) + T*k*8F + T*(4d + 4E + 4k) + 4E*d bytes, C' =
+ * min(C, T)); moe_layer_forward then also keeps each kept row's g and u (fp32)
+ * there for the backward. */
 #define MOE_FLAG_BACKWARD 2u
 
 /* Layer shape.  Capacity C = ceil(T*k*cf/E) unless capacity > 0. */
@@ -323,8 +325,8 @@ moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* h_host,
  *   ws_dev    the workspace of the moe_layer_forward call (bf16 experts, the
  *             linear router) whose gradients these are, sized with
  *             MOE_FLAG_BACKWARD, untouched by any other call since: the
- *             forward's scores, kept-slot order and combine weights are read
- *             from it.
+ *             forward's scores, kept-slot order, combine weights and the
+ *             gate and up projections g, u of each kept row are read from it.
  *   h_dev, w_router_dev, w13_dev, w2_dev   the forward's inputs (bf16)
  *   dout_dev  [T, d] bf16: dL/dout
  *   dP_dev    [E] fp32 or NULL: dL/dP for a load-balancing loss written from

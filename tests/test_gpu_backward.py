@@ -1,10 +1,11 @@
 """GPU parity of the layer's backward pass (moe_layer_backward) against the oracle.
 
 The oracle takes the forward's penalised scores (re-derived from the GPU's logits, bit-exact)
-and its assignment, and computes every gradient in double.  The GPU keeps the gathered and
-intermediate rows in bf16 (x, dL/dout, cw*a, dg, du) with fp32 accumulation, so the gradients
-agree within the layer's 2e-2 relative Frobenius bound; the router's gradients, formed from fp32
-probabilities and fp32 dcw, agree far closer.
+and its assignment, and computes every gradient in double.  The GPU keeps the gathered rows and
+the operands of the weight and input gradients in bf16 (x, dL/dout, cw*a, dg, du) with fp32
+accumulation, so those gradients agree within the layer's 2e-2 relative Frobenius bound.  The
+router's gradients depend on differences dcw_r - sum_r' cw_r' dcw_r' of dot products that can
+cancel, so their inputs stay fp32 (the forward's g and u, W2^T dL/dout): they agree to 1e-3.
 
 At the benchmark sizes, dL/dout is zero outside a sample of tokens (and there is no
 load-balancing term): every gradient then comes from the sampled tokens alone, so the oracle run

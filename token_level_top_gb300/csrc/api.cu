@@ -153,6 +153,7 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
     }
     if (c.router_norm != MOE_ROUTER_NORM_NONE) w.xn = take(T * d * 2);
     if (c.router_hidden > 0) w.zr = take(T * E * 4);
+    if (c.flags & MOE_FLAG_BACKWARD) w.gu = take(T * k * 2 * F * 4);
     if (c.flags & MOE_FLAG_BACKWARD)
         w.bwd = take(backward_bytes(static_cast<long long>(T), c.d_model, c.E, c.k, c.d_ff, backward_rows(c)));
     w.h_stage = take(T * d * 2);
@@ -406,6 +407,7 @@ moe_status_t run_experts(const moe_config_t& c, const WsLayout& L, const void* h
     g.offsets = offsets;
     g.perm = perm;
     g.act = act;
+    if (c.flags & MOE_FLAG_BACKWARD) g.gu_save = ws_at<void>(ws, L.gu);   // kept for moe_layer_backward
     if (launch_gemm(g, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (ev) ev->mark(4);
     GemmLaunch g2 = expert_gemm(c, L, GK_DOWN_SLOTS, ws);
@@ -825,6 +827,7 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* h, const vo
     a.w13 = w13;
     a.w2 = w2;
     a.dout = dout;
+    a.gu = ws_at<float>(ws, L.gu);
     a.dP = dP;
     a.dh = dh;
     a.dw_router = dw_router;

@@ -13,7 +13,8 @@
 //
 // Layout: each expert's kept rows are copied into a zero-padded block of C rows (C the
 // capacity), so that every per-expert product is one strided-batched GEMM of E uniform
-// problems with no host synchronisation.  Those plain GEMMs go to cuBLAS (bf16 inputs, fp32
+// problems with no host synchronisation.  g and u are the ones the forward's gate-up epilogue
+// kept (fp32) when its workspace was sized for the backward.  Those plain GEMMs go to cuBLAS (bf16 inputs, fp32
 // accumulation); the gathers, the SwiGLU and softmax derivatives and the reductions are the
 // kernels below.
 #include <cublas_v2.h>
@@ -33,7 +34,7 @@ __global__ void bwd_pad_kernel(int E, long long C, int d8, int k, const int32_t*
                                const int32_t* __restrict__ perm, const float* __restrict__ cw,
                                const uint4* __restrict__ h, const uint4* __restrict__ dout,
                                uint4* __restrict__ xp, uint4* __restrict__ dop, float* __restrict__ rcw,
-                               int32_t* __restrict__ map)
+                               int32_t* __restrict__ rslot, int32_t* __restrict__ map)
 {
     const long long idx = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -55,6 +56,7 @@ __global__ void bwd_pad_kernel(int E, long long C, int d8, int k, const int32_t*
         }
         if (lane == 0) {
             rcw[idx] = cw[ent];
+            rslot[idx] = off + static_cast<int>(j);
             map[ent] = static_cast<int32_t>(idx);
         }
     } else {
@@ -63,7 +65,10 @@ __global__ void bwd_pad_kernel(int E, long long C, int d8, int k, const int32_t*
             xr[c] = z;
             dr[c] = z;
         }
-        if (lane == 0) rcw[idx] = 0.0f;
+        if (lane == 0) {
+            rcw[idx] = 0.0f;
+            rslot[idx] = -1;
+        }
     }
 }
 
@@ -86,12 +91,14 @@ __device__ __forceinline__ uint2 pack4_bf16(float a, float b, float c, float d)
     return make_uint2(pack_bf16x2(a, b), pack_bf16x2(c, d));
 }
 
-// One block per padded row.  gu [rows, 2F] holds the recomputed g and u in the packed W13
-// column order (block q of 256 columns: g of F-columns [128q, 128q+128), then their u);
-// dap [rows, F] = W2^T dout (before the combine weight).  Writes acw = cw * a (bf16, for
-// dW2), dgu = (dg, du) in the same packed order (bf16, for dx and dW13), and the row's
-// dcw = sum_f dap_f a_f = dout . y.
+// One block per padded row.  gu [T*k, 2F] holds the forward's g and u of each kept slot (bf16,
+// packed W13 column order: block q of 256 columns has g of F-columns [128q, 128q+128), then
+// their u); rslot gives the padded row's slot (-1: padding, g = u = 0).  dap [rows, F] =
+// W2^T dout (bf16, before the combine weight).  Writes acw = cw * a (bf16, for dW2), dgu =
+// (dg, du) in the packed order (bf16, for dx and dW13), and the row's dcw = sum_f dap_f a_f
+// = dout . y.
 __global__ void __launch_bounds__(256) swiglu_bwd_kernel(int F, const float* __restrict__ gu,
+                                                         const int32_t* __restrict__ rslot,
                                                          const float* __restrict__ dap,
                                                          const float* __restrict__ rcw,
                                                          __nv_bfloat16* __restrict__ acw,
@@ -101,15 +108,19 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(int F, const float* __r
     __shared__ float s_red[8];
     const long long row = blockIdx.x;
     const float c = rcw[row];
-    const float* gr = gu + row * 2 * F;
+    const int slot = rslot[row];
+    const float* gr = gu + static_cast<long long>(slot < 0 ? 0 : slot) * 2 * F;
     const float* dr = dap + row * F;
     __nv_bfloat16* ar = acw + row * F;
     __nv_bfloat16* dgr = dgu + row * 2 * F;
     float part = 0.0f;
     for (int f = 4 * threadIdx.x; f < F; f += 4 * blockDim.x) {
         const int q = f >> 7, o = f & 127;
-        const float4 g4 = *reinterpret_cast<const float4*>(gr + 256 * q + o);
-        const float4 u4 = *reinterpret_cast<const float4*>(gr + 256 * q + 128 + o);
+        float4 g4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), u4 = g4;
+        if (slot >= 0) {
+            g4 = *reinterpret_cast<const float4*>(gr + 256 * q + o);
+            u4 = *reinterpret_cast<const float4*>(gr + 256 * q + 128 + o);
+        }
         const float4 d4 = *reinterpret_cast<const float4*>(dr + f);
         const float g[4] = {g4.x, g4.y, g4.z, g4.w}, u[4] = {u4.x, u4.y, u4.z, u4.w};
         const float da[4] = {d4.x, d4.y, d4.z, d4.w};
@@ -300,9 +311,9 @@ int grid_of(long long n, int threads)
 size_t backward_bytes(long long T, int d, int E, int k, int F, long long C)
 {
     const size_t EC = static_cast<size_t>(E) * static_cast<size_t>(C);
-    const size_t per_row = static_cast<size_t>(d) * 2 * 2 + static_cast<size_t>(F) * 2 * 4 +
-                           static_cast<size_t>(F) * 4 + static_cast<size_t>(F) * 2 +
-                           static_cast<size_t>(F) * 2 * 2 + static_cast<size_t>(d) * 4 + 8;
+    const size_t per_row = static_cast<size_t>(d) * 2 * 2 + static_cast<size_t>(F) * 4 +
+                           static_cast<size_t>(F) * 2 + static_cast<size_t>(F) * 2 * 2 +
+                           static_cast<size_t>(d) * 4 + 12;
     return EC * per_row + static_cast<size_t>(T) * k * 4 + static_cast<size_t>(T) * E * 4 +
            static_cast<size_t>(T) * d * 4 + static_cast<size_t>(E) * d * 4 + 16 * 256;
 }
@@ -323,13 +334,13 @@ cudaError_t run_backward(const BackwardArgs& a, cudaStream_t s)
     };
     auto* xp = reinterpret_cast<__nv_bfloat16*>(take(EC * d * 2));
     auto* dop = reinterpret_cast<__nv_bfloat16*>(take(EC * d * 2));
-    auto* gu = reinterpret_cast<float*>(take(EC * 2 * F * 4));
     auto* dap = reinterpret_cast<float*>(take(EC * F * 4));
     auto* acw = reinterpret_cast<__nv_bfloat16*>(take(EC * F * 2));
     auto* dgu = reinterpret_cast<__nv_bfloat16*>(take(EC * 2 * F * 2));
     auto* dx = reinterpret_cast<float*>(take(EC * d * 4));
     auto* rcw = reinterpret_cast<float*>(take(EC * 4));
     auto* dcw = reinterpret_cast<float*>(take(EC * 4));
+    auto* rslot = reinterpret_cast<int32_t*>(take(EC * 4));
     auto* map = reinterpret_cast<int32_t*>(take(static_cast<size_t>(T) * k * 4));
     auto* dz = reinterpret_cast<float*>(take(static_cast<size_t>(T) * E * 4));
     auto* h32 = reinterpret_cast<float*>(take(static_cast<size_t>(T) * d * 4));
@@ -339,19 +350,15 @@ cudaError_t run_backward(const BackwardArgs& a, cudaStream_t s)
                                                                                  -1);
     bwd_pad_kernel<<<static_cast<unsigned>((EC + 7) / 8), 256, 0, s>>>(
         E, C, d / 8, k, a.offsets, a.perm, a.cw, static_cast<const uint4*>(a.h), static_cast<const uint4*>(a.dout),
-        reinterpret_cast<uint4*>(xp), reinterpret_cast<uint4*>(dop), rcw, map);
+        reinterpret_cast<uint4*>(xp), reinterpret_cast<uint4*>(dop), rcw, rslot, map);
     if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
     const cudaDataType BF = CUDA_R_16BF, F32 = CUDA_R_32F;
     const long long W13 = 2LL * F * d, W2s = static_cast<long long>(d) * F;
-    // g, u of every padded row: [C, d] . W13_e^T
-    if (!gemm_rm(hd, false, true, static_cast<int>(C), 2 * F, d, xp, BF, d, C * d, a.w13, BF, d, W13, gu, F32, 2 * F,
-                 C * 2 * F, E, 0.0f))
-        return cudaErrorUnknown;
-    // dap = dout rows . W2_e  ([C, d] . [d, F])
+    // dap = dout rows . W2_e  ([C, d] . [d, F]); g and u come from the forward
     if (!gemm_rm(hd, false, false, static_cast<int>(C), F, d, dop, BF, d, C * d, a.w2, BF, F, W2s, dap, F32, F,
                  C * F, E, 0.0f))
         return cudaErrorUnknown;
-    swiglu_bwd_kernel<<<static_cast<unsigned>(EC), 256, 0, s>>>(F, gu, dap, rcw, acw, dgu, dcw);
+    swiglu_bwd_kernel<<<static_cast<unsigned>(EC), 256, 0, s>>>(F, a.gu, rslot, dap, rcw, acw, dgu, dcw);
     if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
     // dx = (dg, du) . W13_e  ([C, 2F] . [2F, d])
     if (!gemm_rm(hd, false, false, static_cast<int>(C), d, 2 * F, dgu, BF, 2 * F, C * 2 * F, a.w13, BF, d, W13, dx,

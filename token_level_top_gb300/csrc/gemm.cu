@@ -47,6 +47,7 @@ struct GemmParams {
     const float* b_scale;  // FP8: the scale of each weight row (output channel)
     const float* a_scale;  // FP8: the scale of each activation row (slot order)
     float* act_amax;       // FP8 gate-up: per activation row, atomically maxed with max |bf16 act|
+    float* gu_save;          // gate-up, training: g and u of each kept row (fp32, packed W13 order)
     uint32_t tmem_cols;
     const int32_t* offsets;
     const int32_t* perm;
@@ -382,6 +383,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             u[j] = __float_as_uint(__uint_as_float(u[j]) * asc * __ldg(gsc + kExpertBN / 2 + c + j));
                         }
                     }
+                    if (ri < cnt && p.gu_save) {
+                        // g and u kept for the backward pass, in the packed W13 column order
+                        float* gs = p.gu_save + static_cast<size_t>(off + ri) * 2 * p.F + ti.n * kExpertBN + c;
+                        uint4* g4 = reinterpret_cast<uint4*>(gs);
+                        uint4* u4 = reinterpret_cast<uint4*>(gs + kExpertBN / 2);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            g4[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                            u4[j] = make_uint4(u[4 * j], u[4 * j + 1], u[4 * j + 2], u[4 * j + 3]);
+                        }
+                    }
                     if (ri < cnt) {
                         uint32_t pk[16];
 #pragma unroll
@@ -557,6 +569,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     p.b_scale = fp8 ? g.b_scale : nullptr;
     p.a_scale = fp8 ? g.a_scale : nullptr;
     p.act_amax = fp8 ? g.act_amax : nullptr;
+    p.gu_save = (!fp8 && g.kind == GK_GATEUP) ? static_cast<float*>(g.gu_save) : nullptr;
     const int kstep = fp8 ? 2 * kBK : kBK;   // K elements per 128-byte stage row
     auto map = [&](CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
         return fp8 ? make_map_e4m3(tm, ptr, rows, cols, box_rows) : make_map(tm, ptr, rows, cols, box_rows);

@@ -32,6 +32,7 @@ struct WsLayout {
     size_t act_q = 0, x_scale = 0, act_scale = 0, act_amax = 0;
     size_t xn = 0;     // router input after normalisation [T, d] bf16 (router_norm != 0)
     size_t bwd = 0;    // backward scratch (MOE_FLAG_BACKWARD)
+    size_t gu = 0;     // g and u of the kept rows, kept by the forward for the backward [T*k, 2F] fp32
     size_t zr = 0;     // two-layer router logits [T, E] fp32 (router_hidden > 0)
     int nr = 0;        // router GEMM output columns: E, or the hidden width H
     size_t total = 0;
@@ -139,6 +140,7 @@ struct GemmLaunch {
     const float* a_scale;    //   its scale: a_scale per activation row (slot order),
     const float* b_scale;    //   b_scale per weight row (W13: [E*2F], W2: [E*d])
     float* act_amax;         // gate-up: if set, atomically maxed with each act row's max |bf16 value|
+    void* gu_save;           // gate-up (bf16 weights): if set, g and u of each kept row [T*k, 2F] fp32
     int* status;
     long long budget;
 };
@@ -188,6 +190,7 @@ struct BackwardArgs {
     const void* w13;         // [E, 2F, d] bf16
     const void* w2;          // [E, d, F] bf16
     const void* dout;        // [T, d] bf16
+    const float* gu;         // [T*k, 2F] fp32: the forward's g and u of each kept slot
     const float* dP;         // [E] or NULL
     float* dh;               // [T, d]
     float* dw_router;        // [E, d] or NULL

@@ -71,6 +71,9 @@ def parse():
     ap.add_argument("--backward", action="store_true",
                     help="time a training step of the layer: the forward, then moe_layer_backward "
                          "(dL/dout drawn once; every gradient written each step)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of one step captured in a CUDA graph (the same kernels, "
+                         "without per-launch host overhead); the stage split comes from eager steps")
     ap.add_argument("--tau", type=float, default=1.0, help="router temperature")
     ap.add_argument("--router-norm", default="none", choices=["none", "layer", "l2"],
                     help="normalise the token rows before the router (LayerNorm or L2)")
@@ -266,8 +269,10 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(shape, router=None):
+def workload_config(shape, router=None, graph=False):
     extra = {"router": router} if router else {}
+    if graph:
+        extra["launch"] = "CUDA graph replay of one step"
     return {**extra, "workload": shape.name, "T": shape.T, "d_model": shape.d, "E": shape.E, "k": shape.k,
             "d_ff": shape.F, "cf": shape.cf, "lambda": shape.lam,
             "capacity": moe.capacity(shape.T, shape.k, shape.E, shape.cf, shape.capacity),
@@ -341,11 +346,24 @@ def run_ours(args, rank, world, local):
             if bev is not None:
                 bev.record()
 
+    graph = None
+    if args.graph:   # one step captured once (after an eager warm-up on the capture stream)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+    run = graph.replay if graph is not None else step
+
     w0 = torch.cuda.Event(enable_timing=True)
     w1 = torch.cuda.Event(enable_timing=True)
     w0.record()
     for _ in range(args.warmup):
-        step()
+        run()
     w1.record()
     torch.cuda.synchronize()
     step_ms = w0.elapsed_time(w1) / max(args.warmup, 1)
@@ -367,10 +385,13 @@ def run_ours(args, rank, world, local):
         lead = int(1e3 * CLOCK_LEAD_S / max(step_ms, 1e-3)) + 1
     wall0 = time.time()
     for _ in range(lead):
-        step()
+        run()
     t0.record()
     for i in range(args.steps):
-        step(stage_evs[i], bwd_evs[i])
+        if graph is not None:
+            graph.replay()
+        else:
+            step(stage_evs[i], bwd_evs[i])
     t1.record()
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -385,12 +406,18 @@ def run_ours(args, rank, world, local):
     st = moe.device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {st} ({moe.STATUS.get(st)}) after the timed region")
+    n_stage = args.steps
+    if graph is not None:   # the stage split from eager steps after the timed region
+        n_stage = min(args.steps, 50)
+        for i in range(n_stage):
+            step(stage_evs[i], bwd_evs[i])
+        torch.cuda.synchronize()
     stage_ms = {n: statistics.mean(stage_evs[i][j].elapsed_time(stage_evs[i][j + 1])
-                                   for i in range(args.steps))
+                                   for i in range(n_stage))
                 for j, n in enumerate(moe.STAGE_NAMES)}
     if bwd:
         stage_ms["backward"] = statistics.mean(stage_evs[i][-1].elapsed_time(bwd_evs[i])
-                                               for i in range(args.steps))
+                                               for i in range(n_stage))
 
     # end to end from pinned host memory through moe_layer_forward_host (FP8
     # weights: the same copies around moe_layer_forward_fp8, from Python)
@@ -477,7 +504,7 @@ def run_ours(args, rank, world, local):
         "dtype": ("e4m3 expert weights and activations (fp32 row scales), fp32 accumulate"
                   if fp8 else "bf16"),
         "data": "synthetic",
-        "config": workload_config(shape, router_desc),
+        "config": workload_config(shape, router_desc, graph is not None),
         "roofline": roof,
         "expert_gemm_tflops": expert_tflops,
         "weight_stream_gbs": weight_bytes / ((stage_ms["gate_up"] + stage_ms["down"]) * 1e-3) / 1e9,

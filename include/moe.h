@@ -346,6 +346,19 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* h_dev, cons
                                 float* dbias_dev, float* dw13_dev, float* dw2_dev, void* ws_dev,
                                 size_t ws_bytes, void* stream);
 
+/* moe_layer_forward_host without its final synchronisation: enqueues the copy
+ * of h_host into the workspace, the layer, and the copy of the output to
+ * out_host on `stream`, and returns.  h_host and out_host are pinned host
+ * memory; the caller synchronises the stream (or an event recorded after the
+ * call) before reading out_host or changing h_host, and uses ws_dev for no
+ * other call until then.  Two workspaces on two streams let one batch's copies
+ * overlap another batch's kernels. */
+moe_status_t moe_layer_forward_host_async(const moe_config_t* cfg, const void* h_host,
+                                          const void* w_router_dev, const float* bias_dev,
+                                          const float* usage_dev, const void* w13_dev,
+                                          const void* w2_dev, void* out_host, void* ws_dev,
+                                          size_t ws_bytes, void* stream);
+
 /* Failure-path check: launches one kernel whose bounded wait has nothing to
  * wait for; after `budget_cycles` SM clock cycles it records MOE_ERR_TIMEOUT
  * in the workspace status word and returns.  Used by the tests. */

@@ -311,6 +311,30 @@ def test_layer_forward_host_matches_device():
     assert torch.equal(out_host, dev.cpu())
 
 
+@pytest.mark.parametrize("name", ["tiny", "mixtral_prefill"])
+def test_layer_forward_host_async_pipelined(name):
+    """Batches alternate over two workspaces and two streams: each output equals the device
+    call's on the same input, whatever the overlap."""
+    shape = synth.CONFIGS[name]
+    Ld = make_layer(shape)
+    cfg = moe.Config.of(shape)
+    wss = [moe.workspace(cfg), moe.workspace(cfg)]
+    gen = torch.Generator().manual_seed(11)
+    hs = [Ld["h"].cpu()] + [torch.randn(shape.T, shape.d, generator=gen).to(torch.bfloat16) for _ in range(3)]
+    want = [moe.layer_forward(cfg, wss[0], h.cuda(), Ld["wr"], Ld["w13"], Ld["w2"]).cpu() for h in hs]
+    h_hosts = [h.pin_memory() for h in hs]
+    outs = [torch.empty(shape.T, shape.d, dtype=torch.bfloat16).pin_memory() for _ in hs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for i in range(len(hs)):
+        with torch.cuda.stream(streams[i % 2]):
+            moe.layer_forward_host_async(cfg, wss[i % 2], h_hosts[i], Ld["wr"], Ld["w13"], Ld["w2"], outs[i])
+    for st in streams:
+        st.synchronize()
+    for i in range(len(hs)):
+        assert torch.equal(outs[i], want[i]), i
+
+
 def test_stage_events_recorded():
     shape = synth.CONFIGS["tiny"]
     Ld = make_layer(shape)

@@ -763,6 +763,17 @@ moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* h_host,
                                     const void* w13, const void* w2, void* out_host, void* ws,
                                     size_t ws_bytes, void* stream)
 {
+    moe_status_t st = moe_layer_forward_host_async(cfg, h_host, w_router, bias, usage, w13, w2, out_host, ws,
+                                                   ws_bytes, stream);
+    if (st != MOE_OK || !cfg || cfg->T == 0) return st;
+    return cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_layer_forward_host_async(const moe_config_t* cfg, const void* h_host,
+                                          const void* w_router, const float* bias, const float* usage,
+                                          const void* w13, const void* w2, void* out_host, void* ws,
+                                          size_t ws_bytes, void* stream)
+{
     moe_status_t st = check_config(cfg, true);
     if (st != MOE_OK) return st;
     if (!h_host || !out_host) return MOE_ERR_INVALID_ARG;
@@ -779,9 +790,7 @@ moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* h_host,
     st = moe_layer_forward(cfg, h_dev, w_router, bias, usage, w13, w2, out_dev, nullptr, nullptr,
                            nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, ws, ws_bytes, stream);
     if (st != MOE_OK) return st;
-    if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    return cuda_status(cudaStreamSynchronize(s));
+    return cuda_status(cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s));
 }
 
 moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* h, const void* w_router, const void* w13,

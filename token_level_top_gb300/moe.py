@@ -114,6 +114,7 @@ _SIGS = {
     "moe_combine": (I32, [CFG, P, P, P, P, P, P, P]),
     "moe_layer_forward": (I32, [CFG, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_layer_forward_host": (I32, [CFG, P, P, P, P, P, P, P, P, SZ, P]),
+    "moe_layer_forward_host_async": (I32, [CFG, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_debug_timeout_probe": (I32, [P, SZ, ctypes.c_int64, P]),
     "moe_dispatch_static": (I32, [CFG, P, P, P, P, P, P, P, P, P, P, P, P]),
     "moe_quantize_fp8": (I32, [ctypes.c_int64, I32, P, P, P, P]),
@@ -363,6 +364,16 @@ def layer_forward_host(cfg: Config, ws, h_host, wr, w13, w2, out_host, bias=None
     st = lib().moe_layer_forward_host(ctypes.byref(c), _p(h_host), _p(wr), _p(bias), _p(usage),
                                       _p(w13), _p(w2), _p(out_host), _p(ws), ws.numel(), _stream())
     _check(st, "moe_layer_forward_host")
+    return out_host
+
+
+def layer_forward_host_async(cfg: Config, ws, h_host, wr, w13, w2, out_host, bias=None, usage=None):
+    """As layer_forward_host, without the final synchronisation (copies and kernels are enqueued
+    on the current stream; synchronise it before reading out_host)."""
+    c = cfg.c()
+    st = lib().moe_layer_forward_host_async(ctypes.byref(c), _p(h_host), _p(wr), _p(bias), _p(usage),
+                                            _p(w13), _p(w2), _p(out_host), _p(ws), ws.numel(), _stream())
+    _check(st, "moe_layer_forward_host_async")
     return out_host
 
 

@@ -419,51 +419,42 @@ def run_ours(args, rank, world, local):
         stage_ms["backward"] = statistics.mean(stage_evs[i][-1].elapsed_time(bwd_evs[i])
                                                for i in range(n_stage))
 
-    # end to end from pinned host memory through moe_layer_forward_host (FP8
-    # weights: the same copies around moe_layer_forward_fp8, from Python)
+    # end to end from pinned host memory: every step copies its input in and its result back
     h_host = L["h"].cpu().pin_memory()
     o_host = torch.empty(shape.T, shape.d, dtype=torch.bfloat16).pin_memory()
     h_dev = torch.empty_like(L["h"])
 
     dh_host = torch.empty(shape.T, shape.d, dtype=torch.float32).pin_memory() if bwd else None
+    # Every mode keeps two batches in flight the same way; the plain layer goes through the
+    # library's host-buffer call, the others through the binding with explicit copies.
+    wss = [ws, moe.workspace(cfg)]
+    o_hosts = [o_host, torch.empty_like(o_host).pin_memory()]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    h_devs = [h_dev, torch.empty_like(h_dev)]
+    outs = [out, torch.empty_like(out)]
+    dh_hosts = [dh_host, torch.empty_like(dh_host).pin_memory()] if bwd else None
 
-    def e2e_step():
-        if bwd:   # h in, forward, backward, dL/dh out
-            h_dev.copy_(h_host, non_blocking=True)
-            moe.layer_forward(cfg, ws, h_dev, wr, L["w13"], L["w2"], bias, L["usage"], out=out)
-            g = moe.layer_backward(cfg, ws, h_dev, L["wr"], L["w13"], L["w2"], dout)
-            dh_host.copy_(g["dh"], non_blocking=True)
-            torch.cuda.current_stream().synchronize()
-        elif fp8 or variant:
-            h_dev.copy_(h_host, non_blocking=True)
-            moe.layer_forward(cfg, ws, h_dev, wr, L["w13"], L["w2"], bias, L["usage"], out=out)
-            o_host.copy_(out, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
+    def e2e_one(i):
+        j = i % 2
+        if not (bwd or fp8 or variant):
+            moe.layer_forward_host_async(cfg, wss[j], h_host, L["wr"], L["w13"], L["w2"], o_hosts[j], L["bias"],
+                                         L["usage"])
+            return
+        h_devs[j].copy_(h_host, non_blocking=True)
+        moe.layer_forward(cfg, wss[j], h_devs[j], wr, L["w13"], L["w2"], bias, L["usage"], out=outs[j])
+        if bwd:   # dL/dh back to the host
+            g = moe.layer_backward(cfg, wss[j], h_devs[j], L["wr"], L["w13"], L["w2"], dout)
+            dh_hosts[j].copy_(g["dh"], non_blocking=True)
         else:
-            moe.layer_forward_host(cfg, ws, h_host, L["wr"], L["w13"], L["w2"], o_host, L["bias"],
-                                   L["usage"])
+            o_hosts[j].copy_(outs[j], non_blocking=True)
 
-    # The plain layer pipelines through the asynchronous host call: two workspaces on two
-    # streams, so one batch's copies overlap the other's kernels; every step still copies its
-    # input from pinned host memory and its output back, and the region ends at a synchronise.
-    pipelined = not (bwd or fp8 or variant)
-    if pipelined:
-        wss = [ws, moe.workspace(cfg)]
-        o_hosts = [o_host, torch.empty_like(o_host).pin_memory()]
-        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
-
-        def e2e_run(n):
-            torch.cuda.current_stream().synchronize()
-            for i in range(n):
-                with torch.cuda.stream(streams[i % 2]):
-                    moe.layer_forward_host_async(cfg, wss[i % 2], h_host, L["wr"], L["w13"], L["w2"],
-                                                 o_hosts[i % 2], L["bias"], L["usage"])
-            for st_ in streams:
-                st_.synchronize()
-    else:
-        def e2e_run(n):
-            for _ in range(n):
-                e2e_step()
+    def e2e_run(n):
+        torch.cuda.current_stream().synchronize()
+        for i in range(n):
+            with torch.cuda.stream(streams[i % 2]):
+                e2e_one(i)
+        for st_ in streams:
+            st_.synchronize()
 
     e2e_run(2)
     barrier(world)
@@ -533,8 +524,8 @@ def run_ours(args, rank, world, local):
         "clocks": clk,
         "e2e": ({"value": world * T * args.e2e_steps / te, "unit": UNIT,
                  "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * (4 if bwd else 2),
-                 "overlap": ("two workspaces on two streams (moe_layer_forward_host_async)" if pipelined
-                             else "none: each step synchronises")}
+                 "overlap": ("two workspaces on two streams" +
+                             (" (moe_layer_forward_host_async)" if not (bwd or fp8 or variant) else ""))}
                 if args.e2e_steps > 0 else None),
         "gpu_launches": (kernels_per_step(shape.T, fp8, norm, hidden) + (BACKWARD_KERNELS if bwd else 0))
         * args.steps,

@@ -133,6 +133,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int* s_tile_start = reinterpret_cast<int*>(bars + 2 * stages + 4);
     int* s_offs = s_tile_start + (p.E + 1);
     volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(s_offs + (p.E + 1));
+    // FP8: the current tile's weight-row scales, staged by the epilogue warps
+    float* s_bsc = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(s_tmem + 1) + 15) & ~uintptr_t(15));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -341,7 +343,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const TileInfo ti = decode_tile<PAIR>(p, tile, s_tile_start, s_offs, rank);
             const int b = it & 1;
             const uint32_t acc_par = (it >> 1) & 1;
-            if (!mbar_wait(smem_u32(&tfull_bar[b]), acc_par, p.budget)) {
+            const bool staged = FP8 && p.kind != GK_ROUTER;
+            if (staged) {
+                // the tile's weight-row scales into shared memory while its MMAs run
+                // (the 128 epilogue threads, two scales each; named barrier 1)
+                const int et = static_cast<int>(threadIdx.x) - 64;
+                epilogue_sync();   // the previous tile's scales are no longer read
+                for (int i = et; i < kExpertBN; i += 128) {
+                    float v = 0.0f;
+                    if (p.kind == GK_GATEUP)
+                        v = __ldg(p.b_scale + static_cast<size_t>(ti.e) * 2 * p.F + ti.n * kExpertBN + i);
+                    else if (i < p.bn && ti.n * p.bn + i < p.d)
+                        v = __ldg(p.b_scale + static_cast<size_t>(ti.e) * p.d + ti.n * p.bn + i);
+                    s_bsc[i] = v;
+                }
+            }
+            bool got = mbar_wait(smem_u32(&tfull_bar[b]), acc_par, p.budget);
+            // staged: one decision for the 128 threads (none is left at a barrier), and
+            // the barrier that publishes the scales
+            if (staged) got = epilogue_all(got);
+            if (!got) {
                 record_error(p.status, MOE_ERR_TIMEOUT);
                 break;
             }
@@ -367,9 +388,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int ri = ti.m * kBM + row;
                 uint32_t u[32];
                 __nv_bfloat16* dst = p.act + static_cast<size_t>(off + ri) * p.F + ti.n * (kExpertBN / 2);
-                // FP8: the scales of the tile's W1 and W3 rows (packed rows of W13)
-                // and of this thread's activation row
-                const float* gsc = FP8 ? p.b_scale + static_cast<size_t>(ti.e) * 2 * p.F + ti.n * kExpertBN : nullptr;
+                // FP8: the tile's W1 and W3 row scales (packed rows of W13) are in
+                // s_bsc; this thread's activation row scale
                 const float asc = (FP8 && ri < cnt) ? p.a_scale[off + ri] : 0.0f;
                 float rmax = 0.0f;   // FP8: max |act| over this thread's columns
                 for (int c = 0; c < kExpertBN / 2; c += 32) {
@@ -379,8 +399,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (FP8) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            v[j] = __float_as_uint(__uint_as_float(v[j]) * asc * __ldg(gsc + c + j));
-                            u[j] = __float_as_uint(__uint_as_float(u[j]) * asc * __ldg(gsc + kExpertBN / 2 + c + j));
+                            v[j] = __float_as_uint(__uint_as_float(v[j]) * asc * s_bsc[c + j]);
+                            u[j] = __float_as_uint(__uint_as_float(u[j]) * asc * s_bsc[kExpertBN / 2 + c + j]);
                         }
                     }
                     if (ri < cnt && p.gu_save) {
@@ -425,7 +445,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int slot = off + ri;
                 const int col0 = ti.n * p.bn;
                 __nv_bfloat16* dst = p.y_slots + static_cast<size_t>(slot) * p.d + col0;
-                const float* dsc = FP8 ? p.b_scale + static_cast<size_t>(ti.e) * p.d + col0 : nullptr;
                 const float asc = (FP8 && valid) ? p.a_scale[slot] : 0.0f;
                 for (int c = 0; c < p.bn; c += 32) {
                     if (col0 + c >= p.d) break;
@@ -435,7 +454,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             if (col0 + c + j < p.d)
-                                v[j] = __float_as_uint(__uint_as_float(v[j]) * asc * __ldg(dsc + c + j));
+                                v[j] = __float_as_uint(__uint_as_float(v[j]) * asc * s_bsc[c + j]);
                     }
                     if (valid) {
                         uint32_t pk[16];
@@ -532,9 +551,10 @@ namespace {
 
 constexpr int kRouterStages = 4;
 
-size_t gemm_fixed_smem(int E)
+size_t gemm_fixed_smem(int E, bool fp8 = false)
 {
-    return 1024 + 64 + static_cast<size_t>(2 * (E + 1)) * 4 + 16 + 6 * 8;
+    // alignment slack, barriers, tile table, TMEM address; FP8: the staged row scales
+    return 1024 + 64 + static_cast<size_t>(2 * (E + 1)) * 4 + 16 + 6 * 8 + (fp8 ? 16 + 4 * kExpertBN : 0);
 }
 
 }  // namespace
@@ -633,7 +653,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     }
     const uint32_t a_bytes = kBM * kBK * 2;
     const uint32_t b_bytes = static_cast<uint32_t>(pair ? p.bn / 2 : p.bn) * kBK * 2;
-    const size_t fixed = gemm_fixed_smem(g.E);
+    const size_t fixed = gemm_fixed_smem(g.E, fp8);
     const size_t budget_smem = 227 * 1024;
     int stages = static_cast<int>((budget_smem - fixed) / (a_bytes + b_bytes + 16));
     stages = std::max(2, std::min(stages, g.kind == GK_ROUTER ? kRouterStages : 8));

@@ -44,6 +44,7 @@ struct GemmParams {
     int kb_per_split;  // router K blocks per split
     int stages;
     int gather4;       // gate-up: A rows gathered from h with tile::gather4 (else tiled from x_perm)
+    int b_policy;      // L2 policy of the weight loads: 0 default, 1 evict_first, 2 evict_last
     const float* b_scale;  // FP8: the scale of each weight row (output channel)
     const float* a_scale;  // FP8: the scale of each activation row (slot order)
     float* act_amax;       // FP8 gate-up: per activation row, atomically maxed with max |bf16 act|
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        const uint64_t pol_b = p.b_policy == 2 ? l2_policy_evict_last() : l2_policy_evict_first();
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load in flight + its parity
@@ -243,14 +245,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (PAIR) {
                     if (lane == 0) {
                         tma_load_2d_pair(dA, &tmA, x, arow, fb);
-                        tma_load_2d_pair(dB, &tmB, x, brow + rank * (p.bn / 2), fb);
+                        if (p.b_policy)
+                            tma_load_2d_pair_hint(dB, &tmB, x, brow + rank * (p.bn / 2), fb, pol_b);
+                        else
+                            tma_load_2d_pair(dB, &tmB, x, brow + rank * (p.bn / 2), fb);
                     }
                 } else {
                     if (p.kind == GK_GATEUP && p.gather4)
                         tma_gather4(dA + lane * 4 * 128, &tmA, x, r0, r1, r2, r3, fb);
                     else if (lane == 0)
                         tma_load_2d(dA, &tmA, x, arow, fb);
-                    if (lane == 0) tma_load_2d(dB, &tmB, x, brow, fb);
+                    if (lane == 0) {
+                        if (p.b_policy)
+                            tma_load_2d_hint(dB, &tmB, x, brow, fb, pol_b);
+                        else
+                            tma_load_2d(dB, &tmB, x, brow, fb);
+                    }
                 }
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -591,6 +601,9 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     p.act_amax = fp8 ? g.act_amax : nullptr;
     p.gu_save = (!fp8 && g.kind == GK_GATEUP) ? static_cast<float*>(g.gu_save) : nullptr;
     const int kstep = fp8 ? 2 * kBK : kBK;   // K elements per 128-byte stage row
+    // When no expert holds more than one row tile, every weight tile is read by
+    // exactly one tile: its lines go first out of L2, ahead of the token rows.
+    p.b_policy = (g.kind != GK_ROUTER && g.rows_cap > 0 && std::min<long long>(g.rows_cap, g.T) <= kBM) ? 1 : 0;
     auto map = [&](CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
         return fp8 ? make_map_e4m3(tm, ptr, rows, cols, box_rows) : make_map(tm, ptr, rows, cols, box_rows);
     };

@@ -298,21 +298,8 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// L2 eviction policies for the TMA loads (createpolicy, applied to every line a
-// load touches): operands re-read by many tiles are kept (evict_last), operands
-// read by one group of tiles and then never again go first (evict_first).
-__device__ __forceinline__ uint64_t l2_policy_evict_last()
-{
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_normal()
-{
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
+// L2 eviction policy for TMA loads of lines read once and never again
+// (createpolicy, applied to every line a load touches).
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
     uint64_t pol;

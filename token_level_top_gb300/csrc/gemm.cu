@@ -44,7 +44,7 @@ struct GemmParams {
     int kb_per_split;  // router K blocks per split
     int stages;
     int gather4;       // gate-up: A rows gathered from h with tile::gather4 (else tiled from x_perm)
-    int b_policy;      // L2 policy of the weight loads: 0 default, 1 evict_first, 2 evict_last
+    int b_policy;      // L2 policy of the weight loads: 0 default, 1 evict_first
     const float* b_scale;  // FP8: the scale of each weight row (output channel)
     const float* a_scale;  // FP8: the scale of each activation row (slot order)
     float* act_amax;       // FP8 gate-up: per activation row, atomically maxed with max |bf16 act|
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        const uint64_t pol_b = p.b_policy == 2 ? l2_policy_evict_last() : l2_policy_evict_first();
+        const uint64_t pol_b = l2_policy_evict_first();
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load in flight + its parity

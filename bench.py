@@ -243,6 +243,32 @@ def oracle_sample(shape, h, wr, bias, usage, w1, w3, w2, budget_s=12.0, seed=0):
                 t_total=t_total, tokens_per_s=shape.T / t_total)
 
 
+def host_cpu():
+    """The host the oracle is timed on: architecture, CPU model (as /proc/cpuinfo
+    or lscpu names it) and the number of cores the OS reports."""
+    import platform
+    model = None
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for ln in fh:
+                key = ln.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+            for ln in out.splitlines():
+                if ln.lower().startswith("model name"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    return {"machine": platform.machine(), "model": model, "nproc": os.cpu_count()}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -264,7 +290,7 @@ def run_reference(args, rank, world):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(shape),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "host": host_cpu()},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -541,7 +567,8 @@ def run_ours(args, rank, world, local):
             "value": res["tokens_per_s"], "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": (f"route+dispatch of all {T} tokens ({res['t_route_dispatch']:.2f} s), "
                        f"expert FFN of {res['ffn_rows']} of {res['kept']} kept rows "
-                       f"({res['t_ffn_sample']:.1f} s), extrapolated by kept rows")}
+                       f"({res['t_ffn_sample']:.1f} s), extrapolated by kept rows"),
+            "host": host_cpu()}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -215,32 +215,40 @@ def layer_inputs(shape, device="cuda"):
     return L
 
 
-def oracle_sample(shape, h, wr, bias, usage, w1, w3, w2, budget_s=12.0, seed=0):
-    """Time the oracle: route + dispatch of the whole batch, expert FFN + combine
-    of sampled kept rows until ~budget_s; extrapolate by kept rows."""
+def oracle_inputs(h, wr, bias, usage, w1, w3, w2):
+    """The oracle's inputs (bf16 bit patterns and float arrays), converted once."""
+    return dict(h=synth.bf16_bits(h), wr=synth.bf16_bits(wr),
+                bias=None if bias is None else bias.cpu().numpy(),
+                usage=None if usage is None else usage.cpu().numpy(),
+                w1=synth.bf16_bits(w1), w3=synth.bf16_bits(w3), w2=synth.bf16_bits(w2))
+
+
+def oracle_sample(shape, X, budget_s=12.0, seed=0):
+    """Time the oracle: route + dispatch of the whole batch, then the expert FFN
+    of sampled kept rows until ~budget_s; extrapolate the FFN by kept rows."""
     import oracle
-    hb, wb = synth.bf16_bits(h), synth.bf16_bits(wr)
-    bnp = None if bias is None else bias.cpu().numpy()
-    unp = None if usage is None else usage.cpu().numpy()
     C = oracle.capacity(shape.T, shape.k, shape.E, shape.cf, shape.capacity)
     t0 = time.perf_counter()
-    r = oracle.route(shape.k, h=hb, wr=wb, bias=bnp, usage=unp, lam=shape.lam)
+    r = oracle.route(shape.k, h=X["h"], wr=X["wr"], bias=X["bias"], usage=X["usage"], lam=shape.lam)
     d = oracle.dispatch(r["scores"], shape.k, C)
     t_rd = time.perf_counter() - t0
     kept = int(d["offsets"][-1])
-    w1b, w3b, w2b = synth.bf16_bits(w1), synth.bf16_bits(w3), synth.bf16_bits(w2)
     rng = np.random.default_rng(seed)
     order = rng.permutation(kept)
     rows, t_ffn = 0, 0.0
-    while rows < kept and (t_rd + t_ffn) < budget_s:
+    while rows < kept and (rows == 0 or (t_rd + t_ffn) < budget_s):
         i = int(order[rows])
         t1 = time.perf_counter()
-        oracle.expert_slots(hb, w1b, w3b, w2b, d["assign"], d["perm"], i, i + 1)
+        oracle.expert_slots(X["h"], X["w1"], X["w3"], X["w2"], d["assign"], d["perm"], i, i + 1)
         t_ffn += time.perf_counter() - t1
         rows += 1
     t_total = t_rd + (t_ffn / max(rows, 1)) * kept
     return dict(t_route_dispatch=t_rd, ffn_rows=rows, kept=kept, t_ffn_sample=t_ffn,
                 t_total=t_total, tokens_per_s=shape.T / t_total)
+
+
+REF_BUDGET_S = 90.0    # wall-clock bound of the reference (oracle) arm's timed steps
+STEP_MIN_S = 0.5
 
 
 def host_cpu():
@@ -275,17 +283,26 @@ def run_reference(args, rank, world):
     shape = synth.CONFIGS[args.workload]
     h, wr, bias, usage = synth.router_inputs(shape)
     w1, w3, w2 = synth.expert_weights(shape, device="cpu")
-    per_step = max(2.0, 60.0 / max(args.steps + args.warmup, 1))
+    # Each step times route + dispatch of the whole batch (about 0.1 s on the
+    # prefill shape) and at least one expert row (about 0.3 s), so a step takes
+    # at least STEP_MIN_S; the whole run is held to about REF_BUDGET_S by giving
+    # each step budget / (W + K) and, when even STEP_MIN_S per step is too long,
+    # timing fewer steps than asked (the line gives both counts).
+    per_step = max(STEP_MIN_S, REF_BUDGET_S / max(args.steps + args.warmup, 1))
+    steps = args.steps
+    if (args.warmup + steps) * per_step > REF_BUDGET_S:
+        steps = max(1, int(REF_BUDGET_S / per_step) - args.warmup)
+    X = oracle_inputs(h, wr, bias, usage, w1, w3, w2)
     vals = []
-    for i in range(args.warmup + args.steps):
-        res = oracle_sample(shape, h, wr, bias, usage, w1, w3, w2, budget_s=per_step, seed=i)
+    for i in range(args.warmup + steps):
+        res = oracle_sample(shape, X, budget_s=per_step, seed=i)
         if i >= args.warmup:
             vals.append(res)
     v = statistics.median(r["tokens_per_s"] for r in vals)
     sample = (f"per step: route+dispatch of all {shape.T} tokens, expert FFN of "
               f"{vals[-1]['ffn_rows']} of {vals[-1]['kept']} kept rows, extrapolated by kept rows")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup,
+            "steps": steps, "steps_requested": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * shape.T / v, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(shape),
@@ -560,9 +577,9 @@ def run_ours(args, rank, world, local):
         line["metric"] = METRIC + " (training step: forward + backward)"
         line["backward"] = bwd_line
     if want_cpu:
-        res = oracle_sample(shape, L["h"].cpu(), L["wr"].cpu(),
-                            None if L["bias"] is None else L["bias"].cpu(),
-                            None if L["usage"] is None else L["usage"].cpu(), *host_w)
+        X = oracle_inputs(L["h"].cpu(), L["wr"].cpu(), None if L["bias"] is None else L["bias"].cpu(),
+                          None if L["usage"] is None else L["usage"].cpu(), *host_w)
+        res = oracle_sample(shape, X)
         line["cpu_baseline"] = {
             "value": res["tokens_per_s"], "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": (f"route+dispatch of all {T} tokens ({res['t_route_dispatch']:.2f} s), "

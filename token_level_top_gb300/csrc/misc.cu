@@ -212,22 +212,27 @@ __global__ void __launch_bounds__(256) quantize_fp8_block_kernel(
     }
 }
 
-// Each row's max |value| given: one block per row, one pass.
-__global__ void quantize_fp8_amax_kernel(int cols, const uint4* __restrict__ w, const int32_t* __restrict__ perm,
-                                         int k, const int32_t* __restrict__ nrows,
+// Each row's max |value| given: one pass, `parts` blocks per row (each a
+// contiguous piece of it), so that a batch of few rows still spreads over the SMs.
+__global__ void quantize_fp8_amax_kernel(int cols, int parts, const uint4* __restrict__ w,
+                                         const int32_t* __restrict__ perm, int k,
+                                         const int32_t* __restrict__ nrows,
                                          const float* __restrict__ amax_in, uint2* __restrict__ q,
                                          float* __restrict__ scales)
 {
-    const long long row = blockIdx.x;
+    const long long row = blockIdx.x / parts;
+    const int part = static_cast<int>(blockIdx.x - row * parts);
     if (nrows && row >= *nrows) return;
     const float amax = amax_in[row];
     const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
-    if (threadIdx.x == 0) scales[row] = sc;
+    if (part == 0 && threadIdx.x == 0) scales[row] = sc;
     const int c8 = cols / 8;
+    const int piece = (c8 + parts - 1) / parts;
+    const int c_end = min(c8, (part + 1) * piece);
     const uint4* wr = w + (perm ? perm[row] / k : row) * c8;
     uint2* qr = q + row * c8;
 #pragma unroll 4
-    for (int c = threadIdx.x; c < c8; c += blockDim.x) qr[c] = e4m3_8(__ldg(wr + c), sc);
+    for (int c = part * piece + threadIdx.x; c < c_end; c += blockDim.x) qr[c] = e4m3_8(__ldg(wr + c), sc);
 }
 
 // One thread waits on an mbarrier that nothing will ever complete, with the
@@ -299,8 +304,14 @@ cudaError_t launch_quantize_fp8(long long rows, int cols, const void* w, const i
     if (rows <= 0) return cudaSuccess;
     if (amax_in) {
         if (zero_rows || rows > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-        quantize_fp8_amax_kernel<<<static_cast<unsigned>(rows), 256, 0, s>>>(
-            cols, static_cast<const uint4*>(w), perm, k, nrows, amax_in, static_cast<uint2*>(q), scales);
+        // pieces of at least 256 vectors (one per thread), enough blocks for two per SM
+        const long long c8 = cols / 8;
+        long long parts = 1;
+        while (parts < 8 && rows * parts < 2LL * num_sms() && c8 / (2 * parts) >= 256) parts *= 2;
+        if (rows * parts > 0x7FFFFFFFLL) parts = 1;
+        quantize_fp8_amax_kernel<<<static_cast<unsigned>(rows * parts), 256, 0, s>>>(
+            cols, static_cast<int>(parts), static_cast<const uint4*>(w), perm, k, nrows, amax_in,
+            static_cast<uint2*>(q), scales);
         return cudaGetLastError();
     }
     // a block per row while the rows fit one resident wave (a batch of a few

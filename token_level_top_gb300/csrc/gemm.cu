@@ -17,9 +17,13 @@
 //   warp 0    TMA producer: A tile 128 x 64 (tiled, or gathered 4 rows per
 //             tile::gather4 by all 32 lanes) and B tile BN x 64, 128-byte
 //             swizzle, into a ring of `stages` shared-memory slots;
-//   warp 1    allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=16)
-//             into one of two TMEM accumulators and commits to mbarriers;
+//   warp 1    allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=16;
+//             FP8: kind::f8f6f4, K=32) into one of two TMEM accumulators and
+//             commits to mbarriers;
 //   warps 2-5 epilogue: tcgen05.ld of their 32 TMEM lanes, fused math, store.
+// Expert GEMMs whose experts average two or more row tiles run on clusters of
+// two CTAs: each stages its own 128 rows of A and half of the BN weight rows,
+// and CTA 0 issues tcgen05.mma.cta_group::2 (M=256) over both.
 // Tiles are scheduled statically (tile += gridDim.x) from per-expert row
 // counts read on the device, so no host synchronisation is needed.  Every
 // wait is bounded; on expiry the CTA records MOE_ERR_TIMEOUT, drains what it
@@ -66,7 +70,8 @@ struct TileInfo {
 // Expert tiles are numbered expert by expert; within an expert, row units
 // fastest (the row tiles that share a weight tile run together), then column
 // tiles.  In paired mode a unit is two adjacent row tiles, one per CTA of the
-// cluster, which share each weight tile through multicast.
+// cluster; each CTA loads half of the unit's weight tile and the paired MMA
+// reads both halves.
 template <bool PAIR>
 __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile,
                                                 const int* s_tile_start, const int* s_offs,

@@ -251,6 +251,16 @@ REF_BUDGET_S = 90.0    # wall-clock bound of the reference (oracle) arm's timed 
 STEP_MIN_S = 0.5
 
 
+def reference_plan(steps: int, warmup: int):
+    """(seconds per step, steps to time) for the reference arm: the budget split
+    over warm-up and timed steps, at least STEP_MIN_S each, and fewer timed steps
+    than asked (at least one) when that is needed to stay within REF_BUDGET_S."""
+    per_step = max(STEP_MIN_S, REF_BUDGET_S / max(steps + warmup, 1))
+    if (warmup + steps) * per_step > REF_BUDGET_S:
+        steps = max(1, int(REF_BUDGET_S / per_step) - warmup)
+    return per_step, steps
+
+
 def host_cpu():
     """The host the oracle is timed on: architecture, CPU model (as /proc/cpuinfo
     or lscpu names it) and the number of cores the OS reports."""
@@ -288,10 +298,7 @@ def run_reference(args, rank, world):
     # at least STEP_MIN_S; the whole run is held to about REF_BUDGET_S by giving
     # each step budget / (W + K) and, when even STEP_MIN_S per step is too long,
     # timing fewer steps than asked (the line gives both counts).
-    per_step = max(STEP_MIN_S, REF_BUDGET_S / max(args.steps + args.warmup, 1))
-    steps = args.steps
-    if (args.warmup + steps) * per_step > REF_BUDGET_S:
-        steps = max(1, int(REF_BUDGET_S / per_step) - args.warmup)
+    per_step, steps = reference_plan(args.steps, args.warmup)
     X = oracle_inputs(h, wr, bias, usage, w1, w3, w2)
     vals = []
     for i in range(args.warmup + steps):

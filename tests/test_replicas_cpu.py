@@ -40,7 +40,7 @@ def _worker(rank, world, port, out):
 def test_two_gloo_ranks_take_max_time():
     world = 2
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:   # no fork of a multi-threaded parent
         out = m.dict()
         mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)

@@ -6,7 +6,7 @@
 //   p = softmax(s); top-k = the k best s, ties to the lower index   [coreui] §3.1
 //   f_i = picks of i / T, P_i = mean p_i             [cnnetsun] §4.2; [coreui] §3.1
 //
-// Each chunk of kChunk consecutive tokens is routed by a cluster of 1-8
+// Each chunk of kChunk consecutive tokens is routed by a cluster of 1-4
 // blocks (as many as keep the grid within the SMs).  A token is owned
 // by G = min(32, pow2(E)) lanes, each lane holding EPL experts (e = lane + G*j);
 // each lane ranks its experts against all E scores (shuffled through the
@@ -73,9 +73,11 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s)
 {
     if (a.T <= 0) return cudaSuccess;
     // one SM per block: split each chunk over as many blocks (a power of two,
-    // at most 8, the portable cluster size) as keep the grid within the SMs
+    // at most 4) as keep the grid within the SMs.  Clusters of 8 were slower:
+    // the route stage of 16 chunks took 36.9 us with 8 CTAs per chunk, 28.7
+    // with 4 and 28.6 with 2; with 32 chunks 4 beat 2 (35.2 against 38.2 us).
     int cs = 1;
-    while (cs < 8 && a.nchunks * cs * 2 <= num_sms()) cs *= 2;
+    while (cs < 4 && a.nchunks * cs * 2 <= num_sms()) cs *= 2;
     cudaError_t e;
     if (a.E <= 32)
         e = launch_route_cs<1>(a, cs, s);

@@ -209,8 +209,11 @@ def test_expert_ffn_vs_oracle(T, d, E, F, k, cf):
     assert rows.max() <= 4 * OUT_REL_FROB
 
 
-def test_combine_vs_numpy():
-    T, E, k, d = 500, 6, 2, 256
+# one piece per lane below 2048 tokens, two from there; d = 192 leaves most lanes
+# of a row segment past the row's end
+@pytest.mark.parametrize("T,d", [(500, 256), (2500, 192), (2048, 4096)])
+def test_combine_vs_numpy(T, d):
+    E, k = 6, 2
     s = _scores("skew", T, E, 5)
     cfg = _cfg(T, E, k, d=d, cf=1.0)
     ws = moe.workspace(cfg)

@@ -24,6 +24,12 @@ _HDR = os.path.join(_HERE, "moe_oracle.h")
 _LIB = os.path.join(_HERE, "_build", "liboracle.so")
 _lock = threading.Lock()
 _lib = None
+# A library built from an edited copy of moe_oracle.c (the mutation tests plant
+# one mistake each and check that some pin fails); unset, the oracle is built here.
+_LIB_OVERRIDE = os.environ.get("MOE_ORACLE_LIBRARY")
+
+
+CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-fPIC", "-shared", "-Wall"]
 
 
 def build(force: bool = False) -> str:
@@ -32,8 +38,7 @@ def build(force: bool = False) -> str:
     newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
         tmp = _LIB + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-fPIC",
-               "-shared", "-Wall", "-o", tmp, _SRC, "-lm"]
+        cmd = ["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB
@@ -43,8 +48,7 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB)
+            lib = ctypes.CDLL(_LIB_OVERRIDE or build())
             P = ctypes.c_void_p
             I = ctypes.c_int
             lib.oracle_capacity.argtypes = [ctypes.c_int64, I, I, ctypes.c_double, ctypes.c_int64]

@@ -1,0 +1,132 @@
+"""Mutation check of the oracle's pins (CPU only).
+
+Each case plants one plausible mistake in a copy of oracle/moe_oracle.c, builds
+it with the oracle's own flags, and runs the pin suite (tests/test_oracle_pins.py)
+against that library in a child process.  The case passes when the pins named
+beside the mistake fail, so that every pinned branch of the oracle is shown to
+be held by some pin and not by the oracle's agreement with itself.  Mistakes
+that are provably harmless (walking a token's preference order from position 0
+instead of r: every earlier position is held or full) are not listed.
+"""
+import os
+import re
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+PINS = os.path.join(HERE, "test_oracle_pins.py")
+
+# name -> (edits (old, new), each `old` occurring exactly once, pins that must fail)
+MUTANTS = {
+    # capacity and routing ([coreui] §5.2 capacity; [mhpn] §2.3 penalty; top-k order)
+    "capacity_floor": ([("return (num + den - 1) / den;", "return num / den;")],
+                       ["test_capacity_page_value"]),
+    "ties_to_higher_index": ([("    return a < b;\n}", "    return a > b;\n}")],
+                             ["test_preference_matches_sorted_with_ties", "test_equal_logits_pick_lowest_indices"]),
+    "penalty_sign": ([("s[e] = zt - pen;", "s[e] = zt + pen;")], ["test_penalty_is_two_rounded_fp32_ops"]),
+    "penalty_fused": ([("volatile float pen = lambda * usage[e];\n                s[e] = zt - pen;",
+                        "s[e] = fmaf(-lambda, usage[e], zt);")], ["test_penalty_is_two_rounded_fp32_ops"]),
+    "temperature_after_penalty": ([("s[e] = zt - pen;", "s[e] = (z[e] - pen) / tau;")],
+                                  ["test_temperature_comes_before_the_penalty"]),
+    "P_not_averaged": ([("P[e] = T > 0 ? (float)(psum[e] / (double)T) : 0.0f;",
+                         "P[e] = T > 0 ? (float)(psum[e]) : 0.0f;")], ["test_softmax_and_stats_match_scipy"]),
+    # dispatch ([mhpn] §2.3 the 128th token; rank-major order; capacity cap)
+    "rank_minor_order": ([("for (int r = 0; r < k; ++r) {\n            for (int t = 0; t < T; ++t) {",
+                           "for (int t = 0; t < T; ++t) {\n            for (int r = 0; r < k; ++r) {")],
+                         ["test_worked_case_128_identical_tokens", "test_rank_major_order_matters"]),
+    "fill_past_capacity": ([("if (fill[e] >= C) continue;", "if (fill[e] > C) continue;")],
+                           ["test_page_overflow_case", "test_drop_case"]),
+    "no_held_check": ([("if (held) continue;", "(void)held;")], ["test_dispatch_brute_force_tiny"]),
+    "weights_not_renormalised": ([("(float)(p[e] / tot)", "(float)(p[e])")],
+                                 ["test_k1_weight_is_one", "test_reroute_weight_uses_the_expert_actually_used"]),
+    # experts ([mhpn] §3.1 SwiGLU W1 gate, W3 up)
+    "gate_up_swapped": ([("a[j] = silu(g) * u;", "a[j] = silu(u) * g;")],
+                        ["test_gate_and_up_branches_are_not_swapped"]),
+    # e4m3 format and the FP8 expert path ([2kiu] §5.1 quantised experts)
+    "e4m3_ties_away": ([("double m = (q - f > 0.5 || (q - f == 0.5 && fmod(f, 2.0) != 0.0)) ? f + 1.0 : f;\n"
+                         "    if (m == 8.0)",
+                         "double m = (q - f >= 0.5) ? f + 1.0 : f;\n    if (m == 8.0)")],
+                       ["test_e4m3_encode_ties_and_saturation", "test_q8_activation_rounding_hand_case"]),
+    "quant_scale_not_448": ([("amax / 448.0f", "amax / 256.0f")],
+                            ["test_quantize_row_matches_torch", "test_q8_activation_quantisation_is_identity_on_exact_rows"]),
+    "weight_scale_of_row_0": ([("* (double)w->s[r];", "* (double)w->s[0];")],
+                              ["test_q8_experts_equal_bf16_experts_on_exact_weights"]),
+    "token_dequant_drops_scale": ([("xf[i] = oracle_e4m3_value(codes[i]) * (double)sc;",
+                                    "xf[i] = oracle_e4m3_value(codes[i]);")],
+                                  ["test_q8_activation_quantisation_is_identity_on_exact_rows",
+                                   "test_q8_activation_rounding_hand_case"]),
+    "token_rows_not_quantised": ([("for (int i = 0; i < d; ++i) xf[i] = oracle_e4m3_value(codes[i]) * (double)sc;",
+                                   "(void)0;")], ["test_q8_activation_rounding_hand_case"]),
+    "act_not_rounded_to_bf16": ([("tmp[j] = bf16_to_f32(f32_to_bf16_rne((float)a[j]));", "tmp[j] = (float)a[j];")],
+                                ["test_q8_activation_rounding_hand_case"]),
+    "act_scale_of_token_row": ([("oracle_quantize_row(F, tmp, codes, &sc);",
+                                 "for (int j = 0; j < F; ++j) codes[j] = oracle_e4m3_encode(tmp[j] / sc);")],
+                               ["test_q8_activation_quantisation_is_identity_on_exact_rows",
+                                "test_q8_activation_rounding_hand_case"]),
+    "act_max_before_swiglu": ([("        a[j] = silu(g) * u;\n    }",
+                                "        a[j] = silu(g) * u;\n        if (fabs(g) > gmax) gmax = fabs(g);\n    }"),
+                               ("    float sc = 1.0f;\n", "    float sc = 1.0f;\n    double gmax = 0.0;\n"),
+                               ("oracle_quantize_row(F, tmp, codes, &sc);",
+                                "sc = gmax > 0.0 ? (float)gmax / 448.0f : 1.0f; "
+                                "for (int j = 0; j < F; ++j) codes[j] = oracle_e4m3_encode(tmp[j] / sc);")],
+                              ["test_q8_activation_quantisation_is_identity_on_exact_rows",
+                               "test_q8_activation_rounding_hand_case"]),
+}
+
+
+def _build_and_run(name, tmpdir):
+    edits, _ = MUTANTS[name]
+    with open(oracle._SRC) as fh:
+        src = fh.read()
+    for old, new in edits:
+        n = src.count(old)
+        if n != 1:
+            return None, f"edit of {name!r} matches {n} places"
+        src = src.replace(old, new)
+    c = os.path.join(tmpdir, f"{name}.c")
+    so = os.path.join(tmpdir, f"lib{name}.so")
+    with open(c, "w") as fh:
+        fh.write(src)
+    r = subprocess.run(["gcc", *oracle.CFLAGS, "-I", os.path.dirname(oracle._SRC), "-o", so, c, "-lm"],
+                       capture_output=True, text=True)
+    if r.returncode:
+        return None, r.stderr
+    env = dict(os.environ, MOE_ORACLE_LIBRARY=so)
+    r = subprocess.run([sys.executable, "-m", "pytest", PINS, "-q", "-p", "no:cacheprovider", "-rf",
+                        "-k", "not workload_router_statistics"],
+                       capture_output=True, text=True, env=env, cwd=os.path.dirname(HERE), timeout=600)
+    failed = set(re.findall(r"^FAILED \S*::(test_\w+)", r.stdout, re.M))
+    return failed, r.stdout[-3000:]
+
+
+@pytest.fixture(scope="module")
+def mutant_results(tmp_path_factory):
+    tmpdir = str(tmp_path_factory.mktemp("mutants"))
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        futs = {n: ex.submit(_build_and_run, n, tmpdir) for n in MUTANTS}
+        return {n: f.result() for n, f in futs.items()}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_fails_its_pins(name, mutant_results):
+    failed, log = mutant_results[name]
+    assert failed is not None, log
+    missing = [p for p in MUTANTS[name][1] if p not in failed]
+    assert not missing, f"{name}: pins {missing} did not fail\n{log}"
+
+
+def test_unmutated_copy_passes():
+    """The harness itself: the pins pass on an unedited library built the same way."""
+    MUTANTS["_unmutated"] = ([], [])
+    try:
+        import tempfile
+        with tempfile.TemporaryDirectory() as d:
+            failed, log = _build_and_run("_unmutated", d)
+    finally:
+        del MUTANTS["_unmutated"]
+    assert failed == set(), log

@@ -606,6 +606,134 @@ def test_quantize_row_matches_torch():
     assert sc0 == 1.0 and not codes0.any()
 
 
+def _e4m3_codes(values):
+    """Codes of values that e4m3 holds exactly (torch's float8_e4m3fn conversion, a
+    library routine); checked to decode back to the same values."""
+    v = torch.as_tensor(np.asarray(values, np.float64))
+    codes = v.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy(),
+                          v.numpy()), "not exact in e4m3"
+    return codes
+
+
+def _q8_rows(w, scales):
+    """Weights [.., rows, cols] that are e4m3 values times a per-row scale: (codes, scales)."""
+    scales = np.asarray(scales, np.float32)
+    return _e4m3_codes(w / scales[..., None]).reshape(np.shape(w)), scales
+
+
+def test_q8_activation_quantisation_is_identity_on_exact_rows():
+    """quant_act=1 against quant_act=0 where both quantisations are lossless.
+
+    Each token row is e4m3 values times 2^p with 7*2^p (= 448 * 2^(p-6)) its largest
+    magnitude, so the row scale max/448 is the power of two 2^(p-6) and the codes give the
+    row back exactly.  W1 sends column 1 (= 2^p) to every gate, g = 64 * 2^p >= 64, where
+    silu(g) = g/(1 + e^-g) equals g in double; W3 scales the same column by an e4m3 value
+    over 64, so a = silu(g) u is an e4m3 value times 2^p with 448 * 2^p in every row: exact
+    in bf16 and again quantised losslessly.  The two paths must then agree bit for bit.
+    A dequantisation that drops the scale, a scale other than max/448, or an activation
+    scale taken from g, u or x instead of the bf16 activation row breaks the equality."""
+    rng = np.random.default_rng(21)
+    T, d, F, E, k = 5, 16, 8, 3, 2
+    vals = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    vals = torch.from_numpy(vals).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    small = vals[(np.abs(vals) < 448) & (np.abs(vals) >= 2.0 ** -6)]
+    p = rng.integers(0, 3, size=T)
+    x = rng.choice(small, size=(T, d)) * 2.0 ** -6
+    x[:, 0] = 7.0
+    x[:, 1] = 1.0
+    x *= (2.0 ** p)[:, None]
+    h = bf16(x)
+    assert np.array_equal(widen(h), x.astype(np.float32))
+    w1 = np.zeros((E, F, d))
+    w1[:, :, 1] = 64.0
+    w3 = np.zeros((E, F, d))
+    w3[:, :, 1] = rng.choice(small[np.abs(small) <= 64], size=(E, F)) / 64.0
+    w3[:, 0, 1] = 7.0                       # a = 448 * 2^p in every row
+    w2 = rng.choice(small, size=(E, d, F)) * 2.0 ** -9
+    q1, s1 = _q8_rows(w1, np.ones((E, F)))
+    q3, s3 = _q8_rows(w3, np.full((E, F), 2.0 ** -6))
+    q2, s2 = _q8_rows(w2, np.full((E, d), 2.0 ** -9))
+    assign = np.array([[0, 1], [2, 0], [1, -1], [2, 1], [0, 2]], np.int32)
+    cw = rng.random((T, k)).astype(np.float32)
+    toks = np.arange(T, dtype=np.int32)
+    exact = oracle.combine_rows_q8(h, q1, s1, q3, s3, q2, s2, assign, cw, toks, quant_act=False)
+    quant = oracle.combine_rows_q8(h, q1, s1, q3, s3, q2, s2, assign, cw, toks, quant_act=True)
+    assert np.abs(exact).max() > 0
+    assert np.array_equal(quant, exact)
+    perm = np.array([0, 3, 9, 7, 2, 6, 1, 8, 4], np.int32)     # every kept entry once
+    slots = oracle.expert_slots_q8(h, q1, s1, q3, s3, q2, s2, assign, perm, 0, perm.size, quant_act=True)
+    slots0 = oracle.expert_slots_q8(h, q1, s1, q3, s3, q2, s2, assign, perm, 0, perm.size, quant_act=False)
+    assert np.array_equal(slots, slots0)
+
+
+def _rounding_case():
+    """Two token rows, x_B = 2 x_A, one expert (d = 8, F = 4), worked by hand.
+
+    x_A = (7, 1, 2^-6, 2^-4, 1.15625, 0, 0, 0): max 7, so the row scale is 7/448 = 2^-6;
+    x/scale = (448, 64, 1, 4, 74), and 74 lies between the e4m3 values 72 and 80, so the
+    quantised row is x'_A = (7, 1, 2^-6, 2^-4, 1.125, 0, 0, 0); x_B has scale 2^-5 and the
+    same codes, x'_B = 2 x'_A.
+    W1 puts 64 on column 1 in every row: g = 64 (A) and 128 (B), where silu(g) = g in
+    double.  W3 rows: 7 e_1; 2^-6 e_1 + 2^-10 e_2 + 2^-6 e_3; (15/1024) e_4; 2^-3 e_1
+    (e4m3 codes times a row scale of 1, 2^-14, 2^-8, 1).
+      A: u = (7, 2^-6 + 2^-16 + 2^-10, (15/1024) 1.125, 2^-3),
+         a = 64 u = (448, 1 + 2^-4 + 2^-10, 1.0546875, 8).
+         bf16 rounds a_1 = 1.0634765625 to 1.0625 (7 fraction bits); the row max is 448,
+         scale 1; 1.0625 lies halfway between the e4m3 values 1 and 1.125 and ties to the
+         even code, 1; 1.0546875 rounds to 1.  a' = (448, 1, 1, 8).
+         (Quantising the unrounded a_1 would give 1.125; the unquantised token value
+         1.15625 would make a_2 = 1.083984375 and a'_2 = 1.125.)
+      B: a = (1792, 4.25390625, 4.21875, 32) -> bf16 (1792, 4.25, 4.21875, 32), scale
+         1792/448 = 4, a/4 = (448, 1.0625, 1.0546875, 8) -> (448, 1, 1, 8),
+         a' = (1792, 4, 4, 32).
+    W2 rows (e4m3 times 2^-8 or 1): 2^-8 e_0; e_1; 2^-3 e_3; 2^-1 e_1 + 2^-4 e_3; e_2; zeros.
+      y_A = (448/256, 1, 1, 1/2 + 1/2, 1, 0, 0, 0) = (1.75, 1, 1, 1, 1, 0, 0, 0)
+      y_B = (7, 4, 4, 4, 4, 0, 0, 0)."""
+    d, F = 8, 4
+    x = np.zeros((2, d))
+    x[0, :5] = [7, 1, 2.0 ** -6, 2.0 ** -4, 1.15625]
+    x[1] = 2 * x[0]
+    w1 = np.zeros((1, F, d))
+    w1[0, :, 1] = 64
+    w3 = np.zeros((1, F, d))
+    w3[0, 0, 1] = 7
+    w3[0, 1, 1:4] = [2.0 ** -6, 2.0 ** -10, 2.0 ** -6]
+    w3[0, 2, 4] = 15 / 1024
+    w3[0, 3, 1] = 2.0 ** -3
+    w2 = np.zeros((1, d, F))
+    w2[0, 0, 0] = 2.0 ** -8
+    w2[0, 1, 1] = 1
+    w2[0, 2, 3] = 2.0 ** -3
+    w2[0, 3, 1] = 0.5
+    w2[0, 3, 3] = 2.0 ** -4
+    w2[0, 4, 2] = 1
+    q1, s1 = _q8_rows(w1, np.ones((1, F)))
+    q3, s3 = _q8_rows(w3, [[1, 2.0 ** -14, 2.0 ** -8, 1]])
+    q2, s2 = _q8_rows(w2, [[2.0 ** -8, 1, 1, 1, 1, 1, 1, 1]])
+    want = np.array([[1.75, 1, 1, 1, 1, 0, 0, 0], [7, 4, 4, 4, 4, 0, 0, 0]], np.float32)
+    return bf16(x), (q1, s1, q3, s3, q2, s2), want
+
+
+def test_q8_activation_rounding_hand_case():
+    """The bf16 rounding of a = silu(g) u before its quantisation decides an e4m3 code
+    (the tie at 1.0625), and the token row's quantisation decides another (74 -> 72):
+    the hand-worked rows of _rounding_case, through both the token-order and the
+    slot-order oracle functions."""
+    h, q, want = _rounding_case()
+    assign = np.array([[0], [0]], np.int32)
+    cw = np.ones((2, 1), np.float32)
+    got = oracle.combine_rows_q8(h, *q, assign, cw, np.arange(2, dtype=np.int32), quant_act=True)
+    np.testing.assert_array_equal(got, want)
+    slots = oracle.expert_slots_q8(h, *q, assign, np.array([1, 0], np.int32), 0, 2, quant_act=True)
+    np.testing.assert_array_equal(slots, want[::-1])
+    # without quantisation of the token and activation rows the unrounded values reach
+    # the output: a_1 = 1.0634765625 and a_2 = 64 (15/1024) 1.15625 = 1.083984375
+    raw = oracle.combine_rows_q8(h, *q, assign, cw, np.arange(2, dtype=np.int32), quant_act=False)
+    assert raw[0, 1] == np.float32(1.0634765625) and raw[1, 1] == np.float32(4 * 1.0634765625)
+    assert raw[0, 4] == np.float32(1.083984375) and raw[1, 4] == np.float32(4 * 1.083984375)
+
+
 # --------------------------------------------------------------------------- router variants
 # Temperature ([cnnetsun] §3.1 step 3; [2kiu] §2), normalisation before the
 # router ([2kiu] §5.2), the two-layer router silu(x W1) W2 ([cnnetsun] §3.1 step 2).

@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.CONFIG_ORDER)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads measured after the main one (the 'workloads' key)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--fp8-weights", action="store_true",
                     help="expert GEMMs in e4m3: weights quantised per row once (moe_quantize_fp8), "
@@ -205,6 +207,24 @@ def recorded_traffic(kernel: str, workload: str):
     return rec["dram_bytes_per_launch"]
 
 
+SUSTAINED_AFTER_S = 2.0   # a timed region at least this long is held to the sustained peak
+
+
+def tensor_peak(peaks, peak_kind, timed_s, fp8=False):
+    """(TFLOP/s, description): the measured bf16 burst peak for a timed region shorter
+    than SUSTAINED_AFTER_S, the sustained one (a seconds-long loop under the power cap)
+    for a longer one; for e4m3 MMAs times 2, the nominal e4m3 / bf16 ratio."""
+    if timed_s < SUSTAINED_AFTER_S or "bf16_tflops_sustained" not in peaks:
+        v, kind = float(peaks["bf16_tflops"]), (f"{peak_kind} bf16 burst (timed region "
+                                               f"{timed_s:.2f} s < {SUSTAINED_AFTER_S:.0f} s)")
+    else:
+        v, kind = float(peaks["bf16_tflops_sustained"]), (f"{peak_kind} bf16 sustained (timed region "
+                                                          f"{timed_s:.2f} s)")
+    if fp8:
+        v, kind = 2.0 * v, kind + " x 2, the nominal e4m3 / bf16 ratio"
+    return v, kind
+
+
 def layer_inputs(shape, device="cuda"):
     h, wr, bias, usage = synth.router_inputs(shape)
     w1, w3, w2 = synth.expert_weights(shape, device=device)
@@ -290,6 +310,7 @@ def host_cpu():
 def run_reference(args, rank, world):
     if rank != 0:
         return
+    import oracle   # this arm never loads the CUDA library
     shape = synth.CONFIGS[args.workload]
     h, wr, bias, usage = synth.router_inputs(shape)
     w1, w3, w2 = synth.expert_weights(shape, device="cpu")
@@ -312,20 +333,21 @@ def run_reference(args, rank, world):
             "steps": steps, "steps_requested": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * shape.T / v, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(shape),
+            "config": workload_config(shape, capacity_fn=oracle.capacity),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample, "host": host_cpu()},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def workload_config(shape, router=None, graph=False):
+def workload_config(shape, router=None, graph=False, capacity_fn=None):
     extra = {"router": router} if router else {}
     if graph:
         extra["launch"] = "CUDA graph replay of one step"
+    cap = (capacity_fn or moe.capacity)(shape.T, shape.k, shape.E, shape.cf, shape.capacity)
     return {**extra, "workload": shape.name, "T": shape.T, "d_model": shape.d, "E": shape.E, "k": shape.k,
             "d_ff": shape.F, "cf": shape.cf, "lambda": shape.lam,
-            "capacity": moe.capacity(shape.T, shape.k, shape.E, shape.cf, shape.capacity),
+            "capacity": cap,
             "parallelism": "replicas", "l2": "inputs larger than L2: every step streams "
             f"{3 * shape.E * shape.F * shape.d * 2 / 1e9:.2f} GB of expert weights"}
 
@@ -514,33 +536,9 @@ def run_ours(args, rank, world, local):
 
     peaks, peak_kind = load_peaks()
     d, F, T = shape.d, shape.F, shape.T
-    # algorithmic work per launch: kept rows only; every active expert's weights read once
-    flops = {"gate_up": 2.0 * kept * d * 2 * F, "down": 2.0 * kept * F * d}
-    wb = 1 if fp8 else 2   # bytes per weight element (+ 4 per weight row for FP8 scales)
-    # (FP8: the GEMMs read 1-byte activation rows; the act quantisation pass
-    # between them is timed in the down stage)
-    bytes_ = {"gate_up": active * 2.0 * F * (d * wb + 4 * fp8) + kept * d * wb + kept * F * 2,
-              "down": active * 1.0 * d * (F * wb + 4 * fp8) + kept * F * wb + kept * d * 2}
-    dom = max(("gate_up", "down"), key=lambda n: stage_ms[n])
-    peak_tf = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
-    if fp8:   # e4m3 MMAs: the measured bf16 peak times the nominal e4m3 / bf16 ratio (4.5 / 2.25)
-        peak_tf *= 2.0
-    peak_bw = float(peaks["hbm_gbs"])
-    intensity = (flops["gate_up"] + flops["down"]) / (bytes_["gate_up"] + bytes_["down"])
-    sec = stage_ms[dom] * 1e-3
-    if intensity * 1e9 >= peak_tf * 1e12 / peak_bw:     # above the ridge: tensor bound
-        roof = {"bound": "tensor", "achieved": flops[dom] / sec / 1e12, "peak": peak_tf,
-                "unit": "TFLOP/s",
-                "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long loop)"
-                             + (" x 2, the nominal e4m3 / bf16 ratio" if fp8 else "")}
-    else:
-        roof = {"bound": "hbm", "achieved": bytes_[dom] / sec / 1e9, "peak": peak_bw,
-                "unit": "GB/s", "peak_kind": f"{peak_kind} HBM copy bandwidth"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    kname = f"moe_gemm_kernel ({dom.replace('_', '-')}{', e4m3' if fp8 else ''})"
-    roof["traffic"] = recorded_traffic(kname, shape.name)
-    roof["kernel"] = kname
-    roof["algorithmic_per_launch"] = {"flop": flops[dom], "bytes": bytes_[dom]}
+    roof, expert_tflops, weight_gbs = expert_roofline(shape, kept, active, stage_ms, peaks, peak_kind,
+                                                      ms_max * 1e-3, fp8)
+    peak_tf = tensor_peak(peaks, peak_kind, ms_max * 1e-3, fp8)[0]
     bwd_line = None
     if bwd:
         # the backward's GEMM work on the kept rows: g and u recomputed (2 d 2F), W2^T dout
@@ -555,9 +553,6 @@ def run_ours(args, rank, world, local):
                     "frac": bflops / sec_b / 1e12 / peak_tf, "padded_rows": rows_pad, "kept_rows": kept,
                     "gemms": "cuBLAS strided-batched (bf16 in, fp32 accumulate)",
                     "kernels": "this library's: pad, SwiGLU backward, router backward, dh, bias sum"}
-    expert_tflops = (flops["gate_up"] + flops["down"]) / (
-        (stage_ms["gate_up"] + stage_ms["down"]) * 1e-3) / 1e12
-    weight_bytes = 3.0 * active * F * d * wb
     value = world * T * args.steps / (ms_max * 1e-3)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -569,7 +564,7 @@ def run_ours(args, rank, world, local):
         "config": workload_config(shape, router_desc, graph is not None),
         "roofline": roof,
         "expert_gemm_tflops": expert_tflops,
-        "weight_stream_gbs": weight_bytes / ((stage_ms["gate_up"] + stage_ms["down"]) * 1e-3) / 1e9,
+        "weight_stream_gbs": weight_gbs,
         "stages_ms": stage_ms, "kept_rows": kept,
         "clocks": clk,
         "e2e": ({"value": world * T * args.e2e_steps / te, "unit": UNIT,
@@ -593,8 +588,132 @@ def run_ours(args, rank, world, local):
                        f"expert FFN of {res['ffn_rows']} of {res['kept']} kept rows "
                        f"({res['t_ffn_sample']:.1f} s), extrapolated by kept rows"),
             "host": host_cpu()}
+    plain = not (fp8 or bwd or variant or graph is not None)
+    if plain and not args.no_workloads:
+        del L, ws, wss, h_devs, outs
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["workloads"] = {}
+        for name, wfp8 in SIDE_WORKLOADS:
+            if name == shape.name and not wfp8:
+                continue
+            line["workloads"][name + ("_fp8" if wfp8 else "")] = side_workload(name, wfp8, peaks, peak_kind)
+            torch.cuda.empty_cache()
+        line["gpu_launches"] += sum(w["gpu_launches"] for w in line["workloads"].values())
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def expert_roofline(shape, kept, active, stage_ms, peaks, peak_kind, timed_s, fp8):
+    """Roofline of the dominant expert GEMM (gate-up or down) of one layer step: its
+    algorithmic work per launch -- kept rows only, every active expert's weights read
+    once -- over its mean CUDA-event duration; plus the two expert GEMMs' TFLOP/s and
+    weight-streaming GB/s together."""
+    d, F = shape.d, shape.F
+    flops = {"gate_up": 2.0 * kept * d * 2 * F, "down": 2.0 * kept * F * d}
+    wb = 1 if fp8 else 2   # bytes per weight element (+ 4 per weight row for FP8 scales)
+    # (FP8: the GEMMs read 1-byte activation rows; the act quantisation pass
+    # between them is timed in the down stage)
+    bytes_ = {"gate_up": active * 2.0 * F * (d * wb + 4 * fp8) + kept * d * wb + kept * F * 2,
+              "down": active * 1.0 * d * (F * wb + 4 * fp8) + kept * F * wb + kept * d * 2}
+    dom = max(("gate_up", "down"), key=lambda n: stage_ms[n])
+    peak_tf, tf_kind = tensor_peak(peaks, peak_kind, timed_s, fp8)
+    peak_bw = float(peaks["hbm_gbs"])
+    intensity = (flops["gate_up"] + flops["down"]) / (bytes_["gate_up"] + bytes_["down"])
+    sec = stage_ms[dom] * 1e-3
+    if intensity * 1e9 >= peak_tf * 1e12 / peak_bw:     # above the ridge: tensor bound
+        roof = {"bound": "tensor", "achieved": flops[dom] / sec / 1e12, "peak": peak_tf,
+                "unit": "TFLOP/s", "peak_kind": tf_kind}
+    else:
+        roof = {"bound": "hbm", "achieved": bytes_[dom] / sec / 1e9, "peak": peak_bw,
+                "unit": "GB/s", "peak_kind": f"{peak_kind} HBM copy bandwidth"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    kname = f"moe_gemm_kernel ({dom.replace('_', '-')}{', e4m3' if fp8 else ''})"
+    roof["traffic"] = recorded_traffic(kname, shape.name)
+    roof["kernel"] = kname
+    roof["algorithmic_per_launch"] = {"flop": flops[dom], "bytes": bytes_[dom]}
+    gemm_s = (stage_ms["gate_up"] + stage_ms["down"]) * 1e-3
+    expert_tflops = (flops["gate_up"] + flops["down"]) / gemm_s / 1e12
+    weight_gbs = 3.0 * active * F * d * wb / gemm_s / 1e9
+    return roof, expert_tflops, weight_gbs
+
+
+# The other workloads, measured after the main one in the same run (eager steps
+# over a ~0.2 s timed region, and CUDA-graph replays for the launch-bound batches
+# of one routing chunk), each with its dominant expert GEMM's roofline.
+SIDE_WORKLOADS = [("mixtral_decode", False), ("mixtral_decode", True), ("fine_grained", False),
+                  ("skewed", False), ("tiny", False), ("mixtral_prefill", False)]
+SIDE_TIMED_S = 0.2
+
+
+def side_workload(name, fp8, peaks, peak_kind):
+    shape = synth.CONFIGS[name]
+    L = layer_inputs(shape)
+    del L["w1"], L["w3"]
+    if fp8:
+        L["w13"] = moe.quantize_fp8(L["w13"])
+        L["w2"] = moe.quantize_fp8(L["w2"])
+    cfg = moe.Config.of(shape, flags=moe.FLAG_FP8 if fp8 else 0)
+    ws = moe.workspace(cfg)
+    out = torch.empty(shape.T, shape.d, dtype=torch.bfloat16, device="cuda")
+    _, aux = moe.layer_forward(cfg, ws, L["h"], L["wr"], L["w13"], L["w2"], L["bias"], L["usage"],
+                               aux=True, out=out)
+    counts = aux["counts"].cpu()
+    kept, active = int(counts.sum().item()), int((counts > 0).sum().item())
+
+    def step(evs=None):
+        moe.layer_forward(cfg, ws, L["h"], L["wr"], L["w13"], L["w2"], L["bias"], L["usage"],
+                          stage_events=evs, out=out)
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    steps = int(min(400, max(20, 1e3 * SIDE_TIMED_S / max(e0.elapsed_time(e1) / 5, 1e-3))))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)] for _ in range(steps)]
+    e0.record()
+    for i in range(steps):
+        step(evs[i])
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    st = moe.device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"{name}: device status {st} ({moe.STATUS.get(st)})")
+    stage_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
+                for j, n in enumerate(moe.STAGE_NAMES)}
+    roof, tflops, wgbs = expert_roofline(shape, kept, active, stage_ms, peaks, peak_kind, ms * 1e-3, fp8)
+    res = {"tokens_per_s": shape.T * steps / (ms * 1e-3), "ms_per_step": ms / steps, "steps": steps,
+           "dtype": "e4m3 expert weights and activations" if fp8 else "bf16",
+           "kept_rows": kept, "stages_ms": stage_ms, "roofline": roof, "expert_gemm_tflops": tflops,
+           "weight_stream_gbs": wgbs, "weight_stream_frac_of_hbm": wgbs / float(peaks["hbm_gbs"]),
+           "gpu_launches": kernels_per_step(shape.T, fp8) * steps,
+           "config": {k: v for k, v in workload_config(shape).items() if k != "l2"}}
+    if shape.T <= CHUNK:   # launch-bound: the same step replayed from a CUDA graph
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        e0.record()
+        for _ in range(steps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        res["ms_per_step_graph"] = e0.elapsed_time(e1) / steps
+        res["tokens_per_s_graph"] = shape.T * steps / (e0.elapsed_time(e1) * 1e-3)
+        res["gpu_launches"] += kernels_per_step(shape.T, fp8) * (steps + 3)
+        del g
+    del L, ws, out
+    return res
 
 
 def main():

@@ -380,7 +380,9 @@ moe_status_t moe_debug_timeout_probe(void* ws_dev, size_t ws_bytes, int64_t budg
  * Scratch lives in one file-scope device array of MOE_STATIC_SCRATCH_BYTES,
  * held by every GPU that loads the library until the process exits.  Its
  * device address is looked up with cudaGetSymbolAddress during the first call
- * on each device (make that first call before any stream capture).  A config
+ * in each CUDA context -- on each device, and again on a device after a reset
+ * has recreated its context -- and kept for that context (make that first call
+ * before any stream capture).  A config
  * whose scratch does not fit (max(16, E rounded up to 16) + 9k bytes per token
  * plus (8k+4)*E bytes per 256 tokens; about 48k tokens at E=64, k=2) returns
  * MOE_ERR_UNSUPPORTED before anything is enqueued.  The call performs no

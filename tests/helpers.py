@@ -58,6 +58,37 @@ def sample_tokens(T: int, n: int, seed: int, must=()) -> np.ndarray:
     return np.array(toks, np.int32)
 
 
+def tile_tokens(perm: np.ndarray, offsets: np.ndarray, k: int, seed: int, tile: int = 128) -> np.ndarray:
+    """One token per (expert, row tile) of the expert GEMMs: for every 128-slot row tile
+    of every expert's slot range, the token of one of its slots (the tile's last slot
+    for an expert's tail tile, a seeded random one otherwise), so that a fault confined
+    to one row tile or one expert's ragged tail shows in some checked row."""
+    rng = np.random.default_rng(seed)
+    toks = set()
+    for e in range(offsets.shape[0] - 1):
+        off, cnt = int(offsets[e]), int(offsets[e + 1] - offsets[e])
+        for m0 in range(0, cnt, tile):
+            m1 = min(cnt, m0 + tile)
+            j = m1 - 1 if m1 == cnt else int(rng.integers(m0, m1))
+            toks.add(int(perm[off + j]) // k)
+    return np.array(sorted(toks), np.int32)
+
+
+def assert_rows_close(got: np.ndarray, want: np.ndarray, bound: float = OUT_REL_FROB):
+    """The pooled relative Frobenius bound, and a per-row bound of 4x it (rows the
+    oracle gives as exact zeros -- every choice dropped -- must be zero)."""
+    err = rel_frob(got, want)
+    assert err <= bound, f"relative Frobenius error {err:.3e}"
+    nw = np.linalg.norm(np.asarray(want, np.float64), axis=1)
+    ng = np.linalg.norm(np.asarray(got, np.float64) - np.asarray(want, np.float64), axis=1)
+    zero = nw == 0
+    assert (ng[zero] == 0).all(), "a row the oracle gives as zero is not zero"
+    rows = ng[~zero] / nw[~zero]
+    if rows.size:
+        i = int(np.argmax(rows))
+        assert rows[i] <= 4 * bound, f"row {np.flatnonzero(~zero)[i]}: relative error {rows[i]:.3e}"
+
+
 def oracle_dispatch_of(scores: np.ndarray, k: int, C: int):
     return oracle.dispatch(scores, k, C)
 

@@ -11,7 +11,8 @@ import pytest
 import torch
 
 import oracle
-from helpers import OUT_REL_FROB, assert_dispatch_equal, bits, make_layer, np_, rel_frob, sample_tokens
+from helpers import (OUT_REL_FROB, assert_dispatch_equal, assert_rows_close, bits, make_layer, np_, rel_frob,
+                     sample_tokens, tile_tokens)
 from token_level_top_gb300.moe import MoEError
 from token_level_top_gb300 import moe, synth
 
@@ -96,10 +97,10 @@ def test_expert_ffn_fp8_vs_oracle(T, d, E, F, k, cf):
     assert rows.max() <= 4 * OUT_REL_FROB
 
 
-SAMPLE = {"tiny": 256, "mixtral_decode": 10}
+SAMPLE = {"tiny": 256, "mixtral_decode": 10, "mixtral_prefill": 4}
 
 
-@pytest.mark.parametrize("name", ["tiny", "mixtral_decode"])
+@pytest.mark.parametrize("name", ["tiny", "mixtral_decode", "mixtral_prefill"])
 def test_layer_forward_fp8_workloads(name):
     shape = synth.CONFIGS[name]
     Ld = make_layer(shape)
@@ -113,12 +114,14 @@ def test_layer_forward_fp8_workloads(name):
     o_r = oracle.route(shape.k, logits_in=np_(aux["logits"]))
     o_d = oracle.dispatch(o_r["scores"], shape.k, C)
     assert_dispatch_equal(aux, o_d, shape.T, shape.k)
+    # sampled tokens, and one in every (expert, 128-row tile) of the expert GEMMs
+    must = tile_tokens(o_d["perm"], o_d["offsets"], shape.k, shape.seed)
     toks = (np.arange(shape.T, dtype=np.int32) if SAMPLE[name] >= shape.T
-            else sample_tokens(shape.T, SAMPLE[name], shape.seed))
+            else sample_tokens(shape.T, SAMPLE[name], shape.seed, must=must))
     want = oracle.combine_rows_q8(bits(Ld["h"]), o["q1"], o["s1"], o["q3"], o["s3"], o["q2"], o["s2"],
                                   o_d["assign"], o_d["cw"], toks)
     got = np_(out.float())[toks]
-    assert rel_frob(got, want) <= OUT_REL_FROB
+    assert_rows_close(got, want)
 
 
 def test_layer_forward_fp8_deterministic():

@@ -5,6 +5,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
 
 #include "common.cuh"
@@ -78,6 +79,46 @@ struct Ev {
 };
 
 }  // namespace
+
+namespace {
+using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+template <class Fn>
+Fn driver_fn(const char* name)
+{
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(p);
+}
+}  // namespace
+
+unsigned long long context_id()
+{
+    static const PfnCtxGetCurrent get_cur = driver_fn<PfnCtxGetCurrent>("cuCtxGetCurrent");
+    static const PfnCtxGetId get_id = driver_fn<PfnCtxGetId>("cuCtxGetId");
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_cur || !get_id || get_cur(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id + 1;
+}
+
+cudaError_t ensure_smem_limit(const void* fn, int bytes)
+{
+    static std::mutex mu;
+    static std::map<std::pair<unsigned long long, const void*>, int> done;
+    const unsigned long long ctx = context_id();   // 0: no context yet; set it every call until there is one
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find({ctx, fn});
+    if (ctx != 0 && it != done.end() && it->second >= bytes) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && ctx != 0) done[{ctx, fn}] = bytes;
+    return e;
+}
 
 int num_sms()
 {

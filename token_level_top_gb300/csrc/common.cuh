@@ -1,5 +1,5 @@
 // common.cuh -- device helpers shared by the libmoe kernels (sm_103a only):
-// mbarriers with bounded waits, TMA tile / gather4 loads, tcgen05 MMA, TMEM
+// mbarriers with bounded waits, TMA tile loads, tcgen05 MMA, TMEM
 // allocation and loads, and the workspace status word.
 #pragma once
 
@@ -120,18 +120,6 @@ __device__ __forceinline__ void cluster_sync_all()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
-}
-
-// Gathers 4 rows (r0..r3, each one box of the map's inner width, box height
-// 1) into consecutive rows of shared memory at dst.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int x, int r0,
-                                            int r1, int r2, int r3, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-        : "memory");
 }
 
 // ----------------------------------------------------------------- tcgen05

@@ -14,14 +14,15 @@
 // chunks) + (stable rank inside its chunk) -- both written by the route
 // kernel.  Stage 1 (one CTA) scans the chunk histograms per expert, finds the
 // first chunk q1 in which some expert's running count passes C, and leaves
-// the per-chunk bases.  From chunk q1 on, one warp of the CTA replays the
-// entries in windows of 32 consecutive entries of one rank, one per lane:
-// each entry picks its expert under the current full set, __match_any_sync
-// gives it its rank among the window's entries of that expert (slot = fill +
-// rank), a ballot finds the first entry that takes an expert's last slot,
-// everything up to it commits, and entries after it that chose the now-full
-// expert choose again.  A single warp needs no block barriers, which on this
-// sequential chain cost more than the wider windows save.  Stage 2 (grid-wide) writes the entries
+// the per-chunk bases.  From chunk q1 on, 8 warps of the CTA (256 threads,
+// synchronised on named barrier 1) replay the entries in windows of 256
+// consecutive entries of one rank, one per thread: each entry picks its
+// expert under the current full set, __match_any_sync gives it its rank
+// among its warp's entries of that expert and each warp adds the earlier
+// warps' counts of that expert (slot = fill + rank), a block minimum finds the
+// first entry that takes an expert's last slot, everything up to it commits,
+// and entries after it that chose the now-full expert choose again (three
+// barriers per iteration).  Stage 2 (grid-wide) writes the entries
 // before q1, the permutation in slot order and the combine weights
 // ([mhpn] §4.3: router probabilities renormalised over the experts used).
 #include <math.h>
@@ -487,14 +488,9 @@ constexpr size_t kSmallSmemCap = 68 * 1024;   // >= kChunk*(pref_stride(255) + 8
 template <int EPL>
 cudaError_t launch_small(const RouteArgs& ra, const SerialArgs& sa, size_t smem, cudaStream_t s)
 {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(route_dispatch_small_kernel<EPL>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmallSmemCap));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(route_dispatch_small_kernel<EPL>),
+                                      static_cast<int>(kSmallSmemCap));
+    if (e != cudaSuccess) return e;
     route_dispatch_small_kernel<EPL><<<1, detail::kRouteThreads, smem, s>>>(ra, sa);
     return cudaGetLastError();
 }
@@ -525,16 +521,11 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s)
     const size_t smem = need < kSerialSmemCap ? need : kSerialSmemCap;
     sa.stage_cap = static_cast<int>(smem);
     set_fallback(sa);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(dispatch_serial_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSerialSmemCap));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(dispatch_serial_kernel),
+                                      static_cast<int>(kSerialSmemCap));
+    if (e != cudaSuccess) return e;
     dispatch_serial_kernel<<<1, kSerialThreads, smem, s>>>(sa);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dispatch_finish_kernel<<<(a.T + 255) / 256, 256, 0, s>>>(a);
     return cudaGetLastError();

@@ -3,7 +3,7 @@
 //
 //   GK_ROUTER        logits partials  = h . W_r^T          (K split across CTAs)
 //   GK_GATEUP        act = silu(x W1^T) * (x W3^T), x = the slot-ordered token rows
-//                    (tiled from x_perm, or gathered from h by tile::gather4)
+//                    (tiles of x_perm, the rows gathered by a separate pass)
 //   GK_DOWN_SLOTS    y_slots     = act W2^T                 (slot order, bf16)
 //
 // The router is the linear map of the token's hidden state to expert logits
@@ -14,8 +14,7 @@
 // [2kiu] §3 step 5).
 //
 // One CTA per SM (or two for the router), 6 warps:
-//   warp 0    TMA producer: A tile 128 x 64 (tiled, or gathered 4 rows per
-//             tile::gather4 by all 32 lanes) and B tile BN x 64, 128-byte
+//   warp 0    TMA producer: A tile 128 x 64 and B tile BN x 64, 128-byte
 //             swizzle, into a ring of `stages` shared-memory slots;
 //   warp 1    allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=16;
 //             FP8: kind::f8f6f4, K=32) into one of two TMEM accumulators and
@@ -47,7 +46,6 @@ struct GemmParams {
     int splits;        // router K splits
     int kb_per_split;  // router K blocks per split
     int stages;
-    int gather4;       // gate-up: A rows gathered from h with tile::gather4 (else tiled from x_perm)
     int b_policy;      // L2 policy of the weight loads: 0 default, 1 evict_first
     const float* b_scale;  // FP8: the scale of each weight row (output channel)
     const float* a_scale;  // FP8: the scale of each activation row (slot order)
@@ -210,20 +208,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load in flight + its parity
         for (int tile = tile0; tile < total_tiles && ok; tile += tile_step) {
             const TileInfo ti = decode_tile<PAIR>(p, tile, s_tile_start, s_offs, rank);
-            int r0 = 0, r1 = 0, r2 = 0, r3 = 0, arow = 0, brow = 0;
+            int arow = 0, brow = 0;
             if (p.kind == GK_GATEUP) {
-                const int off = s_offs[ti.e];
-                if (p.gather4) {
-                    const int cnt = s_offs[ti.e + 1] - off;
-                    const int j0 = ti.m * kBM + lane * 4;
-                    const int fallback = p.perm[off + ti.m * kBM] / p.topk;  // a valid row
-                    r0 = (j0 + 0 < cnt) ? p.perm[off + j0 + 0] / p.topk : fallback;
-                    r1 = (j0 + 1 < cnt) ? p.perm[off + j0 + 1] / p.topk : fallback;
-                    r2 = (j0 + 2 < cnt) ? p.perm[off + j0 + 2] / p.topk : fallback;
-                    r3 = (j0 + 3 < cnt) ? p.perm[off + j0 + 3] / p.topk : fallback;
-                } else {
-                    arow = off + ti.m * kBM;
-                }
+                arow = s_offs[ti.e] + ti.m * kBM;
                 brow = ti.e * 2 * p.F + ti.n * kExpertBN;
             } else if (p.kind == GK_ROUTER) {
                 arow = ti.m * kBM;
@@ -256,11 +243,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             tma_load_2d_pair(dB, &tmB, x, brow + rank * (p.bn / 2), fb);
                     }
                 } else {
-                    if (p.kind == GK_GATEUP && p.gather4)
-                        tma_gather4(dA + lane * 4 * 128, &tmA, x, r0, r1, r2, r3, fb);
-                    else if (lane == 0)
-                        tma_load_2d(dA, &tmA, x, arow, fb);
                     if (lane == 0) {
+                        tma_load_2d(dA, &tmA, x, arow, fb);
                         if (p.b_policy)
                             tma_load_2d_hint(dB, &tmB, x, brow, fb, pol_b);
                         else
@@ -615,8 +599,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     int grid = 0;
     const int sms = num_sms();
     // Row tiles are paired when the experts average at least two of them.
-    const bool pair = (g.kind != GK_ROUTER) && !g.gather4 && !(fp8 && g.gather4) &&
-                      static_cast<long long>(g.T) * g.topk >= 2LL * kBM * g.E;
+    const bool pair = (g.kind != GK_ROUTER) && static_cast<long long>(g.T) * g.topk >= 2LL * kBM * g.E;
     if (g.kind == GK_ROUTER) {
         p.bn = g.epad;
         p.kb_total = g.d / kBK;
@@ -628,17 +611,11 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
         if (!make_map(&tmB, g.b_ptr, g.E, g.d, p.bn)) return cudaErrorInvalidValue;
         grid = std::min(p.m_tiles * p.splits, router_ctas_per_sm(g.E) * sms);
     } else if (g.kind == GK_GATEUP) {
-        if (fp8 && g.gather4) return cudaErrorInvalidValue;
         p.bn = kExpertBN;
         p.kb_total = g.d / kstep;
         p.n_tiles = g.F / (kExpertBN / 2);
-        p.gather4 = g.gather4;
-        if (g.gather4) {
-            if (!make_map(&tmA, g.a_ptr, g.T, g.d, 1)) return cudaErrorInvalidValue;
-        } else {
-            if (!map(&tmA, g.a_ptr, static_cast<uint64_t>(g.T) * g.topk, g.d, kBM))
-                return cudaErrorInvalidValue;
-        }
+        if (!map(&tmA, g.a_ptr, static_cast<uint64_t>(g.T) * g.topk, g.d, kBM))
+            return cudaErrorInvalidValue;
         if (!map(&tmB, g.b_ptr, static_cast<uint64_t>(g.E) * 2 * g.F, g.d, pair ? kExpertBN / 2 : kExpertBN))
             return cudaErrorInvalidValue;
         const long long mt_max = (static_cast<long long>(g.T) * g.topk + kBM - 1) / kBM + g.E;
@@ -679,21 +656,11 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s)
     p.tmem_cols = pow2_cols(2 * p.bn);
     const size_t smem = fixed + static_cast<size_t>(stages) * (a_bytes + b_bytes + 16);
 
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(moe_gemm_kernel<false, false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(moe_gemm_kernel<true, false>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(moe_gemm_kernel<false, true>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(moe_gemm_kernel<true, true>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    });
+    const void* kfn = pair ? (fp8 ? reinterpret_cast<const void*>(moe_gemm_kernel<true, true>)
+                                  : reinterpret_cast<const void*>(moe_gemm_kernel<true, false>))
+                           : (fp8 ? reinterpret_cast<const void*>(moe_gemm_kernel<false, true>)
+                                  : reinterpret_cast<const void*>(moe_gemm_kernel<false, false>));
+    const cudaError_t attr_err = ensure_smem_limit(kfn, 227 * 1024);
     if (attr_err != cudaSuccess) return attr_err;
     if (grid <= 0) return cudaSuccess;
     if (!pair) {

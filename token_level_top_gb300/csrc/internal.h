@@ -54,6 +54,12 @@ inline size_t dispatch_base_bytes(size_t T, size_t k, size_t nch, size_t E)
 }
 
 bool layout_for(const moe_config_t& c, WsLayout* L);
+// A process-unique id of the current CUDA context (0 if none or unknown):
+// host-side set-up that belongs to a context (function attributes, symbol
+// addresses) is done again in a new one -- another device, or after a reset.
+unsigned long long context_id();
+// Raises fn's dynamic shared-memory limit to `bytes` once per context.
+cudaError_t ensure_smem_limit(const void* fn, int bytes);
 int router_splits(int T, int d, int E);
 int router_ctas_per_sm(int E);   // router GEMM CTAs resident per SM (shared memory bound)
 int num_sms();
@@ -126,7 +132,7 @@ cudaError_t launch_route_dispatch_small(const RouteArgs& ra, const DispatchArgs&
 struct GemmLaunch {
     int kind;
     int E, T, topk, d, F;
-    const void* a_ptr;  // router/gate-up: h [T,d]; down: act [T*k, F]
+    const void* a_ptr;  // router: h [T,d]; gate-up: x_perm [T*k, d]; down: act [T*k, F]
     const void* b_ptr;  // router: W_r [E,d]; gate-up: W13 [E,2F,d]; down: W2 [E,d,F]
     const int32_t* offsets;
     const int32_t* perm;
@@ -134,7 +140,6 @@ struct GemmLaunch {
     void* y_slots;
     float* router_part;
     int splits, epad;
-    int gather4;  // gate-up: gather A rows from h (a_ptr = h) instead of tiles of x_perm
     long long rows_cap;  // most rows an expert can hold (the capacity C), or 0 if unknown
     int fp8;                 // expert GEMMs: a_ptr and b_ptr hold e4m3 rows, each with
     const float* a_scale;    //   its scale: a_scale per activation row (slot order),

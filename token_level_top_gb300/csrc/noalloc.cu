@@ -12,13 +12,17 @@
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds MOE_STATIC_SCRATCH_BYTES of it until the process exits.  Host
 // code cannot use the array's name as a device address (on the host it names
-// a stand-in object), so the device address is looked up once per device with
-// cudaGetSymbolAddress, with that device current, on the first call made on
-// it, and cached.  Every call shares the array and it keeps the previous
+// a stand-in object), so the device address is looked up with
+// cudaGetSymbolAddress, with the caller's device current, on the first call
+// made in each CUDA context (each device, and again after a device reset
+// recreates the context and reloads the library's module there), and cached
+// for that context.  That first call may load the module, so it should come
+// before any stream capture.  Every call shares the array and it keeps the previous
 // call's contents; the only word that must start at zero (the device status
 // word) is cleared at the start of each call.  Calls that overlap on the GPU
 // (different streams, or different host threads, without ordering between
 // them) race on the array.
+#include <map>
 #include <mutex>
 
 #include "common.cuh"
@@ -28,7 +32,6 @@ namespace moe {
 namespace {
 
 constexpr size_t kStaticScratchBytes = MOE_STATIC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_dispatch_scratch[kStaticScratchBytes];
 
@@ -65,22 +68,27 @@ StaticLayout static_layout(const moe_config_t& c)
     return L;
 }
 
-// Device address of the scratch array on the current device (looked up on
-// the first call per device and cached).
+// Device address of the scratch array in the current context: looked up on
+// the first call in each context and cached under the context's id.  A new
+// context (another device, or the device reset) has its own copy of the
+// module and of the array, at an address of its own.
 moe_status_t scratch_address(char** out)
 {
     static std::mutex mu;
-    static void* addr[kMaxDevices] = {};
+    static std::map<unsigned long long, void*> addr;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+    const unsigned long long ctx = context_id();
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-        addr[dev] = p;
+    auto it = ctx ? addr.find(ctx) : addr.end();
+    if (it != addr.end()) {
+        *out = static_cast<char*>(it->second);
+        return MOE_OK;
     }
-    *out = static_cast<char*>(addr[dev]);
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    if (ctx) addr[ctx] = p;
+    *out = static_cast<char*>(p);
     return MOE_OK;
 }
 

@@ -253,14 +253,10 @@ template <int EPL>
 cudaError_t head_launch(int T, int E, int H, int splits, const float* part, const void* w2, const float* bias,
                         float* z, cudaStream_t s)
 {
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        const size_t most = static_cast<size_t>(kMaxRouterWeights2 + kMaxRouterHidden) * 4 +
-                            static_cast<size_t>(kHeadBlockTokens) * kMaxRouterHidden * 4;
-        attr_err = cudaFuncSetAttribute(router_head_kernel<EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(most));
-    });
+    const size_t most = static_cast<size_t>(kMaxRouterWeights2 + kMaxRouterHidden) * 4 +
+                        static_cast<size_t>(kHeadBlockTokens) * kMaxRouterHidden * 4;
+    const cudaError_t attr_err =
+        ensure_smem_limit(reinterpret_cast<const void*>(router_head_kernel<EPL>), static_cast<int>(most));
     if (attr_err != cudaSuccess) return attr_err;
     const int groups = (T + kHeadBlockTokens - 1) / kHeadBlockTokens;
     const int grid = std::min(groups, 2 * num_sms());

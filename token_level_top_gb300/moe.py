@@ -385,18 +385,18 @@ def timeout_probe(ws, budget_cycles: int):
 def dispatch_static(cfg: Config, scores, device="cuda"):
     """moe_dispatch_static: the dispatch with the library's fixed scratch array
     instead of a workspace (for callers that cannot allocate).  The output
-    tensors are allocated here by torch, as any caller's outputs would be."""
+    tensors are allocated here by torch, as any caller's outputs would be, and
+    filled with values the call must overwrite (-1, 0xFF, NaN)."""
     T, E, k = cfg.T, cfg.E, cfg.k
-    out = dict(assign=torch.empty(T, k, dtype=torch.int32, device=device),
-               slot=torch.empty(T, k, dtype=torch.int32, device=device),
-               flags=torch.empty(T, k, dtype=torch.uint8, device=device),
-               counts=torch.empty(E, dtype=torch.int32, device=device),
-               offsets=torch.empty(E + 1, dtype=torch.int32, device=device),
-               perm=torch.full((max(T * k, 1),), -1, dtype=torch.int32, device=device),
-               cw=torch.empty(T, k, dtype=torch.float32, device=device),
-               n_rerouted=torch.zeros(1, dtype=torch.int32, device=device),
-               n_dropped=torch.zeros(1, dtype=torch.int32, device=device),
-               status=torch.full((1,), -1, dtype=torch.int32, device=device))
+
+    def full(shape, v, dt):
+        return torch.full(shape, v, dtype=dt, device=device)
+
+    out = dict(assign=full((T, k), -1, torch.int32), slot=full((T, k), -1, torch.int32),
+               flags=full((T, k), 0xFF, torch.uint8), counts=full((E,), -1, torch.int32),
+               offsets=full((E + 1,), -1, torch.int32), perm=full((max(T * k, 1),), -1, torch.int32),
+               cw=full((T, k), float("nan"), torch.float32), n_rerouted=full((1,), -1, torch.int32),
+               n_dropped=full((1,), -1, torch.int32), status=full((1,), -1, torch.int32))
     c = cfg.c()
     st = lib().moe_dispatch_static(ctypes.byref(c), _p(scores), _p(out["assign"]), _p(out["slot"]),
                                    _p(out["flags"]), _p(out["counts"]), _p(out["offsets"]),

@@ -43,7 +43,7 @@ CLOCK_LEAD_S = 0.25  # untimed lead-in for clock samples when the timed region i
 CHUNK = 256  # tokens per routing chunk; a batch of one chunk routes and dispatches in one kernel
 
 
-BACKWARD_KERNELS = 8   # fill, pad, SwiGLU backward, router backward, dh, two widenings, bias sum
+BACKWARD_KERNELS = 12  # prep, pad, four GEMMs, SwiGLU backward, router backward, dh, dW_r (two), bias sum
 
 
 def kernels_per_step(T, fp8=False, norm=0, hidden=0):
@@ -541,18 +541,17 @@ def run_ours(args, rank, world, local):
     peak_tf = tensor_peak(peaks, peak_kind, ms_max * 1e-3, fp8)[0]
     bwd_line = None
     if bwd:
-        # the backward's GEMM work on the kept rows: g and u recomputed (2 d 2F), W2^T dout
-        # (2 d F), dx (2 2F d), dW2 (2 d F), dW13 (2 2F d) per row; the padded rows of each
-        # expert's block (E x C rows in all) are extra work the GEMMs also do
-        bflops = 16.0 * kept * d * F
+        # the backward's GEMM work on the kept rows: W2^T dout (2 d F), dx (2 2F d), dW2
+        # (2 d F), dW13 (2 2F d) per row (g and u are kept by the forward); each expert's
+        # rows are rounded up to the 128-row tile, which the GEMMs also compute
+        bflops = 12.0 * kept * d * F
         sec_b = stage_ms["backward"] * 1e-3
-        cap = moe.capacity(shape.T, shape.k, shape.E, shape.cf, shape.capacity)
-        rows_pad = shape.E * min(cap, shape.T)
+        rows_pad = int(sum((int(c) + 127) // 128 * 128 for c in counts.tolist()))
         bwd_line = {"stage_ms": stage_ms["backward"], "algorithmic_tflop": bflops / 1e12,
                     "achieved_tflops": bflops / sec_b / 1e12, "peak": peak_tf,
                     "frac": bflops / sec_b / 1e12 / peak_tf, "padded_rows": rows_pad, "kept_rows": kept,
-                    "gemms": "cuBLAS strided-batched (bf16 in, fp32 accumulate)",
-                    "kernels": "this library's: pad, SwiGLU backward, router backward, dh, bias sum"}
+                    "gemms": "this library's tcgen05 grouped GEMM (bf16 in, fp32 accumulate)",
+                    "kernels": "this library's: prep, pad, SwiGLU backward, router backward, dh, dW_r, bias sum"}
     value = world * T * args.steps / (ms_max * 1e-3)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -19,8 +19,9 @@
  *
  * Conventions for every entry point
  *   - Pointers named *_dev are DEVICE pointers owned by the caller; the
- *     library never allocates, frees or synchronises on the forward path
- *     (the lesson of the per-expert cudaMallocAsync leak on [cnnetsun] §5.2).
+ *     library never allocates or frees device memory, and never synchronises
+ *     on the forward or backward path (the lesson of the per-expert
+ *     cudaMallocAsync leak on [cnnetsun] §5.2).
  *     All scratch lives in the caller's workspace `ws` (size from
  *     moe_workspace_size, 256-byte aligned, initialised once with
  *     moe_workspace_init).
@@ -61,9 +62,9 @@ typedef enum {
  * maxima). */
 #define MOE_FLAG_FP8 1u
 /* moe_config_t.flags: size the workspace for moe_layer_backward too (adds
- * about E*C'*(8d + 10F) + T*k*8F + T*(4d + 4E + 4k) + 4E*d bytes, C' =
- * min(C, T)); moe_layer_forward then also keeps each kept row's g and u (fp32)
- * there for the backward. */
+ * about R*(8d + 10F) + T*k*(8F + 8) + 4T*E + 128*E*d bytes, R = min(E*C',
+ * T*k + 127E) with C' = min(C, T) rounded up to 128); moe_layer_forward then
+ * also keeps each kept row's g and u (fp32) there for the backward. */
 #define MOE_FLAG_BACKWARD 2u
 
 /* Layer shape.  Capacity C = ceil(T*k*cf/E) unless capacity > 0. */
@@ -335,9 +336,11 @@ moe_status_t moe_layer_forward_host(const moe_config_t* cfg, const void* h_host,
  * Outputs (fp32, overwritten): dh_dev [T, d]; dw_router_dev [E, d] and
  * dbias_dev [E] (each may be NULL); dw13_dev [E, 2F, d] in the packed W13
  * layout (moe_pack_w13); dw2_dev [E, d, F].
- * Each expert's kept rows are padded to C rows for strided-batched GEMMs;
- * those plain GEMMs run in cuBLAS (the first call on a device creates its
- * cuBLAS handle), the rest in this library's kernels.  Requires
+ * Each expert's kept rows are gathered into a row block padded with zero
+ * rows to a multiple of 128; the four per-expert products (W2^T dL/dout,
+ * dL/dx, dW2, dW13) run on this library's tcgen05 GEMM over those blocks and
+ * everything else in its other kernels (no library GEMM, no allocation).
+ * Requires
  * MOE_FLAG_BACKWARD (MOE_ERR_INVALID_ARG otherwise), router_norm = 0 and
  * router_hidden = 0 (MOE_ERR_UNSUPPORTED otherwise). */
 moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* h_dev, const void* w_router_dev,
@@ -375,7 +378,7 @@ moe_status_t moe_debug_timeout_probe(void* ws_dev, size_t ws_bytes, int64_t budg
  * exists for those callers only.
  *
  * Arguments and outputs are those of moe_dispatch (d_model and d_ff are not
- * used); status_dev (NULL or one int32 on the device) receives the device
+ * used; with T = 0 the per-token arrays may be NULL); status_dev (NULL or one int32 on the device) receives the device
  * status of this call (MOE_OK, or MOE_ERR_NONFINITE for a NaN score).
  * Scratch lives in one file-scope device array of MOE_STATIC_SCRATCH_BYTES,
  * held by every GPU that loads the library until the process exits.  Its

@@ -20,7 +20,8 @@ SRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libmoe.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "moe.h")
-UNITS = ["api.cu", "route.cu", "dispatch.cu", "gemm.cu", "misc.cu", "router.cu", "backward.cu", "noalloc.cu"]
+UNITS = ["api.cu", "route.cu", "dispatch.cu", "gemm.cu", "bwd_gemm.cu", "misc.cu", "router.cu", "backward.cu",
+         "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]
@@ -65,9 +66,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             list(ex.map(run, jobs))
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        # cuBLAS serves the backward pass's plain per-expert GEMMs
-        libdir = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc()))), "lib64")
-        run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcublas", "-Xlinker", f"-rpath={libdir}"])
+        run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs])
         os.replace(tmp, LIB)
     return LIB
 

@@ -62,11 +62,11 @@ int64_t capacity_of(const moe_config_t& c)
     return moe_capacity(c.T, c.k, c.E, c.cf, c.capacity);
 }
 
-// Rows of each expert's padded block in the backward pass: an expert holds at
-// most C slots, and at most one per token.
+// Rows of the backward pass's row blocks (each expert's kept rows rounded up to
+// 128): an expert holds at most C slots, and at most one per token.
 long long backward_rows(const moe_config_t& c)
 {
-    return std::min<long long>(capacity_of(c), std::max(c.T, 0));
+    return backward_block_rows(std::max(c.T, 0), c.E, c.k, capacity_of(c));
 }
 
 struct Ev {
@@ -866,7 +866,7 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* h, const vo
     a.k = c.k;
     a.d = c.d_model;
     a.F = c.d_ff;
-    a.C = backward_rows(c);
+    a.R = backward_rows(c);
     a.tau = c.tau;
     a.scores = ws_at<float>(ws, L.scores);
     a.perm = ws_at<int32_t>(ws, L.perm);
@@ -885,6 +885,8 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const void* h, const vo
     a.dw13 = dw13;
     a.dw2 = dw2;
     a.scratch = ws_at<void>(ws, L.bwd);
+    a.status = ws_at<int>(ws, L.status);
+    a.budget = kSpinBudget;
     return cuda_status(run_backward(a, s));
 }
 

@@ -11,15 +11,16 @@
 // §3.1 for the router's softmax and the load-balancing term written from the mean
 // probabilities, which enters as dL/dP).
 //
-// Layout: each expert's kept rows are copied into a zero-padded block of C rows (C the
-// capacity), so that every per-expert product is one strided-batched GEMM of E uniform
-// problems with no host synchronisation.  g and u are the ones the forward's gate-up epilogue
-// kept (fp32) when its workspace was sized for the backward.  Those plain GEMMs go to cuBLAS (bf16 inputs, fp32
-// accumulation); the gathers, the SwiGLU and softmax derivatives and the reductions are the
-// kernels below.
-#include <cublas_v2.h>
-
-#include <mutex>
+// Layout: each expert's kept rows are copied into a row block padded with zero rows to a
+// multiple of 128 (the GEMM tile height), the blocks back to back in expert order.  The four
+// per-expert products run on this library's tcgen05 GEMM (bwd_gemm.cu): the two input
+// gradients as ragged grouped GEMMs over the blocks' row tiles, the two weight gradients with
+// each expert's kept rows as the reduction dimension (64 rows per step; the zero rows fill the
+// last step).  g and u are the ones the forward's gate-up epilogue kept (fp32) when its
+// workspace was sized for the backward.  The gathers, the SwiGLU and softmax derivatives, the
+// router's two small fp32 products and the reductions are the kernels below.  Nothing is
+// padded beyond the tile; no library GEMM is called.
+#include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
@@ -27,20 +28,62 @@
 namespace moe {
 namespace {
 
-// One warp per padded row idx = e*C + j.  j < count_e: the kept slot s = offsets[e] + j of
-// entry t*k + r = perm[s] -- the token row and dL/dout row, its combine weight, and the
-// entry's padded row in map; else zeros.
-__global__ void bwd_pad_kernel(int E, long long C, int d8, int k, const int32_t* __restrict__ offsets,
-                               const int32_t* __restrict__ perm, const float* __restrict__ cw,
-                               const uint4* __restrict__ h, const uint4* __restrict__ dout,
-                               uint4* __restrict__ xp, uint4* __restrict__ dop, float* __restrict__ rcw,
-                               int32_t* __restrict__ rslot, int32_t* __restrict__ map)
+// One block: poff[e] = sum over e' < e of the kept rows of e' rounded up to 128 (the padded
+// row blocks), poff[E] their total; map and emap (per entry t*k + r: its padded row and its
+// expert) start as -1 (dropped entries keep it).
+__global__ void bwd_prep_kernel(int E, long long n_ent, const int32_t* __restrict__ offsets,
+                                int32_t* __restrict__ poff, int32_t* __restrict__ map, int32_t* __restrict__ emap)
+{
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int carry = 0;
+        for (int base = 0; base <= E; base += 32) {
+            const int e = base + lane;
+            const int rows = (e < E) ? (offsets[e + 1] - offsets[e] + kBM - 1) / kBM * kBM : 0;
+            int incl = rows;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            if (e <= E) poff[e] = carry + incl - rows;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+    for (long long i = threadIdx.x; i < n_ent; i += blockDim.x) {
+        map[i] = -1;
+        emap[i] = -1;
+    }
+}
+
+// The expert whose padded block holds row `row` (poff ascending, row < poff[E]).
+__device__ __forceinline__ int block_of(const int32_t* __restrict__ poff, int E, int row)
+{
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(poff + mid) <= row)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// One warp per padded row of the blocks.  Row j of expert e's block, j < count_e: the kept
+// slot s = offsets[e] + j of entry t*k + r = perm[s] -- the token row and the dL/dout row, its
+// combine weight, and the entry's row and expert in map / emap; j >= count_e: zeros.
+__global__ void bwd_pad_kernel(int E, long long R, int d8, int k, const int32_t* __restrict__ offsets,
+                               const int32_t* __restrict__ poff, const int32_t* __restrict__ perm,
+                               const float* __restrict__ cw, const uint4* __restrict__ h,
+                               const uint4* __restrict__ dout, uint4* __restrict__ xp, uint4* __restrict__ dop,
+                               float* __restrict__ rcw, int32_t* __restrict__ rslot, int32_t* __restrict__ map,
+                               int32_t* __restrict__ emap)
 {
     const long long idx = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (idx >= E * C) return;
-    const int e = static_cast<int>(idx / C);
-    const long long j = idx - e * C;
+    if (idx >= R || idx >= __ldg(poff + E)) return;
+    const int e = block_of(poff, E, static_cast<int>(idx));
+    const long long j = idx - __ldg(poff + e);
     const int off = offsets[e];
     const int cnt = offsets[e + 1] - off;
     uint4* xr = xp + idx * d8;
@@ -58,6 +101,7 @@ __global__ void bwd_pad_kernel(int E, long long C, int d8, int k, const int32_t*
             rcw[idx] = cw[ent];
             rslot[idx] = off + static_cast<int>(j);
             map[ent] = static_cast<int32_t>(idx);
+            emap[ent] = e;
         }
     } else {
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -72,32 +116,19 @@ __global__ void bwd_pad_kernel(int E, long long C, int d8, int k, const int32_t*
     }
 }
 
-__global__ void fill_i32_kernel(int32_t* p, long long n, int32_t v)
-{
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<long long>(gridDim.x) * blockDim.x)
-        p[i] = v;
-}
-
-__global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ a, float* __restrict__ b, long long n)
-{
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<long long>(gridDim.x) * blockDim.x)
-        b[i] = __bfloat162float(a[i]);
-}
-
 __device__ __forceinline__ uint2 pack4_bf16(float a, float b, float c, float d)
 {
     return make_uint2(pack_bf16x2(a, b), pack_bf16x2(c, d));
 }
 
-// One block per padded row.  gu [T*k, 2F] holds the forward's g and u of each kept slot (bf16,
-// packed W13 column order: block q of 256 columns has g of F-columns [128q, 128q+128), then
-// their u); rslot gives the padded row's slot (-1: padding, g = u = 0).  dap [rows, F] =
-// W2^T dout (bf16, before the combine weight).  Writes acw = cw * a (bf16, for dW2), dgu =
+// One block per padded row (rows past the blocks' total exit).  gu [T*k, 2F] holds the
+// forward's g and u of each kept slot (fp32, packed W13 column order: block q of 256 columns
+// has g of F-columns [128q, 128q+128), then their u); rslot gives the padded row's slot (-1:
+// padding, g = u = 0).  dap [rows, F] = W2^T dout (fp32, before the combine weight).  Writes acw = cw * a (bf16, for dW2), dgu =
 // (dg, du) in the packed order (bf16, for dx and dW13), and the row's dcw = sum_f dap_f a_f
 // = dout . y.
-__global__ void __launch_bounds__(256) swiglu_bwd_kernel(int F, const float* __restrict__ gu,
+__global__ void __launch_bounds__(256) swiglu_bwd_kernel(int F, int E, const int32_t* __restrict__ poff,
+                                                         const float* __restrict__ gu,
                                                          const int32_t* __restrict__ rslot,
                                                          const float* __restrict__ dap,
                                                          const float* __restrict__ rcw,
@@ -107,6 +138,7 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(int F, const float* __r
 {
     __shared__ float s_red[8];
     const long long row = blockIdx.x;
+    if (row >= __ldg(poff + E)) return;
     const float c = rcw[row];
     const int slot = rslot[row];
     const float* gr = gu + static_cast<long long>(slot < 0 ? 0 : slot) * 2 * F;
@@ -151,12 +183,13 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(int F, const float* __r
 }
 
 // One warp per token: p = softmax(s) (the forward's penalised scores), the kept ranks from
-// map, cw_r = p_{e_r} / S, dp_e = dP_e / T + (dcw_r - sum_r' dcw_r' cw_r') / S on the kept
+// map (padded row) and emap (expert), cw_r = p_{e_r} / S, dp_e = dP_e / T + (dcw_r - sum_r' dcw_r' cw_r') / S on the kept
 // experts, ds = p (dp - p . dp), dz = ds / tau.
 template <int EPL>
-__global__ void router_bwd_kernel(int T, int E, int k, long long C, float tau, const float* __restrict__ scores,
-                                  const int32_t* __restrict__ map, const float* __restrict__ dcw_row,
-                                  const float* __restrict__ dP, float* __restrict__ dz)
+__global__ void router_bwd_kernel(int T, int E, int k, float tau, const float* __restrict__ scores,
+                                  const int32_t* __restrict__ map, const int32_t* __restrict__ emap,
+                                  const float* __restrict__ dcw_row, const float* __restrict__ dP,
+                                  float* __restrict__ dz)
 {
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -197,12 +230,12 @@ __global__ void router_bwd_kernel(int T, int E, int k, long long C, float tau, c
     for (int r = 0; r < k; ++r) {
         const int idx = map[static_cast<size_t>(t) * k + r];   // the same in every lane
         if (idx < 0) continue;
-        S += prob_of(static_cast<int>(idx / C));
+        S += prob_of(emap[static_cast<size_t>(t) * k + r]);
     }
     for (int r = 0; r < k; ++r) {
         const int idx = map[static_cast<size_t>(t) * k + r];
         if (idx < 0) continue;
-        mdot += dcw_row[idx] * (prob_of(static_cast<int>(idx / C)) / S);
+        mdot += dcw_row[idx] * (prob_of(emap[static_cast<size_t>(t) * k + r]) / S);
     }
     float dp[EPL];
 #pragma unroll
@@ -213,7 +246,7 @@ __global__ void router_bwd_kernel(int T, int E, int k, long long C, float tau, c
     for (int r = 0; r < k; ++r) {
         const int idx = map[static_cast<size_t>(t) * k + r];
         if (idx < 0) continue;
-        const int e = static_cast<int>(idx / C);
+        const int e = emap[static_cast<size_t>(t) * k + r];
         if ((e & 31) == lane) {
 #pragma unroll
             for (int q = 0; q < EPL; ++q)
@@ -233,27 +266,113 @@ __global__ void router_bwd_kernel(int T, int E, int k, long long C, float tau, c
     }
 }
 
-// dh[t] = sum over t's kept ranks, in rank order, of dx of that entry's padded row (fp32).
-__global__ void bwd_dh_kernel(int T, int d, int k, const int32_t* __restrict__ map,
-                              const float4* __restrict__ dx, float4* __restrict__ dh)
+// dh[t] = (sum over t's kept ranks, in rank order, of dx of that entry's padded row)
+//         + sum_e dz[t, e] W_r[e] (expert order), fp32.  A block: kDhTokens tokens x 1024
+// columns, each thread 4 columns of every token; dz of the block's tokens staged in shared
+// memory, each W_r element read once per block.
+constexpr int kDhTokens = 8;
+__global__ void __launch_bounds__(256) bwd_dh_kernel(int T, int d, int E, int k, const int32_t* __restrict__ map,
+                                                     const float4* __restrict__ dx, const float* __restrict__ dz,
+                                                     const __nv_bfloat16* __restrict__ wr, float4* __restrict__ dh)
 {
+    extern __shared__ float s_dz[];   // [kDhTokens][E]
+    const int t0 = blockIdx.x * kDhTokens;
+    const int nt = min(kDhTokens, T - t0);
+    for (int i = threadIdx.x; i < kDhTokens * E; i += blockDim.x) {
+        const int tt = i / E;
+        s_dz[i] = tt < nt ? dz[static_cast<size_t>(t0 + tt) * E + (i - tt * E)] : 0.0f;
+    }
+    __syncthreads();
+    const int c4 = blockIdx.y * blockDim.x + threadIdx.x;   // float4 column
+    if (4 * c4 >= d) return;
+    float4 acc[kDhTokens];
+#pragma unroll
+    for (int tt = 0; tt < kDhTokens; ++tt) acc[tt] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int e = 0; e < E; ++e) {
+        const uint2 w2 = __ldg(reinterpret_cast<const uint2*>(wr + static_cast<size_t>(e) * d) + c4);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2.y));
+#pragma unroll
+        for (int tt = 0; tt < kDhTokens; ++tt) {
+            const float z = s_dz[tt * E + e];
+            acc[tt].x = fmaf(z, a.x, acc[tt].x);
+            acc[tt].y = fmaf(z, a.y, acc[tt].y);
+            acc[tt].z = fmaf(z, b.x, acc[tt].z);
+            acc[tt].w = fmaf(z, b.y, acc[tt].w);
+        }
+    }
     const int d4 = d / 4;
-    const long long n = static_cast<long long>(T) * d4;
+    for (int tt = 0; tt < nt; ++tt) {
+        const long long t = t0 + tt;
+        float4 r = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int q = 0; q < k; ++q) {
+            const int idx = map[t * k + q];
+            if (idx < 0) continue;
+            const float4 v = dx[static_cast<long long>(idx) * d4 + c4];
+            r.x += v.x;
+            r.y += v.y;
+            r.z += v.z;
+            r.w += v.w;
+        }
+        r.x += acc[tt].x;
+        r.y += acc[tt].y;
+        r.z += acc[tt].z;
+        r.w += acc[tt].w;
+        dh[t * d4 + c4] = r;
+    }
+}
+
+// dW_r = dz^T h in two passes.  Pass 1: block (column block of 256, expert group of kWrE,
+// token slice) -> part[slice][e][col] = sum over the slice's tokens, in token order, of
+// dz[t, e] h[t, col].  Pass 2 sums the slices in order.
+constexpr int kWrE = 16;
+constexpr int kWrChunk = 64;
+__global__ void __launch_bounds__(128) bwd_wr_part_kernel(int T, int d, int E, int slice,
+                                                          const float* __restrict__ dz,
+                                                          const __nv_bfloat16* __restrict__ h,
+                                                          float* __restrict__ part)
+{
+    __shared__ float s_z[kWrChunk][kWrE];
+    const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 2;
+    const int e0 = blockIdx.y * kWrE;
+    const int ne = min(kWrE, E - e0);
+    const int ta = blockIdx.z * slice, tb = min(T, ta + slice);
+    float acc[kWrE][2];
+#pragma unroll
+    for (int q = 0; q < kWrE; ++q) acc[q][0] = acc[q][1] = 0.0f;
+    for (int c0 = ta; c0 < tb; c0 += kWrChunk) {
+        const int n = min(kWrChunk, tb - c0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < kWrChunk * kWrE; i += blockDim.x) {
+            const int tt = i / kWrE, q = i - tt * kWrE;
+            s_z[tt][q] = (tt < n && q < ne) ? dz[static_cast<size_t>(c0 + tt) * E + e0 + q] : 0.0f;
+        }
+        __syncthreads();
+        if (col < d) {
+            for (int tt = 0; tt < n; ++tt) {
+                const float2 hv =
+                    __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(h + static_cast<size_t>(c0 + tt) * d + col));
+#pragma unroll
+                for (int q = 0; q < kWrE; ++q) {
+                    acc[q][0] = fmaf(s_z[tt][q], hv.x, acc[q][0]);
+                    acc[q][1] = fmaf(s_z[tt][q], hv.y, acc[q][1]);
+                }
+            }
+        }
+    }
+    if (col >= d) return;
+    for (int q = 0; q < ne; ++q)
+        *reinterpret_cast<float2*>(part + (static_cast<size_t>(blockIdx.z) * E + e0 + q) * d + col) =
+            make_float2(acc[q][0], acc[q][1]);
+}
+
+__global__ void bwd_wr_sum_kernel(long long n, int slices, const float* __restrict__ part, float* __restrict__ out)
+{
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const long long t = i / d4;
-        const int c = static_cast<int>(i - t * d4);
-        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        for (int r = 0; r < k; ++r) {
-            const int idx = map[t * k + r];
-            if (idx < 0) continue;
-            const float4 v = dx[static_cast<long long>(idx) * d4 + c];
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-        }
-        dh[i] = acc;
+        float v = 0.0f;
+        for (int z = 0; z < slices; ++z) v += part[static_cast<size_t>(z) * n + i];
+        out[i] = v;
     }
 }
 
@@ -275,30 +394,6 @@ __global__ void col_sum_kernel(int T, int E, const float* __restrict__ dz, float
     }
 }
 
-cublasHandle_t blas_handle()
-{
-    static std::mutex mu;
-    static cublasHandle_t handles[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!handles[dev] && cublasCreate(&handles[dev]) != CUBLAS_STATUS_SUCCESS) handles[dev] = nullptr;
-    return handles[dev];
-}
-
-// Row-major C[b] (M x N, ldc) = op(A[b]) (M x K) . op(B[b]) (K x N) + beta C[b], for b < batch.
-// ta: A is stored K x M (else M x K); tb: B is stored N x K (else K x N).  As column-major
-// cuBLAS sees it, C^T = op(B)^T op(A)^T.
-bool gemm_rm(cublasHandle_t hd, bool ta, bool tb, int M, int N, int K, const void* A, cudaDataType at,
-             int lda, long long sA, const void* B, cudaDataType bt, int ldb, long long sB, void* C,
-             cudaDataType ct, int ldc, long long sC, int batch, float beta)
-{
-    const float alpha = 1.0f;
-    return cublasGemmStridedBatchedEx(hd, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, N, M, K,
-                                      &alpha, B, bt, ldb, sB, A, at, lda, sA, &beta, C, ct, ldc, sC, batch,
-                                      CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
-}
-
 int grid_of(long long n, int threads)
 {
     const long long want = (n + threads - 1) / threads;
@@ -308,94 +403,120 @@ int grid_of(long long n, int threads)
 
 }  // namespace
 
-size_t backward_bytes(long long T, int d, int E, int k, int F, long long C)
+int wr_slices(long long T) { return static_cast<int>(std::max<long long>(1, std::min<long long>(32, (T + 127) / 128))); }
+
+long long backward_block_rows(long long T, int E, int k, long long C)
 {
-    const size_t EC = static_cast<size_t>(E) * static_cast<size_t>(C);
+    const long long per = (std::min(C, T) + kBM - 1) / kBM * kBM;
+    return std::max<long long>(kBM, std::min(static_cast<long long>(E) * per, T * k + static_cast<long long>(kBM - 1) * E));
+}
+
+size_t backward_bytes(long long T, int d, int E, int k, int F, long long R)
+{
     const size_t per_row = static_cast<size_t>(d) * 2 * 2 + static_cast<size_t>(F) * 4 +
                            static_cast<size_t>(F) * 2 + static_cast<size_t>(F) * 2 * 2 +
                            static_cast<size_t>(d) * 4 + 12;
-    return EC * per_row + static_cast<size_t>(T) * k * 4 + static_cast<size_t>(T) * E * 4 +
-           static_cast<size_t>(T) * d * 4 + static_cast<size_t>(E) * d * 4 + 16 * 256;
+    return static_cast<size_t>(R) * per_row + static_cast<size_t>(T) * k * 8 + static_cast<size_t>(T) * E * 4 +
+           static_cast<size_t>(wr_slices(T)) * E * d * 4 + static_cast<size_t>(E + 1) * 4 + 16 * 256;
 }
 
 cudaError_t run_backward(const BackwardArgs& a, cudaStream_t s)
 {
     const int E = a.E, k = a.k, d = a.d, F = a.F, T = a.T;
-    const long long C = a.C, EC = static_cast<long long>(E) * C;
-    cublasHandle_t hd = blas_handle();
-    if (!hd) return cudaErrorInitializationError;
-    if (cublasSetStream(hd, s) != CUBLAS_STATUS_SUCCESS) return cudaErrorInvalidValue;
-    // carve the scratch (16-byte aligned regions)
+    const long long R = a.R;
+    // carve the scratch (256-byte aligned regions)
     char* p = static_cast<char*>(a.scratch);
     auto take = [&](size_t bytes) {
         char* o = p;
         p += (bytes + 255) / 256 * 256;
         return o;
     };
-    auto* xp = reinterpret_cast<__nv_bfloat16*>(take(EC * d * 2));
-    auto* dop = reinterpret_cast<__nv_bfloat16*>(take(EC * d * 2));
-    auto* dap = reinterpret_cast<float*>(take(EC * F * 4));
-    auto* acw = reinterpret_cast<__nv_bfloat16*>(take(EC * F * 2));
-    auto* dgu = reinterpret_cast<__nv_bfloat16*>(take(EC * 2 * F * 2));
-    auto* dx = reinterpret_cast<float*>(take(EC * d * 4));
-    auto* rcw = reinterpret_cast<float*>(take(EC * 4));
-    auto* dcw = reinterpret_cast<float*>(take(EC * 4));
-    auto* rslot = reinterpret_cast<int32_t*>(take(EC * 4));
+    auto* poff = reinterpret_cast<int32_t*>(take(static_cast<size_t>(E + 1) * 4));
+    auto* xp = reinterpret_cast<__nv_bfloat16*>(take(R * d * 2));
+    auto* dop = reinterpret_cast<__nv_bfloat16*>(take(R * d * 2));
+    auto* dap = reinterpret_cast<float*>(take(R * F * 4));
+    auto* acw = reinterpret_cast<__nv_bfloat16*>(take(R * F * 2));
+    auto* dgu = reinterpret_cast<__nv_bfloat16*>(take(R * 2 * F * 2));
+    auto* dx = reinterpret_cast<float*>(take(R * d * 4));
+    auto* rcw = reinterpret_cast<float*>(take(R * 4));
+    auto* dcw = reinterpret_cast<float*>(take(R * 4));
+    auto* rslot = reinterpret_cast<int32_t*>(take(R * 4));
     auto* map = reinterpret_cast<int32_t*>(take(static_cast<size_t>(T) * k * 4));
+    auto* emap = reinterpret_cast<int32_t*>(take(static_cast<size_t>(T) * k * 4));
     auto* dz = reinterpret_cast<float*>(take(static_cast<size_t>(T) * E * 4));
-    auto* h32 = reinterpret_cast<float*>(take(static_cast<size_t>(T) * d * 4));
-    auto* wr32 = reinterpret_cast<float*>(take(static_cast<size_t>(E) * d * 4));
+    const int slices = wr_slices(T);
+    auto* wr_part = reinterpret_cast<float*>(take(static_cast<size_t>(slices) * E * d * 4));
 
-    fill_i32_kernel<<<grid_of(static_cast<long long>(T) * k, 256), 256, 0, s>>>(map, static_cast<long long>(T) * k,
-                                                                                 -1);
-    bwd_pad_kernel<<<static_cast<unsigned>((EC + 7) / 8), 256, 0, s>>>(
-        E, C, d / 8, k, a.offsets, a.perm, a.cw, static_cast<const uint4*>(a.h), static_cast<const uint4*>(a.dout),
-        reinterpret_cast<uint4*>(xp), reinterpret_cast<uint4*>(dop), rcw, rslot, map);
-    if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
-    const cudaDataType BF = CUDA_R_16BF, F32 = CUDA_R_32F;
-    const long long W13 = 2LL * F * d, W2s = static_cast<long long>(d) * F;
-    // dap = dout rows . W2_e  ([C, d] . [d, F]); g and u come from the forward
-    if (!gemm_rm(hd, false, false, static_cast<int>(C), F, d, dop, BF, d, C * d, a.w2, BF, F, W2s, dap, F32, F,
-                 C * F, E, 0.0f))
-        return cudaErrorUnknown;
-    swiglu_bwd_kernel<<<static_cast<unsigned>(EC), 256, 0, s>>>(F, a.gu, rslot, dap, rcw, acw, dgu, dcw);
-    if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
-    // dx = (dg, du) . W13_e  ([C, 2F] . [2F, d])
-    if (!gemm_rm(hd, false, false, static_cast<int>(C), d, 2 * F, dgu, BF, 2 * F, C * 2 * F, a.w13, BF, d, W13, dx,
-                 F32, d, C * d, E, 0.0f))
-        return cudaErrorUnknown;
-    // dW2_e = dout_e^T (cw a)_e  ([d, C] . [C, F]);  dW13_e = (dg, du)_e^T x_e  ([2F, C] . [C, d])
-    if (!gemm_rm(hd, true, false, d, F, static_cast<int>(C), dop, BF, d, C * d, acw, BF, F, C * F, a.dw2, F32, F,
-                 W2s, E, 0.0f))
-        return cudaErrorUnknown;
-    if (!gemm_rm(hd, true, false, 2 * F, d, static_cast<int>(C), dgu, BF, 2 * F, C * 2 * F, xp, BF, d, C * d, a.dw13,
-                 F32, d, W13, E, 0.0f))
-        return cudaErrorUnknown;
+    bwd_prep_kernel<<<1, 1024, 0, s>>>(E, static_cast<long long>(T) * k, a.offsets, poff, map, emap);
+    bwd_pad_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, s>>>(
+        E, R, d / 8, k, a.offsets, poff, a.perm, a.cw, static_cast<const uint4*>(a.h),
+        static_cast<const uint4*>(a.dout), reinterpret_cast<uint4*>(xp), reinterpret_cast<uint4*>(dop), rcw, rslot,
+        map, emap);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+
+    BwdGemmLaunch g{};
+    g.E = E;
+    g.rows = R;
+    g.offsets = a.offsets;
+    g.status = a.status;
+    g.budget = a.budget;
+    // dL/da before the combine weight: dap = dL/dout rows . W2_e  ([rows, d] . [d, F])
+    g.mode = BG_DGRAD;
+    g.K = d;
+    g.N = F;
+    g.a = dop;
+    g.b = a.w2;
+    g.out = dap;
+    if ((err = launch_bwd_gemm(g, s)) != cudaSuccess) return err;
+    swiglu_bwd_kernel<<<static_cast<unsigned>(R), 256, 0, s>>>(F, E, poff, a.gu, rslot, dap, rcw, acw, dgu, dcw);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    // dx = (dg, du) . W13_e  ([rows, 2F] . [2F, d])
+    g.K = 2 * F;
+    g.N = d;
+    g.a = dgu;
+    g.b = a.w13;
+    g.out = dx;
+    if ((err = launch_bwd_gemm(g, s)) != cudaSuccess) return err;
+    // dW2_e = dL/dout_e^T (cw a)_e  ([d, rows] . [rows, F]);  dW13_e = (dg, du)_e^T x_e  ([2F, rows] . [rows, d])
+    g.mode = BG_WGRAD;
+    g.K = 0;
+    g.Mw = d;
+    g.N = F;
+    g.a = dop;
+    g.b = acw;
+    g.out = a.dw2;
+    if ((err = launch_bwd_gemm(g, s)) != cudaSuccess) return err;
+    g.Mw = 2 * F;
+    g.N = d;
+    g.a = dgu;
+    g.b = xp;
+    g.out = a.dw13;
+    if ((err = launch_bwd_gemm(g, s)) != cudaSuccess) return err;
     // the router
     const int warps = 8;
     const unsigned rgrid = static_cast<unsigned>((T + warps - 1) / warps);
     if (E <= 32)
-        router_bwd_kernel<1><<<rgrid, 32 * warps, 0, s>>>(T, E, k, C, a.tau, a.scores, map, dcw, a.dP, dz);
+        router_bwd_kernel<1><<<rgrid, 32 * warps, 0, s>>>(T, E, k, a.tau, a.scores, map, emap, dcw, a.dP, dz);
     else if (E <= 64)
-        router_bwd_kernel<2><<<rgrid, 32 * warps, 0, s>>>(T, E, k, C, a.tau, a.scores, map, dcw, a.dP, dz);
+        router_bwd_kernel<2><<<rgrid, 32 * warps, 0, s>>>(T, E, k, a.tau, a.scores, map, emap, dcw, a.dP, dz);
     else if (E <= 128)
-        router_bwd_kernel<4><<<rgrid, 32 * warps, 0, s>>>(T, E, k, C, a.tau, a.scores, map, dcw, a.dP, dz);
+        router_bwd_kernel<4><<<rgrid, 32 * warps, 0, s>>>(T, E, k, a.tau, a.scores, map, emap, dcw, a.dP, dz);
     else
-        router_bwd_kernel<8><<<rgrid, 32 * warps, 0, s>>>(T, E, k, C, a.tau, a.scores, map, dcw, a.dP, dz);
-    bwd_dh_kernel<<<grid_of(static_cast<long long>(T) * d / 4, 256), 256, 0, s>>>(
-        T, d, k, map, reinterpret_cast<const float4*>(dx), reinterpret_cast<float4*>(a.dh));
-    bf16_to_f32_kernel<<<grid_of(static_cast<long long>(E) * d, 256), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(a.w_router), wr32, static_cast<long long>(E) * d);
-    if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
-    // dh += dz . W_r  ([T, E] . [E, d])
-    if (!gemm_rm(hd, false, false, T, d, E, dz, F32, E, 0, wr32, F32, d, 0, a.dh, F32, d, 0, 1, 1.0f))
-        return cudaErrorUnknown;
-    if (a.dw_router) {
-        bf16_to_f32_kernel<<<grid_of(static_cast<long long>(T) * d, 256), 256, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(a.h), h32, static_cast<long long>(T) * d);
-        // dW_r = dz^T h  ([E, T] . [T, d])
-        if (!gemm_rm(hd, true, false, E, d, T, dz, F32, E, 0, h32, F32, d, 0, a.dw_router, F32, d, 0, 1, 0.0f))
-            return cudaErrorUnknown;
+        router_bwd_kernel<8><<<rgrid, 32 * warps, 0, s>>>(T, E, k, a.tau, a.scores, map, emap, dcw, a.dP, dz);
+    // dh = the experts' dx rows + dz . W_r
+    const dim3 dgrid(static_cast<unsigned>((T + kDhTokens - 1) / kDhTokens), static_cast<unsigned>((d / 4 + 255) / 256));
+    bwd_dh_kernel<<<dgrid, 256, static_cast<size_t>(kDhTokens) * E * 4, s>>>(
+        T, d, E, k, map, reinterpret_cast<const float4*>(dx), dz, static_cast<const __nv_bfloat16*>(a.w_router),
+        reinterpret_cast<float4*>(a.dh));
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (a.dw_router) {   // dW_r = dz^T h  ([E, T] . [T, d])
+        const int slice = (T + slices - 1) / slices;
+        const dim3 wgrid(static_cast<unsigned>((d / 2 + 127) / 128), static_cast<unsigned>((E + kWrE - 1) / kWrE),
+                         static_cast<unsigned>(slices));
+        bwd_wr_part_kernel<<<wgrid, 128, 0, s>>>(T, d, E, slice, dz, static_cast<const __nv_bfloat16*>(a.h), wr_part);
+        const long long n = static_cast<long long>(E) * d;
+        bwd_wr_sum_kernel<<<grid_of(n, 256), 256, 0, s>>>(n, slices, wr_part, a.dw_router);
     }
     if (a.dbias) col_sum_kernel<<<E, 256, 0, s>>>(T, E, dz, a.dbias);
     return cudaGetLastError();

@@ -537,6 +537,15 @@ bool make_map_e4m3(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t col
     return r == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+bool encode_bf16_map(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows)
+{
+    return make_map(tm, ptr, rows, cols, box_rows);
+}
+
+namespace {
+
 uint32_t pow2_cols(int n)
 {
     uint32_t c = 32;

@@ -1,6 +1,7 @@
 // internal.h -- declarations shared by the libmoe translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -150,6 +151,27 @@ struct GemmLaunch {
     long long budget;
 };
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
+// Tensor map of a row-major bf16 matrix [rows, cols]: boxes of box_rows x 64
+// columns (128 bytes), 128-byte swizzle; zero fill outside the matrix.
+bool encode_bf16_map(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
+// The backward pass's per-expert products (bwd_gemm.cu) over row blocks that
+// hold each expert's kept rows padded with zero rows to a multiple of 128.
+enum BwdGemmMode : int { BG_DGRAD = 0, BG_WGRAD = 1 };
+struct BwdGemmLaunch {
+    int mode, E;
+    long long rows;        // rows of the row-block buffers (room for every expert's padded block)
+    int K;                 // BG_DGRAD: inner dimension (the row block's width, the weights' rows per expert)
+    int N;                 // output columns
+    int Mw;                // BG_WGRAD: output rows per expert (the A row block's width)
+    const void* a;         // BG_DGRAD: row block [rows, K]; BG_WGRAD: row block [rows, Mw]
+    const void* b;         // BG_DGRAD: weights [E*K, N]; BG_WGRAD: row block [rows, N]
+    const int32_t* offsets;  // [E + 1] kept slots per expert (the padded blocks follow from them)
+    float* out;            // BG_DGRAD: [rows, N]; BG_WGRAD: [E, Mw, N]
+    int* status;
+    long long budget;
+};
+cudaError_t launch_bwd_gemm(const BwdGemmLaunch& g, cudaStream_t s);
 
 cudaError_t launch_pack_w13(int E, int F, int d, const void* w1, const void* w3, void* w13,
                             cudaStream_t s);
@@ -184,7 +206,7 @@ cudaError_t launch_router_sum(int T, int E, int splits, const float* part, const
 // offsets, cw) and writes the gradients; scratch holds backward_bytes(...) bytes.
 struct BackwardArgs {
     int T, E, k, d, F;
-    long long C;             // capacity: the rows of each expert's padded block
+    long long R;             // rows of the row blocks: room for every expert's kept rows rounded up to 128
     float tau;               // 0 or 1: none
     const float* scores;     // [T, E] the forward's penalised scores
     const int32_t* perm;     // kept slots in slot order: t*k + r
@@ -203,8 +225,12 @@ struct BackwardArgs {
     float* dw13;             // [E, 2F, d]
     float* dw2;              // [E, d, F]
     void* scratch;
+    int* status;             // device status word
+    long long budget;        // bounded waits
 };
-size_t backward_bytes(long long T, int d, int E, int k, int F, long long C);
+size_t backward_bytes(long long T, int d, int E, int k, int F, long long R);
+// R for backward_bytes: at most sum over experts of (kept rows rounded up to 128).
+long long backward_block_rows(long long T, int E, int k, long long C);
 cudaError_t run_backward(const BackwardArgs& a, cudaStream_t s);
 
 cudaError_t launch_timeout_probe(int* status, long long budget, cudaStream_t s);

@@ -108,8 +108,9 @@ extern "C" moe_status_t moe_dispatch_static(const moe_config_t* cfg, const float
         return MOE_ERR_INVALID_ARG;
     if (cfg->capacity == 0 && !(cfg->cf > 0.0 && cfg->cf <= 100.0)) return MOE_ERR_INVALID_ARG;
     if (cfg->E > 255 || cfg->k > 8) return MOE_ERR_UNSUPPORTED;
-    if (!scores || !assign || !slot || !flags || !counts || !offsets || !perm || !combine_w ||
-        !n_rerouted || !n_dropped)
+    // the per-token arrays may be NULL when there are no tokens
+    if (!counts || !offsets || !n_rerouted || !n_dropped ||
+        (cfg->T > 0 && (!scores || !assign || !slot || !flags || !perm || !combine_w)))
         return MOE_ERR_INVALID_ARG;
     const StaticLayout L = static_layout(*cfg);
     if (L.total > kStaticScratchBytes) return MOE_ERR_UNSUPPORTED;  // batch too large for the array

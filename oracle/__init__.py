@@ -80,6 +80,16 @@ def _load():
             lib.oracle_e4m3_encode.restype = ctypes.c_uint8
             lib.oracle_quantize_row.argtypes = [I, P, P, P]
             lib.oracle_quantize_row.restype = None
+            lib.oracle_e2m1_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e2m1_value.restype = ctypes.c_double
+            lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+            lib.oracle_quantize_row_nvfp4.argtypes = [I, P, P, P, P]
+            lib.oracle_quantize_row_nvfp4.restype = None
+            lib.oracle_combine_rows_q4.argtypes = [I, I, I, I, I] + [P] * 10 + [I] + [P] * 3 + [I, P]
+            lib.oracle_combine_rows_q4.restype = I
+            lib.oracle_expert_slots_q4.argtypes = [I, I, I, I, I] + [P] * 10 + [I, P, P, I, I, P]
+            lib.oracle_expert_slots_q4.restype = I
             _lib = lib
     return _lib
 
@@ -336,4 +346,70 @@ def layer_backward(h, wr, w1, w3, w2, scores, assign, dout, tau=1.0, dP=None):
                                    _ptr(out["dw2"]))
     if st:
         raise OracleError(st, "layer_backward")
+    return out
+
+
+def e2m1_value(code: int) -> float:
+    """Value of a 4-bit e2m1 code (sign, 2-bit exponent bias 1, 1-bit mantissa)."""
+    return float(_load().oracle_e2m1_value(int(code) & 0xF))
+
+
+def e2m1_encode(v: float) -> int:
+    """The e2m1 code nearest to v (ties to the even code), saturating at +-6."""
+    return int(_load().oracle_e2m1_encode(float(v)))
+
+
+def quantize_row_nvfp4(x):
+    """NVFP4 row quantisation: (codes uint8 [n/2] packed, element 2m in the low
+    nibble; e4m3 block scales uint8 [n/16]; fp32 row scale)."""
+    x = _c(x, np.float32)
+    n = x.shape[0]
+    codes = np.empty(n // 2, np.uint8)
+    bs = np.empty(n // 16, np.uint8)
+    sc = np.empty(1, np.float32)
+    _load().oracle_quantize_row_nvfp4(n, _ptr(x), _ptr(codes), _ptr(bs), _ptr(sc))
+    return codes, bs, float(sc[0])
+
+
+def _q4(w):
+    """(codes, block scales, row scales) of the three weight matrices, contiguous."""
+    return [(_c(q, np.uint8), _c(b, np.uint8), _c(sc, np.float32)) for q, b, sc in w]
+
+
+def combine_rows_q4(h, w1, w3, w2, assign, cw, tokens, quant_act=True) -> np.ndarray:
+    """combine_rows with NVFP4 expert weights.  w1, w3: (codes [E,F,d/2], block
+    scales [E,F,d/16], row scales [E,F]); w2: (codes [E,d,F/2], [E,d,F/16], [E,d]).
+    quant_act: token and activation rows NVFP4-quantised per row as well."""
+    h = _c(h, np.uint16)
+    (q1, b1, s1), (q3, b3, s3), (q2, b2, s2) = _q4((w1, w3, w2))
+    assign = _c(assign, np.int32)
+    cw = _c(cw, np.float32)
+    tokens = _c(tokens, np.int32)
+    T, d = h.shape
+    E, F = s1.shape
+    k = assign.shape[1]
+    out = np.empty((tokens.shape[0], d), np.float32)
+    st = _load().oracle_combine_rows_q4(T, d, E, k, F, _ptr(h), _ptr(q1), _ptr(b1), _ptr(s1), _ptr(q3),
+                                        _ptr(b3), _ptr(s3), _ptr(q2), _ptr(b2), _ptr(s2), int(quant_act),
+                                        _ptr(assign), _ptr(cw), _ptr(tokens), tokens.shape[0], _ptr(out))
+    if st:
+        raise OracleError(st, "combine_rows_q4")
+    return out
+
+
+def expert_slots_q4(h, w1, w3, w2, assign, perm, row0: int, row1: int, quant_act=True) -> np.ndarray:
+    """expert_slots with NVFP4 expert weights (layouts and quant_act as combine_rows_q4)."""
+    h = _c(h, np.uint16)
+    (q1, b1, s1), (q3, b3, s3), (q2, b2, s2) = _q4((w1, w3, w2))
+    assign = _c(assign, np.int32)
+    perm = _c(perm, np.int32)
+    T, d = h.shape
+    E, F = s1.shape
+    k = assign.shape[1]
+    out = np.empty((row1 - row0, d), np.float32)
+    st = _load().oracle_expert_slots_q4(T, d, E, k, F, _ptr(h), _ptr(q1), _ptr(b1), _ptr(s1), _ptr(q3),
+                                        _ptr(b3), _ptr(s3), _ptr(q2), _ptr(b2), _ptr(s2), int(quant_act),
+                                        _ptr(assign), _ptr(perm), row0, row1, _ptr(out))
+    if st:
+        raise OracleError(st, "expert_slots_q4")
     return out

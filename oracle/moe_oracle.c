@@ -89,6 +89,56 @@ void oracle_quantize_row(int n, const float* x, uint8_t* codes, float* scale)
     *scale = s;
 }
 
+/* e2m1: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0; exponent 0
+ * is the subnormal 0.5 * m. */
+double oracle_e2m1_value(uint8_t code)
+{
+    const int sign = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    const double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+/* Nearest e2m1 code by the distance to each of the eight magnitudes, ties to
+ * the code whose mantissa bit is 0; beyond 6 the largest magnitude. */
+uint8_t oracle_e2m1_encode(float v)
+{
+    if (isnan(v)) return 0;
+    const uint8_t sign = signbit(v) ? 8 : 0;
+    const double a = fabs((double)v);
+    int best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c < 8; ++c) {
+        const double dd = fabs(a - oracle_e2m1_value((uint8_t)c));
+        if (dd < bd || (dd == bd && (c & 1) == 0 && (best & 1) == 1)) {
+            bd = dd;
+            best = c;
+        }
+    }
+    return sign | (uint8_t)best;
+}
+
+void oracle_quantize_row_nvfp4(int n, const float* x, uint8_t* codes, uint8_t* bscale, float* scale)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    const float s = amax > 0.0f ? amax / 2688.0f : 1.0f;
+    for (int i = 0; i < n / 2; ++i) codes[i] = 0;
+    for (int j = 0; j < n / 16; ++j) {
+        float bmax = 0.0f;
+        for (int i = 16 * j; i < 16 * j + 16; ++i) bmax = fmaxf(bmax, fabsf(x[i]));
+        const float t = bmax / s;
+        const float u = t / 6.0f;
+        const uint8_t b = oracle_e4m3_encode(u);
+        bscale[j] = b;
+        const float den = (float)oracle_e4m3_value(b) * s;
+        for (int i = 16 * j; i < 16 * j + 16; ++i) {
+            const uint8_t c = den > 0.0f ? oracle_e2m1_encode(x[i] / den) : 0;
+            codes[i / 2] |= (uint8_t)(c << (4 * (i & 1)));
+        }
+    }
+    *scale = s;
+}
+
 static uint16_t f32_to_bf16_rne(float f)
 {
     uint32_t u;
@@ -98,17 +148,25 @@ static uint16_t f32_to_bf16_rne(float f)
     return (uint16_t)(u >> 16);
 }
 
-/* One expert's weight matrix: bf16 bits, or e4m3 codes with one scale per row. */
+/* One expert's weight matrix: bf16 bits, e4m3 codes with one scale per row,
+ * or packed e2m1 codes with e4m3 scales per 16 elements and one per row. */
 typedef struct {
     const uint16_t* bf;
     const uint8_t* q;
     const float* s;
     size_t cols;
+    const uint8_t* q4;
+    const uint8_t* bs;
 } Wmat;
 
 static double wval(const Wmat* w, size_t r, size_t c)
 {
     if (w->bf) return (double)bf16_to_f32(w->bf[r * w->cols + c]);
+    if (w->q4) {
+        const size_t i = r * w->cols + c;
+        const uint8_t code = (uint8_t)((w->q4[i / 2] >> (4 * (i & 1))) & 15);
+        return oracle_e2m1_value(code) * oracle_e4m3_value(w->bs[(r * w->cols + c) / 16]) * (double)w->s[r];
+    }
     return oracle_e4m3_value(w->q[r * w->cols + c]) * (double)w->s[r];
 }
 
@@ -374,9 +432,24 @@ int oracle_dispatch(int T, int E, int k, int64_t C, const float* scores,
 
 static double silu(double x) { return x / (1.0 + exp(-x)); }
 
+/* A row replaced by its NVFP4 representation (oracle_quantize_row_nvfp4). */
+static void nvfp4_row(int n, float* x, double* out)
+{
+    uint8_t* codes = (uint8_t*)malloc((size_t)n / 2 + 1);
+    uint8_t* bs = (uint8_t*)malloc((size_t)n / 16 + 1);
+    float sc = 1.0f;
+    oracle_quantize_row_nvfp4(n, x, codes, bs, &sc);
+    for (int i = 0; i < n; ++i)
+        out[i] = oracle_e2m1_value((uint8_t)((codes[i / 2] >> (4 * (i & 1))) & 15)) *
+                 oracle_e4m3_value(bs[i / 16]) * (double)sc;
+    free(codes);
+    free(bs);
+}
+
 /* y = W2 (silu(W1 x) * W3 x) in double; W1, W3 [F][d], W2 [d][F]. */
-/* quant_act: x and a = silu(g)*u enter their products as per-row e4m3 codes
- * times the row scale (a first rounded to bf16, as it is stored). */
+/* quant_act 1: x and a = silu(g)*u enter their products as per-row e4m3 codes
+ * times the row scale (a first rounded to bf16, as it is stored); 2: as their
+ * NVFP4 representation (a again rounded to bf16 first). */
 static void expert_row_w(int d, int F, const uint16_t* x, const Wmat* w1, const Wmat* w3,
                          const Wmat* w2, int quant_act, double* y)
 {
@@ -386,10 +459,13 @@ static void expert_row_w(int d, int F, const uint16_t* x, const Wmat* w1, const 
     uint8_t* codes = (uint8_t*)malloc((size_t)(d > F ? d : F));
     float sc = 1.0f;
     for (int i = 0; i < d; ++i) xf[i] = (double)bf16_to_f32(x[i]);
-    if (quant_act) {
+    if (quant_act == 1) {
         for (int i = 0; i < d; ++i) tmp[i] = (float)xf[i];
         oracle_quantize_row(d, tmp, codes, &sc);
         for (int i = 0; i < d; ++i) xf[i] = oracle_e4m3_value(codes[i]) * (double)sc;
+    } else if (quant_act == 2) {
+        for (int i = 0; i < d; ++i) tmp[i] = (float)xf[i];
+        nvfp4_row(d, tmp, xf);
     }
     for (int j = 0; j < F; ++j) {
         double g = 0.0, u = 0.0;
@@ -399,10 +475,13 @@ static void expert_row_w(int d, int F, const uint16_t* x, const Wmat* w1, const 
         }
         a[j] = silu(g) * u;
     }
-    if (quant_act) {
+    if (quant_act == 1) {
         for (int j = 0; j < F; ++j) tmp[j] = bf16_to_f32(f32_to_bf16_rne((float)a[j]));
         oracle_quantize_row(F, tmp, codes, &sc);
         for (int j = 0; j < F; ++j) a[j] = oracle_e4m3_value(codes[j]) * (double)sc;
+    } else if (quant_act == 2) {
+        for (int j = 0; j < F; ++j) tmp[j] = bf16_to_f32(f32_to_bf16_rne((float)a[j]));
+        nvfp4_row(F, tmp, a);
     }
     free(tmp);
     free(codes);
@@ -418,30 +497,36 @@ static void expert_row_w(int d, int F, const uint16_t* x, const Wmat* w1, const 
 void oracle_expert_row(int d, int F, const uint16_t* x, const uint16_t* w1,
                        const uint16_t* w3, const uint16_t* w2, double* y)
 {
-    const Wmat m1 = {w1, NULL, NULL, (size_t)d}, m3 = {w3, NULL, NULL, (size_t)d},
-               m2 = {w2, NULL, NULL, (size_t)F};
+    const Wmat m1 = {w1, NULL, NULL, (size_t)d, NULL, NULL}, m3 = {w3, NULL, NULL, (size_t)d, NULL, NULL},
+               m2 = {w2, NULL, NULL, (size_t)F, NULL, NULL};
     expert_row_w(d, F, x, &m1, &m3, &m2, 0, y);
 }
 
-/* The weight matrices of expert e: bf16 (q1 == NULL) or e4m3 codes + row scales. */
+/* The weight matrices of expert e: bf16 (q1 == NULL), e4m3 codes + row
+ * scales (b1 == NULL), or packed e2m1 codes + e4m3 block scales + row scales. */
 typedef struct {
     const uint16_t *w1, *w3, *w2;
     const uint8_t *q1, *q3, *q2;
     const float *s1, *s3, *s2;
     int quant_act;
+    const uint8_t *b1, *b3, *b2;
 } ExpertSet;
 
 static void expert_mats(const ExpertSet* x, int e, int d, int F, Wmat* m1, Wmat* m3, Wmat* m2)
 {
     const size_t wsz = (size_t)F * d;
     if (!x->q1) {
-        *m1 = (Wmat){x->w1 + (size_t)e * wsz, NULL, NULL, (size_t)d};
-        *m3 = (Wmat){x->w3 + (size_t)e * wsz, NULL, NULL, (size_t)d};
-        *m2 = (Wmat){x->w2 + (size_t)e * wsz, NULL, NULL, (size_t)F};
+        *m1 = (Wmat){x->w1 + (size_t)e * wsz, NULL, NULL, (size_t)d, NULL, NULL};
+        *m3 = (Wmat){x->w3 + (size_t)e * wsz, NULL, NULL, (size_t)d, NULL, NULL};
+        *m2 = (Wmat){x->w2 + (size_t)e * wsz, NULL, NULL, (size_t)F, NULL, NULL};
+    } else if (x->b1) {
+        *m1 = (Wmat){NULL, NULL, x->s1 + (size_t)e * F, (size_t)d, x->q1 + (size_t)e * wsz / 2, x->b1 + (size_t)e * wsz / 16};
+        *m3 = (Wmat){NULL, NULL, x->s3 + (size_t)e * F, (size_t)d, x->q3 + (size_t)e * wsz / 2, x->b3 + (size_t)e * wsz / 16};
+        *m2 = (Wmat){NULL, NULL, x->s2 + (size_t)e * d, (size_t)F, x->q2 + (size_t)e * wsz / 2, x->b2 + (size_t)e * wsz / 16};
     } else {
-        *m1 = (Wmat){NULL, x->q1 + (size_t)e * wsz, x->s1 + (size_t)e * F, (size_t)d};
-        *m3 = (Wmat){NULL, x->q3 + (size_t)e * wsz, x->s3 + (size_t)e * F, (size_t)d};
-        *m2 = (Wmat){NULL, x->q2 + (size_t)e * wsz, x->s2 + (size_t)e * d, (size_t)F};
+        *m1 = (Wmat){NULL, x->q1 + (size_t)e * wsz, x->s1 + (size_t)e * F, (size_t)d, NULL, NULL};
+        *m3 = (Wmat){NULL, x->q3 + (size_t)e * wsz, x->s3 + (size_t)e * F, (size_t)d, NULL, NULL};
+        *m2 = (Wmat){NULL, x->q2 + (size_t)e * wsz, x->s2 + (size_t)e * d, (size_t)F, NULL, NULL};
     }
 }
 
@@ -478,7 +563,7 @@ int oracle_combine_rows(int T, int d, int E, int k, int F, const uint16_t* h,
                         const int32_t* assign, const float* cw,
                         const int32_t* tokens, int ntok, float* out_rows)
 {
-    const ExpertSet W = {w1, w3, w2, NULL, NULL, NULL, NULL, NULL, NULL, 0};
+    const ExpertSet W = {w1, w3, w2, NULL, NULL, NULL, NULL, NULL, NULL, 0, NULL, NULL, NULL};
     return combine_rows_x(T, d, E, k, F, h, &W, assign, cw, tokens, ntok, out_rows);
 }
 
@@ -487,7 +572,7 @@ int oracle_combine_rows_q8(int T, int d, int E, int k, int F, const uint16_t* h,
                            const uint8_t* q2, const float* s2, int quant_act, const int32_t* assign,
                            const float* cw, const int32_t* tokens, int ntok, float* out_rows)
 {
-    const ExpertSet W = {NULL, NULL, NULL, q1, q3, q2, s1, s3, s2, quant_act};
+    const ExpertSet W = {NULL, NULL, NULL, q1, q3, q2, s1, s3, s2, quant_act ? 1 : 0, NULL, NULL, NULL};
     return combine_rows_x(T, d, E, k, F, h, &W, assign, cw, tokens, ntok, out_rows);
 }
 
@@ -516,7 +601,7 @@ int oracle_expert_slots(int T, int d, int E, int k, int F, const uint16_t* h,
                         const int32_t* assign, const int32_t* perm,
                         int row0, int row1, float* y_slots)
 {
-    const ExpertSet W = {w1, w3, w2, NULL, NULL, NULL, NULL, NULL, NULL, 0};
+    const ExpertSet W = {w1, w3, w2, NULL, NULL, NULL, NULL, NULL, NULL, 0, NULL, NULL, NULL};
     return expert_slots_x(T, d, E, k, F, h, &W, assign, perm, row0, row1, y_slots);
 }
 
@@ -525,7 +610,31 @@ int oracle_expert_slots_q8(int T, int d, int E, int k, int F, const uint16_t* h,
                            const uint8_t* q2, const float* s2, int quant_act, const int32_t* assign,
                            const int32_t* perm, int row0, int row1, float* y_slots)
 {
-    const ExpertSet W = {NULL, NULL, NULL, q1, q3, q2, s1, s3, s2, quant_act};
+    const ExpertSet W = {NULL, NULL, NULL, q1, q3, q2, s1, s3, s2, quant_act ? 1 : 0, NULL, NULL, NULL};
+    return expert_slots_x(T, d, E, k, F, h, &W, assign, perm, row0, row1, y_slots);
+}
+
+int oracle_combine_rows_q4(int T, int d, int E, int k, int F, const uint16_t* h,
+                           const uint8_t* q1, const uint8_t* b1, const float* s1,
+                           const uint8_t* q3, const uint8_t* b3, const float* s3,
+                           const uint8_t* q2, const uint8_t* b2, const float* s2, int quant_act,
+                           const int32_t* assign, const float* cw, const int32_t* tokens, int ntok,
+                           float* out_rows)
+{
+    if (d % 16 != 0 || F % 16 != 0) return 1;
+    const ExpertSet W = {NULL, NULL, NULL, q1, q3, q2, s1, s3, s2, quant_act ? 2 : 0, b1, b3, b2};
+    return combine_rows_x(T, d, E, k, F, h, &W, assign, cw, tokens, ntok, out_rows);
+}
+
+int oracle_expert_slots_q4(int T, int d, int E, int k, int F, const uint16_t* h,
+                           const uint8_t* q1, const uint8_t* b1, const float* s1,
+                           const uint8_t* q3, const uint8_t* b3, const float* s3,
+                           const uint8_t* q2, const uint8_t* b2, const float* s2, int quant_act,
+                           const int32_t* assign, const int32_t* perm, int row0, int row1,
+                           float* y_slots)
+{
+    if (d % 16 != 0 || F % 16 != 0) return 1;
+    const ExpertSet W = {NULL, NULL, NULL, q1, q3, q2, s1, s3, s2, quant_act ? 2 : 0, b1, b3, b2};
     return expert_slots_x(T, d, E, k, F, h, &W, assign, perm, row0, row1, y_slots);
 }
 

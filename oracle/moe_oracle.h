@@ -142,6 +142,45 @@ int oracle_expert_slots_q8(int T, int d, int E, int k, int F, const uint16_t* h,
                            const uint8_t* q2, const float* s2, int quant_act, const int32_t* assign,
                            const int32_t* perm, int row0, int row1, float* y_slots);
 
+/* e2m1 (the 4-bit element of NVFP4): bit 3 sign, bits 2..1 exponent with
+ * bias 1, bit 0 mantissa; exponent 0 holds the subnormal 0.5 * mantissa.  The
+ * magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6 (no infinity, no NaN).  Only the
+ * low 4 bits of `code` are read. */
+double oracle_e2m1_value(uint8_t code);
+
+/* The e2m1 code nearest to v, ties to the code with mantissa bit 0 (even),
+ * magnitudes above 6 saturating to +-6; NaN gives 0. */
+uint8_t oracle_e2m1_encode(float v);
+
+/* NVFP4 row quantisation of x[0..n) (n a multiple of 16), in fp32 steps:
+ *   scale = max|x| / 2688 (= 6 * 448; 1 for an all-zero row);
+ *   block j (x[16j..16j+16)): b_j = e4m3(fl(fl(max|x_i| / scale) / 6)), a
+ *   non-negative e4m3 code (saturating at 448); den_j = fl(value(b_j) * scale);
+ *   code_i = e2m1(fl(x_i / den_j)) (0 for every i when den_j = 0).
+ * x_i is then represented as e2m1(code_i) * value(b_j) * scale.  codes holds
+ * two per byte, element 2m in the low nibble of byte m; bscale[n/16]. */
+void oracle_quantize_row_nvfp4(int n, const float* x, uint8_t* codes, uint8_t* bscale, float* scale);
+
+/* oracle_combine_rows / oracle_expert_slots with NVFP4 expert weights: W1,
+ * W3 [E][F][d] and W2 [E][d][F] as packed e2m1 codes (q1, q3, q2), e4m3 block
+ * scales per 16 consecutive elements of a row (b1, b3 [E][F][d/16], b2
+ * [E][d][F/16]) and fp32 row scales (s1, s3 [E][F], s2 [E][d]); weight =
+ * e2m1(code) * value(block scale) * row scale.  quant_act != 0: each token
+ * row x and each activation row silu(W1 x) * (W3 x) (rounded to bf16 first)
+ * enters its GEMM NVFP4-quantised per row (oracle_quantize_row_nvfp4). */
+int oracle_combine_rows_q4(int T, int d, int E, int k, int F, const uint16_t* h,
+                           const uint8_t* q1, const uint8_t* b1, const float* s1,
+                           const uint8_t* q3, const uint8_t* b3, const float* s3,
+                           const uint8_t* q2, const uint8_t* b2, const float* s2, int quant_act,
+                           const int32_t* assign, const float* cw, const int32_t* tokens, int ntok,
+                           float* out_rows);
+int oracle_expert_slots_q4(int T, int d, int E, int k, int F, const uint16_t* h,
+                           const uint8_t* q1, const uint8_t* b1, const float* s1,
+                           const uint8_t* q3, const uint8_t* b3, const float* s3,
+                           const uint8_t* q2, const uint8_t* b2, const float* s2, int quant_act,
+                           const int32_t* assign, const int32_t* perm, int row0, int row1,
+                           float* y_slots);
+
 /* Backward pass of the layer for one dispatch (training; not on the forward
  * path).  The forward is out[t] = sum over t's kept ranks r of
  * cw[t,r] * y_e(h_t) with e = assign[t,r], y_e(x) = W2_e (silu(W1_e x) * W3_e x),

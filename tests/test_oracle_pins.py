@@ -734,6 +734,204 @@ def test_q8_activation_rounding_hand_case():
     assert raw[0, 4] == np.float32(1.083984375) and raw[1, 4] == np.float32(4 * 1.083984375)
 
 
+# ----------------------------------------------------------------------------- NVFP4 weights
+# e2m1 (the OCP microscaling FP4 element): sign, 2-bit exponent with bias 1, 1-bit mantissa,
+# exponent 0 the subnormal 0.5; NVFP4 groups 16 elements under one e4m3 block scale
+# ([2kiu] §5.1 quantises experts to 4-6 bits; the format choice is this library's).
+
+E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_all_codes():
+    for c in range(16):
+        want = E2M1[c & 7] * (-1.0 if c & 8 else 1.0)
+        got = oracle.e2m1_value(c)
+        assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), c
+
+
+def _e2m1_nearest(v):
+    """Brute force: the magnitude nearest to |v|, ties to the even code (mantissa bit 0)."""
+    a = abs(v)
+    best = min(range(8), key=lambda c: (abs(a - E2M1[c]), c & 1))
+    return best | (8 if math.copysign(1.0, v) < 0 else 0)
+
+
+def test_e2m1_encode_is_nearest_with_ties_to_even():
+    rng = np.random.default_rng(12)
+    grid = np.arange(-64, 65) / 8.0                      # every tie and every code value
+    vals = np.concatenate([grid, rng.uniform(-8, 8, 3000), rng.standard_normal(2000) * 3,
+                           [1e30, -1e30, 6.0001, -5.9999, 0.2499, 0.2501]]).astype(np.float32)
+    for v in vals:
+        assert oracle.e2m1_encode(float(v)) == _e2m1_nearest(float(v)), v
+
+
+def _nvfp4_exact_row(rng, blocks, scale_pow, max_block):
+    """A row that NVFP4 represents exactly: block j is e2m1 values times v_j * 2^scale_pow,
+    v_j an e4m3 power of two, its largest magnitude 6 (so its block scale is v_j), and block
+    `max_block` has v = 448 (so the row scale is 2^scale_pow).  Returns the row and (v_j)."""
+    s = 2.0 ** scale_pow
+    vs = [2.0 ** int(rng.integers(-6, 8)) for _ in range(blocks)]
+    vs[max_block] = 448.0
+    row = []
+    for v in vs:
+        c = rng.choice(E2M1, size=16) * rng.choice([-1.0, 1.0], size=16)
+        c[int(rng.integers(16))] = 6.0 * rng.choice([-1.0, 1.0])
+        row.append(c * v * s)
+    return np.concatenate(row), vs
+
+
+def test_nvfp4_row_quantisation_is_exact_on_representable_rows():
+    """Rows of e2m1 values times power-of-two block scales, with 6 in every block and
+    6 * 448 * 2^p as the row's largest magnitude: the scale is 2^p, every block scale
+    comes back exactly and every code gives its value back (a dropped factor of 6 or
+    448, a block scale taken from the wrong block, or swapped nibbles break this)."""
+    rng = np.random.default_rng(13)
+    for trial in range(20):
+        blocks = int(rng.integers(1, 9))
+        p = int(rng.integers(-12, 4))
+        row, vs = _nvfp4_exact_row(rng, blocks, p, int(rng.integers(blocks)))
+        codes, bs, sc = oracle.quantize_row_nvfp4(row.astype(np.float32))
+        assert sc == 2.0 ** p
+        assert [oracle.e4m3_value(b) for b in bs] == vs
+        vals = [oracle.e2m1_value((codes[i // 2] >> (4 * (i & 1))) & 15) * vs[i // 16] * sc
+                for i in range(row.size)]
+        assert np.array_equal(np.array(vals), row)
+
+
+def test_nvfp4_row_quantisation_hand_case():
+    """32 elements worked by hand.  max|x| = 21, scale = 21 / 2688 = 2^-7.
+    Block 0 = (21, 7, 3.5, 1, zeros): t = 21 / scale = 2688, u = t / 6 = 448 -> block code
+    0x7E; den = 448 * scale = 3.5; x / den = (6, 2, 1, 0.2857...) -> codes 7, 4, 2, 1
+    (0.2857 is nearer 0.5 than 0).
+    Block 1 = (-0.7, 0.35, zeros): t = 0.7 / scale = 89.6, u = 14.93... -> e4m3 15
+    (1.875 * 8, code 0x57); den = 15 * scale = 0.1171875; x / den = (-5.9733, 2.9866)
+    -> codes 15 (-6) and 5 (3: exponent 2, mantissa 1)."""
+    x = np.zeros(32, np.float32)
+    x[:4] = [21, 7, 3.5, 1]
+    x[16:18] = [-0.7, 0.35]
+    codes, bs, sc = oracle.quantize_row_nvfp4(x)
+    assert sc == 2.0 ** -7
+    assert list(bs) == [0x7E, 0x57]
+    nib = [(codes[i // 2] >> (4 * (i & 1))) & 15 for i in range(32)]
+    assert nib[:4] == [7, 4, 2, 1] and nib[16:18] == [15, 5]
+    assert not any(nib[4:16]) and not any(nib[18:])
+
+
+def _q4_weights(rng, E, rows, cols, exact=True):
+    """NVFP4 weights [E, rows, cols]: random codes, random e4m3 block scales (powers of two
+    when `exact`, so that every weight is exact in bf16), power-of-two row scales."""
+    codes = rng.integers(0, 16, size=(E, rows, cols)).astype(np.uint8)
+    if exact:
+        bvals = 2.0 ** rng.integers(-4, 5, size=(E, rows, cols // 16))
+        b = np.vectorize(oracle.e4m3_encode)(bvals.astype(np.float32)).astype(np.uint8)
+    else:
+        b = rng.integers(0x20, 0x60, size=(E, rows, cols // 16)).astype(np.uint8)
+    s = (2.0 ** rng.integers(-10, -4, size=(E, rows))).astype(np.float32)
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    val = (np.vectorize(oracle.e2m1_value)(codes) * np.vectorize(oracle.e4m3_value)(b).repeat(16, axis=2)
+           * s[..., None])
+    return (packed, b, s), val
+
+
+def test_q4_experts_equal_bf16_experts_on_exact_weights():
+    """NVFP4 weights whose values are exact in bf16: without activation quantisation the
+    4-bit path must give the bf16 path's numbers exactly; a block scale moved to the next
+    block changes them."""
+    rng = np.random.default_rng(14)
+    T, d, F, E, k = 5, 32, 48, 3, 2
+    w1, v1 = _q4_weights(rng, E, F, d)
+    w3, v3 = _q4_weights(rng, E, F, d)
+    w2, v2 = _q4_weights(rng, E, d, F)
+    h = bf16(rng.standard_normal((T, d)))
+    assign = np.array([[0, 1], [2, 0], [1, -1], [2, 1], [0, 2]], np.int32)
+    cw = rng.random((T, k)).astype(np.float32)
+    toks = np.arange(T, dtype=np.int32)
+    got = oracle.combine_rows_q4(h, w1, w3, w2, assign, cw, toks, quant_act=False)
+    want = oracle.combine_rows(h, bf16(v1), bf16(v3), bf16(v2), assign, cw, toks)
+    assert np.array_equal(bf16(v1), bf16(v1.astype(np.float32))) and np.array_equal(got, want)
+    bad1 = (w1[0], np.roll(w1[1], 1, axis=2), w1[2])
+    assert not np.array_equal(oracle.combine_rows_q4(h, bad1, w3, w2, assign, cw, toks, quant_act=False), want)
+
+
+def _q4_act_case():
+    """Token rows A and B = 2A (d = 48: three blocks) and one expert (F = 32), built so that
+    both NVFP4 quantisations are exact except where stated.
+    x_A: block 0 = (6, 1, 0, ...) (block scale 256, unit 1), block 1 = (10.5, 0, ...) (the
+    row's largest: scale 10.5 / 2688 = 2^-8, block scale 448), block 2 = (6 * 2^-9, 2^-9,
+    0, ...) (block scale 0.5, unit 2^-9): every code gives its value back.
+    W1: 64 on column 1 in every row: g = 64 (A), 128 (B); silu(g) = g in double.
+    W3 rows: 0: 0.375 e_1; 1: (5/64) e_1 + 2^-5 e_33; 16: 10.5 e_1; the others zero.
+      A: u = (0.375, 5/64 + 2^-14, ..., 10.5 at 16), a = 64 u = (24, 5 + 2^-8, 0, ..., 672).
+      The activation row's largest is 672: scale 0.25; block 0 max 24: block scale 16, unit 4;
+      a_1 rounds to bf16 5 (ulp 2^-5 at 4..8), 5 / 4 = 1.25 is halfway between the e2m1
+      values 1 and 1.5 and ties to 1: a'_1 = 4 (unrounded, 1.2509... -> 1.5: 6).  a'_0 = 24,
+      a'_16 = 672 exactly.  B: g and u double, so a and its scale quadruple (a'_1 = 16).
+    W2 rows: 0: e_1; 1: e_0; 2: 2^-4 e_16; the others zero.
+      y_A = (4, 24, 42, 0, ...), y_B = (16, 96, 168, 0, ...)."""
+    d, F = 48, 32
+    x = np.zeros((2, d))
+    x[0, [0, 1, 16, 32, 33]] = [6, 1, 10.5, 6 * 2.0 ** -9, 2.0 ** -9]
+    x[1] = 2 * x[0]
+
+    def pack(vals, codes_for, bscale_vals, row_scales):
+        rows, cols = vals.shape
+        codes = np.zeros((rows, cols), np.uint8)
+        for r in range(rows):
+            for c in range(cols):
+                v = vals[r, c] / (bscale_vals[r][c // 16] * row_scales[r])
+                codes[r, c] = codes_for[v]
+                assert E2M1[codes[r, c] & 7] * (-1 if codes[r, c] & 8 else 1) == v
+        b = np.array([[oracle.e4m3_encode(v) for v in bv] for bv in bscale_vals], np.uint8)
+        assert all(oracle.e4m3_value(bb) == vv for br, bv in zip(b, bscale_vals) for bb, vv in zip(br, bv))
+        packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+        return packed[None], b[None], np.asarray(row_scales, np.float32)[None]
+
+    enc = {v: i for i, v in enumerate(E2M1)}
+    enc.update({-v: i | 8 for i, v in enumerate(E2M1) if v})
+    w1 = np.zeros((F, d))
+    w1[:, 1] = 64
+    w3 = np.zeros((F, d))
+    w3[0, 1] = 0.375
+    w3[1, 1] = 5 / 64
+    w3[1, 33] = 2.0 ** -5
+    w3[16, 1] = 10.5
+    w2 = np.zeros((d, F))
+    w2[0, 1] = 1
+    w2[1, 0] = 1
+    w2[2, 16] = 2.0 ** -4
+    # block scales and row scales that make every weight an e2m1 value
+    w1q = pack(w1, enc, [[64.0] * 3] * F, [0.25] * F)        # 64 = 4 * 64 * 0.25
+    w3_b = [[1.0] * 3 for _ in range(F)]
+    w3_s = [1.0] * F
+    w3_b[0] = [0.25, 1, 1]                     # 0.375 = 1.5 * 0.25
+    w3_b[1], w3_s[1] = [5.0, 1, 2.0], 2.0 ** -6     # 5/64 = 1 * 5 * 2^-6; 2^-5 = 1 * 2 * 2^-6
+    w3_b[16] = [1.75, 1, 1]                    # 10.5 = 6 * 1.75
+    w3q = pack(w3, enc, w3_b, w3_s)
+    w2_b = [[1.0] * 2 for _ in range(d)]
+    w2_s = [1.0] * d
+    w2_b[2], w2_s[2] = [1, 1.0], 2.0 ** -4
+    w2q = pack(w2, enc, w2_b, w2_s)
+    want = np.zeros((2, d), np.float32)
+    want[0, :3] = [4, 24, 42]
+    want[1, :3] = [16, 96, 168]
+    return bf16(x), w1q, w3q, w2q, want
+
+
+def test_q4_activation_quantisation_hand_case():
+    """The bf16 rounding of the activation before its NVFP4 quantisation decides a code
+    (the tie at 1.25 in units of 4), through the token-order and slot-order functions;
+    quantising without the rounding would give a'_1 = 6."""
+    h, w1, w3, w2, want = _q4_act_case()
+    assign = np.array([[0], [0]], np.int32)
+    cw = np.ones((2, 1), np.float32)
+    got = oracle.combine_rows_q4(h, w1, w3, w2, assign, cw, np.arange(2, dtype=np.int32), quant_act=True)
+    np.testing.assert_array_equal(got, want)
+    slots = oracle.expert_slots_q4(h, w1, w3, w2, assign, np.array([1, 0], np.int32), 0, 2, quant_act=True)
+    np.testing.assert_array_equal(slots, want[::-1])
+    raw = oracle.combine_rows_q4(h, w1, w3, w2, assign, cw, np.arange(2, dtype=np.int32), quant_act=False)
+    assert raw[0, 0] == np.float32(5 + 2.0 ** -8) and raw[1, 0] == np.float32(4 * (5 + 2.0 ** -8))
+
+
 # --------------------------------------------------------------------------- router variants
 # Temperature ([cnnetsun] §3.1 step 3; [2kiu] §2), normalisation before the
 # router ([2kiu] §5.2), the two-layer router silu(x W1) W2 ([cnnetsun] §3.1 step 2).

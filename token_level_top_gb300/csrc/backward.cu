@@ -458,6 +458,7 @@ cudaError_t run_backward(const BackwardArgs& a, cudaStream_t s)
     BwdGemmLaunch g{};
     g.E = E;
     g.rows = R;
+    g.kept = static_cast<long long>(T) * k;
     g.offsets = a.offsets;
     g.status = a.status;
     g.budget = a.budget;

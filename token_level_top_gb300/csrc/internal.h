@@ -161,6 +161,7 @@ enum BwdGemmMode : int { BG_DGRAD = 0, BG_WGRAD = 1 };
 struct BwdGemmLaunch {
     int mode, E;
     long long rows;        // rows of the row-block buffers (room for every expert's padded block)
+    long long kept;        // most kept rows (T*k): BG_DGRAD pairs CTAs when experts average 2+ row tiles
     int K;                 // BG_DGRAD: inner dimension (the row block's width, the weights' rows per expert)
     int N;                 // output columns
     int Mw;                // BG_WGRAD: output rows per expert (the A row block's width)

@@ -46,14 +46,16 @@ CHUNK = 256  # tokens per routing chunk; a batch of one chunk routes and dispatc
 BACKWARD_KERNELS = 12  # prep, pad, four GEMMs, SwiGLU backward, router backward, dh, dW_r (two), bias sum
 
 
-def kernels_per_step(T, fp8=False, norm=0, hidden=0):
+def kernels_per_step(T, quant=None, norm=0, hidden=0):
     """Kernels of this library one layer step launches."""
     # router GEMM, row gather, gate-up, down, combine + route and dispatch:
     # one fused kernel for a single chunk, else route + dispatch replay + finish;
     # FP8: the activation rows are quantised between the two expert GEMMs;
     # router variants: the normalisation before the router GEMM, the
     # two-layer router's second layer after it
-    return 5 + (1 if T <= CHUNK else 3) + (1 if fp8 else 0) + (1 if norm else 0) + (1 if hidden else 0)
+    # (NVFP4 likewise: its token-row quantiser replaces the gather, the
+    # activation rows are quantised between the GEMMs)
+    return 5 + (1 if T <= CHUNK else 3) + (1 if quant else 0) + (1 if norm else 0) + (1 if hidden else 0)
 
 
 def parse():
@@ -67,6 +69,10 @@ def parse():
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the other workloads measured after the main one (the 'workloads' key)")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--nvfp4-weights", action="store_true",
+                    help="expert GEMMs in NVFP4: e2m1 weights with e4m3 scales per 16 elements and a row "
+                         "scale (moe_quantize_w13_nvfp4 / moe_quantize_nvfp4), token and activation rows "
+                         "likewise on the fly")
     ap.add_argument("--fp8-weights", action="store_true",
                     help="expert GEMMs in e4m3: weights quantised per row once (moe_quantize_fp8), "
                          "token and activation rows per row on the fly")
@@ -210,7 +216,16 @@ def recorded_traffic(kernel: str, workload: str):
 SUSTAINED_AFTER_S = 2.0   # a timed region at least this long is held to the sustained peak
 
 
-def tensor_peak(peaks, peak_kind, timed_s, fp8=False):
+# nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): e4m3 4.5, NVFP4 13.5
+QUANT_RATIO = {None: 1.0, "fp8": 2.0, "nvfp4": 6.0}
+# weight bytes per element: codes, plus e4m3 block scales per 16 for NVFP4
+QUANT_BYTES = {None: 2.0, "fp8": 1.0, "nvfp4": 0.5 + 1.0 / 16}
+QUANT_DTYPE = {None: "bf16", "fp8": "e4m3 expert weights and activations (fp32 row scales), fp32 accumulate",
+               "nvfp4": "NVFP4 expert weights and activations (e2m1, e4m3 scales per 16, fp32 row scales), "
+                        "fp32 accumulate"}
+
+
+def tensor_peak(peaks, peak_kind, timed_s, quant=None):
     """(TFLOP/s, description): the measured bf16 burst peak for a timed region shorter
     than SUSTAINED_AFTER_S, the sustained one (a seconds-long loop under the power cap)
     for a longer one; for e4m3 MMAs times 2, the nominal e4m3 / bf16 ratio."""
@@ -220,8 +235,9 @@ def tensor_peak(peaks, peak_kind, timed_s, fp8=False):
     else:
         v, kind = float(peaks["bf16_tflops_sustained"]), (f"{peak_kind} bf16 sustained (timed region "
                                                           f"{timed_s:.2f} s)")
-    if fp8:
-        v, kind = 2.0 * v, kind + " x 2, the nominal e4m3 / bf16 ratio"
+    if quant:
+        r = QUANT_RATIO[quant]
+        v, kind = r * v, kind + f" x {r:g}, the nominal {quant} / bf16 ratio"
     return v, kind
 
 
@@ -366,10 +382,17 @@ def run_ours(args, rank, world, local):
     host_w = (L["w1"].cpu(), L["w3"].cpu(), L["w2"].cpu()) if want_cpu else None
     del L["w1"], L["w3"]
     torch.cuda.empty_cache()
-    fp8 = args.fp8_weights
-    if fp8:   # e4m3 expert weights, one fp32 scale per weight row
+    if args.fp8_weights and args.nvfp4_weights:
+        raise SystemExit("--fp8-weights and --nvfp4-weights exclude each other")
+    quant = "fp8" if args.fp8_weights else ("nvfp4" if args.nvfp4_weights else None)
+    quantized = quant is not None
+    if quant == "fp8":   # e4m3 expert weights, one fp32 scale per weight row
         L["w13"] = moe.quantize_fp8(L["w13"])
         L["w2"] = moe.quantize_fp8(L["w2"])
+    elif quant == "nvfp4":
+        L["w13"] = moe.quantize_w13_nvfp4(L["w13"])
+        L["w2"] = moe.quantize_nvfp4(L["w2"])
+    if quant:
         want_cpu = False
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
@@ -389,9 +412,9 @@ def run_ours(args, rank, world, local):
         bias = None
         router_desc = {"tau": args.tau, "norm": args.router_norm, "hidden": hidden}
     bwd = args.backward
-    if bwd and (fp8 or norm or hidden):
+    if bwd and (quantized or norm or hidden):
         raise SystemExit("--backward runs with bf16 experts and the linear router")
-    flags = (moe.FLAG_FP8 if fp8 else 0) | (moe.FLAG_BACKWARD if bwd else 0)
+    flags = {None: 0, "fp8": moe.FLAG_FP8, "nvfp4": moe.FLAG_NVFP4}[quant] | (moe.FLAG_BACKWARD if bwd else 0)
     cfg = moe.Config.of(shape, flags=flags, tau=args.tau, router_norm=norm,
                         norm_eps=1e-5 if norm == moe.NORM_LAYER else 1e-12, router_hidden=hidden)
     ws = moe.workspace(cfg)
@@ -508,7 +531,7 @@ def run_ours(args, rank, world, local):
 
     def e2e_one(i):
         j = i % 2
-        if not (bwd or fp8 or variant):
+        if not (bwd or quantized or variant):
             moe.layer_forward_host_async(cfg, wss[j], h_host, L["wr"], L["w13"], L["w2"], o_hosts[j], L["bias"],
                                          L["usage"])
             return
@@ -537,8 +560,8 @@ def run_ours(args, rank, world, local):
     peaks, peak_kind = load_peaks()
     d, F, T = shape.d, shape.F, shape.T
     roof, expert_tflops, weight_gbs = expert_roofline(shape, kept, active, stage_ms, peaks, peak_kind,
-                                                      ms_max * 1e-3, fp8)
-    peak_tf = tensor_peak(peaks, peak_kind, ms_max * 1e-3, fp8)[0]
+                                                      ms_max * 1e-3, quant)
+    peak_tf = tensor_peak(peaks, peak_kind, ms_max * 1e-3, quant)[0]
     bwd_line = None
     if bwd:
         # the backward's GEMM work on the kept rows: W2^T dout (2 d F), dx (2 2F d), dW2
@@ -557,8 +580,7 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": ("e4m3 expert weights and activations (fp32 row scales), fp32 accumulate"
-                  if fp8 else "bf16"),
+        "dtype": QUANT_DTYPE[quant],
         "data": "synthetic",
         "config": workload_config(shape, router_desc, graph is not None),
         "roofline": roof,
@@ -569,9 +591,9 @@ def run_ours(args, rank, world, local):
         "e2e": ({"value": world * T * args.e2e_steps / te, "unit": UNIT,
                  "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * (4 if bwd else 2),
                  "overlap": ("two workspaces on two streams" +
-                             (" (moe_layer_forward_host_async)" if not (bwd or fp8 or variant) else ""))}
+                             (" (moe_layer_forward_host_async)" if not (bwd or quantized or variant) else ""))}
                 if args.e2e_steps > 0 else None),
-        "gpu_launches": (kernels_per_step(shape.T, fp8, norm, hidden) + (BACKWARD_KERNELS if bwd else 0))
+        "gpu_launches": (kernels_per_step(shape.T, quant, norm, hidden) + (BACKWARD_KERNELS if bwd else 0))
         * args.steps,
     }
     if bwd:
@@ -587,36 +609,37 @@ def run_ours(args, rank, world, local):
                        f"expert FFN of {res['ffn_rows']} of {res['kept']} kept rows "
                        f"({res['t_ffn_sample']:.1f} s), extrapolated by kept rows"),
             "host": host_cpu()}
-    plain = not (fp8 or bwd or variant or graph is not None)
+    plain = not (quantized or bwd or variant or graph is not None)
     if plain and not args.no_workloads:
         del L, ws, wss, h_devs, outs
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         line["workloads"] = {}
-        for name, wfp8 in SIDE_WORKLOADS:
-            if name == shape.name and not wfp8:
+        for name, wq in SIDE_WORKLOADS:
+            if name == shape.name and not wq:
                 continue
-            line["workloads"][name + ("_fp8" if wfp8 else "")] = side_workload(name, wfp8, peaks, peak_kind)
+            line["workloads"][name + (f"_{wq}" if wq else "")] = side_workload(name, wq, peaks, peak_kind)
             torch.cuda.empty_cache()
         line["gpu_launches"] += sum(w["gpu_launches"] for w in line["workloads"].values())
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
-def expert_roofline(shape, kept, active, stage_ms, peaks, peak_kind, timed_s, fp8):
+def expert_roofline(shape, kept, active, stage_ms, peaks, peak_kind, timed_s, quant):
     """Roofline of the dominant expert GEMM (gate-up or down) of one layer step: its
     algorithmic work per launch -- kept rows only, every active expert's weights read
     once -- over its mean CUDA-event duration; plus the two expert GEMMs' TFLOP/s and
     weight-streaming GB/s together."""
     d, F = shape.d, shape.F
     flops = {"gate_up": 2.0 * kept * d * 2 * F, "down": 2.0 * kept * F * d}
-    wb = 1 if fp8 else 2   # bytes per weight element (+ 4 per weight row for FP8 scales)
-    # (FP8: the GEMMs read 1-byte activation rows; the act quantisation pass
-    # between them is timed in the down stage)
-    bytes_ = {"gate_up": active * 2.0 * F * (d * wb + 4 * fp8) + kept * d * wb + kept * F * 2,
-              "down": active * 1.0 * d * (F * wb + 4 * fp8) + kept * F * wb + kept * d * 2}
+    wb = QUANT_BYTES[quant]   # bytes per weight element (+ 4 per weight row for the row scales)
+    rs = 4 if quant else 0
+    # (quantised: the GEMMs read activation rows of the same width; the act
+    # quantisation pass between them is timed in the down stage)
+    bytes_ = {"gate_up": active * 2.0 * F * (d * wb + rs) + kept * d * wb + kept * F * 2,
+              "down": active * 1.0 * d * (F * wb + rs) + kept * F * wb + kept * d * 2}
     dom = max(("gate_up", "down"), key=lambda n: stage_ms[n])
-    peak_tf, tf_kind = tensor_peak(peaks, peak_kind, timed_s, fp8)
+    peak_tf, tf_kind = tensor_peak(peaks, peak_kind, timed_s, quant)
     peak_bw = float(peaks["hbm_gbs"])
     intensity = (flops["gate_up"] + flops["down"]) / (bytes_["gate_up"] + bytes_["down"])
     sec = stage_ms[dom] * 1e-3
@@ -627,7 +650,8 @@ def expert_roofline(shape, kept, active, stage_ms, peaks, peak_kind, timed_s, fp
         roof = {"bound": "hbm", "achieved": bytes_[dom] / sec / 1e9, "peak": peak_bw,
                 "unit": "GB/s", "peak_kind": f"{peak_kind} HBM copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    kname = f"moe_gemm_kernel ({dom.replace('_', '-')}{', e4m3' if fp8 else ''})"
+    kname = ("moe_gemm_nvfp4_kernel" if quant == "nvfp4" else "moe_gemm_kernel") + \
+        f" ({dom.replace('_', '-')}{', e4m3' if quant == 'fp8' else ''})"
     roof["traffic"] = recorded_traffic(kname, shape.name)
     roof["kernel"] = kname
     roof["algorithmic_per_launch"] = {"flop": flops[dom], "bytes": bytes_[dom]}
@@ -640,19 +664,23 @@ def expert_roofline(shape, kept, active, stage_ms, peaks, peak_kind, timed_s, fp
 # The other workloads, measured after the main one in the same run (eager steps
 # over a ~0.2 s timed region, and CUDA-graph replays for the launch-bound batches
 # of one routing chunk), each with its dominant expert GEMM's roofline.
-SIDE_WORKLOADS = [("mixtral_decode", False), ("mixtral_decode", True), ("fine_grained", False),
-                  ("skewed", False), ("tiny", False), ("mixtral_prefill", False)]
+SIDE_WORKLOADS = [("mixtral_decode", None), ("mixtral_decode", "fp8"), ("mixtral_decode", "nvfp4"),
+                  ("fine_grained", None), ("skewed", None), ("tiny", None), ("mixtral_prefill", None),
+                  ("mixtral_prefill", "fp8"), ("mixtral_prefill", "nvfp4")]
 SIDE_TIMED_S = 0.2
 
 
-def side_workload(name, fp8, peaks, peak_kind):
+def side_workload(name, quant, peaks, peak_kind):
     shape = synth.CONFIGS[name]
     L = layer_inputs(shape)
     del L["w1"], L["w3"]
-    if fp8:
+    if quant == "fp8":
         L["w13"] = moe.quantize_fp8(L["w13"])
         L["w2"] = moe.quantize_fp8(L["w2"])
-    cfg = moe.Config.of(shape, flags=moe.FLAG_FP8 if fp8 else 0)
+    elif quant == "nvfp4":
+        L["w13"] = moe.quantize_w13_nvfp4(L["w13"])
+        L["w2"] = moe.quantize_nvfp4(L["w2"])
+    cfg = moe.Config.of(shape, flags={None: 0, "fp8": moe.FLAG_FP8, "nvfp4": moe.FLAG_NVFP4}[quant])
     ws = moe.workspace(cfg)
     out = torch.empty(shape.T, shape.d, dtype=torch.bfloat16, device="cuda")
     _, aux = moe.layer_forward(cfg, ws, L["h"], L["wr"], L["w13"], L["w2"], L["bias"], L["usage"],
@@ -683,12 +711,12 @@ def side_workload(name, fp8, peaks, peak_kind):
         raise RuntimeError(f"{name}: device status {st} ({moe.STATUS.get(st)})")
     stage_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
                 for j, n in enumerate(moe.STAGE_NAMES)}
-    roof, tflops, wgbs = expert_roofline(shape, kept, active, stage_ms, peaks, peak_kind, ms * 1e-3, fp8)
+    roof, tflops, wgbs = expert_roofline(shape, kept, active, stage_ms, peaks, peak_kind, ms * 1e-3, quant)
     res = {"tokens_per_s": shape.T * steps / (ms * 1e-3), "ms_per_step": ms / steps, "steps": steps,
-           "dtype": "e4m3 expert weights and activations" if fp8 else "bf16",
+           "dtype": QUANT_DTYPE[quant],
            "kept_rows": kept, "stages_ms": stage_ms, "roofline": roof, "expert_gemm_tflops": tflops,
            "weight_stream_gbs": wgbs, "weight_stream_frac_of_hbm": wgbs / float(peaks["hbm_gbs"]),
-           "gpu_launches": kernels_per_step(shape.T, fp8) * steps,
+           "gpu_launches": kernels_per_step(shape.T, quant) * steps,
            "config": {k: v for k, v in workload_config(shape).items() if k != "l2"}}
     if shape.T <= CHUNK:   # launch-bound: the same step replayed from a CUDA graph
         side = torch.cuda.Stream()
@@ -709,7 +737,7 @@ def side_workload(name, fp8, peaks, peak_kind):
         torch.cuda.synchronize()
         res["ms_per_step_graph"] = e0.elapsed_time(e1) / steps
         res["tokens_per_s_graph"] = shape.T * steps / (e0.elapsed_time(e1) * 1e-3)
-        res["gpu_launches"] += kernels_per_step(shape.T, fp8) * (steps + 3)
+        res["gpu_launches"] += kernels_per_step(shape.T, quant) * (steps + 3)
         del g
     del L, ws, out
     return res

@@ -66,6 +66,10 @@ typedef enum {
  * T*k + 127E) with C' = min(C, T) rounded up to 128); moe_layer_forward then
  * also keeps each kept row's g and u (fp32) there for the backward. */
 #define MOE_FLAG_BACKWARD 2u
+/* moe_config_t.flags: size the workspace for the NVFP4 entry points too (adds
+ * about T*k*(d/2 + F/2 + d/16 + F/16 + 12) bytes for the 4-bit token and
+ * activation rows, their block scales, row scales and row maxima). */
+#define MOE_FLAG_NVFP4 4u
 
 /* Layer shape.  Capacity C = ceil(T*k*cf/E) unless capacity > 0. */
 typedef struct {
@@ -77,7 +81,7 @@ typedef struct {
     double cf;        /* capacity factor, read as a decimal with 6 fractional digits */
     int32_t capacity; /* > 0: explicit per-expert capacity, overrides cf */
     float lambda;     /* load-penalty weight (0 = no penalty) */
-    uint32_t flags;   /* 0, or MOE_FLAG_FP8 and/or MOE_FLAG_BACKWARD */
+    uint32_t flags;   /* 0, or any of MOE_FLAG_FP8, MOE_FLAG_BACKWARD, MOE_FLAG_NVFP4 */
     /* Router variants (all zero: the plain linear router, no temperature). */
     float tau;              /* temperature, 0 (= 1) or finite > 0: s = z / tau - lambda*usage */
     uint32_t router_norm;   /* MOE_ROUTER_NORM_*: normalisation of h before the router */
@@ -282,6 +286,65 @@ moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* h_dev,
                                    uint8_t* flags_dev, int32_t* counts_dev, float* f_dev,
                                    float* P_dev, void* const* stage_events, void* ws_dev,
                                    size_t ws_bytes, void* stream);
+
+/* NVFP4 expert path: 4-bit weights and activations.  A row x[0..n) is held
+ * as e2m1 codes (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 with a sign; two per byte,
+ * element 2m in the low nibble), one e4m3 scale per 16 consecutive elements
+ * (a byte; the scales of a row padded to moe_nvfp4_sf_stride(n) bytes) and
+ * one fp32 scale per row, quantised in fp32 steps:
+ *   scale = max|x| / 2688 (= 6 * 448; 1 for an all-zero row);
+ *   per block: b = e4m3(fl(fl(max|x_i| / scale) / 6)), den = fl(value(b) * scale),
+ *   code_i = e2m1(fl(x_i / den)) (nearest, ties to even, saturating; 0 if den = 0);
+ *   x_i ~ e2m1(code_i) * value(b) * scale.
+ * The pages quantise experts to 4-6 bits ([2kiu] §5.1) to move fewer bytes;
+ * the GEMMs multiply the codes on the tensor cores
+ * (tcgen05.mma.kind::mxf4nvf4.block_scale, the block scales applied by the
+ * MMA, fp32 accumulate) and the epilogue applies the two row scales.
+ * moe_nvfp4_sf_stride(cols): bytes per row of block scales (cols/16 rounded up
+ * to a multiple of 16). */
+int32_t moe_nvfp4_sf_stride(int32_t cols);
+
+/* NVFP4 quantisation of a bf16 matrix w_dev [rows, cols] (row-major; cols a
+ * multiple of 32, at most 16384): codes_dev [rows, cols/2] bytes, bscale_dev
+ * [rows, moe_nvfp4_sf_stride(cols)] bytes, scales_dev [rows] fp32.  Use it for
+ * W2 (rows E*d, cols F).  Pointers 16-byte aligned.  Errors:
+ * MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED (cols > 16384), MOE_ERR_MISALIGNED. */
+moe_status_t moe_quantize_nvfp4(int64_t rows, int32_t cols, const void* w_dev, void* codes_dev,
+                                void* bscale_dev, float* scales_dev, void* stream);
+
+/* NVFP4 quantisation of W13 [E, 2F, d] in the moe_pack_w13 layout into this
+ * path's own packing: per expert, 128-row block j holds W1 rows 64j..64j+63 and
+ * then the matching W3 rows, so that one 128-column tile of the 4-bit gate-up
+ * GEMM holds matching gate and up columns.  Outputs as moe_quantize_nvfp4 with
+ * rows E*2F, cols d (row r of the outputs is row r of the new packing). */
+moe_status_t moe_quantize_w13_nvfp4(int32_t E, int32_t d_ff, int32_t d_model, const void* w13_dev,
+                                    void* codes_dev, void* bscale_dev, float* scales_dev, void* stream);
+
+/* moe_expert_ffn with NVFP4 weights (w13 from moe_quantize_w13_nvfp4, w2 from
+ * moe_quantize_nvfp4): each kept slot's token row and each activation row
+ * silu(g)*u (after rounding to bf16) are quantised the same way on the fly,
+ * both GEMMs multiply e2m1 codes with their block scales on the tensor cores
+ * and scale the result by the two row scales.  Needs cfg->flags &
+ * MOE_FLAG_NVFP4 (MOE_ERR_INVALID_ARG otherwise), d a multiple of 128 and d,
+ * F at most 16384 (MOE_ERR_UNSUPPORTED otherwise); y_slots as moe_expert_ffn. */
+moe_status_t moe_expert_ffn_nvfp4(const moe_config_t* cfg, const void* h_dev, const int32_t* perm_dev,
+                                  const int32_t* offsets_dev, const void* w13_q_dev, const void* w13_bscale_dev,
+                                  const float* w13_scale_dev, const void* w2_q_dev, const void* w2_bscale_dev,
+                                  const float* w2_scale_dev, void* y_slots_dev, void* ws_dev, size_t ws_bytes,
+                                  void* stream);
+
+/* moe_layer_forward with the expert GEMMs in NVFP4 (as moe_expert_ffn_nvfp4);
+ * routing, dispatch, the combine and the bf16 router GEMM are unchanged.
+ * Stage events as moe_layer_forward: the prep stage is the token rows'
+ * quantisation, the down stage includes the activation rows'. */
+moe_status_t moe_layer_forward_nvfp4(const moe_config_t* cfg, const void* h_dev, const void* w_router_dev,
+                                     const float* bias_dev, const float* usage_dev, const void* w13_q_dev,
+                                     const void* w13_bscale_dev, const float* w13_scale_dev,
+                                     const void* w2_q_dev, const void* w2_bscale_dev, const float* w2_scale_dev,
+                                     void* out_dev, float* logits_out_dev, int32_t* assign_dev,
+                                     int32_t* slot_dev, uint8_t* flags_dev, int32_t* counts_dev, float* f_dev,
+                                     float* P_dev, void* const* stage_events, void* ws_dev, size_t ws_bytes,
+                                     void* stream);
 
 /* The router variants' logits: z = front end of cfg applied to h, for the
  * router in `router` (see moe_router_t): normalisation of each token row

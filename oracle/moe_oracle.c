@@ -159,13 +159,26 @@ typedef struct {
     const uint8_t* bs;
 } Wmat;
 
+/* The values of all 16 e2m1 and all 256 e4m3 codes (filled from the two
+ * decoders on first use, so that a weight costs two table reads). */
+static double e2m1_tab[16], e4m3_tab[256];
+static int tabs_ready = 0;
+
+static void fill_tabs(void)
+{
+    if (tabs_ready) return;
+    for (int c = 0; c < 16; ++c) e2m1_tab[c] = oracle_e2m1_value((uint8_t)c);
+    for (int c = 0; c < 256; ++c) e4m3_tab[c] = oracle_e4m3_value((uint8_t)c);
+    tabs_ready = 1;
+}
+
 static double wval(const Wmat* w, size_t r, size_t c)
 {
     if (w->bf) return (double)bf16_to_f32(w->bf[r * w->cols + c]);
     if (w->q4) {
         const size_t i = r * w->cols + c;
         const uint8_t code = (uint8_t)((w->q4[i / 2] >> (4 * (i & 1))) & 15);
-        return oracle_e2m1_value(code) * oracle_e4m3_value(w->bs[(r * w->cols + c) / 16]) * (double)w->s[r];
+        return e2m1_tab[code] * e4m3_tab[w->bs[(r * w->cols + c) / 16]] * (double)w->s[r];
     }
     return oracle_e4m3_value(w->q[r * w->cols + c]) * (double)w->s[r];
 }
@@ -623,6 +636,7 @@ int oracle_combine_rows_q4(int T, int d, int E, int k, int F, const uint16_t* h,
 {
     if (d % 16 != 0 || F % 16 != 0) return 1;
     const ExpertSet W = {NULL, NULL, NULL, q1, q3, q2, s1, s3, s2, quant_act ? 2 : 0, b1, b3, b2};
+    fill_tabs();
     return combine_rows_x(T, d, E, k, F, h, &W, assign, cw, tokens, ntok, out_rows);
 }
 
@@ -635,6 +649,7 @@ int oracle_expert_slots_q4(int T, int d, int E, int k, int F, const uint16_t* h,
 {
     if (d % 16 != 0 || F % 16 != 0) return 1;
     const ExpertSet W = {NULL, NULL, NULL, q1, q3, q2, s1, s3, s2, quant_act ? 2 : 0, b1, b3, b2};
+    fill_tabs();
     return expert_slots_x(T, d, E, k, F, h, &W, assign, perm, row0, row1, y_slots);
 }
 

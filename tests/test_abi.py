@@ -64,7 +64,7 @@ def test_workspace_size(L):
         c = _cfg(**bad)
         assert L.moe_workspace_size(ctypes.byref(c)) == 0, bad
     c = _cfg()
-    c.flags = 4   # not a defined flag
+    c.flags = 8   # not a defined flag
     assert L.moe_workspace_size(ctypes.byref(c)) == 0
     # MOE_FLAG_FP8 adds the e4m3 activation rows and the row scales
     c = _cfg()
@@ -72,11 +72,16 @@ def test_workspace_size(L):
     c.flags = moe.FLAG_FP8
     grown = L.moe_workspace_size(ctypes.byref(c))
     assert grown >= base + c.T * c.k * (c.d_ff + 8)
-    # MOE_FLAG_BACKWARD adds the padded per-expert blocks (E x C rows)
+    # MOE_FLAG_BACKWARD adds the per-expert row blocks (each expert's kept rows rounded up
+    # to 128, at most E x C' rows) and the forward's g and u
     c.flags = moe.FLAG_BACKWARD
     cap = moe.capacity(c.T, c.k, c.E, c.cf)
-    assert L.moe_workspace_size(ctypes.byref(c)) >= base + c.E * min(cap, c.T) * (8 * c.d_model + 10 * c.d_ff) + \
+    rows = min(c.E * ((min(cap, c.T) + 127) // 128 * 128), c.T * c.k + 127 * c.E)
+    assert L.moe_workspace_size(ctypes.byref(c)) >= base + rows * (8 * c.d_model + 10 * c.d_ff) + \
         c.T * c.k * 8 * c.d_ff
+    # MOE_FLAG_NVFP4 adds the 4-bit token and activation rows with their scales
+    c.flags = moe.FLAG_NVFP4
+    assert L.moe_workspace_size(ctypes.byref(c)) >= base + c.T * c.k * (c.d_model // 2 + c.d_ff // 2 + 12)
 
 
 FAKE = 0x7f0000000000  # never dereferenced: every case below fails validation first

@@ -54,7 +54,8 @@ MUTANTS = {
                        ["test_e4m3_encode_ties_and_saturation", "test_q8_activation_rounding_hand_case"]),
     "quant_scale_not_448": ([("amax / 448.0f", "amax / 256.0f")],
                             ["test_quantize_row_matches_torch", "test_q8_activation_quantisation_is_identity_on_exact_rows"]),
-    "weight_scale_of_row_0": ([("* (double)w->s[r];", "* (double)w->s[0];")],
+    "weight_scale_of_row_0": ([("return oracle_e4m3_value(w->q[r * w->cols + c]) * (double)w->s[r];",
+                                "return oracle_e4m3_value(w->q[r * w->cols + c]) * (double)w->s[0];")],
                               ["test_q8_experts_equal_bf16_experts_on_exact_weights"]),
     "token_dequant_drops_scale": ([("xf[i] = oracle_e4m3_value(codes[i]) * (double)sc;",
                                     "xf[i] = oracle_e4m3_value(codes[i]);")],
@@ -62,7 +63,8 @@ MUTANTS = {
                                    "test_q8_activation_rounding_hand_case"]),
     "token_rows_not_quantised": ([("for (int i = 0; i < d; ++i) xf[i] = oracle_e4m3_value(codes[i]) * (double)sc;",
                                    "(void)0;")], ["test_q8_activation_rounding_hand_case"]),
-    "act_not_rounded_to_bf16": ([("tmp[j] = bf16_to_f32(f32_to_bf16_rne((float)a[j]));", "tmp[j] = (float)a[j];")],
+    "act_not_rounded_to_bf16": ([("tmp[j] = bf16_to_f32(f32_to_bf16_rne((float)a[j]));\n        oracle_quantize_row(",
+                                  "tmp[j] = (float)a[j];\n        oracle_quantize_row(")],
                                 ["test_q8_activation_rounding_hand_case"]),
     "act_scale_of_token_row": ([("oracle_quantize_row(F, tmp, codes, &sc);",
                                  "for (int j = 0; j < F; ++j) codes[j] = oracle_e4m3_encode(tmp[j] / sc);")],
@@ -70,12 +72,33 @@ MUTANTS = {
                                 "test_q8_activation_rounding_hand_case"]),
     "act_max_before_swiglu": ([("        a[j] = silu(g) * u;\n    }",
                                 "        a[j] = silu(g) * u;\n        if (fabs(g) > gmax) gmax = fabs(g);\n    }"),
-                               ("    float sc = 1.0f;\n", "    float sc = 1.0f;\n    double gmax = 0.0;\n"),
+                               ("malloc((size_t)(d > F ? d : F));\n    float sc = 1.0f;\n",
+                                "malloc((size_t)(d > F ? d : F));\n    float sc = 1.0f;\n    double gmax = 0.0;\n"),
                                ("oracle_quantize_row(F, tmp, codes, &sc);",
                                 "sc = gmax > 0.0 ? (float)gmax / 448.0f : 1.0f; "
                                 "for (int j = 0; j < F; ++j) codes[j] = oracle_e4m3_encode(tmp[j] / sc);")],
                               ["test_q8_activation_quantisation_is_identity_on_exact_rows",
                                "test_q8_activation_rounding_hand_case"]),
+    # NVFP4: e2m1 elements with e4m3 scales per 16 and a row scale ([2kiu] §5.1 4-bit experts)
+    "e2m1_ties_away": ([("if (dd < bd || (dd == bd && (c & 1) == 0 && (best & 1) == 1))", "if (dd <= bd)")],
+                       ["test_e2m1_encode_is_nearest_with_ties_to_even", "test_q4_activation_quantisation_hand_case"]),
+    "nvfp4_scale_448": ([("amax / 2688.0f", "amax / 448.0f")],
+                        ["test_nvfp4_row_quantisation_is_exact_on_representable_rows",
+                         "test_nvfp4_row_quantisation_hand_case"]),
+    "nvfp4_block_scale_not_over_6": ([("const float u = t / 6.0f;", "const float u = t;")],
+                                     ["test_nvfp4_row_quantisation_is_exact_on_representable_rows",
+                                      "test_nvfp4_row_quantisation_hand_case"]),
+    "nvfp4_nibbles_swapped": ([("codes[i / 2] |= (uint8_t)(c << (4 * (i & 1)));",
+                                "codes[i / 2] |= (uint8_t)(c << (4 * (1 - (i & 1))));")],
+                              ["test_nvfp4_row_quantisation_is_exact_on_representable_rows",
+                               "test_nvfp4_row_quantisation_hand_case"]),
+    "q4_weight_blocks_of_32": ([("w->bs[(r * w->cols + c) / 16]", "w->bs[(r * w->cols + c) / 32]")],
+                               ["test_q4_experts_equal_bf16_experts_on_exact_weights"]),
+    "q4_act_not_rounded_to_bf16": ([("tmp[j] = bf16_to_f32(f32_to_bf16_rne((float)a[j]));\n        nvfp4_row(",
+                                     "tmp[j] = (float)a[j];\n        nvfp4_row(")],
+                                   ["test_q4_activation_quantisation_hand_case"]),
+    "q4_token_rows_not_quantised": ([("nvfp4_row(d, tmp, xf);", "(void)0;")],
+                                    ["test_q4_activation_quantisation_hand_case"]),
 }
 
 

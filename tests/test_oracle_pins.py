@@ -858,19 +858,22 @@ def _q4_act_case():
     both NVFP4 quantisations are exact except where stated.
     x_A: block 0 = (6, 1, 0, ...) (block scale 256, unit 1), block 1 = (10.5, 0, ...) (the
     row's largest: scale 10.5 / 2688 = 2^-8, block scale 448), block 2 = (6 * 2^-9, 2^-9,
-    0, ...) (block scale 0.5, unit 2^-9): every code gives its value back.
+    1.25 * 2^-9, 0, ...) (block scale 0.5, unit 2^-9): every code gives its value back
+    except x_34, where 1.25 units lie halfway between 1 and 1.5 and tie to 1: x'_34 = 2^-9.
     W1: 64 on column 1 in every row: g = 64 (A), 128 (B); silu(g) = g in double.
-    W3 rows: 0: 0.375 e_1; 1: (5/64) e_1 + 2^-5 e_33; 16: 10.5 e_1; the others zero.
-      A: u = (0.375, 5/64 + 2^-14, ..., 10.5 at 16), a = 64 u = (24, 5 + 2^-8, 0, ..., 672).
+    W3 rows: 0: 0.375 e_1; 1: (5/64) e_1 + 2^-5 e_33; 2: 96 e_34; 16: 10.5 e_1; others zero.
+      A: u = (0.375, 5/64 + 2^-14, 96 * 2^-9, ..., 10.5 at 16),
+         a = 64 u = (24, 5 + 2^-8, 12, 0, ..., 672).
       The activation row's largest is 672: scale 0.25; block 0 max 24: block scale 16, unit 4;
       a_1 rounds to bf16 5 (ulp 2^-5 at 4..8), 5 / 4 = 1.25 is halfway between the e2m1
-      values 1 and 1.5 and ties to 1: a'_1 = 4 (unrounded, 1.2509... -> 1.5: 6).  a'_0 = 24,
-      a'_16 = 672 exactly.  B: g and u double, so a and its scale quadruple (a'_1 = 16).
-    W2 rows: 0: e_1; 1: e_0; 2: 2^-4 e_16; the others zero.
-      y_A = (4, 24, 42, 0, ...), y_B = (16, 96, 168, 0, ...)."""
+      values 1 and 1.5 and ties to 1: a'_1 = 4 (unrounded, 1.2509... -> 1.5: 6).  a'_2 = 12
+      (3 units; with the unquantised x_34 it would be 15 -> 3.75 units -> 4: 16).  a'_0 = 24,
+      a'_16 = 672 exactly.  B: g and u double, so a and its scale quadruple.
+    W2 rows: 0: e_1; 1: e_0; 2: 2^-4 e_16; 3: e_2; the others zero.
+      y_A = (4, 24, 42, 12, 0, ...), y_B = (16, 96, 168, 48, 0, ...)."""
     d, F = 48, 32
     x = np.zeros((2, d))
-    x[0, [0, 1, 16, 32, 33]] = [6, 1, 10.5, 6 * 2.0 ** -9, 2.0 ** -9]
+    x[0, [0, 1, 16, 32, 33, 34]] = [6, 1, 10.5, 6 * 2.0 ** -9, 2.0 ** -9, 1.25 * 2.0 ** -9]
     x[1] = 2 * x[0]
 
     def pack(vals, codes_for, bscale_vals, row_scales):
@@ -894,17 +897,20 @@ def _q4_act_case():
     w3[0, 1] = 0.375
     w3[1, 1] = 5 / 64
     w3[1, 33] = 2.0 ** -5
+    w3[2, 34] = 96
     w3[16, 1] = 10.5
     w2 = np.zeros((d, F))
     w2[0, 1] = 1
     w2[1, 0] = 1
     w2[2, 16] = 2.0 ** -4
+    w2[3, 2] = 1
     # block scales and row scales that make every weight an e2m1 value
     w1q = pack(w1, enc, [[64.0] * 3] * F, [0.25] * F)        # 64 = 4 * 64 * 0.25
     w3_b = [[1.0] * 3 for _ in range(F)]
     w3_s = [1.0] * F
     w3_b[0] = [0.25, 1, 1]                     # 0.375 = 1.5 * 0.25
     w3_b[1], w3_s[1] = [5.0, 1, 2.0], 2.0 ** -6     # 5/64 = 1 * 5 * 2^-6; 2^-5 = 1 * 2 * 2^-6
+    w3_b[2] = [1, 1, 16.0]                     # 96 = 6 * 16
     w3_b[16] = [1.75, 1, 1]                    # 10.5 = 6 * 1.75
     w3q = pack(w3, enc, w3_b, w3_s)
     w2_b = [[1.0] * 2 for _ in range(d)]
@@ -912,15 +918,16 @@ def _q4_act_case():
     w2_b[2], w2_s[2] = [1, 1.0], 2.0 ** -4
     w2q = pack(w2, enc, w2_b, w2_s)
     want = np.zeros((2, d), np.float32)
-    want[0, :3] = [4, 24, 42]
-    want[1, :3] = [16, 96, 168]
+    want[0, :4] = [4, 24, 42, 12]
+    want[1, :4] = [16, 96, 168, 48]
     return bf16(x), w1q, w3q, w2q, want
 
 
 def test_q4_activation_quantisation_hand_case():
     """The bf16 rounding of the activation before its NVFP4 quantisation decides a code
-    (the tie at 1.25 in units of 4), through the token-order and slot-order functions;
-    quantising without the rounding would give a'_1 = 6."""
+    (the tie at 1.25 in units of 4), and the token row's quantisation decides another
+    (x_34), through the token-order and slot-order functions; quantising without the
+    rounding would give a'_1 = 6, without the token quantisation a'_2 = 16."""
     h, w1, w3, w2, want = _q4_act_case()
     assign = np.array([[0], [0]], np.int32)
     cw = np.ones((2, 1), np.float32)

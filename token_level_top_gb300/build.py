@@ -20,8 +20,8 @@ SRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libmoe.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "moe.h")
-UNITS = ["api.cu", "route.cu", "dispatch.cu", "gemm.cu", "bwd_gemm.cu", "misc.cu", "router.cu", "backward.cu",
-         "noalloc.cu"]
+UNITS = ["api.cu", "route.cu", "dispatch.cu", "gemm.cu", "bwd_gemm.cu", "nvfp4.cu", "misc.cu", "router.cu",
+         "backward.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]

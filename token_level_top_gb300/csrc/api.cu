@@ -27,7 +27,7 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 moe_status_t check_config(const moe_config_t* c, bool need_ff)
 {
     if (!c) return MOE_ERR_INVALID_ARG;
-    if ((c->flags & ~(MOE_FLAG_FP8 | MOE_FLAG_BACKWARD)) != 0) return MOE_ERR_INVALID_ARG;
+    if ((c->flags & ~(MOE_FLAG_FP8 | MOE_FLAG_BACKWARD | MOE_FLAG_NVFP4)) != 0) return MOE_ERR_INVALID_ARG;
     if (c->T < 0 || c->E <= 0 || c->k <= 0) return MOE_ERR_INVALID_ARG;
     if (c->k > c->E) return MOE_ERR_INVALID_ARG;
     if (c->capacity < 0) return MOE_ERR_INVALID_ARG;
@@ -190,7 +190,15 @@ bool layout_for(const moe_config_t& c, WsLayout* L)
         w.act_q = take(T * k * F);
         w.x_scale = take(T * k * 4);
         w.act_scale = take(T * k * 4);
-        w.act_amax = take(T * k * 4);
+    }
+    if (c.flags & (MOE_FLAG_FP8 | MOE_FLAG_NVFP4)) w.act_amax = take(T * k * 4);
+    if (c.flags & MOE_FLAG_NVFP4) {
+        w.x4 = take(T * k * d / 2);
+        w.x4_sf = take(T * k * static_cast<size_t>(nvfp4_sf_stride(static_cast<int>(d))));
+        w.x4_scale = take(T * k * 4);
+        w.a4 = take(T * k * F / 2);
+        w.a4_sf = take(T * k * static_cast<size_t>(nvfp4_sf_stride(static_cast<int>(F))));
+        w.a4_scale = take(T * k * 4);
     }
     if (c.router_norm != MOE_ROUTER_NORM_NONE) w.xn = take(T * d * 2);
     if (c.router_hidden > 0) w.zr = take(T * E * 4);
@@ -405,13 +413,18 @@ GemmLaunch expert_gemm(const moe_config_t& c, const WsLayout& L, int kind, void*
 namespace moe {
 namespace {
 
-// Expert weights: bf16, or e4m3 with one fp32 scale per weight row (s13, s2 non-NULL).
+// Expert weights: bf16, e4m3 with one fp32 scale per weight row (s13, s2
+// non-NULL), or NVFP4 (b13, b2 non-NULL too: e2m1 codes with e4m3 scales per
+// 16 elements and an fp32 scale per row; W13 in the 128-row packing).
 struct ExpertWeights {
     const void* w13;
     const void* w2;
     const float* s13;
     const float* s2;
-    bool fp8() const { return s13 != nullptr; }
+    const void* b13 = nullptr;
+    const void* b2 = nullptr;
+    bool fp8() const { return s13 != nullptr && b13 == nullptr; }
+    bool fp4() const { return b13 != nullptr; }
     void apply(GemmLaunch& g, bool gate_up) const
     {
         g.b_ptr = gate_up ? w13 : w2;
@@ -419,6 +432,17 @@ struct ExpertWeights {
         g.b_scale = gate_up ? s13 : s2;
     }
 };
+
+// NVFP4 weights: every pointer given, the workspace sized for them, and the
+// shapes the 4-bit GEMM takes (d a multiple of 128, rows of at most 16384).
+moe_status_t check_fp4(const moe_config_t& c, const ExpertWeights& W)
+{
+    if (!W.fp4()) return MOE_OK;
+    if (!W.s13 || !W.s2 || !W.b2 || !(c.flags & MOE_FLAG_NVFP4)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(W.b13, 16) || !aligned(W.b2, 16)) return MOE_ERR_MISALIGNED;
+    if (c.d_model % 128 != 0 || c.d_model > 16384 || c.d_ff > 16384) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
 
 // The two expert GEMMs over the kept slots: gather (and, with e4m3 weights,
 // quantise per row) the token rows, gate-up + SwiGLU into act, (quantise act
@@ -431,6 +455,51 @@ moe_status_t run_experts(const moe_config_t& c, const WsLayout& L, const void* h
     void* xg = ws_at<void>(ws, L.xg);
     void* act = ws_at<void>(ws, L.act);
     const int32_t* kept = offsets + c.E;   // device count of kept rows
+    if (W.fp4()) {
+        // token rows of the kept slots quantised per row; gate-up + SwiGLU; the
+        // activation rows quantised per row (their maxima from the gate-up); down
+        float* amax = ws_at<float>(ws, L.act_amax);
+        if (launch_quantize_nvfp4(static_cast<long long>(rows), c.d_model, h, perm, c.k, 0, kept, nullptr,
+                                  ws_at<void>(ws, L.x4), ws_at<void>(ws, L.x4_sf), ws_at<float>(ws, L.x4_scale),
+                                  amax, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (ev) ev->mark(3);
+        F4Launch g{};
+        g.kind = GK_GATEUP;
+        g.E = c.E;
+        g.T = c.T;
+        g.topk = c.k;
+        g.d = c.d_model;
+        g.F = c.d_ff;
+        g.a_codes = ws_at<void>(ws, L.x4);
+        g.a_sf = ws_at<void>(ws, L.x4_sf);
+        g.a_scale = ws_at<float>(ws, L.x4_scale);
+        g.b_codes = W.w13;
+        g.b_sf = W.b13;
+        g.b_scale = W.s13;
+        g.offsets = offsets;
+        g.act = act;
+        g.act_amax = amax;
+        g.status = ws_at<int>(ws, L.status);
+        g.budget = kSpinBudget;
+        if (launch_gemm_nvfp4(g, s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (ev) ev->mark(4);
+        if (launch_quantize_nvfp4(static_cast<long long>(rows), c.d_ff, act, nullptr, 1, 0, kept, amax,
+                                  ws_at<void>(ws, L.a4), ws_at<void>(ws, L.a4_sf), ws_at<float>(ws, L.a4_scale),
+                                  nullptr, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        g.kind = GK_DOWN_SLOTS;
+        g.a_codes = ws_at<void>(ws, L.a4);
+        g.a_sf = ws_at<void>(ws, L.a4_sf);
+        g.a_scale = ws_at<float>(ws, L.a4_scale);
+        g.b_codes = W.w2;
+        g.b_sf = W.b2;
+        g.b_scale = W.s2;
+        g.act = nullptr;
+        g.act_amax = nullptr;
+        g.y_slots = y_slots;
+        return cuda_status(launch_gemm_nvfp4(g, s));
+    }
     if (W.fp8()) {
         if (launch_quantize_fp8(static_cast<long long>(rows), c.d_model, h, perm, c.k, kept, xg,
                                 ws_at<float>(ws, L.x_scale), s, nullptr, ws_at<float>(ws, L.act_amax)) !=
@@ -479,6 +548,8 @@ moe_status_t expert_ffn_impl(const moe_config_t* cfg, const void* h, const int32
     if (!h || !perm || !offsets || !w13 || !w2 || !y_slots) return MOE_ERR_INVALID_ARG;
     if (W.fp8() && (!W.s2 || !(cfg->flags & MOE_FLAG_FP8) || cfg->d_model % 128 != 0))
         return W.s2 && (cfg->flags & MOE_FLAG_FP8) ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+    st = check_fp4(*cfg, W);
+    if (st != MOE_OK) return st;
     if (!aligned(h, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(y_slots, 16))
         return MOE_ERR_MISALIGNED;
     WsLayout L;
@@ -501,6 +572,8 @@ moe_status_t layer_forward_impl(const moe_config_t* cfg, const void* h, const Ro
     if (st != MOE_OK) return st;
     if (W.fp8() && (!(cfg->flags & MOE_FLAG_FP8) || cfg->d_model % 128 != 0))
         return (cfg->flags & MOE_FLAG_FP8) ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID_ARG;
+    st = check_fp4(*cfg, W);
+    if (st != MOE_OK) return st;
     if (!h || !w13 || !w2 || !out || !router_args_ok(*cfg, R)) return MOE_ERR_INVALID_ARG;
     if (!aligned(h, 16) || !router_aligned(R) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16))
         return MOE_ERR_MISALIGNED;
@@ -718,6 +791,58 @@ moe_status_t moe_quantize_fp8(int64_t rows, int32_t cols, const void* w, void* q
     if (!aligned(w, 16) || !aligned(q, 8)) return MOE_ERR_MISALIGNED;
     return cuda_status(
         launch_quantize_fp8(rows, cols, w, nullptr, 1, nullptr, q, scales, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t moe_nvfp4_sf_stride(int32_t cols) { return cols > 0 ? nvfp4_sf_stride(cols) : 0; }
+
+moe_status_t moe_quantize_nvfp4(int64_t rows, int32_t cols, const void* w, void* codes, void* bscale,
+                                float* scales, void* stream)
+{
+    if (rows < 0 || cols <= 0 || cols % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if (cols > 16384) return MOE_ERR_UNSUPPORTED;
+    if (rows == 0) return MOE_OK;
+    if (!w || !codes || !bscale || !scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(bscale, 16)) return MOE_ERR_MISALIGNED;
+    return cuda_status(launch_quantize_nvfp4(rows, cols, w, nullptr, 1, 0, nullptr, nullptr, codes, bscale, scales,
+                                             nullptr, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_quantize_w13_nvfp4(int32_t E, int32_t d_ff, int32_t d_model, const void* w13, void* codes,
+                                    void* bscale, float* scales, void* stream)
+{
+    if (E <= 0 || d_ff <= 0 || d_ff % 128 != 0 || d_model <= 0 || d_model % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if (d_model > 16384) return MOE_ERR_UNSUPPORTED;
+    if (!w13 || !codes || !bscale || !scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned(w13, 16) || !aligned(codes, 16) || !aligned(bscale, 16)) return MOE_ERR_MISALIGNED;
+    return cuda_status(launch_quantize_nvfp4(static_cast<long long>(E) * 2 * d_ff, d_model, w13, nullptr, 1, d_ff,
+                                             nullptr, nullptr, codes, bscale, scales, nullptr,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_expert_ffn_nvfp4(const moe_config_t* cfg, const void* h, const int32_t* perm,
+                                  const int32_t* offsets, const void* w13_q, const void* w13_bscale,
+                                  const float* w13_scale, const void* w2_q, const void* w2_bscale,
+                                  const float* w2_scale, void* y_slots, void* ws, size_t ws_bytes, void* stream)
+{
+    if (!w13_scale || !w2_scale || !w13_bscale || !w2_bscale) return MOE_ERR_INVALID_ARG;
+    return expert_ffn_impl(cfg, h, perm, offsets,
+                           ExpertWeights{w13_q, w2_q, w13_scale, w2_scale, w13_bscale, w2_bscale}, y_slots, ws,
+                           ws_bytes, stream);
+}
+
+moe_status_t moe_layer_forward_nvfp4(const moe_config_t* cfg, const void* h, const void* w_router,
+                                     const float* bias, const float* usage, const void* w13_q,
+                                     const void* w13_bscale, const float* w13_scale, const void* w2_q,
+                                     const void* w2_bscale, const float* w2_scale, void* out, float* logits_out,
+                                     int32_t* assign, int32_t* slot, uint8_t* flags, int32_t* counts, float* f,
+                                     float* P, void* const* stage_events, void* ws, size_t ws_bytes, void* stream)
+{
+    if (!w13_scale || !w2_scale || !w13_bscale || !w2_bscale) return MOE_ERR_INVALID_ARG;
+    if (cfg && (cfg->router_norm != MOE_ROUTER_NORM_NONE || cfg->router_hidden != 0))
+        return MOE_ERR_INVALID_ARG;
+    return layer_forward_impl(cfg, h, RouterWeights{w_router, nullptr, bias, nullptr, nullptr}, usage,
+                              ExpertWeights{w13_q, w2_q, w13_scale, w2_scale, w13_bscale, w2_bscale}, out,
+                              logits_out, assign, slot, flags, counts, f, P, stage_events, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const void* y_slots, const int32_t* assign,

@@ -31,6 +31,9 @@ struct WsLayout {
     // MOE_FLAG_FP8: e4m3 activation rows of the down GEMM and the row scales
     // of both GEMMs' activations (the gate-up codes reuse the xg region)
     size_t act_q = 0, x_scale = 0, act_scale = 0, act_amax = 0;
+    // MOE_FLAG_NVFP4: e2m1 codes, block scales and row scales of the token rows
+    // (gate-up input) and of the activation rows (down input)
+    size_t x4 = 0, x4_sf = 0, x4_scale = 0, a4 = 0, a4_sf = 0, a4_scale = 0;
     size_t xn = 0;     // router input after normalisation [T, d] bf16 (router_norm != 0)
     size_t bwd = 0;    // backward scratch (MOE_FLAG_BACKWARD)
     size_t gu = 0;     // g and u of the kept rows, kept by the forward for the backward [T*k, 2F] fp32
@@ -151,6 +154,36 @@ struct GemmLaunch {
     long long budget;
 };
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
+// NVFP4 (nvfp4.cu): e2m1 codes packed two per byte, e4m3 scales per 16
+// consecutive elements (rows of them padded to nvfp4_sf_stride bytes), an fp32
+// scale per row.  launch_quantize_nvfp4 quantises rows [0, rows) of a bf16
+// matrix [.., cols]: row r reads source row perm[r] / k (perm given), or the
+// W13 row that the 128-row packing puts at r (w13_F = d_ff > 0), or r; rows
+// from *nrows on are skipped; amax_in gives each row's max |value|;
+// zero_rows, when given, gets 0 at each quantised row.  cols <= 16384, a
+// multiple of 32.
+int nvfp4_sf_stride(int cols);
+cudaError_t launch_quantize_nvfp4(long long rows, int cols, const void* w, const int32_t* perm, int k,
+                                  int w13_F, const int32_t* nrows, const float* amax_in, void* codes,
+                                  void* bscale, float* scales, float* zero_rows, cudaStream_t s);
+struct F4Launch {
+    int kind;                 // GK_GATEUP or GK_DOWN_SLOTS
+    int E, T, topk, d, F;
+    const void* a_codes;      // gate-up: token rows [T*k, d/2]; down: activation rows [T*k, F/2]
+    const void* a_sf;         // their block scales [T*k, nvfp4_sf_stride(K)]
+    const float* a_scale;     // their row scales [T*k]
+    const void* b_codes;      // W13 [E*2F, d/2] (128-row packing) or W2 [E*d, F/2]
+    const void* b_sf;
+    const float* b_scale;
+    const int32_t* offsets;
+    void* act;                // gate-up output [T*k, F] bf16
+    float* act_amax;          // gate-up: atomically maxed with each act row's max |bf16 value|
+    void* y_slots;            // down output [T*k, d] bf16
+    int* status;
+    long long budget;
+};
+cudaError_t launch_gemm_nvfp4(const F4Launch& g, cudaStream_t s);
+
 // Tensor map of a row-major bf16 matrix [rows, cols]: boxes of box_rows x 64
 // columns (128 bytes), 128-byte swizzle; zero fill outside the matrix.
 bool encode_bf16_map(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);

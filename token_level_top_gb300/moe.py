@@ -75,6 +75,7 @@ class Config:
 
 FLAG_FP8 = 1   # MOE_FLAG_FP8
 FLAG_BACKWARD = 2   # MOE_FLAG_BACKWARD
+FLAG_NVFP4 = 4   # MOE_FLAG_NVFP4
 NORM_NONE, NORM_LAYER, NORM_L2 = 0, 1, 2   # MOE_ROUTER_NORM_*
 
 
@@ -120,6 +121,11 @@ _SIGS = {
     "moe_quantize_fp8": (I32, [ctypes.c_int64, I32, P, P, P, P]),
     "moe_expert_ffn_fp8": (I32, [CFG, P, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_layer_forward_fp8": (I32, [CFG] + [P] * 18 + [SZ, P]),
+    "moe_nvfp4_sf_stride": (I32, [I32]),
+    "moe_quantize_nvfp4": (I32, [ctypes.c_int64, I32, P, P, P, P, P]),
+    "moe_quantize_w13_nvfp4": (I32, [I32, I32, I32, P, P, P, P, P]),
+    "moe_expert_ffn_nvfp4": (I32, [CFG] + [P] * 10 + [P, SZ, P]),
+    "moe_layer_forward_nvfp4": (I32, [CFG] + [P] * 20 + [SZ, P]),
     "moe_router_logits": (I32, [CFG, P, RTR, P, P, SZ, P]),
     "moe_layer_backward": (I32, [CFG] + [P] * 12 + [SZ, P]),
     "moe_layer_forward_router": (I32, [CFG, P, RTR] + [P] * 15 + [SZ, P]),
@@ -213,7 +219,41 @@ def quantize_fp8(w: torch.Tensor):
 
 def _fp8(w):
     """Expert weights as (q, scales) from quantize_fp8, or None for bf16 weights."""
-    return w if isinstance(w, tuple) else None
+    return w if isinstance(w, tuple) and len(w) == 2 else None
+
+
+def _fp4(w):
+    """Expert weights as (codes, block scales, row scales) from quantize_nvfp4, or None."""
+    return w if isinstance(w, tuple) and len(w) == 3 else None
+
+
+def quantize_nvfp4(w: torch.Tensor):
+    """NVFP4 quantisation (moe_quantize_nvfp4) of a bf16 tensor [..., cols]: returns
+    (codes uint8 [..., cols/2], block scales uint8 [..., moe_nvfp4_sf_stride(cols)],
+    row scales fp32 [rows])."""
+    w = w.contiguous()
+    cols = w.shape[-1]
+    rows = w.numel() // cols
+    sfs = int(lib().moe_nvfp4_sf_stride(cols))
+    q = torch.empty(*w.shape[:-1], cols // 2, dtype=torch.uint8, device=w.device)
+    b = torch.empty(*w.shape[:-1], sfs, dtype=torch.uint8, device=w.device)
+    sc = torch.empty(rows, dtype=torch.float32, device=w.device)
+    _check(lib().moe_quantize_nvfp4(rows, cols, _p(w), _p(q), _p(b), _p(sc), _stream()), "moe_quantize_nvfp4")
+    return q, b, sc
+
+
+def quantize_w13_nvfp4(w13: torch.Tensor):
+    """moe_quantize_w13_nvfp4: W13 [E, 2F, d] bf16 (moe_pack_w13 layout) to NVFP4 in
+    the 4-bit path's 128-row packing (64 W1 rows, then the matching 64 W3 rows)."""
+    w13 = w13.contiguous()
+    E, F2, d = w13.shape
+    sfs = int(lib().moe_nvfp4_sf_stride(d))
+    q = torch.empty(E, F2, d // 2, dtype=torch.uint8, device=w13.device)
+    b = torch.empty(E, F2, sfs, dtype=torch.uint8, device=w13.device)
+    sc = torch.empty(E * F2, dtype=torch.float32, device=w13.device)
+    _check(lib().moe_quantize_w13_nvfp4(E, F2 // 2, d, _p(w13), _p(q), _p(b), _p(sc), _stream()),
+           "moe_quantize_w13_nvfp4")
+    return q, b, sc
 
 
 def route(cfg: Config, ws, h=None, wr=None, bias=None, usage=None, logits_in=None):
@@ -269,7 +309,11 @@ def dispatch(cfg: Config, ws, scores):
 def expert_ffn(cfg: Config, ws, h, perm, offsets, w13, w2):
     y = torch.empty(max(cfg.T * cfg.k, 1), cfg.d_model, dtype=torch.bfloat16, device=ws.device)
     c = cfg.c()
-    if _fp8(w13):
+    if _fp4(w13):
+        (q13, b13, s13), (q2, b2, s2) = w13, w2
+        st = lib().moe_expert_ffn_nvfp4(ctypes.byref(c), _p(h), _p(perm), _p(offsets), _p(q13), _p(b13),
+                                        _p(s13), _p(q2), _p(b2), _p(s2), _p(y), _p(ws), ws.numel(), _stream())
+    elif _fp8(w13):
         (q13, s13), (q2, s2) = w13, w2
         st = lib().moe_expert_ffn_fp8(ctypes.byref(c), _p(h), _p(perm), _p(offsets), _p(q13), _p(s13),
                                       _p(q2), _p(s2), _p(y), _p(ws), ws.numel(), _stream())
@@ -293,8 +337,9 @@ def layer_forward(cfg: Config, ws, h, wr, w13, w2, bias=None, usage=None, aux=Fa
                   stage_events=None, out=None):
     """The fused layer.  Returns out [T, d] bf16 (and a dict of routing outputs when aux).
     wr: the router weight [E, d] bf16, or a Router (any router variant of cfg; its
-    bias is the router's, so bias stays None).  w13 / w2: bf16 tensors, or
-    (q, scales) pairs from quantize_fp8 for e4m3 weights."""
+    bias is the router's, so bias stays None).  w13 / w2: bf16 tensors, (q, scales)
+    pairs from quantize_fp8 for e4m3 weights, or (codes, block scales, row scales)
+    from quantize_w13_nvfp4 / quantize_nvfp4 for NVFP4 weights."""
     dev = ws.device
     T, E, k = cfg.T, cfg.E, cfg.k
     if out is None:
@@ -321,12 +366,18 @@ def layer_forward(cfg: Config, ws, h, wr, w13, w2, bias=None, usage=None, aux=Fa
     tail = (_p(out), g("logits"), g("assign"), g("slot"), g("flags"), g("counts"), g("f"), g("P"), evp,
             _p(ws), ws.numel(), _stream())
     if isinstance(wr, Router):
+        if _fp4(w13):
+            raise ValueError("the router variants take bf16 or e4m3 experts")
         if bias is not None:
             raise ValueError("the router's bias belongs in the Router")
         (q13, s13), (q2, s2) = (w13, w2) if _fp8(w13) else ((w13, None), (w2, None))
         r = wr.c()
         st = lib().moe_layer_forward_router(ctypes.byref(c), _p(h), ctypes.byref(r), _p(usage), _p(q13),
                                             _p(s13), _p(q2), _p(s2), *tail)
+    elif _fp4(w13):   # NVFP4 expert weights: (codes, block scales, row scales)
+        (q13, b13, s13), (q2, b2, s2) = w13, w2
+        st = lib().moe_layer_forward_nvfp4(ctypes.byref(c), _p(h), _p(wr), _p(bias), _p(usage), _p(q13),
+                                           _p(b13), _p(s13), _p(q2), _p(b2), _p(s2), *tail)
     elif _fp8(w13):   # e4m3 expert weights: (q, scales) pairs from quantize_fp8
         (q13, s13), (q2, s2) = w13, w2
         st = lib().moe_layer_forward_fp8(ctypes.byref(c), _p(h), _p(wr), _p(bias), _p(usage), _p(q13),

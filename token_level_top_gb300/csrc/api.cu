@@ -482,6 +482,7 @@ moe_status_t run_experts(const moe_config_t& c, const WsLayout& L, const void* h
         g.act_amax = amax;
         g.status = ws_at<int>(ws, L.status);
         g.budget = kSpinBudget;
+        g.rows_cap = capacity_of(c);
         if (launch_gemm_nvfp4(g, s) != cudaSuccess) return MOE_ERR_CUDA;
         if (ev) ev->mark(4);
         if (launch_quantize_nvfp4(static_cast<long long>(rows), c.d_ff, act, nullptr, 1, 0, kept, amax,

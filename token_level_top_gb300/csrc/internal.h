@@ -179,6 +179,7 @@ struct F4Launch {
     void* act;                // gate-up output [T*k, F] bf16
     float* act_amax;          // gate-up: atomically maxed with each act row's max |bf16 value|
     void* y_slots;            // down output [T*k, d] bf16
+    long long rows_cap;       // most rows an expert can hold (the capacity C), or 0 if unknown
     int* status;
     long long budget;
 };

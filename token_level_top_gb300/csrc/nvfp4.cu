@@ -189,8 +189,10 @@ __global__ void __launch_bounds__(kQThreads) quantize_nvfp4_kernel(
 struct F4Params {
     int kind, E, T, topk, d, F;
     int kb_total;   // K / 256 (stages of 128-byte rows), rounded up
+    int bn;         // N tile: 128 for the gate-up; for the down 64..128 (a multiple of 16)
     int n_tiles;    // N tiles per expert
     int stages;
+    int b_policy;   // 1: weight loads evict_first (every expert holds at most one row tile)
     const float* a_scale;   // per A row (slot order)
     const float* b_scale;   // per weight row
     float* act_amax;
@@ -202,6 +204,17 @@ struct F4Params {
 };
 
 __device__ __forceinline__ float silu_f4(float x) { return x / (1.0f + __expf(-x)); }
+
+// 16 consecutive fp32 TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
 
 // 16 consecutive TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
@@ -260,9 +273,14 @@ __device__ __forceinline__ F4Tile f4_decode(const F4Params& p, int tile, const i
     return t;
 }
 
+// tmA / tmSA: the A codes and block scales in boxes of 128 rows; tmA32 / tmSA32
+// the same in boxes of 32 rows, for tiles whose expert has at most 32 rows there
+// (decode): the MMA still spans 128 rows, the rows past the box hold stale data
+// and their results are not stored.
 __global__ void __launch_bounds__(kF4Threads, 1)
     moe_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                          const __grid_constant__ CUtensorMap tmA32, const __grid_constant__ CUtensorMap tmSA32,
                           const F4Params p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -287,6 +305,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmSA);
         tma_prefetch_desc(&tmSB);
+        tma_prefetch_desc(&tmA32);
+        tma_prefetch_desc(&tmSA32);
         for (int i = 0; i < stages; ++i) {
             mbar_init(smem_u32(&full_bar[i]), 1);
             mbar_init(smem_u32(&empty_bar[i]), 1);
@@ -325,7 +345,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
     const int total = s_start[p.E];
-    const uint32_t idesc = idesc_nvfp4(kBM, kF4BN);
+    const uint32_t idesc = idesc_nvfp4(kBM, p.bn);
     bool ok = true;
 
     if (warp == 0) {
@@ -333,10 +353,13 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
+        const uint64_t pol_b = l2_policy_evict_first();
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
             const F4Tile t = f4_decode(p, tile, s_start, s_offs);
             const int arow = s_offs[t.e] + t.m * kBM;
-            const int brow = (p.kind == GK_GATEUP ? t.e * 2 * p.F : t.e * p.d) + t.n * kF4BN;
+            const int brow = (p.kind == GK_GATEUP ? t.e * 2 * p.F : t.e * p.d) + t.n * p.bn;
+            const bool few = s_offs[t.e + 1] - arow <= 32;   // the tile's rows fit a 32-row box
+            const uint32_t bytes = (few ? 32u : 128u) * (128u + 16u) + static_cast<uint32_t>(p.bn) * (128u + 16u);
             for (int kb = 0; kb < p.kb_total; ++kb) {
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, p.budget))) {
                     ok = false;
@@ -344,12 +367,18 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                 }
                 if (lane == 0) {
                     const uint32_t fb = smem_u32(&full_bar[stage]);
-                    mbar_arrive_expect_tx(fb, kF4Stage);
+                    mbar_arrive_expect_tx(fb, bytes);
                     uint8_t* st = smem + stage * kF4Stage;
-                    tma_load_2d(smem_u32(st), &tmA, kb * 128, arow, fb);
-                    tma_load_2d(smem_u32(st + kF4ABytes), &tmB, kb * 128, brow, fb);
-                    tma_load_2d(smem_u32(st + kF4ABytes + kF4BBytes), &tmSA, kb * 16, arow, fb);
-                    tma_load_2d(smem_u32(st + kF4ABytes + kF4BBytes + kF4SfBytes), &tmSB, kb * 16, brow, fb);
+                    tma_load_2d(smem_u32(st), few ? &tmA32 : &tmA, kb * 128, arow, fb);
+                    tma_load_2d(smem_u32(st + kF4ABytes + kF4BBytes), few ? &tmSA32 : &tmSA, kb * 16, arow, fb);
+                    if (p.b_policy) {
+                        tma_load_2d_hint(smem_u32(st + kF4ABytes), &tmB, kb * 128, brow, fb, pol_b);
+                        tma_load_2d_hint(smem_u32(st + kF4ABytes + kF4BBytes + kF4SfBytes), &tmSB, kb * 16, brow,
+                                         fb, pol_b);
+                    } else {
+                        tma_load_2d(smem_u32(st + kF4ABytes), &tmB, kb * 128, brow, fb);
+                        tma_load_2d(smem_u32(st + kF4ABytes + kF4BBytes + kF4SfBytes), &tmSB, kb * 16, brow, fb);
+                    }
                 }
                 __syncwarp();
                 issued_mask |= 1u << stage;
@@ -380,7 +409,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kF4BN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kF4BN);   // fixed 128-column slots
                 for (int kb = 0; kb < p.kb_total; ++kb) {
                     if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.budget) ||
                         !mbar_wait(smem_u32(&sf_bar[stage]), phase, p.budget)) {
@@ -462,9 +491,11 @@ __global__ void __launch_bounds__(kF4Threads, 1)
             // the tile's weight-row scales while its MMAs run
             epilogue_sync();
             {
-                const long long wrow = (p.kind == GK_GATEUP ? static_cast<long long>(t.e) * 2 * p.F
-                                                            : static_cast<long long>(t.e) * p.d) + t.n * kF4BN + et;
-                s_bsc[et] = __ldg(p.b_scale + wrow);
+                // columns past the expert's weight rows (the down GEMM's last tile) read no scale
+                const int col = t.n * p.bn + et;
+                const int wrows = p.kind == GK_GATEUP ? 2 * p.F : p.d;
+                s_bsc[et] = (et < p.bn && col < wrows) ? __ldg(p.b_scale + static_cast<long long>(t.e) * wrows + col)
+                                                       : 0.0f;
             }
             const bool got = epilogue_all(mbar_wait(smem_u32(&tfull_bar[b]), acc_par, p.budget));
             if (!got) {
@@ -509,10 +540,15 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                     atomicMax(reinterpret_cast<unsigned int*>(p.act_amax + off + ri),
                               __float_as_uint(__bfloat162float(__float2bfloat16_rn(rmax))));
             } else {
-                const int col0 = t.n * kF4BN;
+                const int col0 = t.n * p.bn;
+                const int ncols = min(p.bn, p.d - col0);   // a multiple of 16
                 __nv_bfloat16* dst = p.y_slots + static_cast<size_t>(off + ri) * p.d + col0;
-                for (int c = 0; c < kF4BN; c += 32) {
-                    tmem_ld32(taddr + c, v);
+                for (int c = 0; c < ncols; c += 32) {
+                    const int w = min(32, ncols - c);       // 32, or 16 for the last piece
+                    if (w == 32)
+                        tmem_ld32(taddr + c, v);
+                    else
+                        tmem_ld16(taddr + c, v);
                     tmem_ld_wait(v);
                     if (valid) {
                         uint32_t pk[16];
@@ -523,7 +559,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                         uint4* d4 = reinterpret_cast<uint4*>(dst + c);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                            if (4 * j < w / 2) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                     }
                 }
             }
@@ -602,16 +638,37 @@ cudaError_t launch_gemm_nvfp4(const F4Launch& g, cudaStream_t s)
     const int K = g.kind == GK_GATEUP ? g.d : g.F;       // reduction length
     const int N = g.kind == GK_GATEUP ? 2 * g.F : g.d;   // weight rows of one expert
     if (K % 32 != 0 || N % kF4BN != 0) return cudaErrorInvalidValue;
+    const int sms = num_sms();
     p.kb_total = (K + 255) / 256;
-    p.n_tiles = N / kF4BN;
+    p.bn = kF4BN;
+    // When no expert holds more than one row tile, each weight tile is read by one
+    // tile only: its loads go first out of L2, and the down GEMM's column tile (a
+    // multiple of 16, 64..128) is the one that needs the fewest passes over the
+    // SMs times its width.
+    const bool one_tile = g.rows_cap > 0 && std::min<long long>(g.rows_cap, static_cast<long long>(g.T)) <= kBM;
+    p.b_policy = one_tile ? 1 : 0;
+    if (one_tile && g.kind != GK_GATEUP) {
+        const long long mt = std::min<long long>(g.E, static_cast<long long>(g.T) * g.topk);
+        long long best = -1;
+        for (int bn = kF4BN; bn >= 64; bn -= 16) {
+            const long long cost = (mt * ((N + bn - 1) / bn) + sms - 1) / sms * bn;
+            if (best < 0 || cost < best) {
+                best = cost;
+                p.bn = bn;
+            }
+        }
+    }
+    p.n_tiles = (N + p.bn - 1) / p.bn;
     const uint64_t arows = static_cast<uint64_t>(g.T) * g.topk;
     const uint64_t brows = static_cast<uint64_t>(g.E) * N;
-    CUtensorMap tmA, tmB, tmSA, tmSB;
+    CUtensorMap tmA, tmB, tmSA, tmSB, tmA32, tmSA32;
     const int sfs = nvfp4_sf_stride(K);
     if (!make_byte_map(&tmA, g.a_codes, arows, K / 2, K / 2, kBM, 128) ||
-        !make_byte_map(&tmB, g.b_codes, brows, K / 2, K / 2, kF4BN, 128) ||
+        !make_byte_map(&tmB, g.b_codes, brows, K / 2, K / 2, p.bn, 128) ||
         !make_byte_map(&tmSA, g.a_sf, arows, K / 16, sfs, kBM, 16) ||
-        !make_byte_map(&tmSB, g.b_sf, brows, K / 16, sfs, kF4BN, 16))
+        !make_byte_map(&tmSB, g.b_sf, brows, K / 16, sfs, p.bn, 16) ||
+        !make_byte_map(&tmA32, g.a_codes, arows, K / 2, K / 2, 32, 128) ||
+        !make_byte_map(&tmSA32, g.a_sf, arows, K / 16, sfs, 32, 16))
         return cudaErrorInvalidValue;
     const size_t fixed = 1024 + 64 + static_cast<size_t>(2 * (g.E + 1)) * 4 + 16 + 16 + 4 * kF4BN;
     const int stages = static_cast<int>(std::min<size_t>(kF4MaxStages, (227 * 1024 - fixed) / (kF4Stage + 24)));
@@ -620,9 +677,9 @@ cudaError_t launch_gemm_nvfp4(const F4Launch& g, cudaStream_t s)
     const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(moe_gemm_nvfp4_kernel), 227 * 1024);
     if (e != cudaSuccess) return e;
     const long long mt_max = (static_cast<long long>(g.T) * g.topk + kBM - 1) / kBM + g.E;
-    const int grid = static_cast<int>(std::min<long long>(mt_max * p.n_tiles, num_sms()));
+    const int grid = static_cast<int>(std::min<long long>(mt_max * p.n_tiles, sms));
     if (grid <= 0) return cudaSuccess;
-    moe_gemm_nvfp4_kernel<<<grid, kF4Threads, smem, s>>>(tmA, tmB, tmSA, tmSB, p);
+    moe_gemm_nvfp4_kernel<<<grid, kF4Threads, smem, s>>>(tmA, tmB, tmSA, tmSB, tmA32, tmSA32, p);
     return cudaGetLastError();
 }
 

@@ -444,8 +444,11 @@ cudaError_t launch_bwd_gemm(const BwdGemmLaunch& g, cudaStream_t s)
     if (g.mode == BG_DGRAD) {
         p.kb = g.K / 64;
         p.wrows = g.K;
-        // paired when the experts average two or more row tiles
-        pair = g.kept >= 2LL * kBM * g.E;
+        // paired when the experts average two or more row tiles and the tiles are short:
+        // with a long K (the dx GEMM, K = 2F) a half-empty pair unit per expert and the
+        // fewer, longer units cost more than the pairs save (Mixtral prefill, K = 28672:
+        // 1138 us single, 1222 us paired; K = 4096: 673 us single, 594 us paired)
+        pair = g.kept >= 2LL * kBM * g.E && g.K <= 8192;
         // A: the row block [rows, K] (K-major boxes); B: the weights [E*K, N] (64 x 64 boxes)
         if (!encode_bf16_map(&tmA, g.a, static_cast<uint64_t>(g.rows), static_cast<uint64_t>(g.K), kBM) ||
             !encode_bf16_map(&tmB, g.b, static_cast<uint64_t>(g.E) * g.K, static_cast<uint64_t>(g.N), 64))

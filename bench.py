@@ -463,8 +463,8 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     step_ms = w0.elapsed_time(w1) / max(args.warmup, 1)
     stage_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)]
-                 for _ in range(args.steps)]
-    bwd_evs = [torch.cuda.Event(enable_timing=True) if bwd else None for _ in range(args.steps)]
+                 for _ in range(min(args.steps, 50))]
+    bwd_evs = [torch.cuda.Event(enable_timing=True) if bwd else None for _ in range(min(args.steps, 50))]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -481,12 +481,11 @@ def run_ours(args, rank, world, local):
     wall0 = time.time()
     for _ in range(lead):
         run()
+    # the timed steps carry no stage events (their host-side recording would slow the
+    # launch-bound batches); the stage split comes from instrumented steps afterwards
     t0.record()
     for i in range(args.steps):
-        if graph is not None:
-            graph.replay()
-        else:
-            step(stage_evs[i], bwd_evs[i])
+        run()
     t1.record()
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -501,12 +500,10 @@ def run_ours(args, rank, world, local):
     st = moe.device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {st} ({moe.STATUS.get(st)}) after the timed region")
-    n_stage = args.steps
-    if graph is not None:   # the stage split from eager steps after the timed region
-        n_stage = min(args.steps, 50)
-        for i in range(n_stage):
-            step(stage_evs[i], bwd_evs[i])
-        torch.cuda.synchronize()
+    n_stage = min(args.steps, 50)   # the stage split: eager steps with events, after the timed region
+    for i in range(n_stage):
+        step(stage_evs[i], bwd_evs[i])
+    torch.cuda.synchronize()
     stage_ms = {n: statistics.mean(stage_evs[i][j].elapsed_time(stage_evs[i][j + 1])
                                    for i in range(n_stage))
                 for j, n in enumerate(moe.STAGE_NAMES)}
@@ -620,7 +617,6 @@ def run_ours(args, rank, world, local):
                 continue
             line["workloads"][name + (f"_{wq}" if wq else "")] = side_workload(name, wq, peaks, peak_kind)
             torch.cuda.empty_cache()
-        line["gpu_launches"] += sum(w["gpu_launches"] for w in line["workloads"].values())
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -699,17 +695,21 @@ def side_workload(name, quant, peaks, peak_kind):
     e1.record()
     torch.cuda.synchronize()
     steps = int(min(400, max(20, 1e3 * SIDE_TIMED_S / max(e0.elapsed_time(e1) / 5, 1e-3))))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)] for _ in range(steps)]
     e0.record()
     for i in range(steps):
-        step(evs[i])
+        step()
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     st = moe.device_status(ws)
     if st != 0:
         raise RuntimeError(f"{name}: device status {st} ({moe.STATUS.get(st)})")
-    stage_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
+    n_stage = min(steps, 50)   # the stage split from instrumented steps after the timed ones
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)] for _ in range(n_stage)]
+    for i in range(n_stage):
+        step(evs[i])
+    torch.cuda.synchronize()
+    stage_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_stage))
                 for j, n in enumerate(moe.STAGE_NAMES)}
     roof, tflops, wgbs = expert_roofline(shape, kept, active, stage_ms, peaks, peak_kind, ms * 1e-3, quant)
     res = {"tokens_per_s": shape.T * steps / (ms * 1e-3), "ms_per_step": ms / steps, "steps": steps,

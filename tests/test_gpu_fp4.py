@@ -88,7 +88,8 @@ def test_quantize_w13_nvfp4_packing():
 
 @pytest.mark.parametrize("T,d,E,F,k,cf", [(300, 256, 5, 256, 2, 1.0), (256, 512, 8, 1024, 2, 1.25),
                                           (64, 1024, 8, 2048, 2, 1.25), (700, 128, 3, 256, 2, 1.0),
-                                          (1100, 256, 2, 384, 2, 1.0), (500, 256, 6, 1408, 2, 1.0)])
+                                          (1100, 256, 2, 384, 2, 1.0), (500, 256, 6, 1408, 2, 1.0),
+                                          (600, 384, 3, 256, 2, 1.0)])
 def test_expert_ffn_nvfp4_vs_oracle(T, d, E, F, k, cf):
     shape = synth.MoEShape("t", T=T, d=d, E=E, F=F, k=k, cf=cf, seed=T + F)
     Ld = make_layer(shape)

@@ -19,17 +19,20 @@
 //   when den = 0.  Codes are packed two per byte, element 2m in the low
 //   nibble; block scales are bytes, rows of them padded to 16 bytes.
 //
-// GEMM kernel: one persistent CTA per SM, 10 warps -- warp 0 TMA producer
-// (codes of 128 rows x 256 values of A and of B, and their block scales,
-// 128 rows x 16 bytes each, per stage), warp 1 allocates TMEM and issues the
-// MMAs (M = 128, N = 128) into two accumulators, warps 2-5 the epilogue,
+// GEMM kernel: one persistent CTA per SM, 14 warps -- warp 0 TMA producer
+// (per stage the codes of 128 rows x 256 values of A and of up to 256 rows of
+// B, and their block scales, 16 bytes a row), warp 1 allocates TMEM and issues
+// the MMAs (M = 128, N = the tile width, up to 256), warps 2-5 and 10-13 the
+// epilogue (two warps per lane quarter, each with half of the tile's columns),
 // warps 6-9 copy each stage's block scales from shared memory into TMEM
-// (tcgen05.st), four columns per MMA: column i of lane l (in each of the four
-// 32-lane quarters) holds the four scale bytes of row l + 32i (byte b: the
-// scale of the MMA's b-th block of 16 along K).
+// (tcgen05.st): for each MMA, column i of lane l (in each of the four 32-lane
+// quarters) holds the four scale bytes of row l + 32i of A (4 columns) and of
+// B (N/32 columns, rounded up to 4; byte b: the scale of the MMA's b-th block
+// of 16 along K).  Tiles of up to 128 columns have two TMEM accumulators
+// (the epilogue of one tile overlaps the next tile's MMAs), wider tiles one.
 // The W13 weights of this path are packed in 128-row blocks (64 W1 rows,
-// then the 64 matching W3 rows), so that one 128-column tile holds matching
-// gate and up columns.  Every wait is bounded.
+// then the 64 matching W3 rows), so that each 128 columns of a gate-up tile
+// hold matching gate and up columns.  Every wait is bounded.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -38,14 +41,25 @@
 namespace moe {
 namespace {
 
-constexpr int kF4Threads = 320;   // 10 warps
-constexpr int kF4BN = 128;        // N tile
+constexpr int kF4Threads = 448;   // 14 warps
+constexpr int kF4MaxBN = 256;     // widest N tile
 constexpr uint32_t kF4ABytes = 128 * 128;   // 128 rows x 256 e2m1 values
-constexpr uint32_t kF4BBytes = kF4BN * 128;
-constexpr uint32_t kF4SfBytes = 128 * 16;   // 128 rows x 16 block scales
-constexpr uint32_t kF4Stage = kF4ABytes + kF4BBytes + 2 * kF4SfBytes;   // 36 KB, a multiple of 1024
-constexpr int kF4SfCol = 2 * kF4BN;        // first TMEM column of the block scales
-constexpr int kF4MaxStages = (512 - kF4SfCol) / 32;   // 32 scale columns per stage
+constexpr uint32_t kF4SfABytes = 128 * 16;  // 128 rows x 16 block scales
+constexpr int kF4AccCols = 256;            // TMEM columns of the accumulator(s)
+constexpr int kF4SfCol = kF4AccCols;       // first TMEM column of the block scales
+constexpr int kF4MaxStages = 8;
+
+// Rows of B a stage holds (128, or 256 for tiles wider than 128 columns).
+__host__ __device__ constexpr int f4_b_alloc(int bn) { return bn <= 128 ? 128 : 256; }
+// Bytes of one stage: A codes, B codes, A scales, B scales; a multiple of 1024.
+__host__ __device__ constexpr uint32_t f4_stage_bytes(int bn)
+{
+    return (kF4ABytes + static_cast<uint32_t>(f4_b_alloc(bn)) * 144u + kF4SfABytes + 1023u) / 1024u * 1024u;
+}
+// TMEM columns of the scales of one MMA's B rows: N/32 rounded up to 4.
+__host__ __device__ constexpr int f4_sfb_cols(int bn) { return ((bn + 31) / 32 + 3) / 4 * 4; }
+// TMEM columns of one stage's scales: 4 per MMA for A, f4_sfb_cols for B, 4 MMAs.
+__host__ __device__ constexpr int f4_sf_stage_cols(int bn) { return 16 + 4 * f4_sfb_cols(bn); }
 
 // ---------------------------------------------------------------- e2m1 codes
 // Eight floats to eight e2m1 codes (round to nearest even, saturating),
@@ -189,7 +203,10 @@ __global__ void __launch_bounds__(kQThreads) quantize_nvfp4_kernel(
 struct F4Params {
     int kind, E, T, topk, d, F;
     int kb_total;   // K / 256 (stages of 128-byte rows), rounded up
-    int bn;         // N tile: 128 for the gate-up; for the down 64..128 (a multiple of 16)
+    int bn;         // N tile: 256 (128 where N is not a multiple of 256); the down GEMM
+                    // with one row tile per expert 64..256 (a multiple of 16)
+    int b_rows;     // rows of B a stage holds (f4_b_alloc(bn))
+    uint32_t stage_bytes;
     int n_tiles;    // N tiles per expert
     int stages;
     int b_policy;   // 1: weight loads evict_first (every expert holds at most one row tile)
@@ -203,7 +220,24 @@ struct F4Params {
     long long budget;
 };
 
-__device__ __forceinline__ float silu_f4(float x) { return x / (1.0f + __expf(-x)); }
+// silu(x) = x / (1 + e^-x); for x << 0 the denominator overflows to +inf and the
+// quotient is (-)0, as in IEEE division.
+__device__ __forceinline__ float silu_f4(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
+// Named barrier 1 among the eight epilogue warps (256 threads); f4_epi_all also
+// returns whether `pred` holds in all of them.
+__device__ __forceinline__ void f4_epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ bool f4_epi_all(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 256, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
+}
 
 // 16 consecutive fp32 TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[32])
@@ -224,6 +258,20 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "%13, %14, %15, %16};" ::"r"(taddr),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+        "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
 }
 
@@ -276,7 +324,7 @@ __device__ __forceinline__ F4Tile f4_decode(const F4Params& p, int tile, const i
 // tmA / tmSA: the A codes and block scales in boxes of 128 rows; tmA32 / tmSA32
 // the same in boxes of 32 rows, for tiles whose expert has at most 32 rows there
 // (decode): the MMA still spans 128 rows, the rows past the box hold stale data
-// and their results are not stored.
+// and their results are not stored.  tmB / tmSB: boxes of bn weight rows.
 __global__ void __launch_bounds__(kF4Threads, 1)
     moe_gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
@@ -287,7 +335,13 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int stages = p.stages;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + stages * kF4Stage);
+    const uint32_t sb = p.stage_bytes;
+    const uint32_t off_sfa = kF4ABytes + static_cast<uint32_t>(p.b_rows) * 128u;   // A scales
+    const uint32_t off_sfb = off_sfa + kF4SfABytes;                                 // B scales
+    const int nacc = p.bn <= 128 ? 2 : 1;           // TMEM accumulators
+    const int sfb_cols = f4_sfb_cols(p.bn);          // TMEM scale columns of one MMA's B rows
+    const int sf_cols = f4_sf_stage_cols(p.bn);      // TMEM scale columns of one stage
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(stages) * sb);
     uint64_t* full_bar = bars;
     uint64_t* empty_bar = bars + stages;
     uint64_t* sf_bar = bars + 2 * stages;
@@ -314,7 +368,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&tfull_bar[b]), 1);
-            mbar_init(smem_u32(&tempty_bar[b]), 4);
+            mbar_init(smem_u32(&tempty_bar[b]), 8);   // the eight epilogue warps
         }
         mbar_fence_init();
     }
@@ -368,16 +422,15 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                 if (lane == 0) {
                     const uint32_t fb = smem_u32(&full_bar[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
-                    uint8_t* st = smem + stage * kF4Stage;
+                    uint8_t* st = smem + static_cast<size_t>(stage) * sb;
                     tma_load_2d(smem_u32(st), few ? &tmA32 : &tmA, kb * 128, arow, fb);
-                    tma_load_2d(smem_u32(st + kF4ABytes + kF4BBytes), few ? &tmSA32 : &tmSA, kb * 16, arow, fb);
+                    tma_load_2d(smem_u32(st + off_sfa), few ? &tmSA32 : &tmSA, kb * 16, arow, fb);
                     if (p.b_policy) {
                         tma_load_2d_hint(smem_u32(st + kF4ABytes), &tmB, kb * 128, brow, fb, pol_b);
-                        tma_load_2d_hint(smem_u32(st + kF4ABytes + kF4BBytes + kF4SfBytes), &tmSB, kb * 16, brow,
-                                         fb, pol_b);
+                        tma_load_2d_hint(smem_u32(st + off_sfb), &tmSB, kb * 16, brow, fb, pol_b);
                     } else {
                         tma_load_2d(smem_u32(st + kF4ABytes), &tmB, kb * 128, brow, fb);
-                        tma_load_2d(smem_u32(st + kF4ABytes + kF4BBytes + kF4SfBytes), &tmSB, kb * 16, brow, fb);
+                        tma_load_2d(smem_u32(st + off_sfb), &tmSB, kb * 16, brow, fb);
                     }
                 }
                 __syncwarp();
@@ -402,14 +455,14 @@ __global__ void __launch_bounds__(kF4Threads, 1)
             int it = 0, last_b = -1;
             uint32_t last_par = 0;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-                const int b = it & 1;
-                const uint32_t acc_par = (it >> 1) & 1;
+                const int b = it % nacc;
+                const uint32_t acc_par = static_cast<uint32_t>(it / nacc) & 1u;
                 if (!mbar_wait(smem_u32(&tempty_bar[b]), acc_par ^ 1, p.budget)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kF4BN);   // fixed 128-column slots
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * 128);
                 for (int kb = 0; kb < p.kb_total; ++kb) {
                     if (!mbar_wait(smem_u32(&full_bar[stage]), phase, p.budget) ||
                         !mbar_wait(smem_u32(&sf_bar[stage]), phase, p.budget)) {
@@ -417,13 +470,13 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(smem + stage * kF4Stage);
+                    const uint32_t a0 = smem_u32(smem + static_cast<size_t>(stage) * sb);
                     const uint32_t b0 = a0 + kF4ABytes;
-                    const uint32_t sf0 = tmem_base + static_cast<uint32_t>(kF4SfCol + 32 * stage);
+                    const uint32_t sf0 = tmem_base + static_cast<uint32_t>(kF4SfCol + sf_cols * stage);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)   // K = 64 per instruction: 32 bytes of each row
                         mma_nvfp4(d_tmem, sdesc_k_sw128(a0 + 32 * j), sdesc_k_sw128(b0 + 32 * j), idesc,
-                                  sf0 + 4 * j, sf0 + 16 + 4 * j, (kb > 0 || j > 0) ? 1u : 0u);
+                                  sf0 + 4 * j, sf0 + 16 + sfb_cols * j, (kb > 0 || j > 0) ? 1u : 0u);
                     mma_commit(smem_u32(&empty_bar[stage]));
                     if (++stage == stages) {
                         stage = 0;
@@ -439,7 +492,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
             if (last_b >= 0) mbar_wait(smem_u32(&tfull_bar[last_b]), last_par, p.budget);
         }
         __syncwarp();
-    } else if (warp >= 6) {
+    } else if (warp >= 6 && warp < 10) {
         // ------------------------------------------------------------ block scales into TMEM
         const int q = warp & 3;   // the TMEM lane quarter this warp may access
         int stage = 0;
@@ -452,22 +505,40 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                     break;
                 }
                 // MMA j's scales: column 4j + i of lane 32q + l holds the four scale bytes
-                // (word j) of row l + 32i, the same in each of the four lane quarters
-                const uint8_t* sfs = smem + stage * kF4Stage + kF4ABytes + kF4BBytes;
-                uint4 wa[4], wb[4];
+                // (word j) of A row l + 32i; column 16 + sfb_cols * j + i those of B row
+                // l + 32i; the same in each of the four lane quarters
+                const uint8_t* st = smem + static_cast<size_t>(stage) * sb;
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(kF4SfCol + sf_cols * stage);
+                {
+                    uint4 w[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    wa[i] = *reinterpret_cast<const uint4*>(sfs + (lane + 32 * i) * 16);
-                    wb[i] = *reinterpret_cast<const uint4*>(sfs + kF4SfBytes + (lane + 32 * i) * 16);
+                    for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const uint4*>(st + off_sfa + (lane + 32 * i) * 16);
+                    const uint32_t r[16] = {w[0].x, w[1].x, w[2].x, w[3].x, w[0].y, w[1].y, w[2].y, w[3].y,
+                                            w[0].z, w[1].z, w[2].z, w[3].z, w[0].w, w[1].w, w[2].w, w[3].w};
+                    tmem_st16(taddr, r);
                 }
-                const uint32_t ra[16] = {wa[0].x, wa[1].x, wa[2].x, wa[3].x, wa[0].y, wa[1].y, wa[2].y, wa[3].y,
-                                         wa[0].z, wa[1].z, wa[2].z, wa[3].z, wa[0].w, wa[1].w, wa[2].w, wa[3].w};
-                const uint32_t rb[16] = {wb[0].x, wb[1].x, wb[2].x, wb[3].x, wb[0].y, wb[1].y, wb[2].y, wb[3].y,
-                                         wb[0].z, wb[1].z, wb[2].z, wb[3].z, wb[0].w, wb[1].w, wb[2].w, wb[3].w};
-                const uint32_t taddr =
-                    tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(kF4SfCol + 32 * stage);
-                tmem_st16(taddr, ra);
-                tmem_st16(taddr + 16, rb);
+                if (sfb_cols == 4) {
+                    uint4 w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const uint4*>(st + off_sfb + (lane + 32 * i) * 16);
+                    const uint32_t r[16] = {w[0].x, w[1].x, w[2].x, w[3].x, w[0].y, w[1].y, w[2].y, w[3].y,
+                                            w[0].z, w[1].z, w[2].z, w[3].z, w[0].w, w[1].w, w[2].w, w[3].w};
+                    tmem_st16(taddr + 16, r);
+                } else {   // 8 columns per MMA: rows l + 32i, i < 8 (the stage holds 256 rows)
+                    uint4 w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) w[i] = *reinterpret_cast<const uint4*>(st + off_sfb + (lane + 32 * i) * 16);
+                    uint32_t r[32];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        r[i] = w[i].x;
+                        r[8 + i] = w[i].y;
+                        r[16 + i] = w[i].z;
+                        r[24 + i] = w[i].w;
+                    }
+                    tmem_st32(taddr + 16, r);
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -480,30 +551,32 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;
+        const int q = warp & 3;                    // TMEM lane quarter
         const int row = q * 32 + lane;
-        const int et = static_cast<int>(threadIdx.x) - 64;   // 0..127 over the four warps
+        const int eh = warp >= 10 ? 1 : 0;         // which half of the columns
+        const int et = eh * 128 + (static_cast<int>(threadIdx.x) & 127);   // 0..255 over the eight warps
         int it = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
             const F4Tile t = f4_decode(p, tile, s_start, s_offs);
-            const int b = it & 1;
-            const uint32_t acc_par = (it >> 1) & 1;
-            // the tile's weight-row scales while its MMAs run
-            epilogue_sync();
+            const int b = it % nacc;
+            const uint32_t acc_par = static_cast<uint32_t>(it / nacc) & 1u;
+            // the tile's weight-row scales while its MMAs run; columns past the
+            // expert's weight rows (the down GEMM's last tile) read no scale
+            f4_epi_sync();
             {
-                // columns past the expert's weight rows (the down GEMM's last tile) read no scale
-                const int col = t.n * p.bn + et;
                 const int wrows = p.kind == GK_GATEUP ? 2 * p.F : p.d;
+                const int col = t.n * p.bn + et;
                 s_bsc[et] = (et < p.bn && col < wrows) ? __ldg(p.b_scale + static_cast<long long>(t.e) * wrows + col)
                                                        : 0.0f;
             }
-            const bool got = epilogue_all(mbar_wait(smem_u32(&tfull_bar[b]), acc_par, p.budget));
+            const bool got = f4_epi_all(mbar_wait(smem_u32(&tfull_bar[b]), acc_par, p.budget));
             if (!got) {
                 record_error(p.status, MOE_ERR_TIMEOUT);
                 break;
             }
             tc_fence_after();
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * kF4BN);
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * 128);
             const int off = s_offs[t.e];
             const int cnt = s_offs[t.e + 1] - off;
             const int ri = t.m * kBM + row;
@@ -511,26 +584,30 @@ __global__ void __launch_bounds__(kF4Threads, 1)
             const float asc = valid ? p.a_scale[off + ri] : 0.0f;
             uint32_t v[32], u[32];
             if (p.kind == GK_GATEUP) {
-                // columns [0, 64): gate, [64, 128): the matching up columns
-                __nv_bfloat16* dst = p.act + static_cast<size_t>(off + ri) * p.F + t.n * (kF4BN / 2);
+                // each 128 columns: [0, 64) gate, [64, 128) the matching up columns;
+                // this warp takes 32 of the 64 pairs
+                __nv_bfloat16* dst = p.act + static_cast<size_t>(off + ri) * p.F + t.n * (p.bn / 2);
                 float rmax = 0.0f;
-                for (int c = 0; c < kF4BN / 2; c += 32) {
-                    tmem_ld32(taddr + c, v);
-                    tmem_ld32(taddr + kF4BN / 2 + c, u);
+                for (int h = 0; h < p.bn; h += 128) {
+                    const int c = 32 * eh;
+                    tmem_ld32(taddr + h + c, v);
+                    tmem_ld32(taddr + h + 64 + c, u);
                     tmem_ld_wait2(v, u);
                     if (valid) {
+                        const float* bg = s_bsc + h + c;
+                        const float* bu = s_bsc + h + 64 + c;
                         uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const float g0 = __uint_as_float(v[2 * j]) * asc * s_bsc[c + 2 * j];
-                            const float g1 = __uint_as_float(v[2 * j + 1]) * asc * s_bsc[c + 2 * j + 1];
-                            const float u0 = __uint_as_float(u[2 * j]) * asc * s_bsc[kF4BN / 2 + c + 2 * j];
-                            const float u1 = __uint_as_float(u[2 * j + 1]) * asc * s_bsc[kF4BN / 2 + c + 2 * j + 1];
+                            const float g0 = __uint_as_float(v[2 * j]) * asc * bg[2 * j];
+                            const float g1 = __uint_as_float(v[2 * j + 1]) * asc * bg[2 * j + 1];
+                            const float u0 = __uint_as_float(u[2 * j]) * asc * bu[2 * j];
+                            const float u1 = __uint_as_float(u[2 * j + 1]) * asc * bu[2 * j + 1];
                             const float a0 = silu_f4(g0) * u0, a1 = silu_f4(g1) * u1;
                             pk[j] = pack_bf16x2(a0, a1);
                             rmax = fmaxf(rmax, fmaxf(fabsf(a0), fabsf(a1)));
                         }
-                        uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + h / 2 + c);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
@@ -540,10 +617,11 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                     atomicMax(reinterpret_cast<unsigned int*>(p.act_amax + off + ri),
                               __float_as_uint(__bfloat162float(__float2bfloat16_rn(rmax))));
             } else {
+                // 32-column pieces alternate between the two halves of the epilogue
                 const int col0 = t.n * p.bn;
                 const int ncols = min(p.bn, p.d - col0);   // a multiple of 16
                 __nv_bfloat16* dst = p.y_slots + static_cast<size_t>(off + ri) * p.d + col0;
-                for (int c = 0; c < ncols; c += 32) {
+                for (int c = 32 * eh; c < ncols; c += 64) {
                     const int w = min(32, ncols - c);       // 32, or 16 for the last piece
                     if (w == 32)
                         tmem_ld32(taddr + c, v);
@@ -602,6 +680,14 @@ bool make_byte_map(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t col
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// N tile of a launch: 256 columns (two 128-row blocks of the gate-up's
+// packing; for the down GEMM the last tile of an expert may be partly past its
+// rows), else 128.  Measured on the Mixtral-shaped prefill (4096 tokens, top-2):
+// 256-wide tiles with one accumulator beat 128-wide tiles with two (the second
+// accumulator hides the epilogue, the wider tile halves the reads of A per
+// output column and a stage carries twice the MMA work per byte of A).
+int f4_tile_width(int N) { return N % 256 == 0 ? 256 : 128; }
+
 }  // namespace
 
 int nvfp4_sf_stride(int cols) { return (cols / 16 + 15) / 16 * 16; }
@@ -637,20 +723,20 @@ cudaError_t launch_gemm_nvfp4(const F4Launch& g, cudaStream_t s)
     p.budget = g.budget;
     const int K = g.kind == GK_GATEUP ? g.d : g.F;       // reduction length
     const int N = g.kind == GK_GATEUP ? 2 * g.F : g.d;   // weight rows of one expert
-    if (K % 32 != 0 || N % kF4BN != 0) return cudaErrorInvalidValue;
+    if (K % 32 != 0 || N % 128 != 0) return cudaErrorInvalidValue;
     const int sms = num_sms();
     p.kb_total = (K + 255) / 256;
-    p.bn = kF4BN;
     // When no expert holds more than one row tile, each weight tile is read by one
     // tile only: its loads go first out of L2, and the down GEMM's column tile (a
-    // multiple of 16, 64..128) is the one that needs the fewest passes over the
+    // multiple of 16, 64..256) is the one that needs the fewest passes over the
     // SMs times its width.
     const bool one_tile = g.rows_cap > 0 && std::min<long long>(g.rows_cap, static_cast<long long>(g.T)) <= kBM;
     p.b_policy = one_tile ? 1 : 0;
+    p.bn = f4_tile_width(N);
     if (one_tile && g.kind != GK_GATEUP) {
         const long long mt = std::min<long long>(g.E, static_cast<long long>(g.T) * g.topk);
         long long best = -1;
-        for (int bn = kF4BN; bn >= 64; bn -= 16) {
+        for (int bn = kF4MaxBN; bn >= 64; bn -= 16) {
             const long long cost = (mt * ((N + bn - 1) / bn) + sms - 1) / sms * bn;
             if (best < 0 || cost < best) {
                 best = cost;
@@ -658,6 +744,9 @@ cudaError_t launch_gemm_nvfp4(const F4Launch& g, cudaStream_t s)
             }
         }
     }
+    if (g.kind == GK_GATEUP && N % p.bn != 0) return cudaErrorInvalidValue;
+    p.b_rows = f4_b_alloc(p.bn);
+    p.stage_bytes = f4_stage_bytes(p.bn);
     p.n_tiles = (N + p.bn - 1) / p.bn;
     const uint64_t arows = static_cast<uint64_t>(g.T) * g.topk;
     const uint64_t brows = static_cast<uint64_t>(g.E) * N;
@@ -670,10 +759,15 @@ cudaError_t launch_gemm_nvfp4(const F4Launch& g, cudaStream_t s)
         !make_byte_map(&tmA32, g.a_codes, arows, K / 2, K / 2, 32, 128) ||
         !make_byte_map(&tmSA32, g.a_sf, arows, K / 16, sfs, 32, 16))
         return cudaErrorInvalidValue;
-    const size_t fixed = 1024 + 64 + static_cast<size_t>(2 * (g.E + 1)) * 4 + 16 + 16 + 4 * kF4BN;
-    const int stages = static_cast<int>(std::min<size_t>(kF4MaxStages, (227 * 1024 - fixed) / (kF4Stage + 24)));
+    // shared memory: the stages (each with its three barriers), the two accumulator
+    // barriers, the tile starts and offsets, the TMEM address, the weight-row scales
+    const size_t fixed = 1024 + 64 + static_cast<size_t>(2 * (g.E + 1)) * 4 + 16 + 16 + 4 * kF4MaxBN;
+    const int by_smem = static_cast<int>((227 * 1024 - fixed) / (p.stage_bytes + 24));
+    const int by_tmem = (512 - kF4SfCol) / f4_sf_stage_cols(p.bn);
+    const int stages = std::min(kF4MaxStages, std::min(by_smem, by_tmem));
+    if (stages < 2) return cudaErrorInvalidValue;
     p.stages = stages;
-    const size_t smem = fixed + static_cast<size_t>(stages) * (kF4Stage + 24);
+    const size_t smem = fixed + static_cast<size_t>(stages) * (p.stage_bytes + 24);
     const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(moe_gemm_nvfp4_kernel), 227 * 1024);
     if (e != cudaSuccess) return e;
     const long long mt_max = (static_cast<long long>(g.T) * g.topk + kBM - 1) / kBM + g.E;

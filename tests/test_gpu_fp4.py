@@ -50,6 +50,39 @@ def test_quantize_nvfp4_matches_oracle(rows, cols):
     assert_quantised_equal(got, oracle_rows(w), cols)
 
 
+def _bf16_step(x, n):
+    """x (bf16-exact float32 values) moved by n bf16 steps away from zero."""
+    b = torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16)
+    n = torch.from_numpy(np.broadcast_to(np.asarray(n, np.int16), b.shape).copy())
+    return (b + n).view(torch.bfloat16).float().numpy()
+
+
+def test_quantize_nvfp4_rounding_boundaries():
+    """Elements exactly on each e2m1 rounding boundary of their block (x / den = 0.25,
+    0.75, ..., 5, where the tie goes to the even code) and one bf16 step either side,
+    for divisors den = m 2^n with m = 1.75, 1.25, 1.125: 1 / den is inexact, so the
+    quotient must be rounded exactly as the oracle's IEEE division rounds it."""
+    rng = np.random.default_rng(11)
+    ts = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    rows = []
+    for k in (-7, 0, 5):                      # row scale 2^k: the row max is 2688 2^k
+        for m in (1.75, 1.25, 1.125):
+            for j in (-3, 0, 2):              # block scale m 2^j, divisor den = m 2^(j+k)
+                den = np.float32(m * 2.0 ** (j + k))
+                row = np.zeros(128, np.float32)
+                row[0] = 2688 * 2.0 ** k
+                for blk in range(1, 8):
+                    cand = ts * den
+                    pick = rng.integers(0, 7, 15)
+                    vals = _bf16_step(cand[pick], rng.integers(-1, 2, 15)) * rng.choice([-1, 1], 15)
+                    row[16 * blk] = 6 * den  # the block max: block scale e4m3(m 2^j), exact
+                    row[16 * blk + 1: 16 * blk + 16] = vals
+                rows.append(row)
+    w = torch.from_numpy(np.stack(rows)).to(torch.bfloat16)
+    assert torch.equal(w.float(), torch.from_numpy(np.stack(rows)))   # every value bf16-exact
+    assert_quantised_equal(moe.quantize_nvfp4(w.cuda()), oracle_rows(w), 128)
+
+
 def unpack13(q13, b13, s13, F, d):
     """The 4-bit path's W13 packing (128-row blocks: 64 W1 rows, then the matching 64 W3
     rows) back to W1 and W3: codes [E, 2F, d/2], block scales [E, 2F, stride], scales [E*2F]."""

@@ -94,6 +94,21 @@ __device__ __forceinline__ float e4m3_value(uint32_t b)
     return (b & 0x80u) ? -v : v;
 }
 
+// x / den rounded to nearest even, from y = 1/den rounded to nearest even:
+// q0 = x y, then twice q <- q + (x - q den) y, each remainder taken with one FMA.
+// This is Markstein's correction step (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
+// when y is within half an ulp of 1/den and q within one ulp of x / den, the
+// remainder is exact and q + r y rounds to the correctly rounded quotient.  q0 may
+// miss that by up to half an ulp; the first step brings it within one ulp, the
+// second gives the quotient.  Needs den and 1/den normal (the caller checks).
+__device__ __forceinline__ float div_by(float x, float den, float y)
+{
+    float q = __fmul_rn(x, y);
+    q = __fmaf_rn(__fmaf_rn(-q, den, x), y, q);
+    return __fmaf_rn(__fmaf_rn(-q, den, x), y, q);
+}
+
 __device__ __forceinline__ void bf16x8(const uint4 v, float (&x)[8])
 {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -122,53 +137,70 @@ __device__ __forceinline__ long long source_row(long long r, const int32_t* perm
     return r;
 }
 
-constexpr int kQThreads = 128;
-constexpr int kQMaxGroups = 8;   // 16-element groups per thread: rows up to 128 * 8 * 16 = 16384
+constexpr int kQThreads = 256;
+constexpr int kQMaxGroups = 4;   // 16-element groups per thread: rows up to 256 * 4 * 16 = 16384
 
-// One block per row: the row's groups of 16 stay in registers; the row max is
-// reduced over the block (or given by amax_in), then each group is quantised.
-__global__ void __launch_bounds__(kQThreads) quantize_nvfp4_kernel(
-    long long rows, int cols, const uint4* __restrict__ w, const int32_t* __restrict__ perm, int k, int w13_F,
-    const int32_t* __restrict__ nrows, const float* __restrict__ amax_in, uint2* __restrict__ codes,
+// Threads per row (a power of two, 8..256): the fewest that hold the row's groups
+// at up to kQMaxGroups each; a block of kQThreads quantises kQThreads / tpr rows.
+int quant_threads_per_row(int cols)
+{
+    const int ng = cols / 16;
+    int tpr = 8;
+    while (tpr < kQThreads && tpr * kQMaxGroups < ng) tpr *= 2;
+    return tpr;
+}
+
+// Each row's groups of 16 stay in registers; the row max is reduced over the
+// row's threads (or given by amax_in), then each group is quantised.
+__global__ void __launch_bounds__(kQThreads, 4) quantize_nvfp4_kernel(
+    long long rows, int cols, int tpr, const uint4* __restrict__ w, const int32_t* __restrict__ perm, int k,
+    int w13_F, const int32_t* __restrict__ nrows, const float* __restrict__ amax_in, uint2* __restrict__ codes,
     uint8_t* __restrict__ bscale, int sf_stride, float* __restrict__ scales, float* __restrict__ zero_rows)
 {
     __shared__ float s_wmax[kQThreads / 32];
-    const long long row = blockIdx.x;
-    if (row >= rows || (nrows && row >= *nrows)) return;   // the whole block
+    const int lt = static_cast<int>(threadIdx.x) & (tpr - 1);   // thread within the row
+    const long long row = static_cast<long long>(blockIdx.x) * (kQThreads / tpr) + threadIdx.x / tpr;
+    const bool active = row < rows && !(nrows && row >= *nrows);
     const int ng = cols / 16;
-    const uint4* wr = w + source_row(row, perm, k, w13_F) * (cols / 8);
     uint4 v[2 * kQMaxGroups];
     float gmax[kQMaxGroups];
     float amax = 0.0f;
+    if (active) {
+        const uint4* wr = w + source_row(row, perm, k, w13_F) * (cols / 8);
 #pragma unroll
-    for (int i = 0; i < kQMaxGroups; ++i) {
-        const int g = threadIdx.x + kQThreads * i;
-        gmax[i] = 0.0f;
-        if (g < ng) {
-            v[2 * i] = __ldg(wr + 2 * g);
-            v[2 * i + 1] = __ldg(wr + 2 * g + 1);
-            float x[8];
-            bf16x8(v[2 * i], x);
+        for (int i = 0; i < kQMaxGroups; ++i) {
+            const int g = lt + tpr * i;
+            gmax[i] = 0.0f;
+            if (g < ng) {
+                v[2 * i] = __ldg(wr + 2 * g);
+                v[2 * i + 1] = __ldg(wr + 2 * g + 1);
+                float x[8];
+                bf16x8(v[2 * i], x);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) gmax[i] = fmaxf(gmax[i], fabsf(x[j]));
-            bf16x8(v[2 * i + 1], x);
+                for (int j = 0; j < 8; ++j) gmax[i] = fmaxf(gmax[i], fabsf(x[j]));
+                bf16x8(v[2 * i + 1], x);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) gmax[i] = fmaxf(gmax[i], fabsf(x[j]));
-            amax = fmaxf(amax, gmax[i]);
+                for (int j = 0; j < 8; ++j) gmax[i] = fmaxf(gmax[i], fabsf(x[j]));
+                amax = fmaxf(amax, gmax[i]);
+            }
         }
     }
     if (amax_in) {
-        amax = amax_in[row];
+        if (active) amax = amax_in[row];
     } else {
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        if ((threadIdx.x & 31) == 0) s_wmax[threadIdx.x >> 5] = amax;
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < kQThreads / 32; ++i) amax = fmaxf(amax, s_wmax[i]);
+        // over the row's lanes of this warp, then (rows wider than a warp) its warps
+        for (int off = min(tpr, 32) / 2; off >= 1; off >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (tpr > 32) {
+            if ((threadIdx.x & 31) == 0) s_wmax[threadIdx.x >> 5] = amax;
+            __syncthreads();
+            const int w0 = static_cast<int>(threadIdx.x / tpr) * (tpr / 32);
+            for (int i = 0; i < tpr / 32; ++i) amax = fmaxf(amax, s_wmax[w0 + i]);
+        }
     }
+    if (!active) return;
     const float sc = amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
-    if (threadIdx.x == 0) {
+    if (lt == 0) {
         scales[row] = sc;
         if (zero_rows) zero_rows[row] = 0.0f;
     }
@@ -176,7 +208,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_nvfp4_kernel(
     uint8_t* br = bscale + row * sf_stride;
 #pragma unroll
     for (int i = 0; i < kQMaxGroups; ++i) {
-        const int g = threadIdx.x + kQThreads * i;
+        const int g = lt + tpr * i;
         if (g >= ng) continue;
         const uint32_t b = e4m3_code(__fdiv_rn(__fdiv_rn(gmax[i], sc), 6.0f));
         const float den = __fmul_rn(e4m3_value(b), sc);
@@ -184,7 +216,15 @@ __global__ void __launch_bounds__(kQThreads) quantize_nvfp4_kernel(
         bf16x8(v[2 * i], x0);
         bf16x8(v[2 * i + 1], x1);
         uint2 c = make_uint2(0u, 0u);
-        if (den > 0.0f) {
+        if (den >= 0x1p-100f) {   // den and 1/den normal: the FMA quotient
+            const float y = __frcp_rn(den);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                x0[j] = div_by(x0[j], den, y);
+                x1[j] = div_by(x1[j], den, y);
+            }
+            c = make_uint2(e2m1x8(x0), e2m1x8(x1));
+        } else if (den > 0.0f) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 x0[j] = __fdiv_rn(x0[j], den);
@@ -196,7 +236,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_nvfp4_kernel(
         br[g] = static_cast<uint8_t>(b);
     }
     // the padding of the scale row (never read as a scale: the tensor map ends at ng)
-    if (threadIdx.x < sf_stride - ng) br[ng + threadIdx.x] = 0;
+    for (int i = ng + lt; i < sf_stride; i += tpr) br[i] = 0;
 }
 
 // ---------------------------------------------------------------- the GEMM
@@ -697,9 +737,12 @@ cudaError_t launch_quantize_nvfp4(long long rows, int cols, const void* w, const
                                   void* bscale, float* scales, float* zero_rows, cudaStream_t s)
 {
     if (rows <= 0) return cudaSuccess;
-    if (cols % 32 != 0 || cols > kQThreads * kQMaxGroups * 16 || rows > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    quantize_nvfp4_kernel<<<static_cast<unsigned>(rows), kQThreads, 0, s>>>(
-        rows, cols, static_cast<const uint4*>(w), perm, k, w13_F, nrows, amax_in, static_cast<uint2*>(codes),
+    if (cols % 32 != 0 || cols > kQThreads * kQMaxGroups * 16) return cudaErrorInvalidValue;
+    const int tpr = quant_threads_per_row(cols);
+    const long long blocks = (rows + kQThreads / tpr - 1) / (kQThreads / tpr);
+    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    quantize_nvfp4_kernel<<<static_cast<unsigned>(blocks), kQThreads, 0, s>>>(
+        rows, cols, tpr, static_cast<const uint4*>(w), perm, k, w13_F, nrows, amax_in, static_cast<uint2*>(codes),
         static_cast<uint8_t*>(bscale), nvfp4_sf_stride(cols), scales, zero_rows);
     return cudaGetLastError();
 }

@@ -128,14 +128,20 @@ __device__ __forceinline__ float amax8(const uint4 v, float amax)
     return amax;
 }
 
-__device__ __forceinline__ uint2 e4m3_8(const uint4 v, float sc)
+// 1 / sc rounded, for div_by; 0 when sc is below kFmaDivMin (plain division).
+__device__ __forceinline__ float recip_for_div(float sc) { return sc >= kFmaDivMin ? __frcp_rn(sc) : 0.0f; }
+
+// Eight bf16 values to e4m3 codes of value / sc (y: recip_for_div(sc)).
+__device__ __forceinline__ uint2 e4m3_8(const uint4 v, float sc, float y)
 {
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};
     uint32_t packed[2] = {0, 0};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&words[j]);
-        const float x0 = __bfloat162float(b.x) / sc, x1 = __bfloat162float(b.y) / sc;
+        const float v0 = __bfloat162float(b.x), v1 = __bfloat162float(b.y);
+        const float x0 = y != 0.0f ? div_by(v0, sc, y) : __fdiv_rn(v0, sc);
+        const float x1 = y != 0.0f ? div_by(v1, sc, y) : __fdiv_rn(v1, sc);
         uint16_t two;   // element x0 in the low byte
         asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(two) : "f"(x1), "f"(x0));
         packed[j >> 1] |= static_cast<uint32_t>(two) << (16 * (j & 1));
@@ -166,8 +172,9 @@ __global__ void quantize_fp8_kernel(long long rows, int cols, const uint4* __res
         if (zero_rows) zero_rows[row] = 0.0f;
     }
     uint2* qr = q + row * c8;
+    const float y = recip_for_div(sc);
 #pragma unroll 4
-    for (int c = lane; c < c8; c += 32) qr[c] = e4m3_8(__ldg(wr + c), sc);
+    for (int c = lane; c < c8; c += 32) qr[c] = e4m3_8(__ldg(wr + c), sc, y);
 }
 
 // Each row's max |value| not yet known, rows of at most 256 * 8 * P values:
@@ -205,10 +212,11 @@ __global__ void __launch_bounds__(256) quantize_fp8_block_kernel(
         if (zero_rows) zero_rows[row] = 0.0f;
     }
     uint2* qr = q + row * c8;
+    const float y = recip_for_div(sc);
 #pragma unroll
     for (int i = 0; i < P; ++i) {
         const int c = threadIdx.x + 256 * i;
-        if (c < c8) qr[c] = e4m3_8(v[i], sc);
+        if (c < c8) qr[c] = e4m3_8(v[i], sc, y);
     }
 }
 
@@ -231,8 +239,9 @@ __global__ void quantize_fp8_amax_kernel(int cols, int parts, const uint4* __res
     const int c_end = min(c8, (part + 1) * piece);
     const uint4* wr = w + (perm ? perm[row] / k : row) * c8;
     uint2* qr = q + row * c8;
+    const float y = recip_for_div(sc);
 #pragma unroll 4
-    for (int c = part * piece + threadIdx.x; c < c_end; c += blockDim.x) qr[c] = e4m3_8(__ldg(wr + c), sc);
+    for (int c = part * piece + threadIdx.x; c < c_end; c += blockDim.x) qr[c] = e4m3_8(__ldg(wr + c), sc, y);
 }
 
 // One thread waits on an mbarrier that nothing will ever complete, with the

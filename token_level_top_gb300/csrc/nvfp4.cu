@@ -94,21 +94,6 @@ __device__ __forceinline__ float e4m3_value(uint32_t b)
     return (b & 0x80u) ? -v : v;
 }
 
-// x / den rounded to nearest even, from y = 1/den rounded to nearest even:
-// q0 = x y, then twice q <- q + (x - q den) y, each remainder taken with one FMA.
-// This is Markstein's correction step (P. Markstein, "Computation of elementary
-// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
-// when y is within half an ulp of 1/den and q within one ulp of x / den, the
-// remainder is exact and q + r y rounds to the correctly rounded quotient.  q0 may
-// miss that by up to half an ulp; the first step brings it within one ulp, the
-// second gives the quotient.  Needs den and 1/den normal (the caller checks).
-__device__ __forceinline__ float div_by(float x, float den, float y)
-{
-    float q = __fmul_rn(x, y);
-    q = __fmaf_rn(__fmaf_rn(-q, den, x), y, q);
-    return __fmaf_rn(__fmaf_rn(-q, den, x), y, q);
-}
-
 __device__ __forceinline__ void bf16x8(const uint4 v, float (&x)[8])
 {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -216,7 +201,7 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_nvfp4_kernel(
         bf16x8(v[2 * i], x0);
         bf16x8(v[2 * i + 1], x1);
         uint2 c = make_uint2(0u, 0u);
-        if (den >= 0x1p-100f) {   // den and 1/den normal: the FMA quotient
+        if (den >= kFmaDivMin) {   // den and 1/den normal: the FMA quotient
             const float y = __frcp_rn(den);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {

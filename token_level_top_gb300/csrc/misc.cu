@@ -3,6 +3,7 @@
 // expert outputs, and the bounded-wait failure probe.
 #include "common.cuh"
 #include "internal.h"
+#include "quotient.cuh"
 
 namespace moe {
 namespace {

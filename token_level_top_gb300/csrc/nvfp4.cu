@@ -37,6 +37,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "quotient.cuh"
 
 namespace moe {
 namespace {

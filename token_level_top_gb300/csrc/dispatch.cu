@@ -16,13 +16,19 @@
 // first chunk q1 in which some expert's running count passes C, and leaves
 // the per-chunk bases.  From chunk q1 on, 8 warps of the CTA (256 threads,
 // synchronised on named barrier 1) replay the entries in windows of 256
-// consecutive entries of one rank, one per thread: each entry picks its
-// expert under the current full set, __match_any_sync gives it its rank
-// among its warp's entries of that expert and each warp adds the earlier
-// warps' counts of that expert (slot = fill + rank), a block minimum finds the
-// first entry that takes an expert's last slot, everything up to it commits,
-// and entries after it that chose the now-full expert choose again (three
-// barriers per iteration).  Stage 2 (grid-wide) writes the entries
+// consecutive entries of one rank, one per thread, in rounds.  Each expert has
+// a fill position in the window: the position of the entry that takes its last
+// slot (-1 when it was full before the window, none when it does not fill).
+// In a round every entry picks its expert with the experts whose fill position
+// lies before it counted as full, __match_any_sync gives its rank among its
+// warp's entries of that expert and each warp adds the earlier warps' counts
+// (slot = fill + rank), and the entry with slot C-1 records the expert's new
+// fill position.  Rounds repeat until the positions reproduce themselves; such a
+// fixed point is the sequential fill, and each round settles the next fill in
+// window order (every entry before it sees exactly the experts full at its
+// turn, the other positions never lying before their true ones), so a window
+// takes at most one round per fill in it, plus one; fills that do not interact
+// settle in the same round.  The window then commits.  Stage 2 (grid-wide) writes the entries
 // before q1, the permutation in slot order and the combine weights
 // ([mhpn] §4.3: router probabilities renormalised over the experts used).
 #include <math.h>
@@ -46,6 +52,19 @@ constexpr size_t kSerialSmemCap = 208 * 1024;
 __device__ __forceinline__ void replay_sync()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(kReplayThreads) : "memory");
+}
+
+// Barrier 1 among the replay's threads that also returns whether `pred` holds in any of them.
+__device__ __forceinline__ bool replay_any(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "n"(kReplayThreads)
+        : "memory");
+    return r != 0;
 }
 
 struct SerialArgs {
@@ -91,17 +110,18 @@ __device__ __forceinline__ uint32_t byte_msbs(uint32_t x)
 }
 
 // First of 16 order positions (the low n valid) whose expert is neither full
-// (s_isfull[e] != 0) nor held, or -1.  Every position is looked at without an
-// early exit, so the 16 byte loads overlap; the held test compares 4
-// positions at a time.
+// for the entry at window position `pos` (s_fillpos[e] < pos: the entry taking
+// the expert's last slot comes before it, -1 for experts full before the
+// window) nor held, or -1.  Every position is looked at without an early exit,
+// so the 16 loads overlap; the held test compares 4 positions at a time.
 __device__ __forceinline__ int first_open16(const uint4 v, int n, const Held& held,
-                                            const uint8_t* s_isfull)
+                                            const int16_t* s_fillpos, int pos)
 {
     const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
     uint32_t closed = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-        closed |= static_cast<uint32_t>(s_isfull[(wd[i >> 2] >> (8 * (i & 3))) & 0xFF]) << i;
+        closed |= static_cast<uint32_t>(s_fillpos[(wd[i >> 2] >> (8 * (i & 3))) & 0xFF] < pos) << i;
     for (int q = 0; q < held.n; ++q) {
         const uint32_t rep = held.get(q) * 0x01010101u;
 #pragma unroll
@@ -120,18 +140,18 @@ __device__ __forceinline__ int first_open16(const uint4 v, int n, const Held& he
 // order in global memory.
 template <bool NC>
 __device__ __forceinline__ int choose_expert(const DispatchArgs& a, int t, const uint4* prow, int nw,
-                                             const Held& held, const uint8_t* s_isfull)
+                                             const Held& held, const int16_t* s_fillpos, int pos)
 {
     const int E = a.E;
     for (int w = 0; w < nw; ++w) {
         const int p0 = 16 * w;
         if (p0 >= E) return -1;
-        const int e = first_open16(prow[w], min(16, E - p0), held, s_isfull);
+        const int e = first_open16(prow[w], min(16, E - p0), held, s_fillpos, pos);
         if (e >= 0) return e;
     }
     const uint4* orow = reinterpret_cast<const uint4*>(a.prefs + static_cast<size_t>(t) * pref_stride(E));
     for (int p0 = 16 * nw; p0 < E; p0 += 16) {
-        const int e = first_open16(ld_in<NC>(orow + p0 / 16), min(16, E - p0), held, s_isfull);
+        const int e = first_open16(ld_in<NC>(orow + p0 / 16), min(16, E - p0), held, s_fillpos, pos);
         if (e >= 0) return e;
     }
     return -1;
@@ -148,7 +168,9 @@ __device__ __forceinline__ void dispatch_serial_block(const SerialArgs& sa, uint
     __shared__ int s_seg[kSerialThreads];   // stage 1: per (segment, expert) counts
     __shared__ int s_tot[256];
     __shared__ int s_cnt[kReplayWarps * 256];   // replay: per (warp, expert) window counts
-    __shared__ int s_q1, s_cut, s_estar, s_nre, s_ndrop;
+    __shared__ int16_t s_fpos[256];        // replay: window position that fills each expert
+    __shared__ int16_t s_fnext[256];       // the same from the current round's choices
+    __shared__ int s_q1, s_nre, s_ndrop;
     const DispatchArgs& a = sa.a;
     const int E = a.E, T = a.T, k = a.k, nch = a.nchunks;
     const int Q = k * nch;
@@ -166,7 +188,6 @@ __device__ __forceinline__ void dispatch_serial_block(const SerialArgs& sa, uint
     const int32_t* hist = a.hist;
     if (tid == 0) {
         s_q1 = Q;
-        s_cut = kReplayThreads;
         s_nre = 0;
         s_ndrop = 0;
     }
@@ -290,69 +311,75 @@ __device__ __forceinline__ void dispatch_serial_block(const SerialArgs& sa, uint
                 const size_t ti = static_cast<size_t>(valid ? t - tbeg : 0);
                 const uint4* prow = pfx + ti * nw;
                 Held held;
-                int want = -1, e = -1;
+                int want = -1;
                 if (valid) {
                     for (int q = 0; q < r; ++q) held.add(asg[ti * k + q]);
                     const uint4 w = prow[0];   // r < k <= 8: the first word holds rank r's pick
                     want = ((r < 4 ? w.x : w.y) >> (8 * (r & 3))) & 0xFF;
-                    e = choose_expert<NC>(a, t, prow, nw, held, s_isfull);
                 }
-                bool active = valid;
-                while (true) {
-                    // ranks among the window's active entries that chose the same expert
-                    const uint32_t peers = __match_any_sync(0xffffffffu, active ? e : -2);
+                // fill positions: -1 for experts full before the window, none yet for the rest
+                s_fpos[tid] = s_isfull[tid] ? -1 : kReplayThreads;
+                s_fnext[tid] = kReplayThreads;
+                replay_sync();
+                int e = -1, slot = 0;
+                uint32_t peers = 0;
+                bool leader = false;
+                for (int round = 0;; ++round) {
+                    // every entry chooses under the current fill positions
+                    e = valid ? choose_expert<NC>(a, t, prow, nw, held, s_fpos, tid) : -1;
+                    peers = __match_any_sync(0xffffffffu, valid ? e : -2);
                     const int rnk = __popc(peers & lanemask_lt());
-                    const bool leader = lane == __ffs(peers) - 1;
-                    const bool placed = active && e >= 0;
+                    leader = lane == __ffs(peers) - 1;
+                    const bool placed = valid && e >= 0;
                     if (placed && leader) s_cnt[warp * E + e] = __popc(peers);
                     replay_sync();
                     // slot = fill + the earlier warps' entries of the expert + rank in the warp
-                    int slot = 0;
+                    slot = 0;
                     if (placed) {
                         slot = s_fill[e] + rnk;
 #pragma unroll
                         for (int w = 0; w < kReplayWarps - 1; ++w)
                             if (w < warp) slot += s_cnt[w * E + e];
+                        if (slot == cap - 1) s_fnext[e] = static_cast<int16_t>(tid);   // takes the last slot
                     }
-                    // the first entry of the window that takes an expert's last slot
-                    const uint32_t evw = __ballot_sync(0xffffffffu, placed && slot + 1 == cap);
-                    if (evw && lane == 0) atomicMin(&s_cut, warp * 32 + __ffs(evw) - 1);
                     replay_sync();
                     if (placed && leader) s_cnt[warp * E + e] = 0;   // all reads are done
-                    const int cut = s_cut;
-                    const bool commit = active && tid <= cut;
-                    if (commit) {
-                        const size_t idx = static_cast<size_t>(t) * k + r;
-                        const size_t li = static_cast<size_t>(t - tbeg) * k + r;
-                        if (e >= 0) {
-                            const int fl = (e != want) ? 1 : 0;
-                            a.assign[idx] = e;
-                            a.slot[idx] = slot;
-                            a.flags[idx] = static_cast<uint8_t>(fl);
-                            asg[li] = static_cast<uint8_t>(e);
-                            nre += fl;
-                        } else {
-                            a.assign[idx] = -1;
-                            a.slot[idx] = -1;
-                            a.flags[idx] = 2;
-                            asg[li] = 255;
-                            ++ndrop;
-                        }
+                    bool moved = false;
+                    if (s_fpos[tid] >= 0 && s_fnext[tid] != s_fpos[tid]) {
+                        moved = true;
+                        s_fpos[tid] = s_fnext[tid];
                     }
-                    if (tid == cut) s_estar = e;
-                    // new fill: each warp's leader adds its committed entries of the expert
-                    const uint32_t cmask = __ballot_sync(0xffffffffu, commit);
-                    if (placed && leader) {
-                        const int nc = __popc(peers & cmask);
-                        if (nc && atomicAdd(&s_fill[e], nc) + nc >= cap) s_isfull[e] = 1;
+                    s_fnext[tid] = kReplayThreads;
+                    if (!replay_any(moved)) break;   // the choices reproduce their own fill positions
+                    if (round > E) {                 // unreachable: each round fixes the next fill in order
+                        if (tid == 0) record_error(a.status, MOE_ERR_TIMEOUT);
+                        break;
                     }
-                    replay_sync();
-                    if (cut >= kReplayThreads) break;   // no expert filled in this window
-                    const int estar = s_estar;
-                    active = active && tid > cut;
-                    if (active && e == estar) e = choose_expert<NC>(a, t, prow, nw, held, s_isfull);
-                    if (tid == 0) s_cut = kReplayThreads;   // read by all before the last barrier
                 }
+                // commit the window
+                if (valid) {
+                    const size_t idx = static_cast<size_t>(t) * k + r;
+                    const size_t li = static_cast<size_t>(t - tbeg) * k + r;
+                    if (e >= 0) {
+                        const int fl = (e != want) ? 1 : 0;
+                        a.assign[idx] = e;
+                        a.slot[idx] = slot;
+                        a.flags[idx] = static_cast<uint8_t>(fl);
+                        asg[li] = static_cast<uint8_t>(e);
+                        nre += fl;
+                    } else {
+                        a.assign[idx] = -1;
+                        a.slot[idx] = -1;
+                        a.flags[idx] = 2;
+                        asg[li] = 255;
+                        ++ndrop;
+                    }
+                }
+                if (valid && e >= 0 && leader) {
+                    const int nc = __popc(peers);
+                    if (atomicAdd(&s_fill[e], nc) + nc >= cap) s_isfull[e] = 1;
+                }
+                replay_sync();
             }
         }
     }

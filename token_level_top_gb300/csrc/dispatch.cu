@@ -44,7 +44,8 @@ constexpr int kSerialThreads = 1024;   // stage 1 and the staging
 constexpr int kReplayThreads = 256;    // the replay: one window entry per thread
 constexpr int kReplayWarps = kReplayThreads / 32;
 static_assert(kSerialThreads >= 255, "stage 1 needs a thread per expert");
-static_assert(kReplayThreads <= kSerialThreads && kReplayThreads % 32 == 0, "replay warps");
+static_assert(kReplayThreads <= kSerialThreads && kReplayThreads % 32 == 0 && kReplayThreads >= 256,
+              "replay warps; a thread per expert in the fill-position updates");
 // dynamic shared memory of the standalone replay block (+ about 14 KB static)
 constexpr size_t kSerialSmemCap = 208 * 1024;
 
@@ -318,8 +319,10 @@ __device__ __forceinline__ void dispatch_serial_block(const SerialArgs& sa, uint
                     want = ((r < 4 ? w.x : w.y) >> (8 * (r & 3))) & 0xFF;
                 }
                 // fill positions: -1 for experts full before the window, none yet for the rest
-                s_fpos[tid] = s_isfull[tid] ? -1 : kReplayThreads;
-                s_fnext[tid] = kReplayThreads;
+                if (tid < 256) {
+                    s_fpos[tid] = s_isfull[tid] ? -1 : kReplayThreads;
+                    s_fnext[tid] = kReplayThreads;
+                }
                 replay_sync();
                 int e = -1, slot = 0;
                 uint32_t peers = 0;
@@ -345,11 +348,13 @@ __device__ __forceinline__ void dispatch_serial_block(const SerialArgs& sa, uint
                     replay_sync();
                     if (placed && leader) s_cnt[warp * E + e] = 0;   // all reads are done
                     bool moved = false;
-                    if (s_fpos[tid] >= 0 && s_fnext[tid] != s_fpos[tid]) {
-                        moved = true;
-                        s_fpos[tid] = s_fnext[tid];
+                    if (tid < 256) {
+                        if (s_fpos[tid] >= 0 && s_fnext[tid] != s_fpos[tid]) {
+                            moved = true;
+                            s_fpos[tid] = s_fnext[tid];
+                        }
+                        s_fnext[tid] = kReplayThreads;
                     }
-                    s_fnext[tid] = kReplayThreads;
                     if (!replay_any(moved)) break;   // the choices reproduce their own fill positions
                     if (round > E) {                 // unreachable: each round fixes the next fill in order
                         if (tid == 0) record_error(a.status, MOE_ERR_TIMEOUT);

@@ -44,18 +44,17 @@ namespace {
 
 constexpr int kF4Threads = 448;   // 14 warps
 constexpr int kF4MaxBN = 256;     // widest N tile
-constexpr uint32_t kF4ABytes = 128 * 128;   // 128 rows x 256 e2m1 values
-constexpr uint32_t kF4SfABytes = 128 * 16;  // 128 rows x 16 block scales
 constexpr int kF4AccCols = 256;            // TMEM columns of the accumulator(s)
 constexpr int kF4SfCol = kF4AccCols;       // first TMEM column of the block scales
 constexpr int kF4MaxStages = 8;
 
 // Rows of B a stage holds (128, or 256 for tiles wider than 128 columns).
 __host__ __device__ constexpr int f4_b_alloc(int bn) { return bn <= 128 ? 128 : 256; }
-// Bytes of one stage: A codes, B codes, A scales, B scales; a multiple of 1024.
-__host__ __device__ constexpr uint32_t f4_stage_bytes(int bn)
+// Bytes of one stage: A codes (a_rows rows of 128 bytes: 256 e2m1 values), B
+// codes, A scales, B scales (16 bytes a row); a multiple of 1024.
+__host__ __device__ constexpr uint32_t f4_stage_bytes(int a_rows, int bn)
 {
-    return (kF4ABytes + static_cast<uint32_t>(f4_b_alloc(bn)) * 144u + kF4SfABytes + 1023u) / 1024u * 1024u;
+    return (static_cast<uint32_t>(a_rows) * 144u + static_cast<uint32_t>(f4_b_alloc(bn)) * 144u + 1023u) / 1024u * 1024u;
 }
 // TMEM columns of the scales of one MMA's B rows: N/32 rounded up to 4.
 __host__ __device__ constexpr int f4_sfb_cols(int bn) { return ((bn + 31) / 32 + 3) / 4 * 4; }
@@ -231,6 +230,7 @@ struct F4Params {
     int kb_total;   // K / 256 (stages of 128-byte rows), rounded up
     int bn;         // N tile: 256 (128 where N is not a multiple of 256); the down GEMM
                     // with one row tile per expert 64..256 (a multiple of 16)
+    int a_rows;     // rows of A a stage has room for: 128, or 32 when every tile's rows fit 32
     int b_rows;     // rows of B a stage holds (f4_b_alloc(bn))
     uint32_t stage_bytes;
     int n_tiles;    // N tiles per expert
@@ -362,8 +362,9 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int stages = p.stages;
     const uint32_t sb = p.stage_bytes;
-    const uint32_t off_sfa = kF4ABytes + static_cast<uint32_t>(p.b_rows) * 128u;   // A scales
-    const uint32_t off_sfb = off_sfa + kF4SfABytes;                                 // B scales
+    const uint32_t a_bytes = static_cast<uint32_t>(p.a_rows) * 128u;                 // A codes
+    const uint32_t off_sfa = a_bytes + static_cast<uint32_t>(p.b_rows) * 128u;         // A scales
+    const uint32_t off_sfb = off_sfa + static_cast<uint32_t>(p.a_rows) * 16u;          // B scales
     const int nacc = p.bn <= 128 ? 2 : 1;           // TMEM accumulators
     const int sfb_cols = f4_sfb_cols(p.bn);          // TMEM scale columns of one MMA's B rows
     const int sf_cols = f4_sf_stage_cols(p.bn);      // TMEM scale columns of one stage
@@ -438,7 +439,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
             const F4Tile t = f4_decode(p, tile, s_start, s_offs);
             const int arow = s_offs[t.e] + t.m * kBM;
             const int brow = (p.kind == GK_GATEUP ? t.e * 2 * p.F : t.e * p.d) + t.n * p.bn;
-            const bool few = s_offs[t.e + 1] - arow <= 32;   // the tile's rows fit a 32-row box
+            // the tile's rows fit a 32-row box (always so when the stages have room for 32)
+            const bool few = p.a_rows == 32 || s_offs[t.e + 1] - arow <= 32;
             const uint32_t bytes = (few ? 32u : 128u) * (128u + 16u) + static_cast<uint32_t>(p.bn) * (128u + 16u);
             for (int kb = 0; kb < p.kb_total; ++kb) {
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, p.budget))) {
@@ -452,10 +454,10 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                     tma_load_2d(smem_u32(st), few ? &tmA32 : &tmA, kb * 128, arow, fb);
                     tma_load_2d(smem_u32(st + off_sfa), few ? &tmSA32 : &tmSA, kb * 16, arow, fb);
                     if (p.b_policy) {
-                        tma_load_2d_hint(smem_u32(st + kF4ABytes), &tmB, kb * 128, brow, fb, pol_b);
+                        tma_load_2d_hint(smem_u32(st + a_bytes), &tmB, kb * 128, brow, fb, pol_b);
                         tma_load_2d_hint(smem_u32(st + off_sfb), &tmSB, kb * 16, brow, fb, pol_b);
                     } else {
-                        tma_load_2d(smem_u32(st + kF4ABytes), &tmB, kb * 128, brow, fb);
+                        tma_load_2d(smem_u32(st + a_bytes), &tmB, kb * 128, brow, fb);
                         tma_load_2d(smem_u32(st + off_sfb), &tmSB, kb * 16, brow, fb);
                     }
                 }
@@ -497,7 +499,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                     }
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(smem + static_cast<size_t>(stage) * sb);
-                    const uint32_t b0 = a0 + kF4ABytes;
+                    const uint32_t b0 = a0 + a_bytes;   // (A rows past a_rows read B's bytes: not stored)
                     const uint32_t sf0 = tmem_base + static_cast<uint32_t>(kF4SfCol + sf_cols * stage);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)   // K = 64 per instruction: 32 bytes of each row
@@ -774,8 +776,11 @@ cudaError_t launch_gemm_nvfp4(const F4Launch& g, cudaStream_t s)
         }
     }
     if (g.kind == GK_GATEUP && N % p.bn != 0) return cudaErrorInvalidValue;
+    // with at most 32 rows per expert every tile loads a 32-row A box: the stages
+    // keep room for 32 rows only, which leaves room for more stages
+    p.a_rows = (one_tile && std::min<long long>(g.rows_cap, static_cast<long long>(g.T)) <= 32) ? 32 : 128;
     p.b_rows = f4_b_alloc(p.bn);
-    p.stage_bytes = f4_stage_bytes(p.bn);
+    p.stage_bytes = f4_stage_bytes(p.a_rows, p.bn);
     p.n_tiles = (N + p.bn - 1) / p.bn;
     const uint64_t arows = static_cast<uint64_t>(g.T) * g.topk;
     const uint64_t brows = static_cast<uint64_t>(g.E) * N;

@@ -201,7 +201,9 @@ def recorded_traffic(kernel: str, workload: str):
     if not os.path.exists(p):
         return None
     with open(p) as fh:
-        rec = json.load(fh).get(kernel)
+        recs = json.load(fh)
+    # a capture of the kernel on this workload ("<kernel> @ <workload>"), or its only one
+    rec = recs.get(f"{kernel} @ {workload}") or recs.get(kernel)
     if not rec or rec.get("workload") != workload:
         return None
     h = hashlib.sha256()

@@ -152,6 +152,11 @@ DISPATCH_CASES = [
     ("small-E255-k8", 250, 255, 8, 1.0, 3, "gauss"),
     ("small-E64-deep", 256, 64, 2, 1.0, 2, "identical"),
     ("small-E128-k4", 199, 128, 4, 1.0, 0, "skew"),
+    # capacity well below demand: many fills per replay window, interacting through the
+    # reroutes they cause (up to 9 fixed-point rounds in a window), and drops
+    ("fills-interact-k8", 3000, 64, 8, 0.5, 0, "skew"),
+    ("fills-dense-E256", 6000, 256, 4, 0.4, 0, "gauss"),
+    ("small-many-fills", 256, 32, 4, 0.3, 0, "gauss"),
 ]
 
 

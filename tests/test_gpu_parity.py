@@ -155,7 +155,7 @@ DISPATCH_CASES = [
     # capacity well below demand: many fills per replay window, interacting through the
     # reroutes they cause (up to 9 fixed-point rounds in a window), and drops
     ("fills-interact-k8", 3000, 64, 8, 0.5, 0, "skew"),
-    ("fills-dense-E256", 6000, 256, 4, 0.4, 0, "gauss"),
+    ("fills-dense-E255", 6000, 255, 4, 0.4, 0, "gauss"),
     ("small-many-fills", 256, 32, 4, 0.3, 0, "gauss"),
 ]
 

@@ -20,12 +20,14 @@
 //   nibble; block scales are bytes, rows of them padded to 16 bytes.
 //
 // GEMM kernel: one persistent CTA per SM, 14 warps -- warp 0 TMA producer
-// (per stage the codes of 128 rows x 256 values of A and of up to 256 rows of
-// B, and their block scales, 16 bytes a row), warp 1 allocates TMEM and issues
+// (per stage the block scales, 16 bytes a row, first and on a barrier of their
+// own, then the codes of 128 rows x 256 values of A and of up to 256 rows of
+// B), warp 1 allocates TMEM and issues
 // the MMAs (M = 128, N = the tile width, up to 256), warps 2-5 and 10-13 the
 // epilogue (two warps per lane quarter, each with half of the tile's columns),
 // warps 6-9 copy each stage's block scales from shared memory into TMEM
-// (tcgen05.st): for each MMA, column i of lane l (in each of the four 32-lane
+// (tcgen05.st) as soon as they land, while the codes are still in flight, and
+// arrive on the barrier the MMA thread waits on besides the codes': for each MMA, column i of lane l (in each of the four 32-lane
 // quarters) holds the four scale bytes of row l + 32i of A (4 columns) and of
 // B (N/32 columns, rounded up to 4; byte b: the scale of the MMA's b-th block
 // of 16 along K).  Tiles of up to 128 columns have two TMEM accumulators
@@ -369,12 +371,13 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     const int sfb_cols = f4_sfb_cols(p.bn);          // TMEM scale columns of one MMA's B rows
     const int sf_cols = f4_sf_stage_cols(p.bn);      // TMEM scale columns of one stage
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(stages) * sb);
-    uint64_t* full_bar = bars;
+    uint64_t* full_bar = bars;                 // the stage's codes (A and B) have landed
     uint64_t* empty_bar = bars + stages;
-    uint64_t* sf_bar = bars + 2 * stages;
-    uint64_t* tfull_bar = bars + 3 * stages;
-    uint64_t* tempty_bar = bars + 3 * stages + 2;
-    int* s_start = reinterpret_cast<int*>(bars + 3 * stages + 4);
+    uint64_t* sf_bar = bars + 2 * stages;      // the stage's block scales are in TMEM
+    uint64_t* sfull_bar = bars + 3 * stages;   // the stage's block scales have landed
+    uint64_t* tfull_bar = bars + 4 * stages;
+    uint64_t* tempty_bar = bars + 4 * stages + 2;
+    int* s_start = reinterpret_cast<int*>(bars + 4 * stages + 4);
     int* s_offs = s_start + (p.E + 1);
     volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(s_offs + (p.E + 1));
     float* s_bsc = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(s_tmem + 1) + 15) & ~uintptr_t(15));
@@ -390,6 +393,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         tma_prefetch_desc(&tmSA32);
         for (int i = 0; i < stages; ++i) {
             mbar_init(smem_u32(&full_bar[i]), 1);
+            mbar_init(smem_u32(&sfull_bar[i]), 1);
             mbar_init(smem_u32(&empty_bar[i]), 1);
             mbar_init(smem_u32(&sf_bar[i]), 4);   // the four scale-copying warps
         }
@@ -441,25 +445,30 @@ __global__ void __launch_bounds__(kF4Threads, 1)
             const int brow = (p.kind == GK_GATEUP ? t.e * 2 * p.F : t.e * p.d) + t.n * p.bn;
             // the tile's rows fit a 32-row box (always so when the stages have room for 32)
             const bool few = p.a_rows == 32 || s_offs[t.e + 1] - arow <= 32;
-            const uint32_t bytes = (few ? 32u : 128u) * (128u + 16u) + static_cast<uint32_t>(p.bn) * (128u + 16u);
+            const uint32_t rows = (few ? 32u : 128u) + static_cast<uint32_t>(p.bn);   // A and B rows per stage
             for (int kb = 0; kb < p.kb_total; ++kb) {
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, p.budget))) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
+                    // the block scales first, on their own barrier: the scale warps copy
+                    // them into TMEM while the codes are still in flight
+                    const uint32_t sfb = smem_u32(&sfull_bar[stage]);
                     const uint32_t fb = smem_u32(&full_bar[stage]);
-                    mbar_arrive_expect_tx(fb, bytes);
                     uint8_t* st = smem + static_cast<size_t>(stage) * sb;
+                    mbar_arrive_expect_tx(sfb, rows * 16u);
+                    tma_load_2d(smem_u32(st + off_sfa), few ? &tmSA32 : &tmSA, kb * 16, arow, sfb);
+                    if (p.b_policy)
+                        tma_load_2d_hint(smem_u32(st + off_sfb), &tmSB, kb * 16, brow, sfb, pol_b);
+                    else
+                        tma_load_2d(smem_u32(st + off_sfb), &tmSB, kb * 16, brow, sfb);
+                    mbar_arrive_expect_tx(fb, rows * 128u);
                     tma_load_2d(smem_u32(st), few ? &tmA32 : &tmA, kb * 128, arow, fb);
-                    tma_load_2d(smem_u32(st + off_sfa), few ? &tmSA32 : &tmSA, kb * 16, arow, fb);
-                    if (p.b_policy) {
+                    if (p.b_policy)
                         tma_load_2d_hint(smem_u32(st + a_bytes), &tmB, kb * 128, brow, fb, pol_b);
-                        tma_load_2d_hint(smem_u32(st + off_sfb), &tmSB, kb * 16, brow, fb, pol_b);
-                    } else {
+                    else
                         tma_load_2d(smem_u32(st + a_bytes), &tmB, kb * 128, brow, fb);
-                        tma_load_2d(smem_u32(st + off_sfb), &tmSB, kb * 16, brow, fb);
-                    }
                 }
                 __syncwarp();
                 issued_mask |= 1u << stage;
@@ -473,7 +482,10 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         if (!ok) {
             record_error(p.status, MOE_ERR_TIMEOUT);
             for (int s = 0; s < stages; ++s)
-                if (issued_mask & (1u << s)) mbar_wait(smem_u32(&full_bar[s]), (issued_parity >> s) & 1, p.budget);
+                if (issued_mask & (1u << s)) {
+                    mbar_wait(smem_u32(&sfull_bar[s]), (issued_parity >> s) & 1, p.budget);
+                    mbar_wait(smem_u32(&full_bar[s]), (issued_parity >> s) & 1, p.budget);
+                }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -527,7 +539,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         uint32_t phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             for (int kb = 0; kb < p.kb_total; ++kb) {
-                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[stage]), phase, p.budget))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sfull_bar[stage]), phase, p.budget))) {
                     record_error(p.status, MOE_ERR_TIMEOUT);
                     tile = total;
                     break;
@@ -793,15 +805,15 @@ cudaError_t launch_gemm_nvfp4(const F4Launch& g, cudaStream_t s)
         !make_byte_map(&tmA32, g.a_codes, arows, K / 2, K / 2, 32, 128) ||
         !make_byte_map(&tmSA32, g.a_sf, arows, K / 16, sfs, 32, 16))
         return cudaErrorInvalidValue;
-    // shared memory: the stages (each with its three barriers), the two accumulator
+    // shared memory: the stages (each with its four barriers), the two accumulator
     // barriers, the tile starts and offsets, the TMEM address, the weight-row scales
     const size_t fixed = 1024 + 64 + static_cast<size_t>(2 * (g.E + 1)) * 4 + 16 + 16 + 4 * kF4MaxBN;
-    const int by_smem = static_cast<int>((227 * 1024 - fixed) / (p.stage_bytes + 24));
+    const int by_smem = static_cast<int>((227 * 1024 - fixed) / (p.stage_bytes + 32));
     const int by_tmem = (512 - kF4SfCol) / f4_sf_stage_cols(p.bn);
     const int stages = std::min(kF4MaxStages, std::min(by_smem, by_tmem));
     if (stages < 2) return cudaErrorInvalidValue;
     p.stages = stages;
-    const size_t smem = fixed + static_cast<size_t>(stages) * (p.stage_bytes + 24);
+    const size_t smem = fixed + static_cast<size_t>(stages) * (p.stage_bytes + 32);
     const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(moe_gemm_nvfp4_kernel), 227 * 1024);
     if (e != cudaSuccess) return e;
     const long long mt_max = (static_cast<long long>(g.T) * g.topk + kBM - 1) / kBM + g.E;

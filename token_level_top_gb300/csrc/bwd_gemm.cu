@@ -128,6 +128,14 @@ __device__ __forceinline__ BTile decode(const BwdGemmParams& p, int tile, const 
 // MN-major operand of the pair MMA: each CTA's part is `blocks` 64-column boxes.
 constexpr uint32_t kStageTileBytes = kBoxBytes;
 
+// Arrival on the first CTA's accumulator barrier with a CTA-scope release: the
+// first CTA's MMAs depend only on this CTA's TMEM reads, complete before the
+// arrival (tcgen05.wait::ld), not on the epilogue's fp32 row stores.
+__device__ __forceinline__ void mbar_arrive_peer_cta(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 template <bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -399,7 +407,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 if (PAIR && !leader)   // the leader's MMAs wait for both CTAs' epilogues
-                    mbar_arrive_cluster(map_to_rank(smem_u32(&tempty_bar[b]), 0));
+                    mbar_arrive_peer_cta(map_to_rank(smem_u32(&tempty_bar[b]), 0));
                 else
                     mbar_arrive(smem_u32(&tempty_bar[b]));
             }

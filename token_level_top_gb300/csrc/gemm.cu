@@ -115,6 +115,16 @@ __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)
 // The per-row activation scale and per-row weight scale multiply the
 // accumulator in the epilogue.
 
+// Arrival on the first CTA's accumulator barrier with a CTA-scope release: what
+// the first CTA's MMAs depend on is this CTA's TMEM, whose reads are complete
+// (tcgen05.wait::ld) before the arrival, so no cluster-wide fence over the
+// epilogue's row stores is needed (a cluster-scope release waited for them: the
+// e4m3 prefill gate-up took 637 us with it, 621 us without).
+__device__ __forceinline__ void mbar_arrive_peer_cta(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 template <bool PAIR, bool FP8>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -471,7 +481,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 if (PAIR && !leader)   // the leader's MMAs wait for both CTAs' epilogues
-                    mbar_arrive_cluster(map_to_rank(smem_u32(&tempty_bar[b]), 0));
+                    mbar_arrive_peer_cta(map_to_rank(smem_u32(&tempty_bar[b]), 0));
                 else
                     mbar_arrive(smem_u32(&tempty_bar[b]));
             }

@@ -45,6 +45,9 @@ def test_quantize_nvfp4_matches_oracle(rows, cols):
     if rows > 2:
         w[1, : cols // 2] *= 1e-4              # blocks far below the row's largest value
         w[2, 16:32] = 0                        # an all-zero block
+    if rows > 4:
+        w[3] *= 1e-30                          # block divisors below 2^-92: the plain-division path
+        w[4, : cols // 2] *= 1e-36             # blocks in bf16's subnormal range beside normal ones
     w = w.to(torch.bfloat16)
     got = moe.quantize_nvfp4(w.cuda())
     assert_quantised_equal(got, oracle_rows(w), cols)

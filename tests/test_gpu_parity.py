@@ -177,6 +177,36 @@ def test_dispatch_shared_scores(case):
     np.testing.assert_allclose(np_(g["cw"]), o["cw"], rtol=WEIGHT_RTOL, atol=1e-7)
 
 
+def _random_dispatch_case(i):
+    rng = np.random.default_rng(1000 + i)
+    T = int(rng.choice([1, 7, 64, 200, 256, 257, 700, 1500, 3000]))
+    E = int(rng.choice([2, 3, 8, 16, 33, 64, 128, 200, 255]))
+    k = int(min(E, rng.choice([1, 2, 2, 3, 4, 8])))
+    cf = float(rng.choice([0.2, 0.3, 0.5, 0.8, 1.0, 1.25, 2.0]))
+    cap = int(rng.integers(1, 6)) if rng.random() < 0.15 else 0
+    kind = str(rng.choice(["gauss", "skew", "ties", "runs", "identical"]))
+    return T, E, k, cf, cap, kind
+
+
+@pytest.mark.parametrize("i", range(40))
+def test_dispatch_random_shapes(i):
+    """Seeded random shapes and capacities (many fills per replay window, drops, one-chunk
+    and multi-chunk batches, k up to 8, E up to 255): the dispatch equals the oracle's."""
+    T, E, k, cf, cap, kind = _random_dispatch_case(i)
+    s = _scores(kind, T, E, 77 * i + 5)
+    cfg = _cfg(T, E, k, cf=cf, cap=cap)
+    C = moe.capacity(T, k, E, cf, cap)
+    assert C == oracle.capacity(T, k, E, cf, cap)
+    ws = moe.workspace(cfg)
+    g = moe.dispatch(cfg, ws, torch.from_numpy(s).cuda())
+    assert moe.device_status(ws) == 0
+    o = oracle.dispatch(s, k, C)
+    assert_dispatch_equal(g, o, T, k)
+    assert int(np_(g["n_rerouted"])[0]) == o["n_rerouted"]
+    assert int(np_(g["n_dropped"])[0]) == o["n_dropped"]
+    assert np.array_equal(np_(g["counts"]), o["counts"])
+
+
 def test_dispatch_repeatable():
     s = _scores("skew", 4000, 16, 3)
     cfg = _cfg(4000, 16, 2, cf=1.0)

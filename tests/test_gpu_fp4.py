@@ -166,6 +166,25 @@ def test_layer_forward_nvfp4_workloads(name):
     assert_rows_close(np_(out.float())[toks], want)
 
 
+@pytest.mark.parametrize("T,E,k,cap", [(1, 8, 2, 0), (64, 1, 1, 0), (257, 4, 2, 30), (200, 40, 2, 2),
+                                       (1200, 16, 4, 0)])
+def test_layer_forward_nvfp4_edge_shapes(T, E, k, cap):
+    """One token, one expert, forced small capacities with drops, k = 4: every token's row
+    against the oracle (all-dropped tokens give zero rows)."""
+    shape = synth.MoEShape("edge", T=T, d=128, E=E, F=256, k=k, cf=1.0, capacity=cap, seed=T + E)
+    Ld = make_layer(shape)
+    cfg = moe.Config.of(shape, flags=moe.FLAG_NVFP4)
+    ws = moe.workspace(cfg)
+    q13, q2, (w1, w3, w2) = quantized(Ld, shape)
+    out, aux = moe.layer_forward(cfg, ws, Ld["h"], Ld["wr"], q13, q2, aux=True)
+    assert moe.device_status(ws) == 0
+    C = oracle.capacity(T, k, E, 1.0, cap)
+    o_d = oracle.dispatch(oracle.route(k, logits_in=np_(aux["logits"]))["scores"], k, C)
+    assert_dispatch_equal(aux, o_d, T, k)
+    want = oracle.combine_rows_q4(bits(Ld["h"]), w1, w3, w2, o_d["assign"], o_d["cw"], np.arange(T, dtype=np.int32))
+    assert_rows_close(np_(out.float()), want)
+
+
 def test_layer_forward_nvfp4_deterministic():
     shape = synth.CONFIGS["tiny"]
     Ld = make_layer(shape)

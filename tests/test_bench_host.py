@@ -50,3 +50,18 @@ def test_recorded_traffic_only_for_the_captured_source(tmp_path, monkeypatch):
 def test_recorded_traffic_dropped_after_a_source_change(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", _traffic_root(tmp_path, "int a; // edited", "int a;"))
     assert bench.recorded_traffic("kern", "w") is None
+
+
+def test_recorded_traffic_per_workload_key(tmp_path, monkeypatch):
+    """A second capture of the same kernel on another workload lives under
+    "<kernel> @ <workload>"; the plain key keeps serving its own workload."""
+    root = _traffic_root(tmp_path, "int a;", "int a;")
+    p = tmp_path / "profiles" / "traffic.json"
+    rec = json.loads(p.read_text())
+    rec["kern @ w2"] = dict(rec["kern"], workload="w2", dram_bytes_per_launch=456)
+    p.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", root)
+    assert bench.recorded_traffic("kern", "w") == 123
+    assert bench.recorded_traffic("kern", "w2") == 456
+    assert bench.recorded_traffic("kern", "w3") is None
+

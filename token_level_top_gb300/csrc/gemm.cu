@@ -107,7 +107,16 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile,
     return ti;
 }
 
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
+// silu(x) = x sigmoid(x) = (x/2)(1 + tanh(x/2)), with the hardware tanh approximation
+// (one MUFU operation; its error stays inside the bf16 rounding of the activation).
+// Same box, alternating runs: e4m3 prefill gate-up 624 -> 609 us, bf16 1160 -> 1149 us.
+__device__ __forceinline__ float silu_f(float x)
+{
+    float t;
+    const float h = 0.5f * x;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+    return h * (1.0f + t);
+}
 
 // FP8: e4m3 activations and weights on tcgen05.mma.kind::f8f6f4.  A stage
 // row is 128 bytes either way (64 bf16 or 128 e4m3 values), so the tiles,

@@ -54,7 +54,7 @@ class Config:
     cf: float = 1.25
     capacity: int = 0
     lam: float = 0.0
-    flags: int = 0   # FLAG_FP8: the workspace also serves the e4m3 (FP8) entry points
+    flags: int = 0   # FLAG_FP8 / FLAG_NVFP4 / FLAG_BACKWARD: the workspace also serves those entry points
     tau: float = 1.0           # router temperature
     router_norm: int = 0       # NORM_LAYER / NORM_L2: normalise h before the router
     norm_eps: float = 1e-5

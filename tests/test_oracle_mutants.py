@@ -35,6 +35,22 @@ MUTANTS = {
                                   ["test_temperature_comes_before_the_penalty"]),
     "P_not_averaged": ([("P[e] = T > 0 ? (float)(psum[e] / (double)T) : 0.0f;",
                          "P[e] = T > 0 ? (float)(psum[e]) : 0.0f;")], ["test_softmax_and_stats_match_scipy"]),
+    "P_of_topk_only": ([("for (int e = 0; e < E; ++e) psum[e] += p[e];",
+                         "for (int r = 0; r < k; ++r) psum[order[r]] += p[order[r]];")],
+                       ["test_softmax_and_stats_match_scipy"]),
+    "f_not_over_T": ([("f[e] = T > 0 ? (float)((double)counts_pre[e] / (double)T) : 0.0f;",
+                       "f[e] = T > 0 ? (float)counts_pre[e] : 0.0f;")], ["test_softmax_and_stats_match_scipy"]),
+    "softmax_of_logits": ([("softmax_row(E, s, p);", "softmax_row(E, z, p);")],
+                          ["test_softmax_and_stats_match_scipy", "test_temperature_sharpens_softmax"]),
+    # router front end ([2kiu] §5.2 normalisation; [cnnetsun] §3.1 two-layer router)
+    "layernorm_unbiased_variance": ([("var /= (double)d;", "var /= (double)(d - 1);")],
+                                    ["test_layernorm_worked_example", "test_layernorm_router_reduces_to_torch"]),
+    "layernorm_eps_outside_sqrt": ([("1.0 / sqrt(var + (double)eps)", "1.0 / (sqrt(var) + (double)eps)")],
+                                   ["test_layernorm_router_reduces_to_torch"]),
+    "l2_eps_added": ([("if (nrm < (double)eps) nrm = (double)eps;", "nrm += (double)eps;")],
+                     ["test_l2_norm_eps_is_a_floor"]),
+    "router_hidden_no_silu": ([("a[j] = u / (1.0 + exp(-u));", "a[j] = u;")],
+                              ["test_two_layer_router_identity_is_silu", "test_two_layer_router_reduces_to_torch"]),
     # dispatch ([mhpn] §2.3 the 128th token; rank-major order; capacity cap)
     "rank_minor_order": ([("for (int r = 0; r < k; ++r) {\n            for (int t = 0; t < T; ++t) {",
                            "for (int t = 0; t < T; ++t) {\n            for (int r = 0; r < k; ++r) {")],
@@ -44,10 +60,23 @@ MUTANTS = {
     "no_held_check": ([("if (held) continue;", "(void)held;")], ["test_dispatch_brute_force_tiny"]),
     "weights_not_renormalised": ([("(float)(p[e] / tot)", "(float)(p[e])")],
                                  ["test_k1_weight_is_one", "test_reroute_weight_uses_the_expert_actually_used"]),
+    "reroute_weight_of_first_pick": ([("(float)(p[e] / tot)", "(float)(p[order[(size_t)t * E + r]] / tot)")],
+                                     ["test_reroute_weight_uses_the_expert_actually_used"]),
+    "reroute_flag_against_rank0": ([("flags[idx] = (chosen != pi[r]) ? 1 : 0;",
+                                     "flags[idx] = (chosen != pi[0]) ? 1 : 0;")],
+                                   ["test_dispatch_invariants_random"]),
+    "perm_holds_token": ([("perm[offsets[assign[idx]] + slot[idx]] = (int32_t)idx;",
+                           "perm[offsets[assign[idx]] + slot[idx]] = (int32_t)t;")],
+                         ["test_dispatch_invariants_random"]),
     # experts ([mhpn] §3.1 SwiGLU W1 gate, W3 up)
     "gate_up_swapped": ([("a[j] = silu(g) * u;", "a[j] = silu(u) * g;")],
                         ["test_gate_and_up_branches_are_not_swapped"]),
+    "silu_sign": ([("static double silu(double x) { return x / (1.0 + exp(-x)); }",
+                    "static double silu(double x) { return x / (1.0 + exp(x)); }")],
+                  ["test_dense_swiglu_reduces_to_torch"]),
     # e4m3 format and the FP8 expert path ([2kiu] §5.1 quantised experts)
+    "e4m3_subnormal_step": ([("double q = a / ldexp(1.0, -9);", "double q = a / ldexp(1.0, -10);")],
+                            ["test_e4m3_encode_matches_torch", "test_e4m3_encode_inverts_decode"]),
     "e4m3_ties_away": ([("double m = (q - f > 0.5 || (q - f == 0.5 && fmod(f, 2.0) != 0.0)) ? f + 1.0 : f;\n"
                          "    if (m == 8.0)",
                          "double m = (q - f >= 0.5) ? f + 1.0 : f;\n    if (m == 8.0)")],
@@ -99,6 +128,26 @@ MUTANTS = {
                                    ["test_q4_activation_quantisation_hand_case"]),
     "q4_token_rows_not_quantised": ([("nvfp4_row(d, tmp, xf);", "(void)0;")],
                                     ["test_q4_activation_quantisation_hand_case"]),
+    "q4_weight_row_scale_dropped": ([("e2m1_tab[code] * e4m3_tab[w->bs[(r * w->cols + c) / 16]] * (double)w->s[r];",
+                                      "e2m1_tab[code] * e4m3_tab[w->bs[(r * w->cols + c) / 16]];")],
+                                    ["test_q4_experts_equal_bf16_experts_on_exact_weights"]),
+    "q4_act_blocks_of_32": ([("oracle_e4m3_value(bs[i / 16])", "oracle_e4m3_value(bs[i / 32])")],
+                            ["test_q4_activation_quantisation_hand_case"]),
+    # backward with the routing held fixed ([cnnetsun] §4.2 aux loss; [coreui] §3.1)
+    "bwd_dsilu_drops_term": ([("sg * (1.0 + g[j] * (1.0 - sg))", "sg")],
+                             ["test_backward_dense_swiglu_is_torch_autograd"]),
+    "bwd_dh_misses_up_branch": ([("(double)bf16_to_f32(W1[(size_t)j * d + i]) * dg +\n"
+                                  "                                             (double)bf16_to_f32(W3[(size_t)j * d + i]) * du;",
+                                  "(double)bf16_to_f32(W1[(size_t)j * d + i]) * dg;")],
+                                ["test_backward_dense_swiglu_is_torch_autograd"]),
+    "bwd_renorm_mean_dropped": ([("dp[e] += (dcw[r] - m) / S;", "dp[e] += dcw[r] / S;")],
+                                ["test_backward_matches_torch_autograd"]),
+    "bwd_tau_dropped": ([("const double dz = p[e] * (dp[e] - pd) / (double)tau;",
+                          "const double dz = p[e] * (dp[e] - pd);")], ["test_backward_matches_torch_autograd"]),
+    "bwd_dP_not_over_T": ([("dp[e] = dP ? (double)dP[e] / (double)T : 0.0;", "dp[e] = dP ? (double)dP[e] : 0.0;")],
+                          ["test_backward_dropped_token_gets_only_the_aux_gradient"]),
+    "bwd_dh_misses_router": ([("dh[(size_t)t * d + i] += dz * (double)bf16_to_f32(we[i]);", "(void)we;")],
+                             ["test_backward_matches_torch_autograd"]),
 }
 
 

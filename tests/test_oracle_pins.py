@@ -995,6 +995,16 @@ def test_l2_norm_worked_example_and_torch():
     np.testing.assert_allclose(z, want.numpy().astype(np.float32), rtol=2e-7, atol=1e-7)
 
 
+def test_l2_norm_eps_is_a_floor():
+    """eps bounds the divisor from below (h / max(|h|, eps), torch's normalize): a row shorter
+    than eps is divided by eps itself, a longer row by its norm; eps is not added to the norm."""
+    h = bf16([[0.25, 0.5, 0, 0], [3, 4, 0, 0], [0, 0, 0, 0]])   # norms 0.559, 5, 0
+    z = oracle.router_logits(h, _eye(4), norm=oracle.NORM_L2, eps=1.0)
+    np.testing.assert_allclose(z, [[0.25, 0.5, 0, 0], [0.6, 0.8, 0, 0], [0, 0, 0, 0]], rtol=1e-7)
+    x = torch.nn.functional.normalize(torch.from_numpy(widen(h)).double(), p=2.0, dim=1, eps=1.0)
+    np.testing.assert_allclose(z, x.numpy().astype(np.float32), rtol=1e-7)
+
+
 def test_two_layer_router_identity_is_silu():
     # W1 = W2 = I: z = silu(h); silu(1) = 1 / (1 + e^-1), silu(-1) = -e^-1 / (1 + e^-1)
     z = oracle.router_logits(bf16([[0, 1, -1, 2]]), _eye(4), w2=_eye(4))

@@ -51,6 +51,18 @@ MUTANTS = {
                      ["test_l2_norm_eps_is_a_floor"]),
     "router_hidden_no_silu": ([("a[j] = u / (1.0 + exp(-u));", "a[j] = u;")],
                               ["test_two_layer_router_identity_is_silu", "test_two_layer_router_reduces_to_torch"]),
+    "capacity_override_ignored": ([("if (explicit_cap > 0) return explicit_cap;", "(void)explicit_cap;")],
+                                  ["test_capacity_explicit_override"]),
+    "logits_bias_dropped": ([("                if (bias) acc += (double)bias[e];\n                z[e] = (float)acc;",
+                              "                z[e] = (float)acc;")], ["test_logits_match_float64_matmul"]),
+    "temperature_multiplies": ([("volatile float zt = z[e] / tau;", "volatile float zt = z[e] * tau;")],
+                               ["test_temperature_comes_before_the_penalty", "test_temperature_sharpens_softmax"]),
+    "nan_not_rejected": ([("if (isnan(s_row[e])) return 5;", "(void)0;")], ["test_nan_score_is_an_error"]),
+    "softmax_inf_limit_uniform": ([("p[e] = ((double)s[e] == m) ? 1.0 / n : 0.0;", "p[e] = 1.0 / E;")],
+                                  ["test_softmax_limits"]),
+    "layernorm_gamma_beta_swapped": ([("(gamma ? (double)gamma[i] : 1.0) + (beta ? (double)beta[i] : 0.0)",
+                                       "(beta ? (double)beta[i] : 1.0) + (gamma ? (double)gamma[i] : 0.0)")],
+                                     ["test_layernorm_worked_example", "test_layernorm_router_reduces_to_torch"]),
     # dispatch ([mhpn] §2.3 the 128th token; rank-major order; capacity cap)
     "rank_minor_order": ([("for (int r = 0; r < k; ++r) {\n            for (int t = 0; t < T; ++t) {",
                            "for (int t = 0; t < T; ++t) {\n            for (int r = 0; r < k; ++r) {")],
@@ -68,6 +80,9 @@ MUTANTS = {
     "perm_holds_token": ([("perm[offsets[assign[idx]] + slot[idx]] = (int32_t)idx;",
                            "perm[offsets[assign[idx]] + slot[idx]] = (int32_t)t;")],
                          ["test_dispatch_invariants_random"]),
+    "drop_flag_value": ([("flags[idx] = 2;", "flags[idx] = 3;")], ["test_drop_case"]),
+    "reroutes_counted_for_every_pick": ([("nre += (chosen != pi[r]);", "nre += 1;")],
+                                        ["test_worked_case_128_identical_tokens", "test_page_overflow_case"]),
     # experts ([mhpn] §3.1 SwiGLU W1 gate, W3 up)
     "gate_up_swapped": ([("a[j] = silu(g) * u;", "a[j] = silu(u) * g;")],
                         ["test_gate_and_up_branches_are_not_swapped"]),
@@ -77,6 +92,12 @@ MUTANTS = {
     # e4m3 format and the FP8 expert path ([2kiu] §5.1 quantised experts)
     "e4m3_subnormal_step": ([("double q = a / ldexp(1.0, -9);", "double q = a / ldexp(1.0, -10);")],
                             ["test_e4m3_encode_matches_torch", "test_e4m3_encode_inverts_decode"]),
+    "e4m3_saturates_to_nan": ([("if (a >= 448.0) return sign | 0x7E;", "if (a >= 448.0) return sign | 0x7F;")],
+                              ["test_e4m3_encode_ties_and_saturation"]),
+    "e4m3_nan_encodes_as_zero": ([("if (isnan(v)) return 0x7F;", "if (isnan(v)) return 0;")],
+                                 ["test_e4m3_nan_codes"]),
+    "q8_zero_row_scale_0": ([("const float s = amax > 0.0f ? amax / 448.0f : 1.0f;", "const float s = amax / 448.0f;")],
+                            ["test_quantize_row_matches_torch"]),
     "e4m3_ties_away": ([("double m = (q - f > 0.5 || (q - f == 0.5 && fmod(f, 2.0) != 0.0)) ? f + 1.0 : f;\n"
                          "    if (m == 8.0)",
                          "double m = (q - f >= 0.5) ? f + 1.0 : f;\n    if (m == 8.0)")],
@@ -111,6 +132,14 @@ MUTANTS = {
     # NVFP4: e2m1 elements with e4m3 scales per 16 and a row scale ([2kiu] §5.1 4-bit experts)
     "e2m1_ties_away": ([("if (dd < bd || (dd == bd && (c & 1) == 0 && (best & 1) == 1))", "if (dd <= bd)")],
                        ["test_e2m1_encode_is_nearest_with_ties_to_even", "test_q4_activation_quantisation_hand_case"]),
+    "e2m1_subnormal_doubled": ([("const double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);",
+                                 "const double v = (e == 0) ? 1.0 * m : ldexp(1.0 + 0.5 * m, e - 1);")],
+                               ["test_e2m1_all_codes"]),
+    "nvfp4_zero_row_scale_0": ([("const float s = amax > 0.0f ? amax / 2688.0f : 1.0f;", "const float s = amax / 2688.0f;")],
+                               ["test_nvfp4_zero_row_and_underflowing_block"]),
+    "nvfp4_zero_divisor_saturates": ([("const uint8_t c = den > 0.0f ? oracle_e2m1_encode(x[i] / den) : 0;",
+                                       "const uint8_t c = oracle_e2m1_encode(x[i] / den);")],
+                                     ["test_nvfp4_zero_row_and_underflowing_block"]),
     "nvfp4_scale_448": ([("amax / 2688.0f", "amax / 448.0f")],
                         ["test_nvfp4_row_quantisation_is_exact_on_representable_rows",
                          "test_nvfp4_row_quantisation_hand_case"]),
@@ -140,6 +169,13 @@ MUTANTS = {
                                   "                                             (double)bf16_to_f32(W3[(size_t)j * d + i]) * du;",
                                   "(double)bf16_to_f32(W1[(size_t)j * d + i]) * dg;")],
                                 ["test_backward_dense_swiglu_is_torch_autograd"]),
+    "bwd_dy_without_weight": ([("dy[c] = cw[r] * (double)gt[c];", "dy[c] = (double)gt[c];")],
+                              ["test_backward_matches_torch_autograd"]),
+    "bwd_dw2_of_gate": ([("DW2[(size_t)c * F + j] += dy[c] * a[j];", "DW2[(size_t)c * F + j] += dy[c] * g[j];")],
+                        ["test_backward_dense_swiglu_is_torch_autograd"]),
+    "bwd_dw1_dw3_swapped": ([("DW1[(size_t)j * d + i] += dg * x[i];\n                    DW3[(size_t)j * d + i] += du * x[i];",
+                              "DW1[(size_t)j * d + i] += du * x[i];\n                    DW3[(size_t)j * d + i] += dg * x[i];")],
+                            ["test_backward_dense_swiglu_is_torch_autograd"]),
     "bwd_renorm_mean_dropped": ([("dp[e] += (dcw[r] - m) / S;", "dp[e] += dcw[r] / S;")],
                                 ["test_backward_matches_torch_autograd"]),
     "bwd_tau_dropped": ([("const double dz = p[e] * (dp[e] - pd) / (double)tau;",

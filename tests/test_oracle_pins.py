@@ -525,6 +525,9 @@ def test_e4m3_known_codes(code, value):
 
 def test_e4m3_nan_codes():
     assert math.isnan(oracle.e4m3_value(0x7F)) and math.isnan(oracle.e4m3_value(0xFF))
+    # encoding NaN gives the positive NaN code, as torch's float8_e4m3fn conversion does
+    ref = torch.tensor([float("nan")]).to(torch.float8_e4m3fn).view(torch.uint8).item()
+    assert oracle.e4m3_encode(float("nan")) == ref == 0x7F
 
 
 def test_e4m3_all_codes_match_torch():
@@ -815,6 +818,24 @@ def test_nvfp4_row_quantisation_hand_case():
     nib = [(codes[i // 2] >> (4 * (i & 1))) & 15 for i in range(32)]
     assert nib[:4] == [7, 4, 2, 1] and nib[16:18] == [15, 5]
     assert not any(nib[4:16]) and not any(nib[18:])
+
+
+def test_nvfp4_zero_row_and_underflowing_block():
+    """The two degenerate cases of the row quantisation.  An all-zero row has row scale 1
+    and every code and block scale 0.  A block whose maximum is below about 2^-21 of the
+    row's maximum gets a block scale that rounds to the e4m3 zero: with max 1e-7 against
+    1.0, u = 1e-7 * 2688 / 6 = 4.48e-5, under half the smallest subnormal (2^-10).  Its
+    divisor is then 0, and its codes are 0 (not saturated by x / 0), so the block
+    decodes to zeros."""
+    codes, bs, sc = oracle.quantize_row_nvfp4(np.zeros(32, np.float32))
+    assert sc == 1.0 and not codes.any() and not bs.any()
+    x = np.zeros(32, np.float32)
+    x[0], x[16], x[17] = 1.0, 1e-7, -3e-8
+    codes, bs, sc = oracle.quantize_row_nvfp4(x)
+    assert sc == np.float32(1.0) / np.float32(2688.0)
+    assert bs[0] == 0x7E and bs[1] == 0
+    nib = [(codes[i // 2] >> (4 * (i & 1))) & 15 for i in range(32)]
+    assert nib[0] == 7 and not any(nib[1:])
 
 
 def _q4_weights(rng, E, rows, cols, exact=True):

@@ -8,6 +8,12 @@ The arithmetic lives in ``moe_oracle.c`` (plain C, single thread, built with
 ``-O2 -ffp-contract=off``); this module only builds it, loads it with ctypes
 and marshals numpy arrays.  bf16 tensors are passed as their raw 16-bit
 patterns (``numpy.uint16``); the C code widens them exactly to fp32.
+
+``THREADS`` (1 unless a caller raises it; the test suite does) lets the
+per-row functions (``combine_rows*``, ``expert_slots*``) hand disjoint parts
+of their token list or slot range to that many threads, each a call of the
+same C function on its own rows.  A row's value depends on nothing but its
+inputs, so the results are the same bits for any THREADS.
 """
 from __future__ import annotations
 
@@ -15,6 +21,7 @@ import ctypes
 import os
 import subprocess
 import threading
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -27,6 +34,7 @@ _lib = None
 # A library built from an edited copy of moe_oracle.c (the mutation tests plant
 # one mistake each and check that some pin fails); unset, the oracle is built here.
 _LIB_OVERRIDE = os.environ.get("MOE_ORACLE_LIBRARY")
+THREADS = 1
 
 
 CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-fPIC", "-shared", "-Wall"]
@@ -90,6 +98,9 @@ def _load():
             lib.oracle_combine_rows_q4.restype = I
             lib.oracle_expert_slots_q4.argtypes = [I, I, I, I, I] + [P] * 10 + [I, P, P, I, I, P]
             lib.oracle_expert_slots_q4.restype = I
+            lib.oracle_init_tables.argtypes = []
+            lib.oracle_init_tables.restype = None
+            lib.oracle_init_tables()   # before any thread of _split_calls runs
             _lib = lib
     return _lib
 
@@ -102,6 +113,21 @@ class OracleError(RuntimeError):
 
 def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _split_calls(n: int, call, what: str):
+    """call(i0, i1) -> status for the parts [i0, i1) of range(n), on up to THREADS threads."""
+    _load()
+    parts = max(1, min(int(THREADS), n))
+    bounds = [n * j // parts for j in range(parts + 1)]
+    if parts == 1:
+        sts = [call(0, n)]
+    else:
+        with ThreadPoolExecutor(parts) as ex:
+            sts = list(ex.map(lambda j: call(bounds[j], bounds[j + 1]), range(parts)))
+    st = next((x for x in sts if x), 0)
+    if st:
+        raise OracleError(st, what)
 
 
 def _c(a, dtype):
@@ -222,11 +248,9 @@ def combine_rows(h, w1, w3, w2, assign, cw, tokens) -> np.ndarray:
     E, F, _ = w1.shape
     k = assign.shape[1]
     out = np.empty((tokens.shape[0], d), np.float32)
-    st = _load().oracle_combine_rows(T, d, E, k, F, _ptr(h), _ptr(w1), _ptr(w3), _ptr(w2),
-                                     _ptr(assign), _ptr(cw), _ptr(tokens), tokens.shape[0],
-                                     _ptr(out))
-    if st:
-        raise OracleError(st, "combine_rows")
+    _split_calls(tokens.shape[0], lambda i0, i1: _lib.oracle_combine_rows(
+        T, d, E, k, F, _ptr(h), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(assign), _ptr(cw), _ptr(tokens[i0:i1]),
+        i1 - i0, _ptr(out[i0:i1])), "combine_rows")
     return out
 
 
@@ -239,10 +263,9 @@ def expert_slots(h, w1, w3, w2, assign, perm, row0: int, row1: int) -> np.ndarra
     E, F, _ = w1.shape
     k = assign.shape[1]
     out = np.empty((row1 - row0, d), np.float32)
-    st = _load().oracle_expert_slots(T, d, E, k, F, _ptr(h), _ptr(w1), _ptr(w3), _ptr(w2),
-                                     _ptr(assign), _ptr(perm), row0, row1, _ptr(out))
-    if st:
-        raise OracleError(st, "expert_slots")
+    _split_calls(row1 - row0, lambda i0, i1: _lib.oracle_expert_slots(
+        T, d, E, k, F, _ptr(h), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(assign), _ptr(perm), row0 + i0, row0 + i1,
+        _ptr(out[i0:i1])), "expert_slots")
     return out
 
 
@@ -282,11 +305,9 @@ def combine_rows_q8(h, q1, s1, q3, s3, q2, s2, assign, cw, tokens, quant_act=Tru
     E, F, _ = q1.shape
     k = assign.shape[1]
     out = np.empty((tokens.shape[0], d), np.float32)
-    st = _load().oracle_combine_rows_q8(T, d, E, k, F, _ptr(h), _ptr(q1), _ptr(s1), _ptr(q3), _ptr(s3),
-                                        _ptr(q2), _ptr(s2), int(quant_act), _ptr(assign), _ptr(cw), _ptr(tokens),
-                                        tokens.shape[0], _ptr(out))
-    if st:
-        raise OracleError(st, "combine_rows_q8")
+    _split_calls(tokens.shape[0], lambda i0, i1: _lib.oracle_combine_rows_q8(
+        T, d, E, k, F, _ptr(h), _ptr(q1), _ptr(s1), _ptr(q3), _ptr(s3), _ptr(q2), _ptr(s2), int(quant_act),
+        _ptr(assign), _ptr(cw), _ptr(tokens[i0:i1]), i1 - i0, _ptr(out[i0:i1])), "combine_rows_q8")
     return out
 
 
@@ -301,11 +322,9 @@ def expert_slots_q8(h, q1, s1, q3, s3, q2, s2, assign, perm, row0: int, row1: in
     E, F, _ = q1.shape
     k = assign.shape[1]
     out = np.empty((row1 - row0, d), np.float32)
-    st = _load().oracle_expert_slots_q8(T, d, E, k, F, _ptr(h), _ptr(q1), _ptr(s1), _ptr(q3), _ptr(s3),
-                                        _ptr(q2), _ptr(s2), int(quant_act), _ptr(assign), _ptr(perm), row0, row1,
-                                        _ptr(out))
-    if st:
-        raise OracleError(st, "expert_slots_q8")
+    _split_calls(row1 - row0, lambda i0, i1: _lib.oracle_expert_slots_q8(
+        T, d, E, k, F, _ptr(h), _ptr(q1), _ptr(s1), _ptr(q3), _ptr(s3), _ptr(q2), _ptr(s2), int(quant_act),
+        _ptr(assign), _ptr(perm), row0 + i0, row0 + i1, _ptr(out[i0:i1])), "expert_slots_q8")
     return out
 
 
@@ -389,11 +408,10 @@ def combine_rows_q4(h, w1, w3, w2, assign, cw, tokens, quant_act=True) -> np.nda
     E, F = s1.shape
     k = assign.shape[1]
     out = np.empty((tokens.shape[0], d), np.float32)
-    st = _load().oracle_combine_rows_q4(T, d, E, k, F, _ptr(h), _ptr(q1), _ptr(b1), _ptr(s1), _ptr(q3),
-                                        _ptr(b3), _ptr(s3), _ptr(q2), _ptr(b2), _ptr(s2), int(quant_act),
-                                        _ptr(assign), _ptr(cw), _ptr(tokens), tokens.shape[0], _ptr(out))
-    if st:
-        raise OracleError(st, "combine_rows_q4")
+    _split_calls(tokens.shape[0], lambda i0, i1: _lib.oracle_combine_rows_q4(
+        T, d, E, k, F, _ptr(h), _ptr(q1), _ptr(b1), _ptr(s1), _ptr(q3), _ptr(b3), _ptr(s3), _ptr(q2), _ptr(b2),
+        _ptr(s2), int(quant_act), _ptr(assign), _ptr(cw), _ptr(tokens[i0:i1]), i1 - i0, _ptr(out[i0:i1])),
+        "combine_rows_q4")
     return out
 
 
@@ -407,9 +425,8 @@ def expert_slots_q4(h, w1, w3, w2, assign, perm, row0: int, row1: int, quant_act
     E, F = s1.shape
     k = assign.shape[1]
     out = np.empty((row1 - row0, d), np.float32)
-    st = _load().oracle_expert_slots_q4(T, d, E, k, F, _ptr(h), _ptr(q1), _ptr(b1), _ptr(s1), _ptr(q3),
-                                        _ptr(b3), _ptr(s3), _ptr(q2), _ptr(b2), _ptr(s2), int(quant_act),
-                                        _ptr(assign), _ptr(perm), row0, row1, _ptr(out))
-    if st:
-        raise OracleError(st, "expert_slots_q4")
+    _split_calls(row1 - row0, lambda i0, i1: _lib.oracle_expert_slots_q4(
+        T, d, E, k, F, _ptr(h), _ptr(q1), _ptr(b1), _ptr(s1), _ptr(q3), _ptr(b3), _ptr(s3), _ptr(q2), _ptr(b2),
+        _ptr(s2), int(quant_act), _ptr(assign), _ptr(perm), row0 + i0, row0 + i1, _ptr(out[i0:i1])),
+        "expert_slots_q4")
     return out

@@ -159,8 +159,9 @@ typedef struct {
     const uint8_t* bs;
 } Wmat;
 
-/* The values of all 16 e2m1 and all 256 e4m3 codes (filled from the two
- * decoders on first use, so that a weight costs two table reads). */
+/* The values of all 16 e2m1 and all 256 e4m3 codes, filled from the two
+ * decoders (oracle_init_tables), so that a quantised weight costs table reads
+ * instead of a decode. */
 static double e2m1_tab[16], e4m3_tab[256];
 static int tabs_ready = 0;
 
@@ -172,6 +173,8 @@ static void fill_tabs(void)
     tabs_ready = 1;
 }
 
+void oracle_init_tables(void) { fill_tabs(); }
+
 static double wval(const Wmat* w, size_t r, size_t c)
 {
     if (w->bf) return (double)bf16_to_f32(w->bf[r * w->cols + c]);
@@ -180,7 +183,7 @@ static double wval(const Wmat* w, size_t r, size_t c)
         const uint8_t code = (uint8_t)((w->q4[i / 2] >> (4 * (i & 1))) & 15);
         return e2m1_tab[code] * e4m3_tab[w->bs[(r * w->cols + c) / 16]] * (double)w->s[r];
     }
-    return oracle_e4m3_value(w->q[r * w->cols + c]) * (double)w->s[r];
+    return e4m3_tab[w->q[r * w->cols + c]] * (double)w->s[r];
 }
 
 int64_t oracle_capacity(int64_t T, int k, int E, double cf, int64_t explicit_cap)
@@ -586,6 +589,7 @@ int oracle_combine_rows_q8(int T, int d, int E, int k, int F, const uint16_t* h,
                            const float* cw, const int32_t* tokens, int ntok, float* out_rows)
 {
     const ExpertSet W = {NULL, NULL, NULL, q1, q3, q2, s1, s3, s2, quant_act ? 1 : 0, NULL, NULL, NULL};
+    fill_tabs();
     return combine_rows_x(T, d, E, k, F, h, &W, assign, cw, tokens, ntok, out_rows);
 }
 
@@ -624,6 +628,7 @@ int oracle_expert_slots_q8(int T, int d, int E, int k, int F, const uint16_t* h,
                            const int32_t* perm, int row0, int row1, float* y_slots)
 {
     const ExpertSet W = {NULL, NULL, NULL, q1, q3, q2, s1, s3, s2, quant_act ? 1 : 0, NULL, NULL, NULL};
+    fill_tabs();
     return expert_slots_x(T, d, E, k, F, h, &W, assign, perm, row0, row1, y_slots);
 }
 

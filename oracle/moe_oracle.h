@@ -161,6 +161,12 @@ uint8_t oracle_e2m1_encode(float v);
  * two per byte, element 2m in the low nibble of byte m; bscale[n/16]. */
 void oracle_quantize_row_nvfp4(int n, const float* x, uint8_t* codes, uint8_t* bscale, float* scale);
 
+/* Fill the e2m1 and e4m3 value tables the quantised expert functions read
+ * (each also fills them on first use).  Call it once before calling those
+ * functions from several threads at a time: every other function here keeps
+ * its state on the stack or in its own allocations. */
+void oracle_init_tables(void);
+
 /* oracle_combine_rows / oracle_expert_slots with NVFP4 expert weights: W1,
  * W3 [E][F][d] and W2 [E][d][F] as packed e2m1 codes (q1, q3, q2), e4m3 block
  * scales per 16 consecutive elements of a row (b1, b3 [E][F][d/16], b2

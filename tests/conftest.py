@@ -11,6 +11,10 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running CPU oracle work")
+    # the oracle's per-row functions may split their rows over threads (same bits; the
+    # sampled full-size expert rows are most of the GPU suite's time)
+    import oracle
+    oracle.THREADS = min(16, os.cpu_count() or 1)
 
 
 def pytest_collection_modifyitems(config, items):

@@ -104,8 +104,8 @@ MUTANTS = {
                        ["test_e4m3_encode_ties_and_saturation", "test_q8_activation_rounding_hand_case"]),
     "quant_scale_not_448": ([("amax / 448.0f", "amax / 256.0f")],
                             ["test_quantize_row_matches_torch", "test_q8_activation_quantisation_is_identity_on_exact_rows"]),
-    "weight_scale_of_row_0": ([("return oracle_e4m3_value(w->q[r * w->cols + c]) * (double)w->s[r];",
-                                "return oracle_e4m3_value(w->q[r * w->cols + c]) * (double)w->s[0];")],
+    "weight_scale_of_row_0": ([("return e4m3_tab[w->q[r * w->cols + c]] * (double)w->s[r];",
+                                "return e4m3_tab[w->q[r * w->cols + c]] * (double)w->s[0];")],
                               ["test_q8_experts_equal_bf16_experts_on_exact_weights"]),
     "token_dequant_drops_scale": ([("xf[i] = oracle_e4m3_value(codes[i]) * (double)sc;",
                                     "xf[i] = oracle_e4m3_value(codes[i]);")],

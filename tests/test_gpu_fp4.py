@@ -141,7 +141,7 @@ def test_expert_ffn_nvfp4_vs_oracle(T, d, E, F, k, cf):
     assert_rows_close(np_(y[:n].float()), want)
 
 
-SAMPLE = {"tiny": 256, "mixtral_decode": 10, "mixtral_prefill": 4}
+SAMPLE = {"tiny": 256, "mixtral_decode": 64, "mixtral_prefill": 32}   # >= T: every token
 
 
 @pytest.mark.parametrize("name", ["tiny", "mixtral_decode", "mixtral_prefill"])

@@ -97,7 +97,7 @@ def test_expert_ffn_fp8_vs_oracle(T, d, E, F, k, cf):
     assert rows.max() <= 4 * OUT_REL_FROB
 
 
-SAMPLE = {"tiny": 256, "mixtral_decode": 10, "mixtral_prefill": 4}
+SAMPLE = {"tiny": 256, "mixtral_decode": 64, "mixtral_prefill": 32}   # >= T: every token
 
 
 @pytest.mark.parametrize("name", ["tiny", "mixtral_decode", "mixtral_prefill"])

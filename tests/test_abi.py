@@ -197,3 +197,98 @@ def test_backward_argument_checks(L):
     assert call(c, dh=FAKE + 4) == 3
     assert call(c, nb=n - 256) == 4
     assert call(_cfg(flags=moe.FLAG_BACKWARD, router_hidden=16)) == 2
+
+
+def test_quantiser_argument_checks(L):
+    P = ctypes.c_void_p
+    f = P(FAKE)
+    # e4m3: cols a multiple of 8, rows >= 0; w 16-byte and q 8-byte aligned
+    assert L.moe_quantize_fp8(-1, 64, f, f, f, None) == 1
+    assert L.moe_quantize_fp8(10, 60, f, f, f, None) == 1
+    assert L.moe_quantize_fp8(0, 64, None, None, None, None) == 0     # nothing to do, nothing enqueued
+    assert L.moe_quantize_fp8(10, 64, None, f, f, None) == 1
+    assert L.moe_quantize_fp8(10, 64, P(FAKE + 8), f, f, None) == 3
+    assert L.moe_quantize_fp8(10, 64, f, P(FAKE + 4), f, None) == 3
+    # NVFP4: cols a multiple of 32 and at most 16384; codes and block scales 16-byte aligned
+    assert [L.moe_nvfp4_sf_stride(c) for c in (0, 16, 32, 1408, 4096, 14336)] == [0, 16, 16, 96, 256, 896]
+    assert L.moe_quantize_nvfp4(10, 48, f, f, f, f, None) == 1
+    assert L.moe_quantize_nvfp4(10, 16416, f, f, f, f, None) == 2
+    assert L.moe_quantize_nvfp4(0, 64, None, None, None, None, None) == 0
+    assert L.moe_quantize_nvfp4(10, 64, f, P(FAKE + 8), f, f, None) == 3
+    assert L.moe_quantize_nvfp4(10, 64, f, f, P(FAKE + 8), f, None) == 3
+    assert L.moe_quantize_w13_nvfp4(8, 192, 512, f, f, f, f, None) == 1    # d_ff % 128
+    assert L.moe_quantize_w13_nvfp4(8, 256, 16416, f, f, f, f, None) == 2  # d > 16384
+    assert L.moe_quantize_w13_nvfp4(8, 256, 512, f, f, None, f, None) == 1
+    assert L.moe_quantize_w13_nvfp4(8, 256, 512, P(FAKE + 2), f, f, f, None) == 3
+
+
+def test_quantised_expert_argument_checks(L):
+    P = ctypes.c_void_p
+    f = P(FAKE)
+    plain = _cfg()
+    fp8 = _cfg(flags=moe.FLAG_FP8)
+    fp4 = _cfg(flags=moe.FLAG_NVFP4)
+    n8 = L.moe_workspace_size(ctypes.byref(fp8))
+    n4 = L.moe_workspace_size(ctypes.byref(fp4))
+    assert n8 > L.moe_workspace_size(ctypes.byref(plain)) and n4 > 0
+    # expert FFN: the scales are required; the workspace must be sized for the format
+    assert L.moe_expert_ffn_fp8(ctypes.byref(fp8), f, f, f, f, None, f, f, f, f, n8, None) == 1
+    assert L.moe_expert_ffn_fp8(ctypes.byref(plain), f, f, f, f, f, f, f, f, f, n8, None) == 1
+    assert L.moe_expert_ffn_fp8(ctypes.byref(_cfg(d_model=192, flags=moe.FLAG_FP8)), f, f, f, f, f, f, f, f, f,
+                                n8, None) == 2                                       # d % 128
+    assert L.moe_expert_ffn_nvfp4(ctypes.byref(fp4), f, f, f, f, None, f, f, f, f, f, f, n4, None) == 1
+    assert L.moe_expert_ffn_nvfp4(ctypes.byref(plain), f, f, f, f, f, f, f, f, f, f, f, n4, None) == 1
+    assert L.moe_expert_ffn_nvfp4(ctypes.byref(fp4), f, f, f, f, P(FAKE + 8), f, f, f, f, f, f, n4,
+                                  None) == 3
+    assert L.moe_expert_ffn_nvfp4(ctypes.byref(fp4), f, f, f, f, f, f, f, f, f, f, f, n4 - 256, None) == 4
+    # the layer: h, wr, bias, usage, w13 (codes, block scales, row scales), w2 (same), out, 8 optional
+    # outputs and the stage events, then the workspace
+    lay4 = lambda cfg, n=n4, **o: L.moe_layer_forward_nvfp4(
+        ctypes.byref(cfg), f, f, None, None, f, o.get("b13", f), f, f, f, f, o.get("out", f),
+        *([None] * 8), f, n, None)
+    assert lay4(plain) == 1
+    assert lay4(_cfg(d_model=192, flags=moe.FLAG_NVFP4)) == 2
+    assert lay4(fp4, b13=P(FAKE + 8)) == 3
+    assert lay4(fp4, out=None) == 1
+    assert lay4(fp4, n=n4 - 256) == 4
+    assert lay4(_cfg(flags=moe.FLAG_NVFP4, router_norm=1)) == 1
+    lay8 = lambda cfg, n=n8, s13=f: L.moe_layer_forward_fp8(ctypes.byref(cfg), f, f, None, None, f, s13, f, f,
+                                                           f, *([None] * 8), f, n, None)
+    assert lay8(plain) == 1
+    assert lay8(_cfg(d_model=192, flags=moe.FLAG_FP8)) == 2
+    assert lay8(fp8, n=n8 - 256) == 4
+
+
+def test_backward_static_and_host_argument_checks(L):
+    P = ctypes.c_void_p
+    f = P(FAKE)
+    bw = _cfg(flags=moe.FLAG_BACKWARD)
+    nb = L.moe_workspace_size(ctypes.byref(bw))
+    # backward: h, wr, w13, w2, dout, dP, dh, dwr, dbias, dw13, dw2, then the workspace
+    back = lambda cfg, n=nb, h=f, dw13=f: L.moe_layer_backward(ctypes.byref(cfg), h, f, f, f, f, None, f, None,
+                                                               None, dw13, f, f, n, None)
+    assert back(_cfg()) == 1                                   # the config lacks MOE_FLAG_BACKWARD
+    assert back(_cfg(flags=moe.FLAG_BACKWARD, router_norm=1)) == 2
+    assert back(bw, dw13=None) == 1
+    assert back(bw, h=P(FAKE + 8)) == 3
+    assert back(bw, n=nb - 256) == 4
+    # allocation-free dispatch: scores, assign, slot, flags, counts, offsets, perm, cw, totals, status
+    st = lambda cfg, scores=f, counts=f: L.moe_dispatch_static(ctypes.byref(cfg), scores, f, f, f, counts, f, f,
+                                                               f, f, f, None, None)
+    assert st(_cfg(flags=moe.FLAG_FP8)) == 1
+    assert st(_cfg(E=300)) == 2
+    assert st(_cfg(E=20, k=9)) == 2
+    assert st(_cfg(), counts=None) == 1
+    assert st(_cfg(), scores=None) == 1
+    assert st(_cfg(T=200000, E=64)) == 2                       # scratch beyond the fixed array
+    # host buffers: h_host, wr, bias, usage, w13, w2, out_host, then the workspace
+    c = _cfg()
+    n = L.moe_workspace_size(ctypes.byref(c))
+    host = lambda cfg, h=f, out=f, ws=FAKE, nbytes=n: L.moe_layer_forward_host_async(
+        ctypes.byref(cfg), h, f, None, None, f, f, out, P(ws), nbytes, None)
+    assert host(c, h=None) == 1
+    assert host(c, out=None) == 1
+    assert host(c, ws=FAKE + 64) == 3
+    assert host(c, nbytes=n - 256) == 4
+    assert host(_cfg(k=0)) == 1
+    assert L.moe_layer_forward_host(ctypes.byref(c), None, f, None, None, f, f, f, f, n, None) == 1

@@ -184,6 +184,53 @@ MUTANTS = {
                           ["test_backward_dropped_token_gets_only_the_aux_gradient"]),
     "bwd_dh_misses_router": ([("dh[(size_t)t * d + i] += dz * (double)bf16_to_f32(we[i]);", "(void)we;")],
                              ["test_backward_matches_torch_autograd"]),
+    # further branches: router biases and β, the L2 norm, statistics per rank, the combine
+    # weights, the slot's token, the quantisers' maxima, the backward's router-side terms
+    "router_linear_bias_dropped": ([("for (int i = 0; i < d; ++i) acc += x[i] * (double)bf16_to_f32(we[i]);\n"
+                                    "                if (bias) acc += (double)bias[e];",
+                                    "for (int i = 0; i < d; ++i) acc += x[i] * (double)bf16_to_f32(we[i]);")],
+                                   ["test_layernorm_router_reduces_to_torch"]),
+    "router_hidden_bias_dropped": ([("for (int j = 0; j < hidden; ++j) acc += a[j] * (double)bf16_to_f32(we[j]);\n"
+                                    "                if (bias) acc += (double)bias[e];",
+                                    "for (int j = 0; j < hidden; ++j) acc += a[j] * (double)bf16_to_f32(we[j]);")],
+                                   ["test_two_layer_router_orientation"]),
+    "layernorm_beta_dropped": ([(" + (beta ? (double)beta[i] : 0.0)", "")],
+                               ["test_layernorm_worked_example", "test_layernorm_router_reduces_to_torch"]),
+    "l2_norm_not_rooted": ([("double nrm = sqrt(ss);", "double nrm = ss;")],
+                           ["test_l2_norm_worked_example_and_torch", "test_l2_norm_eps_is_a_floor"]),
+    "counts_pre_of_rank0": ([("counts_pre[order[r]] += 1;", "counts_pre[order[0]] += 1;")],
+                            ["test_softmax_and_stats_match_scipy"]),
+    "topk_p_of_rank0": ([("topk_p[(size_t)t * k + r] = (float)p[order[r]];",
+                          "topk_p[(size_t)t * k + r] = (float)p[order[0]];")], ["test_softmax_and_stats_match_scipy"]),
+    "dispatch_weights_uniform": ([("softmax_row(E, scores + (size_t)t * E, p);\n            double tot = 0.0;",
+                                   "for (int e = 0; e < E; ++e) p[e] = 1.0 / E;\n            double tot = 0.0;")],
+                                 ["test_combine_weight_page_example"]),
+    "combine_ignores_weight": ([("double w = (double)cw[(size_t)t * k + r];", "double w = 1.0;")],
+                               ["test_combine_rows_weights_and_drops"]),
+    "combine_weight_of_rank0": ([("double w = (double)cw[(size_t)t * k + r];", "double w = (double)cw[(size_t)t * k];")],
+                                ["test_combine_rows_weights_and_drops"]),
+    "slot_token_assumes_k2": ([("int t = idx / k;", "int t = idx / 2;")], ["test_q8_activation_rounding_hand_case"]),
+    "q8_row_max_of_first_8": ([("for (int i = 0; i < n; ++i) amax = fmaxf(amax, fabsf(x[i]));\n"
+                                "    const float s = amax > 0.0f ? amax / 448.0f : 1.0f;",
+                                "for (int i = 0; i < 8 && i < n; ++i) amax = fmaxf(amax, fabsf(x[i]));\n"
+                                "    const float s = amax > 0.0f ? amax / 448.0f : 1.0f;")],
+                              ["test_quantize_row_matches_torch"]),
+    "nvfp4_row_max_of_first_block": ([("for (int i = 0; i < n; ++i) amax = fmaxf(amax, fabsf(x[i]));\n"
+                                       "    const float s = amax > 0.0f ? amax / 2688.0f : 1.0f;",
+                                       "for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));\n"
+                                       "    const float s = amax > 0.0f ? amax / 2688.0f : 1.0f;")],
+                                     ["test_nvfp4_row_quantisation_is_exact_on_representable_rows"]),
+    "nvfp4_block_max_of_half": ([("for (int i = 16 * j; i < 16 * j + 16; ++i) bmax = fmaxf(bmax, fabsf(x[i]));",
+                                  "for (int i = 16 * j; i < 16 * j + 8; ++i) bmax = fmaxf(bmax, fabsf(x[i]));")],
+                                ["test_nvfp4_row_quantisation_is_exact_on_representable_rows"]),
+    "bwd_dwr_of_wr": ([("dwr[(size_t)e * d + i] += dz * x[i];",
+                        "dwr[(size_t)e * d + i] += dz * (double)bf16_to_f32(we[i]);")],
+                      ["test_backward_matches_torch_autograd"]),
+    "bwd_dbias_missing": ([("dbias[e] += dz;", "(void)0;")],
+                          ["test_backward_dropped_token_gets_only_the_aux_gradient"]),
+    "bwd_cw_not_renormalised": ([("cw[r] = (e >= 0 && S > 0.0) ? p[e] / S : 0.0;",
+                                  "cw[r] = (e >= 0 && S > 0.0) ? p[e] : 0.0;")],
+                                ["test_backward_matches_torch_autograd"]),
 }
 
 

@@ -255,6 +255,8 @@ def _build_and_run(name, tmpdir):
     r = subprocess.run([sys.executable, "-m", "pytest", PINS, "-q", "-p", "no:cacheprovider", "-rf",
                         "-k", "not workload_router_statistics"],
                        capture_output=True, text=True, env=env, cwd=os.path.dirname(HERE), timeout=600)
+    if r.returncode not in (0, 1):   # 1: some test failed; anything else: the run itself broke
+        return None, f"pin run of {name!r} ended with status {r.returncode}\n{r.stdout[-2000:]}{r.stderr[-1000:]}"
     failed = set(re.findall(r"^FAILED \S*::(test_\w+)", r.stdout, re.M))
     return failed, r.stdout[-3000:]
 
